@@ -1,0 +1,212 @@
+"""Seeded synthetic inputs for the KDA bounded-gate prefill and verify calls.
+
+This module draws random numbers and encodes them; it holds none of the
+method's arithmetic.  Both the fp64 oracle and the CUDA path consume exactly
+the arrays produced here:
+
+* bf16 tensors are returned as ``uint16`` bit patterns, rounded from fp32
+  draws with round-to-nearest-even;
+* per-head / per-channel parameters are ``float32``;
+* sequence boundaries (``cu_seqlens``) and slot ids are ``int32``.
+
+Random numbers come from NumPy's PCG64 ``Generator`` seeded per workload, so
+a workload is a pure function of its name.
+
+Workload recipes (H heads, head dim D = 128, lower_bound = -5,
+scale = 1/sqrt(128) unless stated):
+
+* ``q, k, v, g_raw`` ~ N(0, 1) per element, ``beta_logits`` ~ N(0, 1) per
+  (token, head), all bf16;
+* ``A_log = log(U[1, 16])`` per head, ``dt_bias`` ~ N(0, 0.1) per
+  (head, channel), fp32;
+* state pools ~ N(0, 0.02) (standard deviation 0.02), fp32
+  ``[slots, H, D(k), D(v)]``; slot ids are distinct, drawn as a prefix of a
+  random permutation of the pool.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+import math
+
+import numpy as np
+
+D = 128
+LOWER_BOUND = -5.0
+SCALE = 1.0 / math.sqrt(128.0)
+
+
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round fp32 values to bf16 (nearest, ties to even); return the bit patterns."""
+    b = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    rounding = ((b >> np.uint32(16)) & np.uint32(1)) + np.uint32(0x7FFF)
+    return ((b + rounding) >> np.uint32(16)).astype(np.uint16)
+
+
+def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
+    """Exact widening of bf16 bit patterns to fp32."""
+    return (np.ascontiguousarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+@dataclass
+class PrefillInputs:
+    """One chunked-prefill call: packed varlen tokens ``[T, H, D]``."""
+
+    name: str
+    q: np.ndarray
+    k: np.ndarray
+    v: np.ndarray
+    g: np.ndarray
+    beta: np.ndarray
+    A_log: np.ndarray
+    dt_bias: np.ndarray
+    lower_bound: float
+    scale: float
+    cu_seqlens: np.ndarray
+    pool: np.ndarray | None = None
+    slot_ids: np.ndarray | None = None
+    load_initial: bool = False
+    final_to_pool: bool = False
+    meta: dict = field(default_factory=dict)
+
+    @property
+    def num_seqs(self) -> int:
+        return int(self.cu_seqlens.shape[0] - 1)
+
+    @property
+    def total_tokens(self) -> int:
+        return int(self.cu_seqlens[-1])
+
+    @property
+    def H(self) -> int:
+        return int(self.q.shape[1])
+
+    def initial_states(self) -> np.ndarray | None:
+        """Initial state per sequence, ``[N, H, D, D]`` fp32 (None = zero)."""
+        if not self.load_initial:
+            return None
+        return self.pool[self.slot_ids]
+
+
+@dataclass
+class VerifyInputs:
+    """One speculative-verify call: ``B`` requests with draft blocks of ``T`` tokens."""
+
+    name: str
+    q: np.ndarray
+    k: np.ndarray
+    v: np.ndarray
+    g: np.ndarray
+    beta: np.ndarray
+    A_log: np.ndarray
+    dt_bias: np.ndarray
+    lower_bound: float
+    scale: float
+    B: int
+    T: int
+    pool: np.ndarray
+    slot_ids: np.ndarray
+    meta: dict = field(default_factory=dict)
+
+    @property
+    def H(self) -> int:
+        return int(self.q.shape[1])
+
+
+def _token_tensors(rng, total, H, d, g_mean):
+    shape = (total, H, d)
+    q = f32_to_bf16_bits(rng.standard_normal(shape, dtype=np.float32))
+    k = f32_to_bf16_bits(rng.standard_normal(shape, dtype=np.float32))
+    v = f32_to_bf16_bits(rng.standard_normal(shape, dtype=np.float32))
+    g = f32_to_bf16_bits(rng.standard_normal(shape, dtype=np.float32) + np.float32(g_mean))
+    beta = f32_to_bf16_bits(rng.standard_normal((total, H), dtype=np.float32))
+    return q, k, v, g, beta
+
+
+def _head_params(rng, H, d):
+    A_log = np.log(rng.uniform(1.0, 16.0, size=H)).astype(np.float32)
+    dt_bias = (rng.standard_normal((H, d)) * 0.1).astype(np.float32)
+    return A_log, dt_bias
+
+
+def prefill_inputs(name: str, seq_lens, H: int, *, seed: int, d: int = D,
+                   pool_slots: int | None = None, load_initial: bool = False,
+                   final_to_pool: bool = False, lower_bound: float = LOWER_BOUND,
+                   scale: float | None = None, g_mean: float = 0.0,
+                   state_std: float = 0.02) -> PrefillInputs:
+    """Draw one prefill workload.  Draw order: tokens, head params, pool, slot ids."""
+    seq_lens = [int(x) for x in seq_lens]
+    rng = np.random.default_rng(seed)
+    cu = np.zeros(len(seq_lens) + 1, dtype=np.int32)
+    cu[1:] = np.cumsum(seq_lens)
+    total = int(cu[-1])
+    q, k, v, g, beta = _token_tensors(rng, total, H, d, g_mean)
+    A_log, dt_bias = _head_params(rng, H, d)
+    pool = slot_ids = None
+    if pool_slots is not None:
+        pool = (rng.standard_normal((pool_slots, H, d, d), dtype=np.float32) * np.float32(state_std))
+        slot_ids = rng.permutation(pool_slots)[: len(seq_lens)].astype(np.int32)
+    return PrefillInputs(
+        name=name, q=q, k=k, v=v, g=g, beta=beta, A_log=A_log, dt_bias=dt_bias,
+        lower_bound=float(lower_bound), scale=float(1.0 / math.sqrt(d) if scale is None else scale),
+        cu_seqlens=cu, pool=pool, slot_ids=slot_ids, load_initial=load_initial,
+        final_to_pool=final_to_pool, meta={"seed": seed, "seq_lens": seq_lens})
+
+
+def verify_inputs(name: str, B: int, T: int, H: int, *, seed: int, d: int = D,
+                  pool_slots: int = 256, lower_bound: float = LOWER_BOUND,
+                  g_mean: float = 0.0, state_std: float = 0.02) -> VerifyInputs:
+    """Draw one verify workload.  Draw order: tokens, head params, pool, slot ids."""
+    rng = np.random.default_rng(seed)
+    q, k, v, g, beta = _token_tensors(rng, B * T, H, d, g_mean)
+    A_log, dt_bias = _head_params(rng, H, d)
+    pool = rng.standard_normal((pool_slots, H, d, d), dtype=np.float32) * np.float32(state_std)
+    slot_ids = rng.permutation(pool_slots)[:B].astype(np.int32)
+    return VerifyInputs(
+        name=name, q=q, k=k, v=v, g=g, beta=beta, A_log=A_log, dt_bias=dt_bias,
+        lower_bound=float(lower_bound), scale=float(1.0 / math.sqrt(d)), B=B, T=T,
+        pool=pool, slot_ids=slot_ids, meta={"seed": seed})
+
+
+# ---------------------------------------------------------------------------
+# The five named workloads.
+# ---------------------------------------------------------------------------
+
+def tiny_prefill() -> PrefillInputs:
+    """1 sequence of 256 tokens, H=2, zero initial state, dense final state."""
+    return prefill_inputs("prefill_1x256_h2", [256], 2, seed=1000)
+
+
+def prefill_2048x8() -> PrefillInputs:
+    """8 sequences of 2048 tokens, H=16; initial states gathered from a
+    64-slot pool by slot id, dense final states."""
+    return prefill_inputs("prefill_2048x8_h16", [2048] * 8, 16, seed=1001,
+                          pool_slots=64, load_initial=True)
+
+
+def prefill_8192x4() -> PrefillInputs:
+    """4 sequences of 8192 tokens, H=16; zero initial state, final states
+    written back to a 64-slot pool."""
+    return prefill_inputs("prefill_8192x4_h16", [8192] * 4, 16, seed=1002,
+                          pool_slots=64, final_to_pool=True)
+
+
+def varlen_16384_plus_16(seed: int = 1003) -> PrefillInputs:
+    """One 16384-token sequence followed by 16 sequences with lengths drawn
+    uniformly from [1, 4096]; H=16, zero initial state, dense final states."""
+    rng = np.random.default_rng(seed + 500)
+    lens = [16384] + [int(x) for x in rng.integers(1, 4097, size=16)]
+    return prefill_inputs("prefill_16384+16varlen_h16", lens, 16, seed=seed)
+
+
+def verify_64x8() -> VerifyInputs:
+    """64 requests x draft block of 8 tokens, H=16, 256-slot pool."""
+    return verify_inputs("verify_64x8_h16", 64, 8, 16, seed=1004, pool_slots=256)
+
+
+NAMED = {
+    "prefill_1x256_h2": tiny_prefill,
+    "prefill_2048x8_h16": prefill_2048x8,
+    "prefill_8192x4_h16": prefill_8192x4,
+    "prefill_16384+16varlen_h16": varlen_16384_plus_16,
+    "verify_64x8_h16": verify_64x8,
+}

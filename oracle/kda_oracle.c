@@ -1,0 +1,239 @@
+/*
+ * fp64 CPU oracle for the KDA bounded-gate recurrence.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the bench's
+ * CPU-baseline leg load this library.  It shares no code, header, table or
+ * helper with the CUDA path.
+ *
+ * What is computed, per sequence n, head h, and token t in token order (all
+ * arithmetic in double precision; bf16 inputs are widened exactly):
+ *
+ *   q^ = q / sqrt(sum_c q_c^2 + eps),  k^ likewise
+ *       -- "in-kernel q/k l2norm" (vLLM PR #55737 "Use FlashKDA for KDA
+ *          chunked prefill", PR summary and Purpose).  eps is not printed on
+ *          the pages; the caller passes it (1e-6 is the adopted reading).
+ *   beta = 1 / (1 + exp(-beta_logit))
+ *       -- "raw beta logits" enter the kernel and the sigmoid is applied
+ *          inside it (same PR, summary: "pre-sigmoid beta cast no longer
+ *          needed").
+ *   lambda_c = lower_bound * sigmoid(exp(A_log[h]) * (g_c + dt_bias[h][c]))
+ *       -- the bounded gate, printed verbatim in the same PR summary.  It is
+ *          a per-channel log-decay: alpha_c = exp(lambda_c), lower_bound < 0.
+ *   S <- Diag(alpha) S                      (decay of the dk rows of S)
+ *   u  = beta * (v - S^T k^)                (delta-rule correction)
+ *   S <- S + k^ u^T
+ *   o  = scale * S^T q^
+ *
+ * The three state lines are the KDA delta rule
+ *   S_t = (I - beta k^ k^T) Diag(alpha) S_{t-1} + beta k^ v^T
+ * that the pages call "the same bounded-gate KDA recurrence" (same PR,
+ * summary); expanding the product gives exactly the decay / correction /
+ * rank-1 update above.  The output is read from the updated state S_t.
+ *
+ * State layout: S is dk x dv, row-major (dv fastest), o = S^T q^ has dv
+ * entries.  Verify semantics ("seeds ... with the pool state and writes step
+ * t's state to row (b, t)", TensorRT-LLM PR #21179 "GLM-5.3-Flash FP8
+ * performance fixes on Hopper", KDA verify commit): the per-step state
+ * record for token t is the state after token t.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------------- */
+/* element-level definitions                                                  */
+/* ------------------------------------------------------------------------- */
+
+static double bf16_to_double(uint16_t h)
+{
+    uint32_t bits = ((uint32_t)h) << 16;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return (double)f;
+}
+
+static double sigmoid(double x) { return 1.0 / (1.0 + exp(-x)); }
+
+/* x^ = x / sqrt(sum x^2 + eps) over the d channels of one (token, head). */
+void kda_oracle_l2norm(const double *x, int d, double eps, double *out)
+{
+    double ss = 0.0;
+    for (int c = 0; c < d; ++c) ss += x[c] * x[c];
+    double inv = 1.0 / sqrt(ss + eps);
+    for (int c = 0; c < d; ++c) out[c] = x[c] * inv;
+}
+
+/* lambda_c = lower_bound * sigmoid(exp(A_log) * (g_c + dt_bias_c)). */
+void kda_oracle_gate(const double *g, const double *dt_bias, double A_log,
+                     double lower_bound, int d, double *lambda)
+{
+    double a = exp(A_log);
+    for (int c = 0; c < d; ++c) lambda[c] = lower_bound * sigmoid(a * (g[c] + dt_bias[c]));
+}
+
+/*
+ * One token of the recurrence on a dk x dv state.
+ *   lambda: per-channel log-decay (dk), beta: scalar in [0, 1].
+ *   qh, kh: already normalised query/key (dk), v: value (dv).
+ *   o: output (dv).  S is updated in place.
+ */
+void kda_oracle_step(double *S, int dk, int dv, const double *qh, const double *kh,
+                     const double *v, const double *lambda, double beta,
+                     double scale, double *o)
+{
+    /* S <- Diag(alpha) S */
+    for (int c = 0; c < dk; ++c) {
+        double alpha = exp(lambda[c]);
+        double *row = S + (size_t)c * dv;
+        for (int j = 0; j < dv; ++j) row[j] *= alpha;
+    }
+    /* u = beta (v - S^T k^) */
+    double u[dv];
+    for (int j = 0; j < dv; ++j) {
+        double w = 0.0;
+        for (int c = 0; c < dk; ++c) w += S[(size_t)c * dv + j] * kh[c];
+        u[j] = beta * (v[j] - w);
+    }
+    /* S <- S + k^ u^T */
+    for (int c = 0; c < dk; ++c) {
+        double *row = S + (size_t)c * dv;
+        for (int j = 0; j < dv; ++j) row[j] += kh[c] * u[j];
+    }
+    /* o = scale S^T q^ */
+    for (int j = 0; j < dv; ++j) {
+        double acc = 0.0;
+        for (int c = 0; c < dk; ++c) acc += S[(size_t)c * dv + j] * qh[c];
+        o[j] = scale * acc;
+    }
+}
+
+/*
+ * Core recurrence for one (sequence, head) with the decay and beta given
+ * directly (no gate, no normalisation): used to pin the recurrence on cases
+ * the gate cannot produce exactly (alpha = 1, beta = 1).
+ *   qh, kh: [T, dk]; v: [T, dv]; lambda: [T, dk]; beta: [T]
+ *   S: [dk, dv] in/out; out: [T, dv]; step_states: [T, dk, dv] or NULL.
+ */
+int kda_oracle_core(const double *qh, const double *kh, const double *v,
+                    const double *lambda, const double *beta, int T, int dk, int dv,
+                    double scale, double *S, double *out, double *step_states)
+{
+    if (T < 0 || dk <= 0 || dv <= 0) return 1;
+    for (int t = 0; t < T; ++t) {
+        kda_oracle_step(S, dk, dv, qh + (size_t)t * dk, kh + (size_t)t * dk,
+                        v + (size_t)t * dv, lambda + (size_t)t * dk, beta[t], scale,
+                        out + (size_t)t * dv);
+        if (step_states)
+            memcpy(step_states + (size_t)t * dk * dv, S, sizeof(double) * (size_t)dk * dv);
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------- */
+/* full path over packed varlen sequences and heads                          */
+/* ------------------------------------------------------------------------- */
+
+typedef struct {
+    const uint16_t *q, *k, *v, *g, *beta;
+    const float *A_log, *dt_bias;
+    double lower_bound, scale, eps;
+    const int32_t *cu_seqlens;
+    int num_seqs, H, dk, dv, head_begin, head_end;
+    const double *S0;
+    double *out, *S_final, *step_states;
+    int next_task; /* shared task counter */
+} job_t;
+
+static void run_task(const job_t *J, int n, int h)
+{
+    const int dk = J->dk, dv = J->dv, H = J->H;
+    const size_t state_elems = (size_t)dk * dv;
+    double *S = (double *)calloc(state_elems, sizeof(double));
+    double *x = (double *)malloc(sizeof(double) * (size_t)(dk > dv ? dk : dv));
+    double *qh = (double *)malloc(sizeof(double) * (size_t)dk);
+    double *kh = (double *)malloc(sizeof(double) * (size_t)dk);
+    double *vv = (double *)malloc(sizeof(double) * (size_t)dv);
+    double *gg = (double *)malloc(sizeof(double) * (size_t)dk);
+    double *dtb = (double *)malloc(sizeof(double) * (size_t)dk);
+    double *lam = (double *)malloc(sizeof(double) * (size_t)dk);
+
+    if (J->S0) memcpy(S, J->S0 + ((size_t)n * H + h) * state_elems, sizeof(double) * state_elems);
+    for (int c = 0; c < dk; ++c) dtb[c] = (double)J->dt_bias[(size_t)h * dk + c];
+    const double A_log = (double)J->A_log[h];
+
+    for (int t = J->cu_seqlens[n]; t < J->cu_seqlens[n + 1]; ++t) {
+        const size_t rk = ((size_t)t * H + h) * dk; /* row of q / k / g */
+        const size_t rv = ((size_t)t * H + h) * dv; /* row of v / out   */
+        for (int c = 0; c < dk; ++c) x[c] = bf16_to_double(J->q[rk + c]);
+        kda_oracle_l2norm(x, dk, J->eps, qh);
+        for (int c = 0; c < dk; ++c) x[c] = bf16_to_double(J->k[rk + c]);
+        kda_oracle_l2norm(x, dk, J->eps, kh);
+        for (int j = 0; j < dv; ++j) vv[j] = bf16_to_double(J->v[rv + j]);
+        for (int c = 0; c < dk; ++c) gg[c] = bf16_to_double(J->g[rk + c]);
+        kda_oracle_gate(gg, dtb, A_log, J->lower_bound, dk, lam);
+        double beta = sigmoid(bf16_to_double(J->beta[(size_t)t * H + h]));
+        kda_oracle_step(S, dk, dv, qh, kh, vv, lam, beta, J->scale, J->out + rv);
+        if (J->step_states)
+            memcpy(J->step_states + ((size_t)t * H + h) * state_elems, S,
+                   sizeof(double) * state_elems);
+    }
+    if (J->S_final)
+        memcpy(J->S_final + ((size_t)n * H + h) * state_elems, S, sizeof(double) * state_elems);
+    free(S); free(x); free(qh); free(kh); free(vv); free(gg); free(dtb); free(lam);
+}
+
+static void *worker(void *arg)
+{
+    job_t *J = (job_t *)arg;
+    const int heads = J->head_end - J->head_begin;
+    const int ntasks = J->num_seqs * heads;
+    for (;;) {
+        int i = __atomic_fetch_add(&J->next_task, 1, __ATOMIC_RELAXED);
+        if (i >= ntasks) break;
+        run_task(J, i / heads, J->head_begin + i % heads);
+    }
+    return NULL;
+}
+
+/*
+ * Run every sequence of a packed varlen batch for heads [head_begin, head_end).
+ *   q, k, g: bf16 bits [T_total, H, dk]; v: [T_total, H, dv]; beta_logits: [T_total, H]
+ *   A_log: [H]; dt_bias: [H, dk]; cu_seqlens: [num_seqs + 1], non-decreasing, from 0
+ *   S0: [num_seqs, H, dk, dv] or NULL (zero initial state)
+ *   out: [T_total, H, dv]; S_final: [num_seqs, H, dk, dv] or NULL
+ *   step_states: [T_total, H, dk, dv] or NULL (state after each token)
+ * Only the selected heads' entries of out / S_final / step_states are written.
+ * Returns 0, or 1 on invalid sizes.
+ */
+int kda_oracle_run(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                   const uint16_t *g, const uint16_t *beta_logits,
+                   const float *A_log, const float *dt_bias,
+                   double lower_bound, double scale, double eps,
+                   const int32_t *cu_seqlens, int num_seqs, int H, int dk, int dv,
+                   int head_begin, int head_end, const double *S0,
+                   double *out, double *S_final, double *step_states, int nthreads)
+{
+    if (num_seqs < 0 || H <= 0 || dk <= 0 || dv <= 0) return 1;
+    if (head_begin < 0 || head_end > H || head_begin > head_end) return 1;
+    if (cu_seqlens[0] != 0) return 1;
+    for (int n = 0; n < num_seqs; ++n)
+        if (cu_seqlens[n + 1] < cu_seqlens[n]) return 1;
+    job_t J = {q, k, v, g, beta_logits, A_log, dt_bias, lower_bound, scale, eps,
+               cu_seqlens, num_seqs, H, dk, dv, head_begin, head_end, S0,
+               out, S_final, step_states, 0};
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads == 1) {
+        worker(&J);
+        return 0;
+    }
+    pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nthreads);
+    int started = 0;
+    for (int i = 0; i < nthreads; ++i)
+        if (pthread_create(&th[started], NULL, worker, &J) == 0) ++started;
+    if (started == 0) worker(&J);
+    for (int i = 0; i < started; ++i) pthread_join(th[i], NULL);
+    free(th);
+    return 0;
+}
