@@ -1,0 +1,412 @@
+"""Benchmark of the KDA bounded-gate prefill (and verify) on GB300.
+
+One step = one kda_chunk_prefill call over the 8 x 2048-token, H=16, d=128
+workload (initial states gathered from a 64-slot pool, dense final states),
+inputs resident in HBM.  Also timed: the same call end to end with host
+buffers (pinned H2D of the step's inputs + D2H of its outputs inside the
+timed region), the verify call on 64 requests x 8 draft tokens, and the fp64
+CPU oracle on a bounded sample of the prefill workload.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+N > 1 runs under torchrun, one replica per GPU (weak scaling, no collective on
+the data path; a barrier and a max over ranks bracket the timing).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "KDA prefill tokens/s per layer (H=16,d=128) and % roofline; verify µs/layer"
+WORKLOAD = "prefill_2048x8_h16"
+PAGES_FLASHKDA_US = 49.0  # vLLM PR #55737 (GB300, T=2048x8, per layer): context, another kernel
+L2_BYTES = 129e6
+TOKEN_HEAD_BYTES = 4 * 256 + 2 + 256  # q, k, v, g + beta + out (bf16)
+STATE_BYTES = 128 * 128 * 4
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def prefill_algorithmic_bytes(inp):
+    T, H = inp.total_tokens, inp.H
+    states = inp.num_seqs * H * STATE_BYTES * ((1 if inp.load_initial else 0) + 1)
+    return T * H * TOKEN_HEAD_BYTES + states
+
+
+def verify_algorithmic_bytes(inp):
+    BT, H = inp.B * inp.T, inp.H
+    return BT * H * TOKEN_HEAD_BYTES + inp.B * H * STATE_BYTES * (1 + inp.T)
+
+
+def source_digest():
+    csrc = os.path.join(ROOT, "kda_linear_attention_bounded_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kind):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", f"{kind}_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    with open(path) as f:
+        for line in f:
+            if ":" in line and not line.startswith("#"):
+                k, v = line.split(":", 1)
+                vals[k.strip()] = v.strip()
+    if vals.get("source_digest") != source_digest():
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = "clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown," \
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown," \
+             "clocks_event_reasons.sw_power_cap"
+
+    def __init__(self, device_index):
+        self.device_index = device_index
+        self.samples = []
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50",
+                 "-i", str(self.device_index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        threading.Thread(target=self._read, daemon=True).start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def mark(self, which):
+        if which == "begin":
+            self.t0 = time.time()
+        else:
+            self.t1 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for ts, line in self.samples:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                rows.append((ts, float(parts[0]), float(parts[1]), parts[3:7]))
+            except ValueError:
+                continue
+        inside = [r for r in rows if self.t0 and self.t1 and self.t0 <= r[0] <= self.t1]
+        use = inside or rows
+        if not use:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in use for i, v in enumerate(r[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in use), "sm_max_mhz": max(r[2] for r in use),
+                "reasons": reasons, "samples": len(use), "in_timed_region": bool(inside)}
+
+
+def dist_setup(n_gpus):
+    import torch
+    import torch.distributed as dist
+
+    if n_gpus > 1 or "RANK" in os.environ:
+        rank = int(os.environ.get("RANK", 0))
+        world = int(os.environ.get("WORLD_SIZE", 1))
+        local = int(os.environ.get("LOCAL_RANK", 0))
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+        return rank, world, local
+    return 0, 1, 0
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world, device=None):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the fp64 CPU oracle, as it stands, on the host cores
+# ---------------------------------------------------------------------------
+
+def oracle_sample_rate(inp, seqs, tokens, nthreads):
+    """Run the oracle on `seqs` sequences x all heads, first `tokens` tokens each;
+    return (token-rows processed, seconds)."""
+    import numpy as np
+    import oracle
+
+    starts = inp.cu_seqlens[:seqs]
+    rows = np.concatenate([np.arange(s, s + tokens) for s in starts])
+    cu = (np.arange(seqs + 1) * tokens).astype(np.int32)
+    S0 = inp.initial_states()[:seqs] if inp.load_initial else None
+    t0 = time.perf_counter()
+    oracle.run(inp.q[rows], inp.k[rows], inp.v[rows], inp.g[rows], inp.beta[rows], inp.A_log, inp.dt_bias,
+               inp.lower_bound, inp.scale, cu, S0=S0, nthreads=nthreads)
+    return seqs * tokens, time.perf_counter() - t0
+
+
+def cpu_baseline(inp, budget_s=12.0):
+    import oracle
+
+    oracle.build()
+    nthreads = oracle.default_threads()
+    seqs = min(inp.num_seqs, max(1, nthreads // inp.H) or 1)
+    tok, dt = oracle_sample_rate(inp, seqs, 128, nthreads)  # calibration
+    rate = tok / dt
+    tokens = int(min(2048, max(128, budget_s * rate / seqs)))
+    tok, dt = oracle_sample_rate(inp, seqs, tokens, nthreads)
+    return {"value": tok / dt, "unit": "tokens/s", "cores": nthreads, "kind": "oracle",
+            "sample": f"{seqs} of the {inp.num_seqs} sequences x all {inp.H} heads, first {tokens} tokens each "
+                      f"(fp64 token-by-token, {dt:.1f} s wall)"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", 0))
+    if rank != 0:
+        return
+    import oracle
+    from kda_linear_attention_bounded_gb300 import inputs
+
+    oracle.build()
+    inp = inputs.prefill_2048x8()
+    nthreads = oracle.default_threads()
+    seqs = min(inp.num_seqs, max(1, nthreads // inp.H) or 1)
+    tok, dt = oracle_sample_rate(inp, seqs, 64, nthreads)
+    per_step_budget = 150.0 / max(1, args.steps + args.warmup)
+    tokens = int(min(2048, max(16, per_step_budget * (tok / dt) / seqs)))
+    for _ in range(args.warmup):
+        oracle_sample_rate(inp, seqs, tokens, nthreads)
+    total_tok = 0
+    total_t = 0.0
+    for _ in range(args.steps):
+        t, d = oracle_sample_rate(inp, seqs, tokens, nthreads)
+        total_tok += t
+        total_t += d
+    value = total_tok / total_t
+    sample = f"per step {seqs} sequence(s) x all {inp.H} heads x first {tokens} tokens of {WORKLOAD}"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_t / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "H": inp.H, "d": 128, "tokens_per_step": total_tok // args.steps},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": nthreads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def run_gpu(args):
+    import numpy as np
+    import torch
+
+    rank, world, local = dist_setup(args.gpus)
+    device = torch.device("cuda", local)
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import kda_linear_attention_bounded_gb300 as kda
+    from kda_linear_attention_bounded_gb300 import inputs
+    from gpu_helpers import DevicePrefill, DeviceVerify
+
+    kda.load()
+    inp = inputs.prefill_2048x8()
+    dev = DevicePrefill(inp, device=device)
+    ws = kda.make_workspace(device)
+    stream = torch.cuda.current_stream(device)
+    H, T = inp.H, inp.total_tokens
+    out = torch.empty((T, H, 128), dtype=torch.bfloat16, device=device)
+    final = torch.empty((inp.num_seqs, H, 128, 128), dtype=torch.float32, device=device)
+
+    def step():
+        dev.run(out=out, final_state=final, workspace=ws, stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(device)
+
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.2)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize(device)
+    if sampler:
+        sampler.mark("begin")
+    t_wall = time.perf_counter()
+    for i in range(args.steps):
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize(device)
+    barrier(world)
+    wall = time.perf_counter() - t_wall
+    if sampler:
+        sampler.mark("end")
+    per_launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    elapsed_ms = starts[0].elapsed_time(ends[-1])
+    elapsed_ms = max_over_ranks(elapsed_ms, world, device)
+    clocks = sampler.stop() if sampler else None
+    assert kda.read_device_status(ws) == 0
+
+    tokens_all = T * args.steps * world
+    value = tokens_all / (elapsed_ms / 1e3)
+    avg_launch_s = statistics.mean(per_launch_ms) / 1e3
+    peak, peak_kind = measured_peaks()
+    alg = prefill_algorithmic_bytes(inp)
+    achieved = alg / avg_launch_s / 1e9
+
+    # ---- end to end through the C ABI with host buffers ----
+    host = {name: getattr(dev, name).cpu().pin_memory() for name in ("q", "k", "v", "g", "beta")}
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    final_h = torch.empty(final.shape, dtype=final.dtype).pin_memory()
+    bufs = {name: torch.empty_like(getattr(dev, name)) for name in host}
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_h.numel() * out_h.element_size() + final_h.numel() * final_h.element_size()
+    e2e_steps = max(3, min(args.steps, 100))
+
+    def e2e_step():
+        for name, t in host.items():
+            bufs[name].copy_(t, non_blocking=True)
+        kda.chunk_prefill(bufs["q"], bufs["k"], bufs["v"], bufs["g"], bufs["beta"], dev.A_log, dev.dt_bias, dev.cu,
+                          dev.cu_host, lower_bound=inp.lower_bound, scale=inp.scale, state_pool=dev.pool,
+                          slot_ids=dev.slots, load_initial=True, out=out, final_state=final, workspace=ws,
+                          stream=stream)
+        out_h.copy_(out, non_blocking=True)
+        final_h.copy_(final, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize(device)
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    barrier(world)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, device)
+    e2e_value = T * e2e_steps * world / (e2e_ms / 1e3)
+
+    # ---- verify: 64 requests x 8 draft tokens ----
+    vin = inputs.verify_64x8()
+    vdev = DeviceVerify(vin, device=device)
+    vout = torch.empty((vin.B * vin.T, H, 128), dtype=torch.bfloat16, device=device)
+    inter = torch.empty((vin.B, vin.T, H, 128, 128), dtype=torch.float32, device=device)
+    for _ in range(max(3, args.warmup)):
+        vdev.run(out=vout, intermediate_states=inter, workspace=ws, stream=stream)
+    v_steps = max(3, min(args.steps, 200))
+    v0 = torch.cuda.Event(enable_timing=True)
+    v1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(device)
+    v0.record(stream)
+    for _ in range(v_steps):
+        vdev.run(out=vout, intermediate_states=inter, workspace=ws, stream=stream)
+    v1.record(stream)
+    torch.cuda.synchronize(device)
+    v_us = v0.elapsed_time(v1) * 1e3 / v_steps
+    v_bytes = verify_algorithmic_bytes(vin)
+    v_achieved = v_bytes / (v_us * 1e-6) / 1e9
+
+    del inter, vout
+    if rank != 0:
+        return
+    cpu = None if args.no_cpu_baseline or world > 1 else cpu_baseline(inp)
+    traffic = recorded_traffic("prefill")
+    vtraffic = recorded_traffic("verify")
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": value / (16384 / (PAGES_FLASHKDA_US * 1e-6)),
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "H": H, "d": 128, "tokens_per_step": T, "sequences": inp.num_seqs,
+                   "initial_state": "64-slot pool by slot id", "final_state": "dense",
+                   "l2": f"inputs larger than L2 ({alg / 1e6:.0f} MB algorithmic per step > 129 MB L2)",
+                   "parallelism": f"replicas x{world}",
+                   "vs_baseline_ref": "FlashKDA 49 us/layer at T=2048x8 on GB300 (vLLM PR #55737), context only"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": traffic, "algorithmic_bytes": alg, "avg_launch_us": avg_launch_s * 1e6,
+                     "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else peak_kind},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "steps": e2e_steps},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "verify": {"workload": vin.name, "us_per_layer": v_us, "steps": v_steps,
+                   "roofline": {"bound": "hbm", "achieved": v_achieved, "peak": peak, "unit": "GB/s",
+                                "frac": v_achieved / peak, "traffic": vtraffic, "algorithmic_bytes": v_bytes}},
+        "wall_s_timed_region": wall,
+    }
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,151 @@
+/*
+ * kda.h -- C ABI of libkda: the Kimi Delta Attention (KDA) bounded-gate
+ * recurrence on one GB300 (sm_103a) GPU.
+ *
+ * What the calls compute, per sequence n, head h and token t (token order):
+ *
+ *   q^ = q / sqrt(sum_c q_c^2 + 1e-6),  k^ likewise      ("in-kernel q/k l2norm")
+ *   beta    = sigmoid(beta_logit)                           ("raw beta logits")
+ *   lambda_c = lower_bound * sigmoid(exp(A_log[h]) * (g_c + dt_bias[h][c]))
+ *   S_t = (I - beta k^ k^T) Diag(exp(lambda)) S_{t-1} + beta k^ v^T
+ *   o_t = scale * S_t^T q^
+ *
+ * The gate, the in-kernel l2norm and the raw beta logits are the bounded-gate
+ * KDA recurrence of vLLM PR #55737 "Use FlashKDA for KDA chunked prefill"
+ * (PR summary and Purpose); the verify semantics (pool read-only, one state
+ * record per draft step) are those of TensorRT-LLM PR #21179 "GLM-5.3-Flash
+ * FP8 performance fixes on Hopper" (commit adding the one-launch KDA verify).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - head_dim is fixed at 128 for keys and values (dk = dv = 128).
+ *  - Token tensors are [tokens, H, 128] with the 128 channels of a head
+ *    contiguous and heads packed contiguously (head stride 128 elements); the
+ *    token stride is given in ELEMENTS and may exceed H*128 (tensors read in
+ *    place from a fused projection).  bf16 tensors are passed as uint16_t*
+ *    holding bf16 bit patterns.
+ *  - beta_logits is [tokens, H] bf16 with its own token stride (elements).
+ *  - A_log is fp32 [H]; dt_bias is fp32 [H, 128].
+ *  - States are fp32 [.., H, 128 (key channel), 128 (value channel)],
+ *    row-major, 64 KiB per (slot or sequence, head).
+ *  - Every pointer except cu_seqlens_host is a DEVICE pointer on the current
+ *    device; all must be 16-byte aligned and the token strides multiples of 8
+ *    elements (16 bytes).
+ *  - Ownership: the caller allocates every buffer, including the workspace.
+ *    The library never allocates device memory, never synchronises the
+ *    stream or the device, and launches only on `stream` (a cudaStream_t;
+ *    NULL = legacy default stream).
+ *  - Errors: argument errors are detected on the host before any launch and
+ *    returned as a KDA_ERR_* code with nothing launched.  Bad values that only
+ *    the device can see (a slot id outside [0, num_slots)) make the kernel skip
+ *    that sequence/request and OR a KDA_DEVICE_* bit into the status word at
+ *    the start of the workspace; the word is sticky until kda_workspace_reset.
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define KDA_API __attribute__((visibility("default")))
+#else
+#define KDA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------- */
+#define KDA_OK 0
+#define KDA_ERR_INVALID_ARG 1 /* NULL / misaligned pointer, bad size or stride, bad cu_seqlens */
+#define KDA_ERR_UNSUPPORTED 2 /* lower_bound outside [-10, 0], non-finite scale, too many sequences */
+#define KDA_ERR_WORKSPACE 3   /* workspace NULL, misaligned or smaller than kda_workspace_size() */
+#define KDA_ERR_CUDA 4        /* a CUDA runtime call or kernel launch failed */
+
+/* ---- bits of the device status word (first 4 bytes of the workspace) ---- */
+#define KDA_DEVICE_BAD_SLOT 1u /* a slot id was outside [0, num_slots); that work item was skipped */
+
+/* ---- flags of kda_chunk_prefill ------------------------------------------ */
+#define KDA_LOAD_INITIAL 1  /* S0 of sequence n = state_pool[slot_ids[n]]; else S0 = 0          */
+#define KDA_FINAL_TO_POOL 2 /* final state of sequence n -> state_pool[slot_ids[n]]; else dense */
+
+/* Static, human-readable text for a status code. */
+KDA_API const char *kda_status_string(int status);
+
+/* Bytes of workspace every call needs (a multiple of 256). */
+KDA_API size_t kda_workspace_size(void);
+
+/* Clear the device status word (an async memset on `stream`). */
+KDA_API int kda_workspace_reset(void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Debug helper: wait for `stream`, then copy the device status word into
+ * *device_status.  This is the only call that synchronises.
+ */
+KDA_API int kda_read_device_status(const void *workspace, size_t workspace_bytes,
+                           uint32_t *device_status, void *stream);
+
+/*
+ * Chunked varlen prefill.  Source: vLLM PR #55737 "Use FlashKDA for KDA
+ * chunked prefill" (PR summary: bounded gate, in-kernel q/k l2norm, raw beta
+ * logits, output plus final state, output written straight into the caller's
+ * buffer); host cu_seqlens so that planning never reads device memory:
+ * TensorRT-LLM PR #21179, commit passing cu_seqlens_cpu to chunked prefill.
+ *
+ *  q, k, v          [T_total, H, 128] bf16, token stride qkv_token_stride
+ *  g                [T_total, H, 128] bf16 raw gate input, token stride g_token_stride
+ *  beta_logits      [T_total, H] bf16, token stride beta_token_stride
+ *  A_log [H], dt_bias [H,128] fp32; lower_bound in [-10, 0]; scale finite
+ *  cu_seqlens_dev   [num_seqs + 1] int32 on the device, cu_seqlens_host the
+ *                   same values in host memory (must be equal; starts at 0,
+ *                   non-decreasing).  Zero-length sequences are allowed: their
+ *                   final state is their initial state.
+ *  state_pool       [num_slots, H, 128, 128] fp32; required when flags has
+ *                   KDA_LOAD_INITIAL or KDA_FINAL_TO_POOL, with slot_ids
+ *                   [num_seqs] int32 (distinct when KDA_FINAL_TO_POOL).
+ *  out              [T_total, H, 128] bf16, token stride out_token_stride
+ *  final_state      [num_seqs, H, 128, 128] fp32 dense final states; required
+ *                   unless KDA_FINAL_TO_POOL (then ignored, may be NULL).
+ *  Inputs and outputs must not overlap, except state_pool which may be both
+ *  read and written (each sequence reads its slot before writing it).
+ */
+KDA_API int kda_chunk_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                      int64_t qkv_token_stride, const uint16_t *g, int64_t g_token_stride,
+                      const uint16_t *beta_logits, int64_t beta_token_stride,
+                      const float *A_log, const float *dt_bias, float lower_bound, float scale,
+                      const int32_t *cu_seqlens_dev, const int32_t *cu_seqlens_host,
+                      int num_seqs, int H, float *state_pool, int num_slots,
+                      const int32_t *slot_ids, int flags, uint16_t *out,
+                      int64_t out_token_stride, float *final_state, void *workspace,
+                      size_t workspace_bytes, void *stream);
+
+/*
+ * Speculative-decode verify over a pooled fp32 state.  Source: TensorRT-LLM
+ * PR #21179 "GLM-5.3-Flash FP8 performance fixes on Hopper", commit fusing
+ * the verify loop into one recurrent call that seeds from the pool state and
+ * writes step t's state to row (b, t), the live pool staying read-only.
+ *
+ *  q, k, v, g       [B*T, H, 128] bf16 (request b's draft tokens are rows b*T .. b*T+T-1)
+ *  beta_logits      [B*T, H] bf16
+ *  state_pool       [num_slots, H, 128, 128] fp32, READ ONLY
+ *  slot_ids         [B] int32, any values in [0, num_slots) (repeats allowed)
+ *  out              [B*T, H, 128] bf16
+ *  intermediate_states [B, T, H, 128, 128] fp32: row (b, t) = state after draft token t
+ *  1 <= T <= 64.
+ */
+KDA_API int kda_recurrent_verify(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                         int64_t qkv_token_stride, const uint16_t *g, int64_t g_token_stride,
+                         const uint16_t *beta_logits, int64_t beta_token_stride,
+                         const float *A_log, const float *dt_bias, float lower_bound,
+                         float scale, int B, int T, int H, const float *state_pool,
+                         int num_slots, const int32_t *slot_ids, uint16_t *out,
+                         int64_t out_token_stride, float *intermediate_states,
+                         void *workspace, size_t workspace_bytes, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */

@@ -1,0 +1,190 @@
+"""ctypes binding of libkda (``include/kda.h``), marshalling torch tensors.
+
+Argument marshalling only: every step of the computation runs in libkda's
+CUDA kernels.  PyTorch provides device memory and the current stream.  When
+the library has not been built this module raises instead of computing
+anything another way.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+from . import build as _build
+
+KDA_OK = 0
+KDA_ERR_INVALID_ARG = 1
+KDA_ERR_UNSUPPORTED = 2
+KDA_ERR_WORKSPACE = 3
+KDA_ERR_CUDA = 4
+KDA_DEVICE_BAD_SLOT = 1
+KDA_LOAD_INITIAL = 1
+KDA_FINAL_TO_POOL = 2
+
+#: exported symbols of include/kda.h
+EXPORTS = ("kda_status_string", "kda_workspace_size", "kda_workspace_reset", "kda_read_device_status",
+           "kda_chunk_prefill", "kda_recurrent_verify")
+
+_lib = None
+
+
+class KdaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+        self.status = status
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load():
+    """Load libkda; raise if it has not been built (no fallback exists)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = library_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"libkda is not built ({path} missing): run __graft_entry__.build() "
+                           "or `python -m kda_linear_attention_bounded_gb300.build`")
+    lib = ctypes.CDLL(path)
+    P, I, I64, F, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+    lib.kda_status_string.argtypes = [I]
+    lib.kda_status_string.restype = ctypes.c_char_p
+    lib.kda_workspace_size.argtypes = []
+    lib.kda_workspace_size.restype = SZ
+    lib.kda_workspace_reset.argtypes = [P, SZ, P]
+    lib.kda_workspace_reset.restype = I
+    lib.kda_read_device_status.argtypes = [P, SZ, ctypes.POINTER(ctypes.c_uint32), P]
+    lib.kda_read_device_status.restype = I
+    lib.kda_chunk_prefill.argtypes = [P, P, P, I64, P, I64, P, I64, P, P, F, F, P, P, I, I, P, I, P, I, P,
+                                      I64, P, P, SZ, P]
+    lib.kda_chunk_prefill.restype = I
+    lib.kda_recurrent_verify.argtypes = [P, P, P, I64, P, I64, P, I64, P, P, F, F, I, I, I, P, I, P, P, I64,
+                                         P, P, SZ, P]
+    lib.kda_recurrent_verify.restype = I
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load().kda_status_string(int(status)).decode()
+
+
+def workspace_size() -> int:
+    return int(load().kda_workspace_size())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_ptr(stream, device):
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def make_workspace(device=None, stream=None) -> torch.Tensor:
+    """Allocate (through torch) and clear a workspace for the calls."""
+    ws = torch.empty(workspace_size(), dtype=torch.uint8, device=device or "cuda")
+    rc = load().kda_workspace_reset(_ptr(ws), ws.numel(), _stream_ptr(stream, ws.device))
+    if rc != KDA_OK:
+        raise KdaError(rc, "kda_workspace_reset")
+    return ws
+
+
+def read_device_status(workspace: torch.Tensor, stream=None) -> int:
+    val = ctypes.c_uint32(0)
+    rc = load().kda_read_device_status(_ptr(workspace), workspace.numel(), ctypes.byref(val),
+                                       _stream_ptr(stream, workspace.device))
+    if rc != KDA_OK:
+        raise KdaError(rc, "kda_read_device_status")
+    return int(val.value)
+
+
+def _token_tensor(x, name, H):
+    if x.dtype != torch.bfloat16 or not x.is_cuda or x.dim() != 3:
+        raise ValueError(f"{name}: expected a CUDA bf16 tensor [tokens, H, 128]")
+    if x.shape[1] != H or x.shape[2] != 128 or x.stride(2) != 1 or x.stride(1) != 128:
+        raise ValueError(f"{name}: expected [tokens, {H}, 128] with contiguous heads")
+    return x.stride(0)
+
+
+def _beta_stride(b, H):
+    if b.dtype != torch.bfloat16 or not b.is_cuda or b.dim() != 2 or b.shape[1] != H or b.stride(1) != 1:
+        raise ValueError("beta_logits: expected a CUDA bf16 tensor [tokens, H]")
+    return b.stride(0)
+
+
+def chunk_prefill(q, k, v, g, beta_logits, A_log, dt_bias, cu_seqlens, cu_seqlens_host, *,
+                  lower_bound=-5.0, scale=None, state_pool=None, slot_ids=None, load_initial=False,
+                  final_to_pool=False, out=None, final_state=None, workspace=None, stream=None):
+    """``kda_chunk_prefill``.  Returns ``(out, final_state)`` (final_state is None
+    when the final states go to the pool)."""
+    lib = load()
+    H = q.shape[1]
+    qs = _token_tensor(q, "q", H)
+    if _token_tensor(k, "k", H) != qs or _token_tensor(v, "v", H) != qs:
+        raise ValueError("q, k and v must share one token stride")
+    gs = _token_tensor(g, "g", H)
+    bs = _beta_stride(beta_logits, H)
+    cu_host = torch.as_tensor(cu_seqlens_host, dtype=torch.int32).contiguous()
+    if cu_host.is_cuda:
+        raise ValueError("cu_seqlens_host must be in host memory")
+    N = cu_host.numel() - 1
+    T_total = q.shape[0]
+    dev = q.device
+    if out is None:
+        out = torch.empty((T_total, H, 128), dtype=torch.bfloat16, device=dev)
+    os_ = _token_tensor(out, "out", H)
+    if not final_to_pool and final_state is None:
+        final_state = torch.empty((N, H, 128, 128), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = make_workspace(dev, stream)
+    flags = (KDA_LOAD_INITIAL if load_initial else 0) | (KDA_FINAL_TO_POOL if final_to_pool else 0)
+    if scale is None:
+        scale = 1.0 / math.sqrt(128.0)
+    rc = lib.kda_chunk_prefill(
+        _ptr(q), _ptr(k), _ptr(v), qs, _ptr(g), gs, _ptr(beta_logits), bs, _ptr(A_log), _ptr(dt_bias),
+        float(lower_bound), float(scale), _ptr(cu_seqlens), ctypes.c_void_p(cu_host.data_ptr()), N, H,
+        _ptr(state_pool), 0 if state_pool is None else state_pool.shape[0], _ptr(slot_ids), flags,
+        _ptr(out), os_, _ptr(None if final_to_pool else final_state), _ptr(workspace), workspace.numel(),
+        _stream_ptr(stream, dev))
+    if rc != KDA_OK:
+        raise KdaError(rc, "kda_chunk_prefill")
+    return out, (None if final_to_pool else final_state)
+
+
+def recurrent_verify(q, k, v, g, beta_logits, A_log, dt_bias, state_pool, slot_ids, T, *,
+                     lower_bound=-5.0, scale=None, out=None, intermediate_states=None, workspace=None,
+                     stream=None):
+    """``kda_recurrent_verify``.  Returns ``(out, intermediate_states)``."""
+    lib = load()
+    H = q.shape[1]
+    qs = _token_tensor(q, "q", H)
+    if _token_tensor(k, "k", H) != qs or _token_tensor(v, "v", H) != qs:
+        raise ValueError("q, k and v must share one token stride")
+    gs = _token_tensor(g, "g", H)
+    bs = _beta_stride(beta_logits, H)
+    B = slot_ids.numel()
+    dev = q.device
+    if out is None:
+        out = torch.empty((B * T, H, 128), dtype=torch.bfloat16, device=dev)
+    os_ = _token_tensor(out, "out", H)
+    if intermediate_states is None:
+        intermediate_states = torch.empty((B, T, H, 128, 128), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = make_workspace(dev, stream)
+    if scale is None:
+        scale = 1.0 / math.sqrt(128.0)
+    rc = lib.kda_recurrent_verify(
+        _ptr(q), _ptr(k), _ptr(v), qs, _ptr(g), gs, _ptr(beta_logits), bs, _ptr(A_log), _ptr(dt_bias),
+        float(lower_bound), float(scale), B, int(T), H, _ptr(state_pool), state_pool.shape[0], _ptr(slot_ids),
+        _ptr(out), os_, _ptr(intermediate_states), _ptr(workspace), workspace.numel(), _stream_ptr(stream, dev))
+    if rc != KDA_OK:
+        raise KdaError(rc, "kda_recurrent_verify")
+    return out, intermediate_states

@@ -1,0 +1,163 @@
+// C ABI of libkda (declared in include/kda.h): host-side validation and
+// launch planning.  Every check that can be made on the host is made here,
+// before anything is launched; nothing here allocates device memory or
+// synchronises (except kda_read_device_status, a debug helper).
+#include <cmath>
+#include <cstdint>
+
+#include "kda_common.cuh"
+#include "kda_internal.h"
+
+namespace {
+
+constexpr size_t kWorkspaceBytes = 256;
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool good_stride(int64_t stride, int64_t min_elems) { return stride >= min_elems && stride % 8 == 0; }
+
+int check_workspace(const void *ws, size_t bytes) {
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0 || bytes < kWorkspaceBytes) return KDA_ERR_WORKSPACE;
+  return KDA_OK;
+}
+
+int check_gate(float lower_bound, float scale) {
+  if (!std::isfinite(lower_bound) || !std::isfinite(scale)) return KDA_ERR_UNSUPPORTED;
+  // The chunked kernel represents exp of up to 8 consecutive log-decays in
+  // fp32; |lower_bound| <= 10 keeps that below e^80.  Positive bounds would
+  // make the state grow and are outside the method's convention.
+  if (lower_bound < -10.0f || lower_bound > 0.0f) return KDA_ERR_UNSUPPORTED;
+  return KDA_OK;
+}
+
+int check_token_tensors(const uint16_t *q, const uint16_t *k, const uint16_t *v, int64_t qkv_stride,
+                        const uint16_t *g, int64_t g_stride, const uint16_t *beta,
+                        int64_t beta_stride, const float *A_log, const float *dt_bias,
+                        const uint16_t *out, int64_t out_stride, int H) {
+  if (H <= 0 || H > 4096) return KDA_ERR_INVALID_ARG;
+  const int64_t row = (int64_t)H * kda::kD;
+  if (!q || !k || !v || !g || !beta || !A_log || !dt_bias || !out) return KDA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(out) ||
+      !aligned16(dt_bias))
+    return KDA_ERR_INVALID_ARG;
+  if (!good_stride(qkv_stride, row) || !good_stride(g_stride, row) || !good_stride(out_stride, row))
+    return KDA_ERR_INVALID_ARG;
+  if (beta_stride < H) return KDA_ERR_INVALID_ARG;
+  return KDA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *kda_status_string(int status) {
+  switch (status) {
+    case KDA_OK: return "KDA_OK";
+    case KDA_ERR_INVALID_ARG: return "KDA_ERR_INVALID_ARG: invalid pointer, size, stride or cu_seqlens";
+    case KDA_ERR_UNSUPPORTED: return "KDA_ERR_UNSUPPORTED: lower_bound outside [-10, 0], non-finite scale, or too many sequences";
+    case KDA_ERR_WORKSPACE: return "KDA_ERR_WORKSPACE: workspace missing, misaligned or too small";
+    case KDA_ERR_CUDA: return "KDA_ERR_CUDA: a CUDA call or kernel launch failed";
+    default: return "KDA: unknown status";
+  }
+}
+
+size_t kda_workspace_size(void) { return kWorkspaceBytes; }
+
+int kda_workspace_reset(void *workspace, size_t workspace_bytes, void *stream) {
+  if (int rc = check_workspace(workspace, workspace_bytes)) return rc;
+  return cudaMemsetAsync(workspace, 0, kWorkspaceBytes, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? KDA_OK
+             : KDA_ERR_CUDA;
+}
+
+int kda_read_device_status(const void *workspace, size_t workspace_bytes, uint32_t *device_status,
+                           void *stream) {
+  if (int rc = check_workspace(workspace, workspace_bytes)) return rc;
+  if (!device_status) return KDA_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(device_status, workspace, sizeof(uint32_t), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return KDA_ERR_CUDA;
+  return cudaStreamSynchronize(s) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+int kda_chunk_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v, int64_t qkv_token_stride,
+                      const uint16_t *g, int64_t g_token_stride, const uint16_t *beta_logits,
+                      int64_t beta_token_stride, const float *A_log, const float *dt_bias,
+                      float lower_bound, float scale, const int32_t *cu_seqlens_dev,
+                      const int32_t *cu_seqlens_host, int num_seqs, int H, float *state_pool,
+                      int num_slots, const int32_t *slot_ids, int flags, uint16_t *out,
+                      int64_t out_token_stride, float *final_state, void *workspace,
+                      size_t workspace_bytes, void *stream) {
+  if (int rc = check_workspace(workspace, workspace_bytes)) return rc;
+  if (num_seqs < 0) return KDA_ERR_INVALID_ARG;
+  if (!cu_seqlens_dev || !cu_seqlens_host) return KDA_ERR_INVALID_ARG;
+  if (flags & ~(KDA_LOAD_INITIAL | KDA_FINAL_TO_POOL)) return KDA_ERR_INVALID_ARG;
+  if (cu_seqlens_host[0] != 0) return KDA_ERR_INVALID_ARG;
+  for (int n = 0; n < num_seqs; ++n)
+    if (cu_seqlens_host[n + 1] < cu_seqlens_host[n]) return KDA_ERR_INVALID_ARG;
+  if (num_seqs == 0) return KDA_OK;
+  if (int rc = check_token_tensors(q, k, v, qkv_token_stride, g, g_token_stride, beta_logits,
+                                   beta_token_stride, A_log, dt_bias, out, out_token_stride, H))
+    return rc;
+  if (int rc = check_gate(lower_bound, scale)) return rc;
+  const bool use_pool = flags & (KDA_LOAD_INITIAL | KDA_FINAL_TO_POOL);
+  if (use_pool && (!state_pool || !slot_ids || num_slots <= 0 || !aligned16(state_pool)))
+    return KDA_ERR_INVALID_ARG;
+  if (!(flags & KDA_FINAL_TO_POOL) && (!final_state || !aligned16(final_state))) return KDA_ERR_INVALID_ARG;
+
+  kda::ChunkArgs a{};
+  a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta_logits;
+  a.qkv_stride = qkv_token_stride; a.g_stride = g_token_stride;
+  a.beta_stride = beta_token_stride; a.out_stride = out_token_stride;
+  a.A_log = A_log; a.dt_bias = dt_bias;
+  a.lower_bound = lower_bound; a.scale = scale;
+  a.H = H; a.num_seqs = num_seqs; a.total_tokens = cu_seqlens_host[num_seqs];
+  a.cu_seqlens = cu_seqlens_dev;
+  a.slot_ids = use_pool ? slot_ids : nullptr;
+  a.num_slots = num_slots;
+  a.state_in = (flags & KDA_LOAD_INITIAL) ? state_pool : nullptr;
+  a.state_out_pool = (flags & KDA_FINAL_TO_POOL) ? state_pool : nullptr;
+  a.state_out_dense = (flags & KDA_FINAL_TO_POOL) ? nullptr : final_state;
+  a.out = out;
+  a.status = static_cast<uint32_t *>(workspace);
+  cudaError_t err = kda::launch_chunk_prefill(a, cu_seqlens_host, static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+int kda_recurrent_verify(const uint16_t *q, const uint16_t *k, const uint16_t *v, int64_t qkv_token_stride,
+                         const uint16_t *g, int64_t g_token_stride, const uint16_t *beta_logits,
+                         int64_t beta_token_stride, const float *A_log, const float *dt_bias,
+                         float lower_bound, float scale, int B, int T, int H, const float *state_pool,
+                         int num_slots, const int32_t *slot_ids, uint16_t *out, int64_t out_token_stride,
+                         float *intermediate_states, void *workspace, size_t workspace_bytes,
+                         void *stream) {
+  if (int rc = check_workspace(workspace, workspace_bytes)) return rc;
+  if (B < 0 || T < 1 || T > 64) return KDA_ERR_INVALID_ARG;
+  if (B == 0) return KDA_OK;
+  if (int rc = check_token_tensors(q, k, v, qkv_token_stride, g, g_token_stride, beta_logits,
+                                   beta_token_stride, A_log, dt_bias, out, out_token_stride, H))
+    return rc;
+  if (int rc = check_gate(lower_bound, scale)) return rc;
+  if (!state_pool || !aligned16(state_pool) || num_slots <= 0 || !slot_ids) return KDA_ERR_INVALID_ARG;
+  if (!intermediate_states || !aligned16(intermediate_states)) return KDA_ERR_INVALID_ARG;
+
+  kda::RecurrentArgs a{};
+  a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta_logits;
+  a.qkv_stride = qkv_token_stride; a.g_stride = g_token_stride;
+  a.beta_stride = beta_token_stride; a.out_stride = out_token_stride;
+  a.A_log = A_log; a.dt_bias = dt_bias;
+  a.lower_bound = lower_bound; a.scale = scale;
+  a.H = H;
+  a.cu_seqlens = nullptr;
+  a.T = T;
+  a.slot_ids = slot_ids;
+  a.num_slots = num_slots;
+  a.state_in = state_pool;
+  a.inter = intermediate_states;
+  a.out = out;
+  a.status = static_cast<uint32_t *>(workspace);
+  cudaError_t err = kda::launch_recurrent(a, B, static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,189 @@
+// Token-by-token KDA recurrence on CUDA cores: the speculative-verify kernel.
+//
+// Verify (TensorRT-LLM PR #21179 "GLM-5.3-Flash FP8 performance fixes on
+// Hopper", commit fusing the verify loop): one launch seeds every (request,
+// head) from the pooled fp32 state, runs the T draft tokens and writes the
+// state after each token to intermediate_states[b, t]; the pool is only read.
+//
+// The work is HBM-bound: per (request, head) it reads 64 KiB of state and
+// writes T x 64 KiB of per-step states.  Layout per CTA (one (b, h) pair,
+// 256 threads = 8 warps): warp w owns key channels c = 16w .. 16w+15, lane l
+// owns value channels d = 4l .. 4l+3, so every row of S moves as one
+// coalesced 512-byte warp access of 16-byte vectors (loads of the pool,
+// streaming stores of the per-step states).
+//
+// Per token the state update is rewritten so that ONE cross-warp reduction
+// serves both the correction and the output:
+//   u   = beta (v - S^T (alpha o k^))
+//   o   = scale (S^T (alpha o q^) + (k^ . q^) u)          [= scale S_t^T q^]
+//   S_t = Diag(alpha) S + k^ u^T
+#include "kda_common.cuh"
+#include "kda_internal.h"
+
+namespace kda {
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kTile = kWarps;      // tokens prepared per prologue pass (one per warp)
+constexpr int kRows = kD / kWarps;  // key channels per warp (16)
+
+__global__ void __launch_bounds__(kThreads, 2) recurrent_kernel(RecurrentArgs p) {
+  __shared__ __align__(16) float s_khat[kTile][kD];
+  __shared__ __align__(16) float s_kalpha[kTile][kD];
+  __shared__ __align__(16) float s_qalpha[kTile][kD];
+  __shared__ __align__(16) float s_alpha[kTile][kD];
+  __shared__ __align__(16) float s_v[kTile][kD];
+  __shared__ float s_beta[kTile], s_kq[kTile];
+  __shared__ __align__(16) float s_redk[kWarps][kD];
+  __shared__ __align__(16) float s_redq[kWarps][kD];
+  __shared__ __align__(16) float s_u[kD];
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int h = blockIdx.x % p.H;
+  const int n = blockIdx.x / p.H;
+  const int t_begin = p.cu_seqlens ? p.cu_seqlens[n] : n * p.T;
+  const int t_end = p.cu_seqlens ? p.cu_seqlens[n + 1] : (n + 1) * p.T;
+
+  int slot = -1;
+  if (p.slot_ids) {
+    slot = p.slot_ids[n];
+    if (slot < 0 || slot >= p.num_slots) {
+      if (tid == 0) atomicOr(p.status, KDA_DEVICE_BAD_SLOT);
+      return;
+    }
+  }
+
+  const int row0 = warp * kRows;
+  const int col0 = lane * 4;
+  float S[kRows][4];
+  if (p.state_in) {
+    const float *src = p.state_in + ((size_t)slot * p.H + h) * kD * kD;
+#pragma unroll
+    for (int i = 0; i < kRows; ++i) {
+      float4 x = __ldg(reinterpret_cast<const float4 *>(src + (size_t)(row0 + i) * kD + col0));
+      S[i][0] = x.x; S[i][1] = x.y; S[i][2] = x.z; S[i][3] = x.w;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < kRows; ++i) S[i][0] = S[i][1] = S[i][2] = S[i][3] = 0.f;
+  }
+
+  // per-head gate constants for this lane's 4 channels
+  const float ea = __expf(p.A_log[h]);
+  float dtb[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) dtb[j] = p.dt_bias[h * kD + col0 + j];
+
+  for (int tile = t_begin; tile < t_end; tile += kTile) {
+    const int nt = min(kTile, t_end - tile);
+    // ---- prologue: warp w prepares token tile + w ----
+    if (warp < nt) {
+      const int t = tile + warp;
+      const uint2 qr = *reinterpret_cast<const uint2 *>(p.q + (size_t)t * p.qkv_stride + h * kD + col0);
+      const uint2 kr = *reinterpret_cast<const uint2 *>(p.k + (size_t)t * p.qkv_stride + h * kD + col0);
+      const uint2 vr = *reinterpret_cast<const uint2 *>(p.v + (size_t)t * p.qkv_stride + h * kD + col0);
+      const uint2 gr = *reinterpret_cast<const uint2 *>(p.g + (size_t)t * p.g_stride + h * kD + col0);
+      const uint16_t *qs = reinterpret_cast<const uint16_t *>(&qr);
+      const uint16_t *ks = reinterpret_cast<const uint16_t *>(&kr);
+      const uint16_t *vs = reinterpret_cast<const uint16_t *>(&vr);
+      const uint16_t *gs = reinterpret_cast<const uint16_t *>(&gr);
+      float qf[4], kf[4], qq = 0.f, kk = 0.f;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        qf[j] = bf16_bits_to_f32(qs[j]);
+        kf[j] = bf16_bits_to_f32(ks[j]);
+        qq += qf[j] * qf[j];
+        kk += kf[j] * kf[j];
+      }
+      qq = warp_sum(qq);
+      kk = warp_sum(kk);
+      const float nq = rsqrtf(qq + kL2Eps), nk = rsqrtf(kk + kL2Eps);
+      float kq = 0.f;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float qh = qf[j] * nq, kh = kf[j] * nk;
+        kq += qh * kh;
+        const float lam = p.lower_bound * sigmoid_f(ea * (bf16_bits_to_f32(gs[j]) + dtb[j]));
+        const float alpha = fast_exp2(lam * kLog2e);
+        s_khat[warp][col0 + j] = kh;
+        s_kalpha[warp][col0 + j] = alpha * kh;
+        s_qalpha[warp][col0 + j] = alpha * qh;
+        s_alpha[warp][col0 + j] = alpha;
+        s_v[warp][col0 + j] = bf16_bits_to_f32(vs[j]);
+      }
+      kq = warp_sum(kq);
+      if (lane == 0) {
+        s_kq[warp] = kq;
+        s_beta[warp] = sigmoid_f(bf16_bits_to_f32(p.beta[(size_t)t * p.beta_stride + h]));
+      }
+    }
+    __syncthreads();
+
+    for (int s = 0; s < nt; ++s) {
+      const int t = tile + s;
+      // partial S^T (alpha k^) and S^T (alpha q^) over this warp's 16 rows
+      float pk[4] = {0.f, 0.f, 0.f, 0.f}, pq[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int i = 0; i < kRows; ++i) {
+        const float ka = s_kalpha[s][row0 + i], qa = s_qalpha[s][row0 + i];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          pk[j] = fmaf(S[i][j], ka, pk[j]);
+          pq[j] = fmaf(S[i][j], qa, pq[j]);
+        }
+      }
+      *reinterpret_cast<float4 *>(&s_redk[warp][col0]) = make_float4(pk[0], pk[1], pk[2], pk[3]);
+      *reinterpret_cast<float4 *>(&s_redq[warp][col0]) = make_float4(pq[0], pq[1], pq[2], pq[3]);
+      __syncthreads();
+      if (tid < kD) {
+        float wk = 0.f, wq = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+          wk += s_redk[w][tid];
+          wq += s_redq[w][tid];
+        }
+        const float u = s_beta[s] * (s_v[s][tid] - wk);
+        s_u[tid] = u;
+        const float o = p.scale * (wq + s_kq[s] * u);
+        p.out[(size_t)t * p.out_stride + h * kD + tid] = f32_to_bf16_bits(o);
+      }
+      __syncthreads();
+      const float4 u4 = *reinterpret_cast<const float4 *>(&s_u[col0]);
+      float *rec = p.inter ? p.inter + (((size_t)n * p.T + (t - t_begin)) * p.H + h) * kD * kD : nullptr;
+#pragma unroll
+      for (int i = 0; i < kRows; ++i) {
+        const float a = s_alpha[s][row0 + i], kh = s_khat[s][row0 + i];
+        S[i][0] = fmaf(a, S[i][0], kh * u4.x);
+        S[i][1] = fmaf(a, S[i][1], kh * u4.y);
+        S[i][2] = fmaf(a, S[i][2], kh * u4.z);
+        S[i][3] = fmaf(a, S[i][3], kh * u4.w);
+        if (rec)
+          __stcs(reinterpret_cast<float4 *>(rec + (size_t)(row0 + i) * kD + col0),
+                 make_float4(S[i][0], S[i][1], S[i][2], S[i][3]));
+      }
+    }
+    __syncthreads();
+  }
+
+  float *dst = nullptr;
+  if (p.state_out_pool) dst = p.state_out_pool + ((size_t)slot * p.H + h) * kD * kD;
+  else if (p.state_out_dense) dst = p.state_out_dense + ((size_t)n * p.H + h) * kD * kD;
+  if (dst) {
+#pragma unroll
+    for (int i = 0; i < kRows; ++i)
+      *reinterpret_cast<float4 *>(dst + (size_t)(row0 + i) * kD + col0) =
+          make_float4(S[i][0], S[i][1], S[i][2], S[i][3]);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_recurrent(const RecurrentArgs &args, int num_items, cudaStream_t stream) {
+  if (num_items <= 0) return cudaSuccess;
+  recurrent_kernel<<<num_items * args.H, kThreads, 0, stream>>>(args);
+  return cudaGetLastError();
+}
+
+}  // namespace kda

@@ -1,0 +1,100 @@
+"""Helpers shared by the GPU parity tests: move seeded inputs to the device,
+call the library through its binding, and compare against the oracle."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import kda_linear_attention_bounded_gb300 as kda
+
+# Tolerances of the parity bar (outputs vs the fp64 oracle after the GPU's bf16
+# rounding; states in fp32).
+OUT_REL_L2 = 1e-2
+OUT_MAX_ABS = 3e-2
+STATE_REL_L2 = 5e-3
+
+
+def bf16_dev(bits: np.ndarray, device="cuda") -> torch.Tensor:
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16))
+    return t.to(device).view(torch.bfloat16)
+
+
+def f32_dev(x: np.ndarray, device="cuda") -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(device)
+
+
+def i32_dev(x: np.ndarray, device="cuda") -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.int32)).to(device)
+
+
+def rel_l2(x, ref):
+    x = np.asarray(x, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    den = np.linalg.norm(ref)
+    return float(np.linalg.norm(x - ref) / den) if den > 0 else float(np.linalg.norm(x))
+
+
+def check_out(out_gpu, out_ref, what):
+    x = out_gpu.float().cpu().numpy().astype(np.float64) if torch.is_tensor(out_gpu) else out_gpu
+    assert np.isfinite(x).all(), f"{what}: non-finite GPU output"
+    r = rel_l2(x, out_ref)
+    m = float(np.abs(x - out_ref).max()) if x.size else 0.0
+    assert r <= OUT_REL_L2 and m <= OUT_MAX_ABS, f"{what}: rel-L2 {r:.3e} (<= {OUT_REL_L2}), max-abs {m:.3e} (<= {OUT_MAX_ABS})"
+    return r, m
+
+
+def check_state(s_gpu, s_ref, what):
+    x = s_gpu.cpu().numpy().astype(np.float64) if torch.is_tensor(s_gpu) else s_gpu
+    assert np.isfinite(x).all(), f"{what}: non-finite GPU state"
+    r = rel_l2(x, s_ref)
+    assert r <= STATE_REL_L2, f"{what}: rel-L2 {r:.3e} (<= {STATE_REL_L2})"
+    return r
+
+
+class DevicePrefill:
+    """Device copies of one prefill workload (``inputs.PrefillInputs``)."""
+
+    def __init__(self, inp, device="cuda", token_pad=0):
+        self.inp = inp
+        H = inp.H
+        T = inp.total_tokens
+
+        def tok(bits):
+            if token_pad == 0:
+                return bf16_dev(bits, device)
+            # token stride larger than H*128: embed in a wider row
+            buf = torch.zeros((T, H * 128 + token_pad), dtype=torch.bfloat16, device=device)
+            buf[:, :H * 128] = bf16_dev(bits, device).reshape(T, H * 128)
+            return buf[:, :H * 128].view(T, H, 128)
+
+        self.q, self.k, self.v, self.g = tok(inp.q), tok(inp.k), tok(inp.v), tok(inp.g)
+        self.beta = bf16_dev(inp.beta, device)
+        self.A_log = f32_dev(inp.A_log, device)
+        self.dt_bias = f32_dev(inp.dt_bias, device)
+        self.cu = i32_dev(inp.cu_seqlens, device)
+        self.cu_host = torch.from_numpy(inp.cu_seqlens.astype(np.int32))
+        self.pool = f32_dev(inp.pool, device) if inp.pool is not None else None
+        self.slots = i32_dev(inp.slot_ids, device) if inp.slot_ids is not None else None
+
+    def run(self, **kw):
+        inp = self.inp
+        return kda.chunk_prefill(self.q, self.k, self.v, self.g, self.beta, self.A_log, self.dt_bias, self.cu,
+                                 self.cu_host, lower_bound=inp.lower_bound, scale=inp.scale,
+                                 state_pool=self.pool, slot_ids=self.slots, load_initial=inp.load_initial,
+                                 final_to_pool=inp.final_to_pool, **kw)
+
+
+class DeviceVerify:
+    def __init__(self, inp, device="cuda"):
+        self.inp = inp
+        self.q, self.k, self.v, self.g = (bf16_dev(x, device) for x in (inp.q, inp.k, inp.v, inp.g))
+        self.beta = bf16_dev(inp.beta, device)
+        self.A_log = f32_dev(inp.A_log, device)
+        self.dt_bias = f32_dev(inp.dt_bias, device)
+        self.pool = f32_dev(inp.pool, device)
+        self.slots = i32_dev(inp.slot_ids, device)
+
+    def run(self, **kw):
+        inp = self.inp
+        return kda.recurrent_verify(self.q, self.k, self.v, self.g, self.beta, self.A_log, self.dt_bias, self.pool,
+                                    self.slots, inp.T, lower_bound=inp.lower_bound, scale=inp.scale, **kw)

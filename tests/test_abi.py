@@ -1,0 +1,108 @@
+"""CPU checks of the C ABI: libkda builds, loads without a GPU, exports every
+symbol include/kda.h declares, and rejects bad arguments on the host before
+anything is launched (no CUDA call is reached by these cases)."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from kda_linear_attention_bounded_gb300 import build as kbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kda.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    path = kbuild.build()
+    from kda_linear_attention_bounded_gb300 import _binding
+    return _binding.load()
+
+
+def declared_symbols():
+    src = open(HEADER).read()
+    return sorted(set(re.findall(r"KDA_API\s+[\w\s\*]*?\b(kda_\w+)\s*\(", src)))
+
+
+def test_header_declares_the_entry_points():
+    syms = declared_symbols()
+    for name in ("kda_chunk_prefill", "kda_recurrent_verify", "kda_workspace_size", "kda_status_string"):
+        assert name in syms
+
+
+def test_every_declared_symbol_is_exported(lib):
+    missing = [s for s in declared_symbols() if not hasattr(lib, s)]
+    assert not missing, f"not exported: {missing}"
+
+
+def test_status_strings(lib):
+    from kda_linear_attention_bounded_gb300 import _binding as b
+    for code in range(0, 5):
+        assert b.status_string(code).startswith("KDA_")
+    assert "unknown" in b.status_string(99)
+
+
+def test_workspace_size(lib):
+    n = lib.kda_workspace_size()
+    assert n > 0 and n % 256 == 0
+
+
+# ---- host-side validation (fake, aligned device addresses; never dereferenced) ----
+FAKE = 0x10000000
+P = ctypes.c_void_p
+
+
+def _prefill(lib, *, cu=(0, 4), H=2, lb=-5.0, scale=0.1, ws=FAKE, ws_bytes=256, stride=256, flags=0,
+             q=FAKE, final=FAKE, pool=None, slots=None, nslots=0):
+    cu_host = np.array(cu, np.int32)
+    return lib.kda_chunk_prefill(P(q), P(FAKE), P(FAKE), stride, P(FAKE), stride, P(FAKE), H, P(FAKE), P(FAKE),
+                                 lb, scale, P(FAKE), cu_host.ctypes.data_as(P), len(cu) - 1, H, P(pool), nslots,
+                                 P(slots), flags, P(FAKE), stride, P(final), P(ws), ws_bytes, None)
+
+
+def _verify(lib, *, B=2, T=8, H=2, lb=-5.0, ws=FAKE, pool=FAKE, inter=FAKE):
+    return lib.kda_recurrent_verify(P(FAKE), P(FAKE), P(FAKE), H * 128, P(FAKE), H * 128, P(FAKE), H, P(FAKE),
+                                    P(FAKE), lb, 0.1, B, T, H, P(pool), 4, P(FAKE), P(FAKE), H * 128, P(inter),
+                                    P(ws), 256, None)
+
+
+def test_prefill_rejects_bad_arguments(lib):
+    assert _prefill(lib, ws=None) == 3
+    assert _prefill(lib, ws=FAKE + 16) == 3           # misaligned workspace
+    assert _prefill(lib, ws_bytes=16) == 3
+    assert _prefill(lib, cu=(0, 5, 3)) == 1            # decreasing cu_seqlens
+    assert _prefill(lib, cu=(1, 5)) == 1               # not starting at 0
+    assert _prefill(lib, lb=-20.0) == 2                # outside the supported bound
+    assert _prefill(lib, lb=0.5) == 2
+    assert _prefill(lib, lb=float("nan")) == 2
+    assert _prefill(lib, scale=float("inf")) == 2
+    assert _prefill(lib, stride=100) == 1              # stride below H*128
+    assert _prefill(lib, stride=260) == 1              # stride not a multiple of 8
+    assert _prefill(lib, q=FAKE + 2) == 1              # misaligned pointer
+    assert _prefill(lib, q=None) == 1
+    assert _prefill(lib, final=None) == 1              # dense final state required
+    assert _prefill(lib, flags=1) == 1                 # pool + slot ids required
+    assert _prefill(lib, flags=8) == 1                 # unknown flag
+    assert _prefill(lib, H=0) == 1
+    assert _prefill(lib, cu=(0,)) == 0                 # no sequences: nothing to do
+
+
+def test_verify_rejects_bad_arguments(lib):
+    assert _verify(lib, ws=None) == 3
+    assert _verify(lib, T=0) == 1
+    assert _verify(lib, T=65) == 1
+    assert _verify(lib, B=-1) == 1
+    assert _verify(lib, lb=-11.0) == 2
+    assert _verify(lib, pool=None) == 1
+    assert _verify(lib, inter=None) == 1
+    assert _verify(lib, B=0) == 0                      # no requests: nothing to do
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    from kda_linear_attention_bounded_gb300 import _binding as b
+    monkeypatch.setattr(b, "_lib", None)
+    monkeypatch.setattr(b, "library_path", lambda: str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        b.load()

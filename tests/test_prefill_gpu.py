@@ -1,0 +1,83 @@
+"""Parity of kda_chunk_prefill (CUDA, through the C ABI) with the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from kda_linear_attention_bounded_gb300 import inputs
+import kda_linear_attention_bounded_gb300 as kda
+from gpu_helpers import DevicePrefill, check_out, check_state
+
+pytestmark = pytest.mark.gpu
+
+
+def _parity(inp, token_pad=0, heads=None):
+    dev = DevicePrefill(inp, token_pad=token_pad)
+    pool_before = dev.pool.clone() if dev.pool is not None else None
+    ws = kda.make_workspace()
+    out, final = dev.run(workspace=ws)
+    torch.cuda.synchronize()
+    assert kda.read_device_status(ws) == 0
+    ref_out, ref_S, _ = oracle.run_prefill(inp, heads=heads)
+    hb, he = heads or (0, inp.H)
+    check_out(out[:, hb:he], ref_out[:, hb:he], f"{inp.name} outputs")
+    if inp.final_to_pool:
+        got = dev.pool[torch.from_numpy(inp.slot_ids).long().cuda()]
+        check_state(got[:, hb:he], ref_S[:, hb:he], f"{inp.name} final states (pool)")
+        untouched = np.setdiff1d(np.arange(inp.pool.shape[0]), inp.slot_ids)
+        idx = torch.from_numpy(untouched).long().cuda()
+        assert torch.equal(dev.pool[idx], pool_before[idx]), "pool slots not in slot_ids were modified"
+    else:
+        check_state(final[:, hb:he], ref_S[:, hb:he], f"{inp.name} final states")
+        if pool_before is not None:
+            assert torch.equal(dev.pool, pool_before), "pool modified without KDA_FINAL_TO_POOL"
+    return out, final
+
+
+def test_tiny_1x256_h2():
+    _parity(inputs.tiny_prefill())
+
+
+@pytest.mark.parametrize("lens", [[1], [63], [64], [65], [1, 63, 64, 65, 130, 0, 200], [0, 0, 3]])
+def test_varlen_ragged_pool_in(lens):
+    inp = inputs.prefill_inputs("ragged", lens, 4, seed=11 + len(lens), pool_slots=16, load_initial=True)
+    _parity(inp)
+
+
+def test_varlen_final_to_pool_inplace():
+    inp = inputs.prefill_inputs("inplace", [100, 7, 256], 3, seed=21, pool_slots=8, load_initial=True,
+                                final_to_pool=True)
+    _parity(inp)
+
+
+@pytest.mark.parametrize("case", ["weak_gate", "weak_bound", "bound_-10", "bound_0"])
+def test_decay_regimes(case):
+    kw = dict(weak_gate=dict(g_mean=-8.0), weak_bound=dict(lower_bound=-0.05),
+              **{"bound_-10": dict(lower_bound=-10.0), "bound_0": dict(lower_bound=0.0)})[case]
+    inp = inputs.prefill_inputs(case, [300, 77], 4, seed=31, pool_slots=4, load_initial=True, **kw)
+    _parity(inp)
+
+
+def test_strided_token_rows():
+    inp = inputs.prefill_inputs("strided", [130, 64], 2, seed=41)
+    _parity(inp, token_pad=256)
+
+
+def test_bad_slot_sets_status_and_skips():
+    inp = inputs.prefill_inputs("badslot", [70, 50], 2, seed=51, pool_slots=4, load_initial=True)
+    dev = DevicePrefill(inp)
+    dev.slots[1] = 99
+    ws = kda.make_workspace()
+    out = torch.full((inp.total_tokens, 2, 128), 7.0, dtype=torch.bfloat16, device="cuda")
+    out, final = dev.run(workspace=ws, out=out)
+    torch.cuda.synchronize()
+    assert kda.read_device_status(ws) & kda.KDA_DEVICE_BAD_SLOT
+    ref_out, ref_S, _ = oracle.run_prefill(inp)
+    check_out(out[:70], ref_out[:70], "good sequence next to a bad slot")
+    assert (out[70:].float() == 7.0).all(), "skipped sequence must not be written"
+
+
+@pytest.mark.parametrize("make", [inputs.prefill_2048x8, inputs.prefill_8192x4, inputs.varlen_16384_plus_16],
+                         ids=["2048x8", "8192x4", "16384+16varlen"])
+def test_full_size(make):
+    _parity(make())
