@@ -144,6 +144,34 @@ KDA_API int kda_recurrent_verify(const uint16_t *q, const uint16_t *k, const uin
                          int64_t out_token_stride, float *intermediate_states,
                          void *workspace, size_t workspace_bytes, void *stream);
 
+/*
+ * kda_recurrent_verify without a workspace.  The pages have no counterpart:
+ * this is a convenience for callers that cannot allocate device memory where
+ * they run the layer (an engine plugin whose device memory is planned ahead
+ * and may not grow while executing, or code that must avoid cudaMalloc because
+ * it can synchronise the device).  Arguments and results are those of
+ * kda_recurrent_verify minus the workspace; nothing is allocated.
+ *
+ *  - The scratch (the status word) lives in a fixed 4 KiB device array inside
+ *    libkda, held by every GPU that loads the library until the process exits.
+ *    A call needs kda_workspace_size() bytes of it; if that ever exceeded the
+ *    array the call would return KDA_ERR_WORKSPACE without launching.
+ *  - The first call on a device looks up the array's device address (with
+ *    that device current) and caches it; make that first call before any
+ *    stream capture.
+ *  - Every call shares the one array: the call clears the status word first,
+ *    and calls whose work overlaps on the GPU (different streams, no ordering)
+ *    race on it.  Slot ids outside [0, num_slots) are skipped as in
+ *    kda_recurrent_verify, but this entry point does not report them.
+ */
+KDA_API int kda_recurrent_verify_noalloc(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                                 int64_t qkv_token_stride, const uint16_t *g, int64_t g_token_stride,
+                                 const uint16_t *beta_logits, int64_t beta_token_stride,
+                                 const float *A_log, const float *dt_bias, float lower_bound,
+                                 float scale, int B, int T, int H, const float *state_pool,
+                                 int num_slots, const int32_t *slot_ids, uint16_t *out,
+                                 int64_t out_token_stride, float *intermediate_states, void *stream);
+
 #ifdef __cplusplus
 }
 #endif
