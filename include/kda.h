@@ -66,6 +66,7 @@ extern "C" {
 
 /* ---- bits of the device status word (first 4 bytes of the workspace) ---- */
 #define KDA_DEVICE_BAD_SLOT 1u /* a slot id was outside [0, num_slots); that work item was skipped */
+#define KDA_DEVICE_TIMEOUT 2u  /* a bounded wait inside a kernel gave up (a lost async completion); results are incomplete */
 
 /* ---- flags of kda_chunk_prefill ------------------------------------------ */
 #define KDA_LOAD_INITIAL 1  /* S0 of sequence n = state_pool[slot_ids[n]]; else S0 = 0          */
