@@ -26,14 +26,13 @@
 //    caller's token stride);
 //  * A and P need exp(b_r - b_i) inside the contraction over c, and b spans
 //    up to 64 * |lower_bound| within a chunk -- far outside fp32.  They are
-//    built from 16-row sub-blocks: with m_R = b at row 7 of block R and
-//    a_I = b at row 15 of block I,
-//      same block:  e^(b_r - b_i) = e^(b_r - m_R) * e^(m_R - b_i)   (|exponents| <= 8 |lb|)
-//      block I < R: e^(b_r - b_i) = [e^(b_r - m_R) e^(m_R - a_I)] * e^(a_I - b_i)
-//    The per-channel factor e^(m_R - a_I) (<= 1) depends on both blocks, so
-//    these 16x16x128 products use warp-level mma.sync with that factor
-//    applied to the operand fragments in registers; materialising one scaled
-//    copy per block pair for tcgen05 would multiply the operand preparation.
+//    built from 16-row sub-blocks R.  With m_R = b at row 7 of block R:
+//      same block:   e^(b_r - b_i) = e^(b_r - m_R) * e^(m_R - b_i)      (|exponents| <= 8 |lb|)
+//      block I < R:  e^(b_r - b_i) = e^(b_r - m_R) * e^(m_R - b_i)      (second factor <= 1)
+//    so one M = 128 tcgen05.mma of [F^K; F^Q] (k^, q^ o e^(b - m_R(row)))
+//    against G (k^ o e^(m_R(row) - b)) yields every diagonal 16x16 block of A
+//    and P, and one more MMA per row block R against k^_i o e^(m_R - b_i)
+//    (i < 16R) yields its off-diagonal blocks;
 //  * T by blocked forward substitution in fp32 on CUDA cores.
 #include <cuda.h>
 
@@ -51,8 +50,8 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kC = 64;          // chunk length
-constexpr int kThreads = 256;   // 8 warps
+constexpr int kC = 64;             // chunk length
+constexpr int kThreads = 512;      // 16 warps
 constexpr int kTileBytes = 16384;  // one 64 x 128 bf16 tile
 
 // ---- shared memory map (offsets from a 1024-byte aligned base) ----
@@ -60,22 +59,33 @@ constexpr uint32_t OFF_Q = 0;        // q (TMA) -> Q+ = q^ o e^b, in place
 constexpr uint32_t OFF_K = 16384;    // k (TMA) -> K+ = k^ o e^b, in place
 constexpr uint32_t OFF_V = 32768;    // v (TMA)
 constexpr uint32_t OFF_G = 49152;    // g (TMA) -> K' = k^ o e^(b_63 - b), in place
-constexpr uint32_t OFF_X = 65536;    // phase-dependent scratch, 66560 bytes:
-//   prologue .. A/P products:  F^K, F^Q (k^, q^ o e^(b - m)), G (k^ o e^(m - b)), G' (k^ o e^(a - b))
-constexpr uint32_t X_FK = 0, X_FQ = 16384, X_G = 32768, X_GP = 49152;
-//   after the products:  A fp32 [64][68] | P bf16 | T bf16 | W bf16 [dk][r] | U^T bf16 [dv][i]
+constexpr uint32_t OFF_X = 65536;    // phase-dependent scratch, 73728 bytes:
+//   prologue .. A/P:  [F^K; F^Q] (128 rows) | [G; B_1; B_2; B_3] (64 + 16 + 32 + 48 = 160 rows)
+constexpr uint32_t X_FKQ = 0, X_GB = 32768;
+constexpr int kGBRows = 160;
+__host__ __device__ constexpr int gb_row0(int R) { return R == 0 ? 0 : R == 1 ? 64 : R == 2 ? 80 : 112; }
+//   after A/P:  A fp32 [64][68] | P bf16 | T bf16 | W bf16 [dk][r] | U^T bf16 [dv][i]
 constexpr uint32_t X_A = 0, X_P = 17408, X_T = 25600, X_W = 33792, X_UT = 50176;
-//   during the solve: (I + A)^-1 fp32 [64][68] over W and U^T; T region holds block products
+//   during the solve: (I + A)^-1 fp32 [64][68] over W / U^T; block products in the T region
 constexpr uint32_t X_INV = 33792, X_Y = 25600;
-constexpr int kAStride = 68;  // floats per row of A / (I+A)^-1
-constexpr uint32_t OFF_ST = OFF_X + 66560;   // S^T bf16 [dv][dk] (K-major operand), 32 KB
+//   output staging: O bf16 [64][136] over A
+constexpr uint32_t X_O = 0;
+constexpr int kAStride = 68;   // floats per row of A / (I+A)^-1
+constexpr int kOStride = 136;  // bf16 per row of the staged output
+constexpr uint32_t OFF_ST = OFF_X + 73728;   // S^T bf16 [dv][dk] (K-major operand), 32 KB
 constexpr uint32_t OFF_SMALL = OFF_ST + 32768;
-constexpr uint32_t SM_NQ = 0, SM_NK = 256, SM_BETA = 512, SM_BSUM = 768, SM_GL = 2816, SM_C = 3328,
-                   SM_DTB = 4864, SM_BAR = 5376, SM_TMEM = 5408, SM_ABORT = 5412, SM_END = 5440;
+constexpr uint32_t SM_NQ = 0, SM_NK = 256, SM_BETA = 512, SM_H0 = 768, SM_H1 = 2816, SM_GL = 4864,
+                   SM_DTB = 5376, SM_BAR = 5888, SM_TMEM = 5912, SM_ABORT = 5916, SM_END = 5952;
 constexpr uint32_t kSmemBytes = OFF_SMALL + SM_END + 1024;  // + alignment slack
 
-// ---- TMEM columns (fp32 accumulators, lane = row of the M = 128 tile) ----
+// ---- TMEM columns (fp32, lane = row of the M = 128 tile) ----
+// W^T, U^T, O^T accumulators; S^T (the state, lane = value channel, column =
+// key channel) lives in TMEM for the whole sequence.
 constexpr uint32_t TM_W = 0, TM_U = 64, TM_O = 128, TM_S = 256, TM_COLS = 512;
+// A / P products (same columns as W / U / O, which are free at that point)
+constexpr uint32_t TM_AP_DIAG = 0;
+__host__ __device__ constexpr uint32_t tm_ap_off(int R) { return R == 1 ? 64u : R == 2 ? 80u : 112u; }
+static_assert(tm_ap_off(1) == 64 && tm_ap_off(3) + 48 == 160, "A/P product columns follow the GB tile rows");
 
 struct Params {
   CUtensorMap tq, tk, tv, tg;
@@ -93,23 +103,19 @@ __device__ __forceinline__ float2 unpack_bf16x2(uint32_t v) {
 
 __device__ __forceinline__ float exp_f(float x) { return fast_exp2(x * kLog2e); }
 
-__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
-  __nv_bfloat162 r = __hmul2(*reinterpret_cast<__nv_bfloat162 *>(&a), *reinterpret_cast<__nv_bfloat162 *>(&b));
-  return *reinterpret_cast<uint32_t *>(&r);
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return r;
 }
 
-__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-
-__device__ __forceinline__ void mma_16816(float *d, const uint32_t *a, uint32_t b0, uint32_t b1) {
+// D (16x8 fp32) += A (16x8 tf32, row) * B (8x8 tf32, col); fragments as in the PTX ISA m16n8k8 layout
+__device__ __forceinline__ void mma_1688_tf32(float *d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                              uint32_t b0, uint32_t b1) {
   asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
 // Wait on an mbarrier phase; a wait that gives up records the fault and
@@ -122,11 +128,12 @@ __device__ __forceinline__ void wait_or_flag(uint64_t *bar, uint32_t parity, uin
   }
 }
 
-// Convert 32 fp32 values of one TMEM lane to bf16 and store them as four
-// 16-byte chunks of row `row` (columns col0 .. col0+31) of a row-swizzled tile.
-__device__ __forceinline__ void store_row32_bf16(uint8_t *tile, int R, int row, int col0, const float *v) {
+// Convert 8*n fp32 values to bf16 and store them as n 16-byte chunks of row
+// `row` (columns col0 .. col0+8n-1) of a row-swizzled tile of R rows.
+template <int N16>
+__device__ __forceinline__ void store_row_bf16(uint8_t *tile, int R, int row, int col0, const float *v) {
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
+  for (int j = 0; j < N16; ++j) {
     uint4 w;
     w.x = pack_bf16x2(v[8 * j + 0], v[8 * j + 1]);
     w.y = pack_bf16x2(v[8 * j + 2], v[8 * j + 3]);
@@ -134,6 +141,10 @@ __device__ __forceinline__ void store_row32_bf16(uint8_t *tile, int R, int row, 
     w.w = pack_bf16x2(v[8 * j + 6], v[8 * j + 7]);
     *reinterpret_cast<uint4 *>(tile + swz_offset(R, row, col0 + 8 * j)) = w;
   }
+}
+
+__device__ __forceinline__ float load_beta(const ChunkArgs &a, int tok, int h) {
+  return sigmoid_f(bf16_bits_to_f32(a.beta[(size_t)tok * a.beta_stride + h]));
 }
 
 __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid_constant__ Params p) {
@@ -145,10 +156,10 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
   float *s_nq = reinterpret_cast<float *>(small + SM_NQ);
   float *s_nk = reinterpret_cast<float *>(small + SM_NK);
   float *s_beta = reinterpret_cast<float *>(small + SM_BETA);
-  float *s_bsum = reinterpret_cast<float *>(small + SM_BSUM);   // [4][128]
-  float *s_gl = reinterpret_cast<float *>(small + SM_GL);       // [128] e^(b_63)
-  uint32_t *s_c = reinterpret_cast<uint32_t *>(small + SM_C);   // [6][64] bf16x2 e^(m_R - a_I)
-  float *s_dtb = reinterpret_cast<float *>(small + SM_DTB);     // [128]
+  float *s_h0 = reinterpret_cast<float *>(small + SM_H0);      // [4][128] sum of lambda over rows 0..7 of a block
+  float *s_h1 = reinterpret_cast<float *>(small + SM_H1);      // [4][128] sum of lambda over rows 8..15
+  float *s_gl = reinterpret_cast<float *>(small + SM_GL);      // [128] e^(b_63)
+  float *s_dtb = reinterpret_cast<float *>(small + SM_DTB);    // [128]
   uint64_t *bar_qkv = reinterpret_cast<uint64_t *>(small + SM_BAR);
   uint64_t *bar_g = bar_qkv + 1;
   uint64_t *bar_mma = bar_qkv + 2;
@@ -207,25 +218,33 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
     tma_load_3d(sG, &p.tg, 0, h, t0, bar_g);
     tma_load_3d(sG + 8192, &p.tg, 64, h, t0, bar_g);
   }
+  // beta of the first chunk (later chunks: prefetched one chunk ahead)
+  float beta_next = (tid < kC && tid < len) ? load_beta(a, t0 + tid, h) : 0.f;
 
-  // State S^T in registers: thread owns value channel d and key channels
-  // [64*hh, 64*hh + 64) -- exactly its TMEM lane / column half.
-  const int quad = warp & 3, hh = warp >> 2;
+  // TMEM tiles are read / written by warp w on lanes 32*(w%4) .. +31 and a
+  // quarter (w/4) of the columns.  For S^T: lane = value channel d.
+  const int quad = warp & 3, qc = warp >> 2;
   const int d = quad * 32 + lane;
   const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-  float S[64];
-  if (a.state_in) {
-    const float *src = a.state_in + ((size_t)slot * a.H + h) * kD * kD + d;
+  {
+    float s0[32];
+    if (a.state_in) {
+      const float *src = a.state_in + ((size_t)slot * a.H + h) * kD * kD + d;
 #pragma unroll
-    for (int i = 0; i < 64; ++i) S[i] = src[(size_t)(64 * hh + i) * kD];
-  } else {
+      for (int i = 0; i < 32; ++i) s0[i] = src[(size_t)(32 * qc + i) * kD];
+    } else {
 #pragma unroll
-    for (int i = 0; i < 64; ++i) S[i] = 0.f;
+      for (int i = 0; i < 32; ++i) s0[i] = 0.f;
+    }
+    tmem_st16(tmem + lane_base + TM_S + 32 * qc, s0);
+    tmem_st16(tmem + lane_base + TM_S + 32 * qc + 16, s0 + 16);
+    store_row_bf16<4>(sST, 128, d, 32 * qc, s0);
+    tmem_wait_st();
   }
-#pragma unroll
-  for (int j = 0; j < 2; ++j) store_row32_bf16(sST, 128, d, 64 * hh + 32 * j, S + 32 * j);
   fence_async_smem();
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
 
   const float ea = __expf(a.A_log[h]);
   const float lb = a.lower_bound;
@@ -235,18 +254,19 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
     const int tok0 = t0 + chunk * kC;
     const int valid = min(kC, len - chunk * kC);
     const uint32_t tma_parity = chunk & 1;
+    // -- wait for inputs
     wait_or_flag(bar_qkv, tma_parity, s_abort, a.status);
     wait_or_flag(bar_g, tma_parity, s_abort, a.status);
 
     // ---------------------------------------------- A1: norms, beta, padding
     {
-      const int task = tid >> 1, half = tid & 1;
+      const int task = tid >> 2, part = tid & 3;   // 128 (row, q|k) tasks x 4 threads of 32 channels
       const int r = task & 63;
       const uint8_t *tile = task < 64 ? sQ : sK;
       float ss = 0.f;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const uint4 w = *reinterpret_cast<const uint4 *>(tile + swz_offset(64, r, 64 * half + 8 * j));
+      for (int j = 0; j < 4; ++j) {
+        const uint4 w = *reinterpret_cast<const uint4 *>(tile + swz_offset(64, r, 32 * part + 8 * j));
         const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -255,14 +275,12 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
         }
       }
       ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-      if (half == 0) {
+      ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+      if (part == 0) {
         const float nrm = r < valid ? rsqrtf(ss + kL2Eps) : 0.f;
         (task < 64 ? s_nq : s_nk)[r] = nrm;
       }
-      if (tid < kC) {
-        s_beta[tid] = tid < valid ? sigmoid_f(bf16_bits_to_f32(a.beta[(size_t)(tok0 + tid) * a.beta_stride + h]))
-                                  : 0.f;
-      }
+      if (tid < kC) s_beta[tid] = beta_next;
       if (valid < kC) {  // rows past the sequence end: zero v (the others are masked through beta, norms, lambda)
         for (int idx = tid; idx < (kC - valid) * 16; idx += kThreads) {
           const int r2 = valid + idx / 16, cc = idx % 16;
@@ -274,15 +292,16 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
 
     // ---------------------------------------------- A2: gate, decay, operands
     {
-      const int cp = tid & 63;        // channel pair
-      const int R = tid >> 6;         // 16-row block
+      // thread = (channel pair, 16-row block R, half of the block): 8 rows x 2 channels
+      const int cp = tid & 63, R = (tid >> 6) & 3, half = tid >> 8;
       const int c0 = 2 * cp;
+      const int rb = 16 * R + 8 * half;   // first row of this thread
       const float dtb0 = s_dtb[c0], dtb1 = s_dtb[c0 + 1];
-      float b0[16], b1[16];
+      float b0[8], b1[8];   // cumulative log-decay from the start of this half-block
       float acc0 = 0.f, acc1 = 0.f;
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int r = 16 * R + j;
+      for (int j = 0; j < 8; ++j) {
+        const int r = rb + j;
         const float2 gg = unpack_bf16x2(ld_u32(sG + swz_offset(64, r, c0)));
         const bool ok = r < valid;
         const float l0 = ok ? lb * sigmoid_f(ea * (gg.x + dtb0)) : 0.f;
@@ -292,37 +311,55 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
         b0[j] = acc0;
         b1[j] = acc1;
       }
-      s_bsum[R * kD + c0] = acc0;
-      s_bsum[R * kD + c0 + 1] = acc1;
+      *reinterpret_cast<float2 *>((half ? s_h1 : s_h0) + R * kD + c0) = make_float2(acc0, acc1);
+      // -- gate done
       __syncthreads();
-      float pre[5][2];  // pre[I] = b at the end of block I-1 (prefix), pre[4] = chunk total
-      pre[0][0] = pre[0][1] = 0.f;
+      // absolute anchors of every block: m_I = b at row 7, a_I = b at row 15
+      float mm[4][2], aa[4][2], tot0 = 0.f, tot1 = 0.f;
 #pragma unroll
       for (int I = 0; I < 4; ++I) {
-        pre[I + 1][0] = pre[I][0] + s_bsum[I * kD + c0];
-        pre[I + 1][1] = pre[I][1] + s_bsum[I * kD + c0 + 1];
+        const float2 x0 = *reinterpret_cast<const float2 *>(s_h0 + I * kD + c0);
+        const float2 x1 = *reinterpret_cast<const float2 *>(s_h1 + I * kD + c0);
+        mm[I][0] = tot0 + x0.x;
+        mm[I][1] = tot1 + x0.y;
+        tot0 += x0.x + x1.x;
+        tot1 += x0.y + x1.y;
+        aa[I][0] = tot0;
+        aa[I][1] = tot1;
       }
-      const float m0 = pre[R][0] + b0[7], m1 = pre[R][1] + b1[7];  // b at row 7 of the block
-      if (R == 0) {
-        s_gl[c0] = exp_f(pre[4][0]);
-        s_gl[c0 + 1] = exp_f(pre[4][1]);
-      }
-      // e^(m_R - a_I) for the blocks I < R  (a_I = pre[I + 1])
+      float m0 = 0.f, m1 = 0.f, ar0 = 0.f, ar1 = 0.f, t10 = 0.f, t11 = 0.f;
 #pragma unroll
-      for (int I = 0; I < 3; ++I) {
-        if (I < R) {
-          const int pidx = R * (R - 1) / 2 + I;
-          s_c[pidx * 64 + cp] = pack_bf16x2(exp_f(m0 - pre[I + 1][0]), exp_f(m1 - pre[I + 1][1]));
+      for (int I = 0; I < 4; ++I) {
+        if (I == R) {
+          m0 = mm[I][0]; m1 = mm[I][1];
+          ar0 = aa[I][0]; ar1 = aa[I][1];
         }
       }
-      const float em0 = exp_f(m0), em1 = exp_f(m1);                      // e^(m_R)
-      const float el0 = exp_f(pre[4][0] - m0), el1 = exp_f(pre[4][1] - m1);  // e^(b_63 - m_R)
-      const float eg0 = exp_f(b0[15] - b0[7]), eg1 = exp_f(b1[15] - b1[7]);  // e^(a_R - m_R)
+      {
+        const float2 x1 = *reinterpret_cast<const float2 *>(s_h1 + R * kD + c0);
+        t10 = x1.x;   // b_15 - b_7 of this block
+        t11 = x1.y;
+      }
+      if (R == 0 && half == 0) *reinterpret_cast<float2 *>(s_gl + c0) = make_float2(exp_f(tot0), exp_f(tot1));
+      const float em0 = exp_f(m0), em1 = exp_f(m1);              // e^(m_R)
+      const float el0 = exp_f(tot0 - m0), el1 = exp_f(tot1 - m1);  // e^(b_63 - m_R)
+      const float eg0 = exp_f(t10), eg1 = exp_f(t11);              // e^(a_R - m_R)
+      // rows of this block feed the off-diagonal B tiles of every later block R2:
+      //   B_R2[i] = k^_i e^(m_R2 - b_i) = (k^_i e^(a_R - b_i)) * e^(m_R2 - a_R), both factors <= 1
+      float cr[4][2];
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int r = 16 * R + j;
-        const float e0 = exp_f(b0[j] - b0[7]), e1 = exp_f(b1[j] - b1[7]);
-        const float i0 = exp_f(b0[7] - b0[j]), i1 = exp_f(b1[7] - b1[j]);
+      for (int R2 = 1; R2 < 4; ++R2) {
+        cr[R2][0] = exp_f(fminf(mm[R2][0] - ar0, 0.f));
+        cr[R2][1] = exp_f(fminf(mm[R2][1] - ar1, 0.f));
+      }
+      // b_r - m_R from the thread's own partial sums: half 0 ends at row 7, half 1 starts after it
+      const float base0 = half ? 0.f : b0[7], base1 = half ? 0.f : b1[7];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int r = rb + j;
+        const float x0 = b0[j] - base0, x1 = b1[j] - base1;   // b_r - m_R
+        const float e0 = exp_f(x0), e1 = exp_f(x1);
+        const float i0 = exp_f(-x0), i1 = exp_f(-x1);
         const uint32_t off = swz_offset(64, r, c0);
         const float2 qq = unpack_bf16x2(ld_u32(sQ + off));
         const float2 kk = unpack_bf16x2(ld_u32(sK + off));
@@ -330,158 +367,164 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
         const float qh0 = qq.x * nq, qh1 = qq.y * nq, kh0 = kk.x * nk, kh1 = kk.y * nk;
         const float fk0 = kh0 * e0, fk1 = kh1 * e1, fq0 = qh0 * e0, fq1 = qh1 * e1;
         const float g0 = kh0 * i0, g1 = kh1 * i1;
-        st_u32(sX + X_FK + off, pack_bf16x2(fk0, fk1));
-        st_u32(sX + X_FQ + off, pack_bf16x2(fq0, fq1));
-        st_u32(sX + X_G + off, pack_bf16x2(g0, g1));
-        st_u32(sX + X_GP + off, pack_bf16x2(g0 * eg0, g1 * eg1));
+        st_u32(sX + X_FKQ + swz_offset(128, r, c0), pack_bf16x2(fk0, fk1));
+        st_u32(sX + X_FKQ + swz_offset(128, 64 + r, c0), pack_bf16x2(fq0, fq1));
+        st_u32(sX + X_GB + swz_offset(kGBRows, r, c0), pack_bf16x2(g0, g1));
+        const float gp0 = g0 * eg0, gp1 = g1 * eg1;  // k^ e^(a_R - b)
+#pragma unroll
+        for (int R2 = 1; R2 < 4; ++R2) {
+          if (R2 > R)
+            st_u32(sX + X_GB + swz_offset(kGBRows, gb_row0(R2) + r, c0),
+                   pack_bf16x2(gp0 * cr[R2][0], gp1 * cr[R2][1]));
+        }
         st_u32(sQ + off, pack_bf16x2(fq0 * em0, fq1 * em1));  // Q+
         st_u32(sK + off, pack_bf16x2(fk0 * em0, fk1 * em1));  // K+
         st_u32(sG + off, pack_bf16x2(g0 * el0, g1 * el1));    // K'
       }
     }
+    fence_async_smem();
+    tc_fence_before();
     __syncthreads();
 
-    // ---------------------------------------------- B: A and P (16x16 sub-blocks, mma.sync)
+    // ---------------------------------------------- B: A and P from 16x16 sub-blocks (tcgen05)
+    if (tid == 0) {
+      tc_fence_after();
+      // one 128 x 160 product: columns 0..63 diagonal blocks, then B_1, B_2, B_3
+      const uint32_t fkq = smem_u32(sX + X_FKQ);
+      const uint32_t gb = smem_u32(sX + X_GB);
+#pragma unroll
+      for (int s = 0; s < 8; ++s)
+        mma_bf16(tmem + TM_AP_DIAG, desc_kmajor(fkq, 128, s), desc_kmajor(gb, kGBRows, s),
+                 idesc_bf16(128, kGBRows, false, false), s > 0);
+      mma_commit(bar_mma);
+    }
+    __syncwarp();
+    wait_or_flag(bar_mma, mma_phase & 1, s_abort, a.status);
+    ++mma_phase;
+    tc_fence_after();
+    // -- A/P products done
     {
-      const int g = lane >> 2, t = lane & 3;
-      float accA[2][2][4], accP[2][2][4];  // [item][ntile][4]
-      int items[2] = {warp, warp + 8};
-#pragma unroll
-      for (int it = 0; it < 2; ++it) {
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) accA[it][nt][e] = accP[it][nt][e] = 0.f;
-      }
-      // item index -> (R, I): 0:(0,0) 1:(1,0) 2:(1,1) 3:(2,0) 4:(2,1) 5:(2,2) 6:(3,0) 7:(3,1) 8:(3,2) 9:(3,3)
-      const uint32_t base_fk = smem_u32(sX + X_FK), base_fq = smem_u32(sX + X_FQ);
-      const uint32_t base_g = smem_u32(sX + X_G), base_gp = smem_u32(sX + X_GP);
-#pragma unroll
-      for (int it = 0; it < 2; ++it) {
-        const int item = items[it];
-        if (item < 10) {
-          const int R = item < 1 ? 0 : item < 3 ? 1 : item < 6 ? 2 : 3;
-          const int I = item - R * (R + 1) / 2;
-          const uint32_t bbase = (I == R) ? base_g : base_gp;
-          const int pidx = R * (R - 1) / 2 + I;
-          const int arow = 16 * R + (lane & 15);
-          const int brow = 16 * I + (lane & 7) + 8 * (lane >> 4);
-#pragma unroll
-          for (int s = 0; s < 8; ++s) {
-            uint32_t ak[4], aq[4], bb[4];
-            const uint32_t aoff = swz_offset(64, arow, 16 * s + 8 * (lane >> 4));
-            ldmatrix_x4(base_fk + aoff, ak[0], ak[1], ak[2], ak[3]);
-            ldmatrix_x4(base_fq + aoff, aq[0], aq[1], aq[2], aq[3]);
-            ldmatrix_x4(bbase + swz_offset(64, brow, 16 * s + 8 * ((lane >> 3) & 1)), bb[0], bb[1], bb[2], bb[3]);
-            if (I < R) {
-              const uint32_t clo = s_c[pidx * 64 + 8 * s + t], chi = s_c[pidx * 64 + 8 * s + t + 4];
-              ak[0] = bf16x2_mul(ak[0], clo);
-              ak[1] = bf16x2_mul(ak[1], clo);
-              ak[2] = bf16x2_mul(ak[2], chi);
-              ak[3] = bf16x2_mul(ak[3], chi);
-              aq[0] = bf16x2_mul(aq[0], clo);
-              aq[1] = bf16x2_mul(aq[1], clo);
-              aq[2] = bf16x2_mul(aq[2], chi);
-              aq[3] = bf16x2_mul(aq[3], chi);
-            }
-            mma_16816(accA[it][0], ak, bb[0], bb[1]);
-            mma_16816(accA[it][1], ak, bb[2], bb[3]);
-            mma_16816(accP[it][0], aq, bb[0], bb[1]);
-            mma_16816(accP[it][1], aq, bb[2], bb[3]);
-          }
-        }
-      }
-      __syncthreads();  // every F / G read is done: the X region is reused below
-      // zero the strictly-upper 16x16 blocks of P
-      for (int idx = tid; idx < 6 * 128; idx += kThreads) {
-        const int blk = idx / 128, e = idx % 128;
-        const int R = blk < 3 ? 0 : blk < 5 ? 1 : 2;
-        const int I = blk < 3 ? blk + 1 : blk < 5 ? blk - 1 : 3;
-        const int r = 16 * R + e / 8, i = 16 * I + 2 * (e % 8);
-        st_u32(sX + X_P + swz_offset(64, r, i), 0u);
-      }
+      // lanes 0..63 of the products hold A rows (k), lanes 64..127 P rows (q);
+      // warp = (lane quadrant, column block I)
+      const bool is_p = quad >= 2;
+      const int r = (quad & 1) * 32 + lane;     // row of A / P
+      const int Rr = r >> 4;                     // its 16-row block
+      const int Ra = (quad & 1) * 2;             // first of the two row blocks of this warp
+      const int I = qc;
       float *sA = reinterpret_cast<float *>(sX + X_A);
+      const float bscale = is_p ? 1.f : s_beta[r];
+      uint32_t va[16], vb[16];
+      const int srcA = (I == Ra) ? int(TM_AP_DIAG) + 16 * I : (I < Ra) ? int(tm_ap_off(Ra)) + 16 * I : -1;
+      const int srcB = (I == Ra + 1) ? int(TM_AP_DIAG) + 16 * I : (I < Ra + 1) ? int(tm_ap_off(Ra + 1)) + 16 * I : -1;
+      if (srcA >= 0) tmem_ld16_async(tmem + lane_base + srcA, va);
+      if (srcB >= 0) tmem_ld16_async(tmem + lane_base + srcB, vb);
+      tmem_wait_ld();
+      tmem_tie<16>(va);
+      tmem_tie<16>(vb);
+      const bool mine_a = (Rr == Ra);
+      const int src = mine_a ? srcA : srcB;
+      float v[16];
 #pragma unroll
-      for (int it = 0; it < 2; ++it) {
-        const int item = items[it];
-        if (item < 10) {
-          const int R = item < 1 ? 0 : item < 3 ? 1 : item < 6 ? 2 : 3;
-          const int I = item - R * (R + 1) / 2;
+      for (int e = 0; e < 16; ++e) {
+        const int i = 16 * I + e;
+        const float raw = __uint_as_float(mine_a ? va[e] : vb[e]);
+        const bool keep = (src >= 0) && (is_p ? (i <= r) : (i < r));
+        v[e] = keep ? raw * bscale : 0.f;
+      }
+      if (is_p) {
+        store_row_bf16<2>(sX + X_P, 64, r, 16 * I, v);
+      } else {
 #pragma unroll
-          for (int nt = 0; nt < 2; ++nt) {
-#pragma unroll
-            for (int hr = 0; hr < 2; ++hr) {
-              const int r = 16 * R + g + 8 * hr;
-              const int i = 16 * I + 8 * nt + 2 * t;
-              float a0 = accA[it][nt][2 * hr] * s_beta[r], a1 = accA[it][nt][2 * hr + 1] * s_beta[r];
-              float p0 = accP[it][nt][2 * hr], p1 = accP[it][nt][2 * hr + 1];
-              if (I == R) {
-                a0 = (i < r) ? a0 : 0.f;
-                a1 = (i + 1 < r) ? a1 : 0.f;
-                p0 = (i <= r) ? p0 : 0.f;
-                p1 = (i + 1 <= r) ? p1 : 0.f;
-              }
-              *reinterpret_cast<float2 *>(sA + r * kAStride + i) = make_float2(a0, a1);
-              st_u32(sX + X_P + swz_offset(64, r, i), pack_bf16x2(p0, p1));
-            }
-          }
-        }
+        for (int e = 0; e < 16; e += 4)
+          *reinterpret_cast<float4 *>(sA + r * kAStride + 16 * I + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
       }
     }
+    tc_fence_before();
     __syncthreads();
 
     // ---------------------------------------------- C: T = (I + A)^-1 Diag(beta)
     {
       const float *sA = reinterpret_cast<const float *>(sX + X_A);
       float *sInv = reinterpret_cast<float *>(sX + X_INV);
-      float *sY = reinterpret_cast<float *>(sX + X_Y);
       // C1: inverses of the unit-lower 16x16 diagonal blocks (warp R, lane = column)
       if (warp < 4 && lane < 16) {
         const int R = warp, jc = lane;
         float x[16];
 #pragma unroll
         for (int r = 0; r < 16; ++r) {
-          float v = (r == jc) ? 1.f : 0.f;
+          float lrow[16];
 #pragma unroll
-          for (int m = 0; m < r; ++m) v = fmaf(-sA[(16 * R + r) * kAStride + 16 * R + m], x[m], v);
-          x[r] = v;
+          for (int q4 = 0; q4 < 4; ++q4) {
+            const float4 l4 = *reinterpret_cast<const float4 *>(sA + (16 * R + r) * kAStride + 16 * R + 4 * q4);
+            lrow[4 * q4] = l4.x; lrow[4 * q4 + 1] = l4.y; lrow[4 * q4 + 2] = l4.z; lrow[4 * q4 + 3] = l4.w;
+          }
+          float v0 = (r == jc) ? 1.f : 0.f, v1 = 0.f;
+#pragma unroll
+          for (int m = 0; m < r; ++m) {
+            if (m & 1) v1 = fmaf(-lrow[m], x[m], v1);
+            else v0 = fmaf(-lrow[m], x[m], v0);
+          }
+          x[r] = v0 + v1;
         }
 #pragma unroll
         for (int r = 0; r < 16; ++r) sInv[(16 * R + r) * kAStride + 16 * R + jc] = x[r];
       }
       __syncthreads();
+      // -- diagonal inverses done
       // C2: off-diagonal blocks by distance dd = R - I:
       //   Inv_RI = -Inv_RR * sum_{J=I}^{R-1} A_RJ Inv_JI
-      const int er = tid >> 4, ej = tid & 15;
+      // on the tensor cores in TF32 (m16n8k8): one warp per 16 x 8 half of a block
+      {
+        const int g = lane >> 2, t = lane & 3;
 #pragma unroll 1
-      for (int dd = 1; dd < 4; ++dd) {
-        for (int I = 0; I + dd < 4; ++I) {
-          const int R = I + dd;
-          float y = 0.f;
-          for (int J = I; J < R; ++J) {
+        for (int dd = 1; dd < 4; ++dd) {
+          if (warp < 2 * (4 - dd)) {
+            const int I = warp >> 1, R = I + dd;
+            const int n0 = 16 * I + 8 * (warp & 1);
+            float y[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int J = I; J < R; ++J) {
 #pragma unroll
-            for (int m = 0; m < 16; ++m)
-              y = fmaf(sA[(16 * R + er) * kAStride + 16 * J + m], sInv[(16 * J + m) * kAStride + 16 * I + ej], y);
+              for (int ks = 0; ks < 2; ++ks) {
+                const int kc = 16 * J + 8 * ks;
+                const float *ar = sA + (16 * R + g) * kAStride + kc + t;
+                const float *br = sInv + (kc + t) * kAStride + n0 + g;
+                mma_1688_tf32(y, to_tf32(ar[0]), to_tf32(ar[8 * kAStride]), to_tf32(ar[4]),
+                              to_tf32(ar[8 * kAStride + 4]), to_tf32(br[0]), to_tf32(br[4 * kAStride]));
+              }
+            }
+            float *sYw = reinterpret_cast<float *>(sX + X_Y) + warp * 128;  // Y: 16 x 8
+            *reinterpret_cast<float2 *>(sYw + g * 8 + 2 * t) = make_float2(y[0], y[1]);
+            *reinterpret_cast<float2 *>(sYw + (g + 8) * 8 + 2 * t) = make_float2(y[2], y[3]);
+            __syncwarp();
+            float x[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int ks = 0; ks < 2; ++ks) {
+              const float *ar = sInv + (16 * R + g) * kAStride + 16 * R + 8 * ks + t;
+              const float *br = sYw + (8 * ks + t) * 8 + g;
+              mma_1688_tf32(x, to_tf32(ar[0]), to_tf32(ar[8 * kAStride]), to_tf32(ar[4]),
+                            to_tf32(ar[8 * kAStride + 4]), to_tf32(br[0]), to_tf32(br[32]));
+            }
+            *reinterpret_cast<float2 *>(sInv + (16 * R + g) * kAStride + n0 + 2 * t) = make_float2(-x[0], -x[1]);
+            *reinterpret_cast<float2 *>(sInv + (16 * R + g + 8) * kAStride + n0 + 2 * t) = make_float2(-x[2], -x[3]);
           }
-          sY[I * 256 + er * 16 + ej] = y;
+          __syncthreads();
         }
-        __syncthreads();
-        for (int I = 0; I + dd < 4; ++I) {
-          const int R = I + dd;
-          float x = 0.f;
-#pragma unroll
-          for (int m = 0; m < 16; ++m)
-            x = fmaf(sInv[(16 * R + er) * kAStride + 16 * R + m], sY[I * 256 + m * 16 + ej], x);
-          sInv[(16 * R + er) * kAStride + 16 * I + ej] = -x;
-        }
-        __syncthreads();
       }
+      // -- off-diagonal inverses done
       // C3: T = Inv Diag(beta), lower triangle, bf16 K-major [r][i]
-      for (int idx = tid; idx < kC * kC / 2; idx += kThreads) {
-        const int r = idx / 32, i = 2 * (idx % 32);
-        const float v0 = (i <= r) ? sInv[r * kAStride + i] * s_beta[i] : 0.f;
-        const float v1 = (i + 1 <= r) ? sInv[r * kAStride + i + 1] * s_beta[i + 1] : 0.f;
-        st_u32(sX + X_T + swz_offset(64, r, i), pack_bf16x2(v0, v1));
+      {
+        const int r = tid >> 3, i0 = 8 * (tid & 7);
+        float v[8];
+#pragma unroll
+        for (int e = 0; e < 8; e += 4) {
+          const float4 x4 = *reinterpret_cast<const float4 *>(sInv + r * kAStride + i0 + e);
+          const float4 b4 = *reinterpret_cast<const float4 *>(s_beta + i0 + e);
+          v[e] = (i0 + e <= r) ? x4.x * b4.x : 0.f;
+          v[e + 1] = (i0 + e + 1 <= r) ? x4.y * b4.y : 0.f;
+          v[e + 2] = (i0 + e + 2 <= r) ? x4.z * b4.z : 0.f;
+          v[e + 3] = (i0 + e + 3 <= r) ? x4.w * b4.w : 0.f;
+        }
+        store_row_bf16<1>(sX + X_T, 64, r, i0, v);
       }
     }
     fence_async_smem();
@@ -508,12 +551,13 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
     ++mma_phase;
     tc_fence_after();
 
-    // ---------------------------------------------- E: W^T (TMEM) -> W bf16 [dk][r]; U^T -= S^T W^T
+    // ---------------------------------------------- E: W^T (TMEM) -> W bf16 [dk][r]; U^T -= S^T W^T; decay S
     {
-      float v[32];
-      tmem_ld16(tmem + lane_base + TM_W + 32 * hh, v);
-      tmem_ld16(tmem + lane_base + TM_W + 32 * hh + 16, v + 16);
-      store_row32_bf16(sX + X_W, 128, d, 32 * hh, v);
+      uint32_t v[16];
+      tmem_ld16_async(tmem + lane_base + TM_W + 16 * qc, v);
+      tmem_wait_ld();
+      tmem_tie<16>(v);
+      store_row_bf16<2>(sX + X_W, 128, d, 16 * qc, reinterpret_cast<const float *>(v));
     }
     fence_async_smem();
     tc_fence_before();
@@ -537,17 +581,42 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
         tma_load_3d(sV + 8192, &p.tv, 64, h, nt0, bar_qkv);
       }
     }
+    // while the MMA runs: decay the state in TMEM, S^T <- S^T Diag(e^(b_63)), and fetch the next beta
+    {
+      uint32_t sv[32];
+      tmem_ld16_async(tmem + lane_base + TM_S + 32 * qc, sv);
+      tmem_ld16_async(tmem + lane_base + TM_S + 32 * qc + 16, sv + 16);
+      tmem_wait_ld();
+      tmem_tie<32>(sv);
+      float f[32];
+#pragma unroll
+      for (int i = 0; i < 32; i += 4) {
+        const float4 g4 = *reinterpret_cast<const float4 *>(s_gl + 32 * qc + i);
+        f[i] = __uint_as_float(sv[i]) * g4.x;
+        f[i + 1] = __uint_as_float(sv[i + 1]) * g4.y;
+        f[i + 2] = __uint_as_float(sv[i + 2]) * g4.z;
+        f[i + 3] = __uint_as_float(sv[i + 3]) * g4.w;
+      }
+      tmem_st16(tmem + lane_base + TM_S + 32 * qc, f);
+      tmem_st16(tmem + lane_base + TM_S + 32 * qc + 16, f + 16);
+      tmem_wait_st();
+    }
+    if (tid < kC) {
+      const int nt = (chunk + 1) * kC + tid;
+      beta_next = nt < len ? load_beta(a, t0 + nt, h) : 0.f;
+    }
     __syncwarp();
     wait_or_flag(bar_mma, mma_phase & 1, s_abort, a.status);
     ++mma_phase;
     tc_fence_after();
 
-    // ---------------------------------------------- G: U^T (TMEM) -> bf16 [dv][i]; O^T += U^T P^T; S_acc = U^T K'
+    // ---------------------------------------------- G: U^T (TMEM) -> bf16 [dv][i]; O^T += U^T P^T; S^T += U^T K'
     {
-      float v[32];
-      tmem_ld16(tmem + lane_base + TM_U + 32 * hh, v);
-      tmem_ld16(tmem + lane_base + TM_U + 32 * hh + 16, v + 16);
-      store_row32_bf16(sX + X_UT, 128, d, 32 * hh, v);
+      uint32_t v[16];
+      tmem_ld16_async(tmem + lane_base + TM_U + 16 * qc, v);
+      tmem_wait_ld();
+      tmem_tie<16>(v);
+      store_row_bf16<2>(sX + X_UT, 128, d, 16 * qc, reinterpret_cast<const float *>(v));
     }
     fence_async_smem();
     tc_fence_before();
@@ -560,7 +629,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
 #pragma unroll
       for (int s = 0; s < 4; ++s) mma_bf16(tmem + TM_O, desc_kmajor(ut, 128, s), desc_kmajor(pp, 64, s), id_o, 1);
 #pragma unroll
-      for (int s = 0; s < 4; ++s) mma_bf16(tmem + TM_S, desc_kmajor(ut, 128, s), desc_mnmajor(kq, 64, s), id_s, s > 0);
+      for (int s = 0; s < 4; ++s) mma_bf16(tmem + TM_S, desc_kmajor(ut, 128, s), desc_mnmajor(kq, 64, s), id_s, 1);
       mma_commit(bar_mma);
     }
     __syncwarp();
@@ -574,30 +643,35 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
       tma_load_3d(sG + 8192, &p.tg, 64, h, nt0, bar_g);
     }
 
-    // ---------------------------------------------- I: state update, output
+    // ---------------------------------------------- I: S^T -> bf16 operand, output
     {
+      uint32_t sv[32];
+      tmem_ld16_async(tmem + lane_base + TM_S + 32 * qc, sv);
+      tmem_ld16_async(tmem + lane_base + TM_S + 32 * qc + 16, sv + 16);
+      uint32_t o[16];
+      tmem_ld16_async(tmem + lane_base + TM_O + 16 * qc, o);
+      tmem_wait_ld();
+      tmem_tie<32>(sv);
+      tmem_tie<16>(o);
+      store_row_bf16<4>(sST, 128, d, 32 * qc, reinterpret_cast<const float *>(sv));
+      uint16_t *sO = reinterpret_cast<uint16_t *>(sX + X_O);
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        float acc[16];
-        tmem_ld16(tmem + lane_base + TM_S + 64 * hh + 16 * j, acc);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) S[16 * j + i] = fmaf(s_gl[64 * hh + 16 * j + i], S[16 * j + i], acc[i]);
-      }
-#pragma unroll
-      for (int j = 0; j < 2; ++j) store_row32_bf16(sST, 128, d, 64 * hh + 32 * j, S + 32 * j);
-      float o[32];
-      tmem_ld16(tmem + lane_base + TM_O + 32 * hh, o);
-      tmem_ld16(tmem + lane_base + TM_O + 32 * hh + 16, o + 16);
-      uint16_t *dst = a.out + (size_t)tok0 * a.out_stride + h * kD + d;
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const int r = 32 * hh + i;
-        if (r < valid) dst[(size_t)r * a.out_stride] = f32_to_bf16_bits(a.scale * o[i]);
+      for (int i = 0; i < 16; ++i) sO[(16 * qc + i) * kOStride + d] = f32_to_bf16_bits(a.scale * __uint_as_float(o[i]));
+    }
+    __syncthreads();
+    {
+      const uint16_t *sO = reinterpret_cast<const uint16_t *>(sX + X_O);
+      for (int idx = tid; idx < valid * 16; idx += kThreads) {
+        const int r = idx >> 4, cc = idx & 15;
+        *reinterpret_cast<uint4 *>(a.out + (size_t)(tok0 + r) * a.out_stride + h * kD + 8 * cc) =
+            *reinterpret_cast<const uint4 *>(sO + r * kOStride + 8 * cc);
       }
     }
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
+    tc_fence_after();
+    // -- chunk done
     if (*s_abort) break;
   }
 
@@ -606,8 +680,13 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
   if (a.state_out_pool) dst = a.state_out_pool + ((size_t)slot * a.H + h) * kD * kD;
   else if (a.state_out_dense) dst = a.state_out_dense + ((size_t)n * a.H + h) * kD * kD;
   if (dst) {
+    uint32_t sv[32];
+    tmem_ld16_async(tmem + lane_base + TM_S + 32 * qc, sv);
+    tmem_ld16_async(tmem + lane_base + TM_S + 32 * qc + 16, sv + 16);
+    tmem_wait_ld();
+    tmem_tie<32>(sv);
 #pragma unroll
-    for (int i = 0; i < 64; ++i) dst[(size_t)(64 * hh + i) * kD + d] = S[i];
+    for (int i = 0; i < 32; ++i) dst[(size_t)(32 * qc + i) * kD + d] = __uint_as_float(sv[i]);
   }
   tc_fence_before();
   __syncthreads();
