@@ -55,19 +55,22 @@ constexpr int kThreads = 512;      // 16 warps
 constexpr int kTileBytes = 16384;  // one 64 x 128 bf16 tile
 
 // ---- shared memory map (offsets from a 1024-byte aligned base) ----
-constexpr uint32_t OFF_Q = 0;        // q (TMA) -> Q+ = q^ o e^b, in place
-constexpr uint32_t OFF_K = 16384;    // k (TMA) -> K+ = k^ o e^b, in place
-constexpr uint32_t OFF_V = 32768;    // v (TMA)
-constexpr uint32_t OFF_G = 49152;    // g (TMA) -> K' = k^ o e^(b_63 - b), in place
-constexpr uint32_t OFF_X = 65536;    // phase-dependent scratch, 73728 bytes:
+// WQ: stacked K-major operand [-W (64 rows r); Q+ (64 rows r)] x 128 key channels;
+//     the raw q tile is loaded by TMA into the Q+ rows and converted in place.
+constexpr uint32_t OFF_WQ = 0;       // 32 KB
+constexpr uint32_t OFF_K = 32768;    // k (TMA) -> K+ = k^ o e^b, in place (MN-major operand of W^T)
+constexpr uint32_t OFF_V = 49152;    // v (TMA)
+constexpr uint32_t OFF_G = 65536;    // g (TMA), read by the gate only
+// PK: stacked K-major operand [P (64 rows r); K'^T (128 rows c)] x 64 tokens i, one 128-byte panel
+constexpr uint32_t OFF_PK = 81920;   // 24 KB
+constexpr int kPKRows = 192;
+constexpr uint32_t OFF_X = 106496;   // phase-dependent scratch, 73728 bytes:
 //   prologue .. A/P:  [F^K; F^Q] (128 rows) | [G; B_1; B_2; B_3] (64 + 16 + 32 + 48 = 160 rows)
 constexpr uint32_t X_FKQ = 0, X_GB = 32768;
 constexpr int kGBRows = 160;
 __host__ __device__ constexpr int gb_row0(int R) { return R == 0 ? 0 : R == 1 ? 64 : R == 2 ? 80 : 112; }
-//   after A/P:  A fp32 [64][68] | P bf16 | T bf16 | W bf16 [dk][r] | U^T bf16 [dv][i]
-constexpr uint32_t X_A = 0, X_P = 17408, X_T = 25600, X_W = 33792, X_UT = 50176;
-//   during the solve: (I + A)^-1 fp32 [64][68] over W / U^T; block products in the T region
-constexpr uint32_t X_INV = 33792, X_Y = 25600;
+//   after A/P:  A fp32 [64][68] | T bf16 [r][i] | U^T bf16 [dv][i] | (I+A)^-1 fp32 [64][68] | block products
+constexpr uint32_t X_A = 0, X_T = 17408, X_UT = 25600, X_INV = 41984, X_Y = 59392;
 //   output staging: O bf16 [64][136] over A
 constexpr uint32_t X_O = 0;
 constexpr int kAStride = 68;   // floats per row of A / (I+A)^-1
@@ -75,17 +78,22 @@ constexpr int kOStride = 136;  // bf16 per row of the staged output
 constexpr uint32_t OFF_ST = OFF_X + 73728;   // S^T bf16 [dv][dk] (K-major operand), 32 KB
 constexpr uint32_t OFF_SMALL = OFF_ST + 32768;
 constexpr uint32_t SM_NQ = 0, SM_NK = 256, SM_BETA = 512, SM_H0 = 768, SM_H1 = 2816, SM_GL = 4864,
-                   SM_DTB = 5376, SM_BAR = 5888, SM_TMEM = 5912, SM_ABORT = 5916, SM_END = 5952;
+                   SM_DTB = 5376, SM_BAR = 5888, SM_TMEM = 5928, SM_ABORT = 5932, SM_END = 5952;
 constexpr uint32_t kSmemBytes = OFF_SMALL + SM_END + 1024;  // + alignment slack
+static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+
+// offset of raw q / Q+ element (r, c) inside WQ
+__device__ __forceinline__ uint32_t q_off(int r, int c) { return sm100::swz_offset(128, 64 + r, c); }
 
 // ---- TMEM columns (fp32, lane = row of the M = 128 tile) ----
-// W^T, U^T, O^T accumulators; S^T (the state, lane = value channel, column =
+// W^T | U^T | O^T | S^T; U^T and O^T adjacent (one N = 128 product), O^T and
+// S^T adjacent (one N = 192 product).  S^T (lane = value channel, column =
 // key channel) lives in TMEM for the whole sequence.
-constexpr uint32_t TM_W = 0, TM_U = 64, TM_O = 128, TM_S = 256, TM_COLS = 512;
+constexpr uint32_t TM_W = 0, TM_U = 64, TM_O = 128, TM_S = 192, TM_COLS = 512;
 // A / P products (same columns as W / U / O, which are free at that point)
 constexpr uint32_t TM_AP_DIAG = 0;
 __host__ __device__ constexpr uint32_t tm_ap_off(int R) { return R == 1 ? 64u : R == 2 ? 80u : 112u; }
-static_assert(tm_ap_off(1) == 64 && tm_ap_off(3) + 48 == 160, "A/P product columns follow the GB tile rows");
+static_assert(tm_ap_off(1) == 64 && tm_ap_off(3) + 48 == 160 && 160 <= TM_S, "A/P product columns");
 
 struct Params {
   CUtensorMap tq, tk, tv, tg;
@@ -150,8 +158,8 @@ __device__ __forceinline__ float load_beta(const ChunkArgs &a, int tok, int h) {
 __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid_constant__ Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t *sQ = smem + OFF_Q, *sK = smem + OFF_K, *sV = smem + OFF_V, *sG = smem + OFF_G;
-  uint8_t *sX = smem + OFF_X, *sST = smem + OFF_ST;
+  uint8_t *sWQ = smem + OFF_WQ, *sK = smem + OFF_K, *sV = smem + OFF_V, *sG = smem + OFF_G;
+  uint8_t *sPK = smem + OFF_PK, *sX = smem + OFF_X, *sST = smem + OFF_ST;
   uint8_t *small = smem + OFF_SMALL;
   float *s_nq = reinterpret_cast<float *>(small + SM_NQ);
   float *s_nk = reinterpret_cast<float *>(small + SM_NK);
@@ -160,9 +168,10 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
   float *s_h1 = reinterpret_cast<float *>(small + SM_H1);      // [4][128] sum of lambda over rows 8..15
   float *s_gl = reinterpret_cast<float *>(small + SM_GL);      // [128] e^(b_63)
   float *s_dtb = reinterpret_cast<float *>(small + SM_DTB);    // [128]
-  uint64_t *bar_qkv = reinterpret_cast<uint64_t *>(small + SM_BAR);
-  uint64_t *bar_g = bar_qkv + 1;
-  uint64_t *bar_mma = bar_qkv + 2;
+  uint64_t *bar_q = reinterpret_cast<uint64_t *>(small + SM_BAR);
+  uint64_t *bar_kv = bar_q + 1;
+  uint64_t *bar_g = bar_q + 2;
+  uint64_t *bar_mma = bar_q + 3;
   uint32_t *s_tmem = reinterpret_cast<uint32_t *>(small + SM_TMEM);
   uint32_t *s_abort = reinterpret_cast<uint32_t *>(small + SM_ABORT);
 
@@ -184,9 +193,28 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
     }
   }
 
+  auto load_q = [&](int tok) {
+    mbar_arrive_expect_tx(bar_q, kTileBytes);
+    tma_load_3d(sWQ + 8192, &p.tq, 0, h, tok, bar_q);    // channels 0..63  -> rows 64..127 of panel 0
+    tma_load_3d(sWQ + 24576, &p.tq, 64, h, tok, bar_q);  // channels 64..127 -> rows 64..127 of panel 1
+  };
+  auto load_kv = [&](int tok) {
+    mbar_arrive_expect_tx(bar_kv, 2 * kTileBytes);
+    tma_load_3d(sK, &p.tk, 0, h, tok, bar_kv);
+    tma_load_3d(sK + 8192, &p.tk, 64, h, tok, bar_kv);
+    tma_load_3d(sV, &p.tv, 0, h, tok, bar_kv);
+    tma_load_3d(sV + 8192, &p.tv, 64, h, tok, bar_kv);
+  };
+  auto load_g = [&](int tok) {
+    mbar_arrive_expect_tx(bar_g, kTileBytes);
+    tma_load_3d(sG, &p.tg, 0, h, tok, bar_g);
+    tma_load_3d(sG + 8192, &p.tg, 64, h, tok, bar_g);
+  };
+
   // ---------------------------------------------------------------- setup
   if (tid == 0) {
-    mbar_init(bar_qkv, 1);
+    mbar_init(bar_q, 1);
+    mbar_init(bar_kv, 1);
     mbar_init(bar_g, 1);
     mbar_init(bar_mma, 1);
     *s_abort = 0;
@@ -207,16 +235,9 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
     prefetch_tensormap(&p.tk);
     prefetch_tensormap(&p.tv);
     prefetch_tensormap(&p.tg);
-    mbar_arrive_expect_tx(bar_qkv, 3 * kTileBytes);
-    tma_load_3d(sQ, &p.tq, 0, h, t0, bar_qkv);
-    tma_load_3d(sQ + 8192, &p.tq, 64, h, t0, bar_qkv);
-    tma_load_3d(sK, &p.tk, 0, h, t0, bar_qkv);
-    tma_load_3d(sK + 8192, &p.tk, 64, h, t0, bar_qkv);
-    tma_load_3d(sV, &p.tv, 0, h, t0, bar_qkv);
-    tma_load_3d(sV + 8192, &p.tv, 64, h, t0, bar_qkv);
-    mbar_arrive_expect_tx(bar_g, kTileBytes);
-    tma_load_3d(sG, &p.tg, 0, h, t0, bar_g);
-    tma_load_3d(sG + 8192, &p.tg, 64, h, t0, bar_g);
+    load_q(t0);
+    load_kv(t0);
+    load_g(t0);
   }
   // beta of the first chunk (later chunks: prefetched one chunk ahead)
   float beta_next = (tid < kC && tid < len) ? load_beta(a, t0 + tid, h) : 0.f;
@@ -254,19 +275,21 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
     const int tok0 = t0 + chunk * kC;
     const int valid = min(kC, len - chunk * kC);
     const uint32_t tma_parity = chunk & 1;
+    const bool has_next = chunk + 1 < nchunks;
     // -- wait for inputs
-    wait_or_flag(bar_qkv, tma_parity, s_abort, a.status);
-    wait_or_flag(bar_g, tma_parity, s_abort, a.status);
+    wait_or_flag(bar_q, tma_parity, s_abort, a.status);
+    wait_or_flag(bar_kv, tma_parity, s_abort, a.status);
 
     // ---------------------------------------------- A1: norms, beta, padding
     {
       const int task = tid >> 2, part = tid & 3;   // 128 (row, q|k) tasks x 4 threads of 32 channels
       const int r = task & 63;
-      const uint8_t *tile = task < 64 ? sQ : sK;
       float ss = 0.f;
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const uint4 w = *reinterpret_cast<const uint4 *>(tile + swz_offset(64, r, 32 * part + 8 * j));
+        const int c = 32 * part + 8 * j;
+        const uint8_t *src = task < 64 ? sWQ + q_off(r, c) : sK + swz_offset(64, r, c);
+        const uint4 w = *reinterpret_cast<const uint4 *>(src);
         const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -288,6 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
         }
       }
     }
+    wait_or_flag(bar_g, tma_parity, s_abort, a.status);
     __syncthreads();
 
     // ---------------------------------------------- A2: gate, decay, operands
@@ -314,8 +338,10 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
       *reinterpret_cast<float2 *>((half ? s_h1 : s_h0) + R * kD + c0) = make_float2(acc0, acc1);
       // -- gate done
       __syncthreads();
+      // raw g is no longer read: the next chunk's g may land
+      if (tid == 0 && has_next) load_g(tok0 + kC);
       // absolute anchors of every block: m_I = b at row 7, a_I = b at row 15
-      float mm[4][2], aa[4][2], tot0 = 0.f, tot1 = 0.f;
+      float mm[4][2], tot0 = 0.f, tot1 = 0.f, ar0 = 0.f, ar1 = 0.f, m0 = 0.f, m1 = 0.f;
 #pragma unroll
       for (int I = 0; I < 4; ++I) {
         const float2 x0 = *reinterpret_cast<const float2 *>(s_h0 + I * kD + c0);
@@ -324,26 +350,16 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
         mm[I][1] = tot1 + x0.y;
         tot0 += x0.x + x1.x;
         tot1 += x0.y + x1.y;
-        aa[I][0] = tot0;
-        aa[I][1] = tot1;
-      }
-      float m0 = 0.f, m1 = 0.f, ar0 = 0.f, ar1 = 0.f, t10 = 0.f, t11 = 0.f;
-#pragma unroll
-      for (int I = 0; I < 4; ++I) {
         if (I == R) {
           m0 = mm[I][0]; m1 = mm[I][1];
-          ar0 = aa[I][0]; ar1 = aa[I][1];
+          ar0 = tot0; ar1 = tot1;
         }
       }
-      {
-        const float2 x1 = *reinterpret_cast<const float2 *>(s_h1 + R * kD + c0);
-        t10 = x1.x;   // b_15 - b_7 of this block
-        t11 = x1.y;
-      }
+      const float2 t1 = *reinterpret_cast<const float2 *>(s_h1 + R * kD + c0);  // b_15 - b_7 of this block
       if (R == 0 && half == 0) *reinterpret_cast<float2 *>(s_gl + c0) = make_float2(exp_f(tot0), exp_f(tot1));
       const float em0 = exp_f(m0), em1 = exp_f(m1);              // e^(m_R)
       const float el0 = exp_f(tot0 - m0), el1 = exp_f(tot1 - m1);  // e^(b_63 - m_R)
-      const float eg0 = exp_f(t10), eg1 = exp_f(t11);              // e^(a_R - m_R)
+      const float eg0 = exp_f(t1.x), eg1 = exp_f(t1.y);            // e^(a_R - m_R)
       // rows of this block feed the off-diagonal B tiles of every later block R2:
       //   B_R2[i] = k^_i e^(m_R2 - b_i) = (k^_i e^(a_R - b_i)) * e^(m_R2 - a_R), both factors <= 1
       float cr[4][2];
@@ -354,6 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
       }
       // b_r - m_R from the thread's own partial sums: half 0 ends at row 7, half 1 starts after it
       const float base0 = half ? 0.f : b0[7], base1 = half ? 0.f : b1[7];
+      uint32_t kq0[4], kq1[4];   // K'^T rows c0, c0 + 1 over this thread's 8 tokens
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         const int r = rb + j;
@@ -361,7 +378,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
         const float e0 = exp_f(x0), e1 = exp_f(x1);
         const float i0 = exp_f(-x0), i1 = exp_f(-x1);
         const uint32_t off = swz_offset(64, r, c0);
-        const float2 qq = unpack_bf16x2(ld_u32(sQ + off));
+        const uint32_t qoff = q_off(r, c0);
+        const float2 qq = unpack_bf16x2(ld_u32(sWQ + qoff));
         const float2 kk = unpack_bf16x2(ld_u32(sK + off));
         const float nq = s_nq[r], nk = s_nk[r];
         const float qh0 = qq.x * nq, qh1 = qq.y * nq, kh0 = kk.x * nk, kh1 = kk.y * nk;
@@ -377,10 +395,20 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
             st_u32(sX + X_GB + swz_offset(kGBRows, gb_row0(R2) + r, c0),
                    pack_bf16x2(gp0 * cr[R2][0], gp1 * cr[R2][1]));
         }
-        st_u32(sQ + off, pack_bf16x2(fq0 * em0, fq1 * em1));  // Q+
-        st_u32(sK + off, pack_bf16x2(fk0 * em0, fk1 * em1));  // K+
-        st_u32(sG + off, pack_bf16x2(g0 * el0, g1 * el1));    // K'
+        st_u32(sWQ + qoff, pack_bf16x2(fq0 * em0, fq1 * em1));  // Q+
+        st_u32(sK + off, pack_bf16x2(fk0 * em0, fk1 * em1));    // K+
+        // K' = k^ e^(b_63 - b), collected along tokens for the transposed tile
+        const uint32_t kp = pack_bf16x2(g0 * el0, g1 * el1);
+        if (j & 1) {
+          kq0[j >> 1] = (kq0[j >> 1] & 0xFFFFu) | (kp << 16);
+          kq1[j >> 1] = (kq1[j >> 1] & 0xFFFFu) | (kp & 0xFFFF0000u);
+        } else {
+          kq0[j >> 1] = kp & 0xFFFFu;
+          kq1[j >> 1] = kp >> 16;
+        }
       }
+      *reinterpret_cast<uint4 *>(sPK + swz_offset(kPKRows, 64 + c0, rb)) = make_uint4(kq0[0], kq0[1], kq0[2], kq0[3]);
+      *reinterpret_cast<uint4 *>(sPK + swz_offset(kPKRows, 65 + c0, rb)) = make_uint4(kq1[0], kq1[1], kq1[2], kq1[3]);
     }
     fence_async_smem();
     tc_fence_before();
@@ -432,7 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
         v[e] = keep ? raw * bscale : 0.f;
       }
       if (is_p) {
-        store_row_bf16<2>(sX + X_P, 64, r, 16 * I, v);
+        store_row_bf16<2>(sPK, kPKRows, r, 16 * I, v);
       } else {
 #pragma unroll
         for (int e = 0; e < 16; e += 4)
@@ -531,57 +559,18 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
     tc_fence_before();
     __syncthreads();
 
-    // ---------------------------------------------- D: W^T = K+^T T^T, U^T = V^T T^T, O^T = S^T Q+^T
+    // ---------------------------------------------- D: W^T = K+^T T^T, U^T = V^T T^T; decay S^T, clear O^T
     if (tid == 0) {
       tc_fence_after();
       const uint32_t id_w = idesc_bf16(128, 64, true, false);
-      const uint32_t id_o = idesc_bf16(128, 64, false, false);
       const uint32_t kp = smem_u32(sK), v_ = smem_u32(sV), tt = smem_u32(sX + X_T);
-      const uint32_t st = smem_u32(sST), qp = smem_u32(sQ);
 #pragma unroll
       for (int s = 0; s < 4; ++s) mma_bf16(tmem + TM_W, desc_mnmajor(kp, 64, s), desc_kmajor(tt, 64, s), id_w, s > 0);
 #pragma unroll
       for (int s = 0; s < 4; ++s) mma_bf16(tmem + TM_U, desc_mnmajor(v_, 64, s), desc_kmajor(tt, 64, s), id_w, s > 0);
-#pragma unroll
-      for (int s = 0; s < 8; ++s) mma_bf16(tmem + TM_O, desc_kmajor(st, 128, s), desc_kmajor(qp, 64, s), id_o, s > 0);
       mma_commit(bar_mma);
     }
-    __syncwarp();
-    wait_or_flag(bar_mma, mma_phase & 1, s_abort, a.status);
-    ++mma_phase;
-    tc_fence_after();
-
-    // ---------------------------------------------- E: W^T (TMEM) -> W bf16 [dk][r]; U^T -= S^T W^T; decay S
-    {
-      uint32_t v[16];
-      tmem_ld16_async(tmem + lane_base + TM_W + 16 * qc, v);
-      tmem_wait_ld();
-      tmem_tie<16>(v);
-      store_row_bf16<2>(sX + X_W, 128, d, 16 * qc, reinterpret_cast<const float *>(v));
-    }
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    if (tid == 0) {
-      tc_fence_after();
-      const uint32_t id_u = idesc_bf16(128, 64, false, true, /*negate_a=*/true);
-      const uint32_t st = smem_u32(sST), w_ = smem_u32(sX + X_W);
-#pragma unroll
-      for (int s = 0; s < 8; ++s) mma_bf16(tmem + TM_U, desc_kmajor(st, 128, s), desc_mnmajor(w_, 128, s), id_u, 1);
-      mma_commit(bar_mma);
-      // q, k, v of the next chunk may now land (their tiles are no longer read)
-      if (chunk + 1 < nchunks) {
-        const int nt0 = tok0 + kC;
-        mbar_arrive_expect_tx(bar_qkv, 3 * kTileBytes);
-        tma_load_3d(sQ, &p.tq, 0, h, nt0, bar_qkv);
-        tma_load_3d(sQ + 8192, &p.tq, 64, h, nt0, bar_qkv);
-        tma_load_3d(sK, &p.tk, 0, h, nt0, bar_qkv);
-        tma_load_3d(sK + 8192, &p.tk, 64, h, nt0, bar_qkv);
-        tma_load_3d(sV, &p.tv, 0, h, nt0, bar_qkv);
-        tma_load_3d(sV + 8192, &p.tv, 64, h, nt0, bar_qkv);
-      }
-    }
-    // while the MMA runs: decay the state in TMEM, S^T <- S^T Diag(e^(b_63)), and fetch the next beta
+    // while the MMAs run: S^T <- S^T Diag(e^(b_63)) in TMEM, O^T <- 0, next beta
     {
       uint32_t sv[32];
       tmem_ld16_async(tmem + lane_base + TM_S + 32 * qc, sv);
@@ -599,6 +588,10 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
       }
       tmem_st16(tmem + lane_base + TM_S + 32 * qc, f);
       tmem_st16(tmem + lane_base + TM_S + 32 * qc + 16, f + 16);
+      float z[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) z[i] = 0.f;
+      tmem_st16(tmem + lane_base + TM_O + 16 * qc, z);
       tmem_wait_st();
     }
     if (tid < kC) {
@@ -609,8 +602,39 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
     wait_or_flag(bar_mma, mma_phase & 1, s_abort, a.status);
     ++mma_phase;
     tc_fence_after();
+    // k, v of the next chunk may now land (K+ and V are no longer read)
+    if (tid == 0 && has_next) load_kv(tok0 + kC);
 
-    // ---------------------------------------------- G: U^T (TMEM) -> bf16 [dv][i]; O^T += U^T P^T; S^T += U^T K'
+    // ---------------------------------------------- E: -W into WQ; [U^T | O^T] += S^T [-W; Q+]^T
+    {
+      uint32_t v[16];
+      tmem_ld16_async(tmem + lane_base + TM_W + 16 * qc, v);
+      tmem_wait_ld();
+      tmem_tie<16>(v);
+      // W^T lane = key channel c; W row r = 16*qc + i, column c
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        *reinterpret_cast<uint16_t *>(sWQ + swz_offset(128, 16 * qc + i, d)) = f32_to_bf16_bits(-__uint_as_float(v[i]));
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {
+      tc_fence_after();
+      const uint32_t id_uo = idesc_bf16(128, 128, false, false);
+      const uint32_t st = smem_u32(sST), wq = smem_u32(sWQ);
+#pragma unroll
+      for (int s = 0; s < 8; ++s) mma_bf16(tmem + TM_U, desc_kmajor(st, 128, s), desc_kmajor(wq, 128, s), id_uo, 1);
+      mma_commit(bar_mma);
+    }
+    __syncwarp();
+    wait_or_flag(bar_mma, mma_phase & 1, s_abort, a.status);
+    ++mma_phase;
+    tc_fence_after();
+    // q of the next chunk may now land (Q+ and W are no longer read)
+    if (tid == 0 && has_next) load_q(tok0 + kC);
+
+    // ---------------------------------------------- G: U^T -> bf16 [dv][i]; [O^T | S^T] += U^T [P; K'^T]^T
     {
       uint32_t v[16];
       tmem_ld16_async(tmem + lane_base + TM_U + 16 * qc, v);
@@ -623,25 +647,16 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
     __syncthreads();
     if (tid == 0) {
       tc_fence_after();
-      const uint32_t id_o = idesc_bf16(128, 64, false, false);
-      const uint32_t id_s = idesc_bf16(128, 128, false, true);
-      const uint32_t ut = smem_u32(sX + X_UT), pp = smem_u32(sX + X_P), kq = smem_u32(sG);
+      const uint32_t id_os = idesc_bf16(128, kPKRows, false, false);
+      const uint32_t ut = smem_u32(sX + X_UT), pk = smem_u32(sPK);
 #pragma unroll
-      for (int s = 0; s < 4; ++s) mma_bf16(tmem + TM_O, desc_kmajor(ut, 128, s), desc_kmajor(pp, 64, s), id_o, 1);
-#pragma unroll
-      for (int s = 0; s < 4; ++s) mma_bf16(tmem + TM_S, desc_kmajor(ut, 128, s), desc_mnmajor(kq, 64, s), id_s, 1);
+      for (int s = 0; s < 4; ++s) mma_bf16(tmem + TM_O, desc_kmajor(ut, 128, s), desc_kmajor(pk, kPKRows, s), id_os, 1);
       mma_commit(bar_mma);
     }
     __syncwarp();
     wait_or_flag(bar_mma, mma_phase & 1, s_abort, a.status);
     ++mma_phase;
     tc_fence_after();
-    if (tid == 0 && chunk + 1 < nchunks) {
-      const int nt0 = tok0 + kC;
-      mbar_arrive_expect_tx(bar_g, kTileBytes);
-      tma_load_3d(sG, &p.tg, 0, h, nt0, bar_g);
-      tma_load_3d(sG + 8192, &p.tg, 64, h, nt0, bar_g);
-    }
 
     // ---------------------------------------------- I: S^T -> bf16 operand, output
     {
