@@ -109,8 +109,6 @@ __device__ __forceinline__ float2 unpack_bf16x2(uint32_t v) {
   return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
 }
 
-__device__ __forceinline__ float exp_f(float x) { return fast_exp2(x * kLog2e); }
-
 __device__ __forceinline__ uint32_t to_tf32(float x) {
   uint32_t r;
   asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
@@ -153,6 +151,62 @@ __device__ __forceinline__ void store_row_bf16(uint8_t *tile, int R, int row, in
 
 __device__ __forceinline__ float load_beta(const ChunkArgs &a, int tok, int h) {
   return sigmoid_f(bf16_bits_to_f32(a.beta[(size_t)tok * a.beta_stride + h]));
+}
+
+// ---- packed fp32x2 arithmetic (sm_100 family): one instruction per channel pair ----
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+__device__ __forceinline__ float2 exp2_2(float2 x) { return make_float2(fast_exp2(x.x), fast_exp2(x.y)); }
+__device__ __forceinline__ uint32_t pack2(float2 v) { return pack_bf16x2(v.x, v.y); }
+
+// Operand pass of the prologue for one thread's 8 rows (block RB known at
+// compile time) and one channel pair c0, c0 + 1.  x holds (b_r - m_R) log2(e).
+template <int RB>
+__device__ __forceinline__ void operand_rows(const float2 (&x)[8], int half, int c0, uint8_t *sWQ, uint8_t *sK,
+                                            uint8_t *sX, uint8_t *sPK, const float *s_nq, const float *s_nk,
+                                            float2 em, float2 el, float2 eg, const float2 (&cr)[4]) {
+  const int rb = 16 * RB + 8 * half;
+  uint32_t kq0[4], kq1[4];   // K'^T rows c0, c0 + 1 over this thread's 8 tokens
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int r = rb + j;
+    const float2 e = exp2_2(x[j]);
+    const float2 iv = exp2_2(make_float2(-x[j].x, -x[j].y));
+    const uint32_t off = swz_offset(64, r, c0);
+    const uint32_t qoff = q_off(r, c0);
+    const float nq = s_nq[r], nk = s_nk[r];
+    const float2 qh = mul2(unpack_bf16x2(ld_u32(sWQ + qoff)), make_float2(nq, nq));
+    const float2 kh = mul2(unpack_bf16x2(ld_u32(sK + off)), make_float2(nk, nk));
+    const float2 fk = mul2(kh, e), fq = mul2(qh, e), g = mul2(kh, iv);
+    st_u32(sX + X_FKQ + swz_offset(128, r, c0), pack2(fk));
+    st_u32(sX + X_FKQ + swz_offset(128, 64 + r, c0), pack2(fq));
+    st_u32(sX + X_GB + swz_offset(kGBRows, r, c0), pack2(g));
+    if (RB < 3) {
+      const float2 gp = mul2(g, eg);  // k^ e^(a_R - b)
+#pragma unroll
+      for (int R2 = RB + 1; R2 < 4; ++R2)
+        st_u32(sX + X_GB + swz_offset(kGBRows, gb_row0(R2) + r, c0), pack2(mul2(gp, cr[R2])));
+    }
+    st_u32(sWQ + qoff, pack2(mul2(fq, em)));  // Q+
+    st_u32(sK + off, pack2(mul2(fk, em)));    // K+
+    // K' = k^ e^(b_63 - b), collected along tokens for the transposed tile
+    const uint32_t kp = pack2(mul2(g, el));
+    if (j & 1) {
+      kq0[j >> 1] |= kp << 16;
+      kq1[j >> 1] |= kp & 0xFFFF0000u;
+    } else {
+      kq0[j >> 1] = kp & 0xFFFFu;
+      kq1[j >> 1] = kp >> 16;
+    }
+  }
+  *reinterpret_cast<uint4 *>(sPK + swz_offset(kPKRows, 64 + c0, rb)) = make_uint4(kq0[0], kq0[1], kq0[2], kq0[3]);
+  *reinterpret_cast<uint4 *>(sPK + swz_offset(kPKRows, 65 + c0, rb)) = make_uint4(kq1[0], kq1[1], kq1[2], kq1[3]);
 }
 
 __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid_constant__ Params p) {
@@ -267,8 +321,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
   __syncthreads();
   tc_fence_after();
 
-  const float ea = __expf(a.A_log[h]);
-  const float lb = a.lower_bound;
+  const float nea = -__expf(a.A_log[h]) * kLog2e;  // gate slope, log2 units
+  const float lb2 = a.lower_bound * kLog2e;        // lower bound, log2 units
   uint32_t mma_phase = 0;
 
   for (int chunk = 0; chunk < nchunks; ++chunk) {
@@ -280,9 +334,10 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
     wait_or_flag(bar_q, tma_parity, s_abort, a.status);
     wait_or_flag(bar_kv, tma_parity, s_abort, a.status);
 
-    // ---------------------------------------------- A1: norms, beta, padding
+    // ---------------------------------------------- A: norms, beta, padding, gate, decay, operands
+    // (decays are kept in log2 units: b2 = b * log2(e), so every factor is one ex2)
     {
-      const int task = tid >> 2, part = tid & 3;   // 128 (row, q|k) tasks x 4 threads of 32 channels
+      const int task = tid >> 2, part = tid & 3;   // norms: 128 (row, q|k) tasks x 4 threads of 32 channels
       const int r = task & 63;
       float ss = 0.f;
 #pragma unroll
@@ -312,24 +367,22 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
       }
     }
     wait_or_flag(bar_g, tma_parity, s_abort, a.status);
-    __syncthreads();
-
-    // ---------------------------------------------- A2: gate, decay, operands
     {
       // thread = (channel pair, 16-row block R, half of the block): 8 rows x 2 channels
       const int cp = tid & 63, R = (tid >> 6) & 3, half = tid >> 8;
       const int c0 = 2 * cp;
       const int rb = 16 * R + 8 * half;   // first row of this thread
-      const float dtb0 = s_dtb[c0], dtb1 = s_dtb[c0 + 1];
-      float b0[8], b1[8];   // cumulative log-decay from the start of this half-block
+      // sigmoid(ea (g + dtb)) = 1 / (1 + 2^(nea g + nea dtb)),  nea = -ea log2(e)
+      const float nd0 = nea * s_dtb[c0], nd1 = nea * s_dtb[c0 + 1];
+      float b0[8], b1[8];   // cumulative log2-decay from the start of this half-block
       float acc0 = 0.f, acc1 = 0.f;
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         const int r = rb + j;
         const float2 gg = unpack_bf16x2(ld_u32(sG + swz_offset(64, r, c0)));
         const bool ok = r < valid;
-        const float l0 = ok ? lb * sigmoid_f(ea * (gg.x + dtb0)) : 0.f;
-        const float l1 = ok ? lb * sigmoid_f(ea * (gg.y + dtb1)) : 0.f;
+        const float l0 = ok ? lb2 * fast_rcp(1.f + fast_exp2(fmaf(nea, gg.x, nd0))) : 0.f;
+        const float l1 = ok ? lb2 * fast_rcp(1.f + fast_exp2(fmaf(nea, gg.y, nd1))) : 0.f;
         acc0 += l0;
         acc1 += l1;
         b0[j] = acc0;
@@ -356,59 +409,35 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
         }
       }
       const float2 t1 = *reinterpret_cast<const float2 *>(s_h1 + R * kD + c0);  // b_15 - b_7 of this block
-      if (R == 0 && half == 0) *reinterpret_cast<float2 *>(s_gl + c0) = make_float2(exp_f(tot0), exp_f(tot1));
-      const float em0 = exp_f(m0), em1 = exp_f(m1);              // e^(m_R)
-      const float el0 = exp_f(tot0 - m0), el1 = exp_f(tot1 - m1);  // e^(b_63 - m_R)
-      const float eg0 = exp_f(t1.x), eg1 = exp_f(t1.y);            // e^(a_R - m_R)
+      if (R == 0 && half == 0)
+        *reinterpret_cast<float2 *>(s_gl + c0) = make_float2(fast_exp2(tot0), fast_exp2(tot1));
+      const float em0 = fast_exp2(m0), em1 = fast_exp2(m1);              // e^(m_R)
+      const float el0 = fast_exp2(tot0 - m0), el1 = fast_exp2(tot1 - m1);  // e^(b_63 - m_R)
+      const float eg0 = fast_exp2(t1.x), eg1 = fast_exp2(t1.y);            // e^(a_R - m_R)
       // rows of this block feed the off-diagonal B tiles of every later block R2:
       //   B_R2[i] = k^_i e^(m_R2 - b_i) = (k^_i e^(a_R - b_i)) * e^(m_R2 - a_R), both factors <= 1
       float cr[4][2];
+      cr[0][0] = cr[0][1] = 0.f;
 #pragma unroll
       for (int R2 = 1; R2 < 4; ++R2) {
-        cr[R2][0] = exp_f(fminf(mm[R2][0] - ar0, 0.f));
-        cr[R2][1] = exp_f(fminf(mm[R2][1] - ar1, 0.f));
+        cr[R2][0] = fast_exp2(fminf(mm[R2][0] - ar0, 0.f));
+        cr[R2][1] = fast_exp2(fminf(mm[R2][1] - ar1, 0.f));
       }
       // b_r - m_R from the thread's own partial sums: half 0 ends at row 7, half 1 starts after it
       const float base0 = half ? 0.f : b0[7], base1 = half ? 0.f : b1[7];
-      uint32_t kq0[4], kq1[4];   // K'^T rows c0, c0 + 1 over this thread's 8 tokens
+      float2 x[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int r = rb + j;
-        const float x0 = b0[j] - base0, x1 = b1[j] - base1;   // b_r - m_R
-        const float e0 = exp_f(x0), e1 = exp_f(x1);
-        const float i0 = exp_f(-x0), i1 = exp_f(-x1);
-        const uint32_t off = swz_offset(64, r, c0);
-        const uint32_t qoff = q_off(r, c0);
-        const float2 qq = unpack_bf16x2(ld_u32(sWQ + qoff));
-        const float2 kk = unpack_bf16x2(ld_u32(sK + off));
-        const float nq = s_nq[r], nk = s_nk[r];
-        const float qh0 = qq.x * nq, qh1 = qq.y * nq, kh0 = kk.x * nk, kh1 = kk.y * nk;
-        const float fk0 = kh0 * e0, fk1 = kh1 * e1, fq0 = qh0 * e0, fq1 = qh1 * e1;
-        const float g0 = kh0 * i0, g1 = kh1 * i1;
-        st_u32(sX + X_FKQ + swz_offset(128, r, c0), pack_bf16x2(fk0, fk1));
-        st_u32(sX + X_FKQ + swz_offset(128, 64 + r, c0), pack_bf16x2(fq0, fq1));
-        st_u32(sX + X_GB + swz_offset(kGBRows, r, c0), pack_bf16x2(g0, g1));
-        const float gp0 = g0 * eg0, gp1 = g1 * eg1;  // k^ e^(a_R - b)
+      for (int j = 0; j < 8; ++j) x[j] = make_float2(b0[j] - base0, b1[j] - base1);
+      const float2 em = make_float2(em0, em1), el = make_float2(el0, el1), eg = make_float2(eg0, eg1);
+      float2 crp[4];
 #pragma unroll
-        for (int R2 = 1; R2 < 4; ++R2) {
-          if (R2 > R)
-            st_u32(sX + X_GB + swz_offset(kGBRows, gb_row0(R2) + r, c0),
-                   pack_bf16x2(gp0 * cr[R2][0], gp1 * cr[R2][1]));
-        }
-        st_u32(sWQ + qoff, pack_bf16x2(fq0 * em0, fq1 * em1));  // Q+
-        st_u32(sK + off, pack_bf16x2(fk0 * em0, fk1 * em1));    // K+
-        // K' = k^ e^(b_63 - b), collected along tokens for the transposed tile
-        const uint32_t kp = pack_bf16x2(g0 * el0, g1 * el1);
-        if (j & 1) {
-          kq0[j >> 1] = (kq0[j >> 1] & 0xFFFFu) | (kp << 16);
-          kq1[j >> 1] = (kq1[j >> 1] & 0xFFFFu) | (kp & 0xFFFF0000u);
-        } else {
-          kq0[j >> 1] = kp & 0xFFFFu;
-          kq1[j >> 1] = kp >> 16;
-        }
+      for (int R2 = 0; R2 < 4; ++R2) crp[R2] = make_float2(cr[R2][0], cr[R2][1]);
+      switch (R) {   // warp-uniform
+        case 0: operand_rows<0>(x, half, c0, sWQ, sK, sX, sPK, s_nq, s_nk, em, el, eg, crp); break;
+        case 1: operand_rows<1>(x, half, c0, sWQ, sK, sX, sPK, s_nq, s_nk, em, el, eg, crp); break;
+        case 2: operand_rows<2>(x, half, c0, sWQ, sK, sX, sPK, s_nq, s_nk, em, el, eg, crp); break;
+        default: operand_rows<3>(x, half, c0, sWQ, sK, sX, sPK, s_nq, s_nk, em, el, eg, crp); break;
       }
-      *reinterpret_cast<uint4 *>(sPK + swz_offset(kPKRows, 64 + c0, rb)) = make_uint4(kq0[0], kq0[1], kq0[2], kq0[3]);
-      *reinterpret_cast<uint4 *>(sPK + swz_offset(kPKRows, 65 + c0, rb)) = make_uint4(kq1[0], kq1[1], kq1[2], kq1[3]);
     }
     fence_async_smem();
     tc_fence_before();
