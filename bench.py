@@ -196,19 +196,24 @@ def oracle_sample_rate(inp, seqs, tokens, nthreads):
     return seqs * tokens, time.perf_counter() - t0
 
 
-def cpu_baseline(inp, budget_s=12.0):
+def cpu_baseline(inp, budget_s=30.0):
+    """The oracle on the host cores: the whole workload (all sequences and heads),
+    shortened per sequence only if a calibration run predicts more than
+    `budget_s` seconds of CPU work."""
     import oracle
 
     oracle.build()
     nthreads = oracle.default_threads()
-    seqs = min(inp.num_seqs, max(1, nthreads // inp.H) or 1)
-    tok, dt = oracle_sample_rate(inp, seqs, 128, nthreads)  # calibration
-    rate = tok / dt
-    tokens = int(min(2048, max(128, budget_s * rate / seqs)))
+    seqs = inp.num_seqs
+    full = int(inp.cu_seqlens[1] - inp.cu_seqlens[0])
+    tok, dt = oracle_sample_rate(inp, seqs, 64, nthreads)  # calibration
+    core_s_per_token = dt * nthreads / tok
+    tokens = int(min(full, max(64, budget_s / core_s_per_token / seqs)))
     tok, dt = oracle_sample_rate(inp, seqs, tokens, nthreads)
+    what = "the whole workload" if tokens == full else f"first {tokens} tokens of each sequence"
     return {"value": tok / dt, "unit": "tokens/s", "cores": nthreads, "kind": "oracle",
-            "sample": f"{seqs} of the {inp.num_seqs} sequences x all {inp.H} heads, first {tokens} tokens each "
-                      f"(fp64 token-by-token, {dt:.1f} s wall)"}
+            "sample": f"{what}: {seqs} sequences x all {inp.H} heads, fp64 token-by-token, "
+                      f"{dt:.2f} s wall on {nthreads} threads (~{dt * nthreads:.0f} core-s)"}
 
 
 def run_reference(args):
