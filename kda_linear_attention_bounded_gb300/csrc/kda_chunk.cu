@@ -69,8 +69,8 @@ constexpr uint32_t OFF_X = 106496;   // phase-dependent scratch, 73728 bytes:
 constexpr uint32_t X_FKQ = 0, X_GB = 32768;
 constexpr int kGBRows = 160;
 __host__ __device__ constexpr int gb_row0(int R) { return R == 0 ? 0 : R == 1 ? 64 : R == 2 ? 80 : 112; }
-//   after A/P:  A fp32 [64][68] | T bf16 [r][i] | U^T bf16 [dv][i] | (I+A)^-1 fp32 [64][68] | block products
-constexpr uint32_t X_A = 0, X_T = 17408, X_UT = 25600, X_INV = 41984, X_Y = 59392;
+//   after A/P:  A fp32 [64][68] (later Inv_RR A_RJ) | T bf16 [r][i] | U^T bf16 [dv][i] | (I+A)^-1 fp32 [64][68]
+constexpr uint32_t X_A = 0, X_T = 17408, X_UT = 25600, X_INV = 41984;
 //   output staging: O bf16 [64][136] over A
 constexpr uint32_t X_O = 0;
 constexpr int kAStride = 68;   // floats per row of A / (I+A)^-1
@@ -503,86 +503,99 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
     {
       const float *sA = reinterpret_cast<const float *>(sX + X_A);
       float *sInv = reinterpret_cast<float *>(sX + X_INV);
-      // C1: inverses of the unit-lower 16x16 diagonal blocks (warp R, lane = column)
-      if (warp < 4 && lane < 16) {
-        const int R = warp, jc = lane;
-        float x[16];
+      // C1: inverses of the unit-lower 16x16 diagonal blocks (warp R, lane = column); their part
+      // of T = Inv Diag(beta) goes straight to the bf16 T tile.  Warps 4..15 clear the upper blocks of T.
+      uint16_t *sT16 = reinterpret_cast<uint16_t *>(sX + X_T);
+      if (warp < 4) {
+        if (lane < 16) {
+          const int R = warp, jc = lane;
+          const float bj = s_beta[16 * R + jc];
+          float x[16];
 #pragma unroll
-        for (int r = 0; r < 16; ++r) {
-          float lrow[16];
+          for (int r = 0; r < 16; ++r) {
+            float lrow[16];
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            const float4 l4 = *reinterpret_cast<const float4 *>(sA + (16 * R + r) * kAStride + 16 * R + 4 * q4);
-            lrow[4 * q4] = l4.x; lrow[4 * q4 + 1] = l4.y; lrow[4 * q4 + 2] = l4.z; lrow[4 * q4 + 3] = l4.w;
+            for (int q4 = 0; q4 < 4; ++q4) {
+              const float4 l4 = *reinterpret_cast<const float4 *>(sA + (16 * R + r) * kAStride + 16 * R + 4 * q4);
+              lrow[4 * q4] = l4.x; lrow[4 * q4 + 1] = l4.y; lrow[4 * q4 + 2] = l4.z; lrow[4 * q4 + 3] = l4.w;
+            }
+            float v0 = (r == jc) ? 1.f : 0.f, v1 = 0.f;
+#pragma unroll
+            for (int m = 0; m < r; ++m) {
+              if (m & 1) v1 = fmaf(-lrow[m], x[m], v1);
+              else v0 = fmaf(-lrow[m], x[m], v0);
+            }
+            x[r] = v0 + v1;
           }
-          float v0 = (r == jc) ? 1.f : 0.f, v1 = 0.f;
 #pragma unroll
-          for (int m = 0; m < r; ++m) {
-            if (m & 1) v1 = fmaf(-lrow[m], x[m], v1);
-            else v0 = fmaf(-lrow[m], x[m], v0);
+          for (int r = 0; r < 16; ++r) {
+            sInv[(16 * R + r) * kAStride + 16 * R + jc] = x[r];
+            sT16[swz_offset(64, 16 * R + r, 16 * R + jc) >> 1] = f32_to_bf16_bits(r >= jc ? x[r] * bj : 0.f);
           }
-          x[r] = v0 + v1;
         }
-#pragma unroll
-        for (int r = 0; r < 16; ++r) sInv[(16 * R + r) * kAStride + 16 * R + jc] = x[r];
+      } else {
+        // strictly-upper 16x16 blocks (R, I > R): 6 blocks x 16 rows x 2 chunks of 8 columns
+        for (int idx = tid - 128; idx < 6 * 32; idx += kThreads - 128) {
+          const int blk = idx >> 5, e = idx & 31;
+          const int R = blk < 3 ? 0 : blk < 5 ? 1 : 2;
+          const int I = blk < 3 ? blk + 1 : blk < 5 ? blk - 1 : 3;
+          *reinterpret_cast<uint4 *>(sX + X_T + swz_offset(64, 16 * R + (e >> 1), 16 * I + 8 * (e & 1))) =
+              make_uint4(0, 0, 0, 0);
+        }
       }
       __syncthreads();
       // -- diagonal inverses done
-      // C2: off-diagonal blocks by distance dd = R - I:
-      //   Inv_RI = -Inv_RR * sum_{J=I}^{R-1} A_RJ Inv_JI
-      // on the tensor cores in TF32 (m16n8k8): one warp per 16 x 8 half of a block
+      // C2: off-diagonal blocks.  With L~_RJ = Inv_RR A_RJ (J < R, computed in place over A):
+      //   Inv_RI = - sum_{J=I}^{R-1} L~_RJ Inv_JI.
+      // Each warp owns an 8-column half of one column block I and walks down it, reading only
+      // its own earlier results, so the steps need no CTA-wide barrier.  TF32 m16n8k8 tensor-core MMAs.
       {
+        float *sAw = reinterpret_cast<float *>(sX + X_A);
         const int g = lane >> 2, t = lane & 3;
-#pragma unroll 1
-        for (int dd = 1; dd < 4; ++dd) {
-          if (warp < 2 * (4 - dd)) {
-            const int I = warp >> 1, R = I + dd;
-            const int n0 = 16 * I + 8 * (warp & 1);
-            float y[4] = {0.f, 0.f, 0.f, 0.f};
+        // pre-multiply: 6 block pairs x 2 column halves = 12 warps, all independent
+        if (warp < 12) {
+          const int pr = warp >> 1;                       // (R, J): (1,0) (2,0) (2,1) (3,0) (3,1) (3,2)
+          const int R = pr < 1 ? 1 : pr < 3 ? 2 : 3;
+          const int J = pr - (R * (R - 1)) / 2;
+          const int n0 = 16 * J + 8 * (warp & 1);
+          float y[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int ks = 0; ks < 2; ++ks) {
+            const float *ar = sInv + (16 * R + g) * kAStride + 16 * R + 8 * ks + t;
+            const float *br = sAw + (16 * R + 8 * ks + t) * kAStride + n0 + g;
+            mma_1688_tf32(y, to_tf32(ar[0]), to_tf32(ar[8 * kAStride]), to_tf32(ar[4]),
+                          to_tf32(ar[8 * kAStride + 4]), to_tf32(br[0]), to_tf32(br[4 * kAStride]));
+          }
+          *reinterpret_cast<float2 *>(sAw + (16 * R + g) * kAStride + n0 + 2 * t) = make_float2(y[0], y[1]);
+          *reinterpret_cast<float2 *>(sAw + (16 * R + g + 8) * kAStride + n0 + 2 * t) = make_float2(y[2], y[3]);
+        }
+        __syncthreads();
+        // column walks: warp = (column block I in 0..2, half); I = 0 takes 3 steps, I = 2 one
+        if (warp < 6) {
+          const int I = warp >> 1;
+          const int n0 = 16 * I + 8 * (warp & 1);
+          const float2 bcol = *reinterpret_cast<const float2 *>(s_beta + n0 + 2 * t);
+          for (int R = I + 1; R < 4; ++R) {
+            float x[4] = {0.f, 0.f, 0.f, 0.f};
             for (int J = I; J < R; ++J) {
 #pragma unroll
               for (int ks = 0; ks < 2; ++ks) {
                 const int kc = 16 * J + 8 * ks;
-                const float *ar = sA + (16 * R + g) * kAStride + kc + t;
+                const float *ar = sAw + (16 * R + g) * kAStride + kc + t;
                 const float *br = sInv + (kc + t) * kAStride + n0 + g;
-                mma_1688_tf32(y, to_tf32(ar[0]), to_tf32(ar[8 * kAStride]), to_tf32(ar[4]),
+                mma_1688_tf32(x, to_tf32(ar[0]), to_tf32(ar[8 * kAStride]), to_tf32(ar[4]),
                               to_tf32(ar[8 * kAStride + 4]), to_tf32(br[0]), to_tf32(br[4 * kAStride]));
               }
             }
-            float *sYw = reinterpret_cast<float *>(sX + X_Y) + warp * 128;  // Y: 16 x 8
-            *reinterpret_cast<float2 *>(sYw + g * 8 + 2 * t) = make_float2(y[0], y[1]);
-            *reinterpret_cast<float2 *>(sYw + (g + 8) * 8 + 2 * t) = make_float2(y[2], y[3]);
-            __syncwarp();
-            float x[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int ks = 0; ks < 2; ++ks) {
-              const float *ar = sInv + (16 * R + g) * kAStride + 16 * R + 8 * ks + t;
-              const float *br = sYw + (8 * ks + t) * 8 + g;
-              mma_1688_tf32(x, to_tf32(ar[0]), to_tf32(ar[8 * kAStride]), to_tf32(ar[4]),
-                            to_tf32(ar[8 * kAStride + 4]), to_tf32(br[0]), to_tf32(br[32]));
-            }
             *reinterpret_cast<float2 *>(sInv + (16 * R + g) * kAStride + n0 + 2 * t) = make_float2(-x[0], -x[1]);
             *reinterpret_cast<float2 *>(sInv + (16 * R + g + 8) * kAStride + n0 + 2 * t) = make_float2(-x[2], -x[3]);
+            st_u32(sX + X_T + swz_offset(64, 16 * R + g, n0 + 2 * t), pack_bf16x2(-x[0] * bcol.x, -x[1] * bcol.y));
+            st_u32(sX + X_T + swz_offset(64, 16 * R + g + 8, n0 + 2 * t), pack_bf16x2(-x[2] * bcol.x, -x[3] * bcol.y));
+            __syncwarp();
           }
-          __syncthreads();
         }
       }
-      // -- off-diagonal inverses done
-      // C3: T = Inv Diag(beta), lower triangle, bf16 K-major [r][i]
-      {
-        const int r = tid >> 3, i0 = 8 * (tid & 7);
-        float v[8];
-#pragma unroll
-        for (int e = 0; e < 8; e += 4) {
-          const float4 x4 = *reinterpret_cast<const float4 *>(sInv + r * kAStride + i0 + e);
-          const float4 b4 = *reinterpret_cast<const float4 *>(s_beta + i0 + e);
-          v[e] = (i0 + e <= r) ? x4.x * b4.x : 0.f;
-          v[e + 1] = (i0 + e + 1 <= r) ? x4.y * b4.y : 0.f;
-          v[e + 2] = (i0 + e + 2 <= r) ? x4.z * b4.z : 0.f;
-          v[e + 3] = (i0 + e + 3 <= r) ? x4.w * b4.w : 0.f;
-        }
-        store_row_bf16<1>(sX + X_T, 64, r, i0, v);
-      }
+      // -- T done
     }
     fence_async_smem();
     tc_fence_before();
