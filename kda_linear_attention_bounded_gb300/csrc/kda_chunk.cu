@@ -149,9 +149,6 @@ __device__ __forceinline__ void store_row_bf16(uint8_t *tile, int R, int row, in
   }
 }
 
-__device__ __forceinline__ float load_beta(const ChunkArgs &a, int tok, int h) {
-  return sigmoid_f(bf16_bits_to_f32(a.beta[(size_t)tok * a.beta_stride + h]));
-}
 
 // ---- packed fp32x2 arithmetic (sm_100 family): one instruction per channel pair ----
 __device__ __forceinline__ float2 mul2(float2 a, float2 b) {
@@ -293,8 +290,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
     load_kv(t0);
     load_g(t0);
   }
-  // beta of the first chunk (later chunks: prefetched one chunk ahead)
-  float beta_next = (tid < kC && tid < len) ? load_beta(a, t0 + tid, h) : 0.f;
+  // raw beta logits, fetched one chunk ahead (the sigmoid is applied when they are used)
+  uint16_t beta_raw = (tid < kC && tid < len) ? a.beta[(size_t)(t0 + tid) * a.beta_stride + h] : uint16_t(0);
 
   // TMEM tiles are read / written by warp w on lanes 32*(w%4) .. +31 and a
   // quarter (w/4) of the columns.  For S^T: lane = value channel d.
@@ -358,7 +355,11 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
         const float nrm = r < valid ? rsqrtf(ss + kL2Eps) : 0.f;
         (task < 64 ? s_nq : s_nk)[r] = nrm;
       }
-      if (tid < kC) s_beta[tid] = beta_next;
+      if (tid < kC) {
+        s_beta[tid] = tid < valid ? sigmoid_f(bf16_bits_to_f32(beta_raw)) : 0.f;
+        const int nt = (chunk + 1) * kC + tid;   // next chunk's logit: a whole chunk to arrive
+        beta_raw = nt < len ? a.beta[(size_t)(t0 + nt) * a.beta_stride + h] : uint16_t(0);
+      }
       if (valid < kC) {  // rows past the sequence end: zero v (the others are masked through beta, norms, lambda)
         for (int idx = tid; idx < (kC - valid) * 16; idx += kThreads) {
           const int r2 = valid + idx / 16, cc = idx % 16;
@@ -454,6 +455,26 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
         mma_bf16(tmem + TM_AP_DIAG, desc_kmajor(fkq, 128, s), desc_kmajor(gb, kGBRows, s),
                  idesc_bf16(128, kGBRows, false, false), s > 0);
       mma_commit(bar_mma);
+    }
+    // while the A/P product runs (columns 0..159): S^T <- S^T Diag(e^(b_63)) in TMEM (columns 192..319)
+    {
+      uint32_t sv[32];
+      tmem_ld16_async(tmem + lane_base + TM_S + 32 * qc, sv);
+      tmem_ld16_async(tmem + lane_base + TM_S + 32 * qc + 16, sv + 16);
+      tmem_wait_ld();
+      tmem_tie<32>(sv);
+      float f[32];
+#pragma unroll
+      for (int i = 0; i < 32; i += 4) {
+        const float4 g4 = *reinterpret_cast<const float4 *>(s_gl + 32 * qc + i);
+        f[i] = __uint_as_float(sv[i]) * g4.x;
+        f[i + 1] = __uint_as_float(sv[i + 1]) * g4.y;
+        f[i + 2] = __uint_as_float(sv[i + 2]) * g4.z;
+        f[i + 3] = __uint_as_float(sv[i + 3]) * g4.w;
+      }
+      tmem_st16(tmem + lane_base + TM_S + 32 * qc, f);
+      tmem_st16(tmem + lane_base + TM_S + 32 * qc + 16, f + 16);
+      tmem_wait_st();
     }
     __syncwarp();
     wait_or_flag(bar_mma, mma_phase & 1, s_abort, a.status);
@@ -601,7 +622,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
     tc_fence_before();
     __syncthreads();
 
-    // ---------------------------------------------- D: W^T = K+^T T^T, U^T = V^T T^T; decay S^T, clear O^T
+    // ---------------------------------------------- D: W^T = K+^T T^T, U^T = V^T T^T; clear O^T
     if (tid == 0) {
       tc_fence_after();
       const uint32_t id_w = idesc_bf16(128, 64, true, false);
@@ -612,33 +633,13 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
       for (int s = 0; s < 4; ++s) mma_bf16(tmem + TM_U, desc_mnmajor(v_, 64, s), desc_kmajor(tt, 64, s), id_w, s > 0);
       mma_commit(bar_mma);
     }
-    // while the MMAs run: S^T <- S^T Diag(e^(b_63)) in TMEM, O^T <- 0, next beta
+    // while the MMAs run: O^T <- 0 (its columns were A/P products until now), next beta
     {
-      uint32_t sv[32];
-      tmem_ld16_async(tmem + lane_base + TM_S + 32 * qc, sv);
-      tmem_ld16_async(tmem + lane_base + TM_S + 32 * qc + 16, sv + 16);
-      tmem_wait_ld();
-      tmem_tie<32>(sv);
-      float f[32];
-#pragma unroll
-      for (int i = 0; i < 32; i += 4) {
-        const float4 g4 = *reinterpret_cast<const float4 *>(s_gl + 32 * qc + i);
-        f[i] = __uint_as_float(sv[i]) * g4.x;
-        f[i + 1] = __uint_as_float(sv[i + 1]) * g4.y;
-        f[i + 2] = __uint_as_float(sv[i + 2]) * g4.z;
-        f[i + 3] = __uint_as_float(sv[i + 3]) * g4.w;
-      }
-      tmem_st16(tmem + lane_base + TM_S + 32 * qc, f);
-      tmem_st16(tmem + lane_base + TM_S + 32 * qc + 16, f + 16);
       float z[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) z[i] = 0.f;
       tmem_st16(tmem + lane_base + TM_O + 16 * qc, z);
       tmem_wait_st();
-    }
-    if (tid < kC) {
-      const int nt = (chunk + 1) * kC + tid;
-      beta_next = nt < len ? load_beta(a, t0 + nt, h) : 0.f;
     }
     __syncwarp();
     wait_or_flag(bar_mma, mma_phase & 1, s_abort, a.status);
