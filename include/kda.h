@@ -67,6 +67,7 @@ extern "C" {
 /* ---- bits of the device status word (first 4 bytes of the workspace) ---- */
 #define KDA_DEVICE_BAD_SLOT 1u /* a slot id was outside [0, num_slots); that work item was skipped */
 #define KDA_DEVICE_TIMEOUT 2u  /* a bounded wait inside a kernel gave up (a lost async completion); results are incomplete */
+#define KDA_DEVICE_BAD_COUNT 4u /* an accepted-token count was outside [0, T]; that request was skipped */
 
 /* ---- flags of kda_chunk_prefill ------------------------------------------ */
 #define KDA_LOAD_INITIAL 1  /* S0 of sequence n = state_pool[slot_ids[n]]; else S0 = 0          */
@@ -144,6 +145,27 @@ KDA_API int kda_recurrent_verify(const uint16_t *q, const uint16_t *k, const uin
                          int num_slots, const int32_t *slot_ids, uint16_t *out,
                          int64_t out_token_stride, float *intermediate_states,
                          void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Accept/commit after kda_recurrent_verify.  Source: vLLM PR #55737 "Use
+ * FlashKDA for KDA chunked prefill" (follow-up commit: speculative tokens keep
+ * the recurrent kernel "with num_accepted_tokens rollback"), over the per-step
+ * states of TensorRT-LLM PR #21179's one-launch verify.
+ *
+ * For each request b with n = num_accepted[b] accepted draft tokens, copies
+ * intermediate_states[b, n-1] (all heads) into state_pool[slot_ids[b]]; n = 0
+ * leaves the slot untouched.  Counts outside [0, T] or slots outside
+ * [0, num_slots) skip that request and set a device status bit.
+ *
+ *  state_pool          [num_slots, H, 128, 128] fp32, written
+ *  slot_ids            [B] int32 device, distinct
+ *  num_accepted        [B] int32 device
+ *  intermediate_states [B, T, H, 128, 128] fp32 (as written by kda_recurrent_verify)
+ */
+KDA_API int kda_commit_accepted(float *state_pool, int num_slots, const int32_t *slot_ids,
+                                const int32_t *num_accepted, const float *intermediate_states,
+                                int B, int T, int H, void *workspace, size_t workspace_bytes,
+                                void *stream);
 
 /*
  * kda_recurrent_verify without a workspace.  The pages have no counterpart:

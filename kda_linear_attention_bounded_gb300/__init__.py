@@ -3,11 +3,12 @@
 Two calls, backed by libkda's CUDA kernels (``include/kda.h``):
 
 * :func:`chunk_prefill` -- chunked varlen prefill with a pooled fp32 state;
-* :func:`recurrent_verify` -- speculative-decode verify writing every per-step state.
+* :func:`recurrent_verify` -- speculative-decode verify writing every per-step state;
+* :func:`commit_accepted` -- accept/commit: the state after the last accepted draft token back into the pool.
 
 The binding is loaded on first use and raises if libkda has not been built.
 """
 from ._binding import (  # noqa: F401
-    KDA_DEVICE_BAD_SLOT, KDA_ERR_CUDA, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_WORKSPACE,
-    KDA_FINAL_TO_POOL, KDA_LOAD_INITIAL, KDA_OK, KdaError, chunk_prefill, load, make_workspace,
+    KDA_DEVICE_BAD_COUNT, KDA_DEVICE_BAD_SLOT, KDA_DEVICE_TIMEOUT, KDA_ERR_CUDA, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_WORKSPACE,
+    KDA_FINAL_TO_POOL, KDA_LOAD_INITIAL, KDA_OK, KdaError, chunk_prefill, commit_accepted, load, make_workspace,
     read_device_status, recurrent_verify, status_string, workspace_size)

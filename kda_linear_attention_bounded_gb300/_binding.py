@@ -21,12 +21,14 @@ KDA_ERR_UNSUPPORTED = 2
 KDA_ERR_WORKSPACE = 3
 KDA_ERR_CUDA = 4
 KDA_DEVICE_BAD_SLOT = 1
+KDA_DEVICE_TIMEOUT = 2
+KDA_DEVICE_BAD_COUNT = 4
 KDA_LOAD_INITIAL = 1
 KDA_FINAL_TO_POOL = 2
 
 #: exported symbols of include/kda.h
 EXPORTS = ("kda_status_string", "kda_workspace_size", "kda_workspace_reset", "kda_read_device_status",
-           "kda_chunk_prefill", "kda_recurrent_verify")
+           "kda_chunk_prefill", "kda_recurrent_verify", "kda_commit_accepted", "kda_recurrent_verify_noalloc")
 
 _lib = None
 
@@ -66,6 +68,8 @@ def load():
     lib.kda_recurrent_verify.argtypes = [P, P, P, I64, P, I64, P, I64, P, P, F, F, I, I, I, P, I, P, P, I64,
                                          P, P, SZ, P]
     lib.kda_recurrent_verify.restype = I
+    lib.kda_commit_accepted.argtypes = [P, I, P, P, P, I, I, I, P, SZ, P]
+    lib.kda_commit_accepted.restype = I
     _lib = lib
     return lib
 
@@ -188,3 +192,21 @@ def recurrent_verify(q, k, v, g, beta_logits, A_log, dt_bias, state_pool, slot_i
     if rc != KDA_OK:
         raise KdaError(rc, "kda_recurrent_verify")
     return out, intermediate_states
+
+
+def commit_accepted(state_pool, slot_ids, num_accepted, intermediate_states, *, workspace=None, stream=None):
+    """``kda_commit_accepted``: pool[slot_ids[b]] = intermediate_states[b, num_accepted[b] - 1]."""
+    lib = load()
+    B, T, H = intermediate_states.shape[:3]
+    dev = state_pool.device
+    for name, t, dt in (("slot_ids", slot_ids, torch.int32), ("num_accepted", num_accepted, torch.int32)):
+        if t.dtype != dt or not t.is_cuda or t.numel() != B:
+            raise ValueError(f"{name}: expected a CUDA int32 tensor of {B} entries")
+    if workspace is None:
+        workspace = make_workspace(dev, stream)
+    rc = lib.kda_commit_accepted(_ptr(state_pool), state_pool.shape[0], _ptr(slot_ids), _ptr(num_accepted),
+                                 _ptr(intermediate_states), B, T, H, _ptr(workspace), workspace.numel(),
+                                 _stream_ptr(stream, dev))
+    if rc != KDA_OK:
+        raise KdaError(rc, "kda_commit_accepted")
+    return state_pool

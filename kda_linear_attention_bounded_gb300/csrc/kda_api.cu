@@ -160,4 +160,25 @@ int kda_recurrent_verify(const uint16_t *q, const uint16_t *k, const uint16_t *v
   return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
+int kda_commit_accepted(float *state_pool, int num_slots, const int32_t *slot_ids, const int32_t *num_accepted,
+                        const float *intermediate_states, int B, int T, int H, void *workspace,
+                        size_t workspace_bytes, void *stream) {
+  if (int rc = check_workspace(workspace, workspace_bytes)) return rc;
+  if (B < 0 || T < 1 || T > 64 || H <= 0 || H > 4096) return KDA_ERR_INVALID_ARG;
+  if (B == 0) return KDA_OK;
+  if (!state_pool || !aligned16(state_pool) || num_slots <= 0 || !slot_ids || !num_accepted) return KDA_ERR_INVALID_ARG;
+  if (!intermediate_states || !aligned16(intermediate_states)) return KDA_ERR_INVALID_ARG;
+  kda::CommitArgs a{};
+  a.pool = state_pool;
+  a.num_slots = num_slots;
+  a.slot_ids = slot_ids;
+  a.num_accepted = num_accepted;
+  a.inter = intermediate_states;
+  a.B = B;
+  a.T = T;
+  a.H = H;
+  a.status = static_cast<uint32_t *>(workspace);
+  return kda::launch_commit(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
 }  // extern "C"

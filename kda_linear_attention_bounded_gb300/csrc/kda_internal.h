@@ -48,6 +48,19 @@ struct ChunkArgs {
   uint32_t *status;
 };
 
+// Arguments of the accept/commit copy.
+struct CommitArgs {
+  float *pool;
+  int num_slots;
+  const int32_t *slot_ids;
+  const int32_t *num_accepted;
+  const float *inter;   // [B, T, H, D, D]
+  int B, T, H;
+  uint32_t *status;
+};
+
+cudaError_t launch_commit(const CommitArgs &args, cudaStream_t stream);
+
 // Host-side plan: sequences in the order their CTAs should start (longest
 // first), computed from the host copy of cu_seqlens.
 constexpr int kMaxPlannedSeqs = 2048;

@@ -106,3 +106,15 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(b, "library_path", lambda: str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="not built"):
         b.load()
+
+
+def test_commit_rejects_bad_arguments(lib):
+    c = lambda **kw: lib.kda_commit_accepted(P(kw.get("pool", FAKE)), 4, P(FAKE), P(FAKE), P(kw.get("inter", FAKE)),
+                                             kw.get("B", 2), kw.get("T", 8), 2, P(kw.get("ws", FAKE)), 256, None)
+    assert c(ws=None) == 3
+    assert c(pool=None) == 1
+    assert c(pool=FAKE + 4) == 1
+    assert c(inter=None) == 1
+    assert c(T=0) == 1
+    assert c(T=65) == 1
+    assert c(B=0) == 0
