@@ -159,6 +159,14 @@ __device__ __forceinline__ float2 mul2(float2 a, float2 b) {
       : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
   return d;
 }
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
 __device__ __forceinline__ float2 exp2_2(float2 x) { return make_float2(fast_exp2(x.x), fast_exp2(x.y)); }
 __device__ __forceinline__ uint32_t pack2(float2 v) { return pack_bf16x2(v.x, v.y); }
 
@@ -336,7 +344,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
     {
       const int task = tid >> 2, part = tid & 3;   // norms: 128 (row, q|k) tasks x 4 threads of 32 channels
       const int r = task & 63;
-      float ss = 0.f;
+      float2 ss2 = make_float2(0.f, 0.f);
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int c = 32 * part + 8 * j;
@@ -346,9 +354,10 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prefill_kernel(const __grid
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const float2 f = unpack_bf16x2(ws[e]);
-          ss = fmaf(f.x, f.x, fmaf(f.y, f.y, ss));
+          ss2 = fma2(f, f, ss2);
         }
       }
+      float ss = ss2.x + ss2.y;
       ss += __shfl_xor_sync(0xffffffffu, ss, 1);
       ss += __shfl_xor_sync(0xffffffffu, ss, 2);
       if (part == 0) {
