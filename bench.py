@@ -267,7 +267,7 @@ def run_gpu(args):
     kda.load()
     inp = inputs.prefill_2048x8()
     dev = DevicePrefill(inp, device=device)
-    ws = kda.make_workspace(device)
+    ws = dev.workspace(device)
     stream = torch.cuda.current_stream(device)
     H, T = inp.H, inp.total_tokens
     out = torch.empty((T, H, 128), dtype=torch.bfloat16, device=device)

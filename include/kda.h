@@ -79,6 +79,15 @@ KDA_API const char *kda_status_string(int status);
 /* Bytes of workspace every call needs (a multiple of 256). */
 KDA_API size_t kda_workspace_size(void);
 
+/*
+ * Bytes of workspace kda_chunk_prefill needs for total_tokens tokens in
+ * num_seqs sequences and H heads: kda_workspace_size() plus, for every chunk of
+ * 64 tokens and head, the 74240-byte block the intra-chunk kernel hands to the
+ * state pass (an upper bound: floor(total_tokens / 64) + num_seqs chunks).
+ * Returns 0 for negative sizes or H <= 0.
+ */
+KDA_API size_t kda_prefill_workspace_size(int64_t total_tokens, int num_seqs, int H);
+
 /* Clear the device status word (an async memset on `stream`). */
 KDA_API int kda_workspace_reset(void *workspace, size_t workspace_bytes, void *stream);
 
@@ -112,6 +121,10 @@ KDA_API int kda_read_device_status(const void *workspace, size_t workspace_bytes
  *                   unless KDA_FINAL_TO_POOL (then ignored, may be NULL).
  *  Inputs and outputs must not overlap, except state_pool which may be both
  *  read and written (each sequence reads its slot before writing it).
+ *  workspace        at least kda_prefill_workspace_size(cu_seqlens_host[num_seqs],
+ *                   num_seqs, H) bytes (KDA_ERR_WORKSPACE otherwise); its first
+ *                   word is the device status word, the rest is scratch that
+ *                   the call overwrites.  Concurrent calls need separate workspaces.
  */
 KDA_API int kda_chunk_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                       int64_t qkv_token_stride, const uint16_t *g, int64_t g_token_stride,

@@ -27,8 +27,9 @@ KDA_LOAD_INITIAL = 1
 KDA_FINAL_TO_POOL = 2
 
 #: exported symbols of include/kda.h
-EXPORTS = ("kda_status_string", "kda_workspace_size", "kda_workspace_reset", "kda_read_device_status",
-           "kda_chunk_prefill", "kda_recurrent_verify", "kda_commit_accepted", "kda_recurrent_verify_noalloc")
+EXPORTS = ("kda_status_string", "kda_workspace_size", "kda_prefill_workspace_size", "kda_workspace_reset",
+           "kda_read_device_status", "kda_chunk_prefill", "kda_recurrent_verify", "kda_commit_accepted",
+           "kda_recurrent_verify_noalloc")
 
 _lib = None
 
@@ -58,6 +59,8 @@ def load():
     lib.kda_status_string.restype = ctypes.c_char_p
     lib.kda_workspace_size.argtypes = []
     lib.kda_workspace_size.restype = SZ
+    lib.kda_prefill_workspace_size.argtypes = [I64, I, I]
+    lib.kda_prefill_workspace_size.restype = SZ
     lib.kda_workspace_reset.argtypes = [P, SZ, P]
     lib.kda_workspace_reset.restype = I
     lib.kda_read_device_status.argtypes = [P, SZ, ctypes.POINTER(ctypes.c_uint32), P]
@@ -82,6 +85,11 @@ def workspace_size() -> int:
     return int(load().kda_workspace_size())
 
 
+def prefill_workspace_size(total_tokens: int, num_seqs: int, H: int) -> int:
+    """Bytes of workspace ``chunk_prefill`` needs (status word + one block per chunk and head)."""
+    return int(load().kda_prefill_workspace_size(int(total_tokens), int(num_seqs), int(H)))
+
+
 def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
@@ -92,9 +100,12 @@ def _stream_ptr(stream, device):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
-def make_workspace(device=None, stream=None) -> torch.Tensor:
-    """Allocate (through torch) and clear a workspace for the calls."""
-    ws = torch.empty(workspace_size(), dtype=torch.uint8, device=device or "cuda")
+def make_workspace(device=None, stream=None, nbytes=None) -> torch.Tensor:
+    """Allocate (through torch) and clear a workspace for the calls: at least
+    ``workspace_size()`` bytes, or ``nbytes`` if larger (a prefill needs
+    ``prefill_workspace_size(...)``)."""
+    n = max(workspace_size(), int(nbytes or 0))
+    ws = torch.empty(n, dtype=torch.uint8, device=device or "cuda")
     rc = load().kda_workspace_reset(_ptr(ws), ws.numel(), _stream_ptr(stream, ws.device))
     if rc != KDA_OK:
         raise KdaError(rc, "kda_workspace_reset")
@@ -148,7 +159,7 @@ def chunk_prefill(q, k, v, g, beta_logits, A_log, dt_bias, cu_seqlens, cu_seqlen
     if not final_to_pool and final_state is None:
         final_state = torch.empty((N, H, 128, 128), dtype=torch.float32, device=dev)
     if workspace is None:
-        workspace = make_workspace(dev, stream)
+        workspace = make_workspace(dev, stream, prefill_workspace_size(T_total, N, H))
     flags = (KDA_LOAD_INITIAL if load_initial else 0) | (KDA_FINAL_TO_POOL if final_to_pool else 0)
     if scale is None:
         scale = 1.0 / math.sqrt(128.0)

@@ -7,6 +7,7 @@
 
 #include "kda_common.cuh"
 #include "kda_internal.h"
+#include "kda_prefill_block.h"
 
 namespace {
 
@@ -63,6 +64,11 @@ const char *kda_status_string(int status) {
 
 size_t kda_workspace_size(void) { return kWorkspaceBytes; }
 
+size_t kda_prefill_workspace_size(int64_t total_tokens, int num_seqs, int H) {
+  if (total_tokens < 0 || num_seqs < 0 || H <= 0) return 0;
+  return kda::prefill_workspace_bytes(total_tokens, num_seqs, H);
+}
+
 int kda_workspace_reset(void *workspace, size_t workspace_bytes, void *stream) {
   if (int rc = check_workspace(workspace, workspace_bytes)) return rc;
   return cudaMemsetAsync(workspace, 0, kWorkspaceBytes, static_cast<cudaStream_t>(stream)) == cudaSuccess
@@ -104,6 +110,7 @@ int kda_chunk_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v, i
   if (use_pool && (!state_pool || !slot_ids || num_slots <= 0 || !aligned16(state_pool)))
     return KDA_ERR_INVALID_ARG;
   if (!(flags & KDA_FINAL_TO_POOL) && (!final_state || !aligned16(final_state))) return KDA_ERR_INVALID_ARG;
+  if (workspace_bytes < kda::prefill_workspace_bytes(cu_seqlens_host[num_seqs], num_seqs, H)) return KDA_ERR_WORKSPACE;
 
   kda::ChunkArgs a{};
   a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta_logits;
@@ -120,7 +127,9 @@ int kda_chunk_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v, i
   a.state_out_dense = (flags & KDA_FINAL_TO_POOL) ? nullptr : final_state;
   a.out = out;
   a.status = static_cast<uint32_t *>(workspace);
-  cudaError_t err = kda::launch_chunk_prefill(a, cu_seqlens_host, static_cast<cudaStream_t>(stream));
+  cudaError_t err = kda::launch_chunk_prefill(a, cu_seqlens_host,
+                                              static_cast<uint8_t *>(workspace) + kda::kWorkspaceHeader,
+                                              static_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 

@@ -1,0 +1,574 @@
+// Intra-chunk half of the chunked KDA prefill on sm_103a.
+//
+// One CTA per (chunk of C = 64 tokens, head); every chunk of every sequence is
+// independent here, so the grid covers them all at once, two CTAs per SM.
+// With per-channel log-decays lambda (the bounded gate of vLLM PR #55737 "Use
+// FlashKDA for KDA chunked prefill", PR summary), b_t = sum_{j<=t} lambda_j
+// inside the chunk and k^, q^ the l2-normalised keys / queries, a CTA computes
+// the part of the chunk algebra that does not depend on the state entering the
+// chunk:
+//
+//   A[r,i] = beta_r sum_c k^_rc k^_ic e^(b_rc - b_ic)   (i < r)
+//   P[r,i] = scale  sum_c q^_rc k^_ic e^(b_rc - b_ic)   (i <= r)
+//   T      = (I + A)^-1 Diag(beta)
+//   W = T (k^ o e^b),  U^ = T V,  Q+ = scale q^ o e^b,  K' = k^ o e^(b_63 - b),  e^(b_63)
+//
+// and writes them to the chunk's block of the workspace (kda_prefill_block.h)
+// for the state pass.  This is the token recurrence S_t = (I - beta k^ k^T)
+// Diag(alpha) S_{t-1} + beta k^ v^T unrolled over a chunk: the corrections
+// U = U^ - W S solve (I + A) U = Diag(beta)(V - (k^ o e^b) S).
+//
+// exp(b_r - b_i) spans up to 64 |lower_bound| inside a chunk, far outside
+// fp32.  A and P are built from 16-row sub-blocks R with anchors m_R = b at
+// row 7 of block R:
+//   same block:   e^(b_r - b_i) = e^(b_r - m_R) e^(m_R - b_i)     (|exponents| <= 8 |lb|)
+//   block I < R:  e^(b_r - b_i) = e^(b_r - m_R) e^(m_R - b_i)     (second factor <= 1)
+// so ONE 128 x 160 tcgen05.mma of [F; Q] = [k^; q^] o e^(b - m_R(row)) against
+// [G; B_1; B_2; B_3] (G = k^ o e^(m_R(row) - b); B_R = the rows of blocks < R
+// times e^(m_R - b)) yields every block of A and P that is needed.  T comes
+// from blocked forward substitution (16x16 diagonal inverses on CUDA cores,
+// off-diagonal blocks with TF32 mma.sync), W^T and U^^T from two more
+// tcgen05.mma with M = 128 (lane = key / value channel).
+//
+// Operand tiles are key-channel-major ([channel][token], 128-byte rows): a
+// thread owns two key channels and eight consecutive tokens of each, so every
+// store is one 16-byte chunk; the two channels 2p, 2p + 1 go to rows p and
+// 64 + p ("paired" order, kd_of_rho) so that a warp's stores hit all eight
+// swizzle phases.
+#include <cuda.h>
+
+#include "kda_common.cuh"
+#include "kda_internal.h"
+#include "kda_prefill_block.h"
+#include "kda_sm100.cuh"
+
+namespace kda {
+namespace {
+
+using namespace sm100;
+
+constexpr int kC = kChunk;
+constexpr int kThreads = 256;   // 8 warps; two CTAs per SM
+
+// ---- shared memory map (offsets from a 1024-byte aligned base) ----
+// prologue .. A/P product
+constexpr uint32_t OFF_FQ = 0;        // [F | Q]: 128 rows rho x (64 + 64) tokens, MN-major A operand (32 KB)
+constexpr uint32_t OFF_GB = 32768;    // [G | B_1 | B_2 | B_3]: 128 rows rho x 160 tokens in 3 panels (48 KB)
+constexpr uint32_t OFF_KP = 81920;    // K+^T = (k^ o e^b)^T: 128 rows rho x 64 tokens, K-major A operand (16 KB)
+constexpr uint32_t OFF_QIN = 0, OFF_KIN = 16384, OFF_GIN = 32768;   // TMA tiles, consumed before the operands are written
+// after the A/P product
+constexpr uint32_t OFF_A = 0;         // A (later Inv_RR A_RJ) fp32 [64][68]
+constexpr uint32_t OFF_INV = 17408;   // (I + A)^-1 fp32 [64][68]
+constexpr uint32_t OFF_VIN = 49152;   // v tile (TMA) [token][value channel]
+constexpr uint32_t OFF_T = 65536;     // T bf16 K-major [t][t']
+constexpr uint32_t OFF_PST = 73728;   // P rows of the block's PK tile
+// after the W / U^ products
+constexpr uint32_t OFF_WST = 0, OFF_UST = 16384;   // W^T and U^^T rows of the block
+constexpr uint32_t OFF_SMALL = 98304;
+constexpr uint32_t SM_NQ = 0, SM_NK = 256, SM_BETA = 512, SM_H = 768 /* [2][4][128] f32 */, SM_DTB = 4864,
+                   SM_BAR = 5376, SM_TMEM = 5400, SM_ABORT = 5404, SM_END = 5440;
+constexpr uint32_t kSmemBytes = OFF_SMALL + SM_END + 1024;   // + alignment slack
+static_assert(2 * (kSmemBytes + 1024) <= 233472, "two CTAs per SM");
+constexpr int kAStride = 68;
+constexpr uint32_t kTmemCols = 256;   // A/P product: 160 columns; then W^T 0..63, U^^T 64..127
+
+// first column of B_R inside [G | B_1 | B_2 | B_3] (and of its product in TMEM)
+__host__ __device__ constexpr int gb_col0(int R) { return R == 1 ? 64 : R == 2 ? 80 : 112; }
+constexpr int kGBCols = 160;
+
+__device__ __forceinline__ uint32_t ld_u32(const uint8_t *p) { return *reinterpret_cast<const uint32_t *>(p); }
+
+// Give up a wait after the mbarrier's time limit: record it in the status
+// word and in the CTA's abort flag; later waits of the CTA return at once.
+__device__ __forceinline__ void wait_or_abort(uint64_t *bar, uint32_t parity, volatile uint32_t *abort_flag,
+                                              uint32_t *status) {
+  if (*abort_flag) return;
+  if (!mbar_wait(bar, parity)) {
+    *abort_flag = 1;
+    atomicOr(status, KDA_DEVICE_TIMEOUT);
+  }
+}
+
+// 8 consecutive tokens of the thread's two key channels -> two 16-byte chunks
+__device__ __forceinline__ void put8(uint8_t *tile, int R_rows, int rho, int col0, const float2 (&v)[8]) {
+  const uint4 lo = make_uint4(pack_bf16x2(v[0].x, v[1].x), pack_bf16x2(v[2].x, v[3].x),
+                              pack_bf16x2(v[4].x, v[5].x), pack_bf16x2(v[6].x, v[7].x));
+  const uint4 hi = make_uint4(pack_bf16x2(v[0].y, v[1].y), pack_bf16x2(v[2].y, v[3].y),
+                              pack_bf16x2(v[4].y, v[5].y), pack_bf16x2(v[6].y, v[7].y));
+  *reinterpret_cast<uint4 *>(tile + swz_offset(R_rows, rho, col0)) = lo;
+  *reinterpret_cast<uint4 *>(tile + swz_offset(R_rows, 64 + rho, col0)) = hi;
+}
+
+struct BlockFactors {
+  float2 em;      // e^(m_R)
+  float2 ems;     // scale e^(m_R)
+  float2 el;      // e^(b_63 - m_R)
+  float2 eg;      // e^(a_R - m_R), a_R = b at row 15 of block R
+  float2 cr[4];   // e^(m_R2 - a_R) for R2 > R (both factors of B_R2 stay <= 1)
+};
+
+// Operand rows of 8 tokens (rows t0 .. t0+7 of block R) for key channels
+// (2p, 2p+1); x[j] = (b - m_R) log2(e) of those rows.
+template <int R>
+__device__ __forceinline__ void build_rows(const uint32_t (&kr)[8], const uint32_t (&qr)[8], const float2 (&x)[8],
+                                           int t0, int p, const float *s_nq, const float *s_nk,
+                                           const BlockFactors &f, uint8_t *sm, uint8_t *blk) {
+  float2 kh[8], qh[8], e[8], ie[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const float nk = s_nk[t0 + j], nq = s_nq[t0 + j];
+    kh[j] = mul2(unpack_bf16x2(kr[j]), make_float2(nk, nk));
+    qh[j] = mul2(unpack_bf16x2(qr[j]), make_float2(nq, nq));
+    e[j] = exp2_2(x[j]);
+    ie[j] = exp2_2(make_float2(-x[j].x, -x[j].y));
+  }
+  float2 v[8], w[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) v[j] = mul2(kh[j], e[j]);   // F
+  put8(sm + OFF_FQ, 128, p, t0, v);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) w[j] = mul2(v[j], f.em);    // K+ = F e^(m_R)
+  put8(sm + OFF_KP, 128, p, t0, w);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) v[j] = mul2(qh[j], e[j]);   // Q
+  put8(sm + OFF_FQ, 128, p, 64 + t0, v);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) w[j] = mul2(v[j], f.ems);   // Q+ = scale Q e^(m_R)
+  put8(blk + kBlkWQ, 128, p, 64 + t0, w);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) v[j] = mul2(kh[j], ie[j]);  // G
+  put8(sm + OFF_GB, 128, p, t0, v);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) w[j] = mul2(v[j], f.el);    // K' = G e^(b_63 - m_R)
+  put8(blk + kBlkPK, kBlkPKRows, 64 + p, t0, w);
+  if (R < 3) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = mul2(v[j], f.eg);  // k^ e^(a_R - b) <= |k^|
+#pragma unroll
+    for (int R2 = R + 1; R2 < 4; ++R2) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) w[j] = mul2(v[j], f.cr[R2]);
+      put8(sm + OFF_GB, 128, p, gb_col0(R2) + t0, w);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_constant__ IntraParams prm) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t *small = sm + OFF_SMALL;
+  float *s_nq = reinterpret_cast<float *>(small + SM_NQ);
+  float *s_nk = reinterpret_cast<float *>(small + SM_NK);
+  float *s_beta = reinterpret_cast<float *>(small + SM_BETA);
+  float *s_h = reinterpret_cast<float *>(small + SM_H);     // [half][block][channel]: sum of lambda over 8 rows
+  float *s_dtb = reinterpret_cast<float *>(small + SM_DTB);
+  uint64_t *bar_in = reinterpret_cast<uint64_t *>(small + SM_BAR);
+  uint64_t *bar_v = bar_in + 1;
+  uint64_t *bar_mma = bar_in + 2;
+  uint32_t *s_tmem = reinterpret_cast<uint32_t *>(small + SM_TMEM);
+  volatile uint32_t *s_abort = reinterpret_cast<volatile uint32_t *>(small + SM_ABORT);
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int H = prm.H;
+  const int h = blockIdx.x % H;
+  const int gslot = blockIdx.x / H;
+  // sequence of this chunk slot: the last n with chunk_off[n] <= gslot (never an empty sequence)
+  int n = 0;
+  {
+    int lo = 0, hi = prm.num_seqs - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (prm.chunk_off[mid] <= gslot) lo = mid;
+      else hi = mid - 1;
+    }
+    n = lo;
+  }
+  const int tok0 = prm.tok_off[n] + (gslot - prm.chunk_off[n]) * kC;
+  const int valid = min(kC, prm.tok_off[n + 1] - tok0);
+  uint8_t *blk = prm.blocks + (static_cast<size_t>(gslot) * H + h) * kBlkBytes;
+  if (*reinterpret_cast<volatile uint32_t *>(prm.status) & KDA_DEVICE_TIMEOUT) return;   // an earlier CTA gave up
+
+  if (tid == 0) {
+    mbar_init(bar_in, 1);
+    mbar_init(bar_v, 1);
+    mbar_init(bar_mma, 1);
+    *s_abort = 0;
+    fence_mbar_init();
+    mbar_arrive_expect_tx(bar_in, 3 * 16384);
+    tma_load_3d(sm + OFF_QIN, &prm.tq, 0, h, tok0, bar_in);
+    tma_load_3d(sm + OFF_QIN + 8192, &prm.tq, 64, h, tok0, bar_in);
+    tma_load_3d(sm + OFF_KIN, &prm.tk, 0, h, tok0, bar_in);
+    tma_load_3d(sm + OFF_KIN + 8192, &prm.tk, 64, h, tok0, bar_in);
+    tma_load_3d(sm + OFF_GIN, &prm.tg, 0, h, tok0, bar_in);
+    tma_load_3d(sm + OFF_GIN + 8192, &prm.tg, 64, h, tok0, bar_in);
+  }
+  if (warp == 0) {
+    tmem_alloc(s_tmem, kTmemCols);
+    tmem_relinquish();
+  }
+  if (tid < kD) s_dtb[tid] = prm.dt_bias[h * kD + tid];
+  if (tid >= 128 && tid < 128 + kC) {
+    const int r = tid - 128;
+    s_beta[r] = r < valid ? sigmoid_f(bf16_bits_to_f32(prm.beta[(size_t)(tok0 + r) * prm.beta_stride + h])) : 0.f;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+  wait_or_abort(bar_in, 0, s_abort, prm.status);
+
+  // ------------------------------------------------------------ l2 norms (token-major)
+  {
+    const int r = tid >> 2, part = tid & 3;
+    float2 sq = make_float2(0.f, 0.f), sk = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int c = 32 * part + 8 * j;
+      const uint4 wq = *reinterpret_cast<const uint4 *>(sm + OFF_QIN + swz_offset(64, r, c));
+      const uint4 wk = *reinterpret_cast<const uint4 *>(sm + OFF_KIN + swz_offset(64, r, c));
+      const uint32_t aq[4] = {wq.x, wq.y, wq.z, wq.w}, ak[4] = {wk.x, wk.y, wk.z, wk.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 fq = unpack_bf16x2(aq[e]), fk = unpack_bf16x2(ak[e]);
+        sq = fma2(fq, fq, sq);
+        sk = fma2(fk, fk, sk);
+      }
+    }
+    float ssq = sq.x + sq.y, ssk = sk.x + sk.y;
+    ssq += __shfl_xor_sync(0xffffffffu, ssq, 1);
+    ssk += __shfl_xor_sync(0xffffffffu, ssk, 1);
+    ssq += __shfl_xor_sync(0xffffffffu, ssq, 2);
+    ssk += __shfl_xor_sync(0xffffffffu, ssk, 2);
+    if (part == 0) {
+      s_nq[r] = r < valid ? rsqrtf(ssq + kL2Eps) : 0.f;
+      s_nk[r] = r < valid ? rsqrtf(ssk + kL2Eps) : 0.f;
+    }
+  }
+
+  // ------------------------------------------------------------ gate and in-block decays
+  // thread = (channel pair p, 8-row half `hf` of the blocks Ra and Rb = 3 - Ra); warp-uniform blocks
+  const int p = tid & 63, sel = tid >> 6;
+  const int hf = sel & 1, Ra = sel >> 1, Rb = 3 - Ra;
+  const int c0 = 2 * p;
+  const float nea = -__expf(prm.A_log[h]) * kLog2e;   // lambda = lb sigmoid(ea (g + dtb)); log2 units below
+  const float lb2 = prm.lower_bound * kLog2e;
+  const float2 nd = make_float2(nea * s_dtb[c0], nea * s_dtb[c0 + 1]);
+  uint32_t kr[2][8], qr[2][8];
+  float2 x[2][8];   // (b_t - m_R) log2(e), rows t0 .. t0+7 of each of the two blocks
+#pragma unroll
+  for (int bi = 0; bi < 2; ++bi) {
+    const int R = bi ? Rb : Ra;
+    const int t0 = 16 * R + 8 * hf;
+    float2 lam[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int r = t0 + j;
+      const uint32_t off = swz_offset(64, r, c0);
+      kr[bi][j] = ld_u32(sm + OFF_KIN + off);
+      qr[bi][j] = ld_u32(sm + OFF_QIN + off);
+      const float2 gg = unpack_bf16x2(ld_u32(sm + OFF_GIN + off));
+      // lambda = lb2 / (1 + 2^(nea g + nea dtb))
+      const float l0 = lb2 * fast_rcp(1.f + fast_exp2(fmaf(nea, gg.x, nd.x)));
+      const float l1 = lb2 * fast_rcp(1.f + fast_exp2(fmaf(nea, gg.y, nd.y)));
+      lam[j] = r < valid ? make_float2(l0, l1) : make_float2(0.f, 0.f);
+    }
+    float2 hs;
+    if (hf == 0) {   // rows 0..7: b_t - m_R = -(lambda_{t+1} + ... + lambda_7)
+      x[bi][7] = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int j = 6; j >= 0; --j) x[bi][j] = make_float2(x[bi][j + 1].x - lam[j + 1].x, x[bi][j + 1].y - lam[j + 1].y);
+      hs = make_float2(lam[0].x - x[bi][0].x, lam[0].y - x[bi][0].y);
+    } else {         // rows 8..15: b_t - m_R = lambda_8 + ... + lambda_t
+      float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        acc = make_float2(acc.x + lam[j].x, acc.y + lam[j].y);
+        x[bi][j] = acc;
+      }
+      hs = acc;
+    }
+    *reinterpret_cast<float2 *>(s_h + (hf * 4 + R) * kD + c0) = hs;
+  }
+  __syncthreads();   // norms, half sums visible; q, k, g tiles fully read
+
+  // ------------------------------------------------------------ anchors and operand tiles
+  {
+    float2 hh[2][4];
+#pragma unroll
+    for (int I = 0; I < 4; ++I) {
+      hh[0][I] = *reinterpret_cast<const float2 *>(s_h + I * kD + c0);
+      hh[1][I] = *reinterpret_cast<const float2 *>(s_h + (4 + I) * kD + c0);
+    }
+    float2 m[4], a[4], tot = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int I = 0; I < 4; ++I) {
+      m[I] = make_float2(tot.x + hh[0][I].x, tot.y + hh[0][I].y);
+      a[I] = make_float2(m[I].x + hh[1][I].x, m[I].y + hh[1][I].y);
+      tot = a[I];
+    }
+    if (sel == 0) {   // gamma = e^(b_63) for rho = p and 64 + p
+      float *gam = reinterpret_cast<float *>(blk + kBlkGamma);
+      gam[p] = fast_exp2(tot.x);
+      gam[64 + p] = fast_exp2(tot.y);
+    }
+    auto factors = [&](int R) {
+      BlockFactors f;
+      f.em = exp2_2(m[R]);
+      f.ems = make_float2(f.em.x * prm.scale, f.em.y * prm.scale);
+      f.el = exp2_2(make_float2(tot.x - m[R].x, tot.y - m[R].y));
+      f.eg = exp2_2(hh[1][R]);
+#pragma unroll
+      for (int R2 = 0; R2 < 4; ++R2)
+        f.cr[R2] = R2 > R ? exp2_2(make_float2(fminf(m[R2].x - a[R].x, 0.f), fminf(m[R2].y - a[R].y, 0.f)))
+                          : make_float2(0.f, 0.f);
+      return f;
+    };
+    const BlockFactors fa = factors(Ra), fb = factors(Rb);
+    if (Ra == 0) {
+      build_rows<0>(kr[0], qr[0], x[0], 8 * hf, p, s_nq, s_nk, fa, sm, blk);
+      build_rows<3>(kr[1], qr[1], x[1], 48 + 8 * hf, p, s_nq, s_nk, fb, sm, blk);
+    } else {
+      build_rows<1>(kr[0], qr[0], x[0], 16 + 8 * hf, p, s_nq, s_nk, fa, sm, blk);
+      build_rows<2>(kr[1], qr[1], x[1], 32 + 8 * hf, p, s_nq, s_nk, fb, sm, blk);
+    }
+  }
+  fence_async_smem();
+  tc_fence_before();
+  __syncthreads();
+
+  // ------------------------------------------------------------ A/P product (one 128 x 160 tcgen05.mma)
+  if (tid == 0) {
+    tc_fence_after();
+    const uint32_t fq = smem_u32(sm + OFF_FQ), gb = smem_u32(sm + OFF_GB);
+    const uint32_t id = idesc_bf16(128, kGBCols, true, true);
+#pragma unroll
+    for (int s = 0; s < 8; ++s) mma_bf16(tmem, desc_mnmajor(fq, 128, s), desc_mnmajor(gb, 128, s), id, s > 0);
+    mma_commit(bar_mma);
+  }
+  __syncwarp();
+  wait_or_abort(bar_mma, 0, s_abort, prm.status);
+  tc_fence_after();
+  if (tid == 0) {   // the operand tiles are free: v may land
+    mbar_arrive_expect_tx(bar_v, 16384);
+    tma_load_3d(sm + OFF_VIN, &prm.tv, 0, h, tok0, bar_v);
+    tma_load_3d(sm + OFF_VIN + 8192, &prm.tv, 64, h, tok0, bar_v);
+  }
+
+  // ------------------------------------------------------------ A (fp32) and P (bf16 block rows) from TMEM
+  {
+    // lanes 0..63 of the product hold rows of A (k side), lanes 64..127 rows of P (q side)
+    const int q4 = warp & 3, ib = warp >> 2;
+    const bool is_p = q4 >= 2;
+    const int r = (q4 & 1) * 32 + lane;
+    const int Ra2 = (q4 & 1) * 2;              // row blocks of this warp: Ra2 (lanes 0..15), Ra2 + 1
+    const bool upper = (r >> 4) != Ra2;
+    const uint32_t lane_base = static_cast<uint32_t>(q4 * 32) << 16;
+    const float bscale = is_p ? prm.scale : s_beta[r];
+    float *sA = reinterpret_cast<float *>(sm + OFF_A);
+#pragma unroll
+    for (int ii = 0; ii < 2; ++ii) {
+      const int I = 2 * ib + ii;   // column block
+      const int srcA = (I == Ra2) ? 16 * I : (I < Ra2) ? gb_col0(Ra2) + 16 * I : -1;
+      const int srcB = (I == Ra2 + 1) ? 16 * I : (I < Ra2 + 1) ? gb_col0(Ra2 + 1) + 16 * I : -1;
+      uint32_t va[16], vb[16];
+      if (srcA >= 0) tmem_ld16_async(tmem + lane_base + srcA, va);
+      if (srcB >= 0) tmem_ld16_async(tmem + lane_base + srcB, vb);
+      tmem_wait_ld();
+      tmem_tie<16>(va);
+      tmem_tie<16>(vb);
+      const int src = upper ? srcB : srcA;
+      float v[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const int i = 16 * I + e;
+        const float raw = __uint_as_float(upper ? vb[e] : va[e]);
+        const bool keep = (src >= 0) && (is_p ? (i <= r) : (i < r));
+        v[e] = keep ? raw * bscale : 0.f;
+      }
+      if (is_p) {
+#pragma unroll
+        for (int k8 = 0; k8 < 2; ++k8)
+          *reinterpret_cast<uint4 *>(sm + OFF_PST + swz_offset(64, r, 16 * I + 8 * k8)) =
+              make_uint4(pack_bf16x2(v[8 * k8], v[8 * k8 + 1]), pack_bf16x2(v[8 * k8 + 2], v[8 * k8 + 3]),
+                         pack_bf16x2(v[8 * k8 + 4], v[8 * k8 + 5]), pack_bf16x2(v[8 * k8 + 6], v[8 * k8 + 7]));
+      } else {
+#pragma unroll
+        for (int e = 0; e < 16; e += 4)
+          *reinterpret_cast<float4 *>(sA + r * kAStride + 16 * I + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+
+  // ------------------------------------------------------------ T = (I + A)^-1 Diag(beta)
+  {
+    float *sA = reinterpret_cast<float *>(sm + OFF_A);
+    float *sInv = reinterpret_cast<float *>(sm + OFF_INV);
+    uint16_t *sT16 = reinterpret_cast<uint16_t *>(sm + OFF_T);
+    // diagonal 16x16 blocks (warp R, lane = column): forward substitution; their part of T goes
+    // straight to the bf16 tile.  Warps 4..7 clear the strictly-upper blocks of T.
+    if (warp < 4) {
+      if (lane < 16) {
+        const int R = warp, jc = lane;
+        const float bj = s_beta[16 * R + jc];
+        float xs[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+          float lrow[16];
+#pragma unroll
+          for (int k4 = 0; k4 < 4; ++k4) {
+            const float4 l4 = *reinterpret_cast<const float4 *>(sA + (16 * R + r) * kAStride + 16 * R + 4 * k4);
+            lrow[4 * k4] = l4.x; lrow[4 * k4 + 1] = l4.y; lrow[4 * k4 + 2] = l4.z; lrow[4 * k4 + 3] = l4.w;
+          }
+          float v0 = (r == jc) ? 1.f : 0.f, v1 = 0.f;
+#pragma unroll
+          for (int mm = 0; mm < r; ++mm) {
+            if (mm & 1) v1 = fmaf(-lrow[mm], xs[mm], v1);
+            else v0 = fmaf(-lrow[mm], xs[mm], v0);
+          }
+          xs[r] = v0 + v1;
+        }
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+          sInv[(16 * R + r) * kAStride + 16 * R + jc] = xs[r];
+          sT16[swz_offset(64, 16 * R + r, 16 * R + jc) >> 1] = f32_to_bf16_bits(r >= jc ? xs[r] * bj : 0.f);
+        }
+      }
+    } else {
+      for (int idx = tid - 128; idx < 6 * 32; idx += kThreads - 128) {
+        const int bk = idx >> 5, e = idx & 31;
+        const int R = bk < 3 ? 0 : bk < 5 ? 1 : 2;
+        const int I = bk < 3 ? bk + 1 : bk < 5 ? bk - 1 : 3;
+        *reinterpret_cast<uint4 *>(sm + OFF_T + swz_offset(64, 16 * R + (e >> 1), 16 * I + 8 * (e & 1))) =
+            make_uint4(0, 0, 0, 0);
+      }
+    }
+    __syncthreads();
+    // off-diagonal blocks: with L~_RJ = Inv_RR A_RJ (J < R, in place over A),
+    //   Inv_RI = - sum_{J=I}^{R-1} L~_RJ Inv_JI
+    const int g8 = lane >> 2, t4 = lane & 3;
+    for (int task = warp; task < 12; task += 8) {   // 6 block pairs x 2 column halves
+      const int pr = task >> 1;                     // (R, J): (1,0) (2,0) (2,1) (3,0) (3,1) (3,2)
+      const int R = pr < 1 ? 1 : pr < 3 ? 2 : 3;
+      const int J = pr - (R * (R - 1)) / 2;
+      const int n0 = 16 * J + 8 * (task & 1);
+      float y[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int ks = 0; ks < 2; ++ks) {
+        const float *ar = sInv + (16 * R + g8) * kAStride + 16 * R + 8 * ks + t4;
+        const float *br = sA + (16 * R + 8 * ks + t4) * kAStride + n0 + g8;
+        mma_1688_tf32(y, to_tf32(ar[0]), to_tf32(ar[8 * kAStride]), to_tf32(ar[4]), to_tf32(ar[8 * kAStride + 4]),
+                      to_tf32(br[0]), to_tf32(br[4 * kAStride]));
+      }
+      __syncwarp();
+      *reinterpret_cast<float2 *>(sA + (16 * R + g8) * kAStride + n0 + 2 * t4) = make_float2(y[0], y[1]);
+      *reinterpret_cast<float2 *>(sA + (16 * R + g8 + 8) * kAStride + n0 + 2 * t4) = make_float2(y[2], y[3]);
+    }
+    __syncthreads();
+    // column walks: warp = (column block I in 0..2, half); each reads only its own earlier results
+    if (warp < 6) {
+      const int I = warp >> 1;
+      const int n0 = 16 * I + 8 * (warp & 1);
+      const float2 bcol = *reinterpret_cast<const float2 *>(s_beta + n0 + 2 * t4);
+      for (int R = I + 1; R < 4; ++R) {
+        float xs[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int J = I; J < R; ++J) {
+#pragma unroll
+          for (int ks = 0; ks < 2; ++ks) {
+            const int kc = 16 * J + 8 * ks;
+            const float *ar = sA + (16 * R + g8) * kAStride + kc + t4;
+            const float *br = sInv + (kc + t4) * kAStride + n0 + g8;
+            mma_1688_tf32(xs, to_tf32(ar[0]), to_tf32(ar[8 * kAStride]), to_tf32(ar[4]),
+                          to_tf32(ar[8 * kAStride + 4]), to_tf32(br[0]), to_tf32(br[4 * kAStride]));
+          }
+        }
+        *reinterpret_cast<float2 *>(sInv + (16 * R + g8) * kAStride + n0 + 2 * t4) = make_float2(-xs[0], -xs[1]);
+        *reinterpret_cast<float2 *>(sInv + (16 * R + g8 + 8) * kAStride + n0 + 2 * t4) = make_float2(-xs[2], -xs[3]);
+        *reinterpret_cast<uint32_t *>(sm + OFF_T + swz_offset(64, 16 * R + g8, n0 + 2 * t4)) =
+            pack_bf16x2(-xs[0] * bcol.x, -xs[1] * bcol.y);
+        *reinterpret_cast<uint32_t *>(sm + OFF_T + swz_offset(64, 16 * R + g8 + 8, n0 + 2 * t4)) =
+            pack_bf16x2(-xs[2] * bcol.x, -xs[3] * bcol.y);
+        __syncwarp();
+      }
+    }
+  }
+  fence_async_smem();
+  tc_fence_before();
+  __syncthreads();
+
+  // ------------------------------------------------------------ W^T = K+^T T^T, U^^T = V^T T^T
+  wait_or_abort(bar_v, 0, s_abort, prm.status);
+  if (valid < kC) {   // rows past the sequence end: T's columns there are 0, but v may hold anything
+    for (int idx = tid; idx < (kC - valid) * 16; idx += kThreads) {
+      const int r2 = valid + idx / 16, cc = idx % 16;
+      *reinterpret_cast<uint4 *>(sm + OFF_VIN + swz_offset(64, r2, 8 * cc)) = make_uint4(0, 0, 0, 0);
+    }
+    fence_async_smem();
+    __syncthreads();
+  }
+  if (tid == 0) {
+    tc_fence_after();
+    const uint32_t id_w = idesc_bf16(128, 64, false, false);
+    const uint32_t id_u = idesc_bf16(128, 64, true, false);
+    const uint32_t kp = smem_u32(sm + OFF_KP), vv = smem_u32(sm + OFF_VIN), tt = smem_u32(sm + OFF_T);
+#pragma unroll
+    for (int s = 0; s < 4; ++s) mma_bf16(tmem, desc_kmajor(kp, 128, s), desc_kmajor(tt, 64, s), id_w, s > 0);
+#pragma unroll
+    for (int s = 0; s < 4; ++s) mma_bf16(tmem + 64, desc_mnmajor(vv, 64, s), desc_kmajor(tt, 64, s), id_u, s > 0);
+    mma_commit(bar_mma);
+  }
+  __syncwarp();
+  wait_or_abort(bar_mma, 1, s_abort, prm.status);
+  tc_fence_after();
+  {
+    // warp = (lane quadrant, W^T | U^^T); the thread's row is one 128-byte line of the block tile
+    const int q4 = warp & 3, which = warp >> 2;
+    const int row = q4 * 32 + lane;
+    const uint32_t taddr = tmem + (static_cast<uint32_t>(q4 * 32) << 16) + (which ? 64u : 0u);
+    uint32_t v[64];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) tmem_ld16_async(taddr + 16 * k, v + 16 * k);
+    tmem_wait_ld();
+    tmem_tie<64>(v);
+    uint8_t *dst = sm + (which ? OFF_UST : OFF_WST);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const float *f = reinterpret_cast<const float *>(v + 8 * k);
+      *reinterpret_cast<uint4 *>(dst + swz_offset(128, row, 8 * k)) =
+          make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                     pack_bf16x2(f[6], f[7]));
+    }
+  }
+  fence_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  if (tid == 0) {
+    bulk_store(blk + kBlkWQ, sm + OFF_WST, 16384);
+    bulk_store(blk + kBlkUH, sm + OFF_UST, 16384);
+    bulk_store(blk + kBlkPK, sm + OFF_PST, 8192);
+    bulk_commit();
+    bulk_wait_all();
+  }
+  if (warp == 0) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_chunk_intra(const IntraParams &p, int num_chunks, cudaStream_t stream) {
+  if (num_chunks <= 0) return cudaSuccess;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(chunk_intra_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  chunk_intra_kernel<<<num_chunks * p.H, kThreads, kSmemBytes, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace kda

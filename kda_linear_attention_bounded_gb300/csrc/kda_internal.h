@@ -1,6 +1,7 @@
 // Internal launch interface between the C ABI (kda_api.cu) and the kernels.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -61,11 +62,48 @@ struct CommitArgs {
 
 cudaError_t launch_commit(const CommitArgs &args, cudaStream_t stream);
 
-// Host-side plan: sequences in the order their CTAs should start (longest
-// first), computed from the host copy of cu_seqlens.
-constexpr int kMaxPlannedSeqs = 2048;
+// Sequences planned per launch pair of the chunked prefill (longer batches
+// are split on the host into consecutive groups).
+constexpr int kMaxSeqsPerLaunch = 1024;
 
-cudaError_t launch_chunk_prefill(const ChunkArgs &args, const int32_t *cu_seqlens_host,
+// Intra-chunk kernel: one CTA per (chunk slot, head) of a group of sequences.
+struct IntraParams {
+  CUtensorMap tq, tk, tv, tg;   // [tokens, H, 128] bf16, box 64 channels x 1 head x 64 tokens
+  const uint16_t *beta;
+  int64_t beta_stride;
+  const float *A_log, *dt_bias;
+  float lower_bound, scale;
+  int H, num_seqs;
+  uint8_t *blocks;              // block (chunk slot g, head h) at blocks + (g H + h) kBlkBytes
+  uint32_t *status;
+  int32_t chunk_off[kMaxSeqsPerLaunch + 1];   // first chunk slot of each sequence of the group
+  int32_t tok_off[kMaxSeqsPerLaunch + 1];     // first token of each sequence of the group
+};
+
+// State pass: one CTA per (sequence, head) of a group.
+struct ChainParams {
+  const uint8_t *blocks;
+  const int32_t *slot_ids;      // indexed by seq0 + local sequence
+  int num_slots;
+  const float *state_in;
+  float *state_out_pool;
+  float *state_out_dense;       // indexed by seq0 + local sequence
+  uint16_t *out;
+  int64_t out_stride;
+  uint32_t *status;
+  int H, num_seqs, seq0;
+  int32_t chunk_off[kMaxSeqsPerLaunch + 1];
+  int32_t tok_off[kMaxSeqsPerLaunch + 1];
+  uint16_t order[kMaxSeqsPerLaunch];          // local sequences, longest first
+};
+
+cudaError_t launch_chunk_intra(const IntraParams &p, int num_chunks, cudaStream_t stream);
+cudaError_t launch_chunk_chain(const ChainParams &p, cudaStream_t stream);
+
+// Bytes of workspace kda_chunk_prefill needs (status header + one block per chunk and head).
+size_t prefill_workspace_bytes(int64_t total_tokens, int num_seqs, int H);
+
+cudaError_t launch_chunk_prefill(const ChunkArgs &args, const int32_t *cu_seqlens_host, uint8_t *blocks,
                                  cudaStream_t stream);
 
 }  // namespace kda

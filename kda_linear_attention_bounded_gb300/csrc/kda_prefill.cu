@@ -1,0 +1,126 @@
+// Host planning of the chunked prefill: chunk slots per sequence, TMA tensor
+// maps, and the two launches (intra-chunk kernel over every chunk and head,
+// then the state pass over every sequence and head, longest sequences first).
+// Everything is computed from the host copy of cu_seqlens; nothing here reads
+// device memory or synchronises.
+#include <cuda.h>
+
+#include <algorithm>
+#include <mutex>
+#include <numeric>
+#include <vector>
+
+#include "kda_common.cuh"
+#include "kda_internal.h"
+#include "kda_prefill_block.h"
+
+namespace kda {
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// [tokens, H, 128] bf16 with the given token stride; box = 64 channels x 1 head x 64 tokens,
+// 128-byte swizzle (the row-swizzled tile layout); rows past the tensor's end read as zero
+bool make_token_map(CUtensorMap *map, const void *base, int H, int total_tokens, int64_t token_stride) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(H),
+                        static_cast<cuuint64_t>(std::max(total_tokens, 1))};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(kD * 2), static_cast<cuuint64_t>(token_stride * 2)};
+  cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(kChunk)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+size_t prefill_workspace_bytes(int64_t total_tokens, int num_seqs, int H) {
+  // sum_n ceil(len_n / 64) <= floor(total / 64) + num_seqs
+  const size_t chunks = static_cast<size_t>(std::max<int64_t>(total_tokens, 0) / kChunk) +
+                        static_cast<size_t>(std::max(num_seqs, 0));
+  return kWorkspaceHeader + chunks * static_cast<size_t>(std::max(H, 0)) * kBlkBytes;
+}
+
+cudaError_t launch_chunk_prefill(const ChunkArgs &a, const int32_t *cu_host, uint8_t *blocks, cudaStream_t stream) {
+  if (a.num_seqs <= 0) return cudaSuccess;
+  // host-side staging of the (large) kernel parameter structs; copied at launch
+  static IntraParams *ip = nullptr;
+  static ChainParams *cp = nullptr;
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ip) {
+    ip = new IntraParams();
+    cp = new ChainParams();
+  }
+  if (!make_token_map(&ip->tq, a.q, a.H, a.total_tokens, a.qkv_stride) ||
+      !make_token_map(&ip->tk, a.k, a.H, a.total_tokens, a.qkv_stride) ||
+      !make_token_map(&ip->tv, a.v, a.H, a.total_tokens, a.qkv_stride) ||
+      !make_token_map(&ip->tg, a.g, a.H, a.total_tokens, a.g_stride))
+    return cudaErrorInvalidValue;
+  ip->beta = a.beta;
+  ip->beta_stride = a.beta_stride;
+  ip->A_log = a.A_log;
+  ip->dt_bias = a.dt_bias;
+  ip->lower_bound = a.lower_bound;
+  ip->scale = a.scale;
+  ip->H = a.H;
+  ip->blocks = blocks;
+  ip->status = a.status;
+  cp->blocks = blocks;
+  cp->slot_ids = a.slot_ids;
+  cp->num_slots = a.num_slots;
+  cp->state_in = a.state_in;
+  cp->state_out_pool = a.state_out_pool;
+  cp->state_out_dense = a.state_out_dense;
+  cp->out = a.out;
+  cp->out_stride = a.out_stride;
+  cp->status = a.status;
+  cp->H = a.H;
+
+  std::vector<int> idx;
+  for (int s0 = 0; s0 < a.num_seqs; s0 += kMaxSeqsPerLaunch) {
+    const int ns = std::min(kMaxSeqsPerLaunch, a.num_seqs - s0);
+    int chunks = 0;
+    for (int i = 0; i < ns; ++i) {
+      const int len = cu_host[s0 + i + 1] - cu_host[s0 + i];
+      ip->chunk_off[i] = cp->chunk_off[i] = chunks;
+      ip->tok_off[i] = cp->tok_off[i] = cu_host[s0 + i];
+      chunks += (len + kChunk - 1) / kChunk;
+    }
+    ip->chunk_off[ns] = cp->chunk_off[ns] = chunks;
+    ip->tok_off[ns] = cp->tok_off[ns] = cu_host[s0 + ns];
+    ip->num_seqs = ns;
+    cp->num_seqs = ns;
+    cp->seq0 = s0;
+    idx.resize(ns);
+    std::iota(idx.begin(), idx.end(), 0);
+    std::stable_sort(idx.begin(), idx.end(), [&](int x, int y) {
+      return cp->chunk_off[x + 1] - cp->chunk_off[x] > cp->chunk_off[y + 1] - cp->chunk_off[y];
+    });
+    for (int i = 0; i < ns; ++i) cp->order[i] = static_cast<uint16_t>(idx[i]);
+    cudaError_t e = launch_chunk_intra(*ip, chunks, stream);
+    if (e != cudaSuccess) return e;
+    e = launch_chunk_chain(*cp, stream);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace kda

@@ -76,6 +76,10 @@ class DevicePrefill:
         self.pool = f32_dev(inp.pool, device) if inp.pool is not None else None
         self.slots = i32_dev(inp.slot_ids, device) if inp.slot_ids is not None else None
 
+    def workspace(self, device="cuda"):
+        inp = self.inp
+        return kda.make_workspace(device, nbytes=kda.prefill_workspace_size(inp.total_tokens, inp.num_seqs, inp.H))
+
     def run(self, **kw):
         inp = self.inp
         return kda.chunk_prefill(self.q, self.k, self.v, self.g, self.beta, self.A_log, self.dt_bias, self.cu,

@@ -87,6 +87,21 @@ def test_prefill_rejects_bad_arguments(lib):
     assert _prefill(lib, flags=8) == 1                 # unknown flag
     assert _prefill(lib, H=0) == 1
     assert _prefill(lib, cu=(0,)) == 0                 # no sequences: nothing to do
+    # valid arguments but a workspace without room for the chunk blocks
+    need = lib.kda_prefill_workspace_size(4, 1, 2)
+    assert _prefill(lib, ws_bytes=need - 256) == 3
+
+
+def test_prefill_workspace_size(lib):
+    lib.kda_prefill_workspace_size.restype = ctypes.c_size_t
+    lib.kda_prefill_workspace_size.argtypes = [ctypes.c_int64, ctypes.c_int, ctypes.c_int]
+    block = 74240
+    # header + (floor(T / 64) + num_seqs) chunks x H blocks: an upper bound of sum ceil(len / 64)
+    assert lib.kda_prefill_workspace_size(2048 * 8, 8, 16) == 1024 + (256 + 8) * 16 * block
+    assert lib.kda_prefill_workspace_size(0, 3, 2) == 1024 + 3 * 2 * block
+    assert lib.kda_prefill_workspace_size(130, 1, 1) == 1024 + 3 * block
+    assert lib.kda_prefill_workspace_size(-1, 1, 1) == 0
+    assert lib.kda_prefill_workspace_size(10, 1, 0) == 0
 
 
 def test_verify_rejects_bad_arguments(lib):

@@ -14,7 +14,7 @@ pytestmark = pytest.mark.gpu
 def _parity(inp, token_pad=0, heads=None):
     dev = DevicePrefill(inp, token_pad=token_pad)
     pool_before = dev.pool.clone() if dev.pool is not None else None
-    ws = kda.make_workspace()
+    ws = dev.workspace()
     out, final = dev.run(workspace=ws)
     torch.cuda.synchronize()
     assert kda.read_device_status(ws) == 0
@@ -67,7 +67,7 @@ def test_bad_slot_sets_status_and_skips():
     inp = inputs.prefill_inputs("badslot", [70, 50], 2, seed=51, pool_slots=4, load_initial=True)
     dev = DevicePrefill(inp)
     dev.slots[1] = 99
-    ws = kda.make_workspace()
+    ws = dev.workspace()
     out = torch.full((inp.total_tokens, 2, 128), 7.0, dtype=torch.bfloat16, device="cuda")
     out, final = dev.run(workspace=ws, out=out)
     torch.cuda.synchronize()
