@@ -9,16 +9,20 @@
 //   O  = Q+ S + P U                     (scale already inside Q+ and P)
 //   S' = Diag(e^(b_63)) S + K'^T U
 //
-// All three products run transposed so that TMEM lane = value channel and M =
-// 128: [U^T | O^T] = S^T [W | Q+]^T (N = 64 + 64) and [O^T | S'^T] += U^T [P ;
-// K'^T]^T (N = 64 + 128).  The state's key channels are kept in the blocks'
-// paired order rho; the caller's layout is used only to read S0 and to write
-// the final state.
+// All products run transposed so that TMEM lane = value channel and M = 128:
+// [U^T | O^T] = S^T [W | Q+]^T (N = 128), S'^T += U^T K' (N = 128) and
+// O^T += U^T P^T (N = 64).  Their A operands S^T and U^T are bf16 copies kept
+// in TMEM (tcgen05.mma with A in tensor memory); only the chunk's block comes
+// from shared memory.  The state's key channels stay in the blocks' paired
+// order rho; the caller's layout is used only to read S0 and to write the
+// final state.
 //
-// Per chunk the critical path is the two tcgen05.mma groups and two short
-// epilogues: U^T to bf16 (the A operand of the second product), and S' to the
-// bf16 operand of the next chunk's first product while its decayed copy goes
-// back to TMEM.  The next block arrives by bulk copy a whole chunk ahead.
+// Warps 0..7 run the epilogues (warp w owns TMEM lanes 32 (w % 4) .. +31 and
+// half w / 4 of the columns); warp 8 only issues the MMAs and the bulk copies,
+// so that a blocking MMA issue never delays an epilogue.  Per chunk the
+// critical path is: first product -> U^T epilogue -> state product -> bf16
+// copy of S'.  The state decay and the previous chunk's output run under the
+// first product; blocks are triple-buffered, two chunks ahead.
 #include <cuda.h>
 
 #include "kda_common.cuh"
@@ -32,19 +36,17 @@ namespace {
 using namespace sm100;
 
 constexpr int kC = kChunk;
-constexpr int kThreads = 256;
-constexpr uint32_t kBufStride = 75776;      // kBlkBytes rounded up to 1024
-constexpr uint32_t OFF_ST = 0;              // S^T bf16 K-major [dv][rho] (A of the first product), 32 KB
-constexpr uint32_t OFF_BUF = 32768;         // two blocks
-constexpr uint32_t OFF_UT = OFF_BUF + 2 * kBufStride;   // U^T bf16 K-major [dv][t], 16 KB
-constexpr uint32_t OFF_OST = OFF_UT + 16384;             // output staging bf16 [64][136]
-constexpr int kOStride = 136;
-constexpr uint32_t OFF_SMALL = OFF_OST + 64 * kOStride * 2;
-constexpr uint32_t SM_BAR = 0, SM_TMEM = 32, SM_ABORT = 36, SM_END = 64;
+constexpr int kThreads = 288;   // 8 epilogue warps + 1 issuing warp
+constexpr int kIssuer = 256;    // lane 0 of warp 8
+constexpr int kNumBuf = 3;
+constexpr uint32_t kBufStride = 75776;   // kBlkBytes rounded up to 1024
+constexpr uint32_t OFF_SMALL = kNumBuf * kBufStride;
+constexpr uint32_t SM_BAR = 0 /* full[3], m1, m2s, m2o */, SM_TMEM = 48, SM_ABORT = 52, SM_END = 64;
 constexpr uint32_t kSmemBytes = OFF_SMALL + SM_END + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 static_assert(kBufStride >= kBlkBytes && kBufStride % 1024 == 0, "block buffer");
-constexpr uint32_t TM_U = 0, TM_O = 64, TM_S = 128, kTmemCols = 256;
+// TMEM columns: S^T fp32 | two [U^T | O^T] accumulator pairs | S^T bf16 (A operand) | U^T bf16 (A operand)
+constexpr uint32_t TM_S = 0, TM_UO0 = 128, TM_UO1 = 256, TM_SA = 384, TM_UA = 448, kTmemCols = 512;
 
 __device__ __forceinline__ void wait_or_abort(uint64_t *bar, uint32_t parity, volatile uint32_t *abort_flag,
                                               uint32_t *status) {
@@ -55,21 +57,22 @@ __device__ __forceinline__ void wait_or_abort(uint64_t *bar, uint32_t parity, vo
   }
 }
 
-// 64 fp32 values -> bf16, 128 bytes of row `row` of a row-swizzled tile of R rows from column col0
-__device__ __forceinline__ void store_row64(uint8_t *tile, int R, int row, int col0, const float *v) {
+// 32 fp32 values -> 16 packed bf16 pairs in 16 TMEM columns
+__device__ __forceinline__ void st_bf16_pairs(uint32_t taddr, const float *v) {
+  float w[16];
 #pragma unroll
-  for (int j = 0; j < 8; ++j)
-    *reinterpret_cast<uint4 *>(tile + swz_offset(R, row, col0 + 8 * j)) =
-        make_uint4(pack_bf16x2(v[8 * j], v[8 * j + 1]), pack_bf16x2(v[8 * j + 2], v[8 * j + 3]),
-                   pack_bf16x2(v[8 * j + 4], v[8 * j + 5]), pack_bf16x2(v[8 * j + 6], v[8 * j + 7]));
+  for (int j = 0; j < 16; ++j) w[j] = __uint_as_float(pack_bf16x2(v[2 * j], v[2 * j + 1]));
+  tmem_st16(taddr, w);
 }
 
 __global__ void __launch_bounds__(kThreads, 1) chunk_chain_kernel(const __grid_constant__ ChainParams prm) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t *small = sm + OFF_SMALL;
-  uint64_t *bar_full = reinterpret_cast<uint64_t *>(small + SM_BAR);   // [2]
-  uint64_t *bar_mma = bar_full + 2;
+  uint64_t *bar_full = reinterpret_cast<uint64_t *>(small + SM_BAR);   // [3]: block landed in buffer b
+  uint64_t *bar_m1 = bar_full + 3;    // first product done
+  uint64_t *bar_m2s = bar_full + 4;   // state product done
+  uint64_t *bar_m2o = bar_full + 5;   // output product done
   uint32_t *s_tmem = reinterpret_cast<uint32_t *>(small + SM_TMEM);
   volatile uint32_t *s_abort = reinterpret_cast<volatile uint32_t *>(small + SM_ABORT);
 
@@ -94,12 +97,14 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_chain_kernel(const __grid_c
   }
   float *dst = prm.state_out_pool ? prm.state_out_pool + (static_cast<size_t>(slot) * H + h) * kD * kD
                                   : prm.state_out_dense + (static_cast<size_t>(n) * H + h) * kD * kD;
-  // thread = (value channel d, half of the key channels / tokens)
-  const int quad = warp & 3, hv = warp >> 2;
+  // epilogue thread = (value channel d, half hv of the key channels / tokens)
+  const bool worker = warp < 8;
+  const int quad = warp & 3, hv = (warp >> 2) & 1;
   const int d = quad * 32 + lane;
   const float *src = prm.state_in ? prm.state_in + (static_cast<size_t>(slot) * H + h) * kD * kD : nullptr;
 
   if (nchunks == 0) {   // empty sequence: the final state is the initial one
+    if (!worker) return;
 #pragma unroll 8
     for (int i = 0; i < 64; ++i) {
       const int kd = kd_of_rho(64 * hv + i);
@@ -108,15 +113,13 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_chain_kernel(const __grid_c
     return;
   }
 
-  if (tid == 0) {
-    mbar_init(&bar_full[0], 1);
-    mbar_init(&bar_full[1], 1);
-    mbar_init(bar_mma, 1);
+  if (tid == kIssuer) {
+    for (int i = 0; i < 6; ++i) mbar_init(&bar_full[i], 1);
     *s_abort = 0;
     fence_mbar_init();
-    for (int c = 0; c < 2 && c < nchunks; ++c) {
+    for (int c = 0; c < kNumBuf && c < nchunks; ++c) {
       mbar_arrive_expect_tx(&bar_full[c], kBlkBytes);
-      bulk_load(sm + OFF_BUF + c * kBufStride, blk0 + c * blk_step, kBlkBytes, &bar_full[c]);
+      bulk_load(sm + c * kBufStride, blk0 + c * blk_step, kBlkBytes, &bar_full[c]);
     }
   }
   if (warp == 0) {
@@ -129,56 +132,95 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_chain_kernel(const __grid_c
   const uint32_t tmem = *s_tmem;
   const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
 
-  // S0 -> bf16 operand, and Diag(gamma_0) S0 -> TMEM
-  {
-    float s[64];
+  // S0 (this thread's 64 key channels rho = 64 hv + i) -> TMEM fp32 and the bf16 A operand
+  if (worker) {
 #pragma unroll
-    for (int i = 0; i < 64; ++i) {
-      const int kd = kd_of_rho(64 * hv + i);
-      s[i] = src ? src[static_cast<size_t>(kd) * kD + d] : 0.f;
+    for (int part = 0; part < 2; ++part) {
+      const int col = 64 * hv + 32 * part;
+      float s[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const int kd = kd_of_rho(col + i);
+        s[i] = src ? src[static_cast<size_t>(kd) * kD + d] : 0.f;
+      }
+      tmem_st16(tmem + lane_base + TM_S + col, s);
+      tmem_st16(tmem + lane_base + TM_S + col + 16, s + 16);
+      st_bf16_pairs(tmem + lane_base + TM_SA + col / 2, s);
     }
-    store_row64(sm + OFF_ST, 128, d, 64 * hv, s);
-    wait_or_abort(&bar_full[0], 0, s_abort, prm.status);
-    const float *gam = reinterpret_cast<const float *>(sm + OFF_BUF + kBlkGamma) + 64 * hv;
-#pragma unroll
-    for (int i = 0; i < 64; ++i) s[i] *= gam[i];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) tmem_st16(tmem + lane_base + TM_S + 64 * hv + 16 * k, s + 16 * k);
     tmem_wait_st();
   }
-  fence_async_smem();
   tc_fence_before();
   __syncthreads();
 
-  uint32_t mma_phase = 0;
-  for (int c = 0; c < nchunks; ++c) {
-    const int b = c & 1;
-    uint8_t *buf = sm + OFF_BUF + b * kBufStride;
-    const int tok0 = t0 + c * kC;
-    const int valid = min(kC, len - c * kC);
+  // output of a chunk (accumulated in pair ob) -> `stage` as the 64-token x 128-channel row-swizzled
+  // tile the output tensor map stores (workers)
+  auto out_to_stage = [&](int ob, uint8_t *stage) {
+    uint32_t ov[32];
+    const uint32_t tb = tmem + lane_base + (ob ? TM_UO1 : TM_UO0) + 64 + 32 * hv;
+    tmem_ld16_async(tb, ov);
+    tmem_ld16_async(tb + 16, ov + 16);
+    tmem_wait_ld();
+    tmem_tie<32>(ov);
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      *reinterpret_cast<uint16_t *>(stage + swz_offset(64, 32 * hv + i, d)) = f32_to_bf16_bits(__uint_as_float(ov[i]));
+  };
 
-    // ---- [U^T | O^T] = S^T [W | Q+]^T
-    if (tid == 0) {
+  for (int c = 0; c < nchunks; ++c) {
+    const int b = c % kNumBuf;
+    uint8_t *buf = sm + b * kBufStride;
+    const uint32_t tm_uo = c & 1 ? TM_UO1 : TM_UO0;
+    wait_or_abort(&bar_full[b], (c / kNumBuf) & 1, s_abort, prm.status);
+
+    // ---- [U^T | O^T] = S_c^T [W | Q+]^T  (one N = 128 product, A = S^T bf16 in TMEM)
+    if (tid == kIssuer) {
       tc_fence_after();
-      const uint32_t st = smem_u32(sm + OFF_ST), wq = smem_u32(buf + kBlkWQ);
-      const uint32_t id = idesc_bf16(128, 64, false, true);
+      const uint64_t wq = desc_mnmajor_base(smem_u32(buf + kBlkWQ), 128);
+      const uint32_t id = idesc_bf16(128, 128, false, true);
 #pragma unroll
-      for (int s = 0; s < 8; ++s) mma_bf16(tmem + TM_U, desc_kmajor(st, 128, s), desc_mnmajor(wq, 128, s), id, s > 0);
-#pragma unroll
-      for (int s = 0; s < 8; ++s)
-        mma_bf16(tmem + TM_O, desc_kmajor(st, 128, s), desc_mnmajor(wq + 16384, 128, s), id, s > 0);
-      mma_commit(bar_mma);
+      for (int k = 0; k < 8; ++k) mma_bf16_tmem_a(tmem + tm_uo, tmem + TM_SA + 8 * k, wq + mnmajor_step(k), id, k > 0);
+      mma_commit(bar_m1);
     }
-    __syncwarp();
-    wait_or_abort(bar_mma, mma_phase & 1, s_abort, prm.status);
-    ++mma_phase;
+
+    // ---- under the product: Diag(gamma_c) S_c -> TMEM
+    if (worker) {
+      const int col = 64 * hv;
+      const float *gam = reinterpret_cast<const float *>(buf + kBlkGamma) + col;
+      uint32_t sv[64];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) tmem_ld16_async(tmem + lane_base + TM_S + col + 16 * k, sv + 16 * k);
+      tmem_wait_ld();
+      tmem_tie<64>(sv);
+      float f[64];
+#pragma unroll
+      for (int i = 0; i < 64; ++i) f[i] = __uint_as_float(sv[i]) * gam[i];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) tmem_st16(tmem + lane_base + TM_S + col + 16 * k, f + 16 * k);
+    }
+    // ---- output of chunk c - 1 (its product is done) -> staged in its block buffer -> global
+    if (c > 0) {
+      uint8_t *prev = sm + ((c - 1) % kNumBuf) * kBufStride;
+      wait_or_abort(bar_m2o, (c - 1) & 1, s_abort, prm.status);
+      tc_fence_after();
+      if (worker) out_to_stage((c - 1) & 1, prev);
+      fence_async_smem();
+      __syncthreads();
+      if (tid == kIssuer) {   // chunk c - 1 is not the last one: all 64 rows are valid
+        const int tok = t0 + (c - 1) * kC;
+        tma_store_3d(&prm.tout, 0, h, tok, prev);
+        tma_store_3d(&prm.tout, 64, h, tok, prev + 8192);
+        bulk_commit();
+      }
+    }
+    // ---- wait for the first product
+    wait_or_abort(bar_m1, c & 1, s_abort, prm.status);
     tc_fence_after();
 
-    // ---- U^T = U^^T - (W S)^T -> bf16 [dv][t]
-    {
+    // ---- U^T = U^^T - (W S)^T -> bf16 A operand in TMEM
+    if (worker) {
       uint32_t v[32];
-      tmem_ld16_async(tmem + lane_base + TM_U + 32 * hv, v);
-      tmem_ld16_async(tmem + lane_base + TM_U + 32 * hv + 16, v + 16);
+      tmem_ld16_async(tmem + lane_base + tm_uo + 32 * hv, v);
+      tmem_ld16_async(tmem + lane_base + tm_uo + 32 * hv + 16, v + 16);
       tmem_wait_ld();
       tmem_tie<32>(v);
       float u[32];
@@ -193,78 +235,94 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_chain_kernel(const __grid_c
           u[8 * j + 2 * e + 1] = uh.y - __uint_as_float(v[8 * j + 2 * e + 1]);
         }
       }
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        *reinterpret_cast<uint4 *>(sm + OFF_UT + swz_offset(128, d, 32 * hv + 8 * j)) =
-            make_uint4(pack_bf16x2(u[8 * j], u[8 * j + 1]), pack_bf16x2(u[8 * j + 2], u[8 * j + 3]),
-                       pack_bf16x2(u[8 * j + 4], u[8 * j + 5]), pack_bf16x2(u[8 * j + 6], u[8 * j + 7]));
+      st_bf16_pairs(tmem + lane_base + TM_UA + 16 * hv, u);
     }
-    fence_async_smem();
+    tmem_wait_st();
     tc_fence_before();
     __syncthreads();
 
-    // ---- [O^T | S^T] += U^T [P ; K'^T]^T
-    if (tid == 0) {
+    // ---- S^T += U^T K' (N = 128), then O^T += U^T P^T (N = 64), committed separately
+    if (tid == kIssuer) {
       tc_fence_after();
-      const uint32_t ut = smem_u32(sm + OFF_UT), pk = smem_u32(buf + kBlkPK);
-      const uint32_t id = idesc_bf16(128, kBlkPKRows, false, false);
+      const uint64_t pk = desc_kmajor_base(smem_u32(buf + kBlkPK));
+      const uint32_t id_s = idesc_bf16(128, 128, false, false), id_o = idesc_bf16(128, 64, false, false);
 #pragma unroll
-      for (int s = 0; s < 4; ++s) mma_bf16(tmem + TM_O, desc_kmajor(ut, 128, s), desc_kmajor(pk, kBlkPKRows, s), id, 1);
-      mma_commit(bar_mma);
+      for (int k = 0; k < 4; ++k)
+        mma_bf16_tmem_a(tmem + TM_S, tmem + TM_UA + 8 * k, pk + desc_bytes(64 * 128) + kmajor_step(kBlkPKRows, k),
+                        id_s, 1);
+      mma_commit(bar_m2s);
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        mma_bf16_tmem_a(tmem + tm_uo + 64, tmem + TM_UA + 8 * k, pk + kmajor_step(kBlkPKRows, k), id_o, 1);
+      mma_commit(bar_m2o);
+      // once the output store has read chunk c - 1's buffer, fetch the block two chunks ahead into it
+      if (c > 0 && c + 2 < nchunks) {
+        bulk_wait_read();
+        const int bn = (c + 2) % kNumBuf;
+        mbar_arrive_expect_tx(&bar_full[bn], kBlkBytes);
+        bulk_load(sm + bn * kBufStride, blk0 + (c + 2) * blk_step, kBlkBytes, &bar_full[bn]);
+      }
     }
-    __syncwarp();
-    wait_or_abort(bar_mma, mma_phase & 1, s_abort, prm.status);
-    ++mma_phase;
+    wait_or_abort(bar_m2s, c & 1, s_abort, prm.status);
     tc_fence_after();
-    // the block is consumed: fetch chunk c + 2 into its buffer
-    if (tid == 0 && c + 2 < nchunks) {
-      mbar_arrive_expect_tx(&bar_full[b], kBlkBytes);
-      bulk_load(buf, blk0 + (c + 2) * blk_step, kBlkBytes, &bar_full[b]);
-    }
 
-    // ---- S' -> bf16 operand and Diag(gamma_next) S' -> TMEM (or the final state); O -> staging
-    {
+    // ---- S_{c+1} -> the bf16 A operand of the next chunk's first product
+    if (worker && c + 1 < nchunks) {
+      const int col = 64 * hv;
       uint32_t sv[64];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) tmem_ld16_async(tmem + lane_base + TM_S + 64 * hv + 16 * k, sv + 16 * k);
-      uint32_t ov[32];
-      tmem_ld16_async(tmem + lane_base + TM_O + 32 * hv, ov);
-      tmem_ld16_async(tmem + lane_base + TM_O + 32 * hv + 16, ov + 16);
+      for (int k = 0; k < 4; ++k) tmem_ld16_async(tmem + lane_base + TM_S + col + 16 * k, sv + 16 * k);
       tmem_wait_ld();
       tmem_tie<64>(sv);
-      tmem_tie<32>(ov);
-      float *s = reinterpret_cast<float *>(sv);
-      if (c + 1 < nchunks) {
-        store_row64(sm + OFF_ST, 128, d, 64 * hv, s);
-        wait_or_abort(&bar_full[b ^ 1], ((c + 1) >> 1) & 1, s_abort, prm.status);
-        const float *gam = reinterpret_cast<const float *>(sm + OFF_BUF + (b ^ 1) * kBufStride + kBlkGamma) + 64 * hv;
+      float s[64];
 #pragma unroll
-        for (int i = 0; i < 64; ++i) s[i] *= gam[i];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) tmem_st16(tmem + lane_base + TM_S + 64 * hv + 16 * k, s + 16 * k);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 64; ++i) dst[static_cast<size_t>(kd_of_rho(64 * hv + i)) * kD + d] = s[i];
-      }
-      uint16_t *sO = reinterpret_cast<uint16_t *>(sm + OFF_OST);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) sO[(32 * hv + i) * kOStride + d] = f32_to_bf16_bits(__uint_as_float(ov[i]));
+      for (int i = 0; i < 64; ++i) s[i] = __uint_as_float(sv[i]);
+      st_bf16_pairs(tmem + lane_base + TM_SA + col / 2, s);
+      st_bf16_pairs(tmem + lane_base + TM_SA + col / 2 + 16, s + 32);
       tmem_wait_st();
     }
-    fence_async_smem();
     tc_fence_before();
     __syncthreads();
-    {
-      const uint16_t *sO = reinterpret_cast<const uint16_t *>(sm + OFF_OST);
-      for (int idx = tid; idx < valid * 16; idx += kThreads) {
-        const int r = idx >> 4, cc = idx & 15;
-        *reinterpret_cast<uint4 *>(prm.out + static_cast<size_t>(tok0 + r) * prm.out_stride + h * kD + 8 * cc) =
-            *reinterpret_cast<const uint4 *>(sO + r * kOStride + 8 * cc);
-      }
-    }
     if (*s_abort) break;
   }
 
+  // output of the last chunk, and the final state
+  wait_or_abort(bar_m2o, (nchunks - 1) & 1, s_abort, prm.status);
+  tc_fence_after();
+  uint8_t *last = sm + ((nchunks - 1) % kNumBuf) * kBufStride;
+  const int last_valid = len - (nchunks - 1) * kC;
+  if (worker) out_to_stage((nchunks - 1) & 1, last);
+  fence_async_smem();
+  __syncthreads();
+  if (last_valid == kC) {
+    if (tid == kIssuer) {
+      const int tok = t0 + (nchunks - 1) * kC;
+      tma_store_3d(&prm.tout, 0, h, tok, last);
+      tma_store_3d(&prm.tout, 64, h, tok, last + 8192);
+      bulk_commit();
+    }
+  } else {   // a ragged last chunk: only its valid rows, 16 bytes per thread and step
+    uint16_t *o = prm.out + static_cast<size_t>(t0 + (nchunks - 1) * kC) * prm.out_stride + h * kD;
+    for (int idx = tid; idx < last_valid * 16; idx += kThreads) {
+      const int r = idx >> 4, cc = idx & 15;
+      *reinterpret_cast<uint4 *>(o + static_cast<size_t>(r) * prm.out_stride + 8 * cc) =
+          *reinterpret_cast<const uint4 *>(last + swz_offset(64, r, 8 * cc));
+    }
+  }
+  if (tid == kIssuer) bulk_wait_all();
+  if (worker) {
+#pragma unroll
+    for (int part = 0; part < 2; ++part) {
+      const int col = 64 * hv + 32 * part;
+      uint32_t sv[32];
+      tmem_ld16_async(tmem + lane_base + TM_S + col, sv);
+      tmem_ld16_async(tmem + lane_base + TM_S + col + 16, sv + 16);
+      tmem_wait_ld();
+      tmem_tie<32>(sv);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) dst[static_cast<size_t>(kd_of_rho(col + i)) * kD + d] = __uint_as_float(sv[i]);
+    }
+  }
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {

@@ -188,6 +188,7 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_c
   uint8_t *blk = prm.blocks + (static_cast<size_t>(gslot) * H + h) * kBlkBytes;
   if (*reinterpret_cast<volatile uint32_t *>(prm.status) & KDA_DEVICE_TIMEOUT) return;   // an earlier CTA gave up
 
+  // ------------------------------------------------------------ setup: barriers, TMA of q, k, g, TMEM, beta
   if (tid == 0) {
     mbar_init(bar_in, 1);
     mbar_init(bar_v, 1);
@@ -215,6 +216,7 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_c
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
+  // ------------------------------------------------------------ wait for q, k, g
   wait_or_abort(bar_in, 0, s_abort, prm.status);
 
   // ------------------------------------------------------------ l2 norms (token-major)
@@ -339,10 +341,11 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_c
   // ------------------------------------------------------------ A/P product (one 128 x 160 tcgen05.mma)
   if (tid == 0) {
     tc_fence_after();
-    const uint32_t fq = smem_u32(sm + OFF_FQ), gb = smem_u32(sm + OFF_GB);
+    const uint64_t fq = desc_mnmajor_base(smem_u32(sm + OFF_FQ), 128);
+    const uint64_t gb = desc_mnmajor_base(smem_u32(sm + OFF_GB), 128);
     const uint32_t id = idesc_bf16(128, kGBCols, true, true);
 #pragma unroll
-    for (int s = 0; s < 8; ++s) mma_bf16(tmem, desc_mnmajor(fq, 128, s), desc_mnmajor(gb, 128, s), id, s > 0);
+    for (int s = 0; s < 8; ++s) mma_bf16(tmem, fq + mnmajor_step(s), gb + mnmajor_step(s), id, s > 0);
     mma_commit(bar_mma);
   }
   __syncwarp();
@@ -511,16 +514,19 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_c
     tc_fence_after();
     const uint32_t id_w = idesc_bf16(128, 64, false, false);
     const uint32_t id_u = idesc_bf16(128, 64, true, false);
-    const uint32_t kp = smem_u32(sm + OFF_KP), vv = smem_u32(sm + OFF_VIN), tt = smem_u32(sm + OFF_T);
+    const uint64_t kp = desc_kmajor_base(smem_u32(sm + OFF_KP));
+    const uint64_t vv = desc_mnmajor_base(smem_u32(sm + OFF_VIN), 64);
+    const uint64_t tt = desc_kmajor_base(smem_u32(sm + OFF_T));
 #pragma unroll
-    for (int s = 0; s < 4; ++s) mma_bf16(tmem, desc_kmajor(kp, 128, s), desc_kmajor(tt, 64, s), id_w, s > 0);
+    for (int s = 0; s < 4; ++s) mma_bf16(tmem, kp + kmajor_step(128, s), tt + kmajor_step(64, s), id_w, s > 0);
 #pragma unroll
-    for (int s = 0; s < 4; ++s) mma_bf16(tmem + 64, desc_mnmajor(vv, 64, s), desc_kmajor(tt, 64, s), id_u, s > 0);
+    for (int s = 0; s < 4; ++s) mma_bf16(tmem + 64, vv + mnmajor_step(s), tt + kmajor_step(64, s), id_u, s > 0);
     mma_commit(bar_mma);
   }
   __syncwarp();
   wait_or_abort(bar_mma, 1, s_abort, prm.status);
   tc_fence_after();
+  // ------------------------------------------------------------ W^T, U^^T rows to the staging tiles
   {
     // warp = (lane quadrant, W^T | U^^T); the thread's row is one 128-byte line of the block tile
     const int q4 = warp & 3, which = warp >> 2;
@@ -543,18 +549,20 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_c
   fence_async_smem();
   tc_fence_before();
   __syncthreads();
+  // ------------------------------------------------------------ block write-out, TMEM release
   if (tid == 0) {
     bulk_store(blk + kBlkWQ, sm + OFF_WST, 16384);
     bulk_store(blk + kBlkUH, sm + OFF_UST, 16384);
     bulk_store(blk + kBlkPK, sm + OFF_PST, 8192);
     bulk_commit();
-    bulk_wait_all();
+    bulk_wait_read();
   }
   if (warp == 0) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+  // ------------------------------------------------------------ end
 }
 
 }  // namespace

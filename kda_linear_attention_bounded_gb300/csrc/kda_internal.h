@@ -82,6 +82,7 @@ struct IntraParams {
 
 // State pass: one CTA per (sequence, head) of a group.
 struct ChainParams {
+  CUtensorMap tout;             // output [tokens, H, 128] bf16, box 64 channels x 1 head x 64 tokens
   const uint8_t *blocks;
   const int32_t *slot_ids;      // indexed by seq0 + local sequence
   int num_slots;

@@ -72,7 +72,8 @@ cudaError_t launch_chunk_prefill(const ChunkArgs &a, const int32_t *cu_host, uin
   if (!make_token_map(&ip->tq, a.q, a.H, a.total_tokens, a.qkv_stride) ||
       !make_token_map(&ip->tk, a.k, a.H, a.total_tokens, a.qkv_stride) ||
       !make_token_map(&ip->tv, a.v, a.H, a.total_tokens, a.qkv_stride) ||
-      !make_token_map(&ip->tg, a.g, a.H, a.total_tokens, a.g_stride))
+      !make_token_map(&ip->tg, a.g, a.H, a.total_tokens, a.g_stride) ||
+      !make_token_map(&cp->tout, a.out, a.H, a.total_tokens, a.out_stride))
     return cudaErrorInvalidValue;
   ip->beta = a.beta;
   ip->beta_stride = a.beta_stride;

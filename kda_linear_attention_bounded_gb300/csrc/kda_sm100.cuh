@@ -91,6 +91,14 @@ __device__ __forceinline__ void tma_load_3d(void *smem_dst, const CUtensorMap *m
       : "memory");
 }
 
+// shared -> global tile store through a tensor map, tracked by the issuing thread's bulk groups
+// (rows beyond the tensor's extent are not written)
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, int c0, int c1, int c2, const void *smem_src) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];"
+               ::"l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(smem_src))
+               : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -111,6 +119,9 @@ __device__ __forceinline__ void bulk_store(void *gdst, const void *smem_src, uin
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // wait until every committed bulk store of this thread has completed
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// wait until every committed bulk store of this thread has finished reading shared memory
+// (the global writes complete on their own, at the latest when the grid completes)
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 
 // ---------------------------------------------------------------- fences
 __device__ __forceinline__ void fence_async_smem() {
@@ -220,21 +231,42 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64
       : "memory");
 }
 
+// Same with the A operand in TMEM: lane m holds row m, 32-bit column j holds the bf16 pair
+// (A[m][2j], A[m][2j+1]) (lower K index in the low half); the 16-deep K step s starts 8s columns in.
+__device__ __forceinline__ void mma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                                uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+      ::"r"(d_tmem), "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // arrive on `bar` once every previously issued tcgen05.mma of this thread completes
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                : "memory");
 }
 
-// Descriptors of a row-swizzled tile used as an operand, for the 16-wide K step s.
-//   K-major tile: rows = M/N index (R rows), columns = K.
-__device__ __forceinline__ uint64_t desc_kmajor(uint32_t tile, int R, int s) {
-  return smem_desc(tile + (s >> 2) * R * 128 + (s & 3) * 32, 16, 1024);
+// Descriptors of a row-swizzled tile used as an operand.  The start-address
+// field holds (address >> 4) in the low 14 bits, so the descriptor of
+// tile + offset is desc(tile) + offset / 16 (no carry: shared-memory
+// addresses stay below 256 KB).  Kernels compute one base descriptor per tile
+// and add the compile-time K-step offsets below: a tcgen05.mma whose
+// descriptor comes out of per-instruction address arithmetic issues several
+// times slower than one fed by base + constant.
+//   K-major tile (rows = M or N index, R rows; columns = K): SBO = 1024,
+//     K step s at (s / 4) * R * 128 + (s % 4) * 32 bytes;
+//   MN-major tile (rows = K index, R rows; columns = M or N): LBO = R * 128
+//     (the next 64-wide M/N panel), SBO = 1024, K step s at s * 2048 bytes.
+__device__ __forceinline__ uint64_t desc_kmajor_base(uint32_t tile) { return smem_desc(tile, 16, 1024); }
+__device__ __forceinline__ uint64_t desc_mnmajor_base(uint32_t tile, int R) { return smem_desc(tile, R * 128, 1024); }
+__host__ __device__ constexpr uint64_t kmajor_step(int R, int s) {
+  return static_cast<uint64_t>(((s >> 2) * R * 128 + (s & 3) * 32) >> 4);
 }
-//   MN-major tile: rows = K index (R rows), columns = M/N.
-__device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile, int R, int s) {
-  return smem_desc(tile + s * 2048, R * 128, 1024);
-}
+__host__ __device__ constexpr uint64_t mnmajor_step(int s) { return static_cast<uint64_t>((s * 2048) >> 4); }
+__host__ __device__ constexpr uint64_t desc_bytes(uint32_t bytes) { return static_cast<uint64_t>(bytes >> 4); }
 
 }  // namespace sm100
 }  // namespace kda
