@@ -57,16 +57,17 @@ constexpr uint32_t OFF_GB = 32768;    // [G | B_1 | B_2 | B_3]: 128 rows rho x 1
 constexpr uint32_t OFF_KP = 81920;    // K+^T = (k^ o e^b)^T: 128 rows rho x 64 tokens, K-major A operand (16 KB)
 constexpr uint32_t OFF_QIN = 0, OFF_KIN = 16384, OFF_GIN = 32768;   // TMA tiles, consumed before the operands are written
 // after the A/P product
-constexpr uint32_t OFF_A = 0;         // A (later Inv_RR A_RJ) fp32 [64][68]
-constexpr uint32_t OFF_INV = 17408;   // (I + A)^-1 fp32 [64][68]
-constexpr uint32_t OFF_VIN = 49152;   // v tile (TMA) [token][value channel]
-constexpr uint32_t OFF_T = 65536;     // T bf16 K-major [t][t']
-constexpr uint32_t OFF_PST = 73728;   // P rows of the block's PK tile
+constexpr uint32_t OFF_QST = 0;       // Q+^T rows of the block (16 KB), stored by bulk copy
+constexpr uint32_t OFF_PKST = 16384;  // [P ; K'^T] rows of the block (24 KB), stored by bulk copy; then ...
+constexpr uint32_t OFF_T = 16384;     // ... T bf16 K-major [t][t']
+constexpr uint32_t OFF_A = 40960;     // A fp32 [64][68], turned into (I + A)^-1 in place
+constexpr uint32_t OFF_VIN = 58368;   // v tile (TMA) [token][value channel]
 // after the W / U^ products
-constexpr uint32_t OFF_WST = 0, OFF_UST = 16384;   // W^T and U^^T rows of the block
+constexpr uint32_t OFF_WST = 40960, OFF_UST = 57344;   // W^T and U^^T rows of the block
 constexpr uint32_t OFF_SMALL = 98304;
-constexpr uint32_t SM_NQ = 0, SM_NK = 256, SM_BETA = 512, SM_H = 768 /* [2][4][128] f32 */, SM_DTB = 4864,
-                   SM_BAR = 5376, SM_TMEM = 5400, SM_ABORT = 5404, SM_END = 5440;
+constexpr uint32_t SM_NQ = 0, SM_NK = 256, SM_BETA = 512, SM_H = 768 /* [2][4][128] f32 */,
+                   SM_BAR = 4864, SM_TMEM = 4888, SM_ABORT = 4892, SM_END = 4928;
+constexpr int kCopyThread = 128;      // issues the block's early bulk stores (Q+, [P ; K'])
 constexpr uint32_t kSmemBytes = OFF_SMALL + SM_END + 1024;   // + alignment slack
 static_assert(2 * (kSmemBytes + 1024) <= 233472, "two CTAs per SM");
 constexpr int kAStride = 68;
@@ -89,14 +90,37 @@ __device__ __forceinline__ void wait_or_abort(uint64_t *bar, uint32_t parity, vo
   }
 }
 
-// 8 consecutive tokens of the thread's two key channels -> two 16-byte chunks
+// 8 consecutive tokens of the thread's two key channels -> two 16-byte chunks (rows rho, 64 + rho)
+__device__ __forceinline__ void pack8(const float2 (&v)[8], uint4 &lo, uint4 &hi) {
+  lo = make_uint4(pack_bf16x2(v[0].x, v[1].x), pack_bf16x2(v[2].x, v[3].x), pack_bf16x2(v[4].x, v[5].x),
+                  pack_bf16x2(v[6].x, v[7].x));
+  hi = make_uint4(pack_bf16x2(v[0].y, v[1].y), pack_bf16x2(v[2].y, v[3].y), pack_bf16x2(v[4].y, v[5].y),
+                  pack_bf16x2(v[6].y, v[7].y));
+}
 __device__ __forceinline__ void put8(uint8_t *tile, int R_rows, int rho, int col0, const float2 (&v)[8]) {
-  const uint4 lo = make_uint4(pack_bf16x2(v[0].x, v[1].x), pack_bf16x2(v[2].x, v[3].x),
-                              pack_bf16x2(v[4].x, v[5].x), pack_bf16x2(v[6].x, v[7].x));
-  const uint4 hi = make_uint4(pack_bf16x2(v[0].y, v[1].y), pack_bf16x2(v[2].y, v[3].y),
-                              pack_bf16x2(v[4].y, v[5].y), pack_bf16x2(v[6].y, v[7].y));
+  uint4 lo, hi;
+  pack8(v, lo, hi);
   *reinterpret_cast<uint4 *>(tile + swz_offset(R_rows, rho, col0)) = lo;
   *reinterpret_cast<uint4 *>(tile + swz_offset(R_rows, 64 + rho, col0)) = hi;
+}
+
+// 16 x 8 tile of X Y for X (16 x 8ks) and Y (8ks x 8), both fp32 with row stride kAStride, on TF32
+// tensor cores; fragments in the PTX ISA m16n8k8 layout (g = lane / 4, t = lane % 4)
+__device__ __forceinline__ void mm_16x8(float (&d)[4], const float *X, const float *Y, int ks, int lane) {
+  const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {   // ks <= 4
+    if (k >= ks) break;
+    const float *xa = X + g * kAStride + 8 * k + t;
+    const float *yb = Y + (8 * k + t) * kAStride + g;
+    mma_1688_tf32(d, to_tf32(xa[0]), to_tf32(xa[8 * kAStride]), to_tf32(xa[4]), to_tf32(xa[8 * kAStride + 4]),
+                  to_tf32(yb[0]), to_tf32(yb[4 * kAStride]));
+  }
+}
+__device__ __forceinline__ void st_16x8(float *D, const float (&d)[4], float sgn, int lane) {
+  const int g = lane >> 2, t = lane & 3;
+  *reinterpret_cast<float2 *>(D + g * kAStride + 2 * t) = make_float2(sgn * d[0], sgn * d[1]);
+  *reinterpret_cast<float2 *>(D + (g + 8) * kAStride + 2 * t) = make_float2(sgn * d[2], sgn * d[3]);
 }
 
 struct BlockFactors {
@@ -108,11 +132,13 @@ struct BlockFactors {
 };
 
 // Operand rows of 8 tokens (rows t0 .. t0+7 of block R) for key channels
-// (2p, 2p+1); x[j] = (b - m_R) log2(e) of those rows.
+// (2p, 2p+1); x[j] = (b - m_R) log2(e) of those rows.  The block's Q+ and K'
+// rows come back packed (qp, kq: rows p and 64 + p) and are stored once the
+// operand tiles are free.
 template <int R>
 __device__ __forceinline__ void build_rows(const uint32_t (&kr)[8], const uint32_t (&qr)[8], const float2 (&x)[8],
                                            int t0, int p, const float *s_nq, const float *s_nk,
-                                           const BlockFactors &f, uint8_t *sm, uint8_t *blk) {
+                                           const BlockFactors &f, uint8_t *sm, uint4 (&qp)[2], uint4 (&kq)[2]) {
   float2 kh[8], qh[8], e[8], ie[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
@@ -134,13 +160,13 @@ __device__ __forceinline__ void build_rows(const uint32_t (&kr)[8], const uint32
   put8(sm + OFF_FQ, 128, p, 64 + t0, v);
 #pragma unroll
   for (int j = 0; j < 8; ++j) w[j] = mul2(v[j], f.ems);   // Q+ = scale Q e^(m_R)
-  put8(blk + kBlkWQ, 128, p, 64 + t0, w);
+  pack8(w, qp[0], qp[1]);
 #pragma unroll
   for (int j = 0; j < 8; ++j) v[j] = mul2(kh[j], ie[j]);  // G
   put8(sm + OFF_GB, 128, p, t0, v);
 #pragma unroll
   for (int j = 0; j < 8; ++j) w[j] = mul2(v[j], f.el);    // K' = G e^(b_63 - m_R)
-  put8(blk + kBlkPK, kBlkPKRows, 64 + p, t0, w);
+  pack8(w, kq[0], kq[1]);
   if (R < 3) {
 #pragma unroll
     for (int j = 0; j < 8; ++j) v[j] = mul2(v[j], f.eg);  // k^ e^(a_R - b) <= |k^|
@@ -161,7 +187,6 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_c
   float *s_nk = reinterpret_cast<float *>(small + SM_NK);
   float *s_beta = reinterpret_cast<float *>(small + SM_BETA);
   float *s_h = reinterpret_cast<float *>(small + SM_H);     // [half][block][channel]: sum of lambda over 8 rows
-  float *s_dtb = reinterpret_cast<float *>(small + SM_DTB);
   uint64_t *bar_in = reinterpret_cast<uint64_t *>(small + SM_BAR);
   uint64_t *bar_v = bar_in + 1;
   uint64_t *bar_mma = bar_in + 2;
@@ -207,17 +232,18 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_c
     tmem_alloc(s_tmem, kTmemCols);
     tmem_relinquish();
   }
-  if (tid < kD) s_dtb[tid] = prm.dt_bias[h * kD + tid];
-  if (tid >= 128 && tid < 128 + kC) {
-    const int r = tid - 128;
-    s_beta[r] = r < valid ? sigmoid_f(bf16_bits_to_f32(prm.beta[(size_t)(tok0 + r) * prm.beta_stride + h])) : 0.f;
-  }
+  // per-thread parameters, consumed after the wait for q, k, g (their latency hides under it)
+  const int p = tid & 63, sel = tid >> 6;
+  const int c0 = 2 * p;
+  const float2 dtb = *reinterpret_cast<const float2 *>(prm.dt_bias + h * kD + c0);
+  const uint16_t beta_raw = tid < valid ? prm.beta[(size_t)(tok0 + tid) * prm.beta_stride + h] : uint16_t(0);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
   // ------------------------------------------------------------ wait for q, k, g
   wait_or_abort(bar_in, 0, s_abort, prm.status);
+  if (tid < kC) s_beta[tid] = tid < valid ? sigmoid_f(bf16_bits_to_f32(beta_raw)) : 0.f;
 
   // ------------------------------------------------------------ l2 norms (token-major)
   {
@@ -249,12 +275,10 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_c
 
   // ------------------------------------------------------------ gate and in-block decays
   // thread = (channel pair p, 8-row half `hf` of the blocks Ra and Rb = 3 - Ra); warp-uniform blocks
-  const int p = tid & 63, sel = tid >> 6;
   const int hf = sel & 1, Ra = sel >> 1, Rb = 3 - Ra;
-  const int c0 = 2 * p;
   const float nea = -__expf(prm.A_log[h]) * kLog2e;   // lambda = lb sigmoid(ea (g + dtb)); log2 units below
   const float lb2 = prm.lower_bound * kLog2e;
-  const float2 nd = make_float2(nea * s_dtb[c0], nea * s_dtb[c0 + 1]);
+  const float2 nd = make_float2(nea * dtb.x, nea * dtb.y);
   uint32_t kr[2][8], qr[2][8];
   float2 x[2][8];   // (b_t - m_R) log2(e), rows t0 .. t0+7 of each of the two blocks
 #pragma unroll
@@ -294,6 +318,7 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_c
   __syncthreads();   // norms, half sums visible; q, k, g tiles fully read
 
   // ------------------------------------------------------------ anchors and operand tiles
+  uint4 qp[2][2], kq[2][2];   // packed Q+ / K' rows of the two blocks
   {
     float2 hh[2][4];
 #pragma unroll
@@ -327,11 +352,11 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_c
     };
     const BlockFactors fa = factors(Ra), fb = factors(Rb);
     if (Ra == 0) {
-      build_rows<0>(kr[0], qr[0], x[0], 8 * hf, p, s_nq, s_nk, fa, sm, blk);
-      build_rows<3>(kr[1], qr[1], x[1], 48 + 8 * hf, p, s_nq, s_nk, fb, sm, blk);
+      build_rows<0>(kr[0], qr[0], x[0], 8 * hf, p, s_nq, s_nk, fa, sm, qp[0], kq[0]);
+      build_rows<3>(kr[1], qr[1], x[1], 48 + 8 * hf, p, s_nq, s_nk, fb, sm, qp[1], kq[1]);
     } else {
-      build_rows<1>(kr[0], qr[0], x[0], 16 + 8 * hf, p, s_nq, s_nk, fa, sm, blk);
-      build_rows<2>(kr[1], qr[1], x[1], 32 + 8 * hf, p, s_nq, s_nk, fb, sm, blk);
+      build_rows<1>(kr[0], qr[0], x[0], 16 + 8 * hf, p, s_nq, s_nk, fa, sm, qp[0], kq[0]);
+      build_rows<2>(kr[1], qr[1], x[1], 32 + 8 * hf, p, s_nq, s_nk, fb, sm, qp[1], kq[1]);
     }
   }
   fence_async_smem();
@@ -355,6 +380,15 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_c
     mbar_arrive_expect_tx(bar_v, 16384);
     tma_load_3d(sm + OFF_VIN, &prm.tv, 0, h, tok0, bar_v);
     tma_load_3d(sm + OFF_VIN + 8192, &prm.tv, 64, h, tok0, bar_v);
+  }
+  // the block's Q+ and K' rows go to their staging tiles
+#pragma unroll
+  for (int bi = 0; bi < 2; ++bi) {
+    const int t0 = 16 * (bi ? Rb : Ra) + 8 * hf;
+    *reinterpret_cast<uint4 *>(sm + OFF_QST + swz_offset(128, p, t0)) = qp[bi][0];
+    *reinterpret_cast<uint4 *>(sm + OFF_QST + swz_offset(128, 64 + p, t0)) = qp[bi][1];
+    *reinterpret_cast<uint4 *>(sm + OFF_PKST + swz_offset(kBlkPKRows, 64 + p, t0)) = kq[bi][0];
+    *reinterpret_cast<uint4 *>(sm + OFF_PKST + swz_offset(kBlkPKRows, 128 + p, t0)) = kq[bi][1];
   }
 
   // ------------------------------------------------------------ A (fp32) and P (bf16 block rows) from TMEM
@@ -391,7 +425,7 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_c
       if (is_p) {
 #pragma unroll
         for (int k8 = 0; k8 < 2; ++k8)
-          *reinterpret_cast<uint4 *>(sm + OFF_PST + swz_offset(64, r, 16 * I + 8 * k8)) =
+          *reinterpret_cast<uint4 *>(sm + OFF_PKST + swz_offset(kBlkPKRows, r, 16 * I + 8 * k8)) =
               make_uint4(pack_bf16x2(v[8 * k8], v[8 * k8 + 1]), pack_bf16x2(v[8 * k8 + 2], v[8 * k8 + 3]),
                          pack_bf16x2(v[8 * k8 + 4], v[8 * k8 + 5]), pack_bf16x2(v[8 * k8 + 6], v[8 * k8 + 7]));
       } else {
@@ -401,98 +435,98 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_c
       }
     }
   }
+  fence_async_smem();
   tc_fence_before();
   __syncthreads();
+  if (tid == kCopyThread) {   // Q+ and [P ; K'] rows are complete: store them
+    bulk_store(blk + kBlkWQ + 16384, sm + OFF_QST, 16384);
+    bulk_store(blk + kBlkPK, sm + OFF_PKST, kBlkPKRows * 128);
+    bulk_commit();
+  }
 
   // ------------------------------------------------------------ T = (I + A)^-1 Diag(beta)
+  // Blocked inverse of the unit-lower L = I + A in fp32, 16x16 blocks D_R = L_RR^-1:
+  //   L^-1_10 = -D_1 A_10 D_0,  L^-1_32 = -D_3 A_32 D_2,
+  //   L^-1 (rows 32..63, cols 0..31) = -I_2 A_(23,01) I_1,  I_1, I_2 the inverses of the diagonal 32x32 halves.
+  // Everything happens in place in the A tile: each block of the inverse overwrites the block of A
+  // that is no longer needed, and the temporaries live in its unused strictly-upper part.
   {
     float *sA = reinterpret_cast<float *>(sm + OFF_A);
-    float *sInv = reinterpret_cast<float *>(sm + OFF_INV);
-    uint16_t *sT16 = reinterpret_cast<uint16_t *>(sm + OFF_T);
-    // diagonal 16x16 blocks (warp R, lane = column): forward substitution; their part of T goes
-    // straight to the bf16 tile.  Warps 4..7 clear the strictly-upper blocks of T.
+    float *sInv = sA;
+    // D_R: warps 0, 1; lane = (block R = 2 warp + lane / 16, column jc = lane % 16); right-looking
+    // substitution, so every step is one FMA deep on the column's earlier value
+    if (warp < 2) {
+      const int R = 2 * warp + (lane >> 4), jc = lane & 15;
+      const float *a = sA + (16 * R) * kAStride + 16 * R;
+      float xs[16];
+#pragma unroll
+      for (int r = 0; r < 16; ++r) xs[r] = r == jc ? 1.f : 0.f;
+#pragma unroll
+      for (int m = 0; m < 15; ++m) {
+#pragma unroll
+        for (int r = m + 1; r < 16; ++r) xs[r] = fmaf(-a[r * kAStride + m], xs[m], xs[r]);
+      }
+      __syncwarp();   // every lane of the block has read its A entries
+#pragma unroll
+      for (int r = 0; r < 16; ++r) sInv[(16 * R + r) * kAStride + 16 * R + jc] = xs[r];
+    }
+    __syncthreads();
+    // Every block product below is a set of 16 x 8 output tiles, one per warp task, on TF32
+    // tensor cores (mma.sync m16n8k8) with fp32 accumulation.
+    // Y_1 = A_10 D_0 -> A tile rows 0..15, cols 16..31;  Y_3 = A_32 D_2 -> rows 32..47, cols 48..63
     if (warp < 4) {
-      if (lane < 16) {
-        const int R = warp, jc = lane;
-        const float bj = s_beta[16 * R + jc];
-        float xs[16];
-#pragma unroll
-        for (int r = 0; r < 16; ++r) {
-          float lrow[16];
-#pragma unroll
-          for (int k4 = 0; k4 < 4; ++k4) {
-            const float4 l4 = *reinterpret_cast<const float4 *>(sA + (16 * R + r) * kAStride + 16 * R + 4 * k4);
-            lrow[4 * k4] = l4.x; lrow[4 * k4 + 1] = l4.y; lrow[4 * k4 + 2] = l4.z; lrow[4 * k4 + 3] = l4.w;
-          }
-          float v0 = (r == jc) ? 1.f : 0.f, v1 = 0.f;
-#pragma unroll
-          for (int mm = 0; mm < r; ++mm) {
-            if (mm & 1) v1 = fmaf(-lrow[mm], xs[mm], v1);
-            else v0 = fmaf(-lrow[mm], xs[mm], v0);
-          }
-          xs[r] = v0 + v1;
-        }
-#pragma unroll
-        for (int r = 0; r < 16; ++r) {
-          sInv[(16 * R + r) * kAStride + 16 * R + jc] = xs[r];
-          sT16[swz_offset(64, 16 * R + r, 16 * R + jc) >> 1] = f32_to_bf16_bits(r >= jc ? xs[r] * bj : 0.f);
-        }
-      }
-    } else {
-      for (int idx = tid - 128; idx < 6 * 32; idx += kThreads - 128) {
-        const int bk = idx >> 5, e = idx & 31;
-        const int R = bk < 3 ? 0 : bk < 5 ? 1 : 2;
-        const int I = bk < 3 ? bk + 1 : bk < 5 ? bk - 1 : 3;
-        *reinterpret_cast<uint4 *>(sm + OFF_T + swz_offset(64, 16 * R + (e >> 1), 16 * I + 8 * (e & 1))) =
-            make_uint4(0, 0, 0, 0);
-      }
+      const int lo = warp < 2 ? 0 : 32, nj = warp & 1;
+      float d[4] = {0.f, 0.f, 0.f, 0.f};
+      mm_16x8(d, sA + (lo + 16) * kAStride + lo, sInv + lo * kAStride + lo + 8 * nj, 2, lane);
+      st_16x8(sA + lo * kAStride + lo + 16 + 8 * nj, d, 1.f, lane);
     }
     __syncthreads();
-    // off-diagonal blocks: with L~_RJ = Inv_RR A_RJ (J < R, in place over A),
-    //   Inv_RI = - sum_{J=I}^{R-1} L~_RJ Inv_JI
-    const int g8 = lane >> 2, t4 = lane & 3;
-    for (int task = warp; task < 12; task += 8) {   // 6 block pairs x 2 column halves
-      const int pr = task >> 1;                     // (R, J): (1,0) (2,0) (2,1) (3,0) (3,1) (3,2)
-      const int R = pr < 1 ? 1 : pr < 3 ? 2 : 3;
-      const int J = pr - (R * (R - 1)) / 2;
-      const int n0 = 16 * J + 8 * (task & 1);
-      float y[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int ks = 0; ks < 2; ++ks) {
-        const float *ar = sInv + (16 * R + g8) * kAStride + 16 * R + 8 * ks + t4;
-        const float *br = sA + (16 * R + 8 * ks + t4) * kAStride + n0 + g8;
-        mma_1688_tf32(y, to_tf32(ar[0]), to_tf32(ar[8 * kAStride]), to_tf32(ar[4]), to_tf32(ar[8 * kAStride + 4]),
-                      to_tf32(br[0]), to_tf32(br[4 * kAStride]));
-      }
-      __syncwarp();
-      *reinterpret_cast<float2 *>(sA + (16 * R + g8) * kAStride + n0 + 2 * t4) = make_float2(y[0], y[1]);
-      *reinterpret_cast<float2 *>(sA + (16 * R + g8 + 8) * kAStride + n0 + 2 * t4) = make_float2(y[2], y[3]);
+    // L^-1_10 = -D_1 Y_1 -> sInv rows 16..31, cols 0..15;  L^-1_32 = -D_3 Y_3 -> rows 48..63, cols 32..47
+    if (warp < 4) {
+      const int lo = warp < 2 ? 0 : 32, nj = warp & 1;
+      float d[4] = {0.f, 0.f, 0.f, 0.f};
+      mm_16x8(d, sInv + (lo + 16) * kAStride + lo + 16, sA + lo * kAStride + lo + 16 + 8 * nj, 2, lane);
+      st_16x8(sInv + (lo + 16) * kAStride + lo + 8 * nj, d, -1.f, lane);
     }
     __syncthreads();
-    // column walks: warp = (column block I in 0..2, half); each reads only its own earlier results
-    if (warp < 6) {
-      const int I = warp >> 1;
-      const int n0 = 16 * I + 8 * (warp & 1);
-      const float2 bcol = *reinterpret_cast<const float2 *>(s_beta + n0 + 2 * t4);
-      for (int R = I + 1; R < 4; ++R) {
-        float xs[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int J = I; J < R; ++J) {
+    // Z = A_(23,01) I_1 (32 x 32) -> A tile rows 0..31, cols 32..63; warp = (16-row half mi, 8 columns nj).
+    // I_1 is block-lower: columns 16..31 only see its rows 16..31.
+    {
+      const int mi = warp >> 2, nj = warp & 3;
+      const int k0 = nj < 2 ? 0 : 16;
+      float d[4] = {0.f, 0.f, 0.f, 0.f};
+      mm_16x8(d, sA + (32 + 16 * mi) * kAStride + k0, sInv + k0 * kAStride + 8 * nj, (32 - k0) / 8, lane);
+      st_16x8(sA + (16 * mi) * kAStride + 32 + 8 * nj, d, 1.f, lane);
+    }
+    __syncthreads();
+    // L^-1 (rows 32..63, cols 0..31) = -I_2 Z; I_2 is block-lower: its rows 0..15 only see Z rows 0..15
+    {
+      const int mi = warp >> 2, nj = warp & 3;
+      float d[4] = {0.f, 0.f, 0.f, 0.f};
+      mm_16x8(d, sInv + (32 + 16 * mi) * kAStride + 32, sA + 32 + 8 * nj, mi ? 4 : 2, lane);
+      st_16x8(sInv + (32 + 16 * mi) * kAStride + 8 * nj, d, -1.f, lane);
+    }
+    if (tid == kCopyThread) bulk_wait_read();   // T goes over the [P ; K'] staging tile next
+    __syncthreads();
+    // T = Inv Diag(beta) in bf16, zero above the diagonal (the upper part of sInv is never written):
+    // thread = (row r, 16-column group); consecutive rows per warp keep the 16-byte loads conflict-free
+    {
+      const int r = tid & 63, cg = tid >> 6;
+      const float *irow = sInv + r * kAStride + 16 * cg;
 #pragma unroll
-          for (int ks = 0; ks < 2; ++ks) {
-            const int kc = 16 * J + 8 * ks;
-            const float *ar = sA + (16 * R + g8) * kAStride + kc + t4;
-            const float *br = sInv + (kc + t4) * kAStride + n0 + g8;
-            mma_1688_tf32(xs, to_tf32(ar[0]), to_tf32(ar[8 * kAStride]), to_tf32(ar[4]),
-                          to_tf32(ar[8 * kAStride + 4]), to_tf32(br[0]), to_tf32(br[4 * kAStride]));
-          }
+      for (int k8 = 0; k8 < 2; ++k8) {
+        const float4 i0 = *reinterpret_cast<const float4 *>(irow + 8 * k8);
+        const float4 i1 = *reinterpret_cast<const float4 *>(irow + 8 * k8 + 4);
+        const float iv[8] = {i0.x, i0.y, i0.z, i0.w, i1.x, i1.y, i1.z, i1.w};
+        float t8[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int c = 16 * cg + 8 * k8 + e;
+          t8[e] = c <= r ? iv[e] * s_beta[c] : 0.f;
         }
-        *reinterpret_cast<float2 *>(sInv + (16 * R + g8) * kAStride + n0 + 2 * t4) = make_float2(-xs[0], -xs[1]);
-        *reinterpret_cast<float2 *>(sInv + (16 * R + g8 + 8) * kAStride + n0 + 2 * t4) = make_float2(-xs[2], -xs[3]);
-        *reinterpret_cast<uint32_t *>(sm + OFF_T + swz_offset(64, 16 * R + g8, n0 + 2 * t4)) =
-            pack_bf16x2(-xs[0] * bcol.x, -xs[1] * bcol.y);
-        *reinterpret_cast<uint32_t *>(sm + OFF_T + swz_offset(64, 16 * R + g8 + 8, n0 + 2 * t4)) =
-            pack_bf16x2(-xs[2] * bcol.x, -xs[3] * bcol.y);
-        __syncwarp();
+        *reinterpret_cast<uint4 *>(sm + OFF_T + swz_offset(64, r, 16 * cg + 8 * k8)) =
+            make_uint4(pack_bf16x2(t8[0], t8[1]), pack_bf16x2(t8[2], t8[3]), pack_bf16x2(t8[4], t8[5]),
+                       pack_bf16x2(t8[6], t8[7]));
       }
     }
   }
@@ -553,7 +587,6 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_c
   if (tid == 0) {
     bulk_store(blk + kBlkWQ, sm + OFF_WST, 16384);
     bulk_store(blk + kBlkUH, sm + OFF_UST, 16384);
-    bulk_store(blk + kBlkPK, sm + OFF_PST, 8192);
     bulk_commit();
     bulk_wait_read();
   }
