@@ -2,7 +2,10 @@
 
 One step = one kda_chunk_prefill call over the 8 x 2048-token, H=16, d=128
 workload (initial states gathered from a 64-slot pool, dense final states),
-inputs resident in HBM.  Also timed: the same call end to end with host
+inputs resident in HBM.  The call is two launches: the intra-chunk kernel over
+every (chunk, head) and the state pass over every (sequence, head); the
+roofline line covers the whole call (its algorithmic bytes over its
+CUDA-event time), the per-kernel split is in profiles/.  Also timed: the same call end to end with host
 buffers (pinned H2D of the step's inputs + D2H of its outputs inside the
 timed region), the verify call on 64 requests x 8 draft tokens, and the fp64
 CPU oracle on a bounded sample of the prefill workload.
@@ -55,13 +58,20 @@ def verify_algorithmic_bytes(inp):
     return BT * H * TOKEN_HEAD_BYTES + inp.B * H * STATE_BYTES * (1 + inp.T)
 
 
-def source_digest():
+# sources that decide each kernel's code (a traffic record is valid while they are unchanged)
+KERNEL_SOURCES = {
+    "prefill": ("kda_chunk_intra.cu", "kda_chunk_chain.cu", "kda_prefill.cu", "kda_prefill_block.h", "kda_sm100.cuh",
+                "kda_common.cuh", "kda_internal.h"),
+    "verify": ("kda_recurrent.cu", "kda_common.cuh", "kda_internal.h"),
+}
+
+
+def source_digest(kind):
     csrc = os.path.join(ROOT, "kda_linear_attention_bounded_gb300", "csrc")
     h = hashlib.sha256()
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + f.read())
+    for name in KERNEL_SOURCES[kind]:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
 
 
@@ -77,7 +87,7 @@ def recorded_traffic(kind):
             if ":" in line and not line.startswith("#"):
                 k, v = line.split(":", 1)
                 vals[k.strip()] = v.strip()
-    if vals.get("source_digest") != source_digest():
+    if vals.get("source_digest") != source_digest(kind):
         return None
     try:
         return float(vals["dram_bytes_per_launch"])
@@ -401,11 +411,12 @@ def run_gpu(args):
                    "vs_baseline_ref": "FlashKDA 49 us/layer at T=2048x8 on GB300 (vLLM PR #55737), context only"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic, "algorithmic_bytes": alg, "avg_launch_us": avg_launch_s * 1e6,
+                     "kernels": "chunk_intra_kernel + chunk_chain_kernel (one prefill call)",
                      "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else peak_kind},
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": e2e_steps},
-        "gpu_launches": args.steps,
+        "gpu_launches": 2 * args.steps,
         "clocks": clocks,
         "verify": {"workload": vin.name, "us_per_layer": v_us, "steps": v_steps,
                    "roofline": {"bound": "hbm", "achieved": v_achieved, "peak": peak, "unit": "GB/s",
