@@ -66,7 +66,7 @@ constexpr uint32_t OFF_VIN = 58368;   // v tile (TMA) [token][value channel]
 constexpr uint32_t OFF_WST = 40960, OFF_UST = 57344;   // W^T and U^^T rows of the block
 constexpr uint32_t OFF_SMALL = 98304;
 constexpr uint32_t SM_NQ = 0, SM_NK = 256, SM_BETA = 512, SM_H = 768 /* [2][4][128] f32 */,
-                   SM_BAR = 4864, SM_TMEM = 4888, SM_ABORT = 4892, SM_END = 4928;
+                   SM_BAR = 4864, SM_TMEM = 4888, SM_ABORT = 4892, SM_SEQ = 4896, SM_END = 4928;
 constexpr int kCopyThread = 128;      // issues the block's early bulk stores (Q+, [P ; K'])
 constexpr uint32_t kSmemBytes = OFF_SMALL + SM_END + 1024;   // + alignment slack
 static_assert(2 * (kSmemBytes + 1024) <= 233472, "two CTAs per SM");
@@ -197,19 +197,24 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_c
   const int H = prm.H;
   const int h = blockIdx.x % H;
   const int gslot = blockIdx.x / H;
-  // sequence of this chunk slot: the last n with chunk_off[n] <= gslot (never an empty sequence)
-  int n = 0;
-  {
+  // sequence of this chunk slot: the last n with chunk_off[n] <= gslot (never an empty sequence);
+  // warp 0 searches, the others read the result after the setup barrier
+  int *s_seq = reinterpret_cast<int *>(small + SM_SEQ);
+  int tok0 = 0, valid = 0;
+  if (warp == 0) {
     int lo = 0, hi = prm.num_seqs - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
       if (prm.chunk_off[mid] <= gslot) lo = mid;
       else hi = mid - 1;
     }
-    n = lo;
+    tok0 = prm.tok_off[lo] + (gslot - prm.chunk_off[lo]) * kC;
+    valid = min(kC, prm.tok_off[lo + 1] - tok0);
+    if (lane == 0) {
+      s_seq[0] = tok0;
+      s_seq[1] = valid;
+    }
   }
-  const int tok0 = prm.tok_off[n] + (gslot - prm.chunk_off[n]) * kC;
-  const int valid = min(kC, prm.tok_off[n + 1] - tok0);
   uint8_t *blk = prm.blocks + (static_cast<size_t>(gslot) * H + h) * kBlkBytes;
   if (*reinterpret_cast<volatile uint32_t *>(prm.status) & KDA_DEVICE_TIMEOUT) return;   // an earlier CTA gave up
 
@@ -236,11 +241,15 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_c
   const int p = tid & 63, sel = tid >> 6;
   const int c0 = 2 * p;
   const float2 dtb = *reinterpret_cast<const float2 *>(prm.dt_bias + h * kD + c0);
-  const uint16_t beta_raw = tid < valid ? prm.beta[(size_t)(tok0 + tid) * prm.beta_stride + h] : uint16_t(0);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
+  if (warp != 0) {
+    tok0 = s_seq[0];
+    valid = s_seq[1];
+  }
+  const uint16_t beta_raw = tid < valid ? prm.beta[(size_t)(tok0 + tid) * prm.beta_stride + h] : uint16_t(0);
   // ------------------------------------------------------------ wait for q, k, g
   wait_or_abort(bar_in, 0, s_abort, prm.status);
   if (tid < kC) s_beta[tid] = tid < valid ? sigmoid_f(bf16_bits_to_f32(beta_raw)) : 0.f;
@@ -395,16 +404,17 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_c
   {
     // lanes 0..63 of the product hold rows of A (k side), lanes 64..127 rows of P (q side)
     const int q4 = warp & 3, ib = warp >> 2;
-    const bool is_p = q4 >= 2;
+    const bool is_p = q4 >= 2;                 // warp-uniform
     const int r = (q4 & 1) * 32 + lane;
     const int Ra2 = (q4 & 1) * 2;              // row blocks of this warp: Ra2 (lanes 0..15), Ra2 + 1
-    const bool upper = (r >> 4) != Ra2;
+    const bool upper = lane >= 16;
     const uint32_t lane_base = static_cast<uint32_t>(q4 * 32) << 16;
     const float bscale = is_p ? prm.scale : s_beta[r];
     float *sA = reinterpret_cast<float *>(sm + OFF_A);
 #pragma unroll
     for (int ii = 0; ii < 2; ++ii) {
       const int I = 2 * ib + ii;   // column block
+      // source columns of the two row blocks (warp-uniform); -1: the block is above the diagonal
       const int srcA = (I == Ra2) ? 16 * I : (I < Ra2) ? gb_col0(Ra2) + 16 * I : -1;
       const int srcB = (I == Ra2 + 1) ? 16 * I : (I < Ra2 + 1) ? gb_col0(Ra2 + 1) + 16 * I : -1;
       uint32_t va[16], vb[16];
@@ -413,14 +423,14 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_c
       tmem_wait_ld();
       tmem_tie<16>(va);
       tmem_tie<16>(vb);
-      const int src = upper ? srcB : srcA;
+      // column i = 16 I + e is kept iff i < r (A) or i <= r (P); this also zeroes the blocks above the
+      // diagonal (i > r) whose registers were never loaded
+      const int lim = r - 16 * I + (is_p ? 1 : 0);
       float v[16];
 #pragma unroll
       for (int e = 0; e < 16; ++e) {
-        const int i = 16 * I + e;
         const float raw = __uint_as_float(upper ? vb[e] : va[e]);
-        const bool keep = (src >= 0) && (is_p ? (i <= r) : (i < r));
-        v[e] = keep ? raw * bscale : 0.f;
+        v[e] = e < lim ? raw * bscale : 0.f;
       }
       if (is_p) {
 #pragma unroll
