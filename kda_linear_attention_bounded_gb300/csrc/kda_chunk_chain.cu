@@ -21,8 +21,9 @@
 // half w / 4 of the columns); warp 8 only issues the MMAs and the bulk copies,
 // so that a blocking MMA issue never delays an epilogue.  Per chunk the
 // critical path is: first product -> U^T epilogue -> state product -> bf16
-// copy of S'.  The state decay and the previous chunk's output run under the
-// first product; blocks are triple-buffered, two chunks ahead.
+// copy of S' (which also stores the decayed state for the next state product).
+// The previous chunk's output runs under the first product; blocks are
+// triple-buffered, two chunks ahead.
 #include <cuda.h>
 
 #include "kda_common.cuh"
@@ -132,8 +133,10 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_chain_kernel(const __grid_c
   const uint32_t tmem = *s_tmem;
   const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
 
-  // S0 (this thread's 64 key channels rho = 64 hv + i) -> TMEM fp32 and the bf16 A operand
+  // S0 (this thread's 64 key channels rho = 64 hv + i) -> the bf16 A operand, and Diag(gamma_0) S0 -> TMEM
   if (worker) {
+    wait_or_abort(&bar_full[0], 0, s_abort, prm.status);
+    const float *gam = reinterpret_cast<const float *>(sm + kBlkGamma);
 #pragma unroll
     for (int part = 0; part < 2; ++part) {
       const int col = 64 * hv + 32 * part;
@@ -143,9 +146,11 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_chain_kernel(const __grid_c
         const int kd = kd_of_rho(col + i);
         s[i] = src ? src[static_cast<size_t>(kd) * kD + d] : 0.f;
       }
+      st_bf16_pairs(tmem + lane_base + TM_SA + col / 2, s);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) s[i] *= gam[col + i];
       tmem_st16(tmem + lane_base + TM_S + col, s);
       tmem_st16(tmem + lane_base + TM_S + col + 16, s + 16);
-      st_bf16_pairs(tmem + lane_base + TM_SA + col / 2, s);
     }
     tmem_wait_st();
   }
@@ -182,22 +187,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_chain_kernel(const __grid_c
       mma_commit(bar_m1);
     }
 
-    // ---- under the product: Diag(gamma_c) S_c -> TMEM
-    if (worker) {
-      const int col = 64 * hv;
-      const float *gam = reinterpret_cast<const float *>(buf + kBlkGamma) + col;
-      uint32_t sv[64];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) tmem_ld16_async(tmem + lane_base + TM_S + col + 16 * k, sv + 16 * k);
-      tmem_wait_ld();
-      tmem_tie<64>(sv);
-      float f[64];
-#pragma unroll
-      for (int i = 0; i < 64; ++i) f[i] = __uint_as_float(sv[i]) * gam[i];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) tmem_st16(tmem + lane_base + TM_S + col + 16 * k, f + 16 * k);
-    }
-    // ---- output of chunk c - 1 (its product is done) -> staged in its block buffer -> global
+    // ---- under the product: output of chunk c - 1 (its product is done) -> staged in its block buffer -> global
     if (c > 0) {
       uint8_t *prev = sm + ((c - 1) % kNumBuf) * kBufStride;
       wait_or_abort(bar_m2o, (c - 1) & 1, s_abort, prm.status);
@@ -266,7 +256,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_chain_kernel(const __grid_c
     wait_or_abort(bar_m2s, c & 1, s_abort, prm.status);
     tc_fence_after();
 
-    // ---- S_{c+1} -> the bf16 A operand of the next chunk's first product
+    // ---- S_{c+1} -> the bf16 A operand of the next chunk's first product; Diag(gamma_{c+1}) S_{c+1} -> TMEM
+    // (the decayed copy is only needed by the next chunk's state product)
     if (worker && c + 1 < nchunks) {
       const int col = 64 * hv;
       uint32_t sv[64];
@@ -279,6 +270,13 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_chain_kernel(const __grid_c
       for (int i = 0; i < 64; ++i) s[i] = __uint_as_float(sv[i]);
       st_bf16_pairs(tmem + lane_base + TM_SA + col / 2, s);
       st_bf16_pairs(tmem + lane_base + TM_SA + col / 2 + 16, s + 32);
+      const int bn = (c + 1) % kNumBuf;
+      wait_or_abort(&bar_full[bn], ((c + 1) / kNumBuf) & 1, s_abort, prm.status);
+      const float *gam = reinterpret_cast<const float *>(sm + bn * kBufStride + kBlkGamma) + col;
+#pragma unroll
+      for (int i = 0; i < 64; ++i) s[i] *= gam[i];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) tmem_st16(tmem + lane_base + TM_S + col + 16 * k, s + 16 * k);
       tmem_wait_st();
     }
     tc_fence_before();
