@@ -197,17 +197,19 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_c
   const int H = prm.H;
   const int h = blockIdx.x % H;
   const int gslot = blockIdx.x / H;
-  // sequence of this chunk slot: the last n with chunk_off[n] <= gslot (never an empty sequence);
-  // warp 0 searches, the others read the result after the setup barrier
+  // sequence of this chunk slot: the last n with chunk_off[n] <= gslot (never an empty sequence,
+  // since an empty one shares its chunk_off with the next); warp 0 searches, the others read the
+  // result after the setup barrier
   int *s_seq = reinterpret_cast<int *>(small + SM_SEQ);
   int tok0 = 0, valid = 0;
   if (warp == 0) {
-    int lo = 0, hi = prm.num_seqs - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (prm.chunk_off[mid] <= gslot) lo = mid;
-      else hi = mid - 1;
-    }
+    // two rounds of 32 candidates (num_seqs <= 1024): first the group of 32 sequences, then the sequence;
+    // chunk_off is non-decreasing and chunk_off[0] = 0 <= gslot, so each ballot has lane 0 set
+    const int ns = prm.num_seqs;
+    unsigned m = __ballot_sync(0xffffffffu, 32 * lane < ns && prm.chunk_off[32 * lane] <= gslot);
+    const int seg = 31 - __clz(m);
+    m = __ballot_sync(0xffffffffu, 32 * seg + lane < ns && prm.chunk_off[32 * seg + lane] <= gslot);
+    const int lo = 32 * seg + 31 - __clz(m);
     tok0 = prm.tok_off[lo] + (gslot - prm.chunk_off[lo]) * kC;
     valid = min(kC, prm.tok_off[lo + 1] - tok0);
     if (lane == 0) {
@@ -216,7 +218,6 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_c
     }
   }
   uint8_t *blk = prm.blocks + (static_cast<size_t>(gslot) * H + h) * kBlkBytes;
-  if (*reinterpret_cast<volatile uint32_t *>(prm.status) & KDA_DEVICE_TIMEOUT) return;   // an earlier CTA gave up
 
   // ------------------------------------------------------------ setup: barriers, TMA of q, k, g, TMEM, beta
   if (tid == 0) {
