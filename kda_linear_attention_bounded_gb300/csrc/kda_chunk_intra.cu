@@ -289,6 +289,7 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_c
   const float nea = -__expf(prm.A_log[h]) * kLog2e;   // lambda = lb sigmoid(ea (g + dtb)); log2 units below
   const float lb2 = prm.lower_bound * kLog2e;
   const float2 nd = make_float2(nea * dtb.x, nea * dtb.y);
+  const float2 nea2 = make_float2(nea, nea), lb22 = make_float2(lb2, lb2), one2 = make_float2(1.f, 1.f);
   uint32_t kr[2][8], qr[2][8];
   float2 x[2][8];   // (b_t - m_R) log2(e), rows t0 .. t0+7 of each of the two blocks
 #pragma unroll
@@ -303,10 +304,11 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_c
       kr[bi][j] = ld_u32(sm + OFF_KIN + off);
       qr[bi][j] = ld_u32(sm + OFF_QIN + off);
       const float2 gg = unpack_bf16x2(ld_u32(sm + OFF_GIN + off));
-      // lambda = lb2 / (1 + 2^(nea g + nea dtb))
-      const float l0 = lb2 * fast_rcp(1.f + fast_exp2(fmaf(nea, gg.x, nd.x)));
-      const float l1 = lb2 * fast_rcp(1.f + fast_exp2(fmaf(nea, gg.y, nd.y)));
-      lam[j] = r < valid ? make_float2(l0, l1) : make_float2(0.f, 0.f);
+      // lambda = lb2 / (1 + 2^(nea g + nea dtb)), channel pairs in packed fp32x2
+      const float2 ex = exp2_2(fma2(gg, nea2, nd));
+      const float2 den = fma2(ex, one2, one2);
+      const float2 l = mul2(make_float2(fast_rcp(den.x), fast_rcp(den.y)), lb22);
+      lam[j] = r < valid ? l : make_float2(0.f, 0.f);
     }
     float2 hs;
     if (hf == 0) {   // rows 0..7: b_t - m_R = -(lambda_{t+1} + ... + lambda_7)

@@ -81,3 +81,12 @@ def test_bad_slot_sets_status_and_skips():
                          ids=["2048x8", "8192x4", "16384+16varlen"])
 def test_full_size(make):
     _parity(make())
+
+
+def test_more_sequences_than_one_launch_plans():
+    # 1100 sequences: the planner splits them into two launch pairs of <= 1024 sequences
+    rng = np.random.default_rng(61)
+    lens = [int(x) for x in rng.integers(0, 40, size=1100)]
+    inp = inputs.prefill_inputs("many_seqs", lens, 2, seed=62, pool_slots=1100, load_initial=True,
+                                final_to_pool=True)
+    _parity(inp)
