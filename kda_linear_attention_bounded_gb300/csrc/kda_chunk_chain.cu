@@ -118,6 +118,9 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_chain_kernel(const __grid_c
     for (int i = 0; i < 6; ++i) mbar_init(&bar_full[i], 1);
     *s_abort = 0;
     fence_mbar_init();
+    // this grid may start while the intra-chunk grid is still finishing: the blocks are read only once it
+    // has completed and its writes are visible (everything above and the initial state do not depend on it)
+    grid_dependency_wait();
     for (int c = 0; c < kNumBuf && c < nchunks; ++c) {
       mbar_arrive_expect_tx(&bar_full[c], kBlkBytes);
       bulk_load(sm + c * kBufStride, blk0 + c * blk_step, kBlkBytes, &bar_full[c]);
@@ -133,25 +136,24 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_chain_kernel(const __grid_c
   const uint32_t tmem = *s_tmem;
   const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
 
-  // S0 (this thread's 64 key channels rho = 64 hv + i) -> the bf16 A operand, and Diag(gamma_0) S0 -> TMEM
+  // S0 (this thread's 64 key channels rho = 64 hv + i) -> the bf16 A operand; once the first block is in,
+  // Diag(gamma_0) S0 -> TMEM
   if (worker) {
-    wait_or_abort(&bar_full[0], 0, s_abort, prm.status);
-    const float *gam = reinterpret_cast<const float *>(sm + kBlkGamma);
+    const int col = 64 * hv;
+    float s[64];
 #pragma unroll
-    for (int part = 0; part < 2; ++part) {
-      const int col = 64 * hv + 32 * part;
-      float s[32];
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const int kd = kd_of_rho(col + i);
-        s[i] = src ? src[static_cast<size_t>(kd) * kD + d] : 0.f;
-      }
-      st_bf16_pairs(tmem + lane_base + TM_SA + col / 2, s);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) s[i] *= gam[col + i];
-      tmem_st16(tmem + lane_base + TM_S + col, s);
-      tmem_st16(tmem + lane_base + TM_S + col + 16, s + 16);
+    for (int i = 0; i < 64; ++i) {
+      const int kd = kd_of_rho(col + i);
+      s[i] = src ? src[static_cast<size_t>(kd) * kD + d] : 0.f;
     }
+    st_bf16_pairs(tmem + lane_base + TM_SA + col / 2, s);
+    st_bf16_pairs(tmem + lane_base + TM_SA + col / 2 + 16, s + 32);
+    wait_or_abort(&bar_full[0], 0, s_abort, prm.status);
+    const float *gam = reinterpret_cast<const float *>(sm + kBlkGamma) + col;
+#pragma unroll
+    for (int i = 0; i < 64; ++i) s[i] *= gam[i];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) tmem_st16(tmem + lane_base + TM_S + col + 16 * k, s + 16 * k);
     tmem_wait_st();
   }
   tc_fence_before();
@@ -340,8 +342,19 @@ cudaError_t launch_chunk_chain(const ChainParams &p, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  chunk_chain_kernel<<<p.num_seqs * p.H, kThreads, kSmemBytes, stream>>>(p);
-  return cudaGetLastError();
+  // programmatic dependent launch: the grid may be scheduled while the preceding intra-chunk grid drains
+  // (it waits for that grid's completion before reading any block)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.num_seqs * p.H);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, chunk_chain_kernel, p);
 }
 
 }  // namespace kda

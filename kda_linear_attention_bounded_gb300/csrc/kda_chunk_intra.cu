@@ -66,7 +66,7 @@ constexpr uint32_t OFF_VIN = 58368;   // v tile (TMA) [token][value channel]
 constexpr uint32_t OFF_WST = 40960, OFF_UST = 57344;   // W^T and U^^T rows of the block
 constexpr uint32_t OFF_SMALL = 98304;
 constexpr uint32_t SM_NQ = 0, SM_NK = 256, SM_BETA = 512, SM_H = 768 /* [2][4][128] f32 */,
-                   SM_BAR = 4864, SM_TMEM = 4888, SM_ABORT = 4892, SM_SEQ = 4896, SM_END = 4928;
+                   SM_BAR = 4864, SM_TMEM = 4888, SM_ABORT = 4892, SM_END = 4928;
 constexpr int kCopyThread = 128;      // issues the block's early bulk stores (Q+, [P ; K'])
 constexpr uint32_t kSmemBytes = OFF_SMALL + SM_END + 1024;   // + alignment slack
 static_assert(2 * (kSmemBytes + 1024) <= 233472, "two CTAs per SM");
@@ -193,30 +193,33 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_c
   uint32_t *s_tmem = reinterpret_cast<uint32_t *>(small + SM_TMEM);
   volatile uint32_t *s_abort = reinterpret_cast<volatile uint32_t *>(small + SM_ABORT);
 
+  // every CTA of this grid has started once all have passed here: the state pass may then be scheduled onto
+  // SMs this grid no longer fills (it waits for this grid's completion before reading the blocks)
+  grid_launch_dependents();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int H = prm.H;
   const int h = blockIdx.x % H;
   const int gslot = blockIdx.x / H;
-  // sequence of this chunk slot: the last n with chunk_off[n] <= gslot (never an empty sequence,
-  // since an empty one shares its chunk_off with the next); warp 0 searches, the others read the
-  // result after the setup barrier
-  int *s_seq = reinterpret_cast<int *>(small + SM_SEQ);
-  int tok0 = 0, valid = 0;
-  if (warp == 0) {
-    // two rounds of 32 candidates (num_seqs <= 1024): first the group of 32 sequences, then the sequence;
-    // chunk_off is non-decreasing and chunk_off[0] = 0 <= gslot, so each ballot has lane 0 set
-    const int ns = prm.num_seqs;
-    unsigned m = __ballot_sync(0xffffffffu, 32 * lane < ns && prm.chunk_off[32 * lane] <= gslot);
-    const int seg = 31 - __clz(m);
-    m = __ballot_sync(0xffffffffu, 32 * seg + lane < ns && prm.chunk_off[32 * seg + lane] <= gslot);
-    const int lo = 32 * seg + 31 - __clz(m);
-    tok0 = prm.tok_off[lo] + (gslot - prm.chunk_off[lo]) * kC;
-    valid = min(kC, prm.tok_off[lo + 1] - tok0);
-    if (lane == 0) {
-      s_seq[0] = tok0;
-      s_seq[1] = valid;
+  // first token of chunk slot gs and the end of its sequence: the last n with chunk_off[n] <= gs (an empty
+  // sequence shares its chunk_off with the next one), by an 8-way search whose loads are the same for every
+  // thread (constant-cache broadcasts); invariant chunk_off[lo] <= gs < chunk_off[hi]
+  auto first_token = [&](int gs) {
+    int lo = 0, hi = prm.num_seqs;
+    while (hi - lo > 1) {
+      const int step = (hi - lo + 7) >> 3;
+      int nlo = lo;
+#pragma unroll
+      for (int i = 1; i < 8; ++i) {
+        const int m = lo + i * step;
+        if (m < hi && prm.chunk_off[m] <= gs) nlo = m;
+      }
+      hi = min(hi, nlo + step);
+      lo = nlo;
     }
-  }
+    return make_int2(prm.tok_off[lo] + (gs - prm.chunk_off[lo]) * kC, prm.tok_off[lo + 1]);
+  };
+  const int2 seq_tok = first_token(gslot);
+  const int tok0 = seq_tok.x, valid = min(kC, seq_tok.y - tok0);
   uint8_t *blk = prm.blocks + (static_cast<size_t>(gslot) * H + h) * kBlkBytes;
 
   // ------------------------------------------------------------ setup: barriers, TMA of q, k, g, TMEM, beta
@@ -246,11 +249,18 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_c
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
-  if (warp != 0) {
-    tok0 = s_seq[0];
-    valid = s_seq[1];
-  }
   const uint16_t beta_raw = tid < valid ? prm.beta[(size_t)(tok0 + tid) * prm.beta_stride + h] : uint16_t(0);
+  if (warp == 0) {   // the CTA that starts about one wave after this one finds its q, k, v, g in L2
+    const int nb = static_cast<int>(blockIdx.x) + prm.prefetch_ahead;
+    if (prm.prefetch_ahead > 0 && nb < static_cast<int>(gridDim.x)) {
+      const int t2 = first_token(nb / H).x;
+      if (lane < 8) {
+        const int which = lane >> 1;
+        const CUtensorMap *mp = which == 0 ? &prm.tq : which == 1 ? &prm.tk : which == 2 ? &prm.tv : &prm.tg;
+        tma_prefetch_3d(mp, 64 * (lane & 1), nb % H, t2);
+      }
+    }
+  }
   // ------------------------------------------------------------ wait for q, k, g
   wait_or_abort(bar_in, 0, s_abort, prm.status);
   if (tid < kC) s_beta[tid] = tid < valid ? sigmoid_f(bf16_bits_to_f32(beta_raw)) : 0.f;
@@ -466,40 +476,49 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_c
   {
     float *sA = reinterpret_cast<float *>(sm + OFF_A);
     float *sInv = sA;
-    // D_R: warps 0, 1; lane = (block R = 2 warp + lane / 16, column jc = lane % 16); right-looking
-    // substitution, so every step is one FMA deep on the column's earlier value
-    if (warp < 2) {
-      const int R = 2 * warp + (lane >> 4), jc = lane & 15;
+    // D_R: task (block R, column jc) = 8 warp + lane / 4, so warps 2R and 2R + 1 share block R; lane
+    // q = lane % 4 of a task carries rows q, q + 4, q + 8, q + 12 of its column.  Right-looking: at step m
+    // the lane holding row m broadcasts x_m to its task's lanes, and every later row takes one FMA.
+    {
+      const int q = lane & 3, jc = 8 * (warp & 1) + (lane >> 2), R = warp >> 1;
       const float *a = sA + (16 * R) * kAStride + 16 * R;
-      float xs[16];
+      float xs[4];
 #pragma unroll
-      for (int r = 0; r < 16; ++r) xs[r] = r == jc ? 1.f : 0.f;
+      for (int i = 0; i < 4; ++i) xs[i] = 4 * i + q == jc ? 1.f : 0.f;
 #pragma unroll
       for (int m = 0; m < 15; ++m) {
+        const float xm = __shfl_sync(0xffffffffu, xs[m >> 2], (lane & ~3) | (m & 3));
 #pragma unroll
-        for (int r = m + 1; r < 16; ++r) xs[r] = fmaf(-a[r * kAStride + m], xs[m], xs[r]);
+        for (int i = (m + 1) >> 2; i < 4; ++i) {
+          const int r = 4 * i + q;
+          if (r > m) xs[i] = fmaf(-a[r * kAStride + m], xm, xs[i]);
+        }
       }
-      __syncwarp();   // every lane of the block has read its A entries
+      switch (R) {   // both warps of the block have read its A entries (constant barrier ids)
+        case 0: named_bar_sync<1>(64); break;
+        case 1: named_bar_sync<2>(64); break;
+        case 2: named_bar_sync<3>(64); break;
+        default: named_bar_sync<4>(64); break;
+      }
 #pragma unroll
-      for (int r = 0; r < 16; ++r) sInv[(16 * R + r) * kAStride + 16 * R + jc] = xs[r];
+      for (int i = 0; i < 4; ++i) sInv[(16 * R + 4 * i + q) * kAStride + 16 * R + jc] = xs[i];
     }
     __syncthreads();
     // Every block product below is a set of 16 x 8 output tiles, one per warp task, on TF32
     // tensor cores (mma.sync m16n8k8) with fp32 accumulation.
-    // Y_1 = A_10 D_0 -> A tile rows 0..15, cols 16..31;  Y_3 = A_32 D_2 -> rows 32..47, cols 48..63
+    // Y_1 = A_10 D_0 -> A tile rows 0..15, cols 16..31;  Y_3 = A_32 D_2 -> rows 32..47, cols 48..63;
+    // then L^-1_10 = -D_1 Y_1 -> sInv rows 16..31, cols 0..15;  L^-1_32 = -D_3 Y_3 -> rows 48..63, cols 32..47.
+    // A warp's output tile needs only its own Y tile; the pair barrier keeps A_10 (A_32) intact until both
+    // warps of the pair have read it.
     if (warp < 4) {
       const int lo = warp < 2 ? 0 : 32, nj = warp & 1;
       float d[4] = {0.f, 0.f, 0.f, 0.f};
       mm_16x8(d, sA + (lo + 16) * kAStride + lo, sInv + lo * kAStride + lo + 8 * nj, 2, lane);
       st_16x8(sA + lo * kAStride + lo + 16 + 8 * nj, d, 1.f, lane);
-    }
-    __syncthreads();
-    // L^-1_10 = -D_1 Y_1 -> sInv rows 16..31, cols 0..15;  L^-1_32 = -D_3 Y_3 -> rows 48..63, cols 32..47
-    if (warp < 4) {
-      const int lo = warp < 2 ? 0 : 32, nj = warp & 1;
-      float d[4] = {0.f, 0.f, 0.f, 0.f};
-      mm_16x8(d, sInv + (lo + 16) * kAStride + lo + 16, sA + lo * kAStride + lo + 16 + 8 * nj, 2, lane);
-      st_16x8(sInv + (lo + 16) * kAStride + lo + 8 * nj, d, -1.f, lane);
+      if (warp < 2) named_bar_sync<5>(64); else named_bar_sync<6>(64);
+      float e[4] = {0.f, 0.f, 0.f, 0.f};
+      mm_16x8(e, sInv + (lo + 16) * kAStride + lo + 16, sA + lo * kAStride + lo + 16 + 8 * nj, 2, lane);
+      st_16x8(sInv + (lo + 16) * kAStride + lo + 8 * nj, e, -1.f, lane);
     }
     __syncthreads();
     // Z = A_(23,01) I_1 (32 x 32) -> A tile rows 0..31, cols 32..63; warp = (16-row half mi, 8 columns nj).

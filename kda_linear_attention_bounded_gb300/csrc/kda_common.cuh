@@ -77,6 +77,14 @@ __device__ __forceinline__ uint32_t to_tf32(float x) {
   return r;
 }
 
+// barrier among `count` threads (a multiple of 32) of the CTA, on hardware barrier `id` (1..15; 0 is
+// __syncthreads); also orders their shared-memory accesses
+template <int kId>
+__device__ __forceinline__ void named_bar_sync(int count) {
+  static_assert(kId >= 1 && kId < 16, "barrier 0 is __syncthreads");
+  asm volatile("bar.sync %0, %1;" ::"n"(kId), "r"(count) : "memory");
+}
+
 // D (16x8 fp32) += A (16x8 tf32, row) * B (8x8 tf32, col); fragments as in the PTX ISA m16n8k8 layout
 __device__ __forceinline__ void mma_1688_tf32(float *d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                               uint32_t b0, uint32_t b1) {

@@ -74,6 +74,7 @@ struct IntraParams {
   const float *A_log, *dt_bias;
   float lower_bound, scale;
   int H, num_seqs;
+  int prefetch_ahead;           // a CTA prefetches into L2 the inputs of the CTA this many indices later
   uint8_t *blocks;              // block (chunk slot g, head h) at blocks + (g H + h) kBlkBytes
   uint32_t *status;
   int32_t chunk_off[kMaxSeqsPerLaunch + 1];   // first chunk slot of each sequence of the group

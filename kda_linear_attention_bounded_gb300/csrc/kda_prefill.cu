@@ -82,6 +82,13 @@ cudaError_t launch_chunk_prefill(const ChunkArgs &a, const int32_t *cu_host, uin
   ip->lower_bound = a.lower_bound;
   ip->scale = a.scale;
   ip->H = a.H;
+  {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess && cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
+      ip->prefetch_ahead = 2 * sms;   // two intra-chunk CTAs per SM
+    else
+      ip->prefetch_ahead = 0;
+  }
   ip->blocks = blocks;
   ip->status = a.status;
   cp->blocks = blocks;
