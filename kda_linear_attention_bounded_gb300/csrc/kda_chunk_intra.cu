@@ -200,26 +200,8 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_c
   const int H = prm.H;
   const int h = blockIdx.x % H;
   const int gslot = blockIdx.x / H;
-  // first token of chunk slot gs and the end of its sequence: the last n with chunk_off[n] <= gs (an empty
-  // sequence shares its chunk_off with the next one), by an 8-way search whose loads are the same for every
-  // thread (constant-cache broadcasts); invariant chunk_off[lo] <= gs < chunk_off[hi]
-  auto first_token = [&](int gs) {
-    int lo = 0, hi = prm.num_seqs;
-    while (hi - lo > 1) {
-      const int step = (hi - lo + 7) >> 3;
-      int nlo = lo;
-#pragma unroll
-      for (int i = 1; i < 8; ++i) {
-        const int m = lo + i * step;
-        if (m < hi && prm.chunk_off[m] <= gs) nlo = m;
-      }
-      hi = min(hi, nlo + step);
-      lo = nlo;
-    }
-    return make_int2(prm.tok_off[lo] + (gs - prm.chunk_off[lo]) * kC, prm.tok_off[lo + 1]);
-  };
-  const int2 seq_tok = first_token(gslot);
-  const int tok0 = seq_tok.x, valid = min(kC, seq_tok.y - tok0);
+  // the chunk slot's first token and its tokens (a broadcast load each)
+  const int tok0 = prm.slot_tok0[gslot], valid = prm.slot_valid[gslot];
   uint8_t *blk = prm.blocks + (static_cast<size_t>(gslot) * H + h) * kBlkBytes;
 
   // ------------------------------------------------------------ setup: barriers, TMA of q, k, g, TMEM, beta
@@ -245,22 +227,12 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_c
   const int p = tid & 63, sel = tid >> 6;
   const int c0 = 2 * p;
   const float2 dtb = *reinterpret_cast<const float2 *>(prm.dt_bias + h * kD + c0);
+  const uint16_t beta_raw = tid < valid ? prm.beta[(size_t)(tok0 + tid) * prm.beta_stride + h] : uint16_t(0);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
-  const uint16_t beta_raw = tid < valid ? prm.beta[(size_t)(tok0 + tid) * prm.beta_stride + h] : uint16_t(0);
-  if (warp == 0) {   // the CTA that starts about one wave after this one finds its q, k, v, g in L2
-    const int nb = static_cast<int>(blockIdx.x) + prm.prefetch_ahead;
-    if (prm.prefetch_ahead > 0 && nb < static_cast<int>(gridDim.x)) {
-      const int t2 = first_token(nb / H).x;
-      if (lane < 8) {
-        const int which = lane >> 1;
-        const CUtensorMap *mp = which == 0 ? &prm.tq : which == 1 ? &prm.tk : which == 2 ? &prm.tv : &prm.tg;
-        tma_prefetch_3d(mp, 64 * (lane & 1), nb % H, t2);
-      }
-    }
-  }
+
   // ------------------------------------------------------------ wait for q, k, g
   wait_or_abort(bar_in, 0, s_abort, prm.status);
   if (tid < kC) s_beta[tid] = tid < valid ? sigmoid_f(bf16_bits_to_f32(beta_raw)) : 0.f;
@@ -394,6 +366,18 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_c
 #pragma unroll
     for (int s = 0; s < 8; ++s) mma_bf16(tmem, fq + mnmajor_step(s), gb + mnmajor_step(s), id, s > 0);
     mma_commit(bar_mma);
+    // under the product: the CTA that starts about one wave after this one will find its q, k, v, g in L2
+    const int nb = static_cast<int>(blockIdx.x) + prm.prefetch_ahead;
+    if (prm.prefetch_ahead > 0 && nb < static_cast<int>(gridDim.x)) {
+      const int t2 = prm.slot_tok0[nb / H], h2 = nb % H;
+#pragma unroll
+      for (int x = 0; x < 128; x += 64) {
+        tma_prefetch_3d(&prm.tq, x, h2, t2);
+        tma_prefetch_3d(&prm.tk, x, h2, t2);
+        tma_prefetch_3d(&prm.tg, x, h2, t2);
+        tma_prefetch_3d(&prm.tv, x, h2, t2);
+      }
+    }
   }
   __syncwarp();
   wait_or_abort(bar_mma, 0, s_abort, prm.status);

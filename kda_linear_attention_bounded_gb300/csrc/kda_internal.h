@@ -66,19 +66,22 @@ cudaError_t launch_commit(const CommitArgs &args, cudaStream_t stream);
 // are split on the host into consecutive groups).
 constexpr int kMaxSeqsPerLaunch = 1024;
 
-// Intra-chunk kernel: one CTA per (chunk slot, head) of a group of sequences.
+// Chunk slots per intra-chunk launch (a group's slots are split on the host into consecutive launches).
+constexpr int kMaxSlotsPerLaunch = 4096;
+
+// Intra-chunk kernel: one CTA per (chunk slot, head) of a run of consecutive chunk slots.
 struct IntraParams {
   CUtensorMap tq, tk, tv, tg;   // [tokens, H, 128] bf16, box 64 channels x 1 head x 64 tokens
   const uint16_t *beta;
   int64_t beta_stride;
   const float *A_log, *dt_bias;
   float lower_bound, scale;
-  int H, num_seqs;
+  int H;
   int prefetch_ahead;           // a CTA prefetches into L2 the inputs of the CTA this many indices later
-  uint8_t *blocks;              // block (chunk slot g, head h) at blocks + (g H + h) kBlkBytes
+  uint8_t *blocks;              // block (local chunk slot g, head h) at blocks + (g H + h) kBlkBytes
   uint32_t *status;
-  int32_t chunk_off[kMaxSeqsPerLaunch + 1];   // first chunk slot of each sequence of the group
-  int32_t tok_off[kMaxSeqsPerLaunch + 1];     // first token of each sequence of the group
+  int32_t slot_tok0[kMaxSlotsPerLaunch];   // first token of each local chunk slot
+  uint8_t slot_valid[kMaxSlotsPerLaunch];  // its tokens (1..64)
 };
 
 // State pass: one CTA per (sequence, head) of a group.

@@ -89,7 +89,6 @@ cudaError_t launch_chunk_prefill(const ChunkArgs &a, const int32_t *cu_host, uin
     else
       ip->prefetch_ahead = 0;
   }
-  ip->blocks = blocks;
   ip->status = a.status;
   cp->blocks = blocks;
   cp->slot_ids = a.slot_ids;
@@ -108,13 +107,12 @@ cudaError_t launch_chunk_prefill(const ChunkArgs &a, const int32_t *cu_host, uin
     int chunks = 0;
     for (int i = 0; i < ns; ++i) {
       const int len = cu_host[s0 + i + 1] - cu_host[s0 + i];
-      ip->chunk_off[i] = cp->chunk_off[i] = chunks;
-      ip->tok_off[i] = cp->tok_off[i] = cu_host[s0 + i];
+      cp->chunk_off[i] = chunks;
+      cp->tok_off[i] = cu_host[s0 + i];
       chunks += (len + kChunk - 1) / kChunk;
     }
-    ip->chunk_off[ns] = cp->chunk_off[ns] = chunks;
-    ip->tok_off[ns] = cp->tok_off[ns] = cu_host[s0 + ns];
-    ip->num_seqs = ns;
+    cp->chunk_off[ns] = chunks;
+    cp->tok_off[ns] = cu_host[s0 + ns];
     cp->num_seqs = ns;
     cp->seq0 = s0;
     idx.resize(ns);
@@ -123,8 +121,23 @@ cudaError_t launch_chunk_prefill(const ChunkArgs &a, const int32_t *cu_host, uin
       return cp->chunk_off[x + 1] - cp->chunk_off[x] > cp->chunk_off[y + 1] - cp->chunk_off[y];
     });
     for (int i = 0; i < ns; ++i) cp->order[i] = static_cast<uint16_t>(idx[i]);
-    cudaError_t e = launch_chunk_intra(*ip, chunks, stream);
-    if (e != cudaSuccess) return e;
+    // intra-chunk launches over runs of at most kMaxSlotsPerLaunch chunk slots, each with its slot table
+    cudaError_t e = cudaSuccess;
+    for (int g0 = 0; g0 < chunks; g0 += kMaxSlotsPerLaunch) {
+      const int ng = std::min(kMaxSlotsPerLaunch, chunks - g0);
+      // the sequence holding slot g0, then its chunks in order
+      int i = static_cast<int>(std::upper_bound(cp->chunk_off, cp->chunk_off + ns + 1, g0) - cp->chunk_off) - 1;
+      for (int g = 0; g < ng; ++g) {
+        while (cp->chunk_off[i + 1] <= g0 + g) ++i;
+        const int j = g0 + g - cp->chunk_off[i];
+        const int t = cp->tok_off[i] + j * kChunk;
+        ip->slot_tok0[g] = t;
+        ip->slot_valid[g] = static_cast<uint8_t>(std::min(kChunk, cp->tok_off[i + 1] - t));
+      }
+      ip->blocks = blocks + static_cast<size_t>(g0) * a.H * kBlkBytes;
+      e = launch_chunk_intra(*ip, ng, stream);
+      if (e != cudaSuccess) return e;
+    }
     e = launch_chunk_chain(*cp, stream);
     if (e != cudaSuccess) return e;
   }

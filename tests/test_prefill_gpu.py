@@ -90,3 +90,13 @@ def test_more_sequences_than_one_launch_plans():
     inp = inputs.prefill_inputs("many_seqs", lens, 2, seed=62, pool_slots=1100, load_initial=True,
                                 final_to_pool=True)
     _parity(inp)
+
+
+def test_more_chunk_slots_than_one_intra_launch():
+    # 80 sequences of 3000..4000 tokens, H = 1: about 4400 chunk slots, so the intra-chunk work is split over
+    # two launches and the second one starts inside a sequence
+    rng = np.random.default_rng(71)
+    lens = [int(x) for x in rng.integers(3000, 4001, size=80)]
+    inp = inputs.prefill_inputs("many_slots", lens, 1, seed=72, pool_slots=96, load_initial=True)
+    assert sum((n + 63) // 64 for n in lens) > 4096
+    _parity(inp)
