@@ -37,6 +37,8 @@
 // swizzle phases.
 #include <cuda.h>
 
+#include <type_traits>
+
 #include "kda_common.cuh"
 #include "kda_internal.h"
 #include "kda_prefill_block.h"
@@ -128,7 +130,8 @@ struct BlockFactors {
   float2 ems;     // scale e^(m_R)
   float2 el;      // e^(b_63 - m_R)
   float2 eg;      // e^(a_R - m_R), a_R = b at row 15 of block R
-  float2 cr[4];   // e^(m_R2 - a_R) for R2 > R (both factors of B_R2 stay <= 1)
+  float2 cr[4];   // e^(m_R2 - a_R) for R2 > R; applied after eg, since k^ e^(a_R - b) <= |k^| keeps the
+                  // product representable where eg cr alone (up to 2^-230 at lower_bound -10) is not
 };
 
 // Operand rows of 8 tokens (rows t0 .. t0+7 of block R) for key channels
@@ -171,7 +174,7 @@ __device__ __forceinline__ void build_rows(const uint32_t (&kr)[8], const uint32
 #pragma unroll
     for (int j = 0; j < 8; ++j) v[j] = mul2(v[j], f.eg);  // k^ e^(a_R - b) <= |k^|
 #pragma unroll
-    for (int R2 = R + 1; R2 < 4; ++R2) {
+    for (int R2 = R + 1; R2 < 4; ++R2) {                  // k^ e^(m_R2 - b) for the later blocks R2
 #pragma unroll
       for (int j = 0; j < 8; ++j) w[j] = mul2(v[j], f.cr[R2]);
       put8(sm + OFF_GB, 128, p, gb_col0(R2) + t0, w);
@@ -332,25 +335,29 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_c
       gam[p] = fast_exp2(tot.x);
       gam[64 + p] = fast_exp2(tot.y);
     }
-    auto factors = [&](int R) {
+    // the factors of block R (a compile-time block index, so only the later blocks' factors exist)
+    auto factors = [&](auto Rc) {
+      constexpr int R = decltype(Rc)::value;
       BlockFactors f;
       f.em = exp2_2(m[R]);
       f.ems = make_float2(f.em.x * prm.scale, f.em.y * prm.scale);
       f.el = exp2_2(make_float2(tot.x - m[R].x, tot.y - m[R].y));
       f.eg = exp2_2(hh[1][R]);
 #pragma unroll
-      for (int R2 = 0; R2 < 4; ++R2)
-        f.cr[R2] = R2 > R ? exp2_2(make_float2(fminf(m[R2].x - a[R].x, 0.f), fminf(m[R2].y - a[R].y, 0.f)))
-                          : make_float2(0.f, 0.f);
+      for (int R2 = R + 1; R2 < 4; ++R2)
+        f.cr[R2] = exp2_2(make_float2(fminf(m[R2].x - a[R].x, 0.f), fminf(m[R2].y - a[R].y, 0.f)));
       return f;
     };
-    const BlockFactors fa = factors(Ra), fb = factors(Rb);
+    using R0 = std::integral_constant<int, 0>;
+    using R1 = std::integral_constant<int, 1>;
+    using R2c = std::integral_constant<int, 2>;
+    using R3 = std::integral_constant<int, 3>;
     if (Ra == 0) {
-      build_rows<0>(kr[0], qr[0], x[0], 8 * hf, p, s_nq, s_nk, fa, sm, qp[0], kq[0]);
-      build_rows<3>(kr[1], qr[1], x[1], 48 + 8 * hf, p, s_nq, s_nk, fb, sm, qp[1], kq[1]);
+      build_rows<0>(kr[0], qr[0], x[0], 8 * hf, p, s_nq, s_nk, factors(R0{}), sm, qp[0], kq[0]);
+      build_rows<3>(kr[1], qr[1], x[1], 48 + 8 * hf, p, s_nq, s_nk, factors(R3{}), sm, qp[1], kq[1]);
     } else {
-      build_rows<1>(kr[0], qr[0], x[0], 16 + 8 * hf, p, s_nq, s_nk, fa, sm, qp[0], kq[0]);
-      build_rows<2>(kr[1], qr[1], x[1], 32 + 8 * hf, p, s_nq, s_nk, fb, sm, qp[1], kq[1]);
+      build_rows<1>(kr[0], qr[0], x[0], 16 + 8 * hf, p, s_nq, s_nk, factors(R1{}), sm, qp[0], kq[0]);
+      build_rows<2>(kr[1], qr[1], x[1], 32 + 8 * hf, p, s_nq, s_nk, factors(R2c{}), sm, qp[1], kq[1]);
     }
   }
   fence_async_smem();
