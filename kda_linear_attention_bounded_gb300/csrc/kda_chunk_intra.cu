@@ -58,6 +58,10 @@ constexpr uint32_t OFF_FQ = 0;        // [F | Q]: 128 rows rho x (64 + 64) token
 constexpr uint32_t OFF_GB = 32768;    // [G | B_1 | B_2 | B_3]: 128 rows rho x 160 tokens in 3 panels (48 KB)
 constexpr uint32_t OFF_KP = 81920;    // K+^T = (k^ o e^b)^T: 128 rows rho x 64 tokens, K-major A operand (16 KB)
 constexpr uint32_t OFF_QIN = 0, OFF_KIN = 16384, OFF_GIN = 32768;   // TMA tiles, consumed before the operands are written
+// the q, k, g tiles are unswizzled (only CUDA cores read them): two 64-channel boxes of 64 rows x 128 bytes
+__device__ __forceinline__ uint32_t in_offset(int r, int c) {
+  return static_cast<uint32_t>((c >> 6) * 8192 + r * 128 + (c & 63) * 2);
+}
 // after the A/P product
 constexpr uint32_t OFF_QST = 0;       // Q+^T rows of the block (16 KB), stored by bulk copy
 constexpr uint32_t OFF_PKST = 16384;  // [P ; K'^T] rows of the block (24 KB), stored by bulk copy; then ...
@@ -242,13 +246,16 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_c
 
   // ------------------------------------------------------------ l2 norms (token-major)
   {
+    // thread = (row r, quarter `part` of the channels); the 16-byte chunks of a quarter are visited in a
+    // rotated order so that the eight threads of each quarter-warp read eight different bank groups
     const int r = tid >> 2, part = tid & 3;
+    const int rot = (r & 1) * 2 + (part >> 1);
     float2 sq = make_float2(0.f, 0.f), sk = make_float2(0.f, 0.f);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const int c = 32 * part + 8 * j;
-      const uint4 wq = *reinterpret_cast<const uint4 *>(sm + OFF_QIN + swz_offset(64, r, c));
-      const uint4 wk = *reinterpret_cast<const uint4 *>(sm + OFF_KIN + swz_offset(64, r, c));
+      const int c = 32 * part + 8 * ((j + rot) & 3);
+      const uint4 wq = *reinterpret_cast<const uint4 *>(sm + OFF_QIN + in_offset(r, c));
+      const uint4 wk = *reinterpret_cast<const uint4 *>(sm + OFF_KIN + in_offset(r, c));
       const uint32_t aq[4] = {wq.x, wq.y, wq.z, wq.w}, ak[4] = {wk.x, wk.y, wk.z, wk.w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
@@ -285,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_c
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const int r = t0 + j;
-      const uint32_t off = swz_offset(64, r, c0);
+      const uint32_t off = in_offset(r, c0);
       kr[bi][j] = ld_u32(sm + OFF_KIN + off);
       qr[bi][j] = ld_u32(sm + OFF_QIN + off);
       const float2 gg = unpack_bf16x2(ld_u32(sm + OFF_GIN + off));

@@ -71,7 +71,8 @@ constexpr int kMaxSlotsPerLaunch = 4096;
 
 // Intra-chunk kernel: one CTA per (chunk slot, head) of a run of consecutive chunk slots.
 struct IntraParams {
-  CUtensorMap tq, tk, tv, tg;   // [tokens, H, 128] bf16, box 64 channels x 1 head x 64 tokens
+  CUtensorMap tq, tk, tv, tg;   // [tokens, H, 128] bf16, box 64 channels x 1 head x 64 tokens; q, k, g
+                                // unswizzled, v with the 128-byte swizzle
   const uint16_t *beta;
   int64_t beta_stride;
   const float *A_log, *dt_bias;

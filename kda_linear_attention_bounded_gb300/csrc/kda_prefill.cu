@@ -34,9 +34,11 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// [tokens, H, 128] bf16 with the given token stride; box = 64 channels x 1 head x 64 tokens,
-// 128-byte swizzle (the row-swizzled tile layout); rows past the tensor's end read as zero
-bool make_token_map(CUtensorMap *map, const void *base, int H, int total_tokens, int64_t token_stride) {
+// [tokens, H, 128] bf16 with the given token stride; box = 64 channels x 1 head x 64 tokens, with the
+// 128-byte swizzle (the row-swizzled tile layout of the MMA operands and the output staging) or
+// unswizzled (tiles read only by CUDA cores); rows past the tensor's end read as zero
+bool make_token_map(CUtensorMap *map, const void *base, int H, int total_tokens, int64_t token_stride,
+                    bool swizzled = true) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(H),
@@ -45,7 +47,8 @@ bool make_token_map(CUtensorMap *map, const void *base, int H, int total_tokens,
   cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(kChunk)};
   cuuint32_t estr[3] = {1, 1, 1};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, swizzled ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -69,10 +72,10 @@ cudaError_t launch_chunk_prefill(const ChunkArgs &a, const int32_t *cu_host, uin
     ip = new IntraParams();
     cp = new ChainParams();
   }
-  if (!make_token_map(&ip->tq, a.q, a.H, a.total_tokens, a.qkv_stride) ||
-      !make_token_map(&ip->tk, a.k, a.H, a.total_tokens, a.qkv_stride) ||
+  if (!make_token_map(&ip->tq, a.q, a.H, a.total_tokens, a.qkv_stride, false) ||
+      !make_token_map(&ip->tk, a.k, a.H, a.total_tokens, a.qkv_stride, false) ||
       !make_token_map(&ip->tv, a.v, a.H, a.total_tokens, a.qkv_stride) ||
-      !make_token_map(&ip->tg, a.g, a.H, a.total_tokens, a.g_stride) ||
+      !make_token_map(&ip->tg, a.g, a.H, a.total_tokens, a.g_stride, false) ||
       !make_token_map(&cp->tout, a.out, a.H, a.total_tokens, a.out_stride))
     return cudaErrorInvalidValue;
   ip->beta = a.beta;
