@@ -56,7 +56,7 @@ constexpr int kThreads = 256;   // 8 warps; two CTAs per SM
 // prologue .. A/P product
 constexpr uint32_t OFF_FQ = 0;        // [F | Q]: 128 rows rho x (64 + 64) tokens, MN-major A operand (32 KB)
 constexpr uint32_t OFF_GB = 32768;    // [G | B_1 | B_2 | B_3]: 128 rows rho x 160 tokens in 3 panels (48 KB)
-constexpr uint32_t OFF_KP = 81920;    // K+^T = (k^ o e^b)^T: 128 rows rho x 64 tokens, K-major A operand (16 KB)
+constexpr uint32_t OFF_KP = 82944;    // K+^T = (k^ o e^b)^T: 128 rows rho x 64 tokens, K-major A operand (16 KB)
 constexpr uint32_t OFF_QIN = 0, OFF_KIN = 16384, OFF_GIN = 32768;   // TMA tiles, consumed before the operands are written
 // the q, k, g tiles are unswizzled (only CUDA cores read them): two 64-channel boxes of 64 rows x 128 bytes
 __device__ __forceinline__ uint32_t in_offset(int r, int c) {
@@ -64,13 +64,13 @@ __device__ __forceinline__ uint32_t in_offset(int r, int c) {
 }
 // after the A/P product
 constexpr uint32_t OFF_QST = 0;       // Q+^T rows of the block (16 KB), stored by bulk copy
-constexpr uint32_t OFF_PKST = 16384;  // [P ; K'^T] rows of the block (24 KB), stored by bulk copy; then ...
-constexpr uint32_t OFF_T = 16384;     // ... T bf16 K-major [t][t']
+constexpr uint32_t OFF_PKST = 16384;  // [P ; K'^T] rows of the block (24 KB), stored by bulk copy
 constexpr uint32_t OFF_A = 40960;     // A fp32 [64][68], turned into (I + A)^-1 in place
 constexpr uint32_t OFF_VIN = 58368;   // v tile (TMA) [token][value channel]
+constexpr uint32_t OFF_T = 74752;     // T bf16 K-major [t][t'] (8 KB), written by the inverse's steps
 // after the W / U^ products
 constexpr uint32_t OFF_WST = 40960, OFF_UST = 57344;   // W^T and U^^T rows of the block
-constexpr uint32_t OFF_SMALL = 98304;
+constexpr uint32_t OFF_SMALL = 99328;
 constexpr uint32_t SM_NQ = 0, SM_NK = 256, SM_BETA = 512, SM_H = 768 /* [2][4][128] f32 */,
                    SM_BAR = 4864, SM_TMEM = 4888, SM_ABORT = 4892, SM_END = 4928;
 constexpr int kCopyThread = 128;      // issues the block's early bulk stores (Q+, [P ; K'])
@@ -127,6 +127,15 @@ __device__ __forceinline__ void st_16x8(float *D, const float (&d)[4], float sgn
   const int g = lane >> 2, t = lane & 3;
   *reinterpret_cast<float2 *>(D + g * kAStride + 2 * t) = make_float2(sgn * d[0], sgn * d[1]);
   *reinterpret_cast<float2 *>(D + (g + 8) * kAStride + 2 * t) = make_float2(sgn * d[2], sgn * d[3]);
+}
+
+// the same 16 x 8 tile, times sgn and the column's beta, as bf16 pairs into T (K-major, 128-byte swizzle)
+__device__ __forceinline__ void st_16x8_t(uint8_t *tT, int row0, int col0, const float (&d)[4], float sgn,
+                                          const float *s_beta, int lane) {
+  const int g = lane >> 2, c = col0 + 2 * (lane & 3);
+  const float b0 = sgn * s_beta[c], b1 = sgn * s_beta[c + 1];
+  *reinterpret_cast<uint32_t *>(tT + swz_offset(64, row0 + g, c)) = pack_bf16x2(d[0] * b0, d[1] * b1);
+  *reinterpret_cast<uint32_t *>(tT + swz_offset(64, row0 + g + 8, c)) = pack_bf16x2(d[2] * b0, d[3] * b1);
 }
 
 struct BlockFactors {
@@ -470,10 +479,18 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_c
   //   L^-1_10 = -D_1 A_10 D_0,  L^-1_32 = -D_3 A_32 D_2,
   //   L^-1 (rows 32..63, cols 0..31) = -I_2 A_(23,01) I_1,  I_1, I_2 the inverses of the diagonal 32x32 halves.
   // Everything happens in place in the A tile: each block of the inverse overwrites the block of A
-  // that is no longer needed, and the temporaries live in its unused strictly-upper part.
+  // that is no longer needed, and the temporaries live in its unused strictly-upper part.  Each step also
+  // writes its block of T = L^-1 Diag(beta) in bf16; the six blocks above the diagonal of T are zero.
   {
     float *sA = reinterpret_cast<float *>(sm + OFF_A);
     float *sInv = sA;
+    uint8_t *tT = sm + OFF_T;
+    if (tid < 192) {   // zero blocks (I, J), J > I: 6 blocks x 16 rows x two 16-byte chunks
+      const int b6 = tid >> 5, rr = (tid >> 1) & 15, hc = tid & 1;
+      const int I = b6 < 3 ? 0 : b6 < 5 ? 1 : 2;
+      const int J = b6 < 3 ? b6 + 1 : b6 < 5 ? b6 - 1 : 3;
+      *reinterpret_cast<uint4 *>(tT + swz_offset(64, 16 * I + rr, 16 * J + 8 * hc)) = make_uint4(0, 0, 0, 0);
+    }
     // D_R: task (block R, column jc) = 8 warp + lane / 4, so warps 2R and 2R + 1 share block R; lane
     // q = lane % 4 of a task carries rows q, q + 4, q + 8, q + 12 of its column.  Right-looking: at step m
     // the lane holding row m broadcasts x_m to its task's lanes, and every later row takes one FMA.
@@ -498,8 +515,13 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_c
         case 2: named_bar_sync<3>(64); break;
         default: named_bar_sync<4>(64); break;
       }
+      const float bc = s_beta[16 * R + jc];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) sInv[(16 * R + 4 * i + q) * kAStride + 16 * R + jc] = xs[i];
+      for (int i = 0; i < 4; ++i) {
+        sInv[(16 * R + 4 * i + q) * kAStride + 16 * R + jc] = xs[i];
+        *reinterpret_cast<uint16_t *>(tT + swz_offset(64, 16 * R + 4 * i + q, 16 * R + jc)) =
+            f32_to_bf16_bits(xs[i] * bc);
+      }
     }
     __syncthreads();
     // Every block product below is a set of 16 x 8 output tiles, one per warp task, on TF32
@@ -517,6 +539,7 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_c
       float e[4] = {0.f, 0.f, 0.f, 0.f};
       mm_16x8(e, sInv + (lo + 16) * kAStride + lo + 16, sA + lo * kAStride + lo + 16 + 8 * nj, 2, lane);
       st_16x8(sInv + (lo + 16) * kAStride + lo + 8 * nj, e, -1.f, lane);
+      st_16x8_t(tT, lo + 16, lo + 8 * nj, e, -1.f, s_beta, lane);
     }
     __syncthreads();
     // Z = A_(23,01) I_1 (32 x 32) -> A tile rows 0..31, cols 32..63; warp = (16-row half mi, 8 columns nj).
@@ -529,35 +552,13 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_c
       st_16x8(sA + (16 * mi) * kAStride + 32 + 8 * nj, d, 1.f, lane);
     }
     __syncthreads();
-    // L^-1 (rows 32..63, cols 0..31) = -I_2 Z; I_2 is block-lower: its rows 0..15 only see Z rows 0..15
+    // L^-1 (rows 32..63, cols 0..31) = -I_2 Z; I_2 is block-lower: its rows 0..15 only see Z rows 0..15.
+    // Only T is written: nothing reads this block of the inverse afterwards.
     {
       const int mi = warp >> 2, nj = warp & 3;
       float d[4] = {0.f, 0.f, 0.f, 0.f};
       mm_16x8(d, sInv + (32 + 16 * mi) * kAStride + 32, sA + 32 + 8 * nj, mi ? 4 : 2, lane);
-      st_16x8(sInv + (32 + 16 * mi) * kAStride + 8 * nj, d, -1.f, lane);
-    }
-    if (tid == kCopyThread) bulk_wait_read();   // T goes over the [P ; K'] staging tile next
-    __syncthreads();
-    // T = Inv Diag(beta) in bf16, zero above the diagonal (the upper part of sInv is never written):
-    // thread = (row r, 16-column group); consecutive rows per warp keep the 16-byte loads conflict-free
-    {
-      const int r = tid & 63, cg = tid >> 6;
-      const float *irow = sInv + r * kAStride + 16 * cg;
-#pragma unroll
-      for (int k8 = 0; k8 < 2; ++k8) {
-        const float4 i0 = *reinterpret_cast<const float4 *>(irow + 8 * k8);
-        const float4 i1 = *reinterpret_cast<const float4 *>(irow + 8 * k8 + 4);
-        const float iv[8] = {i0.x, i0.y, i0.z, i0.w, i1.x, i1.y, i1.z, i1.w};
-        float t8[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int c = 16 * cg + 8 * k8 + e;
-          t8[e] = c <= r ? iv[e] * s_beta[c] : 0.f;
-        }
-        *reinterpret_cast<uint4 *>(sm + OFF_T + swz_offset(64, r, 16 * cg + 8 * k8)) =
-            make_uint4(pack_bf16x2(t8[0], t8[1]), pack_bf16x2(t8[2], t8[3]), pack_bf16x2(t8[4], t8[5]),
-                       pack_bf16x2(t8[6], t8[7]));
-      }
+      st_16x8_t(tT, 32 + 16 * mi, 8 * nj, d, -1.f, s_beta, lane);
     }
   }
   fence_async_smem();
@@ -620,6 +621,7 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_c
     bulk_commit();
     bulk_wait_read();
   }
+  if (tid == kCopyThread) bulk_wait_read();   // the Q+ and [P ; K'] rows stored after the A/P read-out
   if (warp == 0) {
     __syncwarp();
     tc_fence_after();
