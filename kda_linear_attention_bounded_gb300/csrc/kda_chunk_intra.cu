@@ -152,15 +152,15 @@ struct BlockFactors {
 // rows come back packed (qp, kq: rows p and 64 + p) and are stored once the
 // operand tiles are free.
 template <int R>
-__device__ __forceinline__ void build_rows(const uint32_t (&kr)[8], const uint32_t (&qr)[8], const float2 (&x)[8],
+__device__ __forceinline__ void build_rows(const uint32_t (&kqw)[16], const float2 (&x)[8],
                                            int t0, int p, const float *s_nq, const float *s_nk,
                                            const BlockFactors &f, uint8_t *sm, uint4 (&qp)[2], uint4 (&kq)[2]) {
   float2 kh[8], qh[8], e[8], ie[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     const float nk = s_nk[t0 + j], nq = s_nq[t0 + j];
-    kh[j] = mul2(unpack_bf16x2(kr[j]), make_float2(nk, nk));
-    qh[j] = mul2(unpack_bf16x2(qr[j]), make_float2(nq, nq));
+    kh[j] = mul2(unpack_bf16x2(kqw[j]), make_float2(nk, nk));
+    qh[j] = mul2(unpack_bf16x2(kqw[8 + j]), make_float2(nq, nq));
     e[j] = exp2_2(x[j]);
     ie[j] = exp2_2(make_float2(-x[j].x, -x[j].y));
   }
@@ -291,19 +291,22 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_c
   const float lb2 = prm.lower_bound * kLog2e;
   const float2 nd = make_float2(nea * dtb.x, nea * dtb.y);
   const float2 nea2 = make_float2(nea, nea), lb22 = make_float2(lb2, lb2), one2 = make_float2(1.f, 1.f);
-  uint32_t kr[2][8], qr[2][8];
   float2 x[2][8];   // (b_t - m_R) log2(e), rows t0 .. t0+7 of each of the two blocks
+  // the thread's k and q words of each block wait in TMEM (its lane, 16 columns per block) until the operand
+  // tiles are built: the input tiles are overwritten there, and registers are short
+  const uint32_t stash = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + 32 * (warp >> 2);
 #pragma unroll
   for (int bi = 0; bi < 2; ++bi) {
     const int R = bi ? Rb : Ra;
     const int t0 = 16 * R + 8 * hf;
     float2 lam[8];
+    uint32_t kq[16];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const int r = t0 + j;
       const uint32_t off = in_offset(r, c0);
-      kr[bi][j] = ld_u32(sm + OFF_KIN + off);
-      qr[bi][j] = ld_u32(sm + OFF_QIN + off);
+      kq[j] = ld_u32(sm + OFF_KIN + off);
+      kq[8 + j] = ld_u32(sm + OFF_QIN + off);
       const float2 gg = unpack_bf16x2(ld_u32(sm + OFF_GIN + off));
       // lambda = lb2 / (1 + 2^(nea g + nea dtb)), channel pairs in packed fp32x2
       const float2 ex = exp2_2(fma2(gg, nea2, nd));
@@ -327,7 +330,9 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_c
       hs = acc;
     }
     *reinterpret_cast<float2 *>(s_h + (hf * 4 + R) * kD + c0) = hs;
+    tmem_st16(stash + 16 * bi, kq);
   }
+  tmem_wait_st();
   __syncthreads();   // norms, half sums visible; q, k, g tiles fully read
 
   // ------------------------------------------------------------ anchors and operand tiles
@@ -368,12 +373,23 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_c
     using R1 = std::integral_constant<int, 1>;
     using R2c = std::integral_constant<int, 2>;
     using R3 = std::integral_constant<int, 3>;
+    // the k and q words of block bi back from TMEM
+    auto words = [&](int bi, uint32_t (&kqw)[16]) {
+      tmem_ld16_async(stash + 16 * bi, kqw);
+      tmem_wait_ld();
+      tmem_tie<16>(kqw);
+    };
+    uint32_t kqw[16];
     if (Ra == 0) {
-      build_rows<0>(kr[0], qr[0], x[0], 8 * hf, p, s_nq, s_nk, factors(R0{}), sm, qp[0], kq[0]);
-      build_rows<3>(kr[1], qr[1], x[1], 48 + 8 * hf, p, s_nq, s_nk, factors(R3{}), sm, qp[1], kq[1]);
+      words(0, kqw);
+      build_rows<0>(kqw, x[0], 8 * hf, p, s_nq, s_nk, factors(R0{}), sm, qp[0], kq[0]);
+      words(1, kqw);
+      build_rows<3>(kqw, x[1], 48 + 8 * hf, p, s_nq, s_nk, factors(R3{}), sm, qp[1], kq[1]);
     } else {
-      build_rows<1>(kr[0], qr[0], x[0], 16 + 8 * hf, p, s_nq, s_nk, factors(R1{}), sm, qp[0], kq[0]);
-      build_rows<2>(kr[1], qr[1], x[1], 32 + 8 * hf, p, s_nq, s_nk, factors(R2c{}), sm, qp[1], kq[1]);
+      words(0, kqw);
+      build_rows<1>(kqw, x[0], 16 + 8 * hf, p, s_nq, s_nk, factors(R1{}), sm, qp[0], kq[0]);
+      words(1, kqw);
+      build_rows<2>(kqw, x[1], 32 + 8 * hf, p, s_nq, s_nk, factors(R2c{}), sm, qp[1], kq[1]);
     }
   }
   fence_async_smem();
