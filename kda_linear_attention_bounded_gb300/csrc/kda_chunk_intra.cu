@@ -292,8 +292,9 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_c
   const float2 nd = make_float2(nea * dtb.x, nea * dtb.y);
   const float2 nea2 = make_float2(nea, nea), lb22 = make_float2(lb2, lb2), one2 = make_float2(1.f, 1.f);
   float2 x[2][8];   // (b_t - m_R) log2(e), rows t0 .. t0+7 of each of the two blocks
-  // the thread's k and q words of each block wait in TMEM (its lane, 16 columns per block) until the operand
-  // tiles are built: the input tiles are overwritten there, and registers are short
+  // the thread's k and q words and its decay exponents of each block wait in TMEM (its lane; columns 0..127,
+  // 16 per block and kind) until the operand tiles are built: the input tiles are overwritten there, and
+  // registers are short
   const uint32_t stash = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + 32 * (warp >> 2);
 #pragma unroll
   for (int bi = 0; bi < 2; ++bi) {
@@ -331,6 +332,7 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_c
     }
     *reinterpret_cast<float2 *>(s_h + (hf * 4 + R) * kD + c0) = hs;
     tmem_st16(stash + 16 * bi, kq);
+    tmem_st16(stash + 64 + 16 * bi, reinterpret_cast<const float *>(x[bi]));
   }
   tmem_wait_st();
   __syncthreads();   // norms, half sums visible; q, k, g tiles fully read
@@ -375,9 +377,14 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_c
     using R3 = std::integral_constant<int, 3>;
     // the k and q words of block bi back from TMEM
     auto words = [&](int bi, uint32_t (&kqw)[16]) {
+      uint32_t xw[16];
       tmem_ld16_async(stash + 16 * bi, kqw);
+      tmem_ld16_async(stash + 64 + 16 * bi, xw);
       tmem_wait_ld();
       tmem_tie<16>(kqw);
+      tmem_tie<16>(xw);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) x[bi][j] = make_float2(__uint_as_float(xw[2 * j]), __uint_as_float(xw[2 * j + 1]));
     };
     uint32_t kqw[16];
     if (Ra == 0) {
@@ -391,6 +398,11 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_c
       words(1, kqw);
       build_rows<2>(kqw, x[1], 32 + 8 * hf, p, s_nq, s_nk, factors(R2c{}), sm, qp[1], kq[1]);
     }
+    // the packed Q+ and K' rows wait in TMEM columns 160..223 (beside the product's 160) until the
+    // operand tiles are free
+    tmem_st16(stash + 160, reinterpret_cast<const uint32_t *>(qp));
+    tmem_st16(stash + 176, reinterpret_cast<const uint32_t *>(kq));
+    tmem_wait_st();
   }
   fence_async_smem();
   tc_fence_before();
@@ -427,6 +439,19 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_c
     tma_load_3d(sm + OFF_VIN + 8192, &prm.tv, 64, h, tok0, bar_v);
   }
   // the block's Q+ and K' rows go to their staging tiles
+  {
+    uint32_t w[32];
+    tmem_ld16_async(stash + 160, w);
+    tmem_ld16_async(stash + 176, w + 16);
+    tmem_wait_ld();
+    tmem_tie<32>(w);
+    const uint4 *wq = reinterpret_cast<const uint4 *>(w);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      (&qp[0][0])[i] = wq[i];
+      (&kq[0][0])[i] = wq[4 + i];
+    }
+  }
 #pragma unroll
   for (int bi = 0; bi < 2; ++bi) {
     const int t0 = 16 * (bi ? Rb : Ra) + 8 * hf;
