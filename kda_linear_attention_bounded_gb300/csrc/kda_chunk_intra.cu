@@ -235,7 +235,7 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_c
     tma_load_3d(sm + OFF_GIN, &prm.tg, 0, h, tok0, bar_in);
     tma_load_3d(sm + OFF_GIN + 8192, &prm.tg, 64, h, tok0, bar_in);
   }
-  if (warp == 0) {
+  if (warp == 1) {   // TMEM by warp 1, beside thread 0's barrier set-up and TMA issue
     tmem_alloc(s_tmem, kTmemCols);
     tmem_relinquish();
   }
@@ -663,7 +663,7 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_c
     bulk_wait_read();
   }
   if (tid == kCopyThread) bulk_wait_read();   // the Q+ and [P ; K'] rows stored after the A/P read-out
-  if (warp == 0) {
+  if (warp == 1) {   // the allocating warp, not held by thread 0's wait for its bulk stores
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
