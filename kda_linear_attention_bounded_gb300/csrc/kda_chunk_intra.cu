@@ -72,7 +72,7 @@ constexpr uint32_t OFF_T = 74752;     // T bf16 K-major [t][t'] (8 KB), written 
 constexpr uint32_t OFF_WST = 40960, OFF_UST = 57344;   // W^T and U^^T rows of the block
 constexpr uint32_t OFF_SMALL = 99328;
 constexpr uint32_t SM_NQ = 0, SM_NK = 256, SM_BETA = 512, SM_H = 768 /* [2][4][128] f32 */,
-                   SM_BAR = 4864, SM_TMEM = 4888, SM_ABORT = 4892, SM_END = 4928;
+                   SM_BAR = 4864, SM_TMEM = 4888, SM_ABORT = 4892, SM_BARU = 4896, SM_END = 4928;
 constexpr int kCopyThread = 128;      // issues the block's early bulk stores (Q+, [P ; K'])
 constexpr uint32_t kSmemBytes = OFF_SMALL + SM_END + 1024;   // + alignment slack
 static_assert(2 * (kSmemBytes + 1024) <= 233472, "two CTAs per SM");
@@ -206,6 +206,7 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_c
   uint64_t *bar_in = reinterpret_cast<uint64_t *>(small + SM_BAR);
   uint64_t *bar_v = bar_in + 1;
   uint64_t *bar_mma = bar_in + 2;
+  uint64_t *bar_u = reinterpret_cast<uint64_t *>(small + SM_BARU);
   uint32_t *s_tmem = reinterpret_cast<uint32_t *>(small + SM_TMEM);
   volatile uint32_t *s_abort = reinterpret_cast<volatile uint32_t *>(small + SM_ABORT);
 
@@ -225,6 +226,7 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_c
     mbar_init(bar_in, 1);
     mbar_init(bar_v, 1);
     mbar_init(bar_mma, 1);
+    mbar_init(bar_u, 1);
     *s_abort = 0;
     fence_mbar_init();
     mbar_arrive_expect_tx(bar_in, 3 * 16384);
@@ -607,8 +609,11 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_c
   __syncthreads();
 
   // ------------------------------------------------------------ W^T = K+^T T^T, U^^T = V^T T^T
-  wait_or_abort(bar_v, 0, s_abort, prm.status);
-  if (valid < kC) {   // rows past the sequence end: T's columns there are 0, but v may hold anything
+  // W^T (which needs no v) commits onto bar_mma, U^^T onto bar_u; each half of the warps then stages and
+  // stores its own rows, so W^T leaves while U^^T is still being formed
+  const bool ragged = valid < kC;
+  if (ragged) {   // rows past the sequence end: T's columns there are 0, but v may hold anything
+    wait_or_abort(bar_v, 0, s_abort, prm.status);
     for (int idx = tid; idx < (kC - valid) * 16; idx += kThreads) {
       const int r2 = valid + idx / 16, cc = idx % 16;
       *reinterpret_cast<uint4 *>(sm + OFF_VIN + swz_offset(64, r2, 8 * cc)) = make_uint4(0, 0, 0, 0);
@@ -625,17 +630,19 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_c
     const uint64_t tt = desc_kmajor_base(smem_u32(sm + OFF_T));
 #pragma unroll
     for (int s = 0; s < 4; ++s) mma_bf16(tmem, kp + kmajor_step(128, s), tt + kmajor_step(64, s), id_w, s > 0);
+    mma_commit(bar_mma);
+    if (!ragged) wait_or_abort(bar_v, 0, s_abort, prm.status);
 #pragma unroll
     for (int s = 0; s < 4; ++s) mma_bf16(tmem + 64, vv + mnmajor_step(s), tt + kmajor_step(64, s), id_u, s > 0);
-    mma_commit(bar_mma);
+    mma_commit(bar_u);
   }
   __syncwarp();
-  wait_or_abort(bar_mma, 1, s_abort, prm.status);
-  tc_fence_after();
   // ------------------------------------------------------------ W^T, U^^T rows to the staging tiles
   {
     // warp = (lane quadrant, W^T | U^^T); the thread's row is one 128-byte line of the block tile
     const int q4 = warp & 3, which = warp >> 2;
+    if (which) wait_or_abort(bar_u, 0, s_abort, prm.status); else wait_or_abort(bar_mma, 1, s_abort, prm.status);
+    tc_fence_after();
     const int row = q4 * 32 + lane;
     const uint32_t taddr = tmem + (static_cast<uint32_t>(q4 * 32) << 16) + (which ? 64u : 0u);
     uint32_t v[64];
@@ -651,19 +658,22 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_c
           make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
                      pack_bf16x2(f[6], f[7]));
     }
+    fence_async_smem();
+    tc_fence_before();
+    if (which) named_bar_sync<8>(128); else named_bar_sync<7>(128);   // this half's rows are staged
   }
-  fence_async_smem();
-  tc_fence_before();
-  __syncthreads();
   // ------------------------------------------------------------ block write-out, TMEM release
   if (tid == 0) {
     bulk_store(blk + kBlkWQ, sm + OFF_WST, 16384);
+    bulk_commit();
+  }
+  if (tid == kCopyThread) {
     bulk_store(blk + kBlkUH, sm + OFF_UST, 16384);
     bulk_commit();
-    bulk_wait_read();
   }
-  if (tid == kCopyThread) bulk_wait_read();   // the Q+ and [P ; K'] rows stored after the A/P read-out
-  if (warp == 1) {   // the allocating warp, not held by thread 0's wait for its bulk stores
+  __syncthreads();   // every TMEM read is done
+  if (tid == 0 || tid == kCopyThread) bulk_wait_read();
+  if (warp == 1) {   // the allocating warp, not held by the waits for the bulk stores
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
