@@ -19,12 +19,12 @@
 // U = U^ - W S solve (I + A) U = Diag(beta)(V - (k^ o e^b) S).
 //
 // exp(b_r - b_i) spans up to 64 |lower_bound| inside a chunk, far outside
-// fp32.  A and P are built from 16-row sub-blocks R with anchors m_R = b at
-// row 7 of block R:
-//   same block:   e^(b_r - b_i) = e^(b_r - m_R) e^(m_R - b_i)     (|exponents| <= 8 |lb|)
+// fp32.  A and P are built from sub-blocks R of 16 rows (32 rows when
+// lower_bound >= -5) with anchors m_R = b at the middle row of block R:
+//   same block:   e^(b_r - b_i) = e^(b_r - m_R) e^(m_R - b_i)     (|exponents| <= 8 |lb| or 16 |lb|)
 //   block I < R:  e^(b_r - b_i) = e^(b_r - m_R) e^(m_R - b_i)     (second factor <= 1)
-// so ONE 128 x 160 tcgen05.mma of [F; Q] = [k^; q^] o e^(b - m_R(row)) against
-// [G; B_1; B_2; B_3] (G = k^ o e^(m_R(row) - b); B_R = the rows of blocks < R
+// so ONE tcgen05.mma (128 x 160, or 128 x 96) of [F; Q] = [k^; q^] o e^(b - m_R(row))
+// against [G; B_1; ...] (G = k^ o e^(m_R(row) - b); B_R = the rows of blocks < R
 // times e^(m_R - b)) yields every block of A and P that is needed.  T comes
 // from blocked forward substitution (16x16 diagonal inverses on CUDA cores,
 // off-diagonal blocks with TF32 mma.sync), W^T and U^^T from two more
@@ -79,9 +79,18 @@ static_assert(2 * (kSmemBytes + 1024) <= 233472, "two CTAs per SM");
 constexpr int kAStride = 68;
 constexpr uint32_t kTmemCols = 256;   // A/P product: 160 columns; then W^T 0..63, U^^T 64..127
 
-// first column of B_R inside [G | B_1 | B_2 | B_3] (and of its product in TMEM)
-__host__ __device__ constexpr int gb_col0(int R) { return R == 1 ? 64 : R == 2 ? 80 : 112; }
-constexpr int kGBCols = 160;
+// Sub-blocks of BLK rows: 16, or 32 when lower_bound >= -5.  The anchored factors reach 2^(+-|x|) with |x| up to
+// (BLK / 2) |lb| log2(e); both the large and the small side must stay inside fp32 / bf16 with room for small
+// key components (2^-115.4 at the limit: 8 rows at |lb| = 10, or 16 rows at |lb| = 5; at 2^-127 the small
+// factor flushes to zero and entries of A are lost).  The stacked tile [G | B_1 | ...] holds B_R2 (the rows
+// of the blocks before R2, anchored at m_R2) from column gb_col0(R2); its width is gb_col0(64 / BLK).
+template <int BLK>
+__host__ __device__ constexpr int gb_col0(int R2) {
+  return BLK == 16 ? (R2 == 1 ? 64 : R2 == 2 ? 80 : R2 == 3 ? 112 : 160) : (R2 == 1 ? 64 : 96);
+}
+template <int BLK>
+constexpr int kGBCols = gb_col0<BLK>(64 / BLK);
+constexpr float kLowerBound32 = -5.0f;   // lower bounds >= this take the 32-row sub-blocks
 
 __device__ __forceinline__ uint32_t ld_u32(const uint8_t *p) { return *reinterpret_cast<const uint32_t *>(p); }
 
@@ -142,7 +151,7 @@ struct BlockFactors {
   float2 em;      // e^(m_R)
   float2 ems;     // scale e^(m_R)
   float2 el;      // e^(b_63 - m_R)
-  float2 eg;      // e^(a_R - m_R), a_R = b at row 15 of block R
+  float2 eg;      // e^(a_R - m_R), a_R = b at the last row of block R
   float2 cr[4];   // e^(m_R2 - a_R) for R2 > R; applied after eg, since k^ e^(a_R - b) <= |k^| keeps the
                   // product representable where eg cr alone (up to 2^-230 at lower_bound -10) is not
 };
@@ -151,7 +160,7 @@ struct BlockFactors {
 // (2p, 2p+1); x[j] = (b - m_R) log2(e) of those rows.  The block's Q+ and K'
 // rows come back packed (qp, kq: rows p and 64 + p) and are stored once the
 // operand tiles are free.
-template <int R>
+template <int R, int BLK>
 __device__ __forceinline__ void build_rows(const uint32_t (&kqw)[16], const float2 (&x)[8],
                                            int t0, int p, const float *s_nq, const float *s_nk,
                                            const BlockFactors &f, uint8_t *sm, uint4 (&qp)[2], uint4 (&kq)[2]) {
@@ -183,18 +192,19 @@ __device__ __forceinline__ void build_rows(const uint32_t (&kqw)[16], const floa
 #pragma unroll
   for (int j = 0; j < 8; ++j) w[j] = mul2(v[j], f.el);    // K' = G e^(b_63 - m_R)
   pack8(w, kq[0], kq[1]);
-  if (R < 3) {
+  if (R < 64 / BLK - 1) {
 #pragma unroll
     for (int j = 0; j < 8; ++j) v[j] = mul2(v[j], f.eg);  // k^ e^(a_R - b) <= |k^|
 #pragma unroll
-    for (int R2 = R + 1; R2 < 4; ++R2) {                  // k^ e^(m_R2 - b) for the later blocks R2
+    for (int R2 = R + 1; R2 < 64 / BLK; ++R2) {           // k^ e^(m_R2 - b) for the later blocks R2
 #pragma unroll
       for (int j = 0; j < 8; ++j) w[j] = mul2(v[j], f.cr[R2]);
-      put8(sm + OFF_GB, 128, p, gb_col0(R2) + t0, w);
+      put8(sm + OFF_GB, 128, p, gb_col0<BLK>(R2) + t0, w);
     }
   }
 }
 
+template <int BLK>
 __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_constant__ IntraParams prm) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -202,7 +212,7 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_c
   float *s_nq = reinterpret_cast<float *>(small + SM_NQ);
   float *s_nk = reinterpret_cast<float *>(small + SM_NK);
   float *s_beta = reinterpret_cast<float *>(small + SM_BETA);
-  float *s_h = reinterpret_cast<float *>(small + SM_H);     // [half][block][channel]: sum of lambda over 8 rows
+  float *s_h = reinterpret_cast<float *>(small + SM_H);     // [quarter][channel]: sum of lambda over 8 rows
   uint64_t *bar_in = reinterpret_cast<uint64_t *>(small + SM_BAR);
   uint64_t *bar_v = bar_in + 1;
   uint64_t *bar_mma = bar_in + 2;
@@ -287,8 +297,12 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_c
   }
 
   // ------------------------------------------------------------ gate and in-block decays
-  // thread = (channel pair p, 8-row half `hf` of the blocks Ra and Rb = 3 - Ra); warp-uniform blocks
+  // thread = (channel pair p, two 8-row quarters of the chunk); warp-uniform quarters.  16-row blocks: the
+  // half `hf` of blocks Ra and Rb = 3 - Ra; 32-row blocks: quarter `sel` of both blocks.  A quarter before
+  // its block's anchor takes its exponents as suffix sums up to its own last row, one after it as prefix sums
+  // from its own first row; with 32-row blocks the outer quarters then add a neighbour quarter's sum.
   const int hf = sel & 1, Ra = sel >> 1, Rb = 3 - Ra;
+  const bool before = BLK == 16 ? hf == 0 : sel < 2;
   const float nea = -__expf(prm.A_log[h]) * kLog2e;   // lambda = lb sigmoid(ea (g + dtb)); log2 units below
   const float lb2 = prm.lower_bound * kLog2e;
   const float2 nd = make_float2(nea * dtb.x, nea * dtb.y);
@@ -300,8 +314,9 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_c
   const uint32_t stash = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + 32 * (warp >> 2);
 #pragma unroll
   for (int bi = 0; bi < 2; ++bi) {
-    const int R = bi ? Rb : Ra;
-    const int t0 = 16 * R + 8 * hf;
+    const int R = BLK == 16 ? (bi ? Rb : Ra) : bi;
+    const int qd = BLK == 16 ? 2 * R + hf : 4 * bi + sel;   // the quarter: rows 8 qd .. 8 qd + 7
+    const int t0 = 8 * qd;
     float2 lam[8];
     uint32_t kq[16];
 #pragma unroll
@@ -318,12 +333,12 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_c
       lam[j] = r < valid ? l : make_float2(0.f, 0.f);
     }
     float2 hs;
-    if (hf == 0) {   // rows 0..7: b_t - m_R = -(lambda_{t+1} + ... + lambda_7)
+    if (before) {    // rows 0..7 of the quarter: b_t - (b at its last row) = -(lambda_{t+1} + ... + lambda_7)
       x[bi][7] = make_float2(0.f, 0.f);
 #pragma unroll
       for (int j = 6; j >= 0; --j) x[bi][j] = make_float2(x[bi][j + 1].x - lam[j + 1].x, x[bi][j + 1].y - lam[j + 1].y);
       hs = make_float2(lam[0].x - x[bi][0].x, lam[0].y - x[bi][0].y);
-    } else {         // rows 8..15: b_t - m_R = lambda_8 + ... + lambda_t
+    } else {         // b_t - (b before its first row) = lambda_0 + ... + lambda_t
       float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
@@ -332,7 +347,7 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_c
       }
       hs = acc;
     }
-    *reinterpret_cast<float2 *>(s_h + (hf * 4 + R) * kD + c0) = hs;
+    *reinterpret_cast<float2 *>(s_h + qd * kD + c0) = hs;   // the quarter's sum
     tmem_st16(stash + 16 * bi, kq);
     tmem_st16(stash + 64 + 16 * bi, reinterpret_cast<const float *>(x[bi]));
   }
@@ -340,45 +355,10 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_c
   __syncthreads();   // norms, half sums visible; q, k, g tiles fully read
 
   // ------------------------------------------------------------ anchors and operand tiles
-  uint4 qp[2][2], kq[2][2];   // packed Q+ / K' rows of the two blocks
+  uint4 qp[2][2], kq[2][2];   // packed Q+ / K' rows of the thread's two quarters
   {
-    float2 hh[2][4];
-#pragma unroll
-    for (int I = 0; I < 4; ++I) {
-      hh[0][I] = *reinterpret_cast<const float2 *>(s_h + I * kD + c0);
-      hh[1][I] = *reinterpret_cast<const float2 *>(s_h + (4 + I) * kD + c0);
-    }
-    float2 m[4], a[4], tot = make_float2(0.f, 0.f);
-#pragma unroll
-    for (int I = 0; I < 4; ++I) {
-      m[I] = make_float2(tot.x + hh[0][I].x, tot.y + hh[0][I].y);
-      a[I] = make_float2(m[I].x + hh[1][I].x, m[I].y + hh[1][I].y);
-      tot = a[I];
-    }
-    if (sel == 0) {   // gamma = e^(b_63) for rho = p and 64 + p
-      float *gam = reinterpret_cast<float *>(blk + kBlkGamma);
-      gam[p] = fast_exp2(tot.x);
-      gam[64 + p] = fast_exp2(tot.y);
-    }
-    // the factors of block R (a compile-time block index, so only the later blocks' factors exist)
-    auto factors = [&](auto Rc) {
-      constexpr int R = decltype(Rc)::value;
-      BlockFactors f;
-      f.em = exp2_2(m[R]);
-      f.ems = make_float2(f.em.x * prm.scale, f.em.y * prm.scale);
-      f.el = exp2_2(make_float2(tot.x - m[R].x, tot.y - m[R].y));
-      f.eg = exp2_2(hh[1][R]);
-#pragma unroll
-      for (int R2 = R + 1; R2 < 4; ++R2)
-        f.cr[R2] = exp2_2(make_float2(fminf(m[R2].x - a[R].x, 0.f), fminf(m[R2].y - a[R].y, 0.f)));
-      return f;
-    };
-    using R0 = std::integral_constant<int, 0>;
-    using R1 = std::integral_constant<int, 1>;
-    using R2c = std::integral_constant<int, 2>;
-    using R3 = std::integral_constant<int, 3>;
-    // the k and q words of block bi back from TMEM
-    auto words = [&](int bi, uint32_t (&kqw)[16]) {
+    // the k and q words and the exponents of quarter bi back from TMEM (exponents shifted by xoff)
+    auto words = [&](int bi, uint32_t (&kqw)[16], float2 xoff) {
       uint32_t xw[16];
       tmem_ld16_async(stash + 16 * bi, kqw);
       tmem_ld16_async(stash + 64 + 16 * bi, xw);
@@ -386,19 +366,91 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_c
       tmem_tie<16>(kqw);
       tmem_tie<16>(xw);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) x[bi][j] = make_float2(__uint_as_float(xw[2 * j]), __uint_as_float(xw[2 * j + 1]));
+      for (int j = 0; j < 8; ++j)
+        x[bi][j] = make_float2(__uint_as_float(xw[2 * j]) + xoff.x, __uint_as_float(xw[2 * j + 1]) + xoff.y);
     };
+    auto gamma_out = [&](float2 tot) {   // gamma = e^(b_63) for rho = p and 64 + p
+      if (sel == 0) {
+        float *gam = reinterpret_cast<float *>(blk + kBlkGamma);
+        gam[p] = fast_exp2(tot.x);
+        gam[64 + p] = fast_exp2(tot.y);
+      }
+    };
+    using R0 = std::integral_constant<int, 0>;
+    using R1 = std::integral_constant<int, 1>;
+    using R2c = std::integral_constant<int, 2>;
+    using R3 = std::integral_constant<int, 3>;
+    const float2 zero2 = make_float2(0.f, 0.f);
     uint32_t kqw[16];
-    if (Ra == 0) {
-      words(0, kqw);
-      build_rows<0>(kqw, x[0], 8 * hf, p, s_nq, s_nk, factors(R0{}), sm, qp[0], kq[0]);
-      words(1, kqw);
-      build_rows<3>(kqw, x[1], 48 + 8 * hf, p, s_nq, s_nk, factors(R3{}), sm, qp[1], kq[1]);
+    if constexpr (BLK == 16) {
+      float2 hh[2][4];   // half sums of block I: rows 0..7 (hh[0]) and 8..15 (hh[1])
+#pragma unroll
+      for (int I = 0; I < 4; ++I) {
+        hh[0][I] = *reinterpret_cast<const float2 *>(s_h + (2 * I) * kD + c0);
+        hh[1][I] = *reinterpret_cast<const float2 *>(s_h + (2 * I + 1) * kD + c0);
+      }
+      float2 m[4], a[4], tot = zero2;   // anchors (b at row 7 of each block) and block ends (row 15)
+#pragma unroll
+      for (int I = 0; I < 4; ++I) {
+        m[I] = make_float2(tot.x + hh[0][I].x, tot.y + hh[0][I].y);
+        a[I] = make_float2(m[I].x + hh[1][I].x, m[I].y + hh[1][I].y);
+        tot = a[I];
+      }
+      gamma_out(tot);
+      // the factors of block R (a compile-time block index, so only the later blocks' factors exist)
+      auto factors = [&](auto Rc) {
+        constexpr int R = decltype(Rc)::value;
+        BlockFactors f;
+        f.em = exp2_2(m[R]);
+        f.ems = make_float2(f.em.x * prm.scale, f.em.y * prm.scale);
+        f.el = exp2_2(make_float2(tot.x - m[R].x, tot.y - m[R].y));
+        f.eg = exp2_2(hh[1][R]);
+#pragma unroll
+        for (int R2 = R + 1; R2 < 4; ++R2)
+          f.cr[R2] = exp2_2(make_float2(fminf(m[R2].x - a[R].x, 0.f), fminf(m[R2].y - a[R].y, 0.f)));
+        return f;
+      };
+      if (Ra == 0) {
+        words(0, kqw, zero2);
+        build_rows<0, 16>(kqw, x[0], 8 * hf, p, s_nq, s_nk, factors(R0{}), sm, qp[0], kq[0]);
+        words(1, kqw, zero2);
+        build_rows<3, 16>(kqw, x[1], 48 + 8 * hf, p, s_nq, s_nk, factors(R3{}), sm, qp[1], kq[1]);
+      } else {
+        words(0, kqw, zero2);
+        build_rows<1, 16>(kqw, x[0], 16 + 8 * hf, p, s_nq, s_nk, factors(R1{}), sm, qp[0], kq[0]);
+        words(1, kqw, zero2);
+        build_rows<2, 16>(kqw, x[1], 32 + 8 * hf, p, s_nq, s_nk, factors(R2c{}), sm, qp[1], kq[1]);
+      }
     } else {
-      words(0, kqw);
-      build_rows<1>(kqw, x[0], 16 + 8 * hf, p, s_nq, s_nk, factors(R1{}), sm, qp[0], kq[0]);
-      words(1, kqw);
-      build_rows<2>(kqw, x[1], 32 + 8 * hf, p, s_nq, s_nk, factors(R2c{}), sm, qp[1], kq[1]);
+      float2 sq[8];   // quarter sums
+#pragma unroll
+      for (int q = 0; q < 8; ++q) sq[q] = *reinterpret_cast<const float2 *>(s_h + q * kD + c0);
+      auto add = [](float2 u, float2 v) { return make_float2(u.x + v.x, u.y + v.y); };
+      // anchors m_R = b at row 15 of block R, block ends a_R = b at its row 31
+      const float2 m0 = add(sq[0], sq[1]);
+      const float2 a0 = add(add(m0, sq[2]), sq[3]);
+      const float2 m1 = add(add(a0, sq[4]), sq[5]);
+      const float2 tot = add(add(m1, sq[6]), sq[7]);
+      gamma_out(tot);
+      auto factors = [&](auto Rc) {
+        constexpr int R = decltype(Rc)::value;
+        const float2 mR = R ? m1 : m0, aR = R ? tot : a0;
+        BlockFactors f;
+        f.em = exp2_2(mR);
+        f.ems = make_float2(f.em.x * prm.scale, f.em.y * prm.scale);
+        f.el = exp2_2(make_float2(tot.x - mR.x, tot.y - mR.y));
+        f.eg = exp2_2(make_float2(aR.x - mR.x, aR.y - mR.y));
+        if (R == 0) f.cr[1] = exp2_2(make_float2(fminf(m1.x - a0.x, 0.f), fminf(m1.y - a0.y, 0.f)));
+        return f;
+      };
+      // quarter sel of each block: the outer quarters measure from the neighbour quarter's far end
+      auto xoff = [&](int R) {
+        return sel == 0 ? make_float2(-sq[4 * R + 1].x, -sq[4 * R + 1].y) : sel == 3 ? sq[4 * R + 2] : zero2;
+      };
+      words(0, kqw, xoff(0));
+      build_rows<0, 32>(kqw, x[0], 8 * sel, p, s_nq, s_nk, factors(R0{}), sm, qp[0], kq[0]);
+      words(1, kqw, xoff(1));
+      build_rows<1, 32>(kqw, x[1], 32 + 8 * sel, p, s_nq, s_nk, factors(R1{}), sm, qp[1], kq[1]);
     }
     // the packed Q+ and K' rows wait in TMEM columns 160..223 (beside the product's 160) until the
     // operand tiles are free
@@ -410,12 +462,12 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_c
   tc_fence_before();
   __syncthreads();
 
-  // ------------------------------------------------------------ A/P product (one 128 x 160 tcgen05.mma)
+  // ------------------------------------------------------------ A/P product (one 128 x 160 or 128 x 96 tcgen05.mma)
   if (tid == 0) {
     tc_fence_after();
     const uint64_t fq = desc_mnmajor_base(smem_u32(sm + OFF_FQ), 128);
     const uint64_t gb = desc_mnmajor_base(smem_u32(sm + OFF_GB), 128);
-    const uint32_t id = idesc_bf16(128, kGBCols, true, true);
+    const uint32_t id = idesc_bf16(128, kGBCols<BLK>, true, true);
 #pragma unroll
     for (int s = 0; s < 8; ++s) mma_bf16(tmem, fq + mnmajor_step(s), gb + mnmajor_step(s), id, s > 0);
     mma_commit(bar_mma);
@@ -456,7 +508,7 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_c
   }
 #pragma unroll
   for (int bi = 0; bi < 2; ++bi) {
-    const int t0 = 16 * (bi ? Rb : Ra) + 8 * hf;
+    const int t0 = BLK == 16 ? 16 * (bi ? Rb : Ra) + 8 * hf : 32 * bi + 8 * sel;
     *reinterpret_cast<uint4 *>(sm + OFF_QST + swz_offset(128, p, t0)) = qp[bi][0];
     *reinterpret_cast<uint4 *>(sm + OFF_QST + swz_offset(128, 64 + p, t0)) = qp[bi][1];
     *reinterpret_cast<uint4 *>(sm + OFF_PKST + swz_offset(kBlkPKRows, 64 + p, t0)) = kq[bi][0];
@@ -469,42 +521,70 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_c
     const int q4 = warp & 3, ib = warp >> 2;
     const bool is_p = q4 >= 2;                 // warp-uniform
     const int r = (q4 & 1) * 32 + lane;
-    const int Ra2 = (q4 & 1) * 2;              // row blocks of this warp: Ra2 (lanes 0..15), Ra2 + 1
-    const bool upper = lane >= 16;
     const uint32_t lane_base = static_cast<uint32_t>(q4 * 32) << 16;
     const float bscale = is_p ? prm.scale : s_beta[r];
     float *sA = reinterpret_cast<float *>(sm + OFF_A);
+    // column i of a row is kept iff i < r (A) or i <= r (P); this also zeroes the blocks above the diagonal,
+    // whose registers are never loaded
+    if constexpr (BLK == 16) {
+      const int Ra2 = (q4 & 1) * 2;              // row blocks of this warp: Ra2 (lanes 0..15), Ra2 + 1
+      const bool upper = lane >= 16;
 #pragma unroll
-    for (int ii = 0; ii < 2; ++ii) {
-      const int I = 2 * ib + ii;   // column block
-      // source columns of the two row blocks (warp-uniform); -1: the block is above the diagonal
-      const int srcA = (I == Ra2) ? 16 * I : (I < Ra2) ? gb_col0(Ra2) + 16 * I : -1;
-      const int srcB = (I == Ra2 + 1) ? 16 * I : (I < Ra2 + 1) ? gb_col0(Ra2 + 1) + 16 * I : -1;
-      uint32_t va[16], vb[16];
-      if (srcA >= 0) tmem_ld16_async(tmem + lane_base + srcA, va);
-      if (srcB >= 0) tmem_ld16_async(tmem + lane_base + srcB, vb);
-      tmem_wait_ld();
-      tmem_tie<16>(va);
-      tmem_tie<16>(vb);
-      // column i = 16 I + e is kept iff i < r (A) or i <= r (P); this also zeroes the blocks above the
-      // diagonal (i > r) whose registers were never loaded
-      const int lim = r - 16 * I + (is_p ? 1 : 0);
-      float v[16];
+      for (int ii = 0; ii < 2; ++ii) {
+        const int I = 2 * ib + ii;   // column block
+        // source columns of the two row blocks (warp-uniform); -1: the block is above the diagonal
+        const int srcA = (I == Ra2) ? 16 * I : (I < Ra2) ? gb_col0<16>(Ra2) + 16 * I : -1;
+        const int srcB = (I == Ra2 + 1) ? 16 * I : (I < Ra2 + 1) ? gb_col0<16>(Ra2 + 1) + 16 * I : -1;
+        uint32_t va[16], vb[16];
+        if (srcA >= 0) tmem_ld16_async(tmem + lane_base + srcA, va);
+        if (srcB >= 0) tmem_ld16_async(tmem + lane_base + srcB, vb);
+        tmem_wait_ld();
+        tmem_tie<16>(va);
+        tmem_tie<16>(vb);
+        const int lim = r - 16 * I + (is_p ? 1 : 0);
+        float v[16];
 #pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        const float raw = __uint_as_float(upper ? vb[e] : va[e]);
-        v[e] = e < lim ? raw * bscale : 0.f;
+        for (int e = 0; e < 16; ++e) {
+          const float raw = __uint_as_float(upper ? vb[e] : va[e]);
+          v[e] = e < lim ? raw * bscale : 0.f;
+        }
+        if (is_p) {
+#pragma unroll
+          for (int k8 = 0; k8 < 2; ++k8)
+            *reinterpret_cast<uint4 *>(sm + OFF_PKST + swz_offset(kBlkPKRows, r, 16 * I + 8 * k8)) =
+                make_uint4(pack_bf16x2(v[8 * k8], v[8 * k8 + 1]), pack_bf16x2(v[8 * k8 + 2], v[8 * k8 + 3]),
+                           pack_bf16x2(v[8 * k8 + 4], v[8 * k8 + 5]), pack_bf16x2(v[8 * k8 + 6], v[8 * k8 + 7]));
+        } else {
+#pragma unroll
+          for (int e = 0; e < 16; e += 4)
+            *reinterpret_cast<float4 *>(sA + r * kAStride + 16 * I + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+        }
       }
+    } else {
+      // 32-row blocks: the warp's lanes are one row block R; ib picks the 32-column block I
+      const int R = q4 & 1, I = ib;
+      const int src = I == R ? 32 * I : I < R ? gb_col0<32>(R) + 32 * I : -1;
+      uint32_t va[32];
+      if (src >= 0) {
+        tmem_ld16_async(tmem + lane_base + src, va);
+        tmem_ld16_async(tmem + lane_base + src + 16, va + 16);
+      }
+      tmem_wait_ld();
+      tmem_tie<32>(va);
+      const int lim = r - 32 * I + (is_p ? 1 : 0);
+      float v[32];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) v[e] = e < lim ? __uint_as_float(va[e]) * bscale : 0.f;
       if (is_p) {
 #pragma unroll
-        for (int k8 = 0; k8 < 2; ++k8)
-          *reinterpret_cast<uint4 *>(sm + OFF_PKST + swz_offset(kBlkPKRows, r, 16 * I + 8 * k8)) =
+        for (int k8 = 0; k8 < 4; ++k8)
+          *reinterpret_cast<uint4 *>(sm + OFF_PKST + swz_offset(kBlkPKRows, r, 32 * I + 8 * k8)) =
               make_uint4(pack_bf16x2(v[8 * k8], v[8 * k8 + 1]), pack_bf16x2(v[8 * k8 + 2], v[8 * k8 + 3]),
                          pack_bf16x2(v[8 * k8 + 4], v[8 * k8 + 5]), pack_bf16x2(v[8 * k8 + 6], v[8 * k8 + 7]));
       } else {
 #pragma unroll
-        for (int e = 0; e < 16; e += 4)
-          *reinterpret_cast<float4 *>(sA + r * kAStride + 16 * I + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+        for (int e = 0; e < 32; e += 4)
+          *reinterpret_cast<float4 *>(sA + r * kAStride + 32 * I + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
       }
     }
   }
@@ -687,11 +767,16 @@ cudaError_t launch_chunk_intra(const IntraParams &p, int num_chunks, cudaStream_
   if (num_chunks <= 0) return cudaSuccess;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(chunk_intra_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(chunk_intra_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(chunk_intra_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  chunk_intra_kernel<<<num_chunks * p.H, kThreads, kSmemBytes, stream>>>(p);
+  if (p.lower_bound >= kLowerBound32)
+    chunk_intra_kernel<32><<<num_chunks * p.H, kThreads, kSmemBytes, stream>>>(p);
+  else
+    chunk_intra_kernel<16><<<num_chunks * p.H, kThreads, kSmemBytes, stream>>>(p);
   return cudaGetLastError();
 }
 

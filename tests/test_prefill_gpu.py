@@ -58,6 +58,15 @@ def test_decay_regimes(case):
     _parity(inp)
 
 
+@pytest.mark.parametrize("lb", [-5.0, -5.1, -10.0])
+def test_saturated_gate_at_the_sub_block_switch(lb):
+    # gate pushed to its bound (lambda = lower_bound on every channel): at -5 the 32-row sub-blocks and at
+    # -10 the 16-row ones see their largest exponents (2^+-115); at -5.1 the kernel takes the 16-row ones
+    inp = inputs.prefill_inputs(f"saturated_{lb}", [200, 64, 33], 2, seed=35, pool_slots=4, load_initial=True,
+                                lower_bound=lb, g_mean=8.0)
+    _parity(inp)
+
+
 def test_strided_token_rows():
     inp = inputs.prefill_inputs("strided", [130, 64], 2, seed=41)
     _parity(inp, token_pad=256)
