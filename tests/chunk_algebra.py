@@ -58,11 +58,12 @@ def chunked_exact(qh, kh, v, lam, beta, scale, S0, C):
     return out, S
 
 
-def anchored_factors(b):
-    """Sub-block factorisation of exp(b_r - b_i) for one chunk of C = 16*nb rows.
+def anchored_factors(b, sub=SUB):
+    """Sub-block factorisation of exp(b_r - b_i) for one chunk of C = sub*nb rows.
 
-    Rows are grouped in 16-row blocks R.  With m_R = b at the block's row 7 and
-    a_R = b at its row 15:
+    Rows are grouped in blocks R of `sub` rows (16, or 32 for the kernel's
+    lower_bound >= -5 variant).  With m_R = b at the block's middle row
+    (sub/2 - 1) and a_R = b at its last row:
       same block:       exp(b_r - b_i) = E_r * Einv_i,  E = exp(b - m_R(r)),  Einv = exp(m_R - b)
       block I < R:      exp(b_r - b_i) = (E_r * c[R,I]) * Gp_i,
                         c[R,I] = exp(m_R - a_I) <= 1,  Gp_i = exp(a_I - b_i) <= 1
@@ -70,11 +71,11 @@ def anchored_factors(b):
     represented (must stay below ~87 for fp32).
     """
     n, dk = b.shape
-    assert n % SUB == 0
-    nb = n // SUB
-    m = b[SUB // 2 - 1::SUB]          # [nb, dk]  row 7 of each block
-    a = b[SUB - 1::SUB]               # [nb, dk]  row 15 of each block
-    blk = np.arange(n) // SUB
+    assert n % sub == 0
+    nb = n // sub
+    m = b[sub // 2 - 1::sub]          # [nb, dk]  middle row of each block
+    a = b[sub - 1::sub]               # [nb, dk]  last row of each block
+    blk = np.arange(n) // sub
     e_exp = b - m[blk]
     einv_exp = m[blk] - b
     gp_exp = a[blk] - b
@@ -87,13 +88,13 @@ def anchored_factors(b):
     return dict(E=E, Einv=Einv, Gp=Gp, c=c, m=m, a=a, worst_exponent=worst)
 
 
-def chunked_anchored(qh, kh, v, lam, beta, scale, S0, C=64):
+def chunked_anchored(qh, kh, v, lam, beta, scale, S0, C=64, sub=SUB):
     """Chunked evaluation with A, P built from the anchored sub-block factors.
 
     Each chunk is padded to C rows with q = k = v = 0, lambda = 0, beta = 0
     (padding rows change neither the state nor the decay).
     """
-    assert C % SUB == 0
+    assert C % sub == 0
     T, dk = qh.shape
     dv = v.shape[1]
     S = np.array(S0, dtype=np.float64, copy=True)
@@ -108,17 +109,17 @@ def chunked_anchored(qh, kh, v, lam, beta, scale, S0, C=64):
         L = np.pad(lam[c0:c1], ((0, pad), (0, 0)))
         bt = np.pad(beta[c0:c1], (0, pad))
         b = np.cumsum(L, axis=0)
-        f = anchored_factors(b)
+        f = anchored_factors(b, sub)
         worst = max(worst, f["worst_exponent"])
         FK, FQ = K * f["E"], Q * f["E"]
         G, Gp = K * f["Einv"], K * f["Gp"]
         A = np.zeros((C, C))
         P = np.zeros((C, C))
-        nb = C // SUB
+        nb = C // sub
         for R in range(nb):
-            rs = slice(R * SUB, (R + 1) * SUB)
+            rs = slice(R * sub, (R + 1) * sub)
             for I in range(R + 1):
-                cs = slice(I * SUB, (I + 1) * SUB)
+                cs = slice(I * sub, (I + 1) * sub)
                 if I == R:
                     A[rs, cs] = FK[rs] @ G[cs].T
                     P[rs, cs] = FQ[rs] @ G[cs].T
@@ -130,7 +131,7 @@ def chunked_anchored(qh, kh, v, lam, beta, scale, S0, C=64):
         A = bt[:, None] * A * (r[:, None] > r[None, :])
         P = P * (r[:, None] >= r[None, :])
         Tm = np.linalg.solve(np.eye(C) + A, np.diag(bt))
-        blk = r // SUB
+        blk = r // sub
         em = np.exp(f["m"])[blk]                 # exp(m_R(r))
         Kplus = FK * em                           # k o exp(b)
         Qplus = FQ * em

@@ -314,7 +314,7 @@ def pin_contraction_bound(O):
 
 def pin_chunked_equals_sequential(O):
     """The chunk-parallel algebra (exact ratios, chunk 1/4/16/64) and the
-    kernel's anchored 16-row sub-block factorisation (chunk 64) reproduce
+    kernel's anchored 16- and 32-row sub-block factorisations (chunk 64) reproduce
     the token-by-token oracle, for weak and strong decay."""
     rng = np.random.default_rng(21)
     for d, T, lam_hi in ((8, 150, 0.05), (8, 200, 5.0), (128, 130, 5.0), (128, 97, 0.02)):
@@ -328,10 +328,11 @@ def pin_chunked_equals_sequential(O):
             o, S = chunk_algebra.chunked_exact(qh, kh, v, lam, beta, 0.2, S0, C)
             _close(o, ref, 1e-10, f"chunked (C={C}, d={d}) outputs")
             _close(S, Sref, 1e-10, f"chunked (C={C}, d={d}) state")
-        o, S, worst = chunk_algebra.chunked_anchored(qh, kh, v, lam, beta, 0.2, S0, 64)
-        _close(o, ref, 1e-10, f"anchored chunk (d={d}) outputs")
-        _close(S, Sref, 1e-10, f"anchored chunk (d={d}) state")
-        assert worst <= 8 * lam_hi + 1e-9
+        for sub in (16, 32):   # the kernel's two sub-block sizes
+            o, S, worst = chunk_algebra.chunked_anchored(qh, kh, v, lam, beta, 0.2, S0, 64, sub)
+            _close(o, ref, 1e-10, f"anchored chunk (d={d}, {sub}-row blocks) outputs")
+            _close(S, Sref, 1e-10, f"anchored chunk (d={d}, {sub}-row blocks) state")
+            assert worst <= sub // 2 * lam_hi + 1e-9
 
 
 ALL_PINS = [
