@@ -73,7 +73,7 @@ constexpr uint32_t OFF_WST = 40960, OFF_UST = 57344;   // W^T and U^^T rows of t
 constexpr uint32_t OFF_SMALL = 99328;
 constexpr uint32_t SM_NQ = 0, SM_NK = 256, SM_BETA = 512, SM_H = 768 /* [2][4][128] f32 */,
                    SM_BAR = 4864, SM_TMEM = 4888, SM_ABORT = 4892, SM_BARU = 4896, SM_END = 4928;
-constexpr int kCopyThread = 128;      // issues the block's early bulk stores (Q+, [P ; K'])
+constexpr int kCopyThread = 128;      // issues the block's early bulk stores (Q+, [P ; K']) and U^^T's
 constexpr uint32_t kSmemBytes = OFF_SMALL + SM_END + 1024;   // + alignment slack
 static_assert(2 * (kSmemBytes + 1024) <= 233472, "two CTAs per SM");
 constexpr int kAStride = 68;
@@ -591,11 +591,6 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_c
   fence_async_smem();
   tc_fence_before();
   __syncthreads();
-  if (tid == kCopyThread) {   // Q+ and [P ; K'] rows are complete: store them
-    bulk_store(blk + kBlkWQ + 16384, sm + OFF_QST, 16384);
-    bulk_store(blk + kBlkPK, sm + OFF_PKST, kBlkPKRows * 128);
-    bulk_commit();
-  }
 
   // ------------------------------------------------------------ T = (I + A)^-1 Diag(beta)
   // Blocked inverse of the unit-lower L = I + A in fp32, 16x16 blocks D_R = L_RR^-1:
@@ -663,6 +658,10 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_c
       mm_16x8(e, sInv + (lo + 16) * kAStride + lo + 16, sA + lo * kAStride + lo + 16 + 8 * nj, 2, lane);
       st_16x8(sInv + (lo + 16) * kAStride + lo + 8 * nj, e, -1.f, lane);
       st_16x8_t(tT, lo + 16, lo + 8 * nj, e, -1.f, s_beta, lane);
+    } else if (tid == kCopyThread) {   // idle in this step: the Q+ and [P ; K'] rows (complete) to the block
+      bulk_store(blk + kBlkWQ + 16384, sm + OFF_QST, 16384);
+      bulk_store(blk + kBlkPK, sm + OFF_PKST, kBlkPKRows * 128);
+      bulk_commit();
     }
     __syncthreads();
     // Z = A_(23,01) I_1 (32 x 32) -> A tile rows 0..31, cols 32..63; warp = (16-row half mi, 8 columns nj).
