@@ -274,9 +274,18 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_chain_kernel(const __grid_c
       st_bf16_pairs(tmem + lane_base + TM_SA + col / 2 + 16, s + 32);
       const int bn = (c + 1) % kNumBuf;
       wait_or_abort(&bar_full[bn], ((c + 1) / kNumBuf) & 1, s_abort, prm.status);
-      const float *gam = reinterpret_cast<const float *>(sm + bn * kBufStride + kBlkGamma) + col;
+      // the block's e^(b_63) for the thread's 64 key channels: 16-byte broadcast loads, packed multiplies
+      const float4 *gam = reinterpret_cast<const float4 *>(sm + bn * kBufStride + kBlkGamma + 4 * col);
 #pragma unroll
-      for (int i = 0; i < 64; ++i) s[i] *= gam[i];
+      for (int i = 0; i < 16; ++i) {
+        const float4 g = gam[i];
+        const float2 lo = mul2(make_float2(s[4 * i], s[4 * i + 1]), make_float2(g.x, g.y));
+        const float2 hi = mul2(make_float2(s[4 * i + 2], s[4 * i + 3]), make_float2(g.z, g.w));
+        s[4 * i] = lo.x;
+        s[4 * i + 1] = lo.y;
+        s[4 * i + 2] = hi.x;
+        s[4 * i + 3] = hi.y;
+      }
 #pragma unroll
       for (int k = 0; k < 4; ++k) tmem_st16(tmem + lane_base + TM_S + col + 16 * k, s + 16 * k);
       tmem_wait_st();
