@@ -71,7 +71,7 @@ constexpr uint32_t OFF_T = 74752;     // T bf16 K-major [t][t'] (8 KB), written 
 // after the W / U^ products
 constexpr uint32_t OFF_WST = 40960, OFF_UST = 57344;   // W^T and U^^T rows of the block
 constexpr uint32_t OFF_SMALL = 99328;
-constexpr uint32_t SM_NQ = 0, SM_NK = 256, SM_BETA = 512, SM_H = 768 /* [2][4][128] f32 */,
+constexpr uint32_t SM_NQ = 0, SM_NK = 256, SM_BETA = 512, SM_H = 768 /* [8 quarters][128] f32 */,
                    SM_BAR = 4864, SM_TMEM = 4888, SM_ABORT = 4892, SM_BARU = 4896, SM_END = 4928;
 constexpr int kCopyThread = 128;      // issues the block's early bulk stores (Q+, [P ; K']) and U^^T's
 constexpr uint32_t kSmemBytes = OFF_SMALL + SM_END + 1024;   // + alignment slack
