@@ -109,3 +109,30 @@ def test_more_chunk_slots_than_one_intra_launch():
     inp = inputs.prefill_inputs("many_slots", lens, 1, seed=72, pool_slots=96, load_initial=True)
     assert sum((n + 63) // 64 for n in lens) > 4096
     _parity(inp)
+
+
+def test_prefill_captured_in_a_cuda_graph():
+    # the call (intra-chunk launch + state pass as its programmatic dependent) replays from a CUDA graph with
+    # the same results as a direct call
+    inp = inputs.prefill_inputs("graph", [130, 64, 200, 1], 2, seed=81, pool_slots=8, load_initial=True)
+    dev = DevicePrefill(inp)
+    ws = dev.workspace()
+    out_ref, final_ref = dev.run(workspace=ws)
+    torch.cuda.synchronize()
+    out_ref, final_ref = out_ref.clone(), final_ref.clone()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        dev.run(workspace=ws)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        out_g, final_g = dev.run(workspace=ws)
+    out_g.zero_()
+    final_g.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert kda.read_device_status(ws) == 0
+    assert torch.equal(out_g, out_ref)
+    assert torch.equal(final_g, final_ref)
