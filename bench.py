@@ -7,8 +7,10 @@ every (chunk, head) and the state pass over every (sequence, head); the
 roofline line covers the whole call (its algorithmic bytes over its
 CUDA-event time), the per-kernel split is in profiles/.  Also timed: the same call end to end with host
 buffers (pinned H2D of the step's inputs + D2H of its outputs inside the
-timed region), the verify call on 64 requests x 8 draft tokens, and the fp64
-CPU oracle on a bounded sample of the prefill workload.
+timed region), the verify call on 64 requests x 8, 4 and 1 tokens and the
+accept/commit after it (each captured in a CUDA graph and replayed, the way a
+serving step runs them), and the fp64 CPU oracle on a bounded sample of the
+prefill workload.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 N > 1 runs under torchrun, one replica per GPU (weak scaling, no collective on
@@ -357,48 +359,77 @@ def run_gpu(args):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, device)
     e2e_value = T * e2e_steps * world / (e2e_ms / 1e3)
 
-    # ---- verify: 64 requests x 8 draft tokens ----
-    vin = inputs.verify_64x8()
-    vdev = DeviceVerify(vin, device=device)
-    vout = torch.empty((vin.B * vin.T, H, 128), dtype=torch.bfloat16, device=device)
-    inter = torch.empty((vin.B, vin.T, H, 128, 128), dtype=torch.float32, device=device)
-    for _ in range(max(3, args.warmup)):
-        vdev.run(out=vout, intermediate_states=inter, workspace=ws, stream=stream)
-    v_steps = max(3, min(args.steps, 200))
-    v0 = torch.cuda.Event(enable_timing=True)
-    v1 = torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize(device)
-    v0.record(stream)
-    for _ in range(v_steps):
-        vdev.run(out=vout, intermediate_states=inter, workspace=ws, stream=stream)
-    v1.record(stream)
-    torch.cuda.synchronize(device)
-    v_us = v0.elapsed_time(v1) * 1e3 / v_steps
-    v_bytes = verify_algorithmic_bytes(vin)
-    v_achieved = v_bytes / (v_us * 1e-6) / 1e9
+    # ---- verify (64 requests x 8, 4 and 1 tokens) and accept/commit, timed as CUDA-graph replays ----
+    def graph_time_us(calls, steps):
+        """Mean µs per call of ``calls`` (callables on the current stream) captured once
+        in a CUDA graph and replayed; the calls rotate so each one sees cold L2."""
+        side = torch.cuda.Stream(device)
+        side.wait_stream(torch.cuda.current_stream(device))
+        with torch.cuda.stream(side):
+            for c in calls:
+                c()
+        torch.cuda.current_stream(device).wait_stream(side)
+        torch.cuda.synchronize(device)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for c in calls:
+                c()
+        for _ in range(3):
+            graph.replay()
+        reps = max(3, math.ceil(steps / len(calls)))
+        g0 = torch.cuda.Event(enable_timing=True)
+        g1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(device)
+        g0.record()
+        for _ in range(reps):
+            graph.replay()
+        g1.record()
+        torch.cuda.synchronize(device)
+        return g0.elapsed_time(g1) * 1e3 / (reps * len(calls)), reps * len(calls)
+
+    def time_verify(vin):
+        """One verify call per rotation set: disjoint slot sets and separate per-step buffers, as many as it
+        takes for one rotation to move more than 3x the L2 (the pool rows and states are then read cold)."""
+        vdev = DeviceVerify(vin, device=device)
+        per_call = verify_algorithmic_bytes(vin)
+        n_rot = min(vin.pool.shape[0] // vin.B, max(1, math.ceil(3 * L2_BYTES / per_call)))
+        others = np.setdiff1d(np.arange(vin.pool.shape[0]), vin.slot_ids)
+        others = np.random.default_rng(11).permutation(others)
+        slot_sets = [vdev.slots] + [torch.from_numpy(others[r * vin.B:(r + 1) * vin.B].astype(np.int32)).to(device)
+                                    for r in range(n_rot - 1)]
+        vout = torch.empty((vin.B * vin.T, H, 128), dtype=torch.bfloat16, device=device)
+        inters = [torch.empty((vin.B, vin.T, H, 128, 128), dtype=torch.float32, device=device) for _ in range(n_rot)]
+
+        def call(r):
+            return lambda: kda.recurrent_verify(vdev.q, vdev.k, vdev.v, vdev.g, vdev.beta, vdev.A_log, vdev.dt_bias,
+                                                vdev.pool, slot_sets[r], vin.T, lower_bound=vin.lower_bound,
+                                                scale=vin.scale, out=vout, intermediate_states=inters[r],
+                                                workspace=ws)
+        us, n = graph_time_us([call(r) for r in range(n_rot)], max(3, min(args.steps, 200)))
+        achieved = per_call / (us * 1e-6) / 1e9
+        rec = {"workload": vin.name, "T": vin.T, "us_per_layer": us, "calls_timed": n, "rotation_sets": n_rot,
+               "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                            "frac": achieved / peak, "traffic": None, "algorithmic_bytes": per_call}}
+        return rec, vdev, inters[0]
+
+    vrec, vdev, inter = time_verify(inputs.verify_64x8())
+    vrec["roofline"]["traffic"] = recorded_traffic("verify")
+    vvariants = [time_verify(make())[0] for make in (inputs.verify_64x4, inputs.verify_64x1)]
+    vin = vdev.inp
 
     # ---- accept/commit after verify: 1..8 accepted tokens per request ----
     n_acc = torch.from_numpy(np.random.default_rng(7).integers(1, vin.T + 1, size=vin.B).astype(np.int32)).to(device)
-    for _ in range(3):
-        kda.commit_accepted(vdev.pool, vdev.slots, n_acc, inter, workspace=ws, stream=stream)
-    c0 = torch.cuda.Event(enable_timing=True)
-    c1 = torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize(device)
-    c0.record(stream)
-    for _ in range(v_steps):
-        kda.commit_accepted(vdev.pool, vdev.slots, n_acc, inter, workspace=ws, stream=stream)
-    c1.record(stream)
-    torch.cuda.synchronize(device)
-    c_us = c0.elapsed_time(c1) * 1e3 / v_steps
+    c_us, c_steps = graph_time_us(
+        [lambda: kda.commit_accepted(vdev.pool, vdev.slots, n_acc, inter, workspace=ws)], max(3, min(args.steps, 200)))
     c_bytes = 2 * vin.B * H * STATE_BYTES
     c_achieved = c_bytes / (c_us * 1e-6) / 1e9
+    assert kda.read_device_status(ws) == 0
 
-    del inter, vout
+    del inter
     if rank != 0:
         return
     cpu = None if args.no_cpu_baseline or world > 1 else cpu_baseline(inp)
     traffic = recorded_traffic("prefill")
-    vtraffic = recorded_traffic("verify")
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
@@ -418,10 +449,9 @@ def run_gpu(args):
                 "steps": e2e_steps},
         "gpu_launches": 2 * args.steps,
         "clocks": clocks,
-        "verify": {"workload": vin.name, "us_per_layer": v_us, "steps": v_steps,
-                   "roofline": {"bound": "hbm", "achieved": v_achieved, "peak": peak, "unit": "GB/s",
-                                "frac": v_achieved / peak, "traffic": vtraffic, "algorithmic_bytes": v_bytes}},
-        "commit": {"workload": vin.name + " (1..8 accepted per request)", "us_per_layer": c_us, "steps": v_steps,
+        "verify": vrec,
+        "verify_variants": vvariants,
+        "commit": {"workload": vin.name + " (1..8 accepted per request)", "us_per_layer": c_us, "calls_timed": c_steps,
                    "roofline": {"bound": "hbm", "achieved": c_achieved, "peak": peak, "unit": "GB/s",
                                 "frac": c_achieved / peak, "algorithmic_bytes": c_bytes}},
         "wall_s_timed_region": wall,

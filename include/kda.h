@@ -69,6 +69,16 @@ extern "C" {
 #define KDA_DEVICE_TIMEOUT 2u  /* a bounded wait inside a kernel gave up (a lost async completion); results are incomplete */
 #define KDA_DEVICE_BAD_COUNT 4u /* an accepted-token count was outside [0, T]; that request was skipped */
 
+/*
+ * Slot id of a padding row.  A batch captured in a CUDA graph for a bucket of
+ * B requests and replayed with fewer live requests fills the unused rows of
+ * slot_ids with this value; kda_recurrent_verify and kda_commit_accepted skip
+ * such rows without touching their outputs or setting a status bit (a padded
+ * batch runs only its live rows, TensorRT-LLM PR #21179, breakable prefill
+ * CUDA graphs commit).  Any other id outside [0, num_slots) is an error.
+ */
+#define KDA_PAD_SLOT_ID (-1)
+
 /* ---- flags of kda_chunk_prefill ------------------------------------------ */
 #define KDA_LOAD_INITIAL 1  /* S0 of sequence n = state_pool[slot_ids[n]]; else S0 = 0          */
 #define KDA_FINAL_TO_POOL 2 /* final state of sequence n -> state_pool[slot_ids[n]]; else dense */
@@ -145,10 +155,16 @@ KDA_API int kda_chunk_prefill(const uint16_t *q, const uint16_t *k, const uint16
  *  q, k, v, g       [B*T, H, 128] bf16 (request b's draft tokens are rows b*T .. b*T+T-1)
  *  beta_logits      [B*T, H] bf16
  *  state_pool       [num_slots, H, 128, 128] fp32, READ ONLY
- *  slot_ids         [B] int32, any values in [0, num_slots) (repeats allowed)
+ *  slot_ids         [B] int32, any values in [0, num_slots) (repeats allowed),
+ *                   or KDA_PAD_SLOT_ID for a padding row (its out rows and
+ *                   intermediate_states rows are left as they were)
  *  out              [B*T, H, 128] bf16
  *  intermediate_states [B, T, H, 128, 128] fp32: row (b, t) = state after draft token t
  *  1 <= T <= 64.
+ *
+ * The call reads no device memory on the host and derives its launch from
+ * (B, T, H) alone, so it can be captured in a CUDA graph once per (B, T)
+ * bucket and replayed with new token data and slot ids in the same buffers.
  */
 KDA_API int kda_recurrent_verify(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                          int64_t qkv_token_stride, const uint16_t *g, int64_t g_token_stride,
@@ -168,10 +184,11 @@ KDA_API int kda_recurrent_verify(const uint16_t *q, const uint16_t *k, const uin
  * For each request b with n = num_accepted[b] accepted draft tokens, copies
  * intermediate_states[b, n-1] (all heads) into state_pool[slot_ids[b]]; n = 0
  * leaves the slot untouched.  Counts outside [0, T] or slots outside
- * [0, num_slots) skip that request and set a device status bit.
+ * [0, num_slots) skip that request and set a device status bit, except
+ * KDA_PAD_SLOT_ID rows, which are skipped without one.
  *
  *  state_pool          [num_slots, H, 128, 128] fp32, written
- *  slot_ids            [B] int32 device, distinct
+ *  slot_ids            [B] int32 device, distinct (padding rows excepted)
  *  num_accepted        [B] int32 device
  *  intermediate_states [B, T, H, 128, 128] fp32 (as written by kda_recurrent_verify)
  */

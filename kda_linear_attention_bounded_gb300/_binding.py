@@ -25,6 +25,7 @@ KDA_DEVICE_TIMEOUT = 2
 KDA_DEVICE_BAD_COUNT = 4
 KDA_LOAD_INITIAL = 1
 KDA_FINAL_TO_POOL = 2
+KDA_PAD_SLOT_ID = -1
 
 #: exported symbols of include/kda.h
 EXPORTS = ("kda_status_string", "kda_workspace_size", "kda_prefill_workspace_size", "kda_workspace_reset",

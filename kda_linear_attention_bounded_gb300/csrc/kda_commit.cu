@@ -3,7 +3,7 @@
 // (vLLM PR #55737 "Use FlashKDA for KDA chunked prefill", follow-up commit:
 // spec tokens keep the recurrent kernel "with num_accepted_tokens rollback";
 // the per-step states are the rows written by the one-launch verify of
-// TensorRT-LLM PR #21179).  n = 0 leaves the pool untouched.
+// TensorRT-LLM PR #21179).  n = 0 and padding rows leave the pool untouched.
 //
 // A pure HBM copy: one CTA per (request, head) moves 64 KiB with 16-byte
 // loads and stores.
@@ -22,6 +22,7 @@ __global__ void __launch_bounds__(kThreads) commit_kernel(CommitArgs p) {
   const int n = p.num_accepted[b];
   if (n == 0) return;
   const int slot = p.slot_ids[b];
+  if (slot == KDA_PAD_SLOT_ID) return;   // padding row of a bucketed batch
   if (n < 0 || n > p.T || slot < 0 || slot >= p.num_slots) {
     if (threadIdx.x == 0) atomicOr(p.status, (n < 0 || n > p.T) ? KDA_DEVICE_BAD_COUNT : KDA_DEVICE_BAD_SLOT);
     return;

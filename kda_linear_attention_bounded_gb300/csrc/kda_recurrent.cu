@@ -49,6 +49,7 @@ __global__ void __launch_bounds__(kThreads, 2) recurrent_kernel(RecurrentArgs p)
   int slot = -1;
   if (p.slot_ids) {
     slot = p.slot_ids[n];
+    if (slot == KDA_PAD_SLOT_ID) return;   // padding row of a bucketed batch
     if (slot < 0 || slot >= p.num_slots) {
       if (tid == 0) atomicOr(p.status, KDA_DEVICE_BAD_SLOT);
       return;

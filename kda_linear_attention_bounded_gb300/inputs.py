@@ -203,10 +203,23 @@ def verify_64x8() -> VerifyInputs:
     return verify_inputs("verify_64x8_h16", 64, 8, 16, seed=1004, pool_slots=256)
 
 
+def verify_64x4() -> VerifyInputs:
+    """64 requests x draft block of 4 tokens (MTP-3: three drafts plus the
+    bonus token), H=16, 256-slot pool."""
+    return verify_inputs("verify_64x4_h16", 64, 4, 16, seed=1005, pool_slots=256)
+
+
+def verify_64x1() -> VerifyInputs:
+    """64 requests x 1 token (plain decode step), H=16, 256-slot pool."""
+    return verify_inputs("verify_64x1_h16", 64, 1, 16, seed=1006, pool_slots=256)
+
+
 NAMED = {
     "prefill_1x256_h2": tiny_prefill,
     "prefill_2048x8_h16": prefill_2048x8,
     "prefill_8192x4_h16": prefill_8192x4,
     "prefill_16384+16varlen_h16": varlen_16384_plus_16,
     "verify_64x8_h16": verify_64x8,
+    "verify_64x4_h16": verify_64x4,
+    "verify_64x1_h16": verify_64x1,
 }

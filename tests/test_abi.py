@@ -32,6 +32,14 @@ def test_header_declares_the_entry_points():
         assert name in syms
 
 
+def test_binding_constants_match_the_header():
+    from kda_linear_attention_bounded_gb300 import _binding as b
+    defines = re.findall(r"#define\s+(KDA_[A-Z_0-9]+)\s+\(?(-?\d+)u?\)?", open(HEADER).read())
+    assert len(defines) >= 11
+    for name, value in defines:
+        assert getattr(b, name) == int(value), name
+
+
 def test_every_declared_symbol_is_exported(lib):
     missing = [s for s in declared_symbols() if not hasattr(lib, s)]
     assert not missing, f"not exported: {missing}"
