@@ -9,8 +9,10 @@ CUDA-event time), the per-kernel split is in profiles/.  Also timed: the same ca
 buffers (pinned H2D of the step's inputs + D2H of its outputs inside the
 timed region), the verify call on 64 requests x 8, 4 and 1 tokens and the
 accept/commit after it (each captured in a CUDA graph and replayed, the way a
-serving step runs them), and the fp64 CPU oracle on a bounded sample of the
-prefill workload.
+serving step runs them), one speculative-decoding step (a 4 x 2048-token
+prefill segment beside 64 verify requests x 4 tokens, every output row stored
+by index into the layer output), and the fp64 CPU oracle on a bounded sample
+of the prefill workload.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 N > 1 runs under torchrun, one replica per GPU (weak scaling, no collective on
@@ -58,6 +60,14 @@ def prefill_algorithmic_bytes(inp):
 def verify_algorithmic_bytes(inp):
     BT, H = inp.B * inp.T, inp.H
     return BT * H * TOKEN_HEAD_BYTES + inp.B * H * STATE_BYTES * (1 + inp.T)
+
+
+def spec_step_algorithmic_bytes(inp):
+    """Both segments' bytes (prefill: initial and final state per sequence and head) plus the int32 row index of
+    every token."""
+    p, v = inp.prefill, inp.verify
+    return (prefill_algorithmic_bytes(p) + verify_algorithmic_bytes(v) +
+            4 * (p.total_tokens + v.B * v.T))
 
 
 # sources that decide each kernel's code (a traffic record is valid while they are unchanged)
@@ -274,7 +284,7 @@ def run_gpu(args):
     sys.path.insert(0, os.path.join(ROOT, "tests"))
     import kda_linear_attention_bounded_gb300 as kda
     from kda_linear_attention_bounded_gb300 import inputs
-    from gpu_helpers import DevicePrefill, DeviceVerify
+    from gpu_helpers import DevicePrefill, DeviceSpecStep, DeviceVerify
 
     kda.load()
     inp = inputs.prefill_2048x8()
@@ -426,6 +436,31 @@ def run_gpu(args):
     assert kda.read_device_status(ws) == 0
 
     del inter
+
+    # ---- one spec step: prefill segment + verify segment, outputs written by index into the layer output ----
+    sdev = DeviceSpecStep(inputs.spec_step_2048x4_64x4(), device=device)
+    sin = sdev.inp
+    s_ws = sdev.workspace()
+    s_out = sdev.new_out()
+    s_inter = torch.empty((sin.verify.B, sin.verify.T, H, 128, 128), dtype=torch.float32, device=device)
+    for _ in range(3):
+        sdev.run(out=s_out, intermediate_states=s_inter, workspace=s_ws)
+    s_steps = max(3, min(args.steps, 200))
+    s0 = torch.cuda.Event(enable_timing=True)
+    s1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(device)
+    s0.record(stream)
+    for _ in range(s_steps):
+        sdev.run(out=s_out, intermediate_states=s_inter, workspace=s_ws, stream=stream)
+    s1.record(stream)
+    torch.cuda.synchronize(device)
+    assert kda.read_device_status(s_ws) == 0
+    s_us = s0.elapsed_time(s1) * 1e3 / s_steps
+    s_bytes = spec_step_algorithmic_bytes(sin)
+    s_achieved = s_bytes / (s_us * 1e-6) / 1e9
+    s_tokens = sin.prefill.total_tokens + sin.verify.B * sin.verify.T
+    del sdev, s_ws, s_out, s_inter
+
     if rank != 0:
         return
     cpu = None if args.no_cpu_baseline or world > 1 else cpu_baseline(inp)
@@ -451,6 +486,10 @@ def run_gpu(args):
         "clocks": clocks,
         "verify": vrec,
         "verify_variants": vvariants,
+        "spec_step": {"workload": sin.name, "us_per_layer": s_us, "steps": s_steps, "tokens": s_tokens,
+                      "tokens_per_s": s_tokens / (s_us * 1e-6), "launches_per_call": 3,
+                      "roofline": {"bound": "hbm", "achieved": s_achieved, "peak": peak, "unit": "GB/s",
+                                   "frac": s_achieved / peak, "algorithmic_bytes": s_bytes}},
         "commit": {"workload": vin.name + " (1..8 accepted per request)", "us_per_layer": c_us, "calls_timed": c_steps,
                    "roofline": {"bound": "hbm", "achieved": c_achieved, "peak": peak, "unit": "GB/s",
                                 "frac": c_achieved / peak, "algorithmic_bytes": c_bytes}},

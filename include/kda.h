@@ -68,6 +68,7 @@ extern "C" {
 #define KDA_DEVICE_BAD_SLOT 1u /* a slot id was outside [0, num_slots); that work item was skipped */
 #define KDA_DEVICE_TIMEOUT 2u  /* a bounded wait inside a kernel gave up (a lost async completion); results are incomplete */
 #define KDA_DEVICE_BAD_COUNT 4u /* an accepted-token count was outside [0, T]; that request was skipped */
+#define KDA_DEVICE_BAD_INDEX 8u /* an output row index was outside [0, num_out_tokens); that row was not written */
 
 /*
  * Slot id of a padding row.  A batch captured in a CUDA graph for a bucket of
@@ -82,6 +83,19 @@ extern "C" {
 /* ---- flags of kda_chunk_prefill ------------------------------------------ */
 #define KDA_LOAD_INITIAL 1  /* S0 of sequence n = state_pool[slot_ids[n]]; else S0 = 0          */
 #define KDA_FINAL_TO_POOL 2 /* final state of sequence n -> state_pool[slot_ids[n]]; else dense */
+
+/*
+ * q, k, v, g and beta_logits of one set of tokens, laid out as in the
+ * conventions above (used by kda_spec_step, which takes two such sets).
+ */
+typedef struct kda_token_tensors {
+  const uint16_t *q, *k, *v;     /* [tokens, H, 128] bf16 */
+  int64_t qkv_token_stride;      /* elements, shared by q, k, v */
+  const uint16_t *g;             /* [tokens, H, 128] bf16 raw gate input */
+  int64_t g_token_stride;
+  const uint16_t *beta_logits;   /* [tokens, H] bf16 */
+  int64_t beta_token_stride;
+} kda_token_tensors;
 
 /* Static, human-readable text for a status code. */
 KDA_API const char *kda_status_string(int status);
@@ -98,7 +112,8 @@ KDA_API size_t kda_workspace_size(void);
  */
 KDA_API size_t kda_prefill_workspace_size(int64_t total_tokens, int num_seqs, int H);
 
-/* Clear the device status word (an async memset on `stream`). */
+/* Clear the device status word and the rest of the first kda_workspace_size()
+ * bytes (an async memset on `stream`). */
 KDA_API int kda_workspace_reset(void *workspace, size_t workspace_bytes, void *stream);
 
 /*
@@ -196,6 +211,56 @@ KDA_API int kda_commit_accepted(float *state_pool, int num_slots, const int32_t 
                                 const int32_t *num_accepted, const float *intermediate_states,
                                 int B, int T, int H, void *workspace, size_t workspace_bytes,
                                 void *stream);
+
+/*
+ * One speculative-decoding step of a KDA layer: the prefill segment (the
+ * non-speculative tokens, chunked, as kda_chunk_prefill) and the verify
+ * segment (B requests x T draft tokens, as kda_recurrent_verify) in one call,
+ * both writing their outputs straight into the layer's output rows through
+ * the step's index arrays.  Source: vLLM PR #55737 "Use FlashKDA for KDA
+ * chunked prefill", follow-up commit: in a step that carries spec-decode
+ * tokens the prefill segment runs on the chunked kernel, its outputs are
+ * scattered by non_spec_token_indx, the spec tokens' by spec_token_indx
+ * (recurrent kernel, num_accepted_tokens rollback), and the merge writes
+ * directly into core_attn_out.  Here no intermediate output buffer and no
+ * merge pass exist: each kernel stores its rows at their final place.
+ *
+ *  prefill          tokens of the prefill segment ([T_p, H, 128], T_p =
+ *                   cu_seqlens_host[num_seqs]); may be NULL when num_seqs == 0
+ *  cu_seqlens_dev / cu_seqlens_host / num_seqs / prefill_slot_ids / flags /
+ *  final_state      as in kda_chunk_prefill (num_seqs == 0: no prefill segment)
+ *  spec             tokens of the verify segment ([B*T, H, 128]); may be NULL when B == 0
+ *  B, T, spec_slot_ids, intermediate_states
+ *                   as in kda_recurrent_verify (B == 0: no verify segment;
+ *                   KDA_PAD_SLOT_ID rows are skipped)
+ *  A_log, dt_bias, lower_bound, scale, H, state_pool, num_slots
+ *                   shared by both segments (one layer)
+ *  core_attn_out    [num_out_tokens, H, 128] bf16, token stride out_token_stride
+ *  non_spec_token_indx [T_p] int32 device: output row of prefill token i
+ *  spec_token_indx  [B*T] int32 device: output row of verify token j (= b*T + t)
+ *
+ * Preconditions: the output rows named by the two index arrays are distinct
+ * (rows named by neither are left as they were).  An index outside
+ * [0, num_out_tokens) leaves that row unwritten and sets KDA_DEVICE_BAD_INDEX.
+ * The pool slots the prefill segment writes back (KDA_FINAL_TO_POOL) are not
+ * among spec_slot_ids.  Launch order on `stream`: the prefill's two kernels,
+ * then the verify kernel as a programmatic dependent of the state pass, so
+ * that verify CTAs run on the SMs the state pass leaves free; the call's work
+ * is complete, for whatever the stream runs next, when its last kernel is.
+ * workspace: at least kda_prefill_workspace_size(T_p, num_seqs, H) bytes,
+ * cleared once by kda_workspace_reset before its first use (the step keeps a
+ * counter beside the status word and leaves it at zero).  Arguments of both
+ * segments are checked before anything is launched.
+ */
+KDA_API int kda_spec_step(const kda_token_tensors *prefill, const int32_t *cu_seqlens_dev,
+                          const int32_t *cu_seqlens_host, int num_seqs, const int32_t *prefill_slot_ids,
+                          int flags, float *final_state, const kda_token_tensors *spec, int B, int T,
+                          const int32_t *spec_slot_ids, float *intermediate_states, const float *A_log,
+                          const float *dt_bias, float lower_bound, float scale, int H, float *state_pool,
+                          int num_slots, uint16_t *core_attn_out, int64_t out_token_stride,
+                          int64_t num_out_tokens, const int32_t *non_spec_token_indx,
+                          const int32_t *spec_token_indx, void *workspace, size_t workspace_bytes,
+                          void *stream);
 
 /*
  * kda_recurrent_verify without a workspace.  The pages have no counterpart:

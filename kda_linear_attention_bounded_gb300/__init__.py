@@ -1,14 +1,16 @@
 """KDA bounded-gate linear attention on GB300 (sm_103a).
 
-Two calls, backed by libkda's CUDA kernels (``include/kda.h``):
+Four calls, backed by libkda's CUDA kernels (``include/kda.h``):
 
 * :func:`chunk_prefill` -- chunked varlen prefill with a pooled fp32 state;
 * :func:`recurrent_verify` -- speculative-decode verify writing every per-step state;
-* :func:`commit_accepted` -- accept/commit: the state after the last accepted draft token back into the pool.
+* :func:`commit_accepted` -- accept/commit: the state after the last accepted draft token back into the pool;
+* :func:`spec_step` -- one speculative-decoding step: prefill segment and verify segment in one call, their
+  outputs written straight into the layer's output rows by index.
 
 The binding is loaded on first use and raises if libkda has not been built.
 """
 from ._binding import (  # noqa: F401
-    KDA_DEVICE_BAD_COUNT, KDA_DEVICE_BAD_SLOT, KDA_DEVICE_TIMEOUT, KDA_ERR_CUDA, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_WORKSPACE,
+    KDA_DEVICE_BAD_COUNT, KDA_DEVICE_BAD_INDEX, KDA_DEVICE_BAD_SLOT, KDA_DEVICE_TIMEOUT, KDA_ERR_CUDA, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_WORKSPACE,
     KDA_FINAL_TO_POOL, KDA_LOAD_INITIAL, KDA_OK, KDA_PAD_SLOT_ID, KdaError, chunk_prefill, commit_accepted, load, make_workspace,
-    prefill_workspace_size, read_device_status, recurrent_verify, status_string, workspace_size)
+    prefill_workspace_size, read_device_status, recurrent_verify, spec_step, status_string, workspace_size)

@@ -23,6 +23,7 @@ KDA_ERR_CUDA = 4
 KDA_DEVICE_BAD_SLOT = 1
 KDA_DEVICE_TIMEOUT = 2
 KDA_DEVICE_BAD_COUNT = 4
+KDA_DEVICE_BAD_INDEX = 8
 KDA_LOAD_INITIAL = 1
 KDA_FINAL_TO_POOL = 2
 KDA_PAD_SLOT_ID = -1
@@ -30,9 +31,16 @@ KDA_PAD_SLOT_ID = -1
 #: exported symbols of include/kda.h
 EXPORTS = ("kda_status_string", "kda_workspace_size", "kda_prefill_workspace_size", "kda_workspace_reset",
            "kda_read_device_status", "kda_chunk_prefill", "kda_recurrent_verify", "kda_commit_accepted",
-           "kda_recurrent_verify_noalloc")
+           "kda_recurrent_verify_noalloc", "kda_spec_step")
 
 _lib = None
+
+
+class TokenTensors(ctypes.Structure):
+    """``kda_token_tensors``: q, k, v, g, beta_logits of one set of tokens."""
+    _fields_ = [("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+                ("qkv_token_stride", ctypes.c_int64), ("g", ctypes.c_void_p), ("g_token_stride", ctypes.c_int64),
+                ("beta_logits", ctypes.c_void_p), ("beta_token_stride", ctypes.c_int64)]
 
 
 class KdaError(RuntimeError):
@@ -74,6 +82,10 @@ def load():
     lib.kda_recurrent_verify.restype = I
     lib.kda_commit_accepted.argtypes = [P, I, P, P, P, I, I, I, P, SZ, P]
     lib.kda_commit_accepted.restype = I
+    TT = ctypes.POINTER(TokenTensors)
+    lib.kda_spec_step.argtypes = [TT, P, P, I, P, I, P, TT, I, I, P, P, P, P, F, F, I, P, I, P, I64, I64, P, P, P,
+                                  SZ, P]
+    lib.kda_spec_step.restype = I
     _lib = lib
     return lib
 
@@ -222,3 +234,68 @@ def commit_accepted(state_pool, slot_ids, num_accepted, intermediate_states, *, 
     if rc != KDA_OK:
         raise KdaError(rc, "kda_commit_accepted")
     return state_pool
+
+
+def _token_struct(tensors, H):
+    """(q, k, v, g, beta_logits) -> (TokenTensors, tokens)."""
+    q, k, v, g, beta = tensors
+    qs = _token_tensor(q, "q", H)
+    if _token_tensor(k, "k", H) != qs or _token_tensor(v, "v", H) != qs:
+        raise ValueError("q, k and v must share one token stride")
+    if k.shape[0] != q.shape[0] or v.shape[0] != q.shape[0] or g.shape[0] != q.shape[0] or beta.shape[0] != q.shape[0]:
+        raise ValueError("q, k, v, g and beta_logits must have the same number of tokens")
+    tt = TokenTensors(q.data_ptr(), k.data_ptr(), v.data_ptr(), qs, g.data_ptr(), _token_tensor(g, "g", H),
+                      beta.data_ptr(), _beta_stride(beta, H))
+    return tt, q.shape[0]
+
+
+def spec_step(prefill, cu_seqlens, cu_seqlens_host, spec, T, A_log, dt_bias, state_pool, core_attn_out,
+              non_spec_token_indx, spec_token_indx, *, prefill_slot_ids=None, spec_slot_ids=None,
+              load_initial=False, final_to_pool=False, final_state=None, intermediate_states=None,
+              lower_bound=-5.0, scale=None, workspace=None, stream=None):
+    """``kda_spec_step``: the prefill segment and the verify segment of one speculative-decoding step, their
+    outputs written into ``core_attn_out`` rows ``non_spec_token_indx`` / ``spec_token_indx``.
+
+    ``prefill`` and ``spec`` are ``(q, k, v, g, beta_logits)`` tuples (or None for an absent segment).
+    Returns ``(core_attn_out, final_state, intermediate_states)``."""
+    lib = load()
+    H = core_attn_out.shape[1]
+    os_ = _token_tensor(core_attn_out, "core_attn_out", H)
+    dev = core_attn_out.device
+    pre = spc = None
+    N = B = Tp = 0
+    cu_host = None
+    if prefill is not None:
+        pre, Tp = _token_struct(prefill, H)
+        cu_host = torch.as_tensor(cu_seqlens_host, dtype=torch.int32).contiguous()
+        if cu_host.is_cuda:
+            raise ValueError("cu_seqlens_host must be in host memory")
+        N = cu_host.numel() - 1
+        if not final_to_pool and final_state is None:
+            final_state = torch.empty((N, H, 128, 128), dtype=torch.float32, device=dev)
+    if spec is not None:
+        spc, Bt = _token_struct(spec, H)
+        if Bt % T:
+            raise ValueError("spec segment: tokens must be a multiple of T")
+        B = Bt // T
+        if intermediate_states is None:
+            intermediate_states = torch.empty((B, T, H, 128, 128), dtype=torch.float32, device=dev)
+    for name, idx, n in (("non_spec_token_indx", non_spec_token_indx, Tp), ("spec_token_indx", spec_token_indx, B * T)):
+        if n and (idx is None or idx.dtype != torch.int32 or not idx.is_cuda or idx.numel() != n or not idx.is_contiguous()):
+            raise ValueError(f"{name}: expected a contiguous CUDA int32 tensor of {n} entries")
+    if workspace is None:
+        workspace = make_workspace(dev, stream, prefill_workspace_size(Tp, N, H))
+    flags = (KDA_LOAD_INITIAL if load_initial else 0) | (KDA_FINAL_TO_POOL if final_to_pool else 0)
+    if scale is None:
+        scale = 1.0 / math.sqrt(128.0)
+    rc = lib.kda_spec_step(
+        None if pre is None else ctypes.byref(pre), _ptr(cu_seqlens),
+        None if cu_host is None else ctypes.c_void_p(cu_host.data_ptr()), N, _ptr(prefill_slot_ids), flags,
+        _ptr(None if final_to_pool else final_state), None if spc is None else ctypes.byref(spc), B, int(T),
+        _ptr(spec_slot_ids), _ptr(intermediate_states), _ptr(A_log), _ptr(dt_bias), float(lower_bound),
+        float(scale), H, _ptr(state_pool), 0 if state_pool is None else state_pool.shape[0], _ptr(core_attn_out),
+        os_, core_attn_out.shape[0], _ptr(non_spec_token_indx), _ptr(spec_token_indx), _ptr(workspace),
+        workspace.numel(), _stream_ptr(stream, dev))
+    if rc != KDA_OK:
+        raise KdaError(rc, "kda_spec_step")
+    return core_attn_out, (None if final_to_pool else final_state), intermediate_states

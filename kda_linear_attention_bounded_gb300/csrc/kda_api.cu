@@ -12,6 +12,8 @@
 namespace {
 
 constexpr size_t kWorkspaceBytes = 256;
+static_assert(kda::kDoneCounterOffset + sizeof(uint32_t) <= kWorkspaceBytes,
+              "the spec step's CTA counter must sit in the cleared header");
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -44,6 +46,85 @@ int check_token_tensors(const uint16_t *q, const uint16_t *k, const uint16_t *v,
   if (!good_stride(qkv_stride, row) || !good_stride(g_stride, row) || !good_stride(out_stride, row))
     return KDA_ERR_INVALID_ARG;
   if (beta_stride < H) return KDA_ERR_INVALID_ARG;
+  return KDA_OK;
+}
+
+// Host-side checks of one prefill call; on success fills `a` (no launch).
+int prepare_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v, int64_t qkv_token_stride,
+                    const uint16_t *g, int64_t g_token_stride, const uint16_t *beta_logits,
+                    int64_t beta_token_stride, const float *A_log, const float *dt_bias, float lower_bound,
+                    float scale, const int32_t *cu_seqlens_dev, const int32_t *cu_seqlens_host, int num_seqs,
+                    int H, float *state_pool, int num_slots, const int32_t *slot_ids, int flags, uint16_t *out,
+                    int64_t out_token_stride, float *final_state, void *workspace, size_t workspace_bytes,
+                    kda::ChunkArgs *a) {
+  if (int rc = check_workspace(workspace, workspace_bytes)) return rc;
+  if (num_seqs < 0) return KDA_ERR_INVALID_ARG;
+  if (!cu_seqlens_dev || !cu_seqlens_host) return KDA_ERR_INVALID_ARG;
+  if (flags & ~(KDA_LOAD_INITIAL | KDA_FINAL_TO_POOL)) return KDA_ERR_INVALID_ARG;
+  if (cu_seqlens_host[0] != 0) return KDA_ERR_INVALID_ARG;
+  for (int n = 0; n < num_seqs; ++n)
+    if (cu_seqlens_host[n + 1] < cu_seqlens_host[n]) return KDA_ERR_INVALID_ARG;
+  *a = kda::ChunkArgs{};
+  if (num_seqs == 0) return KDA_OK;   // a->num_seqs = 0: nothing to launch
+  if (int rc = check_token_tensors(q, k, v, qkv_token_stride, g, g_token_stride, beta_logits,
+                                   beta_token_stride, A_log, dt_bias, out, out_token_stride, H))
+    return rc;
+  if (int rc = check_gate(lower_bound, scale)) return rc;
+  const bool use_pool = flags & (KDA_LOAD_INITIAL | KDA_FINAL_TO_POOL);
+  if (use_pool && (!state_pool || !slot_ids || num_slots <= 0 || !aligned16(state_pool)))
+    return KDA_ERR_INVALID_ARG;
+  if (!(flags & KDA_FINAL_TO_POOL) && (!final_state || !aligned16(final_state))) return KDA_ERR_INVALID_ARG;
+  if (workspace_bytes < kda::prefill_workspace_bytes(cu_seqlens_host[num_seqs], num_seqs, H)) return KDA_ERR_WORKSPACE;
+
+  a->q = q; a->k = k; a->v = v; a->g = g; a->beta = beta_logits;
+  a->qkv_stride = qkv_token_stride; a->g_stride = g_token_stride;
+  a->beta_stride = beta_token_stride; a->out_stride = out_token_stride;
+  a->A_log = A_log; a->dt_bias = dt_bias;
+  a->lower_bound = lower_bound; a->scale = scale;
+  a->H = H; a->num_seqs = num_seqs; a->total_tokens = cu_seqlens_host[num_seqs];
+  a->cu_seqlens = cu_seqlens_dev;
+  a->slot_ids = use_pool ? slot_ids : nullptr;
+  a->num_slots = num_slots;
+  a->state_in = (flags & KDA_LOAD_INITIAL) ? state_pool : nullptr;
+  a->state_out_pool = (flags & KDA_FINAL_TO_POOL) ? state_pool : nullptr;
+  a->state_out_dense = (flags & KDA_FINAL_TO_POOL) ? nullptr : final_state;
+  a->out = out;
+  a->status = static_cast<uint32_t *>(workspace);
+  return KDA_OK;
+}
+
+// Host-side checks of one verify call; on success fills `a` (no launch).
+int prepare_verify(const uint16_t *q, const uint16_t *k, const uint16_t *v, int64_t qkv_token_stride,
+                   const uint16_t *g, int64_t g_token_stride, const uint16_t *beta_logits, int64_t beta_token_stride,
+                   const float *A_log, const float *dt_bias, float lower_bound, float scale, int B, int T, int H,
+                   const float *state_pool, int num_slots, const int32_t *slot_ids, uint16_t *out,
+                   int64_t out_token_stride, float *intermediate_states, void *workspace, size_t workspace_bytes,
+                   kda::RecurrentArgs *a) {
+  if (int rc = check_workspace(workspace, workspace_bytes)) return rc;
+  if (B < 0 || T < 1 || T > 64) return KDA_ERR_INVALID_ARG;
+  *a = kda::RecurrentArgs{};
+  if (B == 0) return KDA_OK;
+  if (int rc = check_token_tensors(q, k, v, qkv_token_stride, g, g_token_stride, beta_logits,
+                                   beta_token_stride, A_log, dt_bias, out, out_token_stride, H))
+    return rc;
+  if (int rc = check_gate(lower_bound, scale)) return rc;
+  if (!state_pool || !aligned16(state_pool) || num_slots <= 0 || !slot_ids) return KDA_ERR_INVALID_ARG;
+  if (!intermediate_states || !aligned16(intermediate_states)) return KDA_ERR_INVALID_ARG;
+
+  a->q = q; a->k = k; a->v = v; a->g = g; a->beta = beta_logits;
+  a->qkv_stride = qkv_token_stride; a->g_stride = g_token_stride;
+  a->beta_stride = beta_token_stride; a->out_stride = out_token_stride;
+  a->A_log = A_log; a->dt_bias = dt_bias;
+  a->lower_bound = lower_bound; a->scale = scale;
+  a->H = H;
+  a->cu_seqlens = nullptr;
+  a->T = T;
+  a->slot_ids = slot_ids;
+  a->num_slots = num_slots;
+  a->state_in = state_pool;
+  a->inter = intermediate_states;
+  a->out = out;
+  a->status = static_cast<uint32_t *>(workspace);
   return KDA_OK;
 }
 
@@ -94,39 +175,12 @@ int kda_chunk_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v, i
                       int num_slots, const int32_t *slot_ids, int flags, uint16_t *out,
                       int64_t out_token_stride, float *final_state, void *workspace,
                       size_t workspace_bytes, void *stream) {
-  if (int rc = check_workspace(workspace, workspace_bytes)) return rc;
-  if (num_seqs < 0) return KDA_ERR_INVALID_ARG;
-  if (!cu_seqlens_dev || !cu_seqlens_host) return KDA_ERR_INVALID_ARG;
-  if (flags & ~(KDA_LOAD_INITIAL | KDA_FINAL_TO_POOL)) return KDA_ERR_INVALID_ARG;
-  if (cu_seqlens_host[0] != 0) return KDA_ERR_INVALID_ARG;
-  for (int n = 0; n < num_seqs; ++n)
-    if (cu_seqlens_host[n + 1] < cu_seqlens_host[n]) return KDA_ERR_INVALID_ARG;
-  if (num_seqs == 0) return KDA_OK;
-  if (int rc = check_token_tensors(q, k, v, qkv_token_stride, g, g_token_stride, beta_logits,
-                                   beta_token_stride, A_log, dt_bias, out, out_token_stride, H))
+  kda::ChunkArgs a;
+  if (int rc = prepare_prefill(q, k, v, qkv_token_stride, g, g_token_stride, beta_logits, beta_token_stride, A_log,
+                               dt_bias, lower_bound, scale, cu_seqlens_dev, cu_seqlens_host, num_seqs, H, state_pool,
+                               num_slots, slot_ids, flags, out, out_token_stride, final_state, workspace,
+                               workspace_bytes, &a))
     return rc;
-  if (int rc = check_gate(lower_bound, scale)) return rc;
-  const bool use_pool = flags & (KDA_LOAD_INITIAL | KDA_FINAL_TO_POOL);
-  if (use_pool && (!state_pool || !slot_ids || num_slots <= 0 || !aligned16(state_pool)))
-    return KDA_ERR_INVALID_ARG;
-  if (!(flags & KDA_FINAL_TO_POOL) && (!final_state || !aligned16(final_state))) return KDA_ERR_INVALID_ARG;
-  if (workspace_bytes < kda::prefill_workspace_bytes(cu_seqlens_host[num_seqs], num_seqs, H)) return KDA_ERR_WORKSPACE;
-
-  kda::ChunkArgs a{};
-  a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta_logits;
-  a.qkv_stride = qkv_token_stride; a.g_stride = g_token_stride;
-  a.beta_stride = beta_token_stride; a.out_stride = out_token_stride;
-  a.A_log = A_log; a.dt_bias = dt_bias;
-  a.lower_bound = lower_bound; a.scale = scale;
-  a.H = H; a.num_seqs = num_seqs; a.total_tokens = cu_seqlens_host[num_seqs];
-  a.cu_seqlens = cu_seqlens_dev;
-  a.slot_ids = use_pool ? slot_ids : nullptr;
-  a.num_slots = num_slots;
-  a.state_in = (flags & KDA_LOAD_INITIAL) ? state_pool : nullptr;
-  a.state_out_pool = (flags & KDA_FINAL_TO_POOL) ? state_pool : nullptr;
-  a.state_out_dense = (flags & KDA_FINAL_TO_POOL) ? nullptr : final_state;
-  a.out = out;
-  a.status = static_cast<uint32_t *>(workspace);
   cudaError_t err = kda::launch_chunk_prefill(a, cu_seqlens_host,
                                               static_cast<uint8_t *>(workspace) + kda::kWorkspaceHeader,
                                               static_cast<cudaStream_t>(stream));
@@ -140,33 +194,61 @@ int kda_recurrent_verify(const uint16_t *q, const uint16_t *k, const uint16_t *v
                          int num_slots, const int32_t *slot_ids, uint16_t *out, int64_t out_token_stride,
                          float *intermediate_states, void *workspace, size_t workspace_bytes,
                          void *stream) {
-  if (int rc = check_workspace(workspace, workspace_bytes)) return rc;
-  if (B < 0 || T < 1 || T > 64) return KDA_ERR_INVALID_ARG;
-  if (B == 0) return KDA_OK;
-  if (int rc = check_token_tensors(q, k, v, qkv_token_stride, g, g_token_stride, beta_logits,
-                                   beta_token_stride, A_log, dt_bias, out, out_token_stride, H))
+  kda::RecurrentArgs a;
+  if (int rc = prepare_verify(q, k, v, qkv_token_stride, g, g_token_stride, beta_logits, beta_token_stride, A_log,
+                              dt_bias, lower_bound, scale, B, T, H, state_pool, num_slots, slot_ids, out,
+                              out_token_stride, intermediate_states, workspace, workspace_bytes, &a))
     return rc;
-  if (int rc = check_gate(lower_bound, scale)) return rc;
-  if (!state_pool || !aligned16(state_pool) || num_slots <= 0 || !slot_ids) return KDA_ERR_INVALID_ARG;
-  if (!intermediate_states || !aligned16(intermediate_states)) return KDA_ERR_INVALID_ARG;
-
-  kda::RecurrentArgs a{};
-  a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta_logits;
-  a.qkv_stride = qkv_token_stride; a.g_stride = g_token_stride;
-  a.beta_stride = beta_token_stride; a.out_stride = out_token_stride;
-  a.A_log = A_log; a.dt_bias = dt_bias;
-  a.lower_bound = lower_bound; a.scale = scale;
-  a.H = H;
-  a.cu_seqlens = nullptr;
-  a.T = T;
-  a.slot_ids = slot_ids;
-  a.num_slots = num_slots;
-  a.state_in = state_pool;
-  a.inter = intermediate_states;
-  a.out = out;
-  a.status = static_cast<uint32_t *>(workspace);
   cudaError_t err = kda::launch_recurrent(a, B, static_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+int kda_spec_step(const kda_token_tensors *prefill, const int32_t *cu_seqlens_dev, const int32_t *cu_seqlens_host,
+                  int num_seqs, const int32_t *prefill_slot_ids, int flags, float *final_state,
+                  const kda_token_tensors *spec, int B, int T, const int32_t *spec_slot_ids,
+                  float *intermediate_states, const float *A_log, const float *dt_bias, float lower_bound,
+                  float scale, int H, float *state_pool, int num_slots, uint16_t *core_attn_out,
+                  int64_t out_token_stride, int64_t num_out_tokens, const int32_t *non_spec_token_indx,
+                  const int32_t *spec_token_indx, void *workspace, size_t workspace_bytes, void *stream) {
+  if (num_seqs < 0 || B < 0 || num_out_tokens < 0 || (num_seqs > 0 && !prefill) || (B > 0 && !spec))
+    return KDA_ERR_INVALID_ARG;
+  if (int rc = check_workspace(workspace, workspace_bytes)) return rc;
+  kda::ChunkArgs pa{};       // an absent segment keeps num_seqs = 0 / B = 0 and is not checked further
+  kda::RecurrentArgs va{};
+  if (num_seqs > 0) {
+    const kda_token_tensors &p = *prefill;
+    if (int rc = prepare_prefill(p.q, p.k, p.v, p.qkv_token_stride, p.g, p.g_token_stride, p.beta_logits,
+                                 p.beta_token_stride, A_log, dt_bias, lower_bound, scale, cu_seqlens_dev,
+                                 cu_seqlens_host, num_seqs, H, state_pool, num_slots, prefill_slot_ids, flags,
+                                 core_attn_out, out_token_stride, final_state, workspace, workspace_bytes, &pa))
+      return rc;
+  }
+  if (B > 0) {
+    const kda_token_tensors &s = *spec;
+    if (int rc = prepare_verify(s.q, s.k, s.v, s.qkv_token_stride, s.g, s.g_token_stride, s.beta_logits,
+                                s.beta_token_stride, A_log, dt_bias, lower_bound, scale, B, T, H, state_pool,
+                                num_slots, spec_slot_ids, core_attn_out, out_token_stride, intermediate_states,
+                                workspace, workspace_bytes, &va))
+      return rc;
+  }
+  const bool has_prefill = pa.num_seqs > 0 && pa.total_tokens > 0, has_spec = B > 0;
+  if ((has_prefill && !non_spec_token_indx) || (has_spec && !spec_token_indx)) return KDA_ERR_INVALID_ARG;
+  if (num_out_tokens > INT32_MAX) return KDA_ERR_INVALID_ARG;
+  pa.out_index = non_spec_token_indx;
+  pa.num_out_rows = num_out_tokens;
+  va.out_index = spec_token_indx;
+  va.num_out_rows = num_out_tokens;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // the prefill's two kernels, then the verify grid as a programmatic dependent of the state pass: the state
+  // pass occupies one SM per (sequence, head) and the verify CTAs fill the others while it runs
+  if (pa.num_seqs > 0) {
+    if (kda::launch_chunk_prefill(pa, cu_seqlens_host, static_cast<uint8_t *>(workspace) + kda::kWorkspaceHeader,
+                                  st) != cudaSuccess)
+      return KDA_ERR_CUDA;
+    va.done_counter = reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(workspace) + kda::kDoneCounterOffset);
+  }
+  if (has_spec && kda::launch_recurrent(va, B, st) != cudaSuccess) return KDA_ERR_CUDA;
+  return KDA_OK;
 }
 
 int kda_commit_accepted(float *state_pool, int num_slots, const int32_t *slot_ids, const int32_t *num_accepted,

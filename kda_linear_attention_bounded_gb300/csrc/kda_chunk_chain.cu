@@ -88,6 +88,10 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_chain_kernel(const __grid_c
   const uint8_t *blk0 = prm.blocks + (static_cast<size_t>(prm.chunk_off[nl]) * H + h) * kBlkBytes;
   const size_t blk_step = static_cast<size_t>(H) * kBlkBytes;
 
+  // every CTA of this grid has started once all have passed here: a grid launched after it as a programmatic
+  // dependent (the verify segment of a spec step) may then use the SMs this grid leaves free
+  grid_launch_dependents();
+
   int slot = 0;
   if (prm.slot_ids) {
     slot = prm.slot_ids[n];
@@ -161,6 +165,36 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_chain_kernel(const __grid_c
 
   // output of a chunk (accumulated in pair ob) -> `stage` as the 64-token x 128-channel row-swizzled
   // tile the output tensor map stores (workers)
+  // Scattered output (out_index set): item k of a thread is i = tid + k kThreads of the chunk's rows x 16
+  // sixteen-byte pieces.  The output rows of a chunk are fetched one chunk ahead into registers, so the
+  // store under the next chunk's first product waits on no global load.
+  constexpr int kRowItems = (kC * 16 + kThreads - 1) / kThreads;
+  int32_t orow[kRowItems];
+  auto load_rows = [&](int tok, int rows) {
+#pragma unroll
+    for (int k = 0; k < kRowItems; ++k) {
+      const int i = tid + k * kThreads;
+      orow[k] = i < rows * 16 ? prm.out_index[tok + (i >> 4)] : 0;
+    }
+  };
+  // staged rows 0 .. rows-1 -> the rows in orow (an index outside [0, num_out_rows) skips its piece)
+  auto store_rows_indexed = [&](const uint8_t *stage, int rows) {
+#pragma unroll
+    for (int k = 0; k < kRowItems; ++k) {
+      const int i = tid + k * kThreads;
+      if (i >= rows * 16) break;
+      const int r = i >> 4, cc = i & 15;
+      const int64_t row = orow[k];
+      if (row < 0 || row >= prm.num_out_rows) {
+        if (cc == 0) atomicOr(prm.status, KDA_DEVICE_BAD_INDEX);
+        continue;
+      }
+      *reinterpret_cast<uint4 *>(prm.out + row * prm.out_stride + h * kD + 8 * cc) =
+          *reinterpret_cast<const uint4 *>(stage + swz_offset(64, r, 8 * cc));
+    }
+  };
+  if (prm.out_index && nchunks > 0) load_rows(t0, min(kC, len));
+
   auto out_to_stage = [&](int ob, uint8_t *stage) {
     uint32_t ov[32];
     const uint32_t tb = tmem + lane_base + (ob ? TM_UO1 : TM_UO0) + 64 + 32 * hv;
@@ -197,7 +231,10 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_chain_kernel(const __grid_c
       if (worker) out_to_stage((c - 1) & 1, prev);
       fence_async_smem();
       __syncthreads();
-      if (tid == kIssuer) {   // chunk c - 1 is not the last one: all 64 rows are valid
+      if (prm.out_index) {    // rows scattered to the layer's output rows; then fetch chunk c's rows
+        store_rows_indexed(prev, kC);
+        load_rows(t0 + c * kC, min(kC, len - c * kC));
+      } else if (tid == kIssuer) {   // chunk c - 1 is not the last one: all 64 rows are valid
         const int tok = t0 + (c - 1) * kC;
         tma_store_3d(&prm.tout, 0, h, tok, prev);
         tma_store_3d(&prm.tout, 64, h, tok, prev + 8192);
@@ -303,7 +340,9 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_chain_kernel(const __grid_c
   if (worker) out_to_stage((nchunks - 1) & 1, last);
   fence_async_smem();
   __syncthreads();
-  if (last_valid == kC) {
+  if (prm.out_index) {
+    store_rows_indexed(last, last_valid);
+  } else if (last_valid == kC) {
     if (tid == kIssuer) {
       const int tok = t0 + (nchunks - 1) * kC;
       tma_store_3d(&prm.tout, 0, h, tok, last);

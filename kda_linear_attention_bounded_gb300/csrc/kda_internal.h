@@ -27,8 +27,17 @@ struct RecurrentArgs {
   float *state_out_dense;    // [items, H, D, D] final states, or null
   float *inter;              // [items, T, H, D, D] per-step states, or null
   uint16_t *out;
+  const int32_t *out_index;  // output row of each token, or null (row = token)
+  int64_t num_out_rows;      // rows of out (bounds out_index)
   uint32_t *status;
+  // non-null: the grid is launched as a programmatic dependent of the preceding grid; a zeroed counter in the
+  // workspace (kDoneCounterOffset) through which the CTA that finishes last waits for that grid
+  uint32_t *done_counter;
 };
+
+// Byte offset in the workspace of the counter a programmatic-dependent verify grid counts its CTAs with
+// (inside the part kda_workspace_reset clears).
+constexpr size_t kDoneCounterOffset = 128;
 
 cudaError_t launch_recurrent(const RecurrentArgs &args, int num_items, cudaStream_t stream);
 
@@ -46,6 +55,8 @@ struct ChunkArgs {
   float *state_out_pool;
   float *state_out_dense;
   uint16_t *out;
+  const int32_t *out_index;  // output row of each token, or null (row = token)
+  int64_t num_out_rows;      // rows of out (bounds out_index)
   uint32_t *status;
 };
 
@@ -96,6 +107,8 @@ struct ChainParams {
   float *state_out_dense;       // indexed by seq0 + local sequence
   uint16_t *out;
   int64_t out_stride;
+  const int32_t *out_index;     // output row of each token (global token index), or null: TMA tensor stores
+  int64_t num_out_rows;
   uint32_t *status;
   int H, num_seqs, seq0;
   int32_t chunk_off[kMaxSeqsPerLaunch + 1];

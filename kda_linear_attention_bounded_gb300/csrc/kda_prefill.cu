@@ -76,7 +76,7 @@ cudaError_t launch_chunk_prefill(const ChunkArgs &a, const int32_t *cu_host, uin
       !make_token_map(&ip->tk, a.k, a.H, a.total_tokens, a.qkv_stride, false) ||
       !make_token_map(&ip->tv, a.v, a.H, a.total_tokens, a.qkv_stride) ||
       !make_token_map(&ip->tg, a.g, a.H, a.total_tokens, a.g_stride, false) ||
-      !make_token_map(&cp->tout, a.out, a.H, a.total_tokens, a.out_stride))
+      (!a.out_index && !make_token_map(&cp->tout, a.out, a.H, a.total_tokens, a.out_stride)))
     return cudaErrorInvalidValue;
   ip->beta = a.beta;
   ip->beta_stride = a.beta_stride;
@@ -101,6 +101,8 @@ cudaError_t launch_chunk_prefill(const ChunkArgs &a, const int32_t *cu_host, uin
   cp->state_out_dense = a.state_out_dense;
   cp->out = a.out;
   cp->out_stride = a.out_stride;
+  cp->out_index = a.out_index;   // with an index the output tensor map is not used
+  cp->num_out_rows = a.num_out_rows;
   cp->status = a.status;
   cp->H = a.H;
 

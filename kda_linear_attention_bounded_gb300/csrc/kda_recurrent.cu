@@ -19,6 +19,7 @@
 //   S_t = Diag(alpha) S + k^ u^T
 #include "kda_common.cuh"
 #include "kda_internal.h"
+#include "kda_sm100.cuh"
 
 namespace kda {
 
@@ -29,13 +30,15 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kTile = kWarps;      // tokens prepared per prologue pass (one per warp)
 constexpr int kRows = kD / kWarps;  // key channels per warp (16)
 
-__global__ void __launch_bounds__(kThreads, 2) recurrent_kernel(RecurrentArgs p) {
+// One (request, head) work item.  Every return is taken by the whole CTA.
+__device__ __forceinline__ void recurrent_item(const RecurrentArgs &p) {
   __shared__ __align__(16) float s_khat[kTile][kD];
   __shared__ __align__(16) float s_kalpha[kTile][kD];
   __shared__ __align__(16) float s_qalpha[kTile][kD];
   __shared__ __align__(16) float s_alpha[kTile][kD];
   __shared__ __align__(16) float s_v[kTile][kD];
   __shared__ float s_beta[kTile], s_kq[kTile];
+  __shared__ int64_t s_row[kTile];   // output row of each token of the tile
   __shared__ __align__(16) float s_redk[kWarps][kD];
   __shared__ __align__(16) float s_redq[kWarps][kD];
   __shared__ __align__(16) float s_u[kD];
@@ -118,6 +121,15 @@ __global__ void __launch_bounds__(kThreads, 2) recurrent_kernel(RecurrentArgs p)
       if (lane == 0) {
         s_kq[warp] = kq;
         s_beta[warp] = sigmoid_f(bf16_bits_to_f32(p.beta[(size_t)t * p.beta_stride + h]));
+        int64_t row = t;
+        if (p.out_index) {   // the output row of this token in the layer's output (-1: none)
+          row = p.out_index[t];
+          if (row < 0 || row >= p.num_out_rows) {
+            atomicOr(p.status, KDA_DEVICE_BAD_INDEX);
+            row = -1;
+          }
+        }
+        s_row[warp] = row;
       }
     }
     __syncthreads();
@@ -148,7 +160,8 @@ __global__ void __launch_bounds__(kThreads, 2) recurrent_kernel(RecurrentArgs p)
         const float u = s_beta[s] * (s_v[s][tid] - wk);
         s_u[tid] = u;
         const float o = p.scale * (wq + s_kq[s] * u);
-        p.out[(size_t)t * p.out_stride + h * kD + tid] = f32_to_bf16_bits(o);
+        const int64_t row = s_row[s];
+        if (row >= 0) p.out[row * p.out_stride + h * kD + tid] = f32_to_bf16_bits(o);
       }
       __syncthreads();
       const float4 u4 = *reinterpret_cast<const float4 *>(&s_u[col0]);
@@ -179,12 +192,40 @@ __global__ void __launch_bounds__(kThreads, 2) recurrent_kernel(RecurrentArgs p)
   }
 }
 
+__global__ void __launch_bounds__(kThreads, 2) recurrent_kernel(RecurrentArgs p) {
+  recurrent_item(p);
+  if (p.done_counter) {
+    // launched as a programmatic dependent of the grid before it, which it does not read from: the CTA that
+    // finishes last waits for that grid's completion, so this grid's completion implies it for whatever the
+    // stream runs next; it then clears the counter for the next call on the same workspace
+    __syncthreads();
+    if (threadIdx.x == 0 && atomicAdd(p.done_counter, 1u) == gridDim.x - 1) {
+      sm100::grid_dependency_wait();
+      *p.done_counter = 0;
+    }
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_recurrent(const RecurrentArgs &args, int num_items, cudaStream_t stream) {
   if (num_items <= 0) return cudaSuccess;
-  recurrent_kernel<<<num_items * args.H, kThreads, 0, stream>>>(args);
-  return cudaGetLastError();
+  if (!args.done_counter) {
+    recurrent_kernel<<<num_items * args.H, kThreads, 0, stream>>>(args);
+    return cudaGetLastError();
+  }
+  // programmatic dependent launch: CTAs may be scheduled onto SMs the preceding grid leaves free once every
+  // CTA of that grid has signalled launch_dependents
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(num_items * args.H);
+  cfg.blockDim = dim3(kThreads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, recurrent_kernel, args);
 }
 
 }  // namespace kda

@@ -167,6 +167,69 @@ def verify_inputs(name: str, B: int, T: int, H: int, *, seed: int, d: int = D,
         pool=pool, slot_ids=slot_ids, meta={"seed": seed})
 
 
+@dataclass
+class SpecStepInputs:
+    """One speculative-decoding step of a layer: a prefill segment and a verify
+    segment that share the layer's head parameters and state pool, and the
+    output row of every token of either segment."""
+
+    name: str
+    prefill: PrefillInputs
+    verify: VerifyInputs
+    non_spec_token_indx: np.ndarray   # [prefill tokens] int32
+    spec_token_indx: np.ndarray       # [B * T] int32
+    num_out_tokens: int
+    meta: dict = field(default_factory=dict)
+
+    @property
+    def H(self) -> int:
+        return self.prefill.H
+
+
+def spec_step_inputs(name: str, prefill_lens, B: int, T: int, H: int, *, seed: int, d: int = D,
+                     pool_slots: int | None = None, load_initial: bool = True, final_to_pool: bool = True,
+                     order: str = "spec_first", extra_rows: int = 0, lower_bound: float = LOWER_BOUND,
+                     g_mean: float = 0.0, state_std: float = 0.02) -> SpecStepInputs:
+    """Draw one spec step.  Draw order: prefill tokens, verify tokens, head params,
+    pool, slot ids (one permutation: the prefill sequences' slots, then the
+    requests'), output rows.
+
+    ``order``: ``"spec_first"`` puts the verify tokens in rows 0 .. B*T-1 and
+    the prefill tokens after them (decode requests ahead of prefills in the
+    batch); ``"interleaved"`` gives every token a random row.  ``extra_rows``
+    output rows belong to no token."""
+    prefill_lens = [int(x) for x in prefill_lens]
+    rng = np.random.default_rng(seed)
+    cu = np.zeros(len(prefill_lens) + 1, dtype=np.int32)
+    cu[1:] = np.cumsum(prefill_lens)
+    tp = int(cu[-1])
+    pq, pk, pv, pg, pb = _token_tensors(rng, tp, H, d, g_mean)
+    sq, sk, sv, sg, sb = _token_tensors(rng, B * T, H, d, g_mean)
+    A_log, dt_bias = _head_params(rng, H, d)
+    n_slots = pool_slots if pool_slots is not None else len(prefill_lens) + B + 2
+    pool = rng.standard_normal((n_slots, H, d, d), dtype=np.float32) * np.float32(state_std)
+    perm = rng.permutation(n_slots).astype(np.int32)
+    pslots, sslots = perm[:len(prefill_lens)], perm[len(prefill_lens):len(prefill_lens) + B]
+    n_out = tp + B * T + extra_rows
+    if order == "spec_first":
+        rows = np.arange(n_out, dtype=np.int32)
+    elif order == "interleaved":
+        rows = rng.permutation(n_out).astype(np.int32)
+    else:
+        raise ValueError(f"unknown order {order!r}")
+    scale = float(1.0 / math.sqrt(d))
+    pre = PrefillInputs(name=name + ":prefill", q=pq, k=pk, v=pv, g=pg, beta=pb, A_log=A_log, dt_bias=dt_bias,
+                        lower_bound=float(lower_bound), scale=scale, cu_seqlens=cu, pool=pool, slot_ids=pslots,
+                        load_initial=load_initial, final_to_pool=final_to_pool,
+                        meta={"seed": seed, "seq_lens": prefill_lens})
+    ver = VerifyInputs(name=name + ":verify", q=sq, k=sk, v=sv, g=sg, beta=sb, A_log=A_log, dt_bias=dt_bias,
+                       lower_bound=float(lower_bound), scale=scale, B=B, T=T, pool=pool, slot_ids=sslots,
+                       meta={"seed": seed})
+    return SpecStepInputs(name=name, prefill=pre, verify=ver, non_spec_token_indx=rows[B * T:B * T + tp].copy(),
+                          spec_token_indx=rows[:B * T].copy(), num_out_tokens=n_out,
+                          meta={"seed": seed, "order": order})
+
+
 # ---------------------------------------------------------------------------
 # The five named workloads.
 # ---------------------------------------------------------------------------
@@ -214,6 +277,13 @@ def verify_64x1() -> VerifyInputs:
     return verify_inputs("verify_64x1_h16", 64, 1, 16, seed=1006, pool_slots=256)
 
 
+def spec_step_2048x4_64x4() -> SpecStepInputs:
+    """One spec step of a layer: a prefill segment of 4 x 2048 tokens (initial
+    states from the pool, final states back to it) beside 64 verify requests x
+    4 tokens (MTP-3), H=16, 256-slot pool, verify tokens in the first rows."""
+    return spec_step_inputs("spec_step_2048x4+64x4_h16", [2048] * 4, 64, 4, 16, seed=1007, pool_slots=256)
+
+
 NAMED = {
     "prefill_1x256_h2": tiny_prefill,
     "prefill_2048x8_h16": prefill_2048x8,
@@ -222,4 +292,5 @@ NAMED = {
     "verify_64x8_h16": verify_64x8,
     "verify_64x4_h16": verify_64x4,
     "verify_64x1_h16": verify_64x1,
+    "spec_step_2048x4+64x4_h16": spec_step_2048x4_64x4,
 }

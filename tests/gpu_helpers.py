@@ -102,3 +102,41 @@ class DeviceVerify:
         inp = self.inp
         return kda.recurrent_verify(self.q, self.k, self.v, self.g, self.beta, self.A_log, self.dt_bias, self.pool,
                                     self.slots, inp.T, lower_bound=inp.lower_bound, scale=inp.scale, **kw)
+
+
+class DeviceSpecStep:
+    """Device copies of one spec step (``inputs.SpecStepInputs``): both segments read the one pool and the
+    one set of head parameters."""
+
+    SENTINEL = 5.0   # value of output rows that belong to no token
+
+    def __init__(self, inp, device="cuda"):
+        self.inp = inp
+        self.pre = DevicePrefill(inp.prefill, device)
+        self.ver = DeviceVerify(inp.verify, device)
+        self.pool = self.pre.pool
+        self.ver.pool = self.pool
+        self.ns_idx = i32_dev(inp.non_spec_token_indx, device)
+        self.s_idx = i32_dev(inp.spec_token_indx, device)
+        self.device = device
+
+    def workspace(self):
+        p = self.inp.prefill
+        return kda.make_workspace(self.device, nbytes=kda.prefill_workspace_size(p.total_tokens, p.num_seqs, p.H))
+
+    def new_out(self):
+        return torch.full((self.inp.num_out_tokens, self.inp.H, 128), self.SENTINEL, dtype=torch.bfloat16,
+                          device=self.device)
+
+    def run(self, out=None, **kw):
+        inp, pre, ver = self.inp, self.pre, self.ver
+        p, v = inp.prefill, inp.verify
+        if out is None:
+            out = self.new_out()
+        has_pre, has_spec = p.num_seqs > 0, v.B > 0
+        return kda.spec_step(
+            (pre.q, pre.k, pre.v, pre.g, pre.beta) if has_pre else None, pre.cu, pre.cu_host,
+            (ver.q, ver.k, ver.v, ver.g, ver.beta) if has_spec else None, v.T, pre.A_log, pre.dt_bias, self.pool,
+            out, self.ns_idx, self.s_idx, prefill_slot_ids=pre.slots, spec_slot_ids=ver.slots,
+            load_initial=p.load_initial, final_to_pool=p.final_to_pool, lower_bound=p.lower_bound, scale=p.scale,
+            **kw)

@@ -123,6 +123,35 @@ def test_verify_rejects_bad_arguments(lib):
     assert _verify(lib, B=0) == 0                      # no requests: nothing to do
 
 
+def _spec_step(lib, *, cu=(0, 4), B=2, T=8, H=2, pre=True, spec=True, pre_stride=256, spec_stride=256,
+               ns_idx=FAKE, s_idx=FAKE, n_out=100, ws_bytes=None, lb=-5.0):
+    from kda_linear_attention_bounded_gb300._binding import TokenTensors
+    cu_host = np.array(cu, np.int32)
+    ws_bytes = lib.kda_prefill_workspace_size(int(cu[-1]), len(cu) - 1, H) if ws_bytes is None else ws_bytes
+    tp = TokenTensors(FAKE, FAKE, FAKE, pre_stride, FAKE, pre_stride, FAKE, H)
+    ts = TokenTensors(FAKE, FAKE, FAKE, spec_stride, FAKE, spec_stride, FAKE, H)
+    return lib.kda_spec_step(ctypes.byref(tp) if pre else None, P(FAKE), cu_host.ctypes.data_as(P), len(cu) - 1,
+                             None, 0, P(FAKE), ctypes.byref(ts) if spec else None, B, T, P(FAKE), P(FAKE), P(FAKE),
+                             P(FAKE), lb, 0.1, H, P(FAKE), 4, P(FAKE), H * 128, n_out, P(ns_idx), P(s_idx), P(FAKE),
+                             ws_bytes, None)
+
+
+def test_spec_step_rejects_bad_arguments(lib):
+    # every check of both segments runs before anything is launched
+    assert _spec_step(lib, pre=False) == 1            # a prefill segment without its tensors
+    assert _spec_step(lib, spec=False) == 1           # a verify segment without its tensors
+    assert _spec_step(lib, pre_stride=100) == 1
+    assert _spec_step(lib, spec_stride=260) == 1
+    assert _spec_step(lib, T=0) == 1
+    assert _spec_step(lib, cu=(0, 5, 3)) == 1
+    assert _spec_step(lib, ns_idx=None) == 1          # prefill tokens need their output rows
+    assert _spec_step(lib, s_idx=None) == 1           # and so do the verify tokens
+    assert _spec_step(lib, n_out=-1) == 1
+    assert _spec_step(lib, lb=-11.0) == 2
+    assert _spec_step(lib, ws_bytes=256) == 3         # no room for the prefill's chunk blocks
+    assert _spec_step(lib, cu=(0,), B=0, pre=False, spec=False, ns_idx=None, s_idx=None) == 0   # empty step
+
+
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     from kda_linear_attention_bounded_gb300 import _binding as b
     monkeypatch.setattr(b, "_lib", None)
