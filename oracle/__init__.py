@@ -65,6 +65,8 @@ class Oracle:
         lib.kda_oracle_gate.restype = None
         lib.kda_oracle_l2norm.argtypes = [P, I, Dbl, P]
         lib.kda_oracle_l2norm.restype = None
+        lib.kda_oracle_gated_rmsnorm.argtypes = [P, P, P, Dbl, I, I, P, P]
+        lib.kda_oracle_gated_rmsnorm.restype = None
         self.lib = lib
 
     def run(self, q, k, v, g, beta_logits, A_log, dt_bias, lower_bound, scale, cu_seqlens, *,
@@ -152,6 +154,22 @@ class Oracle:
         self.lib.kda_oracle_l2norm(_ptr(x), x.shape[0], float(eps), _ptr(out))
         return out
 
+    def gated_rmsnorm(self, x, z, w, eps):
+        """Sigmoid-gated RMSNorm over the last axis: ``x`` rows (any float, widened to fp64), ``z`` the bf16
+        gate bits of the same shape, ``w`` the weight of the last axis.  Returns ``y`` (fp64, shape of x)
+        and ``rstd`` (fp64, x's shape without the last axis)."""
+        x = _c(x, np.float64)
+        z = _c(z, np.uint16)
+        w = _c(w, np.float64)
+        if z.shape != x.shape or w.shape != (x.shape[-1],):
+            raise ValueError("gated_rmsnorm: z must match x and w the last axis")
+        d = x.shape[-1]
+        rows = x.size // d if d else 0
+        y = np.empty_like(x)
+        rstd = np.empty(x.shape[:-1])
+        self.lib.kda_oracle_gated_rmsnorm(_ptr(x), _ptr(z), _ptr(w), float(eps), rows, d, _ptr(y), _ptr(rstd))
+        return y, rstd
+
 
 _default = None
 
@@ -186,3 +204,7 @@ def gate(*a, **kw):
 
 def l2norm(*a, **kw):
     return get().l2norm(*a, **kw)
+
+
+def gated_rmsnorm(*a, **kw):
+    return get().gated_rmsnorm(*a, **kw)

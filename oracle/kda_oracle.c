@@ -65,6 +65,32 @@ void kda_oracle_l2norm(const double *x, int d, double eps, double *out)
     for (int c = 0; c < d; ++c) out[c] = x[c] * inv;
 }
 
+/*
+ * Sigmoid-gated RMSNorm of output rows ("sigmoid RMSNorm" / "gated norm" on
+ * BF16, D = 128 rows: sglang PR #42489 "Improve GLM-5.3-Flash DFlash decoding
+ * on B300", Modifications and review thread; its kernel checks compare the
+ * output and rstd).  The pages print no formula; the reading taken: per row
+ * of d channels (one token and head), the row is normalised first and gated
+ * after,
+ *   rstd = 1 / sqrt(mean_c x_c^2 + eps)
+ *   y_c  = x_c * rstd * w_c * sigmoid(z_c)
+ * with the weight w shared by the heads and z the bf16 gate row.
+ */
+void kda_oracle_gated_rmsnorm(const double *x, const uint16_t *z, const double *w, double eps,
+                              int rows, int d, double *y, double *rstd)
+{
+    for (int r = 0; r < rows; ++r) {
+        const double *xr = x + (size_t)r * d;
+        double ms = 0.0;
+        for (int c = 0; c < d; ++c) ms += xr[c] * xr[c];
+        ms /= d;
+        double inv_rms = 1.0 / sqrt(ms + eps);
+        rstd[r] = inv_rms;
+        for (int c = 0; c < d; ++c)
+            y[(size_t)r * d + c] = xr[c] * inv_rms * w[c] * sigmoid(bf16_to_double(z[(size_t)r * d + c]));
+    }
+}
+
 /* lambda_c = lower_bound * sigmoid(exp(A_log) * (g_c + dt_bias_c)). */
 void kda_oracle_gate(const double *g, const double *dt_bias, double A_log,
                      double lower_bound, int d, double *lambda)

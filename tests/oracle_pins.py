@@ -335,6 +335,36 @@ def pin_chunked_equals_sequential(O):
             assert worst <= sub // 2 * lam_hi + 1e-9
 
 
+# --------------------------------------------------------------------------
+# sigmoid-gated RMSNorm of the output rows
+# --------------------------------------------------------------------------
+
+def pin_gated_rmsnorm(O):
+    """Closed forms of y = x rstd w sigmoid(z), rstd = (mean x^2 + eps)^(-1/2): a constant row (the mean, not the
+    sum, of squares; eps under the root; the gate after the norm, varying along the row; a sigmoid of it; the
+    weight per channel), the zero gate (sigmoid 0 = 1/2 exactly) and the scale invariance it leaves."""
+    d = 128
+    rng = np.random.default_rng(31)
+    z = f32_to_bf16_bits(rng.standard_normal(d).astype(np.float32) * 2.0)
+    zd = bf16_bits_to_f32(z).astype(np.float64)
+    w = rng.uniform(0.5, 1.5, d)
+    for c, eps in ((3.0, 1e-6), (-0.25, 1e-5), (1e-3, 1e-6)):
+        y, rstd = O.gated_rmsnorm(np.full(d, c), z, w, eps)
+        inv = 1.0 / math.sqrt(c * c + eps)
+        _close(rstd * 1e-3, inv * 1e-3, 1e-14, f"rstd of a constant row {c}")
+        _close(y, c * inv * w * expit(zd), 1e-14, f"gated norm of a constant row {c}")
+    x = rng.standard_normal((5, d)) * rng.uniform(0.1, 10.0, (5, 1))
+    zero = np.zeros((5, d), np.uint16)   # bf16 +0.0
+    y, rstd = O.gated_rmsnorm(x, zero, np.ones(d), 0.0)
+    _close((y ** 2).mean(axis=1), np.full(5, 0.25), 1e-13, "zero gate, eps 0: mean of y^2 is 1/4")
+    _close(y * 2.0 / rstd[:, None], x, 1e-12, "zero gate: y = x rstd / 2")
+    y2, _ = O.gated_rmsnorm(x * 7.5, zero, np.ones(d), 0.0)
+    _close(y2, y, 1e-13, "scale invariance with eps 0")
+    ms = (x ** 2).mean(axis=1)
+    y3, _ = O.gated_rmsnorm(x, zero, np.ones(d), 0.3)
+    _close((y3 ** 2).mean(axis=1), 0.25 * ms / (ms + 0.3), 1e-13, "eps under the root: mean y^2 = ms / (ms + eps) / 4")
+
+
 ALL_PINS = [
     pin_worked_example,
     pin_gate_special_cases,
@@ -349,4 +379,5 @@ ALL_PINS = [
     pin_qk_scale_invariance,
     pin_contraction_bound,
     pin_chunked_equals_sequential,
+    pin_gated_rmsnorm,
 ]

@@ -24,6 +24,12 @@ MUTANTS = {
     "A_log_not_exponentiated": ("double a = exp(A_log);", "double a = A_log;"),
     "norm_not_sqrt": ("double inv = 1.0 / sqrt(ss + eps);", "double inv = 1.0 / (ss + eps);"),
     "sigmoid_sign": ("return 1.0 / (1.0 + exp(-x));", "return 1.0 / (1.0 + exp(x));"),
+    "rmsnorm_sum_not_mean": ("ms /= d;", "(void)0;"),
+    "rmsnorm_eps_outside_root": ("double inv_rms = 1.0 / sqrt(ms + eps);", "double inv_rms = 1.0 / (sqrt(ms) + eps);"),
+    "rmsnorm_no_weight": ("xr[c] * inv_rms * w[c] * sigmoid(", "xr[c] * inv_rms * sigmoid("),
+    "rmsnorm_gate_sign": ("sigmoid(bf16_to_double(z[(size_t)r * d + c]))", "sigmoid(-bf16_to_double(z[(size_t)r * d + c]))"),
+    "rmsnorm_ungated": ("* w[c] * sigmoid(bf16_to_double(z[(size_t)r * d + c]));", "* w[c];"),
+    "rmsnorm_rstd_not_inverse": ("rstd[r] = inv_rms;", "rstd[r] = 1.0 / inv_rms;"),
 }
 
 
