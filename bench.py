@@ -62,6 +62,10 @@ def verify_algorithmic_bytes(inp):
     return BT * H * TOKEN_HEAD_BYTES + inp.B * H * STATE_BYTES * (1 + inp.T)
 
 
+# the gated RMSNorm of an output row and head: the bf16 gate row read and the fp32 rstd written
+NORM_BYTES_PER_ROW = 256 + 4
+
+
 def spec_step_algorithmic_bytes(inp):
     """Both segments' bytes (prefill: initial and final state per sequence and head) plus the int32 row index of
     every token."""
@@ -284,7 +288,7 @@ def run_gpu(args):
     sys.path.insert(0, os.path.join(ROOT, "tests"))
     import kda_linear_attention_bounded_gb300 as kda
     from kda_linear_attention_bounded_gb300 import inputs
-    from gpu_helpers import DevicePrefill, DeviceSpecStep, DeviceVerify
+    from gpu_helpers import DevicePrefill, DeviceSpecStep, DeviceVerify, bf16_dev, f32_dev
 
     kda.load()
     inp = inputs.prefill_2048x8()
@@ -437,6 +441,46 @@ def run_gpu(args):
 
     del inter
 
+    # ---- the same prefill and verify with the sigmoid-gated RMSNorm fused into the output epilogue ----
+    ni = inputs.norm_inputs(T, H, seed=1100)
+    pnorm = kda.OutputNorm(bf16_dev(ni.gate, device), f32_dev(ni.weight, device), ni.eps,
+                           torch.empty((T, H), dtype=torch.float32, device=device))
+    for _ in range(3):
+        dev.run(out=out, final_state=final, workspace=ws, stream=stream, norm=pnorm)
+    n_steps = max(3, min(args.steps, 200))
+    n0 = torch.cuda.Event(enable_timing=True)
+    n1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(device)
+    n0.record(stream)
+    for _ in range(n_steps):
+        dev.run(out=out, final_state=final, workspace=ws, stream=stream, norm=pnorm)
+    n1.record(stream)
+    torch.cuda.synchronize(device)
+    pn_us = n0.elapsed_time(n1) * 1e3 / n_steps
+    pn_bytes = alg + T * H * NORM_BYTES_PER_ROW
+    vni = inputs.norm_inputs(vin.B * vin.T, H, seed=1101)
+    vnorm = kda.OutputNorm(bf16_dev(vni.gate, device), f32_dev(vni.weight, device), vni.eps,
+                           torch.empty((vin.B * vin.T, H), dtype=torch.float32, device=device))
+    vn_out = torch.empty((vin.B * vin.T, H, 128), dtype=torch.bfloat16, device=device)
+    vn_inter = torch.empty((vin.B, vin.T, H, 128, 128), dtype=torch.float32, device=device)
+    vn_us, vn_calls = graph_time_us(
+        [lambda: vdev.run(out=vn_out, intermediate_states=vn_inter, workspace=ws, norm=vnorm)],
+        max(3, min(args.steps, 200)))
+    vn_bytes = verify_algorithmic_bytes(vin) + vin.B * vin.T * H * NORM_BYTES_PER_ROW
+    assert kda.read_device_status(ws) == 0
+    del vn_out, vn_inter, pnorm, vnorm
+    gated = {
+        "prefill": {"workload": inp.name, "us_per_layer": pn_us, "steps": n_steps,
+                    "extra_us_vs_plain": pn_us - avg_launch_s * 1e6,
+                    "roofline": {"bound": "hbm", "achieved": pn_bytes / (pn_us * 1e-6) / 1e9, "peak": peak,
+                                 "unit": "GB/s", "frac": pn_bytes / (pn_us * 1e-6) / 1e9 / peak,
+                                 "algorithmic_bytes": pn_bytes}},
+        "verify": {"workload": vin.name, "us_per_layer": vn_us, "calls_timed": vn_calls,
+                   "roofline": {"bound": "hbm", "achieved": vn_bytes / (vn_us * 1e-6) / 1e9, "peak": peak,
+                                "unit": "GB/s", "frac": vn_bytes / (vn_us * 1e-6) / 1e9 / peak,
+                                "algorithmic_bytes": vn_bytes}},
+    }
+
     # ---- one spec step: prefill segment + verify segment, outputs written by index into the layer output ----
     sdev = DeviceSpecStep(inputs.spec_step_2048x4_64x4(), device=device)
     sin = sdev.inp
@@ -490,6 +534,7 @@ def run_gpu(args):
                       "tokens_per_s": s_tokens / (s_us * 1e-6), "launches_per_call": 3,
                       "roofline": {"bound": "hbm", "achieved": s_achieved, "peak": peak, "unit": "GB/s",
                                    "frac": s_achieved / peak, "algorithmic_bytes": s_bytes}},
+        "gated_norm": gated,
         "commit": {"workload": vin.name + " (1..8 accepted per request)", "us_per_layer": c_us, "calls_timed": c_steps,
                    "roofline": {"bound": "hbm", "achieved": c_achieved, "peak": peak, "unit": "GB/s",
                                 "frac": c_achieved / peak, "algorithmic_bytes": c_bytes}},

@@ -97,6 +97,27 @@ typedef struct kda_token_tensors {
   int64_t beta_token_stride;
 } kda_token_tensors;
 
+/*
+ * Optional sigmoid-gated RMSNorm applied to every output row before it is
+ * stored ("sigmoid RMSNorm" / "gated norm" on BF16 D = 128 rows with output
+ * and rstd compared: sglang PR #42489 "Improve GLM-5.3-Flash DFlash decoding
+ * on B300", Modifications and review thread).  Per output row r and head h,
+ * with o the attention output of that row and head:
+ *   rstd = 1 / sqrt(mean_c o_c^2 + eps),  y_c = o_c * rstd * weight_c * sigmoid(gate_c)
+ * and y (bf16) is stored instead of o.  The pages print no formula; this
+ * normalise-then-gate form is the reading taken.  The verify kernel applies
+ * it to its fp32 output in its epilogue; the prefill's rows are normalised
+ * from their stored bf16 values by one more row-parallel kernel after the
+ * state pass (on every SM, at HBM speed), which the call launches last.
+ */
+typedef struct kda_output_norm {
+  const uint16_t *gate;          /* [rows, H, 128] bf16, row = the output row; token stride below */
+  int64_t gate_token_stride;     /* elements, a multiple of 8 and >= H*128 */
+  const float *weight;           /* [128] fp32, shared by the heads */
+  float eps;                     /* >= 0 */
+  float *rstd;                   /* [rows, H] fp32 (row-major), or NULL */
+} kda_output_norm;
+
 /* Static, human-readable text for a status code. */
 KDA_API const char *kda_status_string(int status);
 
@@ -142,6 +163,8 @@ KDA_API int kda_read_device_status(const void *workspace, size_t workspace_bytes
  *                   KDA_LOAD_INITIAL or KDA_FINAL_TO_POOL, with slot_ids
  *                   [num_seqs] int32 (distinct when KDA_FINAL_TO_POOL).
  *  out              [T_total, H, 128] bf16, token stride out_token_stride
+ *  norm             NULL, or the gated RMSNorm applied to each output row
+ *                   (gate and rstd rows are token rows)
  *  final_state      [num_seqs, H, 128, 128] fp32 dense final states; required
  *                   unless KDA_FINAL_TO_POOL (then ignored, may be NULL).
  *  Inputs and outputs must not overlap, except state_pool which may be both
@@ -158,8 +181,8 @@ KDA_API int kda_chunk_prefill(const uint16_t *q, const uint16_t *k, const uint16
                       const int32_t *cu_seqlens_dev, const int32_t *cu_seqlens_host,
                       int num_seqs, int H, float *state_pool, int num_slots,
                       const int32_t *slot_ids, int flags, uint16_t *out,
-                      int64_t out_token_stride, float *final_state, void *workspace,
-                      size_t workspace_bytes, void *stream);
+                      int64_t out_token_stride, const kda_output_norm *norm, float *final_state,
+                      void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * Speculative-decode verify over a pooled fp32 state.  Source: TensorRT-LLM
@@ -174,6 +197,8 @@ KDA_API int kda_chunk_prefill(const uint16_t *q, const uint16_t *k, const uint16
  *                   or KDA_PAD_SLOT_ID for a padding row (its out rows and
  *                   intermediate_states rows are left as they were)
  *  out              [B*T, H, 128] bf16
+ *  norm             NULL, or the gated RMSNorm applied to each output row
+ *                   (gate and rstd rows are token rows b*T + t)
  *  intermediate_states [B, T, H, 128, 128] fp32: row (b, t) = state after draft token t
  *  1 <= T <= 64.
  *
@@ -187,8 +212,9 @@ KDA_API int kda_recurrent_verify(const uint16_t *q, const uint16_t *k, const uin
                          const float *A_log, const float *dt_bias, float lower_bound,
                          float scale, int B, int T, int H, const float *state_pool,
                          int num_slots, const int32_t *slot_ids, uint16_t *out,
-                         int64_t out_token_stride, float *intermediate_states,
-                         void *workspace, size_t workspace_bytes, void *stream);
+                         int64_t out_token_stride, const kda_output_norm *norm,
+                         float *intermediate_states, void *workspace, size_t workspace_bytes,
+                         void *stream);
 
 /*
  * Accept/commit after kda_recurrent_verify.  Source: vLLM PR #55737 "Use
@@ -238,6 +264,8 @@ KDA_API int kda_commit_accepted(float *state_pool, int num_slots, const int32_t 
  *  core_attn_out    [num_out_tokens, H, 128] bf16, token stride out_token_stride
  *  non_spec_token_indx [T_p] int32 device: output row of prefill token i
  *  spec_token_indx  [B*T] int32 device: output row of verify token j (= b*T + t)
+ *  norm             NULL, or the gated RMSNorm applied to each output row
+ *                   (gate and rstd rows are output rows of core_attn_out)
  *
  * Preconditions: the output rows named by the two index arrays are distinct
  * (rows named by neither are left as they were).  An index outside
@@ -258,7 +286,8 @@ KDA_API int kda_spec_step(const kda_token_tensors *prefill, const int32_t *cu_se
                           const int32_t *spec_slot_ids, float *intermediate_states, const float *A_log,
                           const float *dt_bias, float lower_bound, float scale, int H, float *state_pool,
                           int num_slots, uint16_t *core_attn_out, int64_t out_token_stride,
-                          int64_t num_out_tokens, const int32_t *non_spec_token_indx,
+                          int64_t num_out_tokens, const kda_output_norm *norm,
+                          const int32_t *non_spec_token_indx,
                           const int32_t *spec_token_indx, void *workspace, size_t workspace_bytes,
                           void *stream);
 

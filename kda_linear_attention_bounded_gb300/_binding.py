@@ -43,6 +43,38 @@ class TokenTensors(ctypes.Structure):
                 ("beta_logits", ctypes.c_void_p), ("beta_token_stride", ctypes.c_int64)]
 
 
+class _OutputNormC(ctypes.Structure):
+    """``kda_output_norm``."""
+    _fields_ = [("gate", ctypes.c_void_p), ("gate_token_stride", ctypes.c_int64), ("weight", ctypes.c_void_p),
+                ("eps", ctypes.c_float), ("rstd", ctypes.c_void_p)]
+
+
+class OutputNorm:
+    """Sigmoid-gated RMSNorm of the output rows (``kda_output_norm``):
+    ``y = o * rstd * weight * sigmoid(gate)``, ``rstd = (mean o^2 + eps)^-1/2`` per (row, head).
+
+    gate: CUDA bf16 ``[rows, H, 128]`` (rows as the call's output rows); weight: CUDA fp32 ``[128]``;
+    rstd: optional CUDA fp32 ``[rows, H]`` written by the call."""
+
+    def __init__(self, gate, weight, eps=1e-6, rstd=None):
+        self.gate, self.weight, self.eps, self.rstd = gate, weight, float(eps), rstd
+
+    def as_c(self, H):
+        gs = _token_tensor(self.gate, "norm gate", H)
+        w = self.weight
+        if w.dtype != torch.float32 or not w.is_cuda or w.numel() != 128 or not w.is_contiguous():
+            raise ValueError("norm weight: expected a contiguous CUDA fp32 tensor of 128 entries")
+        r = self.rstd
+        if r is not None and (r.dtype != torch.float32 or not r.is_cuda or r.dim() != 2 or r.shape[1] != H
+                              or not r.is_contiguous()):
+            raise ValueError("norm rstd: expected a contiguous CUDA fp32 tensor [rows, H]")
+        return _OutputNormC(self.gate.data_ptr(), gs, w.data_ptr(), self.eps, None if r is None else r.data_ptr())
+
+
+def _norm_arg(norm, H):
+    return None if norm is None else ctypes.byref(norm.as_c(H))
+
+
 class KdaError(RuntimeError):
     def __init__(self, status: int, what: str):
         super().__init__(f"{what}: {status_string(status)} (status {status})")
@@ -74,17 +106,18 @@ def load():
     lib.kda_workspace_reset.restype = I
     lib.kda_read_device_status.argtypes = [P, SZ, ctypes.POINTER(ctypes.c_uint32), P]
     lib.kda_read_device_status.restype = I
+    NP = ctypes.POINTER(_OutputNormC)
     lib.kda_chunk_prefill.argtypes = [P, P, P, I64, P, I64, P, I64, P, P, F, F, P, P, I, I, P, I, P, I, P,
-                                      I64, P, P, SZ, P]
+                                      I64, NP, P, P, SZ, P]
     lib.kda_chunk_prefill.restype = I
     lib.kda_recurrent_verify.argtypes = [P, P, P, I64, P, I64, P, I64, P, P, F, F, I, I, I, P, I, P, P, I64,
-                                         P, P, SZ, P]
+                                         NP, P, P, SZ, P]
     lib.kda_recurrent_verify.restype = I
     lib.kda_commit_accepted.argtypes = [P, I, P, P, P, I, I, I, P, SZ, P]
     lib.kda_commit_accepted.restype = I
     TT = ctypes.POINTER(TokenTensors)
-    lib.kda_spec_step.argtypes = [TT, P, P, I, P, I, P, TT, I, I, P, P, P, P, F, F, I, P, I, P, I64, I64, P, P, P,
-                                  SZ, P]
+    lib.kda_spec_step.argtypes = [TT, P, P, I, P, I, P, TT, I, I, P, P, P, P, F, F, I, P, I, P, I64, I64, NP, P, P,
+                                  P, SZ, P]
     lib.kda_spec_step.restype = I
     _lib = lib
     return lib
@@ -150,9 +183,9 @@ def _beta_stride(b, H):
 
 def chunk_prefill(q, k, v, g, beta_logits, A_log, dt_bias, cu_seqlens, cu_seqlens_host, *,
                   lower_bound=-5.0, scale=None, state_pool=None, slot_ids=None, load_initial=False,
-                  final_to_pool=False, out=None, final_state=None, workspace=None, stream=None):
+                  final_to_pool=False, out=None, final_state=None, norm=None, workspace=None, stream=None):
     """``kda_chunk_prefill``.  Returns ``(out, final_state)`` (final_state is None
-    when the final states go to the pool)."""
+    when the final states go to the pool).  ``norm``: an :class:`OutputNorm` applied to the output rows."""
     lib = load()
     H = q.shape[1]
     qs = _token_tensor(q, "q", H)
@@ -180,17 +213,18 @@ def chunk_prefill(q, k, v, g, beta_logits, A_log, dt_bias, cu_seqlens, cu_seqlen
         _ptr(q), _ptr(k), _ptr(v), qs, _ptr(g), gs, _ptr(beta_logits), bs, _ptr(A_log), _ptr(dt_bias),
         float(lower_bound), float(scale), _ptr(cu_seqlens), ctypes.c_void_p(cu_host.data_ptr()), N, H,
         _ptr(state_pool), 0 if state_pool is None else state_pool.shape[0], _ptr(slot_ids), flags,
-        _ptr(out), os_, _ptr(None if final_to_pool else final_state), _ptr(workspace), workspace.numel(),
-        _stream_ptr(stream, dev))
+        _ptr(out), os_, _norm_arg(norm, H), _ptr(None if final_to_pool else final_state), _ptr(workspace),
+        workspace.numel(), _stream_ptr(stream, dev))
     if rc != KDA_OK:
         raise KdaError(rc, "kda_chunk_prefill")
     return out, (None if final_to_pool else final_state)
 
 
 def recurrent_verify(q, k, v, g, beta_logits, A_log, dt_bias, state_pool, slot_ids, T, *,
-                     lower_bound=-5.0, scale=None, out=None, intermediate_states=None, workspace=None,
+                     lower_bound=-5.0, scale=None, out=None, intermediate_states=None, norm=None, workspace=None,
                      stream=None):
-    """``kda_recurrent_verify``.  Returns ``(out, intermediate_states)``."""
+    """``kda_recurrent_verify``.  Returns ``(out, intermediate_states)``.  ``norm``: an :class:`OutputNorm`
+    applied to the output rows."""
     lib = load()
     H = q.shape[1]
     qs = _token_tensor(q, "q", H)
@@ -212,7 +246,8 @@ def recurrent_verify(q, k, v, g, beta_logits, A_log, dt_bias, state_pool, slot_i
     rc = lib.kda_recurrent_verify(
         _ptr(q), _ptr(k), _ptr(v), qs, _ptr(g), gs, _ptr(beta_logits), bs, _ptr(A_log), _ptr(dt_bias),
         float(lower_bound), float(scale), B, int(T), H, _ptr(state_pool), state_pool.shape[0], _ptr(slot_ids),
-        _ptr(out), os_, _ptr(intermediate_states), _ptr(workspace), workspace.numel(), _stream_ptr(stream, dev))
+        _ptr(out), os_, _norm_arg(norm, H), _ptr(intermediate_states), _ptr(workspace), workspace.numel(),
+        _stream_ptr(stream, dev))
     if rc != KDA_OK:
         raise KdaError(rc, "kda_recurrent_verify")
     return out, intermediate_states
@@ -252,11 +287,12 @@ def _token_struct(tensors, H):
 def spec_step(prefill, cu_seqlens, cu_seqlens_host, spec, T, A_log, dt_bias, state_pool, core_attn_out,
               non_spec_token_indx, spec_token_indx, *, prefill_slot_ids=None, spec_slot_ids=None,
               load_initial=False, final_to_pool=False, final_state=None, intermediate_states=None,
-              lower_bound=-5.0, scale=None, workspace=None, stream=None):
+              lower_bound=-5.0, scale=None, norm=None, workspace=None, stream=None):
     """``kda_spec_step``: the prefill segment and the verify segment of one speculative-decoding step, their
     outputs written into ``core_attn_out`` rows ``non_spec_token_indx`` / ``spec_token_indx``.
 
-    ``prefill`` and ``spec`` are ``(q, k, v, g, beta_logits)`` tuples (or None for an absent segment).
+    ``prefill`` and ``spec`` are ``(q, k, v, g, beta_logits)`` tuples (or None for an absent segment);
+    ``norm``: an :class:`OutputNorm` over the rows of ``core_attn_out``.
     Returns ``(core_attn_out, final_state, intermediate_states)``."""
     lib = load()
     H = core_attn_out.shape[1]
@@ -294,7 +330,8 @@ def spec_step(prefill, cu_seqlens, cu_seqlens_host, spec, T, A_log, dt_bias, sta
         _ptr(None if final_to_pool else final_state), None if spc is None else ctypes.byref(spc), B, int(T),
         _ptr(spec_slot_ids), _ptr(intermediate_states), _ptr(A_log), _ptr(dt_bias), float(lower_bound),
         float(scale), H, _ptr(state_pool), 0 if state_pool is None else state_pool.shape[0], _ptr(core_attn_out),
-        os_, core_attn_out.shape[0], _ptr(non_spec_token_indx), _ptr(spec_token_indx), _ptr(workspace),
+        os_, core_attn_out.shape[0], _norm_arg(norm, H), _ptr(non_spec_token_indx), _ptr(spec_token_indx),
+        _ptr(workspace),
         workspace.numel(), _stream_ptr(stream, dev))
     if rc != KDA_OK:
         raise KdaError(rc, "kda_spec_step")

@@ -49,14 +49,31 @@ int check_token_tensors(const uint16_t *q, const uint16_t *k, const uint16_t *v,
   return KDA_OK;
 }
 
+// Host-side checks of the optional output norm; fills `n` (gate == nullptr when absent).
+int check_norm(const kda_output_norm *norm, int H, kda::OutNorm *n) {
+  *n = kda::OutNorm{};
+  if (!norm) return KDA_OK;
+  if (!norm->gate || !aligned16(norm->gate) || !good_stride(norm->gate_token_stride, (int64_t)H * kda::kD))
+    return KDA_ERR_INVALID_ARG;
+  if (!norm->weight || !aligned16(norm->weight)) return KDA_ERR_INVALID_ARG;
+  if (!std::isfinite(norm->eps) || norm->eps < 0.0f) return KDA_ERR_INVALID_ARG;
+  if (norm->rstd && (reinterpret_cast<uintptr_t>(norm->rstd) & 3u) != 0) return KDA_ERR_INVALID_ARG;
+  n->gate = norm->gate;
+  n->gate_stride = norm->gate_token_stride;
+  n->weight = norm->weight;
+  n->eps = norm->eps;
+  n->rstd = norm->rstd;
+  return KDA_OK;
+}
+
 // Host-side checks of one prefill call; on success fills `a` (no launch).
 int prepare_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v, int64_t qkv_token_stride,
                     const uint16_t *g, int64_t g_token_stride, const uint16_t *beta_logits,
                     int64_t beta_token_stride, const float *A_log, const float *dt_bias, float lower_bound,
                     float scale, const int32_t *cu_seqlens_dev, const int32_t *cu_seqlens_host, int num_seqs,
                     int H, float *state_pool, int num_slots, const int32_t *slot_ids, int flags, uint16_t *out,
-                    int64_t out_token_stride, float *final_state, void *workspace, size_t workspace_bytes,
-                    kda::ChunkArgs *a) {
+                    int64_t out_token_stride, const kda_output_norm *norm, float *final_state, void *workspace,
+                    size_t workspace_bytes, kda::ChunkArgs *a) {
   if (int rc = check_workspace(workspace, workspace_bytes)) return rc;
   if (num_seqs < 0) return KDA_ERR_INVALID_ARG;
   if (!cu_seqlens_dev || !cu_seqlens_host) return KDA_ERR_INVALID_ARG;
@@ -75,6 +92,7 @@ int prepare_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v, int
     return KDA_ERR_INVALID_ARG;
   if (!(flags & KDA_FINAL_TO_POOL) && (!final_state || !aligned16(final_state))) return KDA_ERR_INVALID_ARG;
   if (workspace_bytes < kda::prefill_workspace_bytes(cu_seqlens_host[num_seqs], num_seqs, H)) return KDA_ERR_WORKSPACE;
+  if (int rc = check_norm(norm, H, &a->norm)) return rc;
 
   a->q = q; a->k = k; a->v = v; a->g = g; a->beta = beta_logits;
   a->qkv_stride = qkv_token_stride; a->g_stride = g_token_stride;
@@ -98,8 +116,8 @@ int prepare_verify(const uint16_t *q, const uint16_t *k, const uint16_t *v, int6
                    const uint16_t *g, int64_t g_token_stride, const uint16_t *beta_logits, int64_t beta_token_stride,
                    const float *A_log, const float *dt_bias, float lower_bound, float scale, int B, int T, int H,
                    const float *state_pool, int num_slots, const int32_t *slot_ids, uint16_t *out,
-                   int64_t out_token_stride, float *intermediate_states, void *workspace, size_t workspace_bytes,
-                   kda::RecurrentArgs *a) {
+                   int64_t out_token_stride, const kda_output_norm *norm, float *intermediate_states,
+                   void *workspace, size_t workspace_bytes, kda::RecurrentArgs *a) {
   if (int rc = check_workspace(workspace, workspace_bytes)) return rc;
   if (B < 0 || T < 1 || T > 64) return KDA_ERR_INVALID_ARG;
   *a = kda::RecurrentArgs{};
@@ -110,6 +128,7 @@ int prepare_verify(const uint16_t *q, const uint16_t *k, const uint16_t *v, int6
   if (int rc = check_gate(lower_bound, scale)) return rc;
   if (!state_pool || !aligned16(state_pool) || num_slots <= 0 || !slot_ids) return KDA_ERR_INVALID_ARG;
   if (!intermediate_states || !aligned16(intermediate_states)) return KDA_ERR_INVALID_ARG;
+  if (int rc = check_norm(norm, H, &a->norm)) return rc;
 
   a->q = q; a->k = k; a->v = v; a->g = g; a->beta = beta_logits;
   a->qkv_stride = qkv_token_stride; a->g_stride = g_token_stride;
@@ -126,6 +145,20 @@ int prepare_verify(const uint16_t *q, const uint16_t *k, const uint16_t *v, int6
   a->out = out;
   a->status = static_cast<uint32_t *>(workspace);
   return KDA_OK;
+}
+
+// The gated RMSNorm pass over a prefill's stored rows (nothing when the call has no norm).
+cudaError_t launch_prefill_norm(const kda::ChunkArgs &a, cudaStream_t stream) {
+  if (!a.norm.gate || a.num_seqs <= 0) return cudaSuccess;
+  kda::GatedNormArgs n{};
+  n.out = a.out;
+  n.out_stride = a.out_stride;
+  n.row_index = a.out_index;
+  n.num_rows = a.out_index ? a.num_out_rows : a.total_tokens;
+  n.num_tokens = a.total_tokens;
+  n.H = a.H;
+  n.norm = a.norm;
+  return kda::launch_gated_norm(n, stream);
 }
 
 }  // namespace
@@ -173,17 +206,18 @@ int kda_chunk_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v, i
                       float lower_bound, float scale, const int32_t *cu_seqlens_dev,
                       const int32_t *cu_seqlens_host, int num_seqs, int H, float *state_pool,
                       int num_slots, const int32_t *slot_ids, int flags, uint16_t *out,
-                      int64_t out_token_stride, float *final_state, void *workspace,
-                      size_t workspace_bytes, void *stream) {
+                      int64_t out_token_stride, const kda_output_norm *norm, float *final_state,
+                      void *workspace, size_t workspace_bytes, void *stream) {
   kda::ChunkArgs a;
   if (int rc = prepare_prefill(q, k, v, qkv_token_stride, g, g_token_stride, beta_logits, beta_token_stride, A_log,
                                dt_bias, lower_bound, scale, cu_seqlens_dev, cu_seqlens_host, num_seqs, H, state_pool,
-                               num_slots, slot_ids, flags, out, out_token_stride, final_state, workspace,
+                               num_slots, slot_ids, flags, out, out_token_stride, norm, final_state, workspace,
                                workspace_bytes, &a))
     return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t err = kda::launch_chunk_prefill(a, cu_seqlens_host,
-                                              static_cast<uint8_t *>(workspace) + kda::kWorkspaceHeader,
-                                              static_cast<cudaStream_t>(stream));
+                                              static_cast<uint8_t *>(workspace) + kda::kWorkspaceHeader, st);
+  if (err == cudaSuccess) err = launch_prefill_norm(a, st);
   return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
@@ -192,12 +226,12 @@ int kda_recurrent_verify(const uint16_t *q, const uint16_t *k, const uint16_t *v
                          int64_t beta_token_stride, const float *A_log, const float *dt_bias,
                          float lower_bound, float scale, int B, int T, int H, const float *state_pool,
                          int num_slots, const int32_t *slot_ids, uint16_t *out, int64_t out_token_stride,
-                         float *intermediate_states, void *workspace, size_t workspace_bytes,
-                         void *stream) {
+                         const kda_output_norm *norm, float *intermediate_states, void *workspace,
+                         size_t workspace_bytes, void *stream) {
   kda::RecurrentArgs a;
   if (int rc = prepare_verify(q, k, v, qkv_token_stride, g, g_token_stride, beta_logits, beta_token_stride, A_log,
                               dt_bias, lower_bound, scale, B, T, H, state_pool, num_slots, slot_ids, out,
-                              out_token_stride, intermediate_states, workspace, workspace_bytes, &a))
+                              out_token_stride, norm, intermediate_states, workspace, workspace_bytes, &a))
     return rc;
   cudaError_t err = kda::launch_recurrent(a, B, static_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
@@ -208,8 +242,9 @@ int kda_spec_step(const kda_token_tensors *prefill, const int32_t *cu_seqlens_de
                   const kda_token_tensors *spec, int B, int T, const int32_t *spec_slot_ids,
                   float *intermediate_states, const float *A_log, const float *dt_bias, float lower_bound,
                   float scale, int H, float *state_pool, int num_slots, uint16_t *core_attn_out,
-                  int64_t out_token_stride, int64_t num_out_tokens, const int32_t *non_spec_token_indx,
-                  const int32_t *spec_token_indx, void *workspace, size_t workspace_bytes, void *stream) {
+                  int64_t out_token_stride, int64_t num_out_tokens, const kda_output_norm *norm,
+                  const int32_t *non_spec_token_indx, const int32_t *spec_token_indx, void *workspace,
+                  size_t workspace_bytes, void *stream) {
   if (num_seqs < 0 || B < 0 || num_out_tokens < 0 || (num_seqs > 0 && !prefill) || (B > 0 && !spec))
     return KDA_ERR_INVALID_ARG;
   if (int rc = check_workspace(workspace, workspace_bytes)) return rc;
@@ -220,14 +255,14 @@ int kda_spec_step(const kda_token_tensors *prefill, const int32_t *cu_seqlens_de
     if (int rc = prepare_prefill(p.q, p.k, p.v, p.qkv_token_stride, p.g, p.g_token_stride, p.beta_logits,
                                  p.beta_token_stride, A_log, dt_bias, lower_bound, scale, cu_seqlens_dev,
                                  cu_seqlens_host, num_seqs, H, state_pool, num_slots, prefill_slot_ids, flags,
-                                 core_attn_out, out_token_stride, final_state, workspace, workspace_bytes, &pa))
+                                 core_attn_out, out_token_stride, norm, final_state, workspace, workspace_bytes, &pa))
       return rc;
   }
   if (B > 0) {
     const kda_token_tensors &s = *spec;
     if (int rc = prepare_verify(s.q, s.k, s.v, s.qkv_token_stride, s.g, s.g_token_stride, s.beta_logits,
                                 s.beta_token_stride, A_log, dt_bias, lower_bound, scale, B, T, H, state_pool,
-                                num_slots, spec_slot_ids, core_attn_out, out_token_stride, intermediate_states,
+                                num_slots, spec_slot_ids, core_attn_out, out_token_stride, norm, intermediate_states,
                                 workspace, workspace_bytes, &va))
       return rc;
   }
@@ -248,6 +283,7 @@ int kda_spec_step(const kda_token_tensors *prefill, const int32_t *cu_seqlens_de
     va.done_counter = reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(workspace) + kda::kDoneCounterOffset);
   }
   if (has_spec && kda::launch_recurrent(va, B, st) != cudaSuccess) return KDA_ERR_CUDA;
+  if (launch_prefill_norm(pa, st) != cudaSuccess) return KDA_ERR_CUDA;   // the prefill rows' norm, last
   return KDA_OK;
 }
 

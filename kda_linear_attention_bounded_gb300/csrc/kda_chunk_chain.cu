@@ -165,9 +165,10 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_chain_kernel(const __grid_c
 
   // output of a chunk (accumulated in pair ob) -> `stage` as the 64-token x 128-channel row-swizzled
   // tile the output tensor map stores (workers)
-  // Scattered output (out_index set): item k of a thread is i = tid + k kThreads of the chunk's rows x 16
-  // sixteen-byte pieces.  The output rows of a chunk are fetched one chunk ahead into registers, so the
-  // store under the next chunk's first product waits on no global load.
+  // Scattered output (out_index set): item k of a thread is piece i = tid + k kThreads of the chunk's rows x 16
+  // sixteen-byte pieces.  The output rows of a chunk are fetched one chunk ahead into registers, so the store
+  // under the next chunk's first product waits on no global load.
+  const bool row_pass = prm.out_index != nullptr;
   constexpr int kRowItems = (kC * 16 + kThreads - 1) / kThreads;
   int32_t orow[kRowItems];
   auto load_rows = [&](int tok, int rows) {
@@ -178,7 +179,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_chain_kernel(const __grid_c
     }
   };
   // staged rows 0 .. rows-1 -> the rows in orow (an index outside [0, num_out_rows) skips its piece)
-  auto store_rows_indexed = [&](const uint8_t *stage, int rows) {
+  auto store_rows = [&](const uint8_t *stage, int rows) {
 #pragma unroll
     for (int k = 0; k < kRowItems; ++k) {
       const int i = tid + k * kThreads;
@@ -193,7 +194,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_chain_kernel(const __grid_c
           *reinterpret_cast<const uint4 *>(stage + swz_offset(64, r, 8 * cc));
     }
   };
-  if (prm.out_index && nchunks > 0) load_rows(t0, min(kC, len));
+  if (row_pass && nchunks > 0) load_rows(t0, min(kC, len));
 
   auto out_to_stage = [&](int ob, uint8_t *stage) {
     uint32_t ov[32];
@@ -231,8 +232,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_chain_kernel(const __grid_c
       if (worker) out_to_stage((c - 1) & 1, prev);
       fence_async_smem();
       __syncthreads();
-      if (prm.out_index) {    // rows scattered to the layer's output rows; then fetch chunk c's rows
-        store_rows_indexed(prev, kC);
+      if (row_pass) {    // rows scattered to the layer's output rows; then fetch chunk c's rows
+        store_rows(prev, kC);
         load_rows(t0 + c * kC, min(kC, len - c * kC));
       } else if (tid == kIssuer) {   // chunk c - 1 is not the last one: all 64 rows are valid
         const int tok = t0 + (c - 1) * kC;
@@ -340,8 +341,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_chain_kernel(const __grid_c
   if (worker) out_to_stage((nchunks - 1) & 1, last);
   fence_async_smem();
   __syncthreads();
-  if (prm.out_index) {
-    store_rows_indexed(last, last_valid);
+  if (row_pass) {
+    store_rows(last, last_valid);
   } else if (last_valid == kC) {
     if (tid == kIssuer) {
       const int tok = t0 + (nchunks - 1) * kC;

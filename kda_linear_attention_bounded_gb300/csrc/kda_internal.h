@@ -9,6 +9,15 @@
 
 namespace kda {
 
+// Sigmoid-gated RMSNorm of the output rows (gate == nullptr: none).
+struct OutNorm {
+  const uint16_t *gate;   // [rows, H, 128] bf16, indexed by the output row
+  int64_t gate_stride;
+  const float *weight;    // [128]
+  float eps;
+  float *rstd;            // [rows, H], or null
+};
+
 // Arguments of the token-by-token kernel (verify).
 struct RecurrentArgs {
   const uint16_t *q, *k, *v, *g, *beta;
@@ -29,6 +38,7 @@ struct RecurrentArgs {
   uint16_t *out;
   const int32_t *out_index;  // output row of each token, or null (row = token)
   int64_t num_out_rows;      // rows of out (bounds out_index)
+  OutNorm norm;
   uint32_t *status;
   // non-null: the grid is launched as a programmatic dependent of the preceding grid; a zeroed counter in the
   // workspace (kDoneCounterOffset) through which the CTA that finishes last waits for that grid
@@ -57,6 +67,7 @@ struct ChunkArgs {
   uint16_t *out;
   const int32_t *out_index;  // output row of each token, or null (row = token)
   int64_t num_out_rows;      // rows of out (bounds out_index)
+  OutNorm norm;
   uint32_t *status;
 };
 
@@ -107,14 +118,27 @@ struct ChainParams {
   float *state_out_dense;       // indexed by seq0 + local sequence
   uint16_t *out;
   int64_t out_stride;
-  const int32_t *out_index;     // output row of each token (global token index), or null: TMA tensor stores
+  const int32_t *out_index;     // output row of each token (global token index), or null (row = token)
   int64_t num_out_rows;
+                                // (with out_index the rows are stored one by one, else by TMA)
   uint32_t *status;
   int H, num_seqs, seq0;
   int32_t chunk_off[kMaxSeqsPerLaunch + 1];
   int32_t tok_off[kMaxSeqsPerLaunch + 1];
   uint16_t order[kMaxSeqsPerLaunch];          // local sequences, longest first
 };
+
+// Gated RMSNorm of stored output rows, in place (the prefill's rows, after its state pass).
+struct GatedNormArgs {
+  uint16_t *out;
+  int64_t out_stride;
+  const int32_t *row_index;   // output row of token t, or null (row = t)
+  int64_t num_rows;           // rows of out (bounds row_index)
+  int num_tokens, H;
+  OutNorm norm;
+};
+
+cudaError_t launch_gated_norm(const GatedNormArgs &args, cudaStream_t stream);
 
 cudaError_t launch_chunk_intra(const IntraParams &p, int num_chunks, cudaStream_t stream);
 cudaError_t launch_chunk_chain(const ChainParams &p, cudaStream_t stream);

@@ -39,6 +39,8 @@ __device__ __forceinline__ void recurrent_item(const RecurrentArgs &p) {
   __shared__ __align__(16) float s_v[kTile][kD];
   __shared__ float s_beta[kTile], s_kq[kTile];
   __shared__ int64_t s_row[kTile];   // output row of each token of the tile
+  __shared__ __align__(16) float s_gz[kTile][kD];   // sigmoid of the output norm's gate (with a norm)
+  __shared__ float s_sq[4];                           // per-warp sums of o^2 (with a norm)
   __shared__ __align__(16) float s_redk[kWarps][kD];
   __shared__ __align__(16) float s_redq[kWarps][kD];
   __shared__ __align__(16) float s_u[kD];
@@ -85,6 +87,19 @@ __device__ __forceinline__ void recurrent_item(const RecurrentArgs &p) {
     // ---- prologue: warp w prepares token tile + w ----
     if (warp < nt) {
       const int t = tile + warp;
+      // the output row of this token in the layer's output (-1: none; every lane loads the same index)
+      int64_t row = t;
+      if (p.out_index) {
+        row = p.out_index[t];
+        if (row < 0 || row >= p.num_out_rows) row = -1;
+      }
+      if (p.norm.gate) {
+        uint2 zr = make_uint2(0u, 0u);
+        if (row >= 0) zr = *reinterpret_cast<const uint2 *>(p.norm.gate + row * p.norm.gate_stride + h * kD + col0);
+        const float2 z01 = unpack_bf16x2(zr.x), z23 = unpack_bf16x2(zr.y);
+        *reinterpret_cast<float4 *>(&s_gz[warp][col0]) =
+            make_float4(sigmoid_f(z01.x), sigmoid_f(z01.y), sigmoid_f(z23.x), sigmoid_f(z23.y));
+      }
       const uint2 qr = *reinterpret_cast<const uint2 *>(p.q + (size_t)t * p.qkv_stride + h * kD + col0);
       const uint2 kr = *reinterpret_cast<const uint2 *>(p.k + (size_t)t * p.qkv_stride + h * kD + col0);
       const uint2 vr = *reinterpret_cast<const uint2 *>(p.v + (size_t)t * p.qkv_stride + h * kD + col0);
@@ -121,14 +136,7 @@ __device__ __forceinline__ void recurrent_item(const RecurrentArgs &p) {
       if (lane == 0) {
         s_kq[warp] = kq;
         s_beta[warp] = sigmoid_f(bf16_bits_to_f32(p.beta[(size_t)t * p.beta_stride + h]));
-        int64_t row = t;
-        if (p.out_index) {   // the output row of this token in the layer's output (-1: none)
-          row = p.out_index[t];
-          if (row < 0 || row >= p.num_out_rows) {
-            atomicOr(p.status, KDA_DEVICE_BAD_INDEX);
-            row = -1;
-          }
-        }
+        if (row < 0) atomicOr(p.status, KDA_DEVICE_BAD_INDEX);
         s_row[warp] = row;
       }
     }
@@ -159,8 +167,16 @@ __device__ __forceinline__ void recurrent_item(const RecurrentArgs &p) {
         }
         const float u = s_beta[s] * (s_v[s][tid] - wk);
         s_u[tid] = u;
-        const float o = p.scale * (wq + s_kq[s] * u);
+        float o = p.scale * (wq + s_kq[s] * u);
         const int64_t row = s_row[s];
+        if (p.norm.gate) {   // gated RMSNorm over the 128 channels (warps 0..3)
+          const float sq = warp_sum(o * o);
+          if (lane == 0) s_sq[warp] = sq;
+          named_bar_sync<1>(kD);
+          const float rstd = rsqrtf((s_sq[0] + s_sq[1] + s_sq[2] + s_sq[3]) * (1.0f / kD) + p.norm.eps);
+          o = o * rstd * p.norm.weight[tid] * s_gz[s][tid];
+          if (tid == 0 && row >= 0 && p.norm.rstd) p.norm.rstd[row * p.H + h] = rstd;
+        }
         if (row >= 0) p.out[row * p.out_stride + h * kD + tid] = f32_to_bf16_bits(o);
       }
       __syncthreads();

@@ -230,6 +230,24 @@ def spec_step_inputs(name: str, prefill_lens, B: int, T: int, H: int, *, seed: i
                           meta={"seed": seed, "order": order})
 
 
+@dataclass
+class NormInputs:
+    """Inputs of the sigmoid-gated RMSNorm of the output rows: the bf16 gate
+    ``[rows, H, D]`` (bit patterns), the fp32 weight ``[D]`` and eps."""
+
+    gate: np.ndarray
+    weight: np.ndarray
+    eps: float
+
+
+def norm_inputs(rows: int, H: int, *, seed: int, d: int = D, eps: float = 1e-6) -> NormInputs:
+    """gate ~ N(0, 1) per element (bf16), weight ~ U[0.5, 1.5] per channel."""
+    rng = np.random.default_rng(seed)
+    gate = f32_to_bf16_bits(rng.standard_normal((rows, H, d), dtype=np.float32))
+    weight = rng.uniform(0.5, 1.5, d).astype(np.float32)
+    return NormInputs(gate=gate, weight=weight, eps=float(eps))
+
+
 # ---------------------------------------------------------------------------
 # The five named workloads.
 # ---------------------------------------------------------------------------

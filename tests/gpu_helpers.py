@@ -140,3 +140,47 @@ class DeviceSpecStep:
             out, self.ns_idx, self.s_idx, prefill_slot_ids=pre.slots, spec_slot_ids=ver.slots,
             load_initial=p.load_initial, final_to_pool=p.final_to_pool, lower_bound=p.lower_bound, scale=p.scale,
             **kw)
+
+
+def device_norm(ni, H, rows=None, device="cuda", with_rstd=True):
+    """An OutputNorm on the device from ``inputs.NormInputs`` (rstd buffer NaN-filled)."""
+    gate = bf16_dev(ni.gate, device)
+    rows = gate.shape[0] if rows is None else rows
+    rstd = torch.full((rows, H), float("nan"), dtype=torch.float32, device=device) if with_rstd else None
+    return kda.OutputNorm(gate, f32_dev(ni.weight, device), ni.eps, rstd)
+
+
+# Normalised outputs y = o rstd w sigmoid(z) are scale-free per row: a row whose attention output is far below
+# the typical output scale (strong decay, k^.q^ near 0) keeps the relative error the bf16 products of the chunked
+# path leave on it (up to ~1 % measured), and the normalisation turns that into an absolute error of y.  So the
+# element-wise bar applies to the norm STAGE -- the GPU's y against the oracle's norm of the GPU's own attention
+# output: one bf16 rounding of y plus one of its input, |dy| <= 2^-7 |y| + 1e-5, rstd within 1e-3 -- and the
+# end-to-end result (the oracle's norm of the oracle's output) is held to the tensor-wide bars: rel-L2 <= 1e-2
+# for y (the output bar) and <= 5e-3 for rstd (the state bar).
+
+
+def check_norm(y_gpu, rstd_gpu, x_ref, z_bits, ni, what, x_gpu=None):
+    """The gated RMSNorm of the GPU against the oracle's: end to end (the oracle's norm of the oracle's output
+    rows ``x_ref``) and, given ``x_gpu`` (the GPU's un-normalised output rows from the same call without the
+    norm), the norm stage alone (bars above)."""
+    import oracle
+    w = ni.weight.astype(np.float64)
+    y = y_gpu.float().cpu().numpy().astype(np.float64) if torch.is_tensor(y_gpu) else y_gpu
+    assert np.isfinite(y).all(), f"{what}: non-finite normalised output"
+    y_ref, rstd_ref = oracle.gated_rmsnorm(x_ref, z_bits, w, ni.eps)
+    r = rel_l2(y, y_ref)
+    assert r <= OUT_REL_L2, f"{what}: normalised outputs rel-L2 {r:.3e} (<= {OUT_REL_L2})"
+    rs = None
+    if rstd_gpu is not None:
+        rs = rstd_gpu.cpu().numpy().astype(np.float64) if torch.is_tensor(rstd_gpu) else rstd_gpu
+        assert np.isfinite(rs).all(), f"{what}: rstd not written everywhere"
+        rr = rel_l2(rs, rstd_ref)
+        assert rr <= STATE_REL_L2, f"{what}: rstd rel-L2 {rr:.3e} (<= {STATE_REL_L2})"
+    if x_gpu is not None:
+        xg = x_gpu.float().cpu().numpy().astype(np.float64) if torch.is_tensor(x_gpu) else x_gpu
+        y_st, rstd_st = oracle.gated_rmsnorm(xg, z_bits, w, ni.eps)
+        bad = np.abs(y - y_st) > 2.0 ** -7 * np.abs(y_st) + 1e-5
+        assert not bad.any(), f"{what}: norm stage off on {int(bad.sum())} elements (max {float(np.abs(y - y_st).max()):.3e})"
+        if rs is not None:
+            rel = float(np.abs(rs / rstd_st - 1.0).max())
+            assert rel <= 1e-3, f"{what}: norm stage rstd relative error {rel:.3e} (<= 1e-3)"

@@ -63,17 +63,22 @@ P = ctypes.c_void_p
 
 
 def _prefill(lib, *, cu=(0, 4), H=2, lb=-5.0, scale=0.1, ws=FAKE, ws_bytes=256, stride=256, flags=0,
-             q=FAKE, final=FAKE, pool=None, slots=None, nslots=0):
+             q=FAKE, final=FAKE, pool=None, slots=None, nslots=0, norm=None):
     cu_host = np.array(cu, np.int32)
     return lib.kda_chunk_prefill(P(q), P(FAKE), P(FAKE), stride, P(FAKE), stride, P(FAKE), H, P(FAKE), P(FAKE),
                                  lb, scale, P(FAKE), cu_host.ctypes.data_as(P), len(cu) - 1, H, P(pool), nslots,
-                                 P(slots), flags, P(FAKE), stride, P(final), P(ws), ws_bytes, None)
+                                 P(slots), flags, P(FAKE), stride, norm, P(final), P(ws), ws_bytes, None)
 
 
-def _verify(lib, *, B=2, T=8, H=2, lb=-5.0, ws=FAKE, pool=FAKE, inter=FAKE):
+def _verify(lib, *, B=2, T=8, H=2, lb=-5.0, ws=FAKE, pool=FAKE, inter=FAKE, norm=None):
     return lib.kda_recurrent_verify(P(FAKE), P(FAKE), P(FAKE), H * 128, P(FAKE), H * 128, P(FAKE), H, P(FAKE),
-                                    P(FAKE), lb, 0.1, B, T, H, P(pool), 4, P(FAKE), P(FAKE), H * 128, P(inter),
+                                    P(FAKE), lb, 0.1, B, T, H, P(pool), 4, P(FAKE), P(FAKE), H * 128, norm, P(inter),
                                     P(ws), 256, None)
+
+
+def _norm(gate=FAKE, stride=256, weight=FAKE, eps=1e-6, rstd=None):
+    from kda_linear_attention_bounded_gb300._binding import _OutputNormC
+    return ctypes.byref(_OutputNormC(gate, stride, weight, eps, rstd))
 
 
 def test_prefill_rejects_bad_arguments(lib):
@@ -124,7 +129,7 @@ def test_verify_rejects_bad_arguments(lib):
 
 
 def _spec_step(lib, *, cu=(0, 4), B=2, T=8, H=2, pre=True, spec=True, pre_stride=256, spec_stride=256,
-               ns_idx=FAKE, s_idx=FAKE, n_out=100, ws_bytes=None, lb=-5.0):
+               ns_idx=FAKE, s_idx=FAKE, n_out=100, ws_bytes=None, lb=-5.0, norm=None):
     from kda_linear_attention_bounded_gb300._binding import TokenTensors
     cu_host = np.array(cu, np.int32)
     ws_bytes = lib.kda_prefill_workspace_size(int(cu[-1]), len(cu) - 1, H) if ws_bytes is None else ws_bytes
@@ -132,8 +137,8 @@ def _spec_step(lib, *, cu=(0, 4), B=2, T=8, H=2, pre=True, spec=True, pre_stride
     ts = TokenTensors(FAKE, FAKE, FAKE, spec_stride, FAKE, spec_stride, FAKE, H)
     return lib.kda_spec_step(ctypes.byref(tp) if pre else None, P(FAKE), cu_host.ctypes.data_as(P), len(cu) - 1,
                              None, 0, P(FAKE), ctypes.byref(ts) if spec else None, B, T, P(FAKE), P(FAKE), P(FAKE),
-                             P(FAKE), lb, 0.1, H, P(FAKE), 4, P(FAKE), H * 128, n_out, P(ns_idx), P(s_idx), P(FAKE),
-                             ws_bytes, None)
+                             P(FAKE), lb, 0.1, H, P(FAKE), 4, P(FAKE), H * 128, n_out, norm, P(ns_idx), P(s_idx),
+                             P(FAKE), ws_bytes, None)
 
 
 def test_spec_step_rejects_bad_arguments(lib):
@@ -150,6 +155,16 @@ def test_spec_step_rejects_bad_arguments(lib):
     assert _spec_step(lib, lb=-11.0) == 2
     assert _spec_step(lib, ws_bytes=256) == 3         # no room for the prefill's chunk blocks
     assert _spec_step(lib, cu=(0,), B=0, pre=False, spec=False, ns_idx=None, s_idx=None) == 0   # empty step
+
+
+def test_output_norm_is_checked_on_the_host(lib):
+    # every call rejects a bad norm descriptor before launching anything
+    for bad in (_norm(gate=None), _norm(gate=FAKE + 2), _norm(stride=100), _norm(stride=260), _norm(weight=None),
+                _norm(weight=FAKE + 4), _norm(eps=-1.0), _norm(eps=float("nan")), _norm(rstd=FAKE + 2)):
+        assert _prefill(lib, norm=bad, ws_bytes=lib.kda_prefill_workspace_size(4, 1, 2)) == 1
+        assert _verify(lib, norm=bad) == 1
+        assert _spec_step(lib, norm=bad) == 1
+    assert _prefill(lib, cu=(0,), norm=_norm(gate=None)) == 0    # nothing to do: the norm is not looked at
 
 
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
