@@ -340,38 +340,64 @@ def run_gpu(args):
     achieved = alg / avg_launch_s / 1e9
 
     # ---- end to end through the C ABI with host buffers ----
+    # Every step copies its inputs from pinned host memory, runs the call and copies its outputs back.  The
+    # steps are pipelined the way a serving loop runs them: step i+1's host-to-device copies (own stream)
+    # overlap step i's kernels, and step i's device-to-host copies (own stream) overlap step i+1's; device
+    # buffers are double-buffered and ordered by events.
     host = {name: getattr(dev, name).cpu().pin_memory() for name in ("q", "k", "v", "g", "beta")}
-    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    final_h = torch.empty(final.shape, dtype=final.dtype).pin_memory()
-    bufs = {name: torch.empty_like(getattr(dev, name)) for name in host}
+    out_h = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
+    final_h = [torch.empty(final.shape, dtype=final.dtype).pin_memory() for _ in range(2)]
+    bufs = [{name: torch.empty_like(getattr(dev, name)) for name in host} for _ in range(2)]
+    outs = [torch.empty_like(out) for _ in range(2)]
+    finals = [torch.empty_like(final) for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in host.values())
-    d2h = out_h.numel() * out_h.element_size() + final_h.numel() * final_h.element_size()
+    d2h = out_h[0].numel() * out_h[0].element_size() + final_h[0].numel() * final_h[0].element_size()
     e2e_steps = max(3, min(args.steps, 100))
+    s_h2d = torch.cuda.Stream(device)
+    s_d2h = torch.cuda.Stream(device)
+    ev = {k: [torch.cuda.Event() for _ in range(2)] for k in ("h2d", "comp", "d2h")}
+    for k in ev:
+        for e in ev[k]:
+            e.record(stream)
 
-    def e2e_step():
-        for name, t in host.items():
-            bufs[name].copy_(t, non_blocking=True)
-        kda.chunk_prefill(bufs["q"], bufs["k"], bufs["v"], bufs["g"], bufs["beta"], dev.A_log, dev.dt_bias, dev.cu,
-                          dev.cu_host, lower_bound=inp.lower_bound, scale=inp.scale, state_pool=dev.pool,
-                          slot_ids=dev.slots, load_initial=True, out=out, final_state=final, workspace=ws,
-                          stream=stream)
-        out_h.copy_(out, non_blocking=True)
-        final_h.copy_(final, non_blocking=True)
+    def e2e_step(i):
+        b = i & 1
+        with torch.cuda.stream(s_h2d):
+            s_h2d.wait_event(ev["comp"][b])          # the call that last read buffer b has finished
+            for name, t in host.items():
+                bufs[b][name].copy_(t, non_blocking=True)
+            ev["h2d"][b].record(s_h2d)
+        stream.wait_event(ev["h2d"][b])
+        stream.wait_event(ev["d2h"][b])              # output buffer b has been copied out
+        kda.chunk_prefill(bufs[b]["q"], bufs[b]["k"], bufs[b]["v"], bufs[b]["g"], bufs[b]["beta"], dev.A_log,
+                          dev.dt_bias, dev.cu, dev.cu_host, lower_bound=inp.lower_bound, scale=inp.scale,
+                          state_pool=dev.pool, slot_ids=dev.slots, load_initial=True, out=outs[b],
+                          final_state=finals[b], workspace=ws, stream=stream)
+        ev["comp"][b].record(stream)
+        with torch.cuda.stream(s_d2h):
+            s_d2h.wait_event(ev["comp"][b])
+            out_h[b].copy_(outs[b], non_blocking=True)
+            final_h[b].copy_(finals[b], non_blocking=True)
+            ev["d2h"][b].record(s_d2h)
 
-    for _ in range(3):
-        e2e_step()
+    for i in range(3):
+        e2e_step(i)
     torch.cuda.synchronize(device)
     barrier(world)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    e1.record(stream)
+    e0.record(s_h2d)
+    for i in range(e2e_steps):
+        e2e_step(i)
+    s_h2d.wait_stream(s_d2h)
+    e1.record(s_h2d)
     torch.cuda.synchronize(device)
     barrier(world)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, device)
     e2e_value = T * e2e_steps * world / (e2e_ms / 1e3)
+    # the results of the last step came back intact
+    assert torch.equal(out_h[(e2e_steps - 1) & 1], outs[(e2e_steps - 1) & 1].cpu())
+    del bufs, outs, finals
 
     # ---- verify (64 requests x 8, 4 and 1 tokens) and accept/commit, timed as CUDA-graph replays ----
     def graph_time_us(calls, steps):
@@ -525,7 +551,9 @@ def run_gpu(args):
                      "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else peak_kind},
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "steps": e2e_steps},
+                "steps": e2e_steps, "ms_per_step": e2e_ms / e2e_steps,
+                "pipelining": "step i+1's host-to-device copies and step i-1's device-to-host copies on their own "
+                              "streams overlap step i's call (double-buffered device buffers)"},
         "gpu_launches": 2 * args.steps,
         "clocks": clocks,
         "verify": vrec,
