@@ -48,6 +48,17 @@ def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
 
 
 @dataclass
+class ConvInputs:
+    """The short causal convolutions of q, k and v: weights ``[3 (q, k, v), H, D, W]`` fp32 (tap W-1 on the
+    current input), SiLU after each, and a pool of windows ``[slots, 3, W-1, H, D]`` (bf16 bit patterns: the
+    W-1 previous raw inputs, oldest first) beside the state pool, indexed by the same slot ids."""
+
+    weight: np.ndarray
+    silu: bool
+    pool: np.ndarray
+
+
+@dataclass
 class PrefillInputs:
     """One chunked-prefill call: packed varlen tokens ``[T, H, D]``."""
 
@@ -67,6 +78,7 @@ class PrefillInputs:
     load_initial: bool = False
     final_to_pool: bool = False
     meta: dict = field(default_factory=dict)
+    conv: ConvInputs | None = None
 
     @property
     def num_seqs(self) -> int:
@@ -106,10 +118,20 @@ class VerifyInputs:
     pool: np.ndarray
     slot_ids: np.ndarray
     meta: dict = field(default_factory=dict)
+    conv: ConvInputs | None = None
 
     @property
     def H(self) -> int:
         return int(self.q.shape[1])
+
+
+def conv_inputs(H: int, slots: int, *, seed: int, d: int = D, W: int = 4, silu: bool = True,
+                weight_std: float = 0.5) -> ConvInputs:
+    """weights ~ N(0, weight_std) per tap, windows ~ N(0, 1) (bf16)."""
+    rng = np.random.default_rng(seed)
+    weight = (rng.standard_normal((3, H, d, W)) * weight_std).astype(np.float32)
+    pool = f32_to_bf16_bits(rng.standard_normal((slots, 3, W - 1, H, d), dtype=np.float32))
+    return ConvInputs(weight=weight, silu=bool(silu), pool=pool)
 
 
 def _token_tensors(rng, total, H, d, g_mean):

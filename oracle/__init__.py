@@ -43,6 +43,12 @@ def default_threads() -> int:
     return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
 
 
+def bf16_widen(bits):
+    """bf16 bit patterns -> fp64 (exact)."""
+    b = np.ascontiguousarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
+    return b.view(np.float32).astype(np.float64)
+
+
 def _ptr(a):
     return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
 
@@ -59,6 +65,11 @@ class Oracle:
         P, I, Dbl = ctypes.c_void_p, ctypes.c_int, ctypes.c_double
         lib.kda_oracle_run.argtypes = [P, P, P, P, P, P, P, Dbl, Dbl, Dbl, P, I, I, I, I, I, I, P, P, P, P, I]
         lib.kda_oracle_run.restype = I
+        lib.kda_oracle_run_conv.argtypes = [P, P, P, P, P, P, P, Dbl, Dbl, Dbl, P, I, I, I, I, I, I, P, P, P, P, I,
+                                            P, I, I, P, P, P]
+        lib.kda_oracle_run_conv.restype = I
+        lib.kda_oracle_conv_step.argtypes = [P, P, P, I, I, I, P]
+        lib.kda_oracle_conv_step.restype = None
         lib.kda_oracle_core.argtypes = [P, P, P, P, P, I, I, I, Dbl, P, P, P]
         lib.kda_oracle_core.restype = I
         lib.kda_oracle_gate.argtypes = [P, P, Dbl, Dbl, I, P]
@@ -103,9 +114,65 @@ class Oracle:
             raise ValueError(f"oracle rejected the arguments (rc={rc})")
         return out, S_final, steps
 
+    def run_conv(self, q, k, v, g, beta_logits, A_log, dt_bias, lower_bound, scale, cu_seqlens, conv_w, silu, *,
+                 win0=None, S0=None, heads=None, record_steps=False, record_windows=False, want_final=True,
+                 nthreads=None, eps=L2NORM_EPS):
+        """:meth:`run` with q, k and v first passed through their short causal convolutions.
+
+        conv_w: ``[3 (q, k, v), H, d, W]`` (tap W-1 on the current input); silu: apply SiLU after each
+        convolution; win0: ``[N, 3, W-1, H, d]`` initial windows (raw inputs, oldest first) or None for zero.
+        Returns ``out``, ``S_final``, ``steps`` as :meth:`run`, then ``win_final [N, 3, W-1, H, d]`` (or None)
+        and ``win_steps [T, 3, W-1, H, d]`` (the window after each token, or None), all fp64."""
+        q, k, v, g = (_c(x, np.uint16) for x in (q, k, v, g))
+        beta_logits = _c(beta_logits, np.uint16)
+        A_log = _c(A_log, np.float32)
+        dt_bias = _c(dt_bias, np.float32)
+        cu = _c(cu_seqlens, np.int32)
+        T, H, dk = q.shape
+        dv = v.shape[2]
+        N = cu.shape[0] - 1
+        w = _c(conv_w, np.float64)
+        W = w.shape[-1]
+        if w.shape != (3, H, dk, W) or dk != dv:
+            raise ValueError("conv_w must be [3, H, d, W] with dk == dv == d")
+        hb, he = (0, H) if heads is None else heads
+        S0d = None if S0 is None else _c(S0, np.float64)
+        w0 = None if win0 is None else _c(win0, np.float64)
+        out = np.full((T, H, dv), np.nan)
+        S_final = np.full((N, H, dk, dv), np.nan) if want_final else None
+        steps = np.full((T, H, dk, dv), np.nan) if record_steps else None
+        wf = np.full((N, 3, W - 1, H, dk), np.nan) if want_final else None
+        ws = np.full((T, 3, W - 1, H, dk), np.nan) if record_windows else None
+        rc = self.lib.kda_oracle_run_conv(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta_logits), _ptr(A_log), _ptr(dt_bias),
+            float(lower_bound), float(scale), float(eps), _ptr(cu), N, H, dk, dv, hb, he,
+            _ptr(S0d), _ptr(out), _ptr(S_final), _ptr(steps), int(nthreads or default_threads()),
+            _ptr(w), W, 1 if silu else 0, _ptr(w0), _ptr(wf), _ptr(ws))
+        if rc != 0:
+            raise ValueError(f"oracle rejected the arguments (rc={rc})")
+        return out, S_final, steps, wf, ws
+
+    def conv_step(self, win, x, w, silu):
+        """One step of one short convolution row: returns ``(y, new window)``; win ``[W-1, d]``, x ``[d]``,
+        w ``[d, W]``."""
+        win = _c(win, np.float64).copy()
+        x = _c(x, np.float64)
+        w = _c(w, np.float64)
+        d, W = w.shape
+        y = np.empty(d)
+        self.lib.kda_oracle_conv_step(_ptr(win), _ptr(x), _ptr(w), W, d, 1 if silu else 0, _ptr(y))
+        return y, win
+
     def run_prefill(self, inp, **kw):
         """Oracle for a prefill workload object (the ``inputs`` module's ``PrefillInputs``)."""
         S0 = inp.initial_states() if inp.load_initial else None
+        if inp.conv is not None:   # returns the final windows too
+            c = inp.conv
+            win0 = bf16_widen(c.pool[inp.slot_ids]) if inp.load_initial else None
+            out, S, steps, wf, _ = self.run_conv(inp.q, inp.k, inp.v, inp.g, inp.beta, inp.A_log, inp.dt_bias,
+                                                 inp.lower_bound, inp.scale, inp.cu_seqlens, c.weight, c.silu,
+                                                 win0=win0, S0=S0, **kw)
+            return out, S, steps, wf
         return self.run(inp.q, inp.k, inp.v, inp.g, inp.beta, inp.A_log, inp.dt_bias,
                         inp.lower_bound, inp.scale, inp.cu_seqlens, S0=S0, **kw)
 
@@ -116,6 +183,14 @@ class Oracle:
         each draft token)."""
         cu = (np.arange(inp.B + 1) * inp.T).astype(np.int32)
         S0 = inp.pool[inp.slot_ids]
+        if inp.conv is not None:   # returns the per-step windows too: [B, T, 3, W-1, H, d]
+            c = inp.conv
+            out, _, steps, _, ws = self.run_conv(inp.q, inp.k, inp.v, inp.g, inp.beta, inp.A_log, inp.dt_bias,
+                                                 inp.lower_bound, inp.scale, cu, c.weight, c.silu,
+                                                 win0=bf16_widen(c.pool[inp.slot_ids]), S0=S0, record_steps=True,
+                                                 record_windows=True, want_final=False, **kw)
+            return (out, steps.reshape(inp.B, inp.T, inp.H, steps.shape[-2], steps.shape[-1]),
+                    ws.reshape(inp.B, inp.T, *ws.shape[1:]))
         out, _, steps = self.run(inp.q, inp.k, inp.v, inp.g, inp.beta, inp.A_log, inp.dt_bias,
                                  inp.lower_bound, inp.scale, cu, S0=S0, record_steps=True,
                                  want_final=False, **kw)
@@ -208,3 +283,11 @@ def l2norm(*a, **kw):
 
 def gated_rmsnorm(*a, **kw):
     return get().gated_rmsnorm(*a, **kw)
+
+
+def run_conv(*a, **kw):
+    return get().run_conv(*a, **kw)
+
+
+def conv_step(*a, **kw):
+    return get().conv_step(*a, **kw)

@@ -91,6 +91,31 @@ void kda_oracle_gated_rmsnorm(const double *x, const uint16_t *z, const double *
     }
 }
 
+/*
+ * Short causal depthwise convolution of one input row ("three short
+ * convolutions" on q, k and v per step, with per-step windows:
+ * TensorRT-LLM PR #21179 "GLM-5.3-Flash FP8 performance fixes on Hopper",
+ * KDA verify commit).  The pages print neither the width nor an activation;
+ * the reading taken: W taps per channel, tap W-1 on the current input and tap
+ * j on the input W-1-j tokens back,
+ *   y_c = act( sum_{j<W-1} w_c[j] win[j]_c + w_c[W-1] x_c ),  act = SiLU or none,
+ * where win holds the W-1 previous inputs of the sequence, oldest first
+ * (seeded from the carried window, zero for a fresh sequence).  The window
+ * then drops its oldest row and appends x.
+ */
+void kda_oracle_conv_step(double *win, const double *x, const double *w, int W, int d, int silu, double *y)
+{
+    for (int c = 0; c < d; ++c) {
+        double acc = w[(size_t)c * W + (W - 1)] * x[c];
+        for (int j = 0; j < W - 1; ++j) acc += w[(size_t)c * W + j] * win[(size_t)j * d + c];
+        y[c] = silu ? acc * sigmoid(acc) : acc;
+    }
+    for (int j = 0; j + 1 < W - 1; ++j)
+        for (int c = 0; c < d; ++c) win[(size_t)j * d + c] = win[(size_t)(j + 1) * d + c];
+    if (W > 1)
+        for (int c = 0; c < d; ++c) win[(size_t)(W - 2) * d + c] = x[c];
+}
+
 /* lambda_c = lower_bound * sigmoid(exp(A_log) * (g_c + dt_bias_c)). */
 void kda_oracle_gate(const double *g, const double *dt_bias, double A_log,
                      double lower_bound, int d, double *lambda)
@@ -169,6 +194,12 @@ typedef struct {
     int num_seqs, H, dk, dv, head_begin, head_end;
     const double *S0;
     double *out, *S_final, *step_states;
+    /* optional short convolution of q, k, v (dk == dv == d): weights [3][H][d][W]; windows [.][3][W-1][H][d] */
+    const double *conv_w;
+    int conv_W, conv_silu;
+    const double *conv_win0;   /* [num_seqs] initial windows, or NULL (zero) */
+    double *conv_win_final;    /* [num_seqs] final windows, or NULL */
+    double *conv_win_steps;    /* [T_total] window after each token, or NULL */
     int next_task; /* shared task counter */
 } job_t;
 
@@ -189,14 +220,43 @@ static void run_task(const job_t *J, int n, int h)
     for (int c = 0; c < dk; ++c) dtb[c] = (double)J->dt_bias[(size_t)h * dk + c];
     const double A_log = (double)J->A_log[h];
 
+    /* short convolution windows of this (sequence, head): [3][W-1][d] */
+    const int W = J->conv_w ? J->conv_W : 0, d = dk;
+    const size_t win_rows = W > 1 ? (size_t)(W - 1) : 0;
+    double *win = W ? (double *)calloc(3 * win_rows * (size_t)d + 1, sizeof(double)) : NULL;
+    double *raw = W ? (double *)malloc(sizeof(double) * (size_t)d) : NULL;
+    if (W && J->conv_win0)
+        for (int m = 0; m < 3; ++m)
+            for (size_t j = 0; j < win_rows; ++j)
+                memcpy(win + ((size_t)m * win_rows + j) * d,
+                       J->conv_win0 + ((((size_t)n * 3 + m) * win_rows + j) * H + h) * d, sizeof(double) * d);
+
     for (int t = J->cu_seqlens[n]; t < J->cu_seqlens[n + 1]; ++t) {
         const size_t rk = ((size_t)t * H + h) * dk; /* row of q / k / g */
         const size_t rv = ((size_t)t * H + h) * dv; /* row of v / out   */
-        for (int c = 0; c < dk; ++c) x[c] = bf16_to_double(J->q[rk + c]);
-        kda_oracle_l2norm(x, dk, J->eps, qh);
-        for (int c = 0; c < dk; ++c) x[c] = bf16_to_double(J->k[rk + c]);
-        kda_oracle_l2norm(x, dk, J->eps, kh);
-        for (int j = 0; j < dv; ++j) vv[j] = bf16_to_double(J->v[rv + j]);
+        if (W) {   /* q, k, v through their short convolutions, then as below */
+            const uint16_t *src[3] = {J->q + rk, J->k + rk, J->v + rv};
+            double *dst[3] = {x, kh, vv};
+            for (int m = 0; m < 3; ++m) {
+                for (int c = 0; c < d; ++c) raw[c] = bf16_to_double(src[m][c]);
+                kda_oracle_conv_step(win + (size_t)m * win_rows * d, raw,
+                                     J->conv_w + ((size_t)m * H + h) * d * W, W, d, J->conv_silu, dst[m]);
+            }
+            kda_oracle_l2norm(x, dk, J->eps, qh);
+            memcpy(x, kh, sizeof(double) * dk);
+            kda_oracle_l2norm(x, dk, J->eps, kh);
+            if (J->conv_win_steps)
+                for (int m = 0; m < 3; ++m)
+                    for (size_t j = 0; j < win_rows; ++j)
+                        memcpy(J->conv_win_steps + ((((size_t)t * 3 + m) * win_rows + j) * H + h) * d,
+                               win + ((size_t)m * win_rows + j) * d, sizeof(double) * d);
+        } else {
+            for (int c = 0; c < dk; ++c) x[c] = bf16_to_double(J->q[rk + c]);
+            kda_oracle_l2norm(x, dk, J->eps, qh);
+            for (int c = 0; c < dk; ++c) x[c] = bf16_to_double(J->k[rk + c]);
+            kda_oracle_l2norm(x, dk, J->eps, kh);
+            for (int j = 0; j < dv; ++j) vv[j] = bf16_to_double(J->v[rv + j]);
+        }
         for (int c = 0; c < dk; ++c) gg[c] = bf16_to_double(J->g[rk + c]);
         kda_oracle_gate(gg, dtb, A_log, J->lower_bound, dk, lam);
         double beta = sigmoid(bf16_to_double(J->beta[(size_t)t * H + h]));
@@ -207,7 +267,12 @@ static void run_task(const job_t *J, int n, int h)
     }
     if (J->S_final)
         memcpy(J->S_final + ((size_t)n * H + h) * state_elems, S, sizeof(double) * state_elems);
-    free(S); free(x); free(qh); free(kh); free(vv); free(gg); free(dtb); free(lam);
+    if (W && J->conv_win_final)
+        for (int m = 0; m < 3; ++m)
+            for (size_t j = 0; j < win_rows; ++j)
+                memcpy(J->conv_win_final + ((((size_t)n * 3 + m) * win_rows + j) * H + h) * d,
+                       win + ((size_t)m * win_rows + j) * d, sizeof(double) * d);
+    free(S); free(x); free(qh); free(kh); free(vv); free(gg); free(dtb); free(lam); free(win); free(raw);
 }
 
 static void *worker(void *arg)
@@ -233,6 +298,16 @@ static void *worker(void *arg)
  * Only the selected heads' entries of out / S_final / step_states are written.
  * Returns 0, or 1 on invalid sizes.
  */
+int kda_oracle_run_conv(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                        const uint16_t *g, const uint16_t *beta_logits,
+                        const float *A_log, const float *dt_bias,
+                        double lower_bound, double scale, double eps,
+                        const int32_t *cu_seqlens, int num_seqs, int H, int dk, int dv,
+                        int head_begin, int head_end, const double *S0,
+                        double *out, double *S_final, double *step_states, int nthreads,
+                        const double *conv_w, int conv_W, int conv_silu, const double *conv_win0,
+                        double *conv_win_final, double *conv_win_steps);
+
 int kda_oracle_run(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                    const uint16_t *g, const uint16_t *beta_logits,
                    const float *A_log, const float *dt_bias,
@@ -241,14 +316,38 @@ int kda_oracle_run(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                    int head_begin, int head_end, const double *S0,
                    double *out, double *S_final, double *step_states, int nthreads)
 {
+    return kda_oracle_run_conv(q, k, v, g, beta_logits, A_log, dt_bias, lower_bound, scale, eps, cu_seqlens,
+                               num_seqs, H, dk, dv, head_begin, head_end, S0, out, S_final, step_states, nthreads,
+                               NULL, 0, 0, NULL, NULL, NULL);
+}
+
+/*
+ * kda_oracle_run with q, k and v first passed through their short causal
+ * convolutions (kda_oracle_conv_step), when conv_w is not NULL:
+ *   conv_w: [3 (q, k, v)][H][d][W]; conv_win0 / conv_win_final: [num_seqs][3][W-1][H][d]
+ *   (initial windows or NULL for zero, final windows or NULL); conv_win_steps:
+ *   [T_total][3][W-1][H][d] the window after each token, or NULL.  Needs dk == dv.
+ */
+int kda_oracle_run_conv(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                        const uint16_t *g, const uint16_t *beta_logits,
+                        const float *A_log, const float *dt_bias,
+                        double lower_bound, double scale, double eps,
+                        const int32_t *cu_seqlens, int num_seqs, int H, int dk, int dv,
+                        int head_begin, int head_end, const double *S0,
+                        double *out, double *S_final, double *step_states, int nthreads,
+                        const double *conv_w, int conv_W, int conv_silu, const double *conv_win0,
+                        double *conv_win_final, double *conv_win_steps)
+{
     if (num_seqs < 0 || H <= 0 || dk <= 0 || dv <= 0) return 1;
+    if (conv_w && (conv_W < 1 || dk != dv)) return 1;
     if (head_begin < 0 || head_end > H || head_begin > head_end) return 1;
     if (cu_seqlens[0] != 0) return 1;
     for (int n = 0; n < num_seqs; ++n)
         if (cu_seqlens[n + 1] < cu_seqlens[n]) return 1;
     job_t J = {q, k, v, g, beta_logits, A_log, dt_bias, lower_bound, scale, eps,
                cu_seqlens, num_seqs, H, dk, dv, head_begin, head_end, S0,
-               out, S_final, step_states, 0};
+               out, S_final, step_states, conv_w, conv_W, conv_silu, conv_win0,
+               conv_win_final, conv_win_steps, 0};
     if (nthreads < 1) nthreads = 1;
     if (nthreads == 1) {
         worker(&J);

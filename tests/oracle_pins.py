@@ -365,6 +365,93 @@ def pin_gated_rmsnorm(O):
     _close((y3 ** 2).mean(axis=1), 0.25 * ms / (ms + 0.3), 1e-13, "eps under the root: mean y^2 = ms / (ms + eps) / 4")
 
 
+# --------------------------------------------------------------------------
+# short causal convolutions of q, k, v
+# --------------------------------------------------------------------------
+
+def pin_short_conv_step(O):
+    """One channel row of the short convolution: the impulse response reads the taps in order (tap W-1 on the
+    current input), a random signal matches numpy's convolve with the reversed taps, SiLU is z sigmoid(z), and
+    the window ends holding the last W-1 inputs (oldest first)."""
+    rng = np.random.default_rng(41)
+    d, W, T = 6, 4, 23
+    w = rng.standard_normal((d, W))
+    # impulse at t = 0 from a zero window: y_t = w[:, W-1-t]
+    win = np.zeros((W - 1, d))
+    for t in range(W + 2):
+        x = np.ones(d) if t == 0 else np.zeros(d)
+        y, win = O.conv_step(win, x, w, False)
+        _close(y, w[:, W - 1 - t] if t < W else np.zeros(d), 1e-15, f"impulse response at t = {t}")
+    # a random signal, zero window: numpy convolve with reversed taps; SiLU on top
+    xs = rng.standard_normal((T, d))
+    for silu in (False, True):
+        win = np.zeros((W - 1, d))
+        ys = []
+        for t in range(T):
+            y, win = O.conv_step(win, xs[t], w, silu)
+            ys.append(y)
+        ref = np.stack([np.convolve(xs[:, c], w[c, ::-1])[:T] for c in range(d)], axis=1)
+        if silu:
+            ref = ref * expit(ref)
+        _close(np.array(ys), ref, 1e-13, f"random signal vs numpy convolve (silu={silu})")
+        _close(win, xs[T - (W - 1):], 0.0, "the window holds the last W-1 inputs, oldest first")
+    # a carried window continues the signal: the first W-1 outputs see it
+    win0 = rng.standard_normal((W - 1, d))
+    y0, _ = O.conv_step(win0, xs[0], w, False)
+    _close(y0, (w[:, :W - 1] * win0.T).sum(axis=1) + w[:, W - 1] * xs[0], 1e-14, "first output uses the window")
+
+
+def pin_short_conv_in_the_path(O):
+    """The convolutions feed the recurrence: identity taps without SiLU reproduce the plain run; general taps
+    equal an independent numpy convolution of each of q, k, v fed to the core (so q's convolution reaches q,
+    k's k, v's v); running in two pieces with the final window carried equals one run."""
+    rng = np.random.default_rng(42)
+    d, H, T, W = 16, 2, 29, 4
+    f = lambda *sh: f32_to_bf16_bits(rng.standard_normal(sh).astype(np.float32))
+    q, k, v, g, beta = f(T, H, d), f(T, H, d), f(T, H, d), f(T, H, d), f(T, H)
+    A_log = np.log(rng.uniform(1, 4, H)).astype(np.float32)
+    dtb = (rng.standard_normal((H, d)) * 0.1).astype(np.float32)
+    cu = np.array([0, T], np.int32)
+    lb, scale = -2.0, 0.3
+    ident = np.zeros((3, H, d, W))
+    ident[..., W - 1] = 1.0
+    out_id, S_id, _, _, _ = O.run_conv(q, k, v, g, beta, A_log, dtb, lb, scale, cu, ident, False)
+    out_pl, S_pl, _ = O.run(q, k, v, g, beta, A_log, dtb, lb, scale, cu)
+    _close(out_id, out_pl, 1e-14, "identity taps: outputs of the plain run")
+    _close(S_id, S_pl, 1e-14, "identity taps: final state of the plain run")
+    w = rng.standard_normal((3, H, d, W)) * 0.6
+    win0 = rng.standard_normal((1, 3, W - 1, H, d))
+    out, S, _, wf, _ = O.run_conv(q, k, v, g, beta, A_log, dtb, lb, scale, cu, w, True, win0=win0)
+    for h in range(H):
+        conv = []
+        for m, x in enumerate((q, k, v)):
+            xs = np.concatenate([win0[0, m, :, h, :], _widen(x[:, h, :])])   # window rows, then the inputs
+            z = np.stack([np.convolve(xs[:, c], w[m, h, c, ::-1])[W - 1:W - 1 + T] for c in range(d)], axis=1)
+            conv.append(z * expit(z))
+        qh = conv[0] / np.sqrt((conv[0] ** 2).sum(axis=1, keepdims=True) + oracle_eps())
+        kh = conv[1] / np.sqrt((conv[1] ** 2).sum(axis=1, keepdims=True) + oracle_eps())
+        lam = lb * expit(math.exp(A_log[h]) * (_widen(g[:, h, :]) + dtb[h]))
+        bt = expit(_widen(beta[:, h]))
+        o_ref, S_ref, _ = O.core(qh, kh, conv[2], lam, bt, scale)
+        _close(out[:, h], o_ref, 1e-12, f"head {h}: conv'd q/k/v fed to the core")
+        _close(S[0, h], S_ref, 1e-12, f"head {h}: final state")
+        for m, x in enumerate((q, k, v)):
+            _close(wf[0, m, :, h], _widen(x[T - (W - 1):, h, :]), 0.0, f"head {h}: final window of input {m}")
+    cut = 11
+    o1, S1, _, w1, _ = O.run_conv(q[:cut], k[:cut], v[:cut], g[:cut], beta[:cut], A_log, dtb, lb, scale,
+                                  np.array([0, cut], np.int32), w, True, win0=win0)
+    o2, S2, _, w2, _ = O.run_conv(q[cut:], k[cut:], v[cut:], g[cut:], beta[cut:], A_log, dtb, lb, scale,
+                                  np.array([0, T - cut], np.int32), w, True, win0=w1, S0=S1)
+    _close(np.concatenate([o1, o2]), out, 1e-13, "split with the window carried: outputs")
+    _close(S2, S, 1e-13, "split with the window carried: final state")
+    _close(w2, wf, 0.0, "split with the window carried: final window")
+
+
+def oracle_eps():
+    import oracle
+    return oracle.L2NORM_EPS
+
+
 ALL_PINS = [
     pin_worked_example,
     pin_gate_special_cases,
@@ -380,4 +467,6 @@ ALL_PINS = [
     pin_contraction_bound,
     pin_chunked_equals_sequential,
     pin_gated_rmsnorm,
+    pin_short_conv_step,
+    pin_short_conv_in_the_path,
 ]

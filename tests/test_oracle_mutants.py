@@ -30,6 +30,13 @@ MUTANTS = {
     "rmsnorm_gate_sign": ("sigmoid(bf16_to_double(z[(size_t)r * d + c]))", "sigmoid(-bf16_to_double(z[(size_t)r * d + c]))"),
     "rmsnorm_ungated": ("* w[c] * sigmoid(bf16_to_double(z[(size_t)r * d + c]));", "* w[c];"),
     "rmsnorm_rstd_not_inverse": ("rstd[r] = inv_rms;", "rstd[r] = 1.0 / inv_rms;"),
+    "conv_taps_reversed": ("acc += w[(size_t)c * W + j] * win[(size_t)j * d + c];",
+                           "acc += w[(size_t)c * W + (W - 2 - j)] * win[(size_t)j * d + c];"),
+    "conv_window_not_shifted": ("win[(size_t)j * d + c] = win[(size_t)(j + 1) * d + c];", "(void)0;"),
+    "conv_no_silu": ("y[c] = silu ? acc * sigmoid(acc) : acc;", "y[c] = acc;"),
+    "conv_silu_as_sigmoid": ("y[c] = silu ? acc * sigmoid(acc) : acc;", "y[c] = silu ? sigmoid(acc) : acc;"),
+    "conv_q_k_swapped": ("double *dst[3] = {x, kh, vv};", "double *dst[3] = {kh, x, vv};"),
+    "conv_window_not_seeded": ("if (W && J->conv_win0)", "if (W && J->conv_win0 && 0)"),
 }
 
 
