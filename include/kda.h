@@ -118,6 +118,31 @@ typedef struct kda_output_norm {
   float *rstd;                   /* [rows, H] fp32 (row-major), or NULL */
 } kda_output_norm;
 
+/*
+ * Optional short causal convolutions of q, k and v ("three short
+ * convolutions" per step with per-step windows: TensorRT-LLM PR #21179
+ * "GLM-5.3-Flash FP8 performance fixes on Hopper", KDA verify commit).  With
+ * one, the q, k, v tensors a call receives are the RAW inputs of the
+ * convolutions; per channel c of each of the three and per token,
+ *   y_c = act( w_c[0] x_{t-3} + w_c[1] x_{t-2} + w_c[2] x_{t-1} + w_c[3] x_t )
+ * with act = SiLU or none, and y replaces q, k, v in the recurrence.  Inputs
+ * before a sequence's first token come from its window: the 3 previous raw
+ * inputs, oldest first, kept per pool slot beside the recurrent state.  The
+ * pages print neither the width nor the activation: width 4 and SiLU are the
+ * readings taken (the activation is selectable).
+ */
+#define KDA_CONV_NONE 0
+#define KDA_CONV_SILU 1
+typedef struct kda_short_conv {
+  const float *weight;           /* [3 (q, k, v), H, 128, 4] fp32; tap 3 on the current input */
+  int activation;                /* KDA_CONV_SILU or KDA_CONV_NONE */
+  uint16_t *window_pool;         /* [num_slots, 3, 3, H, 128] bf16 raw inputs: tensor, row (oldest first), head, channel */
+  uint16_t *window_dense;        /* kda_chunk_prefill: [num_seqs, 3, 3, H, 128] final windows when the final
+                                    states are dense (else NULL); ignored elsewhere */
+  uint16_t *step_windows;        /* kda_recurrent_verify: [B, T, 3, 3, H, 128] window after each draft token;
+                                    kda_commit_accepted: the same records, read */
+} kda_short_conv;
+
 /* Static, human-readable text for a status code. */
 KDA_API const char *kda_status_string(int status);
 
@@ -165,6 +190,10 @@ KDA_API int kda_read_device_status(const void *workspace, size_t workspace_bytes
  *  out              [T_total, H, 128] bf16, token stride out_token_stride
  *  norm             NULL, or the gated RMSNorm applied to each output row
  *                   (gate and rstd rows are token rows)
+ *  conv             NULL, or the short convolutions of q, k, v (q, k, v are then
+ *                   their raw inputs): a sequence starts from its slot's window
+ *                   with KDA_LOAD_INITIAL (else from zeros) and its final window
+ *                   goes to the pool with KDA_FINAL_TO_POOL (else to window_dense)
  *  final_state      [num_seqs, H, 128, 128] fp32 dense final states; required
  *                   unless KDA_FINAL_TO_POOL (then ignored, may be NULL).
  *  Inputs and outputs must not overlap, except state_pool which may be both
@@ -181,8 +210,9 @@ KDA_API int kda_chunk_prefill(const uint16_t *q, const uint16_t *k, const uint16
                       const int32_t *cu_seqlens_dev, const int32_t *cu_seqlens_host,
                       int num_seqs, int H, float *state_pool, int num_slots,
                       const int32_t *slot_ids, int flags, uint16_t *out,
-                      int64_t out_token_stride, const kda_output_norm *norm, float *final_state,
-                      void *workspace, size_t workspace_bytes, void *stream);
+                      int64_t out_token_stride, const kda_output_norm *norm,
+                      const kda_short_conv *conv, float *final_state, void *workspace,
+                      size_t workspace_bytes, void *stream);
 
 /*
  * Speculative-decode verify over a pooled fp32 state.  Source: TensorRT-LLM
@@ -199,6 +229,10 @@ KDA_API int kda_chunk_prefill(const uint16_t *q, const uint16_t *k, const uint16
  *  out              [B*T, H, 128] bf16
  *  norm             NULL, or the gated RMSNorm applied to each output row
  *                   (gate and rstd rows are token rows b*T + t)
+ *  conv             NULL, or the short convolutions of q, k, v (q, k, v are then
+ *                   their raw inputs): request b starts from window_pool[slot_ids[b]]
+ *                   (read only) and the window after each draft token t goes to
+ *                   step_windows[b, t]
  *  intermediate_states [B, T, H, 128, 128] fp32: row (b, t) = state after draft token t
  *  1 <= T <= 64.
  *
@@ -213,8 +247,8 @@ KDA_API int kda_recurrent_verify(const uint16_t *q, const uint16_t *k, const uin
                          float scale, int B, int T, int H, const float *state_pool,
                          int num_slots, const int32_t *slot_ids, uint16_t *out,
                          int64_t out_token_stride, const kda_output_norm *norm,
-                         float *intermediate_states, void *workspace, size_t workspace_bytes,
-                         void *stream);
+                         const kda_short_conv *conv, float *intermediate_states, void *workspace,
+                         size_t workspace_bytes, void *stream);
 
 /*
  * Accept/commit after kda_recurrent_verify.  Source: vLLM PR #55737 "Use
@@ -226,7 +260,9 @@ KDA_API int kda_recurrent_verify(const uint16_t *q, const uint16_t *k, const uin
  * intermediate_states[b, n-1] (all heads) into state_pool[slot_ids[b]]; n = 0
  * leaves the slot untouched.  Counts outside [0, T] or slots outside
  * [0, num_slots) skip that request and set a device status bit, except
- * KDA_PAD_SLOT_ID rows, which are skipped without one.
+ * KDA_PAD_SLOT_ID rows, which are skipped without one.  With conv, the window
+ * after token n-1 (conv->step_windows[b, n-1]) goes to conv->window_pool[slot]
+ * in the same way.
  *
  *  state_pool          [num_slots, H, 128, 128] fp32, written
  *  slot_ids            [B] int32 device, distinct (padding rows excepted)
@@ -235,8 +271,8 @@ KDA_API int kda_recurrent_verify(const uint16_t *q, const uint16_t *k, const uin
  */
 KDA_API int kda_commit_accepted(float *state_pool, int num_slots, const int32_t *slot_ids,
                                 const int32_t *num_accepted, const float *intermediate_states,
-                                int B, int T, int H, void *workspace, size_t workspace_bytes,
-                                void *stream);
+                                const kda_short_conv *conv, int B, int T, int H, void *workspace,
+                                size_t workspace_bytes, void *stream);
 
 /*
  * One speculative-decoding step of a KDA layer: the prefill segment (the
@@ -266,6 +302,8 @@ KDA_API int kda_commit_accepted(float *state_pool, int num_slots, const int32_t 
  *  spec_token_indx  [B*T] int32 device: output row of verify token j (= b*T + t)
  *  norm             NULL, or the gated RMSNorm applied to each output row
  *                   (gate and rstd rows are output rows of core_attn_out)
+ *  conv             NULL, or the short convolutions of q, k, v for both segments,
+ *                   as in kda_chunk_prefill and kda_recurrent_verify
  *
  * Preconditions: the output rows named by the two index arrays are distinct
  * (rows named by neither are left as they were).  An index outside
@@ -287,7 +325,7 @@ KDA_API int kda_spec_step(const kda_token_tensors *prefill, const int32_t *cu_se
                           const float *dt_bias, float lower_bound, float scale, int H, float *state_pool,
                           int num_slots, uint16_t *core_attn_out, int64_t out_token_stride,
                           int64_t num_out_tokens, const kda_output_norm *norm,
-                          const int32_t *non_spec_token_indx,
+                          const kda_short_conv *conv, const int32_t *non_spec_token_indx,
                           const int32_t *spec_token_indx, void *workspace, size_t workspace_bytes,
                           void *stream);
 

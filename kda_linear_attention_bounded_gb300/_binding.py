@@ -27,6 +27,8 @@ KDA_DEVICE_BAD_INDEX = 8
 KDA_LOAD_INITIAL = 1
 KDA_FINAL_TO_POOL = 2
 KDA_PAD_SLOT_ID = -1
+KDA_CONV_NONE = 0
+KDA_CONV_SILU = 1
 
 #: exported symbols of include/kda.h
 EXPORTS = ("kda_status_string", "kda_workspace_size", "kda_prefill_workspace_size", "kda_workspace_reset",
@@ -71,6 +73,39 @@ class OutputNorm:
         return _OutputNormC(self.gate.data_ptr(), gs, w.data_ptr(), self.eps, None if r is None else r.data_ptr())
 
 
+class _ShortConvC(ctypes.Structure):
+    """``kda_short_conv``."""
+    _fields_ = [("weight", ctypes.c_void_p), ("activation", ctypes.c_int), ("window_pool", ctypes.c_void_p),
+                ("window_dense", ctypes.c_void_p), ("step_windows", ctypes.c_void_p)]
+
+
+class ShortConv:
+    """Short causal convolutions of q, k, v (``kda_short_conv``); q, k, v passed to a call are then their raw
+    inputs.  weight: CUDA fp32 ``[3, H, 128, 4]``; window_pool: CUDA bf16 ``[slots, 3, 3, H, 128]``;
+    window_dense: prefill, ``[num_seqs, 3, 3, H, 128]`` final windows with dense final states; step_windows:
+    verify / commit, ``[B, T, 3, 3, H, 128]``."""
+
+    def __init__(self, weight, window_pool, silu=True, window_dense=None, step_windows=None):
+        self.weight, self.window_pool, self.silu = weight, window_pool, bool(silu)
+        self.window_dense, self.step_windows = window_dense, step_windows
+
+    def as_c(self):
+        w = self.weight
+        if w.dtype != torch.float32 or not w.is_cuda or w.dim() != 4 or w.shape[2:] != (128, 4) or not w.is_contiguous():
+            raise ValueError("conv weight: expected a contiguous CUDA fp32 tensor [3, H, 128, 4]")
+        for name in ("window_pool", "window_dense", "step_windows"):
+            t = getattr(self, name)
+            if t is not None and (t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous()):
+                raise ValueError(f"conv {name}: expected a contiguous CUDA bf16 tensor")
+        return _ShortConvC(w.data_ptr(), KDA_CONV_SILU if self.silu else KDA_CONV_NONE,
+                           *(None if t is None else t.data_ptr()
+                             for t in (self.window_pool, self.window_dense, self.step_windows)))
+
+
+def _conv_arg(conv):
+    return None if conv is None else ctypes.byref(conv.as_c())
+
+
 def _norm_arg(norm, H):
     return None if norm is None else ctypes.byref(norm.as_c(H))
 
@@ -107,17 +142,18 @@ def load():
     lib.kda_read_device_status.argtypes = [P, SZ, ctypes.POINTER(ctypes.c_uint32), P]
     lib.kda_read_device_status.restype = I
     NP = ctypes.POINTER(_OutputNormC)
+    CP = ctypes.POINTER(_ShortConvC)
     lib.kda_chunk_prefill.argtypes = [P, P, P, I64, P, I64, P, I64, P, P, F, F, P, P, I, I, P, I, P, I, P,
-                                      I64, NP, P, P, SZ, P]
+                                      I64, NP, CP, P, P, SZ, P]
     lib.kda_chunk_prefill.restype = I
     lib.kda_recurrent_verify.argtypes = [P, P, P, I64, P, I64, P, I64, P, P, F, F, I, I, I, P, I, P, P, I64,
-                                         NP, P, P, SZ, P]
+                                         NP, CP, P, P, SZ, P]
     lib.kda_recurrent_verify.restype = I
-    lib.kda_commit_accepted.argtypes = [P, I, P, P, P, I, I, I, P, SZ, P]
+    lib.kda_commit_accepted.argtypes = [P, I, P, P, P, CP, I, I, I, P, SZ, P]
     lib.kda_commit_accepted.restype = I
     TT = ctypes.POINTER(TokenTensors)
-    lib.kda_spec_step.argtypes = [TT, P, P, I, P, I, P, TT, I, I, P, P, P, P, F, F, I, P, I, P, I64, I64, NP, P, P,
-                                  P, SZ, P]
+    lib.kda_spec_step.argtypes = [TT, P, P, I, P, I, P, TT, I, I, P, P, P, P, F, F, I, P, I, P, I64, I64, NP, CP, P,
+                                  P, P, SZ, P]
     lib.kda_spec_step.restype = I
     _lib = lib
     return lib
@@ -183,7 +219,8 @@ def _beta_stride(b, H):
 
 def chunk_prefill(q, k, v, g, beta_logits, A_log, dt_bias, cu_seqlens, cu_seqlens_host, *,
                   lower_bound=-5.0, scale=None, state_pool=None, slot_ids=None, load_initial=False,
-                  final_to_pool=False, out=None, final_state=None, norm=None, workspace=None, stream=None):
+                  final_to_pool=False, out=None, final_state=None, norm=None, conv=None, workspace=None,
+                  stream=None):
     """``kda_chunk_prefill``.  Returns ``(out, final_state)`` (final_state is None
     when the final states go to the pool).  ``norm``: an :class:`OutputNorm` applied to the output rows."""
     lib = load()
@@ -213,16 +250,16 @@ def chunk_prefill(q, k, v, g, beta_logits, A_log, dt_bias, cu_seqlens, cu_seqlen
         _ptr(q), _ptr(k), _ptr(v), qs, _ptr(g), gs, _ptr(beta_logits), bs, _ptr(A_log), _ptr(dt_bias),
         float(lower_bound), float(scale), _ptr(cu_seqlens), ctypes.c_void_p(cu_host.data_ptr()), N, H,
         _ptr(state_pool), 0 if state_pool is None else state_pool.shape[0], _ptr(slot_ids), flags,
-        _ptr(out), os_, _norm_arg(norm, H), _ptr(None if final_to_pool else final_state), _ptr(workspace),
-        workspace.numel(), _stream_ptr(stream, dev))
+        _ptr(out), os_, _norm_arg(norm, H), _conv_arg(conv), _ptr(None if final_to_pool else final_state),
+        _ptr(workspace), workspace.numel(), _stream_ptr(stream, dev))
     if rc != KDA_OK:
         raise KdaError(rc, "kda_chunk_prefill")
     return out, (None if final_to_pool else final_state)
 
 
 def recurrent_verify(q, k, v, g, beta_logits, A_log, dt_bias, state_pool, slot_ids, T, *,
-                     lower_bound=-5.0, scale=None, out=None, intermediate_states=None, norm=None, workspace=None,
-                     stream=None):
+                     lower_bound=-5.0, scale=None, out=None, intermediate_states=None, norm=None, conv=None,
+                     workspace=None, stream=None):
     """``kda_recurrent_verify``.  Returns ``(out, intermediate_states)``.  ``norm``: an :class:`OutputNorm`
     applied to the output rows."""
     lib = load()
@@ -246,15 +283,17 @@ def recurrent_verify(q, k, v, g, beta_logits, A_log, dt_bias, state_pool, slot_i
     rc = lib.kda_recurrent_verify(
         _ptr(q), _ptr(k), _ptr(v), qs, _ptr(g), gs, _ptr(beta_logits), bs, _ptr(A_log), _ptr(dt_bias),
         float(lower_bound), float(scale), B, int(T), H, _ptr(state_pool), state_pool.shape[0], _ptr(slot_ids),
-        _ptr(out), os_, _norm_arg(norm, H), _ptr(intermediate_states), _ptr(workspace), workspace.numel(),
-        _stream_ptr(stream, dev))
+        _ptr(out), os_, _norm_arg(norm, H), _conv_arg(conv), _ptr(intermediate_states), _ptr(workspace),
+        workspace.numel(), _stream_ptr(stream, dev))
     if rc != KDA_OK:
         raise KdaError(rc, "kda_recurrent_verify")
     return out, intermediate_states
 
 
-def commit_accepted(state_pool, slot_ids, num_accepted, intermediate_states, *, workspace=None, stream=None):
-    """``kda_commit_accepted``: pool[slot_ids[b]] = intermediate_states[b, num_accepted[b] - 1]."""
+def commit_accepted(state_pool, slot_ids, num_accepted, intermediate_states, *, conv=None, workspace=None,
+                    stream=None):
+    """``kda_commit_accepted``: pool[slot_ids[b]] = intermediate_states[b, num_accepted[b] - 1] (and, with
+    ``conv``, conv.window_pool[slot_ids[b]] = conv.step_windows[b, num_accepted[b] - 1])."""
     lib = load()
     B, T, H = intermediate_states.shape[:3]
     dev = state_pool.device
@@ -264,7 +303,8 @@ def commit_accepted(state_pool, slot_ids, num_accepted, intermediate_states, *, 
     if workspace is None:
         workspace = make_workspace(dev, stream)
     rc = lib.kda_commit_accepted(_ptr(state_pool), state_pool.shape[0], _ptr(slot_ids), _ptr(num_accepted),
-                                 _ptr(intermediate_states), B, T, H, _ptr(workspace), workspace.numel(),
+                                 _ptr(intermediate_states), _conv_arg(conv), B, T, H, _ptr(workspace),
+                                 workspace.numel(),
                                  _stream_ptr(stream, dev))
     if rc != KDA_OK:
         raise KdaError(rc, "kda_commit_accepted")
@@ -287,7 +327,7 @@ def _token_struct(tensors, H):
 def spec_step(prefill, cu_seqlens, cu_seqlens_host, spec, T, A_log, dt_bias, state_pool, core_attn_out,
               non_spec_token_indx, spec_token_indx, *, prefill_slot_ids=None, spec_slot_ids=None,
               load_initial=False, final_to_pool=False, final_state=None, intermediate_states=None,
-              lower_bound=-5.0, scale=None, norm=None, workspace=None, stream=None):
+              lower_bound=-5.0, scale=None, norm=None, conv=None, workspace=None, stream=None):
     """``kda_spec_step``: the prefill segment and the verify segment of one speculative-decoding step, their
     outputs written into ``core_attn_out`` rows ``non_spec_token_indx`` / ``spec_token_indx``.
 
@@ -330,7 +370,8 @@ def spec_step(prefill, cu_seqlens, cu_seqlens_host, spec, T, A_log, dt_bias, sta
         _ptr(None if final_to_pool else final_state), None if spc is None else ctypes.byref(spc), B, int(T),
         _ptr(spec_slot_ids), _ptr(intermediate_states), _ptr(A_log), _ptr(dt_bias), float(lower_bound),
         float(scale), H, _ptr(state_pool), 0 if state_pool is None else state_pool.shape[0], _ptr(core_attn_out),
-        os_, core_attn_out.shape[0], _norm_arg(norm, H), _ptr(non_spec_token_indx), _ptr(spec_token_indx),
+        os_, core_attn_out.shape[0], _norm_arg(norm, H), _conv_arg(conv), _ptr(non_spec_token_indx),
+        _ptr(spec_token_indx),
         _ptr(workspace),
         workspace.numel(), _stream_ptr(stream, dev))
     if rc != KDA_OK:

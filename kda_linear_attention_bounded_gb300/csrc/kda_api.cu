@@ -66,14 +66,28 @@ int check_norm(const kda_output_norm *norm, int H, kda::OutNorm *n) {
   return KDA_OK;
 }
 
+// Host-side checks of the optional short convolutions; fills `c` (weight == nullptr when absent).
+int check_conv(const kda_short_conv *conv, kda::ShortConv *c) {
+  *c = kda::ShortConv{};
+  if (!conv) return KDA_OK;
+  if (!conv->weight || !aligned16(conv->weight)) return KDA_ERR_INVALID_ARG;
+  if (conv->activation != KDA_CONV_NONE && conv->activation != KDA_CONV_SILU) return KDA_ERR_INVALID_ARG;
+  c->weight = conv->weight;
+  c->silu = conv->activation == KDA_CONV_SILU;
+  c->window_pool = conv->window_pool;
+  c->window_dense = conv->window_dense;
+  c->step_windows = conv->step_windows;
+  return KDA_OK;
+}
+
 // Host-side checks of one prefill call; on success fills `a` (no launch).
 int prepare_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v, int64_t qkv_token_stride,
                     const uint16_t *g, int64_t g_token_stride, const uint16_t *beta_logits,
                     int64_t beta_token_stride, const float *A_log, const float *dt_bias, float lower_bound,
                     float scale, const int32_t *cu_seqlens_dev, const int32_t *cu_seqlens_host, int num_seqs,
                     int H, float *state_pool, int num_slots, const int32_t *slot_ids, int flags, uint16_t *out,
-                    int64_t out_token_stride, const kda_output_norm *norm, float *final_state, void *workspace,
-                    size_t workspace_bytes, kda::ChunkArgs *a) {
+                    int64_t out_token_stride, const kda_output_norm *norm, const kda_short_conv *conv,
+                    float *final_state, void *workspace, size_t workspace_bytes, kda::ChunkArgs *a) {
   if (int rc = check_workspace(workspace, workspace_bytes)) return rc;
   if (num_seqs < 0) return KDA_ERR_INVALID_ARG;
   if (!cu_seqlens_dev || !cu_seqlens_host) return KDA_ERR_INVALID_ARG;
@@ -93,6 +107,7 @@ int prepare_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v, int
   if (!(flags & KDA_FINAL_TO_POOL) && (!final_state || !aligned16(final_state))) return KDA_ERR_INVALID_ARG;
   if (workspace_bytes < kda::prefill_workspace_bytes(cu_seqlens_host[num_seqs], num_seqs, H)) return KDA_ERR_WORKSPACE;
   if (int rc = check_norm(norm, H, &a->norm)) return rc;
+  if (conv) return KDA_ERR_UNSUPPORTED;   // the prefill's convolutions are not built yet
 
   a->q = q; a->k = k; a->v = v; a->g = g; a->beta = beta_logits;
   a->qkv_stride = qkv_token_stride; a->g_stride = g_token_stride;
@@ -116,8 +131,9 @@ int prepare_verify(const uint16_t *q, const uint16_t *k, const uint16_t *v, int6
                    const uint16_t *g, int64_t g_token_stride, const uint16_t *beta_logits, int64_t beta_token_stride,
                    const float *A_log, const float *dt_bias, float lower_bound, float scale, int B, int T, int H,
                    const float *state_pool, int num_slots, const int32_t *slot_ids, uint16_t *out,
-                   int64_t out_token_stride, const kda_output_norm *norm, float *intermediate_states,
-                   void *workspace, size_t workspace_bytes, kda::RecurrentArgs *a) {
+                   int64_t out_token_stride, const kda_output_norm *norm, const kda_short_conv *conv,
+                   float *intermediate_states, void *workspace, size_t workspace_bytes,
+                   kda::RecurrentArgs *a) {
   if (int rc = check_workspace(workspace, workspace_bytes)) return rc;
   if (B < 0 || T < 1 || T > 64) return KDA_ERR_INVALID_ARG;
   *a = kda::RecurrentArgs{};
@@ -129,6 +145,10 @@ int prepare_verify(const uint16_t *q, const uint16_t *k, const uint16_t *v, int6
   if (!state_pool || !aligned16(state_pool) || num_slots <= 0 || !slot_ids) return KDA_ERR_INVALID_ARG;
   if (!intermediate_states || !aligned16(intermediate_states)) return KDA_ERR_INVALID_ARG;
   if (int rc = check_norm(norm, H, &a->norm)) return rc;
+  if (int rc = check_conv(conv, &a->conv)) return rc;
+  if (conv && (!conv->window_pool || !aligned16(conv->window_pool) || !conv->step_windows ||
+               !aligned16(conv->step_windows)))
+    return KDA_ERR_INVALID_ARG;
 
   a->q = q; a->k = k; a->v = v; a->g = g; a->beta = beta_logits;
   a->qkv_stride = qkv_token_stride; a->g_stride = g_token_stride;
@@ -206,12 +226,12 @@ int kda_chunk_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v, i
                       float lower_bound, float scale, const int32_t *cu_seqlens_dev,
                       const int32_t *cu_seqlens_host, int num_seqs, int H, float *state_pool,
                       int num_slots, const int32_t *slot_ids, int flags, uint16_t *out,
-                      int64_t out_token_stride, const kda_output_norm *norm, float *final_state,
-                      void *workspace, size_t workspace_bytes, void *stream) {
+                      int64_t out_token_stride, const kda_output_norm *norm, const kda_short_conv *conv,
+                      float *final_state, void *workspace, size_t workspace_bytes, void *stream) {
   kda::ChunkArgs a;
   if (int rc = prepare_prefill(q, k, v, qkv_token_stride, g, g_token_stride, beta_logits, beta_token_stride, A_log,
                                dt_bias, lower_bound, scale, cu_seqlens_dev, cu_seqlens_host, num_seqs, H, state_pool,
-                               num_slots, slot_ids, flags, out, out_token_stride, norm, final_state, workspace,
+                               num_slots, slot_ids, flags, out, out_token_stride, norm, conv, final_state, workspace,
                                workspace_bytes, &a))
     return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -226,12 +246,12 @@ int kda_recurrent_verify(const uint16_t *q, const uint16_t *k, const uint16_t *v
                          int64_t beta_token_stride, const float *A_log, const float *dt_bias,
                          float lower_bound, float scale, int B, int T, int H, const float *state_pool,
                          int num_slots, const int32_t *slot_ids, uint16_t *out, int64_t out_token_stride,
-                         const kda_output_norm *norm, float *intermediate_states, void *workspace,
-                         size_t workspace_bytes, void *stream) {
+                         const kda_output_norm *norm, const kda_short_conv *conv, float *intermediate_states,
+                         void *workspace, size_t workspace_bytes, void *stream) {
   kda::RecurrentArgs a;
   if (int rc = prepare_verify(q, k, v, qkv_token_stride, g, g_token_stride, beta_logits, beta_token_stride, A_log,
                               dt_bias, lower_bound, scale, B, T, H, state_pool, num_slots, slot_ids, out,
-                              out_token_stride, norm, intermediate_states, workspace, workspace_bytes, &a))
+                              out_token_stride, norm, conv, intermediate_states, workspace, workspace_bytes, &a))
     return rc;
   cudaError_t err = kda::launch_recurrent(a, B, static_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
@@ -243,8 +263,8 @@ int kda_spec_step(const kda_token_tensors *prefill, const int32_t *cu_seqlens_de
                   float *intermediate_states, const float *A_log, const float *dt_bias, float lower_bound,
                   float scale, int H, float *state_pool, int num_slots, uint16_t *core_attn_out,
                   int64_t out_token_stride, int64_t num_out_tokens, const kda_output_norm *norm,
-                  const int32_t *non_spec_token_indx, const int32_t *spec_token_indx, void *workspace,
-                  size_t workspace_bytes, void *stream) {
+                  const kda_short_conv *conv, const int32_t *non_spec_token_indx, const int32_t *spec_token_indx,
+                  void *workspace, size_t workspace_bytes, void *stream) {
   if (num_seqs < 0 || B < 0 || num_out_tokens < 0 || (num_seqs > 0 && !prefill) || (B > 0 && !spec))
     return KDA_ERR_INVALID_ARG;
   if (int rc = check_workspace(workspace, workspace_bytes)) return rc;
@@ -255,15 +275,16 @@ int kda_spec_step(const kda_token_tensors *prefill, const int32_t *cu_seqlens_de
     if (int rc = prepare_prefill(p.q, p.k, p.v, p.qkv_token_stride, p.g, p.g_token_stride, p.beta_logits,
                                  p.beta_token_stride, A_log, dt_bias, lower_bound, scale, cu_seqlens_dev,
                                  cu_seqlens_host, num_seqs, H, state_pool, num_slots, prefill_slot_ids, flags,
-                                 core_attn_out, out_token_stride, norm, final_state, workspace, workspace_bytes, &pa))
+                                 core_attn_out, out_token_stride, norm, conv, final_state, workspace, workspace_bytes,
+                                 &pa))
       return rc;
   }
   if (B > 0) {
     const kda_token_tensors &s = *spec;
     if (int rc = prepare_verify(s.q, s.k, s.v, s.qkv_token_stride, s.g, s.g_token_stride, s.beta_logits,
                                 s.beta_token_stride, A_log, dt_bias, lower_bound, scale, B, T, H, state_pool,
-                                num_slots, spec_slot_ids, core_attn_out, out_token_stride, norm, intermediate_states,
-                                workspace, workspace_bytes, &va))
+                                num_slots, spec_slot_ids, core_attn_out, out_token_stride, norm, conv,
+                                intermediate_states, workspace, workspace_bytes, &va))
       return rc;
   }
   const bool has_prefill = pa.num_seqs > 0 && pa.total_tokens > 0, has_spec = B > 0;
@@ -288,8 +309,8 @@ int kda_spec_step(const kda_token_tensors *prefill, const int32_t *cu_seqlens_de
 }
 
 int kda_commit_accepted(float *state_pool, int num_slots, const int32_t *slot_ids, const int32_t *num_accepted,
-                        const float *intermediate_states, int B, int T, int H, void *workspace,
-                        size_t workspace_bytes, void *stream) {
+                        const float *intermediate_states, const kda_short_conv *conv, int B, int T, int H,
+                        void *workspace, size_t workspace_bytes, void *stream) {
   if (int rc = check_workspace(workspace, workspace_bytes)) return rc;
   if (B < 0 || T < 1 || T > 64 || H <= 0 || H > 4096) return KDA_ERR_INVALID_ARG;
   if (B == 0) return KDA_OK;
@@ -301,6 +322,12 @@ int kda_commit_accepted(float *state_pool, int num_slots, const int32_t *slot_id
   a.slot_ids = slot_ids;
   a.num_accepted = num_accepted;
   a.inter = intermediate_states;
+  if (conv) {
+    if (!conv->window_pool || !aligned16(conv->window_pool) || !conv->step_windows || !aligned16(conv->step_windows))
+      return KDA_ERR_INVALID_ARG;
+    a.step_windows = conv->step_windows;
+    a.window_pool = conv->window_pool;
+  }
   a.B = B;
   a.T = T;
   a.H = H;

@@ -27,6 +27,16 @@ __global__ void __launch_bounds__(kThreads) commit_kernel(CommitArgs p) {
     if (threadIdx.x == 0) atomicOr(p.status, (n < 0 || n > p.T) ? KDA_DEVICE_BAD_COUNT : KDA_DEVICE_BAD_SLOT);
     return;
   }
+  if (p.step_windows) {   // the conv window after token n-1: 3 tensors x 3 rows x 128 channels of this head
+    constexpr int kRows = 3 * (kConvW - 1), kVec = kRows * kD / 8;   // 16-byte pieces
+    for (int i = threadIdx.x; i < kVec; i += kThreads) {
+      const int row = i / (kD / 8), piece = i % (kD / 8);   // row = tensor * 3 + window row
+      const uint4 *wsrc = reinterpret_cast<const uint4 *>(
+          p.step_windows + ((((size_t)b * p.T + (n - 1)) * kRows + row) * p.H + h) * kD) + piece;
+      uint4 *wdst = reinterpret_cast<uint4 *>(p.window_pool + (((size_t)slot * kRows + row) * p.H + h) * kD) + piece;
+      *wdst = *wsrc;
+    }
+  }
   const float4 *src = reinterpret_cast<const float4 *>(p.inter + (((size_t)b * p.T + (n - 1)) * p.H + h) * kD * kD);
   float4 *dst = reinterpret_cast<float4 *>(p.pool + ((size_t)slot * p.H + h) * kD * kD);
   constexpr int kVec = kD * kD / 4;   // 4096 float4

@@ -18,6 +18,16 @@ struct OutNorm {
   float *rstd;            // [rows, H], or null
 };
 
+// Short causal convolutions of q, k, v (weight == nullptr: none).  Width 4.
+constexpr int kConvW = 4;
+struct ShortConv {
+  const float *weight;        // [3, H, 128, 4]
+  int silu;
+  uint16_t *window_pool;      // [slots, 3, 3, H, 128] bf16
+  uint16_t *window_dense;     // prefill: [num_seqs, 3, 3, H, 128], or null
+  uint16_t *step_windows;     // verify: [B, T, 3, 3, H, 128]
+};
+
 // Arguments of the token-by-token kernel (verify).
 struct RecurrentArgs {
   const uint16_t *q, *k, *v, *g, *beta;
@@ -39,6 +49,7 @@ struct RecurrentArgs {
   const int32_t *out_index;  // output row of each token, or null (row = token)
   int64_t num_out_rows;      // rows of out (bounds out_index)
   OutNorm norm;
+  ShortConv conv;
   uint32_t *status;
   // non-null: the grid is launched as a programmatic dependent of the preceding grid; a zeroed counter in the
   // workspace (kDoneCounterOffset) through which the CTA that finishes last waits for that grid
@@ -78,6 +89,8 @@ struct CommitArgs {
   const int32_t *slot_ids;
   const int32_t *num_accepted;
   const float *inter;   // [B, T, H, D, D]
+  const uint16_t *step_windows;   // [B, T, 3, 3, H, 128] conv windows, or null
+  uint16_t *window_pool;          // [slots, 3, 3, H, 128]
   int B, T, H;
   uint32_t *status;
 };

@@ -61,5 +61,6 @@ extern "C" int kda_recurrent_verify_noalloc(const uint16_t *q, const uint16_t *k
   if (cudaMemsetAsync(scratch, 0, need, static_cast<cudaStream_t>(stream)) != cudaSuccess) return KDA_ERR_CUDA;
   return kda_recurrent_verify(q, k, v, qkv_token_stride, g, g_token_stride, beta_logits, beta_token_stride, A_log,
                               dt_bias, lower_bound, scale, B, T, H, state_pool, num_slots, slot_ids, out,
-                              out_token_stride, nullptr, intermediate_states, scratch, kNoAllocScratchBytes, stream);
+                              out_token_stride, nullptr, nullptr, intermediate_states, scratch, kNoAllocScratchBytes,
+                              stream);
 }

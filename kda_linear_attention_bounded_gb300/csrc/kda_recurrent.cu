@@ -30,7 +30,9 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kTile = kWarps;      // tokens prepared per prologue pass (one per warp)
 constexpr int kRows = kD / kWarps;  // key channels per warp (16)
 
-// One (request, head) work item.  Every return is taken by the whole CTA.
+// One (request, head) work item.  Every return is taken by the whole CTA.  The optional short convolutions
+// and output norm are compile-time switches, so the plain call carries none of their code.
+template <bool kConv, bool kNorm>
 __device__ __forceinline__ void recurrent_item(const RecurrentArgs &p) {
   __shared__ __align__(16) float s_khat[kTile][kD];
   __shared__ __align__(16) float s_kalpha[kTile][kD];
@@ -93,26 +95,68 @@ __device__ __forceinline__ void recurrent_item(const RecurrentArgs &p) {
         row = p.out_index[t];
         if (row < 0 || row >= p.num_out_rows) row = -1;
       }
-      if (p.norm.gate) {
+      if (kNorm) {
         uint2 zr = make_uint2(0u, 0u);
         if (row >= 0) zr = *reinterpret_cast<const uint2 *>(p.norm.gate + row * p.norm.gate_stride + h * kD + col0);
         const float2 z01 = unpack_bf16x2(zr.x), z23 = unpack_bf16x2(zr.y);
         *reinterpret_cast<float4 *>(&s_gz[warp][col0]) =
             make_float4(sigmoid_f(z01.x), sigmoid_f(z01.y), sigmoid_f(z23.x), sigmoid_f(z23.y));
       }
-      const uint2 qr = *reinterpret_cast<const uint2 *>(p.q + (size_t)t * p.qkv_stride + h * kD + col0);
-      const uint2 kr = *reinterpret_cast<const uint2 *>(p.k + (size_t)t * p.qkv_stride + h * kD + col0);
-      const uint2 vr = *reinterpret_cast<const uint2 *>(p.v + (size_t)t * p.qkv_stride + h * kD + col0);
       const uint2 gr = *reinterpret_cast<const uint2 *>(p.g + (size_t)t * p.g_stride + h * kD + col0);
-      const uint16_t *qs = reinterpret_cast<const uint16_t *>(&qr);
-      const uint16_t *ks = reinterpret_cast<const uint16_t *>(&kr);
-      const uint16_t *vs = reinterpret_cast<const uint16_t *>(&vr);
       const uint16_t *gs = reinterpret_cast<const uint16_t *>(&gr);
-      float qf[4], kf[4], qq = 0.f, kk = 0.f;
+      float qf[4], kf[4], vf[4], qq = 0.f, kk = 0.f;
+      if (!kConv) {
+        const uint2 qr = *reinterpret_cast<const uint2 *>(p.q + (size_t)t * p.qkv_stride + h * kD + col0);
+        const uint2 kr = *reinterpret_cast<const uint2 *>(p.k + (size_t)t * p.qkv_stride + h * kD + col0);
+        const uint2 vr = *reinterpret_cast<const uint2 *>(p.v + (size_t)t * p.qkv_stride + h * kD + col0);
+        const float2 q01 = unpack_bf16x2(qr.x), q23 = unpack_bf16x2(qr.y);
+        const float2 k01 = unpack_bf16x2(kr.x), k23 = unpack_bf16x2(kr.y);
+        const float2 v01 = unpack_bf16x2(vr.x), v23 = unpack_bf16x2(vr.y);
+        qf[0] = q01.x; qf[1] = q01.y; qf[2] = q23.x; qf[3] = q23.y;
+        kf[0] = k01.x; kf[1] = k01.y; kf[2] = k23.x; kf[3] = k23.y;
+        vf[0] = v01.x; vf[1] = v01.y; vf[2] = v23.x; vf[3] = v23.y;
+      } else {
+        // short causal convolutions of q, k, v over this lane's 4 channels: the raw inputs 3, 2, 1 and 0
+        // tokens back (the request's own tokens, else its slot's window, oldest row first); the window
+        // after this token (the inputs 2, 1, 0 back) is recorded for the commit
+        const int r = t - t_begin;
+        const uint16_t *base[3] = {p.q, p.k, p.v};
+        float *dst[3] = {qf, kf, vf};
+#pragma unroll
+        for (int m = 0; m < 3; ++m) {
+          uint2 xr[kConvW];
+#pragma unroll
+          for (int j = 0; j < kConvW; ++j) {
+            const int back = kConvW - 1 - j;
+            xr[j] = r - back >= 0
+                        ? *reinterpret_cast<const uint2 *>(base[m] + (size_t)(t - back) * p.qkv_stride + h * kD + col0)
+                        : *reinterpret_cast<const uint2 *>(
+                              p.conv.window_pool +
+                              ((((size_t)slot * 3 + m) * (kConvW - 1) + (kConvW - 1 + r - back)) * p.H + h) * kD + col0);
+          }
+          if (p.conv.step_windows) {
+#pragma unroll
+            for (int j = 0; j < kConvW - 1; ++j)
+              *reinterpret_cast<uint2 *>(
+                  p.conv.step_windows +
+                  (((((size_t)n * p.T + r) * 3 + m) * (kConvW - 1) + j) * p.H + h) * kD + col0) = xr[j + 1];
+          }
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float4 w = *reinterpret_cast<const float4 *>(p.conv.weight + (((size_t)m * p.H + h) * kD + col0 + e) * kConvW);
+            const float wt[kConvW] = {w.x, w.y, w.z, w.w};
+            float acc = 0.f;
+#pragma unroll
+            for (int j = 0; j < kConvW; ++j) {
+              const float2 x2 = unpack_bf16x2(e < 2 ? xr[j].x : xr[j].y);
+              acc = fmaf(wt[j], (e & 1) ? x2.y : x2.x, acc);
+            }
+            dst[m][e] = p.conv.silu ? acc * sigmoid_f(acc) : acc;
+          }
+        }
+      }
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        qf[j] = bf16_bits_to_f32(qs[j]);
-        kf[j] = bf16_bits_to_f32(ks[j]);
         qq += qf[j] * qf[j];
         kk += kf[j] * kf[j];
       }
@@ -130,7 +174,7 @@ __device__ __forceinline__ void recurrent_item(const RecurrentArgs &p) {
         s_kalpha[warp][col0 + j] = alpha * kh;
         s_qalpha[warp][col0 + j] = alpha * qh;
         s_alpha[warp][col0 + j] = alpha;
-        s_v[warp][col0 + j] = bf16_bits_to_f32(vs[j]);
+        s_v[warp][col0 + j] = vf[j];
       }
       kq = warp_sum(kq);
       if (lane == 0) {
@@ -169,7 +213,7 @@ __device__ __forceinline__ void recurrent_item(const RecurrentArgs &p) {
         s_u[tid] = u;
         float o = p.scale * (wq + s_kq[s] * u);
         const int64_t row = s_row[s];
-        if (p.norm.gate) {   // gated RMSNorm over the 128 channels (warps 0..3)
+        if (kNorm) {   // gated RMSNorm over the 128 channels (warps 0..3)
           const float sq = warp_sum(o * o);
           if (lane == 0) s_sq[warp] = sq;
           named_bar_sync<1>(kD);
@@ -208,8 +252,9 @@ __device__ __forceinline__ void recurrent_item(const RecurrentArgs &p) {
   }
 }
 
+template <bool kConv, bool kNorm>
 __global__ void __launch_bounds__(kThreads, 2) recurrent_kernel(RecurrentArgs p) {
-  recurrent_item(p);
+  recurrent_item<kConv, kNorm>(p);
   if (p.done_counter) {
     // launched as a programmatic dependent of the grid before it, which it does not read from: the CTA that
     // finishes last waits for that grid's completion, so this grid's completion implies it for whatever the
@@ -224,10 +269,10 @@ __global__ void __launch_bounds__(kThreads, 2) recurrent_kernel(RecurrentArgs p)
 
 }  // namespace
 
-cudaError_t launch_recurrent(const RecurrentArgs &args, int num_items, cudaStream_t stream) {
-  if (num_items <= 0) return cudaSuccess;
+template <bool kConv, bool kNorm>
+cudaError_t launch_variant(const RecurrentArgs &args, int num_items, cudaStream_t stream) {
   if (!args.done_counter) {
-    recurrent_kernel<<<num_items * args.H, kThreads, 0, stream>>>(args);
+    recurrent_kernel<kConv, kNorm><<<num_items * args.H, kThreads, 0, stream>>>(args);
     return cudaGetLastError();
   }
   // programmatic dependent launch: CTAs may be scheduled onto SMs the preceding grid leaves free once every
@@ -241,7 +286,16 @@ cudaError_t launch_recurrent(const RecurrentArgs &args, int num_items, cudaStrea
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, recurrent_kernel, args);
+  return cudaLaunchKernelEx(&cfg, recurrent_kernel<kConv, kNorm>, args);
+}
+
+cudaError_t launch_recurrent(const RecurrentArgs &args, int num_items, cudaStream_t stream) {
+  if (num_items <= 0) return cudaSuccess;
+  const bool conv = args.conv.weight != nullptr, norm = args.norm.gate != nullptr;
+  if (conv) return norm ? launch_variant<true, true>(args, num_items, stream)
+                        : launch_variant<true, false>(args, num_items, stream);
+  return norm ? launch_variant<false, true>(args, num_items, stream)
+              : launch_variant<false, false>(args, num_items, stream);
 }
 
 }  // namespace kda

@@ -184,3 +184,21 @@ def check_norm(y_gpu, rstd_gpu, x_ref, z_bits, ni, what, x_gpu=None):
         if rs is not None:
             rel = float(np.abs(rs / rstd_st - 1.0).max())
             assert rel <= 1e-3, f"{what}: norm stage rstd relative error {rel:.3e} (<= 1e-3)"
+
+
+def device_conv(ci, device="cuda", B=None, T=None, N=None):
+    """A ShortConv on the device from ``inputs.ConvInputs`` (a copy of its window pool), with per-step window
+    records for B x T verify tokens and/or dense final windows for N sequences (0xFFFF-filled: bf16 NaN)."""
+    _, H, d, _ = ci.weight.shape
+    steps = dense = None
+    if B is not None:
+        steps = torch.full((B, T, 3, 3, H, d), -1, dtype=torch.int16, device=device).view(torch.bfloat16)
+    if N is not None:
+        dense = torch.full((N, 3, 3, H, d), -1, dtype=torch.int16, device=device).view(torch.bfloat16)
+    return kda.ShortConv(f32_dev(ci.weight, device), bf16_dev(ci.pool, device), ci.silu, window_dense=dense,
+                         step_windows=steps)
+
+
+def widen_bf16(t):
+    """A bf16 CUDA tensor -> fp64 NumPy (exact)."""
+    return t.float().cpu().numpy().astype(np.float64)

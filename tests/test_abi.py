@@ -63,17 +63,22 @@ P = ctypes.c_void_p
 
 
 def _prefill(lib, *, cu=(0, 4), H=2, lb=-5.0, scale=0.1, ws=FAKE, ws_bytes=256, stride=256, flags=0,
-             q=FAKE, final=FAKE, pool=None, slots=None, nslots=0, norm=None):
+             q=FAKE, final=FAKE, pool=None, slots=None, nslots=0, norm=None, conv=None):
     cu_host = np.array(cu, np.int32)
     return lib.kda_chunk_prefill(P(q), P(FAKE), P(FAKE), stride, P(FAKE), stride, P(FAKE), H, P(FAKE), P(FAKE),
                                  lb, scale, P(FAKE), cu_host.ctypes.data_as(P), len(cu) - 1, H, P(pool), nslots,
-                                 P(slots), flags, P(FAKE), stride, norm, P(final), P(ws), ws_bytes, None)
+                                 P(slots), flags, P(FAKE), stride, norm, conv, P(final), P(ws), ws_bytes, None)
 
 
-def _verify(lib, *, B=2, T=8, H=2, lb=-5.0, ws=FAKE, pool=FAKE, inter=FAKE, norm=None):
+def _verify(lib, *, B=2, T=8, H=2, lb=-5.0, ws=FAKE, pool=FAKE, inter=FAKE, norm=None, conv=None):
     return lib.kda_recurrent_verify(P(FAKE), P(FAKE), P(FAKE), H * 128, P(FAKE), H * 128, P(FAKE), H, P(FAKE),
-                                    P(FAKE), lb, 0.1, B, T, H, P(pool), 4, P(FAKE), P(FAKE), H * 128, norm, P(inter),
-                                    P(ws), 256, None)
+                                    P(FAKE), lb, 0.1, B, T, H, P(pool), 4, P(FAKE), P(FAKE), H * 128, norm, conv,
+                                    P(inter), P(ws), 256, None)
+
+
+def _conv(weight=FAKE, act=1, pool=FAKE, dense=None, steps=FAKE):
+    from kda_linear_attention_bounded_gb300._binding import _ShortConvC
+    return ctypes.byref(_ShortConvC(weight, act, pool, dense, steps))
 
 
 def _norm(gate=FAKE, stride=256, weight=FAKE, eps=1e-6, rstd=None):
@@ -129,7 +134,7 @@ def test_verify_rejects_bad_arguments(lib):
 
 
 def _spec_step(lib, *, cu=(0, 4), B=2, T=8, H=2, pre=True, spec=True, pre_stride=256, spec_stride=256,
-               ns_idx=FAKE, s_idx=FAKE, n_out=100, ws_bytes=None, lb=-5.0, norm=None):
+               ns_idx=FAKE, s_idx=FAKE, n_out=100, ws_bytes=None, lb=-5.0, norm=None, conv=None):
     from kda_linear_attention_bounded_gb300._binding import TokenTensors
     cu_host = np.array(cu, np.int32)
     ws_bytes = lib.kda_prefill_workspace_size(int(cu[-1]), len(cu) - 1, H) if ws_bytes is None else ws_bytes
@@ -137,8 +142,8 @@ def _spec_step(lib, *, cu=(0, 4), B=2, T=8, H=2, pre=True, spec=True, pre_stride
     ts = TokenTensors(FAKE, FAKE, FAKE, spec_stride, FAKE, spec_stride, FAKE, H)
     return lib.kda_spec_step(ctypes.byref(tp) if pre else None, P(FAKE), cu_host.ctypes.data_as(P), len(cu) - 1,
                              None, 0, P(FAKE), ctypes.byref(ts) if spec else None, B, T, P(FAKE), P(FAKE), P(FAKE),
-                             P(FAKE), lb, 0.1, H, P(FAKE), 4, P(FAKE), H * 128, n_out, norm, P(ns_idx), P(s_idx),
-                             P(FAKE), ws_bytes, None)
+                             P(FAKE), lb, 0.1, H, P(FAKE), 4, P(FAKE), H * 128, n_out, norm, conv, P(ns_idx),
+                             P(s_idx), P(FAKE), ws_bytes, None)
 
 
 def test_spec_step_rejects_bad_arguments(lib):
@@ -177,7 +182,8 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
 
 def test_commit_rejects_bad_arguments(lib):
     c = lambda **kw: lib.kda_commit_accepted(P(kw.get("pool", FAKE)), 4, P(FAKE), P(FAKE), P(kw.get("inter", FAKE)),
-                                             kw.get("B", 2), kw.get("T", 8), 2, P(kw.get("ws", FAKE)), 256, None)
+                                             kw.get("conv"), kw.get("B", 2), kw.get("T", 8), 2, P(kw.get("ws", FAKE)),
+                                             256, None)
     assert c(ws=None) == 3
     assert c(pool=None) == 1
     assert c(pool=FAKE + 4) == 1
@@ -185,3 +191,12 @@ def test_commit_rejects_bad_arguments(lib):
     assert c(T=0) == 1
     assert c(T=65) == 1
     assert c(B=0) == 0
+    assert c(conv=_conv(pool=None)) == 1
+    assert c(conv=_conv(steps=FAKE + 8)) == 1
+
+
+def test_short_conv_is_checked_on_the_host(lib):
+    for bad in (_conv(weight=None), _conv(weight=FAKE + 4), _conv(act=2), _conv(pool=None), _conv(steps=None),
+                _conv(pool=FAKE + 2)):
+        assert _verify(lib, conv=bad) == 1
+        assert _spec_step(lib, conv=bad, cu=(0,), pre=False) == 1

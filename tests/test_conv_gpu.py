@@ -1,0 +1,118 @@
+"""Parity of the short causal convolutions of q, k, v (CUDA, through the C ABI) with the fp64 oracle: verify
+from the slots' windows with per-step window records, the commit of the accepted window, and the spec step."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from kda_linear_attention_bounded_gb300 import inputs
+import kda_linear_attention_bounded_gb300 as kda
+from gpu_helpers import DeviceVerify, check_out, check_state, device_conv, i32_dev, widen_bf16
+
+pytestmark = pytest.mark.gpu
+
+
+def _verify_with_conv(inp, heads=None):
+    dev = DeviceVerify(inp)
+    conv = device_conv(inp.conv, B=inp.B, T=inp.T)
+    pool_before = conv.window_pool.clone()
+    ws = kda.make_workspace()
+    out, inter = dev.run(workspace=ws, conv=conv)
+    torch.cuda.synchronize()
+    assert kda.read_device_status(ws) == 0
+    assert torch.equal(conv.window_pool, pool_before), "verify must not write the window pool"
+    ref_out, ref_steps, ref_win = oracle.run_verify(inp, heads=heads)
+    hb, he = heads if heads else (0, inp.H)
+    check_out(out[:, hb:he], ref_out[:, hb:he], f"{inp.name} outputs with the convolutions")
+    check_state(inter[:, :, hb:he], ref_steps[:, :, hb:he], f"{inp.name} per-step states with the convolutions")
+    got = widen_bf16(conv.step_windows)
+    assert np.array_equal(got[..., hb:he, :], ref_win[..., hb:he, :]), "per-step windows differ from the oracle's"
+    return dev, conv, inter, ws
+
+
+@pytest.mark.parametrize("T,silu", [(1, True), (3, True), (8, True), (5, False)])
+def test_verify_with_short_conv_small(T, silu):
+    inp = inputs.verify_inputs("conv_small", 3, T, 2, seed=600 + T, pool_slots=5)
+    inp.conv = inputs.conv_inputs(2, 5, seed=610 + T, silu=silu)
+    _verify_with_conv(inp)
+
+
+def test_verify_with_short_conv_64x4_h16_full():
+    inp = inputs.verify_64x4()
+    inp.conv = inputs.conv_inputs(16, 256, seed=620)
+    _verify_with_conv(inp, heads=(0, 8))
+
+
+def test_commit_with_short_conv():
+    inp = inputs.verify_inputs("conv_commit", 5, 4, 2, seed=630, pool_slots=7)
+    inp.conv = inputs.conv_inputs(2, 7, seed=631)
+    dev, conv, inter, ws = _verify_with_conv(inp)
+    n_acc = np.array([0, 1, 4, 2, 3], np.int32)
+    pool_before, win_before = dev.pool.clone(), conv.window_pool.clone()
+    kda.commit_accepted(dev.pool, dev.slots, i32_dev(n_acc), inter, conv=conv, workspace=ws)
+    torch.cuda.synchronize()
+    assert kda.read_device_status(ws) == 0
+    for b, n in enumerate(n_acc):
+        s = int(inp.slot_ids[b])
+        if n == 0:
+            assert torch.equal(conv.window_pool[s], win_before[s]) and torch.equal(dev.pool[s], pool_before[s])
+        else:
+            assert torch.equal(conv.window_pool[s], conv.step_windows[b, n - 1]), f"request {b}: window not committed"
+            assert torch.equal(dev.pool[s], inter[b, n - 1])
+    others = np.setdiff1d(np.arange(7), inp.slot_ids)
+    idx = torch.from_numpy(others).long().cuda()
+    assert torch.equal(conv.window_pool[idx], win_before[idx])
+
+
+def test_verify_then_commit_then_verify_continues_the_sequence():
+    # two verify steps with the accepted window and state committed between them equal one run over the
+    # accepted tokens followed by the next block: the window carries the convolution across the steps
+    H, T = 2, 4
+    first = inputs.verify_inputs("conv_chain", 2, T, H, seed=640, pool_slots=3)
+    first.conv = inputs.conv_inputs(H, 3, seed=641)
+    dev, conv, inter, ws = _verify_with_conv(first)
+    n_acc = np.array([2, 4], np.int32)
+    kda.commit_accepted(dev.pool, dev.slots, i32_dev(n_acc), inter, conv=conv, workspace=ws)
+    second = inputs.verify_inputs("conv_chain2", 2, T, H, seed=642, pool_slots=3)
+    second.slot_ids = first.slot_ids
+    second.A_log, second.dt_bias = first.A_log, first.dt_bias
+    dev2 = DeviceVerify(second)
+    conv2 = kda.ShortConv(conv.weight, conv.window_pool, conv.silu,
+                          step_windows=torch.empty_like(conv.step_windows))
+    out2, _ = kda.recurrent_verify(dev2.q, dev2.k, dev2.v, dev2.g, dev2.beta, dev.A_log, dev.dt_bias, dev.pool,
+                                   dev.slots, T, lower_bound=second.lower_bound, scale=second.scale, conv=conv2,
+                                   workspace=ws)
+    torch.cuda.synchronize()
+    assert kda.read_device_status(ws) == 0
+    # the oracle: per request, the accepted tokens of the first block then the second block, in one run
+    for b in range(2):
+        n = int(n_acc[b])
+        rows1 = slice(b * T, b * T + n)
+        rows2 = slice(b * T, b * T + T)
+        cat = lambda a1, a2: np.concatenate([a1[rows1], a2[rows2]])
+        s = int(first.slot_ids[b])
+        ref, _, _, _, _ = oracle.run_conv(
+            cat(first.q, second.q), cat(first.k, second.k), cat(first.v, second.v), cat(first.g, second.g),
+            cat(first.beta, second.beta), first.A_log, first.dt_bias, first.lower_bound, first.scale,
+            np.array([0, n + T], np.int32), first.conv.weight, first.conv.silu,
+            win0=oracle.bf16_widen(first.conv.pool[s:s + 1]), S0=first.pool[s:s + 1])
+        check_out(out2[b * T:(b + 1) * T], ref[n:], f"request {b}: second block after committing {n} tokens")
+
+
+def test_spec_step_verify_segment_with_short_conv():
+    inp = inputs.verify_inputs("conv_step", 4, 3, 2, seed=650, pool_slots=6)
+    inp.conv = inputs.conv_inputs(2, 6, seed=651)
+    dev = DeviceVerify(inp)
+    conv = device_conv(inp.conv, B=inp.B, T=inp.T)
+    rows = np.random.default_rng(652).permutation(inp.B * inp.T + 3)[:inp.B * inp.T].astype(np.int32)
+    out = torch.zeros((inp.B * inp.T + 3, 2, 128), dtype=torch.bfloat16, device="cuda")
+    ws = kda.make_workspace()
+    out, _, inter = kda.spec_step(None, None, None, (dev.q, dev.k, dev.v, dev.g, dev.beta), inp.T, dev.A_log,
+                                  dev.dt_bias, dev.pool, out, None, i32_dev(rows), spec_slot_ids=dev.slots,
+                                  lower_bound=inp.lower_bound, scale=inp.scale, conv=conv, workspace=ws)
+    torch.cuda.synchronize()
+    assert kda.read_device_status(ws) == 0
+    ref_out, ref_steps, ref_win = oracle.run_verify(inp)
+    check_out(out[torch.from_numpy(rows).long().cuda()], ref_out, "spec step verify rows with the convolutions")
+    check_state(inter, ref_steps, "spec step per-step states with the convolutions")
+    assert np.array_equal(widen_bf16(conv.step_windows), ref_win)
