@@ -107,7 +107,10 @@ int prepare_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v, int
   if (!(flags & KDA_FINAL_TO_POOL) && (!final_state || !aligned16(final_state))) return KDA_ERR_INVALID_ARG;
   if (workspace_bytes < kda::prefill_workspace_bytes(cu_seqlens_host[num_seqs], num_seqs, H)) return KDA_ERR_WORKSPACE;
   if (int rc = check_norm(norm, H, &a->norm)) return rc;
-  if (conv) return KDA_ERR_UNSUPPORTED;   // the prefill's convolutions are not built yet
+  if (int rc = check_conv(conv, &a->conv)) return rc;
+  if (conv && ((use_pool && (!conv->window_pool || !aligned16(conv->window_pool))) ||
+               (!(flags & KDA_FINAL_TO_POOL) && (!conv->window_dense || !aligned16(conv->window_dense)))))
+    return KDA_ERR_INVALID_ARG;
 
   a->q = q; a->k = k; a->v = v; a->g = g; a->beta = beta_logits;
   a->qkv_stride = qkv_token_stride; a->g_stride = g_token_stride;

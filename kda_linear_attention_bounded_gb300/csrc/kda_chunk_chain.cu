@@ -108,8 +108,37 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_chain_kernel(const __grid_c
   const int d = quad * 32 + lane;
   const float *src = prm.state_in ? prm.state_in + (static_cast<size_t>(slot) * H + h) * kD * kD : nullptr;
 
+  // The sequence's final short-convolution window (with conv): the last 3 raw inputs of q, k and v, rows of the
+  // initial window (the slot's, else zeros) where the sequence has fewer than 3 tokens.  Every piece is read
+  // before any is written (`sync` between), since the initial and final windows may be the same pool slot; the
+  // intra-chunk grid, which reads initial windows, has completed when this runs.
+  auto write_window = [&](auto sync) {
+    constexpr int kRows = 3 * (kConvW - 1), kPieces = kRows * kD / 8;   // 144 pieces of 16 bytes
+    const int row = tid / 16, cc = tid % 16, m = row / (kConvW - 1), j = row % (kConvW - 1);
+    uint4 val = make_uint4(0u, 0u, 0u, 0u);
+    if (tid < kPieces) {
+      if (len + j < kConvW - 1) {
+        if (prm.conv_load_initial)
+          val = *reinterpret_cast<const uint4 *>(
+              prm.conv.window_pool + ((static_cast<size_t>(slot) * kRows + m * (kConvW - 1) + len + j) * H + h) * kD + 8 * cc);
+      } else {
+        const uint16_t *x = m == 0 ? prm.xq : m == 1 ? prm.xk : prm.xv;
+        val = *reinterpret_cast<const uint4 *>(x + static_cast<int64_t>(t0 + len + j - (kConvW - 1)) * prm.qkv_stride +
+                                               h * kD + 8 * cc);
+      }
+    }
+    sync();
+    if (tid < kPieces) {
+      uint16_t *w = prm.state_out_pool
+                        ? prm.conv.window_pool + ((static_cast<size_t>(slot) * kRows + row) * H + h) * kD
+                        : prm.conv.window_dense + ((static_cast<size_t>(n) * kRows + row) * H + h) * kD;
+      *reinterpret_cast<uint4 *>(w + 8 * cc) = val;
+    }
+  };
+
   if (nchunks == 0) {   // empty sequence: the final state is the initial one
     if (!worker) return;
+    if (prm.conv.weight) write_window([] { named_bar_sync<1>(256); });
 #pragma unroll 8
     for (int i = 0; i < 64; ++i) {
       const int kd = kd_of_rho(64 * hv + i);
@@ -372,6 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_chain_kernel(const __grid_c
       for (int i = 0; i < 32; ++i) dst[static_cast<size_t>(kd_of_rho(col + i)) * kD + d] = __uint_as_float(sv[i]);
     }
   }
+  if (prm.conv.weight) write_window([] { __syncthreads(); });
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {

@@ -72,7 +72,9 @@ constexpr uint32_t OFF_T = 74752;     // T bf16 K-major [t][t'] (8 KB), written 
 constexpr uint32_t OFF_WST = 40960, OFF_UST = 57344;   // W^T and U^^T rows of the block
 constexpr uint32_t OFF_SMALL = 99328;
 constexpr uint32_t SM_NQ = 0, SM_NK = 256, SM_BETA = 512, SM_H = 768 /* [8 quarters][128] f32 */,
-                   SM_BAR = 4864, SM_TMEM = 4888, SM_ABORT = 4892, SM_BARU = 4896, SM_END = 4928;
+                   SM_BAR = 4864, SM_TMEM = 4888, SM_ABORT = 4892, SM_BARU = 4896,
+                   SM_HALO = 4928 /* short convolutions: [3 tensors][3 rows][64 channel pairs] u32 */,
+                   SM_VW = 7232 /* v's taps [128 channels][4] f32 */, SM_END = 9280;
 constexpr int kCopyThread = 128;      // issues the block's early bulk stores (Q+, [P ; K']) and U^^T's
 constexpr uint32_t kSmemBytes = OFF_SMALL + SM_END + 1024;   // + alignment slack
 static_assert(2 * (kSmemBytes + 1024) <= 233472, "two CTAs per SM");
@@ -204,7 +206,36 @@ __device__ __forceinline__ void build_rows(const uint32_t (&kqw)[16], const floa
   }
 }
 
-template <int BLK>
+// SiLU through tanh: x sigmoid(x) = x/2 (1 + tanh(x/2))
+__device__ __forceinline__ float silu_tanh(float x) {
+  float t;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(0.5f * x));
+  return 0.5f * x * (1.0f + t);
+}
+
+// Short causal convolution down one channel pair of a bf16 tile, in place: rows r0 .. r0+n-1 at byte offsets
+// off(r) from `tile`, the raw inputs of rows r0-3 .. r0-1 in x0 .. x2 (oldest first), taps wa / wb of the two
+// channels (tap 3 on the current row).  Rows at or past `valid` become 0.
+template <typename Off>
+__device__ __forceinline__ void conv_pair(uint8_t *tile, Off off, int r0, int n, int valid, float2 x0, float2 x1,
+                                          float2 x2, float4 wa, float4 wb, bool silu) {
+  for (int r = r0; r < r0 + n; ++r) {
+    uint32_t *p = reinterpret_cast<uint32_t *>(tile + off(r));
+    const float2 x = unpack_bf16x2(*p);
+    float y0 = fmaf(wa.w, x.x, fmaf(wa.z, x2.x, fmaf(wa.y, x1.x, wa.x * x0.x)));
+    float y1 = fmaf(wb.w, x.y, fmaf(wb.z, x2.y, fmaf(wb.y, x1.y, wb.x * x0.y)));
+    if (silu) {
+      y0 = silu_tanh(y0);
+      y1 = silu_tanh(y1);
+    }
+    *p = r < valid ? pack_bf16x2(y0, y1) : 0u;
+    x0 = x1;
+    x1 = x2;
+    x2 = x;
+  }
+}
+
+template <int BLK, bool kConv>
 __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_constant__ IntraParams prm) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -228,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_c
   const int h = blockIdx.x % H;
   const int gslot = blockIdx.x / H;
   // the chunk slot's first token and its tokens (a broadcast load each)
-  const int tok0 = prm.slot_tok0[gslot], valid = prm.slot_valid[gslot];
+  const int tok0 = prm.slot_tok0[gslot], valid = prm.slot_valid[gslot] & (kSlotFirst - 1);
   uint8_t *blk = prm.blocks + (static_cast<size_t>(gslot) * H + h) * kBlkBytes;
 
   // ------------------------------------------------------------ setup: barriers, TMA of q, k, g, TMEM, beta
@@ -251,6 +282,32 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_c
     tmem_alloc(s_tmem, kTmemCols);
     tmem_relinquish();
   }
+  // short convolutions: the 3 raw inputs before the chunk for q, k, v (the previous tokens of the sequence,
+  // else the slot's window for its first chunk, else zeros) and v's taps go to shared memory; this thread's
+  // q or k taps to registers (thread = tensor tid / 128, channel pair tid % 64, half of the rows)
+  uint32_t *s_halo = reinterpret_cast<uint32_t *>(small + SM_HALO);
+  float4 cwa = make_float4(0.f, 0.f, 0.f, 0.f), cwb = cwa;
+  if (kConv) {
+    const bool first = prm.slot_valid[gslot] & kSlotFirst;
+    const int slot = first && prm.conv_load_initial ? prm.slot_ids[prm.seq0 + prm.slot_seq[gslot]] : -1;
+    for (int i = tid; i < 3 * 3 * 64; i += kThreads) {
+      const int m = i / 192, j = (i / 64) % 3, w = i % 64;
+      uint32_t x = 0u;
+      if (!first) {
+        const uint16_t *src = m == 0 ? prm.xq : m == 1 ? prm.xk : prm.xv;
+        x = *reinterpret_cast<const uint32_t *>(src + static_cast<int64_t>(tok0 - 3 + j) * prm.qkv_stride + h * kD + 2 * w);
+      } else if (slot >= 0) {
+        x = *reinterpret_cast<const uint32_t *>(prm.conv.window_pool +
+                                                ((static_cast<size_t>(slot) * 9 + m * 3 + j) * H + h) * kD + 2 * w);
+      }
+      s_halo[i] = x;
+    }
+    float4 *s_vw = reinterpret_cast<float4 *>(small + SM_VW);
+    if (tid < kD) s_vw[tid] = *reinterpret_cast<const float4 *>(prm.conv.weight + ((2 * static_cast<size_t>(H) + h) * kD + tid) * 4);
+    const int cm = tid >> 7, c = 2 * (tid & 63);
+    cwa = *reinterpret_cast<const float4 *>(prm.conv.weight + ((static_cast<size_t>(cm) * H + h) * kD + c) * 4);
+    cwb = *reinterpret_cast<const float4 *>(prm.conv.weight + ((static_cast<size_t>(cm) * H + h) * kD + c + 1) * 4);
+  }
   // per-thread parameters, consumed after the wait for q, k, g (their latency hides under it)
   const int p = tid & 63, sel = tid >> 6;
   const int c0 = 2 * p;
@@ -264,6 +321,24 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_c
   // ------------------------------------------------------------ wait for q, k, g
   wait_or_abort(bar_in, 0, s_abort, prm.status);
   if (tid < kC) s_beta[tid] = tid < valid ? sigmoid_f(bf16_bits_to_f32(beta_raw)) : 0.f;
+
+  // ------------------------------------------------------------ short convolutions of q and k, in place
+  if (kConv) {
+    const int cm = tid >> 7, cp = tid & 63, half = (tid >> 6) & 1;
+    uint8_t *tile = sm + (cm == 0 ? OFF_QIN : OFF_KIN);
+    const int c = 2 * cp;
+    auto off = [c](int r) { return in_offset(r, c); };
+    uint32_t h0, h1, h2;
+    if (half == 0) {
+      h0 = s_halo[cm * 192 + cp]; h1 = s_halo[cm * 192 + 64 + cp]; h2 = s_halo[cm * 192 + 128 + cp];
+    } else {   // rows 29 .. 31, read before the first half overwrites them
+      h0 = ld_u32(tile + off(29)); h1 = ld_u32(tile + off(30)); h2 = ld_u32(tile + off(31));
+    }
+    __syncthreads();
+    conv_pair(tile, off, 32 * half, 32, valid, unpack_bf16x2(h0), unpack_bf16x2(h1), unpack_bf16x2(h2), cwa, cwb,
+              prm.conv.silu != 0);
+    __syncthreads();
+  }
 
   // ------------------------------------------------------------ l2 norms (token-major)
   {
@@ -691,7 +766,26 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_c
   // W^T (which needs no v) commits onto bar_mma, U^^T onto bar_u; each half of the warps then stages and
   // stores its own rows, so W^T leaves while U^^T is still being formed
   const bool ragged = valid < kC;
-  if (ragged) {   // rows past the sequence end: T's columns there are 0, but v may hold anything
+  if (kConv) {   // v's short convolution, in place in its swizzled operand tile (rows past the end become 0)
+    wait_or_abort(bar_v, 0, s_abort, prm.status);
+    const int cp = tid & 63, quarter = tid >> 6, c = 2 * cp;
+    auto off = [c](int r) { return swz_offset(64, r, c); };
+    const float4 *s_vw = reinterpret_cast<const float4 *>(small + SM_VW);
+    const float4 wa = s_vw[c], wb = s_vw[c + 1];
+    uint8_t *tile = sm + OFF_VIN;
+    uint32_t h0, h1, h2;
+    if (quarter == 0) {
+      h0 = s_halo[2 * 192 + cp]; h1 = s_halo[2 * 192 + 64 + cp]; h2 = s_halo[2 * 192 + 128 + cp];
+    } else {
+      const int r0 = 16 * quarter;
+      h0 = ld_u32(tile + off(r0 - 3)); h1 = ld_u32(tile + off(r0 - 2)); h2 = ld_u32(tile + off(r0 - 1));
+    }
+    __syncthreads();
+    conv_pair(tile, off, 16 * quarter, 16, valid, unpack_bf16x2(h0), unpack_bf16x2(h1), unpack_bf16x2(h2), wa, wb,
+              prm.conv.silu != 0);
+    fence_async_smem();
+    __syncthreads();
+  } else if (ragged) {   // rows past the sequence end: T's columns there are 0, but v may hold anything
     wait_or_abort(bar_v, 0, s_abort, prm.status);
     for (int idx = tid; idx < (kC - valid) * 16; idx += kThreads) {
       const int r2 = valid + idx / 16, cc = idx % 16;
@@ -710,7 +804,7 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_c
 #pragma unroll
     for (int s = 0; s < 4; ++s) mma_bf16(tmem, kp + kmajor_step(128, s), tt + kmajor_step(64, s), id_w, s > 0);
     mma_commit(bar_mma);
-    if (!ragged) wait_or_abort(bar_v, 0, s_abort, prm.status);
+    if (!ragged && !kConv) wait_or_abort(bar_v, 0, s_abort, prm.status);
 #pragma unroll
     for (int s = 0; s < 4; ++s) mma_bf16(tmem + 64, vv + mnmajor_step(s), tt + kmajor_step(64, s), id_u, s > 0);
     mma_commit(bar_u);
@@ -766,16 +860,17 @@ cudaError_t launch_chunk_intra(const IntraParams &p, int num_chunks, cudaStream_
   if (num_chunks <= 0) return cudaSuccess;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(chunk_intra_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(chunk_intra_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    cudaError_t e = cudaSuccess;
+    for (auto fn : {chunk_intra_kernel<16, false>, chunk_intra_kernel<32, false>, chunk_intra_kernel<16, true>,
+                    chunk_intra_kernel<32, true>})
+      if (e == cudaSuccess) e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  if (p.lower_bound >= kLowerBound32)
-    chunk_intra_kernel<32><<<num_chunks * p.H, kThreads, kSmemBytes, stream>>>(p);
-  else
-    chunk_intra_kernel<16><<<num_chunks * p.H, kThreads, kSmemBytes, stream>>>(p);
+  const bool blk32 = p.lower_bound >= kLowerBound32, conv = p.conv.weight != nullptr;
+  auto fn = blk32 ? (conv ? chunk_intra_kernel<32, true> : chunk_intra_kernel<32, false>)
+                  : (conv ? chunk_intra_kernel<16, true> : chunk_intra_kernel<16, false>);
+  fn<<<num_chunks * p.H, kThreads, kSmemBytes, stream>>>(p);
   return cudaGetLastError();
 }
 

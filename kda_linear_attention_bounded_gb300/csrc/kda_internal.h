@@ -79,6 +79,7 @@ struct ChunkArgs {
   const int32_t *out_index;  // output row of each token, or null (row = token)
   int64_t num_out_rows;      // rows of out (bounds out_index)
   OutNorm norm;
+  ShortConv conv;            // with conv.weight, q, k, v are the convolutions' raw inputs
   uint32_t *status;
 };
 
@@ -116,9 +117,19 @@ struct IntraParams {
   int prefetch_ahead;           // a CTA prefetches into L2 the inputs of the CTA this many indices later
   uint8_t *blocks;              // block (local chunk slot g, head h) at blocks + (g H + h) kBlkBytes
   uint32_t *status;
+  // short convolutions (conv.weight set): raw q, k, v, and the windows that a sequence's first chunk starts from
+  ShortConv conv;
+  const uint16_t *xq, *xk, *xv;
+  int64_t qkv_stride;
+  const int32_t *slot_ids;      // pool slot of each sequence (indexed by seq0 + local sequence)
+  int seq0;
+  int conv_load_initial;        // first chunks start from the slot's window (else from zeros)
   int32_t slot_tok0[kMaxSlotsPerLaunch];   // first token of each local chunk slot
-  uint8_t slot_valid[kMaxSlotsPerLaunch];  // its tokens (1..64)
+  uint8_t slot_valid[kMaxSlotsPerLaunch];  // its tokens (1..64) | kSlotFirst for a sequence's first chunk
+  int16_t slot_seq[kMaxSlotsPerLaunch];    // its sequence, local to the group
 };
+constexpr uint8_t kSlotFirst = 128;
+static_assert(sizeof(IntraParams) <= 32764, "kernel parameters are limited to 32764 bytes");
 
 // State pass: one CTA per (sequence, head) of a group.
 struct ChainParams {
@@ -134,6 +145,12 @@ struct ChainParams {
   const int32_t *out_index;     // output row of each token (global token index), or null (row = token)
   int64_t num_out_rows;
                                 // (with out_index the rows are stored one by one, else by TMA)
+  // short convolutions (conv.weight set): each sequence's final window goes to the pool with the final state,
+  // else to conv.window_dense
+  ShortConv conv;
+  const uint16_t *xq, *xk, *xv;
+  int64_t qkv_stride;
+  int conv_load_initial;
   uint32_t *status;
   int H, num_seqs, seq0;
   int32_t chunk_off[kMaxSeqsPerLaunch + 1];

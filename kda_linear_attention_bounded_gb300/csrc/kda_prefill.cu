@@ -93,6 +93,15 @@ cudaError_t launch_chunk_prefill(const ChunkArgs &a, const int32_t *cu_host, uin
       ip->prefetch_ahead = 0;
   }
   ip->status = a.status;
+  ip->conv = a.conv;
+  ip->xq = a.q; ip->xk = a.k; ip->xv = a.v;
+  ip->qkv_stride = a.qkv_stride;
+  ip->slot_ids = a.slot_ids;
+  ip->conv_load_initial = a.state_in != nullptr;
+  cp->conv = a.conv;
+  cp->xq = a.q; cp->xk = a.k; cp->xv = a.v;
+  cp->qkv_stride = a.qkv_stride;
+  cp->conv_load_initial = a.state_in != nullptr;
   cp->blocks = blocks;
   cp->slot_ids = a.slot_ids;
   cp->num_slots = a.num_slots;
@@ -120,6 +129,7 @@ cudaError_t launch_chunk_prefill(const ChunkArgs &a, const int32_t *cu_host, uin
     cp->tok_off[ns] = cu_host[s0 + ns];
     cp->num_seqs = ns;
     cp->seq0 = s0;
+    ip->seq0 = s0;
     idx.resize(ns);
     std::iota(idx.begin(), idx.end(), 0);
     std::stable_sort(idx.begin(), idx.end(), [&](int x, int y) {
@@ -137,7 +147,8 @@ cudaError_t launch_chunk_prefill(const ChunkArgs &a, const int32_t *cu_host, uin
         const int j = g0 + g - cp->chunk_off[i];
         const int t = cp->tok_off[i] + j * kChunk;
         ip->slot_tok0[g] = t;
-        ip->slot_valid[g] = static_cast<uint8_t>(std::min(kChunk, cp->tok_off[i + 1] - t));
+        ip->slot_valid[g] = static_cast<uint8_t>(std::min(kChunk, cp->tok_off[i + 1] - t) | (j == 0 ? kSlotFirst : 0));
+        ip->slot_seq[g] = static_cast<int16_t>(i);
       }
       ip->blocks = blocks + static_cast<size_t>(g0) * a.H * kBlkBytes;
       e = launch_chunk_intra(*ip, ng, stream);

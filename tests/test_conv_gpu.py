@@ -116,3 +116,102 @@ def test_spec_step_verify_segment_with_short_conv():
     check_out(out[torch.from_numpy(rows).long().cuda()], ref_out, "spec step verify rows with the convolutions")
     check_state(inter, ref_steps, "spec step per-step states with the convolutions")
     assert np.array_equal(widen_bf16(conv.step_windows), ref_win)
+
+
+def _prefill_with_conv(inp, heads=None):
+    from gpu_helpers import DevicePrefill
+    dev = DevicePrefill(inp)
+    conv = device_conv(inp.conv, N=None if inp.final_to_pool else inp.num_seqs)
+    ws = dev.workspace()
+    out, final = dev.run(workspace=ws, conv=conv)
+    torch.cuda.synchronize()
+    assert kda.read_device_status(ws) == 0
+    ref_out, ref_S, _, ref_win = oracle.run_prefill(inp, heads=heads)
+    hb, he = heads if heads else (0, inp.H)
+    check_out(out[:, hb:he], ref_out[:, hb:he], f"{inp.name} outputs with the convolutions")
+    if inp.final_to_pool:
+        slots = torch.from_numpy(inp.slot_ids).long().cuda()
+        check_state(dev.pool[slots][:, hb:he], ref_S[:, hb:he], f"{inp.name} final states (pool)")
+        got_win = widen_bf16(conv.window_pool[slots])
+    else:
+        check_state(final[:, hb:he], ref_S[:, hb:he], f"{inp.name} final states (dense)")
+        got_win = widen_bf16(conv.window_dense)
+    assert np.array_equal(got_win[..., hb:he, :], ref_win[..., hb:he, :]), "final windows differ from the oracle's"
+    return dev, conv
+
+
+@pytest.mark.parametrize("lb", [-5.0, -8.0])
+def test_prefill_with_short_conv_small(lb):
+    # full chunks, a one-token and a two-token sequence (their final windows keep rows of the initial one), a
+    # zero-length one, a ragged last chunk; both sub-block sizes of the intra-chunk kernel
+    inp = inputs.prefill_inputs("conv_prefill", [130, 64, 1, 0, 77, 2], 2, seed=700, pool_slots=8,
+                                load_initial=True, final_to_pool=True, lower_bound=lb)
+    inp.conv = inputs.conv_inputs(2, 8, seed=701)
+    _prefill_with_conv(inp)
+
+
+def test_prefill_with_short_conv_zero_start_dense_final():
+    inp = inputs.prefill_inputs("conv_prefill_dense", [100, 3, 65], 3, seed=710)
+    inp.conv = inputs.conv_inputs(3, 4, seed=711, silu=False)
+    _prefill_with_conv(inp)
+
+
+def test_prefill_with_short_conv_2048x8_h16_full():
+    inp = inputs.prefill_2048x8()
+    inp.final_to_pool = True
+    inp.conv = inputs.conv_inputs(16, 64, seed=720)
+    _prefill_with_conv(inp, heads=(0, 4))
+
+
+def test_prefill_then_verify_continue_through_the_window():
+    # a prefill that leaves its final state and window in the pool, then a verify block from them, equals one
+    # oracle run over both token sets
+    H, T = 2, 5
+    pre = inputs.prefill_inputs("conv_pv", [77, 130], H, seed=730, pool_slots=4, load_initial=True,
+                                final_to_pool=True)
+    pre.conv = inputs.conv_inputs(H, 4, seed=731)
+    dev, conv = _prefill_with_conv(pre)
+    ver = inputs.verify_inputs("conv_pv2", 2, T, H, seed=732, pool_slots=4)
+    dver = DeviceVerify(ver)
+    conv2 = kda.ShortConv(conv.weight, conv.window_pool, conv.silu,
+                          step_windows=torch.empty((2, T, 3, 3, H, 128), dtype=torch.bfloat16, device="cuda"))
+    ws = kda.make_workspace()
+    out, _ = kda.recurrent_verify(dver.q, dver.k, dver.v, dver.g, dver.beta, dev.A_log, dev.dt_bias, dev.pool,
+                                  dev.slots, T, lower_bound=pre.lower_bound, scale=pre.scale, conv=conv2,
+                                  workspace=ws)
+    torch.cuda.synchronize()
+    assert kda.read_device_status(ws) == 0
+    for b in range(2):
+        a, e = int(pre.cu_seqlens[b]), int(pre.cu_seqlens[b + 1])
+        cat = lambda x1, x2: np.concatenate([x1[a:e], x2[b * T:(b + 1) * T]])
+        s = int(pre.slot_ids[b])
+        ref, _, _, _, _ = oracle.run_conv(cat(pre.q, ver.q), cat(pre.k, ver.k), cat(pre.v, ver.v),
+                                          cat(pre.g, ver.g), cat(pre.beta, ver.beta), pre.A_log, pre.dt_bias,
+                                          pre.lower_bound, pre.scale, np.array([0, e - a + T], np.int32),
+                                          pre.conv.weight, pre.conv.silu,
+                                          win0=oracle.bf16_widen(pre.conv.pool[s:s + 1]), S0=pre.pool[s:s + 1])
+        check_out(out[b * T:(b + 1) * T], ref[e - a:], f"sequence {b}: verify block after its prefill")
+
+
+def test_spec_step_with_short_conv_both_segments():
+    from gpu_helpers import DeviceSpecStep
+    inp = inputs.spec_step_inputs("conv_step2", [90, 64, 2], 4, 3, 2, seed=740, order="interleaved", extra_rows=2)
+    ci = inputs.conv_inputs(2, inp.prefill.pool.shape[0], seed=741)
+    inp.prefill.conv = inp.verify.conv = ci
+    dev = DeviceSpecStep(inp)
+    conv = device_conv(ci, B=inp.verify.B, T=inp.verify.T)
+    ws = dev.workspace()
+    out, _, inter = dev.run(workspace=ws, conv=conv)
+    torch.cuda.synchronize()
+    assert kda.read_device_status(ws) == 0
+    p_out, p_S, _, p_win = oracle.run_prefill(inp.prefill)
+    v_out, v_steps, v_win = oracle.run_verify(inp.verify)
+    ns = torch.from_numpy(inp.non_spec_token_indx).long().cuda()
+    sp = torch.from_numpy(inp.spec_token_indx).long().cuda()
+    check_out(out[ns], p_out, "spec step prefill rows with the convolutions")
+    check_out(out[sp], v_out, "spec step verify rows with the convolutions")
+    check_state(inter, v_steps, "spec step per-step states with the convolutions")
+    pslots = torch.from_numpy(inp.prefill.slot_ids).long().cuda()
+    check_state(dev.pool[pslots], p_S, "spec step prefill final states")
+    assert np.array_equal(widen_bf16(conv.window_pool[pslots]), p_win), "prefill final windows"
+    assert np.array_equal(widen_bf16(conv.step_windows), v_win), "verify per-step windows"
