@@ -64,6 +64,8 @@ def verify_algorithmic_bytes(inp):
 
 # the gated RMSNorm of an output row and head: the bf16 gate row read and the fp32 rstd written
 NORM_BYTES_PER_ROW = 256 + 4
+# one short-convolution window of a (sequence or step, head): 3 raw inputs of q, k and v, bf16
+CONV_WINDOW_BYTES = 3 * 3 * 128 * 2
 
 
 def spec_step_algorithmic_bytes(inp):
@@ -507,6 +509,45 @@ def run_gpu(args):
                                 "algorithmic_bytes": vn_bytes}},
     }
 
+    # ---- the same prefill and verify with the short causal convolutions of q, k, v fused into their prologues ----
+    ci = inputs.conv_inputs(H, inp.pool.shape[0], seed=1200)
+    pconv = kda.ShortConv(f32_dev(ci.weight, device), bf16_dev(ci.pool, device), ci.silu,
+                          window_dense=torch.empty((inp.num_seqs, 3, 3, H, 128), dtype=torch.bfloat16, device=device))
+    for _ in range(3):
+        dev.run(out=out, final_state=final, workspace=ws, stream=stream, conv=pconv)
+    c0 = torch.cuda.Event(enable_timing=True)
+    c1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(device)
+    c0.record(stream)
+    for _ in range(n_steps):
+        dev.run(out=out, final_state=final, workspace=ws, stream=stream, conv=pconv)
+    c1.record(stream)
+    torch.cuda.synchronize(device)
+    pc_us = c0.elapsed_time(c1) * 1e3 / n_steps
+    pc_bytes = alg + 2 * inp.num_seqs * H * CONV_WINDOW_BYTES
+    vci = inputs.conv_inputs(H, vin.pool.shape[0], seed=1201)
+    vconv = kda.ShortConv(f32_dev(vci.weight, device), bf16_dev(vci.pool, device), vci.silu,
+                          step_windows=torch.empty((vin.B, vin.T, 3, 3, H, 128), dtype=torch.bfloat16, device=device))
+    vc_out = torch.empty((vin.B * vin.T, H, 128), dtype=torch.bfloat16, device=device)
+    vc_inter = torch.empty((vin.B, vin.T, H, 128, 128), dtype=torch.float32, device=device)
+    vc_us, vc_calls = graph_time_us(
+        [lambda: vdev.run(out=vc_out, intermediate_states=vc_inter, workspace=ws, conv=vconv)],
+        max(3, min(args.steps, 200)))
+    vc_bytes = verify_algorithmic_bytes(vin) + vin.B * H * CONV_WINDOW_BYTES * (1 + vin.T)
+    assert kda.read_device_status(ws) == 0
+    del vc_out, vc_inter, pconv, vconv
+    short_conv = {
+        "prefill": {"workload": inp.name, "us_per_layer": pc_us, "steps": n_steps,
+                    "extra_us_vs_plain": pc_us - avg_launch_s * 1e6,
+                    "roofline": {"bound": "hbm", "achieved": pc_bytes / (pc_us * 1e-6) / 1e9, "peak": peak,
+                                 "unit": "GB/s", "frac": pc_bytes / (pc_us * 1e-6) / 1e9 / peak,
+                                 "algorithmic_bytes": pc_bytes}},
+        "verify": {"workload": vin.name, "us_per_layer": vc_us, "calls_timed": vc_calls,
+                   "roofline": {"bound": "hbm", "achieved": vc_bytes / (vc_us * 1e-6) / 1e9, "peak": peak,
+                                "unit": "GB/s", "frac": vc_bytes / (vc_us * 1e-6) / 1e9 / peak,
+                                "algorithmic_bytes": vc_bytes}},
+    }
+
     # ---- one spec step: prefill segment + verify segment, outputs written by index into the layer output ----
     sdev = DeviceSpecStep(inputs.spec_step_2048x4_64x4(), device=device)
     sin = sdev.inp
@@ -563,6 +604,7 @@ def run_gpu(args):
                       "roofline": {"bound": "hbm", "achieved": s_achieved, "peak": peak, "unit": "GB/s",
                                    "frac": s_achieved / peak, "algorithmic_bytes": s_bytes}},
         "gated_norm": gated,
+        "short_conv": short_conv,
         "commit": {"workload": vin.name + " (1..8 accepted per request)", "us_per_layer": c_us, "calls_timed": c_steps,
                    "roofline": {"bound": "hbm", "achieved": c_achieved, "peak": peak, "unit": "GB/s",
                                 "frac": c_achieved / peak, "algorithmic_bytes": c_bytes}},

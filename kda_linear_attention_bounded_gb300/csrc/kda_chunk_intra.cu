@@ -206,29 +206,31 @@ __device__ __forceinline__ void build_rows(const uint32_t (&kqw)[16], const floa
   }
 }
 
-// SiLU through tanh: x sigmoid(x) = x/2 (1 + tanh(x/2))
-__device__ __forceinline__ float silu_tanh(float x) {
-  float t;
-  asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(0.5f * x));
-  return 0.5f * x * (1.0f + t);
-}
-
 // Short causal convolution down one channel pair of a bf16 tile, in place: rows r0 .. r0+n-1 at byte offsets
 // off(r) from `tile`, the raw inputs of rows r0-3 .. r0-1 in x0 .. x2 (oldest first), taps wa / wb of the two
 // channels (tap 3 on the current row).  Rows at or past `valid` become 0.
-template <typename Off>
-__device__ __forceinline__ void conv_pair(uint8_t *tile, Off off, int r0, int n, int valid, float2 x0, float2 x1,
+template <int N, typename Off>
+__device__ __forceinline__ void conv_pair(uint8_t *tile, Off off, int r0, int valid, float2 x0, float2 x1,
                                           float2 x2, float4 wa, float4 wb, bool silu) {
-  for (int r = r0; r < r0 + n; ++r) {
-    uint32_t *p = reinterpret_cast<uint32_t *>(tile + off(r));
-    const float2 x = unpack_bf16x2(*p);
-    float y0 = fmaf(wa.w, x.x, fmaf(wa.z, x2.x, fmaf(wa.y, x1.x, wa.x * x0.x)));
-    float y1 = fmaf(wb.w, x.y, fmaf(wb.z, x2.y, fmaf(wb.y, x1.y, wb.x * x0.y)));
-    if (silu) {
-      y0 = silu_tanh(y0);
-      y1 = silu_tanh(y1);
+  // the two channels side by side in packed fp32x2 arithmetic; the N inputs first (independent loads)
+  const float2 w0 = make_float2(wa.x, wb.x), w1 = make_float2(wa.y, wb.y), w2 = make_float2(wa.z, wb.z),
+               w3 = make_float2(wa.w, wb.w), half2 = make_float2(0.5f, 0.5f);
+  uint32_t raw[N];
+#pragma unroll
+  for (int i = 0; i < N; ++i) raw[i] = *reinterpret_cast<const uint32_t *>(tile + off(r0 + i));
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    const int r = r0 + i;
+    const float2 x = unpack_bf16x2(raw[i]);
+    float2 y = fma2(w3, x, fma2(w2, x2, fma2(w1, x1, mul2(w0, x0))));
+    if (silu) {   // x sigmoid(x) = x/2 + x/2 tanh(x/2)
+      const float2 hy = mul2(y, half2);
+      float t0, t1;
+      asm("tanh.approx.f32 %0, %1;" : "=f"(t0) : "f"(hy.x));
+      asm("tanh.approx.f32 %0, %1;" : "=f"(t1) : "f"(hy.y));
+      y = fma2(hy, make_float2(t0, t1), hy);
     }
-    *p = r < valid ? pack_bf16x2(y0, y1) : 0u;
+    *reinterpret_cast<uint32_t *>(tile + off(r)) = r < valid ? pack_bf16x2(y.x, y.y) : 0u;
     x0 = x1;
     x1 = x2;
     x2 = x;
@@ -285,25 +287,31 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_c
   // short convolutions: the 3 raw inputs before the chunk for q, k, v (the previous tokens of the sequence,
   // else the slot's window for its first chunk, else zeros) and v's taps go to shared memory; this thread's
   // q or k taps to registers (thread = tensor tid / 128, channel pair tid % 64, half of the rows)
+  // (the loads are issued here and land in shared memory after the wait for q, k, g, which hides them)
   uint32_t *s_halo = reinterpret_cast<uint32_t *>(small + SM_HALO);
-  float4 cwa = make_float4(0.f, 0.f, 0.f, 0.f), cwb = cwa;
+  float4 cwa = make_float4(0.f, 0.f, 0.f, 0.f), cwb = cwa, vw = cwa;
+  constexpr int kHaloWords = 3 * 3 * 64, kHaloPerThread = (kHaloWords + kThreads - 1) / kThreads;
+  uint32_t halo[kHaloPerThread];
   if (kConv) {
     const bool first = prm.slot_valid[gslot] & kSlotFirst;
     const int slot = first && prm.conv_load_initial ? prm.slot_ids[prm.seq0 + prm.slot_seq[gslot]] : -1;
-    for (int i = tid; i < 3 * 3 * 64; i += kThreads) {
+#pragma unroll
+    for (int k = 0; k < kHaloPerThread; ++k) {
+      const int i = tid + k * kThreads;
       const int m = i / 192, j = (i / 64) % 3, w = i % 64;
       uint32_t x = 0u;
-      if (!first) {
-        const uint16_t *src = m == 0 ? prm.xq : m == 1 ? prm.xk : prm.xv;
-        x = *reinterpret_cast<const uint32_t *>(src + static_cast<int64_t>(tok0 - 3 + j) * prm.qkv_stride + h * kD + 2 * w);
-      } else if (slot >= 0) {
-        x = *reinterpret_cast<const uint32_t *>(prm.conv.window_pool +
-                                                ((static_cast<size_t>(slot) * 9 + m * 3 + j) * H + h) * kD + 2 * w);
+      if (i < kHaloWords) {
+        if (!first) {
+          const uint16_t *src = m == 0 ? prm.xq : m == 1 ? prm.xk : prm.xv;
+          x = *reinterpret_cast<const uint32_t *>(src + static_cast<int64_t>(tok0 - 3 + j) * prm.qkv_stride + h * kD + 2 * w);
+        } else if (slot >= 0) {
+          x = *reinterpret_cast<const uint32_t *>(prm.conv.window_pool +
+                                                  ((static_cast<size_t>(slot) * 9 + m * 3 + j) * H + h) * kD + 2 * w);
+        }
       }
-      s_halo[i] = x;
+      halo[k] = x;
     }
-    float4 *s_vw = reinterpret_cast<float4 *>(small + SM_VW);
-    if (tid < kD) s_vw[tid] = *reinterpret_cast<const float4 *>(prm.conv.weight + ((2 * static_cast<size_t>(H) + h) * kD + tid) * 4);
+    if (tid < kD) vw = *reinterpret_cast<const float4 *>(prm.conv.weight + ((2 * static_cast<size_t>(H) + h) * kD + tid) * 4);
     const int cm = tid >> 7, c = 2 * (tid & 63);
     cwa = *reinterpret_cast<const float4 *>(prm.conv.weight + ((static_cast<size_t>(cm) * H + h) * kD + c) * 4);
     cwb = *reinterpret_cast<const float4 *>(prm.conv.weight + ((static_cast<size_t>(cm) * H + h) * kD + c + 1) * 4);
@@ -324,19 +332,24 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_c
 
   // ------------------------------------------------------------ short convolutions of q and k, in place
   if (kConv) {
+#pragma unroll
+    for (int k = 0; k < kHaloPerThread; ++k)
+      if (tid + k * kThreads < kHaloWords) s_halo[tid + k * kThreads] = halo[k];
+    if (tid < kD) reinterpret_cast<float4 *>(small + SM_VW)[tid] = vw;
     const int cm = tid >> 7, cp = tid & 63, half = (tid >> 6) & 1;
     uint8_t *tile = sm + (cm == 0 ? OFF_QIN : OFF_KIN);
     const int c = 2 * cp;
     auto off = [c](int r) { return in_offset(r, c); };
-    uint32_t h0, h1, h2;
-    if (half == 0) {
-      h0 = s_halo[cm * 192 + cp]; h1 = s_halo[cm * 192 + 64 + cp]; h2 = s_halo[cm * 192 + 128 + cp];
-    } else {   // rows 29 .. 31, read before the first half overwrites them
+    uint32_t h0 = 0u, h1 = 0u, h2 = 0u;
+    if (half == 1) {   // rows 29 .. 31, read before the first half overwrites them
       h0 = ld_u32(tile + off(29)); h1 = ld_u32(tile + off(30)); h2 = ld_u32(tile + off(31));
     }
     __syncthreads();
-    conv_pair(tile, off, 32 * half, 32, valid, unpack_bf16x2(h0), unpack_bf16x2(h1), unpack_bf16x2(h2), cwa, cwb,
-              prm.conv.silu != 0);
+    if (half == 0) {
+      h0 = s_halo[cm * 192 + cp]; h1 = s_halo[cm * 192 + 64 + cp]; h2 = s_halo[cm * 192 + 128 + cp];
+    }
+    conv_pair<32>(tile, off, 32 * half, valid, unpack_bf16x2(h0), unpack_bf16x2(h1), unpack_bf16x2(h2), cwa, cwb,
+                  prm.conv.silu != 0);
     __syncthreads();
   }
 
@@ -781,8 +794,8 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_c
       h0 = ld_u32(tile + off(r0 - 3)); h1 = ld_u32(tile + off(r0 - 2)); h2 = ld_u32(tile + off(r0 - 1));
     }
     __syncthreads();
-    conv_pair(tile, off, 16 * quarter, 16, valid, unpack_bf16x2(h0), unpack_bf16x2(h1), unpack_bf16x2(h2), wa, wb,
-              prm.conv.silu != 0);
+    conv_pair<16>(tile, off, 16 * quarter, valid, unpack_bf16x2(h0), unpack_bf16x2(h1), unpack_bf16x2(h2), wa, wb,
+                  prm.conv.silu != 0);
     fence_async_smem();
     __syncthreads();
   } else if (ragged) {   // rows past the sequence end: T's columns there are 0, but v may hold anything
