@@ -294,7 +294,8 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_c
   uint32_t halo[kHaloPerThread];
   if (kConv) {
     const bool first = prm.slot_valid[gslot] & kSlotFirst;
-    const int slot = first && prm.conv_load_initial ? prm.slot_ids[prm.seq0 + prm.slot_seq[gslot]] : -1;
+    int slot = first && prm.conv_load_initial ? prm.slot_ids[prm.seq0 + prm.slot_seq[gslot]] : -1;
+    if (slot >= prm.num_slots) slot = -1;   // out of range: no window is read (the state pass sets the status bit)
 #pragma unroll
     for (int k = 0; k < kHaloPerThread; ++k) {
       const int i = tid + k * kThreads;

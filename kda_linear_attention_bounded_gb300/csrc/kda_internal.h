@@ -122,6 +122,7 @@ struct IntraParams {
   const uint16_t *xq, *xk, *xv;
   int64_t qkv_stride;
   const int32_t *slot_ids;      // pool slot of each sequence (indexed by seq0 + local sequence)
+  int num_slots;                // a slot outside [0, num_slots) reads a zero window (the state pass reports it)
   int seq0;
   int conv_load_initial;        // first chunks start from the slot's window (else from zeros)
   int32_t slot_tok0[kMaxSlotsPerLaunch];   // first token of each local chunk slot

@@ -97,6 +97,7 @@ cudaError_t launch_chunk_prefill(const ChunkArgs &a, const int32_t *cu_host, uin
   ip->xq = a.q; ip->xk = a.k; ip->xv = a.v;
   ip->qkv_stride = a.qkv_stride;
   ip->slot_ids = a.slot_ids;
+  ip->num_slots = a.num_slots;
   ip->conv_load_initial = a.state_in != nullptr;
   cp->conv = a.conv;
   cp->xq = a.q; cp->xk = a.k; cp->xv = a.v;

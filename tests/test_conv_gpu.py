@@ -215,3 +215,24 @@ def test_spec_step_with_short_conv_both_segments():
     check_state(dev.pool[pslots], p_S, "spec step prefill final states")
     assert np.array_equal(widen_bf16(conv.window_pool[pslots]), p_win), "prefill final windows"
     assert np.array_equal(widen_bf16(conv.step_windows), v_win), "verify per-step windows"
+
+
+def test_prefill_with_short_conv_bad_slot():
+    # a slot id outside the pool: that sequence is skipped with the status bit, its chunks read no window, and
+    # the other sequence is unaffected
+    from gpu_helpers import DevicePrefill
+    inp = inputs.prefill_inputs("conv_bad_slot", [70, 90], 2, seed=750, pool_slots=4, load_initial=True,
+                                final_to_pool=True)
+    inp.conv = inputs.conv_inputs(2, 4, seed=751)
+    dev = DevicePrefill(inp)
+    dev.slots[1] = 4   # == num_slots
+    conv = device_conv(inp.conv)
+    ws = dev.workspace()
+    out, _ = dev.run(workspace=ws, conv=conv)
+    torch.cuda.synchronize()
+    assert kda.read_device_status(ws) & kda.KDA_DEVICE_BAD_SLOT
+    ref_out, ref_S, _, ref_win = oracle.run_prefill(inp)
+    check_out(out[:70], ref_out[:70], "the sequence beside a bad slot")
+    s0 = int(inp.slot_ids[0])
+    check_state(dev.pool[s0], ref_S[0], "its final state")
+    assert np.array_equal(widen_bf16(conv.window_pool[s0]), ref_win[0]), "its final window"
