@@ -236,3 +236,31 @@ def test_prefill_with_short_conv_bad_slot():
     s0 = int(inp.slot_ids[0])
     check_state(dev.pool[s0], ref_S[0], "its final state")
     assert np.array_equal(widen_bf16(conv.window_pool[s0]), ref_win[0]), "its final window"
+
+
+def test_spec_step_with_short_conv_and_gated_norm():
+    # every option at once: convolutions on both segments, the gated norm on every output row
+    from gpu_helpers import DeviceSpecStep, check_norm, device_norm
+    inp = inputs.spec_step_inputs("conv_norm_step", [100, 7], 3, 4, 2, seed=760, order="interleaved", extra_rows=1)
+    ci = inputs.conv_inputs(2, inp.prefill.pool.shape[0], seed=761)
+    inp.prefill.conv = inp.verify.conv = ci
+    dev = DeviceSpecStep(inp)
+    conv = device_conv(ci, B=inp.verify.B, T=inp.verify.T)
+    ni = inputs.norm_inputs(inp.num_out_tokens, 2, seed=762)
+    norm = device_norm(ni, 2)
+    ws = dev.workspace()
+    out, _, inter = dev.run(workspace=ws, conv=conv, norm=norm)
+    torch.cuda.synchronize()
+    assert kda.read_device_status(ws) == 0
+    p_out, p_S, _, p_win = oracle.run_prefill(inp.prefill)
+    v_out, v_steps, v_win = oracle.run_verify(inp.verify)
+    ns, sp = inp.non_spec_token_indx, inp.spec_token_indx
+    y = out.float().cpu().numpy()
+    r = norm.rstd.cpu().numpy()
+    check_norm(y[ns], r[ns], p_out, ni.gate[ns], ni, "prefill rows, convolutions + norm")
+    check_norm(y[sp], r[sp], v_out, ni.gate[sp], ni, "verify rows, convolutions + norm")
+    check_state(inter, v_steps, "per-step states, convolutions + norm")
+    pslots = torch.from_numpy(inp.prefill.slot_ids).long().cuda()
+    check_state(dev.pool[pslots], p_S, "prefill final states, convolutions + norm")
+    assert np.array_equal(widen_bf16(conv.window_pool[pslots]), p_win)
+    assert np.array_equal(widen_bf16(conv.step_windows), v_win)
