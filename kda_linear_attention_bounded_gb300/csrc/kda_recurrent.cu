@@ -30,10 +30,41 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kTile = kWarps;      // tokens prepared per prologue pass (one per warp)
 constexpr int kRows = kD / kWarps;  // key channels per warp (16)
 
-// One (request, head) work item.  Every return is taken by the whole CTA.  The optional short convolutions
-// and output norm are compile-time switches, so the plain call carries none of their code.
-template <bool kConv, bool kNorm>
+// kVC consecutive floats (4, 2 or 1) as one load / store
+template <int kVC>
+__device__ __forceinline__ void load_vc(float *d, const float *src) {
+  if constexpr (kVC == 4) {
+    const float4 x = __ldg(reinterpret_cast<const float4 *>(src));
+    d[0] = x.x; d[1] = x.y; d[2] = x.z; d[3] = x.w;
+  } else if constexpr (kVC == 2) {
+    const float2 x = __ldg(reinterpret_cast<const float2 *>(src));
+    d[0] = x.x; d[1] = x.y;
+  } else {
+    d[0] = __ldg(src);
+  }
+}
+template <int kVC, bool kStream>
+__device__ __forceinline__ void store_vc(float *dst, const float *v) {
+  if constexpr (kVC == 4) {
+    const float4 x = make_float4(v[0], v[1], v[2], v[3]);
+    if (kStream) __stcs(reinterpret_cast<float4 *>(dst), x); else *reinterpret_cast<float4 *>(dst) = x;
+  } else if constexpr (kVC == 2) {
+    const float2 x = make_float2(v[0], v[1]);
+    if (kStream) __stcs(reinterpret_cast<float2 *>(dst), x); else *reinterpret_cast<float2 *>(dst) = x;
+  } else {
+    if (kStream) __stcs(dst, v[0]); else *dst = v[0];
+  }
+}
+
+// One work item: (request, head) and, with kP > 1, one of kP slices of the value channels (the columns of S are
+// independent in the recurrence; every slice recomputes the key side).  Every return is taken by the whole CTA.
+// The optional short convolutions and output norm are compile-time switches, so the plain call carries none of
+// their code; they need whole rows (kP == 1).
+template <bool kConv, bool kNorm, int kP>
 __device__ __forceinline__ void recurrent_item(const RecurrentArgs &p) {
+  static_assert(kP == 1 || (!kConv && !kNorm), "the value-channel split is for the plain call");
+  constexpr int kVC = 4 / kP;          // value channels per lane
+  constexpr int kCols = kD / kP;       // value channels per CTA
   __shared__ __align__(16) float s_khat[kTile][kD];
   __shared__ __align__(16) float s_kalpha[kTile][kD];
   __shared__ __align__(16) float s_qalpha[kTile][kD];
@@ -48,8 +79,9 @@ __device__ __forceinline__ void recurrent_item(const RecurrentArgs &p) {
   __shared__ __align__(16) float s_u[kD];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int h = blockIdx.x % p.H;
-  const int n = blockIdx.x / p.H;
+  const int part = blockIdx.x % kP;
+  const int h = (blockIdx.x / kP) % p.H;
+  const int n = blockIdx.x / (kP * p.H);
   const int t_begin = p.cu_seqlens ? p.cu_seqlens[n] : n * p.T;
   const int t_end = p.cu_seqlens ? p.cu_seqlens[n + 1] : (n + 1) * p.T;
 
@@ -64,18 +96,18 @@ __device__ __forceinline__ void recurrent_item(const RecurrentArgs &p) {
   }
 
   const int row0 = warp * kRows;
-  const int col0 = lane * 4;
-  float S[kRows][4];
+  const int col0 = lane * 4;                      // this lane's 4 key channels (q, k, gate)
+  const int vcol = part * kCols + lane * kVC;     // this lane's kVC value channels (columns of S)
+  float S[kRows][kVC];
   if (p.state_in) {
     const float *src = p.state_in + ((size_t)slot * p.H + h) * kD * kD;
 #pragma unroll
-    for (int i = 0; i < kRows; ++i) {
-      float4 x = __ldg(reinterpret_cast<const float4 *>(src + (size_t)(row0 + i) * kD + col0));
-      S[i][0] = x.x; S[i][1] = x.y; S[i][2] = x.z; S[i][3] = x.w;
-    }
+    for (int i = 0; i < kRows; ++i) load_vc<kVC>(S[i], src + (size_t)(row0 + i) * kD + vcol);
   } else {
 #pragma unroll
-    for (int i = 0; i < kRows; ++i) S[i][0] = S[i][1] = S[i][2] = S[i][3] = 0.f;
+    for (int i = 0; i < kRows; ++i)
+#pragma unroll
+      for (int j = 0; j < kVC; ++j) S[i][j] = 0.f;
   }
 
   // per-head gate constants for this lane's 4 channels
@@ -108,13 +140,22 @@ __device__ __forceinline__ void recurrent_item(const RecurrentArgs &p) {
       if (!kConv) {
         const uint2 qr = *reinterpret_cast<const uint2 *>(p.q + (size_t)t * p.qkv_stride + h * kD + col0);
         const uint2 kr = *reinterpret_cast<const uint2 *>(p.k + (size_t)t * p.qkv_stride + h * kD + col0);
-        const uint2 vr = *reinterpret_cast<const uint2 *>(p.v + (size_t)t * p.qkv_stride + h * kD + col0);
         const float2 q01 = unpack_bf16x2(qr.x), q23 = unpack_bf16x2(qr.y);
         const float2 k01 = unpack_bf16x2(kr.x), k23 = unpack_bf16x2(kr.y);
-        const float2 v01 = unpack_bf16x2(vr.x), v23 = unpack_bf16x2(vr.y);
         qf[0] = q01.x; qf[1] = q01.y; qf[2] = q23.x; qf[3] = q23.y;
         kf[0] = k01.x; kf[1] = k01.y; kf[2] = k23.x; kf[3] = k23.y;
-        vf[0] = v01.x; vf[1] = v01.y; vf[2] = v23.x; vf[3] = v23.y;
+        // this lane's kVC value channels of the CTA's slice
+        const uint16_t *vp = p.v + (size_t)t * p.qkv_stride + h * kD + vcol;
+        if constexpr (kVC == 4) {
+          const uint2 vr = *reinterpret_cast<const uint2 *>(vp);
+          const float2 v01 = unpack_bf16x2(vr.x), v23 = unpack_bf16x2(vr.y);
+          vf[0] = v01.x; vf[1] = v01.y; vf[2] = v23.x; vf[3] = v23.y;
+        } else if constexpr (kVC == 2) {
+          const float2 v01 = unpack_bf16x2(*reinterpret_cast<const uint32_t *>(vp));
+          vf[0] = v01.x; vf[1] = v01.y;
+        } else {
+          vf[0] = bf16_bits_to_f32(*vp);
+        }
       } else {
         // short causal convolutions of q, k, v over this lane's 4 channels: the raw inputs 3, 2, 1 and 0
         // tokens back (the request's own tokens, else its slot's window, oldest row first); the window
@@ -174,8 +215,9 @@ __device__ __forceinline__ void recurrent_item(const RecurrentArgs &p) {
         s_kalpha[warp][col0 + j] = alpha * kh;
         s_qalpha[warp][col0 + j] = alpha * qh;
         s_alpha[warp][col0 + j] = alpha;
-        s_v[warp][col0 + j] = vf[j];
       }
+#pragma unroll
+      for (int j = 0; j < kVC; ++j) s_v[warp][lane * kVC + j] = vf[j];
       kq = warp_sum(kq);
       if (lane == 0) {
         s_kq[warp] = kq;
@@ -188,21 +230,26 @@ __device__ __forceinline__ void recurrent_item(const RecurrentArgs &p) {
 
     for (int s = 0; s < nt; ++s) {
       const int t = tile + s;
-      // partial S^T (alpha k^) and S^T (alpha q^) over this warp's 16 rows
-      float pk[4] = {0.f, 0.f, 0.f, 0.f}, pq[4] = {0.f, 0.f, 0.f, 0.f};
+      // partial S^T (alpha k^) and S^T (alpha q^) over this warp's 16 rows, for the lane's value channels
+      float pk[kVC], pq[kVC];
+#pragma unroll
+      for (int j = 0; j < kVC; ++j) pk[j] = pq[j] = 0.f;
 #pragma unroll
       for (int i = 0; i < kRows; ++i) {
         const float ka = s_kalpha[s][row0 + i], qa = s_qalpha[s][row0 + i];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 0; j < kVC; ++j) {
           pk[j] = fmaf(S[i][j], ka, pk[j]);
           pq[j] = fmaf(S[i][j], qa, pq[j]);
         }
       }
-      *reinterpret_cast<float4 *>(&s_redk[warp][col0]) = make_float4(pk[0], pk[1], pk[2], pk[3]);
-      *reinterpret_cast<float4 *>(&s_redq[warp][col0]) = make_float4(pq[0], pq[1], pq[2], pq[3]);
+#pragma unroll
+      for (int j = 0; j < kVC; ++j) {
+        s_redk[warp][lane * kVC + j] = pk[j];
+        s_redq[warp][lane * kVC + j] = pq[j];
+      }
       __syncthreads();
-      if (tid < kD) {
+      if (tid < kCols) {   // thread = the slice's value channel tid
         float wk = 0.f, wq = 0.f;
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) {
@@ -221,21 +268,19 @@ __device__ __forceinline__ void recurrent_item(const RecurrentArgs &p) {
           o = o * rstd * p.norm.weight[tid] * s_gz[s][tid];
           if (tid == 0 && row >= 0 && p.norm.rstd) p.norm.rstd[row * p.H + h] = rstd;
         }
-        if (row >= 0) p.out[row * p.out_stride + h * kD + tid] = f32_to_bf16_bits(o);
+        if (row >= 0) p.out[row * p.out_stride + h * kD + part * kCols + tid] = f32_to_bf16_bits(o);
       }
       __syncthreads();
-      const float4 u4 = *reinterpret_cast<const float4 *>(&s_u[col0]);
+      float uu[kVC];
+#pragma unroll
+      for (int j = 0; j < kVC; ++j) uu[j] = s_u[lane * kVC + j];
       float *rec = p.inter ? p.inter + (((size_t)n * p.T + (t - t_begin)) * p.H + h) * kD * kD : nullptr;
 #pragma unroll
       for (int i = 0; i < kRows; ++i) {
         const float a = s_alpha[s][row0 + i], kh = s_khat[s][row0 + i];
-        S[i][0] = fmaf(a, S[i][0], kh * u4.x);
-        S[i][1] = fmaf(a, S[i][1], kh * u4.y);
-        S[i][2] = fmaf(a, S[i][2], kh * u4.z);
-        S[i][3] = fmaf(a, S[i][3], kh * u4.w);
-        if (rec)
-          __stcs(reinterpret_cast<float4 *>(rec + (size_t)(row0 + i) * kD + col0),
-                 make_float4(S[i][0], S[i][1], S[i][2], S[i][3]));
+#pragma unroll
+        for (int j = 0; j < kVC; ++j) S[i][j] = fmaf(a, S[i][j], kh * uu[j]);
+        if (rec) store_vc<kVC, true>(rec + (size_t)(row0 + i) * kD + vcol, S[i]);
       }
     }
     __syncthreads();
@@ -246,15 +291,13 @@ __device__ __forceinline__ void recurrent_item(const RecurrentArgs &p) {
   else if (p.state_out_dense) dst = p.state_out_dense + ((size_t)n * p.H + h) * kD * kD;
   if (dst) {
 #pragma unroll
-    for (int i = 0; i < kRows; ++i)
-      *reinterpret_cast<float4 *>(dst + (size_t)(row0 + i) * kD + col0) =
-          make_float4(S[i][0], S[i][1], S[i][2], S[i][3]);
+    for (int i = 0; i < kRows; ++i) store_vc<kVC, false>(dst + (size_t)(row0 + i) * kD + vcol, S[i]);
   }
 }
 
-template <bool kConv, bool kNorm>
+template <bool kConv, bool kNorm, int kP>
 __global__ void __launch_bounds__(kThreads, 2) recurrent_kernel(RecurrentArgs p) {
-  recurrent_item<kConv, kNorm>(p);
+  recurrent_item<kConv, kNorm, kP>(p);
   if (p.done_counter) {
     // launched as a programmatic dependent of the grid before it, which it does not read from: the CTA that
     // finishes last waits for that grid's completion, so this grid's completion implies it for whatever the
@@ -269,16 +312,17 @@ __global__ void __launch_bounds__(kThreads, 2) recurrent_kernel(RecurrentArgs p)
 
 }  // namespace
 
-template <bool kConv, bool kNorm>
+template <bool kConv, bool kNorm, int kP>
 cudaError_t launch_variant(const RecurrentArgs &args, int num_items, cudaStream_t stream) {
+  const unsigned grid = static_cast<unsigned>(num_items) * args.H * kP;
   if (!args.done_counter) {
-    recurrent_kernel<kConv, kNorm><<<num_items * args.H, kThreads, 0, stream>>>(args);
+    recurrent_kernel<kConv, kNorm, kP><<<grid, kThreads, 0, stream>>>(args);
     return cudaGetLastError();
   }
   // programmatic dependent launch: CTAs may be scheduled onto SMs the preceding grid leaves free once every
   // CTA of that grid has signalled launch_dependents
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(num_items * args.H);
+  cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -286,16 +330,24 @@ cudaError_t launch_variant(const RecurrentArgs &args, int num_items, cudaStream_
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, recurrent_kernel<kConv, kNorm>, args);
+  return cudaLaunchKernelEx(&cfg, recurrent_kernel<kConv, kNorm, kP>, args);
 }
 
 cudaError_t launch_recurrent(const RecurrentArgs &args, int num_items, cudaStream_t stream) {
   if (num_items <= 0) return cudaSuccess;
   const bool conv = args.conv.weight != nullptr, norm = args.norm.gate != nullptr;
-  if (conv) return norm ? launch_variant<true, true>(args, num_items, stream)
-                        : launch_variant<true, false>(args, num_items, stream);
-  return norm ? launch_variant<false, true>(args, num_items, stream)
-              : launch_variant<false, false>(args, num_items, stream);
+  if (conv) return norm ? launch_variant<true, true, 1>(args, num_items, stream)
+                        : launch_variant<true, false, 1>(args, num_items, stream);
+  if (norm) return launch_variant<false, true, 1>(args, num_items, stream);
+  // a small batch fills fewer SMs than one wave of (request, head) CTAs: split each item's value channels over
+  // 2 or 4 CTAs while the grid still fits in one wave (two CTAs per SM)
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    sms = 0;
+  const long long items = static_cast<long long>(num_items) * args.H, wave = 2LL * sms;
+  if (items * 4 <= wave) return launch_variant<false, false, 4>(args, num_items, stream);
+  if (items * 2 <= wave) return launch_variant<false, false, 2>(args, num_items, stream);
+  return launch_variant<false, false, 1>(args, num_items, stream);
 }
 
 }  // namespace kda
