@@ -8,6 +8,17 @@ Four calls, backed by libkda's CUDA kernels (``include/kda.h``):
 * :func:`spec_step` -- one speculative-decoding step: prefill segment and verify segment in one call, their
   outputs written straight into the layer's output rows by index.
 
+Optional parts of a layer step, taken by the calls above:
+
+* :class:`OutputNorm` -- sigmoid-gated RMSNorm of every output row (``norm=``);
+* :class:`ShortConv` -- short causal convolutions of q, k, v with their windows in a pool beside the state
+  pool (``conv=``; verify records per-step windows, the commit copies the accepted one);
+* :data:`KDA_PAD_SLOT_ID` -- the slot id of a padding row in a batch captured in a CUDA graph per bucket.
+
+Every call launches only on the given (or current) stream, allocates nothing beyond what the caller passes
+(the wrappers allocate missing outputs and workspaces through torch), and reports device-side problems
+through the workspace's status word (:func:`read_device_status`).
+
 The binding is loaded on first use and raises if libkda has not been built.
 """
 from ._binding import (  # noqa: F401
