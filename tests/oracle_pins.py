@@ -375,13 +375,15 @@ def pin_short_conv_step(O):
     the window ends holding the last W-1 inputs (oldest first)."""
     rng = np.random.default_rng(41)
     d, W, T = 6, 4, 23
+    # impulse at t = 0 from a zero window: y_t = w[:, Wi-1-t], for the kernels' width and others
+    for Wi in (1, 2, 3, 4, 5):
+        wi = rng.standard_normal((d, Wi))
+        win = np.zeros((Wi - 1, d))
+        for t in range(Wi + 2):
+            x = np.ones(d) if t == 0 else np.zeros(d)
+            y, win = O.conv_step(win, x, wi, False)
+            _close(y, wi[:, Wi - 1 - t] if t < Wi else np.zeros(d), 1e-15, f"W = {Wi}: impulse response at t = {t}")
     w = rng.standard_normal((d, W))
-    # impulse at t = 0 from a zero window: y_t = w[:, W-1-t]
-    win = np.zeros((W - 1, d))
-    for t in range(W + 2):
-        x = np.ones(d) if t == 0 else np.zeros(d)
-        y, win = O.conv_step(win, x, w, False)
-        _close(y, w[:, W - 1 - t] if t < W else np.zeros(d), 1e-15, f"impulse response at t = {t}")
     # a random signal, zero window: numpy convolve with reversed taps; SiLU on top
     xs = rng.standard_normal((T, d))
     for silu in (False, True):
