@@ -264,3 +264,14 @@ def test_spec_step_with_short_conv_and_gated_norm():
     check_state(dev.pool[pslots], p_S, "prefill final states, convolutions + norm")
     assert np.array_equal(widen_bf16(conv.window_pool[pslots]), p_win)
     assert np.array_equal(widen_bf16(conv.step_windows), v_win)
+
+
+def test_prefill_with_short_conv_over_several_launch_groups():
+    # 1100 short sequences (two launch groups of <= 1024): each group's first chunks find their slots' windows
+    # through the group's sequence offset, and each sequence's final window lands in its own slot
+    rng = np.random.default_rng(770)
+    lens = [int(x) for x in rng.integers(0, 40, size=1100)]
+    inp = inputs.prefill_inputs("conv_many_seqs", lens, 2, seed=771, pool_slots=1100, load_initial=True,
+                                final_to_pool=True)
+    inp.conv = inputs.conv_inputs(2, 1100, seed=772)
+    _prefill_with_conv(inp)
