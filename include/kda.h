@@ -109,6 +109,9 @@ typedef struct kda_token_tensors {
  * it to its fp32 output in its epilogue; the prefill's rows are normalised
  * from their stored bf16 values by one more row-parallel kernel after the
  * state pass (on every SM, at HBM speed), which the call launches last.
+ * Caller-owned device memory; gate and weight 16-byte aligned, rstd 4-byte;
+ * a NULL gate or weight, a bad alignment or stride, or eps < 0 / NaN returns
+ * KDA_ERR_INVALID_ARG before anything is launched.
  */
 typedef struct kda_output_norm {
   const uint16_t *gate;          /* [rows, H, 128] bf16, row = the output row; token stride below */
@@ -130,6 +133,12 @@ typedef struct kda_output_norm {
  * inputs, oldest first, kept per pool slot beside the recurrent state.  The
  * pages print neither the width nor the activation: width 4 and SiLU are the
  * readings taken (the activation is selectable).
+ * Caller-owned device memory, every pointer 16-byte aligned.  A NULL or
+ * misaligned weight, an unknown activation, or a buffer the call needs that is
+ * NULL or misaligned (the pool when the call reads or writes windows there,
+ * window_dense for dense final states, step_windows for verify and commit)
+ * returns KDA_ERR_INVALID_ARG before anything is launched.  Pool slots outside
+ * [0, num_slots) behave as for the recurrent state (skipped, status bit).
  */
 #define KDA_CONV_NONE 0
 #define KDA_CONV_SILU 1
