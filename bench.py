@@ -11,8 +11,12 @@ timed region), the verify call on 64 requests x 8, 4 and 1 tokens and the
 accept/commit after it (each captured in a CUDA graph and replayed, the way a
 serving step runs them), one speculative-decoding step (a 4 x 2048-token
 prefill segment beside 64 verify requests x 4 tokens, every output row stored
-by index into the layer output), and the fp64 CPU oracle on a bounded sample
-of the prefill workload.
+by index into the layer output), the other prefill workloads (1 x 256 at H=2,
+4 x 8192, and 16384 + 16 varlen sequences with its long sequence also timed
+alone) as their own calls, and the fp64 CPU oracle on each workload (bounded
+samples where the whole would take long).  Per-call times are CUDA events on
+the launching stream and the reported per-layer figures are their median; SM
+clocks are sampled through NVML inside the timed region.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 N > 1 runs under torchrun, one replica per GPU (weak scaling, no collective on
@@ -113,32 +117,97 @@ def recorded_traffic(kind):
         return None
 
 
+class _Nvml:
+    """NVML through ctypes (reads only): SM clock, its maximum and the active clock-event reasons."""
+
+    # nvmlClocksEventReasons bits (nvml.h)
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown"}
+    CLOCK_SM = 1
+
+    def __init__(self, uuid):
+        import ctypes
+        self.ct = ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        if lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(self.h)) != 0:
+            raise OSError(f"no NVML device {uuid}")
+        self.reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        self.lib = lib
+        v = ctypes.c_uint(0)
+        lib.nvmlDeviceGetMaxClockInfo(self.h, self.CLOCK_SM, ctypes.byref(v))
+        self.max_mhz = float(v.value)
+
+    def sample(self):
+        ct = self.ct
+        clk = ct.c_uint(0)
+        rs = ct.c_ulonglong(0)
+        if self.lib.nvmlDeviceGetClockInfo(self.h, self.CLOCK_SM, ct.byref(clk)) != 0:
+            return None
+        self.reasons_fn(self.h, ct.byref(rs))
+        return float(clk.value), self.max_mhz, [n for bit, n in self.REASONS.items() if rs.value & bit]
+
+
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    """SM clock and throttle reasons sampled while running: through NVML every 0.5 ms (so that samples land
+    inside even a few-millisecond timed region), else nvidia-smi every 50 ms."""
 
     FIELDS = "clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown," \
              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown," \
              "clocks_event_reasons.sw_power_cap"
+    SMI_NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
     def __init__(self, device_index):
         self.device_index = device_index
-        self.samples = []
+        self.samples = []   # (time, sm_mhz, sm_max_mhz, [reasons])
         self.proc = None
+        self.nvml = None
+        self.running = False
         self.t0 = self.t1 = None
+        self.source = None
 
     def start(self):
+        try:
+            import torch
+            uuid = "GPU-" + str(torch.cuda.get_device_properties(self.device_index).uuid)
+            self.nvml = _Nvml(uuid)
+            self.source = "nvml, 0.5 ms"
+        except Exception:
+            self.nvml = None
+        self.running = True
+        if self.nvml is not None:
+            threading.Thread(target=self._poll, daemon=True).start()
+            return
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50",
                  "-i", str(self.device_index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.source = "nvidia-smi, 50 ms"
         except OSError:
             self.proc = None
             return
         threading.Thread(target=self._read, daemon=True).start()
 
+    def _poll(self):
+        while self.running:
+            s = self.nvml.sample()
+            if s is not None:
+                self.samples.append((time.time(), *s))
+            time.sleep(0.0005)
+
     def _read(self):
         for line in self.proc.stdout:
-            self.samples.append((time.time(), line.strip()))
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                reasons = [self.SMI_NAMES[i] for i, v in enumerate(parts[3:7]) if v.lower() == "active"]
+                self.samples.append((time.time(), float(parts[0]), float(parts[1]), reasons))
+            except ValueError:
+                continue
 
     def mark(self, which):
         if which == "begin":
@@ -147,31 +216,23 @@ class ClockSampler:
             self.t1 = time.time()
 
     def stop(self):
-        if self.proc is None:
-            return None
-        time.sleep(0.1)
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-        rows = []
-        for ts, line in self.samples:
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 7:
-                continue
+        self.running = False
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
             try:
-                rows.append((ts, float(parts[0]), float(parts[1]), parts[3:7]))
-            except ValueError:
-                continue
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        time.sleep(0.01)
+        rows = list(self.samples)
         inside = [r for r in rows if self.t0 and self.t1 and self.t0 <= r[0] <= self.t1]
         use = inside or rows
         if not use:
             return None
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in use for i, v in enumerate(r[3]) if v.lower() == "active"})
+        reasons = sorted({n for r in use for n in r[3]})
         return {"sm_mhz": statistics.median(r[1] for r in use), "sm_max_mhz": max(r[2] for r in use),
-                "reasons": reasons, "samples": len(use), "in_timed_region": bool(inside)}
+                "reasons": reasons, "samples": len(use), "in_timed_region": bool(inside), "source": self.source}
 
 
 def dist_setup(n_gpus):
@@ -209,39 +270,54 @@ def max_over_ranks(x, world, device=None):
 # ---------------------------------------------------------------------------
 
 def oracle_sample_rate(inp, seqs, tokens, nthreads):
-    """Run the oracle on `seqs` sequences x all heads, first `tokens` tokens each;
-    return (token-rows processed, seconds)."""
+    """Run the oracle on the first `seqs` sequences x all heads, the first `tokens` tokens of each (fewer where a
+    sequence is shorter); return (token-rows processed, seconds)."""
     import numpy as np
     import oracle
 
     starts = inp.cu_seqlens[:seqs]
-    rows = np.concatenate([np.arange(s, s + tokens) for s in starts])
-    cu = (np.arange(seqs + 1) * tokens).astype(np.int32)
+    lens = [min(tokens, int(inp.cu_seqlens[i + 1] - inp.cu_seqlens[i])) for i in range(seqs)]
+    rows = np.concatenate([np.arange(s, s + n) for s, n in zip(starts, lens)])
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
     S0 = inp.initial_states()[:seqs] if inp.load_initial else None
     t0 = time.perf_counter()
     oracle.run(inp.q[rows], inp.k[rows], inp.v[rows], inp.g[rows], inp.beta[rows], inp.A_log, inp.dt_bias,
                inp.lower_bound, inp.scale, cu, S0=S0, nthreads=nthreads)
-    return seqs * tokens, time.perf_counter() - t0
+    return int(cu[-1]), time.perf_counter() - t0
 
 
 def cpu_baseline(inp, budget_s=30.0):
-    """The oracle on the host cores: the whole workload (all sequences and heads),
-    shortened per sequence only if a calibration run predicts more than
-    `budget_s` seconds of CPU work."""
+    """The oracle on the host cores: the whole workload (all sequences and heads), shortened per sequence only if
+    a calibration run predicts more than `budget_s` seconds of wall time on those cores."""
     import oracle
 
     oracle.build()
     nthreads = oracle.default_threads()
     seqs = inp.num_seqs
-    full = int(inp.cu_seqlens[1] - inp.cu_seqlens[0])
+    longest = int(max(inp.cu_seqlens[1:] - inp.cu_seqlens[:-1]))
     tok, dt = oracle_sample_rate(inp, seqs, 64, nthreads)  # calibration
-    core_s_per_token = dt * nthreads / tok
-    tokens = int(min(full, max(64, budget_s / core_s_per_token / seqs)))
+    wall_s_per_token = dt / tok
+    tokens = int(min(longest, max(64, budget_s / wall_s_per_token / seqs)))
     tok, dt = oracle_sample_rate(inp, seqs, tokens, nthreads)
-    what = "the whole workload" if tokens == full else f"first {tokens} tokens of each sequence"
+    what = "the whole workload" if tokens >= longest else f"first {tokens} tokens of each sequence"
     return {"value": tok / dt, "unit": "tokens/s", "cores": nthreads, "kind": "oracle",
-            "sample": f"{what}: {seqs} sequences x all {inp.H} heads, fp64 token-by-token, "
+            "us_per_layer_equiv": dt * 1e6 * inp.total_tokens / tok,
+            "sample": f"{what}: {seqs} sequences x all {inp.H} heads ({tok} tokens), fp64 token-by-token, "
                       f"{dt:.2f} s wall on {nthreads} threads (~{dt * nthreads:.0f} core-s)"}
+
+
+def cpu_baseline_verify(inp):
+    """The oracle on a verify workload (every request and head, every per-step state recorded)."""
+    import oracle
+
+    oracle.build()
+    nthreads = oracle.default_threads()
+    t0 = time.perf_counter()
+    oracle.run_verify(inp, nthreads=nthreads)
+    dt = time.perf_counter() - t0
+    return {"value": dt * 1e6, "unit": "us/layer", "cores": nthreads, "kind": "oracle",
+            "sample": f"the whole workload: {inp.B} requests x {inp.T} tokens x all {inp.H} heads with every "
+                      f"per-step state, fp64 token-by-token, {dt:.2f} s wall on {nthreads} threads"}
 
 
 def run_reference(args):
@@ -287,10 +363,9 @@ def run_gpu(args):
 
     rank, world, local = dist_setup(args.gpus)
     device = torch.device("cuda", local)
-    sys.path.insert(0, os.path.join(ROOT, "tests"))
     import kda_linear_attention_bounded_gb300 as kda
     from kda_linear_attention_bounded_gb300 import inputs
-    from gpu_helpers import DevicePrefill, DeviceSpecStep, DeviceVerify, bf16_dev, f32_dev
+    from kda_linear_attention_bounded_gb300.device import DevicePrefill, DeviceSpecStep, DeviceVerify, bf16_dev, f32_dev
 
     kda.load()
     inp = inputs.prefill_2048x8()
@@ -312,6 +387,8 @@ def run_gpu(args):
     if sampler:
         sampler.start()
         time.sleep(0.2)
+    switch = sys.getswitchinterval()
+    sys.setswitchinterval(0.0002)   # lets the sampling thread run between the step launches
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     barrier(world)
@@ -328,6 +405,7 @@ def run_gpu(args):
     wall = time.perf_counter() - t_wall
     if sampler:
         sampler.mark("end")
+    sys.setswitchinterval(switch)
     per_launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     elapsed_ms = starts[0].elapsed_time(ends[-1])
     elapsed_ms = max_over_ranks(elapsed_ms, world, device)
@@ -337,9 +415,10 @@ def run_gpu(args):
     tokens_all = T * args.steps * world
     value = tokens_all / (elapsed_ms / 1e3)
     avg_launch_s = statistics.mean(per_launch_ms) / 1e3
+    med_launch_s = statistics.median(per_launch_ms) / 1e3
     peak, peak_kind = measured_peaks()
     alg = prefill_algorithmic_bytes(inp)
-    achieved = alg / avg_launch_s / 1e9
+    achieved = alg / med_launch_s / 1e9
 
     # ---- end to end through the C ABI with host buffers ----
     # Every step copies its inputs from pinned host memory, runs the call and copies its outputs back.  The
@@ -572,9 +651,69 @@ def run_gpu(args):
     s_tokens = sin.prefill.total_tokens + sin.verify.B * sin.verify.T
     del sdev, s_ws, s_out, s_inter
 
+    # ---- the other prefill workloads, each timed as its own call (median of per-call CUDA events) ----
+    def time_prefill(pinp, steps, note=None):
+        pdev = DevicePrefill(pinp, device=device)
+        pws = pdev.workspace(device)
+        pout = torch.empty((pinp.total_tokens, pinp.H, 128), dtype=torch.bfloat16, device=device)
+        pfinal = None if pinp.final_to_pool else torch.empty((pinp.num_seqs, pinp.H, 128, 128), dtype=torch.float32,
+                                                             device=device)
+
+        def call():
+            pdev.run(out=pout, final_state=pfinal, workspace=pws, stream=stream)
+
+        for _ in range(3):
+            call()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        torch.cuda.synchronize(device)
+        for a, b in ev:
+            a.record(stream)
+            call()
+            b.record(stream)
+        torch.cuda.synchronize(device)
+        assert kda.read_device_status(pws) == 0
+        us = sorted(a.elapsed_time(b) * 1e3 for a, b in ev)
+        med = statistics.median(us)
+        nbytes = prefill_algorithmic_bytes(pinp)
+        ach = nbytes / (med * 1e-6) / 1e9
+        lens = pinp.cu_seqlens[1:] - pinp.cu_seqlens[:-1]
+        rec = {"workload": pinp.name, "tokens": pinp.total_tokens, "sequences": pinp.num_seqs, "H": pinp.H,
+               "longest_sequence": int(lens.max()), "chunks_of_longest": int((lens.max() + 63) // 64),
+               "us_per_layer": med, "us_per_layer_min": us[0], "us_per_layer_max": us[-1], "calls_timed": steps,
+               "tokens_per_s": pinp.total_tokens / (med * 1e-6),
+               "roofline": {"bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak,
+                            "algorithmic_bytes": nbytes},
+               "l2": "inputs larger than L2" if nbytes > L2_BYTES else "fits in L2: launch-latency-bound"}
+        if note:
+            rec["note"] = note
+        return rec
+
+    w_steps = max(20, min(args.steps, 200))
+    workloads = {}
+    for make in (inputs.tiny_prefill, inputs.prefill_8192x4, inputs.varlen_16384_plus_16):
+        winp = make()
+        workloads[winp.name] = time_prefill(winp, w_steps)
+        if winp.name.startswith("prefill_16384"):
+            # the long sequence of this workload alone: its state recurrence is one serial chain of 256 chunks per
+            # head, the part of the workload that no number of SMs shortens (the pages quote 16384 x 1 as well)
+            n0 = int(winp.cu_seqlens[1])
+            long_inp = inputs.PrefillInputs(
+                name="prefill_16384x1_h16 (the long sequence of prefill_16384+16varlen_h16 alone)",
+                q=winp.q[:n0], k=winp.k[:n0], v=winp.v[:n0], g=winp.g[:n0], beta=winp.beta[:n0], A_log=winp.A_log,
+                dt_bias=winp.dt_bias, lower_bound=winp.lower_bound, scale=winp.scale,
+                cu_seqlens=winp.cu_seqlens[:2].copy())
+            rec = time_prefill(long_inp, w_steps)
+            rec["us_per_chunk"] = rec["us_per_layer"] / rec["chunks_of_longest"]
+            workloads[winp.name]["long_sequence"] = rec
+        if rank == 0 and not args.no_cpu_baseline and world == 1:
+            workloads[winp.name]["cpu_baseline"] = cpu_baseline(winp, budget_s=5.0)
+        del winp
+
     if rank != 0:
         return
-    cpu = None if args.no_cpu_baseline or world > 1 else cpu_baseline(inp)
+    cpu = None if args.no_cpu_baseline or world > 1 else cpu_baseline(inp, budget_s=10.0)
+    if cpu is not None:
+        vrec["cpu_baseline"] = cpu_baseline_verify(vin)
     traffic = recorded_traffic("prefill")
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
@@ -587,7 +726,8 @@ def run_gpu(args):
                    "parallelism": f"replicas x{world}",
                    "vs_baseline_ref": "FlashKDA 49 us/layer at T=2048x8 on GB300 (vLLM PR #55737), context only"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": traffic, "algorithmic_bytes": alg, "avg_launch_us": avg_launch_s * 1e6,
+                     "traffic": traffic, "algorithmic_bytes": alg, "median_launch_us": med_launch_s * 1e6,
+                     "avg_launch_us": avg_launch_s * 1e6,
                      "kernels": "chunk_intra_kernel + chunk_chain_kernel (one prefill call)",
                      "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else peak_kind},
         "cpu_baseline": cpu,
@@ -597,6 +737,7 @@ def run_gpu(args):
                               "streams overlap step i's call (double-buffered device buffers)"},
         "gpu_launches": 2 * args.steps,
         "clocks": clocks,
+        "workloads": workloads,
         "verify": vrec,
         "verify_variants": vvariants,
         "spec_step": {"workload": sin.name, "us_per_layer": s_us, "steps": s_steps, "tokens": s_tokens,

@@ -353,9 +353,12 @@ KDA_API int kda_spec_step(const kda_token_tensors *prefill, const int32_t *cu_se
  *  - The first call on a device looks up the array's device address (with
  *    that device current) and caches it; make that first call before any
  *    stream capture.
- *  - Every call shares the one array: the call clears the status word first,
- *    and calls whose work overlaps on the GPU (different streams, no ordering)
- *    race on it.  Slot ids outside [0, num_slots) are skipped as in
+ *  - The arguments are checked on the host first, exactly as
+ *    kda_recurrent_verify checks them; a rejected call returns its status and
+ *    queues nothing on the stream.
+ *  - Every call shares the one array: an accepted call clears the status word
+ *    (one memset on the stream) before its kernel, and calls whose work
+ *    overlaps on the GPU (different streams, no ordering) race on it.  Slot ids outside [0, num_slots) are skipped as in
  *    kda_recurrent_verify, but this entry point does not report them.
  */
 KDA_API int kda_recurrent_verify_noalloc(const uint16_t *q, const uint16_t *k, const uint16_t *v,

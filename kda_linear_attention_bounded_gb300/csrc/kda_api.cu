@@ -186,6 +186,18 @@ cudaError_t launch_prefill_norm(const kda::ChunkArgs &a, cudaStream_t stream) {
 
 }  // namespace
 
+int kda::check_verify_call(const uint16_t *q, const uint16_t *k, const uint16_t *v, int64_t qkv_token_stride,
+                           const uint16_t *g, int64_t g_token_stride, const uint16_t *beta_logits,
+                           int64_t beta_token_stride, const float *A_log, const float *dt_bias, float lower_bound,
+                           float scale, int B, int T, int H, const float *state_pool, int num_slots,
+                           const int32_t *slot_ids, uint16_t *out, int64_t out_token_stride,
+                           float *intermediate_states, void *workspace, size_t workspace_bytes) {
+  kda::RecurrentArgs a;
+  return prepare_verify(q, k, v, qkv_token_stride, g, g_token_stride, beta_logits, beta_token_stride, A_log, dt_bias,
+                        lower_bound, scale, B, T, H, state_pool, num_slots, slot_ids, out, out_token_stride, nullptr,
+                        nullptr, intermediate_states, workspace, workspace_bytes, &a);
+}
+
 extern "C" {
 
 const char *kda_status_string(int status) {

@@ -62,6 +62,15 @@ constexpr size_t kDoneCounterOffset = 128;
 
 cudaError_t launch_recurrent(const RecurrentArgs &args, int num_items, cudaStream_t stream);
 
+// Host-side checks of one kda_recurrent_verify call without launching anything (the checks the call itself makes
+// first); returns KDA_OK or the status the call would return.
+int check_verify_call(const uint16_t *q, const uint16_t *k, const uint16_t *v, int64_t qkv_token_stride,
+                      const uint16_t *g, int64_t g_token_stride, const uint16_t *beta_logits,
+                      int64_t beta_token_stride, const float *A_log, const float *dt_bias, float lower_bound,
+                      float scale, int B, int T, int H, const float *state_pool, int num_slots,
+                      const int32_t *slot_ids, uint16_t *out, int64_t out_token_stride, float *intermediate_states,
+                      void *workspace, size_t workspace_bytes);
+
 // Arguments of the chunked prefill kernel.
 struct ChunkArgs {
   const uint16_t *q, *k, *v, *g, *beta;

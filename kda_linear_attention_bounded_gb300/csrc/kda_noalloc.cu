@@ -57,6 +57,12 @@ extern "C" int kda_recurrent_verify_noalloc(const uint16_t *q, const uint16_t *k
   if (need > kNoAllocScratchBytes) return KDA_ERR_WORKSPACE;  // built-in scratch too small for this build
   void *scratch = nullptr;
   if (int rc = noalloc_scratch(&scratch)) return rc;
+  // Every argument is checked before anything is queued on the stream: a rejected call adds no device work.
+  if (int rc = kda::check_verify_call(q, k, v, qkv_token_stride, g, g_token_stride, beta_logits, beta_token_stride,
+                                      A_log, dt_bias, lower_bound, scale, B, T, H, state_pool, num_slots, slot_ids,
+                                      out, out_token_stride, intermediate_states, scratch, kNoAllocScratchBytes))
+    return rc;
+  if (B == 0) return KDA_OK;
   // The array keeps whatever the previous call left; the status word must start at zero.
   if (cudaMemsetAsync(scratch, 0, need, static_cast<cudaStream_t>(stream)) != cudaSuccess) return KDA_ERR_CUDA;
   return kda_recurrent_verify(q, k, v, qkv_token_stride, g, g_token_stride, beta_logits, beta_token_stride, A_log,

@@ -2,29 +2,21 @@
 call the library through its binding, and compare against the oracle."""
 from __future__ import annotations
 
+import json
+import os
+
 import numpy as np
 import torch
 
 import kda_linear_attention_bounded_gb300 as kda
+from kda_linear_attention_bounded_gb300.device import (  # noqa: F401  (re-exported for the tests)
+    DevicePrefill, DeviceSpecStep, DeviceVerify, bf16_dev, f32_dev, i32_dev)
 
 # Tolerances of the parity bar (outputs vs the fp64 oracle after the GPU's bf16
 # rounding; states in fp32).
 OUT_REL_L2 = 1e-2
 OUT_MAX_ABS = 3e-2
 STATE_REL_L2 = 5e-3
-
-
-def bf16_dev(bits: np.ndarray, device="cuda") -> torch.Tensor:
-    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16))
-    return t.to(device).view(torch.bfloat16)
-
-
-def f32_dev(x: np.ndarray, device="cuda") -> torch.Tensor:
-    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(device)
-
-
-def i32_dev(x: np.ndarray, device="cuda") -> torch.Tensor:
-    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.int32)).to(device)
 
 
 def rel_l2(x, ref):
@@ -34,112 +26,91 @@ def rel_l2(x, ref):
     return float(np.linalg.norm(x - ref) / den) if den > 0 else float(np.linalg.norm(x))
 
 
-def check_out(out_gpu, out_ref, what):
-    x = out_gpu.float().cpu().numpy().astype(np.float64) if torch.is_tensor(out_gpu) else out_gpu
+# The bar for the worst single (sequence or request, head) pair: twice the tensor-wide bar.  A tensor-wide
+# figure alone hides one bad pair among many (one pair at 10x the bar moves the tensor-wide rel-L2 of 128 pairs
+# by under 1x); the factor 2 leaves room for the spread of a pair's error around the tensor-wide value.
+PAIR_FACTOR = 2.0
+
+# Where each check appends its figures (one JSON line per check), when set: the margins table is built from it.
+_LOG = os.environ.get("KDA_PARITY_LOG")
+
+
+def _log(kind, what, **fig):
+    if _LOG:
+        with open(_LOG, "a") as f:
+            f.write(json.dumps({"kind": kind, "what": what, **fig}) + "\n")
+
+
+def _pair_rel(err2, ref2):
+    """Per-pair rel-L2 from per-pair sums of squared errors and of squared reference values; a pair whose
+    reference is zero reports its absolute error norm."""
+    err2 = np.asarray(err2, dtype=np.float64)
+    ref2 = np.asarray(ref2, dtype=np.float64)
+    out = np.sqrt(err2)
+    nz = ref2 > 0
+    out[nz] = np.sqrt(err2[nz] / ref2[nz])
+    return out
+
+
+def _token_segments(rows, segments):
+    """[start, end) row ranges of the pairs' sequences: ``segments`` is a cu_seqlens array (prefill rows in token
+    order), an int T (verify: consecutive blocks of T rows), or None (all rows one segment)."""
+    if segments is None:
+        return [(0, rows)]
+    if isinstance(segments, (int, np.integer)):
+        T = int(segments)
+        return [(b * T, (b + 1) * T) for b in range(rows // T)]
+    cu = np.asarray(segments, dtype=np.int64)
+    return [(int(a), int(b)) for a, b in zip(cu[:-1], cu[1:]) if b > a]
+
+
+def check_out(out_gpu, out_ref, what, segments=None):
+    """Outputs ``[rows, H, d]`` against the oracle: tensor-wide rel-L2 and max-abs, and the rel-L2 of every
+    (segment, head) pair (``segments`` as in ``_token_segments``), the worst within ``PAIR_FACTOR`` x the bar."""
+    x = out_gpu.float().cpu().numpy().astype(np.float64) if torch.is_tensor(out_gpu) else np.asarray(out_gpu, np.float64)
+    ref = np.asarray(out_ref, dtype=np.float64)
     assert np.isfinite(x).all(), f"{what}: non-finite GPU output"
-    r = rel_l2(x, out_ref)
-    m = float(np.abs(x - out_ref).max()) if x.size else 0.0
-    assert r <= OUT_REL_L2 and m <= OUT_MAX_ABS, f"{what}: rel-L2 {r:.3e} (<= {OUT_REL_L2}), max-abs {m:.3e} (<= {OUT_MAX_ABS})"
+    r = rel_l2(x, ref)
+    m = float(np.abs(x - ref).max()) if x.size else 0.0
+    worst = (0.0, None)
+    if x.size and x.ndim == 3:
+        d2 = ((x - ref) ** 2).sum(axis=2)      # [rows, H]
+        r2 = (ref ** 2).sum(axis=2)
+        for (a, b) in _token_segments(x.shape[0], segments):
+            pr = _pair_rel(d2[a:b].sum(axis=0), r2[a:b].sum(axis=0))
+            h = int(np.argmax(pr))
+            if pr[h] > worst[0]:
+                worst = (float(pr[h]), (a, b, h))
+    _log("out", what, rel_l2=r, max_abs=m, worst_pair=worst[0], worst_at=worst[1])
+    assert r <= OUT_REL_L2 and m <= OUT_MAX_ABS, (
+        f"{what}: rel-L2 {r:.3e} (<= {OUT_REL_L2}), max-abs {m:.3e} (<= {OUT_MAX_ABS}); "
+        f"worst (rows, head) {worst[1]}: {worst[0]:.3e}")
+    assert worst[0] <= PAIR_FACTOR * OUT_REL_L2, (
+        f"{what}: worst (rows, head) pair {worst[1]} rel-L2 {worst[0]:.3e} (<= {PAIR_FACTOR * OUT_REL_L2}); "
+        f"tensor-wide {r:.3e}")
     return r, m
 
 
 def check_state(s_gpu, s_ref, what):
-    x = s_gpu.cpu().numpy().astype(np.float64) if torch.is_tensor(s_gpu) else s_gpu
+    """States against the oracle: tensor-wide rel-L2 and the rel-L2 of every (sequence or request, head) pair,
+    the worst within ``PAIR_FACTOR`` x the bar.  Shapes: ``[N, H, d, d]`` (final states; pair (n, h)),
+    ``[B, T, H, d, d]`` (per-step states; pair (b, h) over its T steps), ``[H, d, d]`` or ``[d, d]``."""
+    x = s_gpu.cpu().numpy().astype(np.float64) if torch.is_tensor(s_gpu) else np.asarray(s_gpu, np.float64)
+    ref = np.asarray(s_ref, dtype=np.float64)
     assert np.isfinite(x).all(), f"{what}: non-finite GPU state"
-    r = rel_l2(x, s_ref)
-    assert r <= STATE_REL_L2, f"{what}: rel-L2 {r:.3e} (<= {STATE_REL_L2})"
+    r = rel_l2(x, ref)
+    d2, r2 = (x - ref) ** 2, ref ** 2
+    axes = {5: (1, 3, 4), 4: (2, 3), 3: (1, 2), 2: (0, 1)}.get(x.ndim)
+    worst, at = 0.0, None
+    if axes is not None and x.size:
+        pr = _pair_rel(d2.sum(axis=axes), r2.sum(axis=axes))
+        idx = np.unravel_index(int(np.argmax(pr)), pr.shape) if pr.ndim else ()
+        worst, at = float(np.max(pr)), tuple(int(i) for i in idx)
+    _log("state", what, rel_l2=r, worst_pair=worst, worst_at=at)
+    assert r <= STATE_REL_L2, f"{what}: rel-L2 {r:.3e} (<= {STATE_REL_L2}); worst pair {at}: {worst:.3e}"
+    assert worst <= PAIR_FACTOR * STATE_REL_L2, (
+        f"{what}: worst pair {at} rel-L2 {worst:.3e} (<= {PAIR_FACTOR * STATE_REL_L2}); tensor-wide {r:.3e}")
     return r
-
-
-class DevicePrefill:
-    """Device copies of one prefill workload (``inputs.PrefillInputs``)."""
-
-    def __init__(self, inp, device="cuda", token_pad=0):
-        self.inp = inp
-        H = inp.H
-        T = inp.total_tokens
-
-        def tok(bits):
-            if token_pad == 0:
-                return bf16_dev(bits, device)
-            # token stride larger than H*128: embed in a wider row
-            buf = torch.zeros((T, H * 128 + token_pad), dtype=torch.bfloat16, device=device)
-            buf[:, :H * 128] = bf16_dev(bits, device).reshape(T, H * 128)
-            return buf[:, :H * 128].view(T, H, 128)
-
-        self.q, self.k, self.v, self.g = tok(inp.q), tok(inp.k), tok(inp.v), tok(inp.g)
-        self.beta = bf16_dev(inp.beta, device)
-        self.A_log = f32_dev(inp.A_log, device)
-        self.dt_bias = f32_dev(inp.dt_bias, device)
-        self.cu = i32_dev(inp.cu_seqlens, device)
-        self.cu_host = torch.from_numpy(inp.cu_seqlens.astype(np.int32))
-        self.pool = f32_dev(inp.pool, device) if inp.pool is not None else None
-        self.slots = i32_dev(inp.slot_ids, device) if inp.slot_ids is not None else None
-
-    def workspace(self, device="cuda"):
-        inp = self.inp
-        return kda.make_workspace(device, nbytes=kda.prefill_workspace_size(inp.total_tokens, inp.num_seqs, inp.H))
-
-    def run(self, **kw):
-        inp = self.inp
-        return kda.chunk_prefill(self.q, self.k, self.v, self.g, self.beta, self.A_log, self.dt_bias, self.cu,
-                                 self.cu_host, lower_bound=inp.lower_bound, scale=inp.scale,
-                                 state_pool=self.pool, slot_ids=self.slots, load_initial=inp.load_initial,
-                                 final_to_pool=inp.final_to_pool, **kw)
-
-
-class DeviceVerify:
-    def __init__(self, inp, device="cuda"):
-        self.inp = inp
-        self.q, self.k, self.v, self.g = (bf16_dev(x, device) for x in (inp.q, inp.k, inp.v, inp.g))
-        self.beta = bf16_dev(inp.beta, device)
-        self.A_log = f32_dev(inp.A_log, device)
-        self.dt_bias = f32_dev(inp.dt_bias, device)
-        self.pool = f32_dev(inp.pool, device)
-        self.slots = i32_dev(inp.slot_ids, device)
-
-    def run(self, **kw):
-        inp = self.inp
-        return kda.recurrent_verify(self.q, self.k, self.v, self.g, self.beta, self.A_log, self.dt_bias, self.pool,
-                                    self.slots, inp.T, lower_bound=inp.lower_bound, scale=inp.scale, **kw)
-
-
-class DeviceSpecStep:
-    """Device copies of one spec step (``inputs.SpecStepInputs``): both segments read the one pool and the
-    one set of head parameters."""
-
-    SENTINEL = 5.0   # value of output rows that belong to no token
-
-    def __init__(self, inp, device="cuda"):
-        self.inp = inp
-        self.pre = DevicePrefill(inp.prefill, device)
-        self.ver = DeviceVerify(inp.verify, device)
-        self.pool = self.pre.pool
-        self.ver.pool = self.pool
-        self.ns_idx = i32_dev(inp.non_spec_token_indx, device)
-        self.s_idx = i32_dev(inp.spec_token_indx, device)
-        self.device = device
-
-    def workspace(self):
-        p = self.inp.prefill
-        return kda.make_workspace(self.device, nbytes=kda.prefill_workspace_size(p.total_tokens, p.num_seqs, p.H))
-
-    def new_out(self):
-        return torch.full((self.inp.num_out_tokens, self.inp.H, 128), self.SENTINEL, dtype=torch.bfloat16,
-                          device=self.device)
-
-    def run(self, out=None, **kw):
-        inp, pre, ver = self.inp, self.pre, self.ver
-        p, v = inp.prefill, inp.verify
-        if out is None:
-            out = self.new_out()
-        has_pre, has_spec = p.num_seqs > 0, v.B > 0
-        return kda.spec_step(
-            (pre.q, pre.k, pre.v, pre.g, pre.beta) if has_pre else None, pre.cu, pre.cu_host,
-            (ver.q, ver.k, ver.v, ver.g, ver.beta) if has_spec else None, v.T, pre.A_log, pre.dt_bias, self.pool,
-            out, self.ns_idx, self.s_idx, prefill_slot_ids=pre.slots, spec_slot_ids=ver.slots,
-            load_initial=p.load_initial, final_to_pool=p.final_to_pool, lower_bound=p.lower_bound, scale=p.scale,
-            **kw)
 
 
 def device_norm(ni, H, rows=None, device="cuda", with_rstd=True):

@@ -23,7 +23,7 @@ def _verify_with_conv(inp, heads=None):
     assert torch.equal(conv.window_pool, pool_before), "verify must not write the window pool"
     ref_out, ref_steps, ref_win = oracle.run_verify(inp, heads=heads)
     hb, he = heads if heads else (0, inp.H)
-    check_out(out[:, hb:he], ref_out[:, hb:he], f"{inp.name} outputs with the convolutions")
+    check_out(out[:, hb:he], ref_out[:, hb:he], f"{inp.name} outputs with the convolutions", segments=inp.T)
     check_state(inter[:, :, hb:he], ref_steps[:, :, hb:he], f"{inp.name} per-step states with the convolutions")
     got = widen_bf16(conv.step_windows)
     assert np.array_equal(got[..., hb:he, :], ref_win[..., hb:he, :]), "per-step windows differ from the oracle's"
@@ -96,7 +96,8 @@ def test_verify_then_commit_then_verify_continues_the_sequence():
             cat(first.beta, second.beta), first.A_log, first.dt_bias, first.lower_bound, first.scale,
             np.array([0, n + T], np.int32), first.conv.weight, first.conv.silu,
             win0=oracle.bf16_widen(first.conv.pool[s:s + 1]), S0=first.pool[s:s + 1])
-        check_out(out2[b * T:(b + 1) * T], ref[n:], f"request {b}: second block after committing {n} tokens")
+        check_out(out2[b * T:(b + 1) * T], ref[n:], f"request {b}: second block after committing {n} tokens",
+                  segments=T)
 
 
 def test_spec_step_verify_segment_with_short_conv():
@@ -113,7 +114,8 @@ def test_spec_step_verify_segment_with_short_conv():
     torch.cuda.synchronize()
     assert kda.read_device_status(ws) == 0
     ref_out, ref_steps, ref_win = oracle.run_verify(inp)
-    check_out(out[torch.from_numpy(rows).long().cuda()], ref_out, "spec step verify rows with the convolutions")
+    check_out(out[torch.from_numpy(rows).long().cuda()], ref_out, "spec step verify rows with the convolutions",
+              segments=inp.T)
     check_state(inter, ref_steps, "spec step per-step states with the convolutions")
     assert np.array_equal(widen_bf16(conv.step_windows), ref_win)
 
@@ -128,7 +130,7 @@ def _prefill_with_conv(inp, heads=None):
     assert kda.read_device_status(ws) == 0
     ref_out, ref_S, _, ref_win = oracle.run_prefill(inp, heads=heads)
     hb, he = heads if heads else (0, inp.H)
-    check_out(out[:, hb:he], ref_out[:, hb:he], f"{inp.name} outputs with the convolutions")
+    check_out(out[:, hb:he], ref_out[:, hb:he], f"{inp.name} outputs with the convolutions", segments=inp.cu_seqlens)
     if inp.final_to_pool:
         slots = torch.from_numpy(inp.slot_ids).long().cuda()
         check_state(dev.pool[slots][:, hb:he], ref_S[:, hb:he], f"{inp.name} final states (pool)")
@@ -190,7 +192,7 @@ def test_prefill_then_verify_continue_through_the_window():
                                           pre.lower_bound, pre.scale, np.array([0, e - a + T], np.int32),
                                           pre.conv.weight, pre.conv.silu,
                                           win0=oracle.bf16_widen(pre.conv.pool[s:s + 1]), S0=pre.pool[s:s + 1])
-        check_out(out[b * T:(b + 1) * T], ref[e - a:], f"sequence {b}: verify block after its prefill")
+        check_out(out[b * T:(b + 1) * T], ref[e - a:], f"sequence {b}: verify block after its prefill", segments=T)
 
 
 def test_spec_step_with_short_conv_both_segments():
@@ -208,8 +210,8 @@ def test_spec_step_with_short_conv_both_segments():
     v_out, v_steps, v_win = oracle.run_verify(inp.verify)
     ns = torch.from_numpy(inp.non_spec_token_indx).long().cuda()
     sp = torch.from_numpy(inp.spec_token_indx).long().cuda()
-    check_out(out[ns], p_out, "spec step prefill rows with the convolutions")
-    check_out(out[sp], v_out, "spec step verify rows with the convolutions")
+    check_out(out[ns], p_out, "spec step prefill rows with the convolutions", segments=inp.prefill.cu_seqlens)
+    check_out(out[sp], v_out, "spec step verify rows with the convolutions", segments=inp.verify.T)
     check_state(inter, v_steps, "spec step per-step states with the convolutions")
     pslots = torch.from_numpy(inp.prefill.slot_ids).long().cuda()
     check_state(dev.pool[pslots], p_S, "spec step prefill final states")
@@ -232,7 +234,7 @@ def test_prefill_with_short_conv_bad_slot():
     torch.cuda.synchronize()
     assert kda.read_device_status(ws) & kda.KDA_DEVICE_BAD_SLOT
     ref_out, ref_S, _, ref_win = oracle.run_prefill(inp)
-    check_out(out[:70], ref_out[:70], "the sequence beside a bad slot")
+    check_out(out[:70], ref_out[:70], "the sequence beside a bad slot", segments=[0, 70])
     s0 = int(inp.slot_ids[0])
     check_state(dev.pool[s0], ref_S[0], "its final state")
     assert np.array_equal(widen_bf16(conv.window_pool[s0]), ref_win[0]), "its final window"

@@ -20,7 +20,7 @@ def _parity(inp, token_pad=0, heads=None):
     assert kda.read_device_status(ws) == 0
     ref_out, ref_S, _ = oracle.run_prefill(inp, heads=heads)
     hb, he = heads or (0, inp.H)
-    check_out(out[:, hb:he], ref_out[:, hb:he], f"{inp.name} outputs")
+    check_out(out[:, hb:he], ref_out[:, hb:he], f"{inp.name} outputs", segments=inp.cu_seqlens)
     if inp.final_to_pool:
         got = dev.pool[torch.from_numpy(inp.slot_ids).long().cuda()]
         check_state(got[:, hb:he], ref_S[:, hb:he], f"{inp.name} final states (pool)")
@@ -82,7 +82,7 @@ def test_bad_slot_sets_status_and_skips():
     torch.cuda.synchronize()
     assert kda.read_device_status(ws) & kda.KDA_DEVICE_BAD_SLOT
     ref_out, ref_S, _ = oracle.run_prefill(inp)
-    check_out(out[:70], ref_out[:70], "good sequence next to a bad slot")
+    check_out(out[:70], ref_out[:70], "good sequence next to a bad slot", segments=[0, 70])
     assert (out[70:].float() == 7.0).all(), "skipped sequence must not be written"
 
 
@@ -90,6 +90,19 @@ def test_bad_slot_sets_status_and_skips():
                          ids=["2048x8", "8192x4", "16384+16varlen"])
 def test_full_size(make):
     _parity(make())
+
+
+@pytest.mark.parametrize("decay", ["weak_bound", "weak_gate"])
+@pytest.mark.parametrize("lens", [[8192] * 4, [16384]], ids=["8192x4", "16384x1"])
+def test_full_length_weak_decay(lens, decay):
+    # Weak decay over 128 or 256 chunks: with lower_bound -0.05, or the gate logits centred at -8 (lambda ~ -1e-3
+    # per step), the state keeps what enters it for thousands of tokens, so an error the state path makes in one
+    # chunk (the rounding of the state the products read, a wrong carry) reaches the final state and every later
+    # output instead of being forgotten within a few tokens as at the workloads' decay.
+    kw = dict(weak_bound=dict(lower_bound=-0.05), weak_gate=dict(g_mean=-8.0))[decay]
+    inp = inputs.prefill_inputs(f"{decay}_{len(lens)}x{lens[0]}", lens, 16, seed=90 + len(lens), pool_slots=16,
+                                load_initial=True, final_to_pool=len(lens) > 1, **kw)
+    _parity(inp)
 
 
 def test_more_sequences_than_one_launch_plans():

@@ -77,7 +77,8 @@ def _check_step(inp, heads=None):
     if p.num_seqs:
         o_out, o_final, _ = oracle.run_prefill(p, heads=(hb, he))
         if p.total_tokens:
-            check_out(out[ns][:, hb:he], o_out[:, hb:he], f"{inp.name} prefill rows heads {hb}:{he}")
+            check_out(out[ns][:, hb:he], o_out[:, hb:he], f"{inp.name} prefill rows heads {hb}:{he}",
+                      segments=p.cu_seqlens)
         if p.final_to_pool:
             slots = torch.from_numpy(p.slot_ids).long().cuda()
             check_state(dev.pool[slots][:, hb:he], o_final[:, hb:he], f"{inp.name} final states in the pool")
@@ -85,7 +86,7 @@ def _check_step(inp, heads=None):
             check_state(final[:, hb:he], o_final[:, hb:he], f"{inp.name} dense final states")
     if v.B:
         o_vout, o_steps = oracle.run_verify(v, heads=(hb, he))
-        check_out(out[sp][:, hb:he], o_vout[:, hb:he], f"{inp.name} verify rows heads {hb}:{he}")
+        check_out(out[sp][:, hb:he], o_vout[:, hb:he], f"{inp.name} verify rows heads {hb}:{he}", segments=v.T)
         check_state(inter[:, :, hb:he], o_steps[:, :, hb:he], f"{inp.name} per-step states heads {hb}:{he}")
     # slots the prefill does not write back keep their state (the verify only reads the pool)
     written = set(p.slot_ids.tolist()) if (p.num_seqs and p.final_to_pool) else set()

@@ -24,7 +24,7 @@ def _parity(inp, head_groups=1):
     for hb in range(0, H, step):
         he = hb + step
         ref_out, ref_steps = oracle.run_verify(inp, heads=(hb, he))
-        check_out(out[:, hb:he], ref_out[:, hb:he], f"{inp.name} outputs heads {hb}:{he}")
+        check_out(out[:, hb:he], ref_out[:, hb:he], f"{inp.name} outputs heads {hb}:{he}", segments=inp.T)
         check_state(inter[:, :, hb:he], ref_steps[:, :, hb:he], f"{inp.name} per-step states heads {hb}:{he}")
 
 
@@ -60,7 +60,7 @@ def test_verify_bad_slot():
     assert kda.read_device_status(ws) & kda.KDA_DEVICE_BAD_SLOT
     assert (out[:4].float() == 3.0).all()
     ref_out, ref_steps = oracle.run_verify(inp)
-    check_out(out[4:], ref_out[4:], "good request next to a bad slot")
+    check_out(out[4:], ref_out[4:], "good request next to a bad slot", segments=inp.T)
     check_state(inter[1], ref_steps[1], "good request states")
 
 
@@ -84,7 +84,7 @@ def test_verify_padding_rows_are_skipped():
         if b in pad:
             assert (out[rows].float() == 3.0).all() and (inter[b] == 7.0).all(), f"padding row {b} was written"
         else:
-            check_out(out[rows], ref_out[rows], f"live request {b}")
+            check_out(out[rows], ref_out[rows], f"live request {b}", segments=inp.T)
             check_state(inter[b], ref_steps[b], f"live request {b} states")
 
 
@@ -143,7 +143,7 @@ def test_verify_and_commit_replay_from_a_bucket_graph(T):
         assert torch.equal(inter[:live], ref_inter), f"live={live}: replayed per-step states differ"
         assert torch.equal(dev.pool, fresh.pool), f"live={live}: pool after the replayed commit differs"
         o_out, o_steps = oracle.run_verify(new)
-        check_out(out[:rows], o_out, f"bucket T={T} live={live} outputs")
+        check_out(out[:rows], o_out, f"bucket T={T} live={live} outputs", segments=T)
         check_state(inter[:live], o_steps, f"bucket T={T} live={live} per-step states")
         for b in range(live):
             s = int(new.slot_ids[b])
