@@ -83,6 +83,15 @@ extern "C" {
 /* ---- flags of kda_chunk_prefill ------------------------------------------ */
 #define KDA_LOAD_INITIAL 1  /* S0 of sequence n = state_pool[slot_ids[n]]; else S0 = 0          */
 #define KDA_FINAL_TO_POOL 2 /* final state of sequence n -> state_pool[slot_ids[n]]; else dense */
+/* Execution path of kda_chunk_prefill (at most one of the two; neither: the library picks).  Both paths
+ * compute the same result within rounding.
+ *  KDA_TWO_PASS  the intra-chunk kernel over every chunk and head, then the state pass over every
+ *                (sequence, head), the chunks' operands handed over through the workspace;
+ *  KDA_FUSED     one kernel, one CTA per (sequence, head), every chunk's operands kept on chip; it
+ *                applies without short convolutions and with lower_bound >= -5 (else the call returns
+ *                KDA_ERR_UNSUPPORTED). */
+#define KDA_TWO_PASS 4
+#define KDA_FUSED 8
 
 /*
  * q, k, v, g and beta_logits of one set of tokens, laid out as in the
@@ -210,7 +219,10 @@ KDA_API int kda_read_device_status(const void *workspace, size_t workspace_bytes
  *  workspace        at least kda_prefill_workspace_size(cu_seqlens_host[num_seqs],
  *                   num_seqs, H) bytes (KDA_ERR_WORKSPACE otherwise); its first
  *                   word is the device status word, the rest is scratch that
- *                   the call overwrites.  Concurrent calls need separate workspaces.
+ *                   the call overwrites (the fused path uses only the header).
+ *                   Concurrent calls need separate workspaces.
+ *  flags            KDA_LOAD_INITIAL | KDA_FINAL_TO_POOL, and at most one of
+ *                   KDA_TWO_PASS, KDA_FUSED; other bits: KDA_ERR_INVALID_ARG.
  */
 KDA_API int kda_chunk_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                       int64_t qkv_token_stride, const uint16_t *g, int64_t g_token_stride,

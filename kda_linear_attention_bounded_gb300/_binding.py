@@ -26,6 +26,8 @@ KDA_DEVICE_BAD_COUNT = 4
 KDA_DEVICE_BAD_INDEX = 8
 KDA_LOAD_INITIAL = 1
 KDA_FINAL_TO_POOL = 2
+KDA_TWO_PASS = 4
+KDA_FUSED = 8
 KDA_PAD_SLOT_ID = -1
 KDA_CONV_NONE = 0
 KDA_CONV_SILU = 1
@@ -220,9 +222,10 @@ def _beta_stride(b, H):
 def chunk_prefill(q, k, v, g, beta_logits, A_log, dt_bias, cu_seqlens, cu_seqlens_host, *,
                   lower_bound=-5.0, scale=None, state_pool=None, slot_ids=None, load_initial=False,
                   final_to_pool=False, out=None, final_state=None, norm=None, conv=None, workspace=None,
-                  stream=None):
+                  stream=None, path=None):
     """``kda_chunk_prefill``.  Returns ``(out, final_state)`` (final_state is None
-    when the final states go to the pool).  ``norm``: an :class:`OutputNorm` applied to the output rows."""
+    when the final states go to the pool).  ``norm``: an :class:`OutputNorm` applied to the output rows.
+    ``path``: None (the library picks), ``"two_pass"`` (``KDA_TWO_PASS``) or ``"fused"`` (``KDA_FUSED``)."""
     lib = load()
     H = q.shape[1]
     qs = _token_tensor(q, "q", H)
@@ -243,7 +246,8 @@ def chunk_prefill(q, k, v, g, beta_logits, A_log, dt_bias, cu_seqlens, cu_seqlen
         final_state = torch.empty((N, H, 128, 128), dtype=torch.float32, device=dev)
     if workspace is None:
         workspace = make_workspace(dev, stream, prefill_workspace_size(T_total, N, H))
-    flags = (KDA_LOAD_INITIAL if load_initial else 0) | (KDA_FINAL_TO_POOL if final_to_pool else 0)
+    flags = (KDA_LOAD_INITIAL if load_initial else 0) | (KDA_FINAL_TO_POOL if final_to_pool else 0) | \
+        {None: 0, "two_pass": KDA_TWO_PASS, "fused": KDA_FUSED}[path]
     if scale is None:
         scale = 1.0 / math.sqrt(128.0)
     rc = lib.kda_chunk_prefill(

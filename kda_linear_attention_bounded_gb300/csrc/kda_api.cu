@@ -91,7 +91,8 @@ int prepare_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v, int
   if (int rc = check_workspace(workspace, workspace_bytes)) return rc;
   if (num_seqs < 0) return KDA_ERR_INVALID_ARG;
   if (!cu_seqlens_dev || !cu_seqlens_host) return KDA_ERR_INVALID_ARG;
-  if (flags & ~(KDA_LOAD_INITIAL | KDA_FINAL_TO_POOL)) return KDA_ERR_INVALID_ARG;
+  if (flags & ~(KDA_LOAD_INITIAL | KDA_FINAL_TO_POOL | KDA_TWO_PASS | KDA_FUSED)) return KDA_ERR_INVALID_ARG;
+  if ((flags & KDA_TWO_PASS) && (flags & KDA_FUSED)) return KDA_ERR_INVALID_ARG;
   if (cu_seqlens_host[0] != 0) return KDA_ERR_INVALID_ARG;
   for (int n = 0; n < num_seqs; ++n)
     if (cu_seqlens_host[n + 1] < cu_seqlens_host[n]) return KDA_ERR_INVALID_ARG;
@@ -126,6 +127,10 @@ int prepare_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v, int
   a->state_out_dense = (flags & KDA_FINAL_TO_POOL) ? nullptr : final_state;
   a->out = out;
   a->status = static_cast<uint32_t *>(workspace);
+  a->path = (flags & KDA_TWO_PASS) ? kda::PrefillPath::kTwoPass
+            : (flags & KDA_FUSED)  ? kda::PrefillPath::kFused
+                                   : kda::PrefillPath::kAuto;
+  if (a->path == kda::PrefillPath::kFused && !kda::fused_prefill_applies(*a)) return KDA_ERR_UNSUPPORTED;
   return KDA_OK;
 }
 

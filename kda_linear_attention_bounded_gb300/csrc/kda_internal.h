@@ -71,6 +71,8 @@ int check_verify_call(const uint16_t *q, const uint16_t *k, const uint16_t *v, i
                       const int32_t *slot_ids, uint16_t *out, int64_t out_token_stride, float *intermediate_states,
                       void *workspace, size_t workspace_bytes);
 
+enum class PrefillPath { kAuto, kTwoPass, kFused };
+
 // Arguments of the chunked prefill kernel.
 struct ChunkArgs {
   const uint16_t *q, *k, *v, *g, *beta;
@@ -90,7 +92,11 @@ struct ChunkArgs {
   OutNorm norm;
   ShortConv conv;            // with conv.weight, q, k, v are the convolutions' raw inputs
   uint32_t *status;
+  PrefillPath path;          // forced by the caller, or picked by launch_chunk_prefill
 };
+
+// Whether the fused prefill kernel serves a call (else the intra-chunk kernel + state pass do).
+bool fused_prefill_applies(const ChunkArgs &args);
 
 // Arguments of the accept/commit copy.
 struct CommitArgs {
@@ -167,6 +173,32 @@ struct ChainParams {
   int32_t tok_off[kMaxSeqsPerLaunch + 1];
   uint16_t order[kMaxSeqsPerLaunch];          // local sequences, longest first
 };
+
+// Fused prefill: one CTA per (sequence, head) of a group builds each chunk's WY operands and runs the state
+// recurrence over them without leaving the SM (kda_prefill_fused.cu).
+struct FusedParams {
+  CUtensorMap tq, tk, tg;       // [tokens, H, 128] bf16, box 64 channels x 1 head x 64 tokens, unswizzled
+  CUtensorMap tv;               // the same for v, 128-byte swizzle (an MMA operand)
+  CUtensorMap tout;             // output, 128-byte swizzle
+  const uint16_t *beta;
+  int64_t beta_stride;
+  const float *A_log, *dt_bias;
+  float lower_bound, scale;
+  const int32_t *slot_ids;      // indexed by seq0 + local sequence
+  int num_slots;
+  const float *state_in;
+  float *state_out_pool;
+  float *state_out_dense;       // indexed by seq0 + local sequence
+  uint16_t *out;
+  int64_t out_stride;
+  uint32_t *status;
+  int H, num_seqs, seq0;
+  int32_t tok_off[kMaxSeqsPerLaunch + 1];
+  uint16_t order[kMaxSeqsPerLaunch];          // local sequences, longest first
+};
+static_assert(sizeof(FusedParams) <= 32764, "kernel parameters are limited to 32764 bytes");
+
+cudaError_t launch_prefill_fused(const FusedParams &p, cudaStream_t stream);
 
 // Gated RMSNorm of stored output rows, in place (the prefill's rows, after its state pass).
 struct GatedNormArgs {

@@ -61,8 +61,72 @@ size_t prefill_workspace_bytes(int64_t total_tokens, int num_seqs, int H) {
   return kWorkspaceHeader + chunks * static_cast<size_t>(std::max(H, 0)) * kBlkBytes;
 }
 
+bool fused_prefill_applies(const ChunkArgs &a) {
+  // the fused kernel takes the 32-row anchored sub-blocks only, writes rows in token order and has no short
+  // convolutions
+  return a.conv.weight == nullptr && a.out_index == nullptr && a.lower_bound >= -5.0f;
+}
+
+namespace {
+
+// The path the library takes when the caller does not force one: the fused kernel where it applies and is
+// expected to be faster.  Measured on GB300 (2048 x 8, 8192 x 4, 16384 + 16 varlen, H = 16) the fused kernel's
+// per-chunk producer latency keeps it behind the two-kernel path, so it is not preferred yet.
+bool fused_prefill_preferred(const ChunkArgs &a, const int32_t *cu_host) {
+  (void)cu_host;
+  return fused_prefill_applies(a) && false;
+}
+
+cudaError_t launch_fused(const ChunkArgs &a, const int32_t *cu_host, cudaStream_t stream) {
+  static FusedParams *fp = nullptr;
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!fp) fp = new FusedParams();
+  if (!make_token_map(&fp->tq, a.q, a.H, a.total_tokens, a.qkv_stride, false) ||
+      !make_token_map(&fp->tk, a.k, a.H, a.total_tokens, a.qkv_stride, false) ||
+      !make_token_map(&fp->tg, a.g, a.H, a.total_tokens, a.g_stride, false) ||
+      !make_token_map(&fp->tv, a.v, a.H, a.total_tokens, a.qkv_stride) ||
+      !make_token_map(&fp->tout, a.out, a.H, a.total_tokens, a.out_stride))
+    return cudaErrorInvalidValue;
+  fp->beta = a.beta;
+  fp->beta_stride = a.beta_stride;
+  fp->A_log = a.A_log;
+  fp->dt_bias = a.dt_bias;
+  fp->lower_bound = a.lower_bound;
+  fp->scale = a.scale;
+  fp->slot_ids = a.slot_ids;
+  fp->num_slots = a.num_slots;
+  fp->state_in = a.state_in;
+  fp->state_out_pool = a.state_out_pool;
+  fp->state_out_dense = a.state_out_dense;
+  fp->out = a.out;
+  fp->out_stride = a.out_stride;
+  fp->status = a.status;
+  fp->H = a.H;
+  std::vector<int> idx;
+  for (int s0 = 0; s0 < a.num_seqs; s0 += kMaxSeqsPerLaunch) {
+    const int ns = std::min(kMaxSeqsPerLaunch, a.num_seqs - s0);
+    for (int i = 0; i <= ns; ++i) fp->tok_off[i] = cu_host[s0 + i];
+    fp->num_seqs = ns;
+    fp->seq0 = s0;
+    idx.resize(ns);
+    std::iota(idx.begin(), idx.end(), 0);
+    std::stable_sort(idx.begin(), idx.end(), [&](int x, int y) {
+      return fp->tok_off[x + 1] - fp->tok_off[x] > fp->tok_off[y + 1] - fp->tok_off[y];
+    });
+    for (int i = 0; i < ns; ++i) fp->order[i] = static_cast<uint16_t>(idx[i]);
+    const cudaError_t e = launch_prefill_fused(*fp, stream);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace
+
 cudaError_t launch_chunk_prefill(const ChunkArgs &a, const int32_t *cu_host, uint8_t *blocks, cudaStream_t stream) {
   if (a.num_seqs <= 0) return cudaSuccess;
+  if (a.path == PrefillPath::kFused || (a.path == PrefillPath::kAuto && fused_prefill_preferred(a, cu_host)))
+    return launch_fused(a, cu_host, stream);
   // host-side staging of the (large) kernel parameter structs; copied at launch
   static IntraParams *ip = nullptr;
   static ChainParams *cp = nullptr;

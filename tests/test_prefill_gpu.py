@@ -11,11 +11,11 @@ from gpu_helpers import DevicePrefill, check_out, check_state
 pytestmark = pytest.mark.gpu
 
 
-def _parity(inp, token_pad=0, heads=None):
+def _parity(inp, token_pad=0, heads=None, path=None):
     dev = DevicePrefill(inp, token_pad=token_pad)
     pool_before = dev.pool.clone() if dev.pool is not None else None
     ws = dev.workspace()
-    out, final = dev.run(workspace=ws)
+    out, final = dev.run(workspace=ws, path=path)
     torch.cuda.synchronize()
     assert kda.read_device_status(ws) == 0
     ref_out, ref_S, _ = oracle.run_prefill(inp, heads=heads)
@@ -38,24 +38,32 @@ def test_tiny_1x256_h2():
     _parity(inputs.tiny_prefill())
 
 
+PATHS = [None, "fused"]   # the library's pick, and the fused kernel forced
+
+
+@pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("lens", [[1], [63], [64], [65], [1, 63, 64, 65, 130, 0, 200], [0, 0, 3]])
-def test_varlen_ragged_pool_in(lens):
+def test_varlen_ragged_pool_in(lens, path):
     inp = inputs.prefill_inputs("ragged", lens, 4, seed=11 + len(lens), pool_slots=16, load_initial=True)
-    _parity(inp)
+    _parity(inp, path=path)
 
 
-def test_varlen_final_to_pool_inplace():
+@pytest.mark.parametrize("path", PATHS)
+def test_varlen_final_to_pool_inplace(path):
     inp = inputs.prefill_inputs("inplace", [100, 7, 256], 3, seed=21, pool_slots=8, load_initial=True,
                                 final_to_pool=True)
-    _parity(inp)
+    _parity(inp, path=path)
 
 
+@pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("case", ["weak_gate", "weak_bound", "bound_-10", "bound_0"])
-def test_decay_regimes(case):
+def test_decay_regimes(case, path):
     kw = dict(weak_gate=dict(g_mean=-8.0), weak_bound=dict(lower_bound=-0.05),
               **{"bound_-10": dict(lower_bound=-10.0), "bound_0": dict(lower_bound=0.0)})[case]
+    if path == "fused" and case == "bound_-10":
+        pytest.skip("the fused kernel takes lower_bound >= -5")
     inp = inputs.prefill_inputs(case, [300, 77], 4, seed=31, pool_slots=4, load_initial=True, **kw)
-    _parity(inp)
+    _parity(inp, path=path)
 
 
 @pytest.mark.parametrize("lb", [-5.0, -5.1, -10.0])
@@ -65,20 +73,24 @@ def test_saturated_gate_at_the_sub_block_switch(lb):
     inp = inputs.prefill_inputs(f"saturated_{lb}", [200, 64, 33], 2, seed=35, pool_slots=4, load_initial=True,
                                 lower_bound=lb, g_mean=8.0)
     _parity(inp)
+    if lb >= -5.0:
+        _parity(inp, path="fused")
 
 
-def test_strided_token_rows():
+@pytest.mark.parametrize("path", PATHS)
+def test_strided_token_rows(path):
     inp = inputs.prefill_inputs("strided", [130, 64], 2, seed=41)
-    _parity(inp, token_pad=256)
+    _parity(inp, token_pad=256, path=path)
 
 
-def test_bad_slot_sets_status_and_skips():
+@pytest.mark.parametrize("path", PATHS)
+def test_bad_slot_sets_status_and_skips(path):
     inp = inputs.prefill_inputs("badslot", [70, 50], 2, seed=51, pool_slots=4, load_initial=True)
     dev = DevicePrefill(inp)
     dev.slots[1] = 99
     ws = dev.workspace()
     out = torch.full((inp.total_tokens, 2, 128), 7.0, dtype=torch.bfloat16, device="cuda")
-    out, final = dev.run(workspace=ws, out=out)
+    out, final = dev.run(workspace=ws, out=out, path=path)
     torch.cuda.synchronize()
     assert kda.read_device_status(ws) & kda.KDA_DEVICE_BAD_SLOT
     ref_out, ref_S, _ = oracle.run_prefill(inp)
@@ -86,15 +98,28 @@ def test_bad_slot_sets_status_and_skips():
     assert (out[70:].float() == 7.0).all(), "skipped sequence must not be written"
 
 
+@pytest.mark.parametrize("path", ["fused", "two_pass"])
 @pytest.mark.parametrize("make", [inputs.prefill_2048x8, inputs.prefill_8192x4, inputs.varlen_16384_plus_16],
                          ids=["2048x8", "8192x4", "16384+16varlen"])
-def test_full_size(make):
-    _parity(make())
+def test_full_size(make, path):
+    # the fused one-kernel path (KDA_FUSED) and the two-kernel path (KDA_TWO_PASS)
+    _parity(make(), path=path)
 
 
+@pytest.mark.parametrize("lens", [[1, 63, 64, 65, 130, 0, 200], [1000, 3, 700]])
+def test_fused_and_two_pass_paths_agree(lens):
+    # both paths on the same ragged batch: each within the bar of the oracle, and close to one another
+    inp = inputs.prefill_inputs("paths", lens, 4, seed=17, pool_slots=12, load_initial=True)
+    out_f, fin_f = _parity(inp, path="fused")
+    out_t, fin_t = _parity(inp, path="two_pass")
+    assert float((out_f.float() - out_t.float()).abs().max()) <= 3e-2
+    assert float((fin_f - fin_t).norm() / fin_t.norm()) <= 5e-3
+
+
+@pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("decay", ["weak_bound", "weak_gate"])
 @pytest.mark.parametrize("lens", [[8192] * 4, [16384]], ids=["8192x4", "16384x1"])
-def test_full_length_weak_decay(lens, decay):
+def test_full_length_weak_decay(lens, decay, path):
     # Weak decay over 128 or 256 chunks: with lower_bound -0.05, or the gate logits centred at -8 (lambda ~ -1e-3
     # per step), the state keeps what enters it for thousands of tokens, so an error the state path makes in one
     # chunk (the rounding of the state the products read, a wrong carry) reaches the final state and every later
@@ -102,16 +127,17 @@ def test_full_length_weak_decay(lens, decay):
     kw = dict(weak_bound=dict(lower_bound=-0.05), weak_gate=dict(g_mean=-8.0))[decay]
     inp = inputs.prefill_inputs(f"{decay}_{len(lens)}x{lens[0]}", lens, 16, seed=90 + len(lens), pool_slots=16,
                                 load_initial=True, final_to_pool=len(lens) > 1, **kw)
-    _parity(inp)
+    _parity(inp, path=path)
 
 
-def test_more_sequences_than_one_launch_plans():
-    # 1100 sequences: the planner splits them into two launch pairs of <= 1024 sequences
+@pytest.mark.parametrize("path", PATHS)
+def test_more_sequences_than_one_launch_plans(path):
+    # 1100 sequences: the planner splits them into two launch groups of <= 1024 sequences
     rng = np.random.default_rng(61)
     lens = [int(x) for x in rng.integers(0, 40, size=1100)]
     inp = inputs.prefill_inputs("many_seqs", lens, 2, seed=62, pool_slots=1100, load_initial=True,
                                 final_to_pool=True)
-    _parity(inp)
+    _parity(inp, path=path)
 
 
 def test_more_chunk_slots_than_one_intra_launch():
@@ -124,24 +150,25 @@ def test_more_chunk_slots_than_one_intra_launch():
     _parity(inp)
 
 
-def test_prefill_captured_in_a_cuda_graph():
+@pytest.mark.parametrize("path", PATHS)
+def test_prefill_captured_in_a_cuda_graph(path):
     # the call (intra-chunk launch + state pass as its programmatic dependent) replays from a CUDA graph with
     # the same results as a direct call
     inp = inputs.prefill_inputs("graph", [130, 64, 200, 1], 2, seed=81, pool_slots=8, load_initial=True)
     dev = DevicePrefill(inp)
     ws = dev.workspace()
-    out_ref, final_ref = dev.run(workspace=ws)
+    out_ref, final_ref = dev.run(workspace=ws, path=path)
     torch.cuda.synchronize()
     out_ref, final_ref = out_ref.clone(), final_ref.clone()
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(side):
-        dev.run(workspace=ws)
+        dev.run(workspace=ws, path=path)
     torch.cuda.current_stream().wait_stream(side)
     torch.cuda.synchronize()
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
-        out_g, final_g = dev.run(workspace=ws)
+        out_g, final_g = dev.run(workspace=ws, path=path)
     out_g.zero_()
     final_g.zero_()
     graph.replay()
