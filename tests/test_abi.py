@@ -104,7 +104,7 @@ def test_prefill_rejects_bad_arguments(lib):
     assert _prefill(lib, flags=1) == 1                 # pool + slot ids required
     assert _prefill(lib, flags=16) == 1                # unknown flag
     assert _prefill(lib, flags=4 | 8) == 1             # both execution paths forced
-    assert _prefill(lib, flags=8, lb=-6.0) == 2        # the fused path takes lower_bound >= -5 only
+    assert _prefill(lib, flags=8, lb=-6.0, ws_bytes=1 << 30) == 2   # the fused path takes lower_bound >= -5 only
     assert _prefill(lib, H=0) == 1
     assert _prefill(lib, cu=(0,)) == 0                 # no sequences: nothing to do
     # valid arguments but a workspace without room for the chunk blocks
