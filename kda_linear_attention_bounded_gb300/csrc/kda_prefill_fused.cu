@@ -20,14 +20,24 @@
 // chunk but its output rows (and the final state) leaves the SM: per token and
 // head the call moves q, k, v, g, beta and the output through HBM once.
 //
-// The producer's steps are those of the two-kernel path's intra-chunk kernel
-// (kda_chunk_intra.cu) with 32-row anchored sub-blocks (lower_bound >= -5):
-// l2 norms, gate and in-quarter decay sums (log2 units), the operand tiles,
-// one 128 x 96 tcgen05.mma for A and P, the blocked inverse (fp32 16x16
-// diagonal blocks, TF32 mma.sync off-diagonal steps), and W^T, U^^T on
-// tcgen05.  The chain's steps are those of the state pass
-// (kda_chunk_chain.cu): [U^T | O^T] = S^T [W | Q+]^T with S^T's bf16 copy as a
-// TMEM A operand, the U^T epilogue, S^T += U^T K' and O^T += U^T P^T, and the
+// The producer follows the two-kernel path's intra-chunk kernel
+// (kda_chunk_intra.cu) with 32-row anchored sub-blocks (lower_bound >= -5),
+// reorganised so that less of it sits on the per-chunk critical path:
+//  * the l2 norms are folded into scalings: the operand tiles hold the raw k, q
+//    (times their decay factors), A and P take their row / column norms when
+//    they are read out of TMEM, T is stored twice (T_U = Diag(n_k) T and
+//    T_W = Diag(n_k) T Diag(n_k)), so that the chain's U' = Diag(n_k) U meets the
+//    raw K' and P, and the output rows take n_q when they are read out; the norms
+//    themselves are computed while the A/P product runs;
+//  * W comes from the F tile (k e^(b - m_R)) in two K = 32 products, one per
+//    32-row block, combined with the per-channel factors e^(m_R) when W^T is read
+//    out, so there is no separate k e^b tile;
+//  * U^' = T_U V is accumulated straight into the TMEM columns where the chain's
+//    first product then adds -W'S (the chain keeps -S as its bf16 operand and the
+//    producer stores -Q+), so U' arrives in TMEM in fp32 without a staging pass;
+// The chain follows the state pass (kda_chunk_chain.cu): [U^T | O^T] =
+// (-S)^T [W | -Q+]^T with the bf16 copy of -S as a TMEM A operand, the U^T
+// epilogue (fp32 -> bf16 in place), S^T += U^T K' and O^T += U^T P^T, and the
 // decay of the state by the next chunk's gamma.
 //
 // Synchronisation (mbarriers, one phase per chunk):
@@ -58,35 +68,36 @@ constexpr int kChainIssuer = 256;   // first chain thread: issues the chain's MM
 constexpr int kBarProd = 7, kBarChain = 8;   // hardware barriers of the two groups (1..6: the inverse's warp pairs)
 
 // ---- shared memory (offsets from a 1024-byte aligned base) ----
-constexpr uint32_t OFF_BUF = 0;                    // one chunk's operands in the block layout (74240 B)
+constexpr uint32_t OFF_BUF = 0;                    // one chunk's operands for the chain, in the block layout
+constexpr uint32_t OFF_TW = OFF_BUF + kBlkUH;      // (its U^ tile is unused here) T_W bf16 K-major [t][t'] (8 KB)
+constexpr uint32_t OFF_TU = OFF_TW + 8192;         //                             T_U bf16 K-major (8 KB)
 constexpr uint32_t OFF_QIN = 75776;                // q, k, g tiles (TMA, unswizzled), 16 KB each
 constexpr uint32_t OFF_KIN = OFF_QIN + 16384;
 constexpr uint32_t OFF_GIN = OFF_QIN + 32768;
 constexpr uint32_t OFF_OPS = OFF_QIN + 49152;      // producer operand region (64 KB)
-constexpr uint32_t OFF_FQ = OFF_OPS;               // [F | Q]: 128 rows rho x (64 + 64) tokens, MN-major
+constexpr uint32_t OFF_FQ = OFF_OPS;               // [F | Q]: 128 rows rho x (64 + 64) tokens; F stays for W
 constexpr uint32_t OFF_GB = OFF_OPS + 32768;       // [G | B_1]: 128 rows rho x 96 tokens in two panels
 // after the A/P product
-constexpr uint32_t OFF_KP = OFF_OPS;               // K+^T: 128 rows rho x 64 tokens, K-major A operand
-constexpr uint32_t OFF_A = OFF_OPS + 16384;        // A fp32 [64][68], inverted in place
+constexpr uint32_t OFF_A = OFF_OPS + 16384;        // A fp32 [64][68], inverted in place (over Q and G)
 constexpr uint32_t OFF_V = OFF_OPS + 33792;        // v tile (TMA, 128-byte swizzle)
-constexpr uint32_t OFF_T = OFF_OPS + 50176;        // T bf16 K-major [t][t']
 constexpr uint32_t OFF_STAGE = OFF_OPS + 65536;    // output tile staging for the TMA store (16 KB)
 constexpr uint32_t OFF_SMALL = OFF_STAGE + 16384;
-constexpr uint32_t SM_NQ = 0, SM_NK = 256, SM_BETA = 512 /* [2][64] */, SM_H = 1024 /* [8 quarters][128] */,
-                   SM_GAMMA = 5120 /* [2][128] */, SM_BAR = 6144, SM_TMEM = 6272, SM_ABORT = 6276, SM_END = 6288;
+constexpr uint32_t SM_NQ = 0 /* [3][64] */, SM_NK = 768, SM_BETA = 1024 /* [2][64] */, SM_H = 1536 /* [8][128] */,
+                   SM_GAMMA = 5632 /* [2][128] */, SM_EM = 6656 /* [2 blocks][128] */, SM_BAR = 7680,
+                   SM_TMEM = 7808, SM_ABORT = 7812, SM_END = 7824;
 constexpr uint32_t kSmemBytes = OFF_SMALL + SM_END + 1024;   // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
-static_assert(OFF_QIN >= kBlkBytes && OFF_QIN % 1024 == 0 && OFF_V % 1024 == 0 && OFF_T % 1024 == 0 &&
-              OFF_STAGE % 1024 == 0, "layout");
-static_assert(OFF_A + 64 * 68 * 4 <= OFF_V && OFF_T + 8192 <= OFF_OPS + 65536, "operand region");
+static_assert(OFF_QIN >= kBlkBytes && OFF_QIN % 1024 == 0 && OFF_V % 1024 == 0 && OFF_TW % 1024 == 0 &&
+              OFF_STAGE % 1024 == 0 && OFF_TU + 8192 <= OFF_BUF + kBlkPK, "layout");
+static_assert(OFF_A + 64 * 68 * 4 <= OFF_V && OFF_V + 16384 <= OFF_OPS + 65536, "operand region");
 constexpr int kAStride = 68;
 
 // ---- TMEM columns ----
 constexpr uint32_t TM_S = 0;      // S^T fp32 (lane = value channel, column = key channel rho)
-constexpr uint32_t TM_XU = 128;   // (W S)^T of the first product; U^T's bf16 pairs overwrite it in place
+constexpr uint32_t TM_XU = 128;   // U^'^T from the producer, then U'^T after the first product; bf16 pairs in place
 constexpr uint32_t TM_O0 = 192;   // O^T, two buffers (chunk parity)
-constexpr uint32_t TM_SA = 320;   // S^T bf16 (A operand of the first product)
-constexpr uint32_t TM_P = 384;    // producer: A/P product (96 columns), then W^T (0..63) and U^^T (64..127)
+constexpr uint32_t TM_SA = 320;   // -S^T bf16 (A operand of the first product)
+constexpr uint32_t TM_P = 384;    // producer: A/P product (96 columns), then W's two block products (64 + 64)
 constexpr uint32_t kTmemCols = 512;
 
 // barrier indices in the SM_BAR array
@@ -127,13 +138,6 @@ __device__ __forceinline__ void pack8(const float2 (&v)[8], uint4 &lo, uint4 &hi
   hi = make_uint4(pack_bf16x2(v[0].y, v[1].y), pack_bf16x2(v[2].y, v[3].y), pack_bf16x2(v[4].y, v[5].y),
                   pack_bf16x2(v[6].y, v[7].y));
 }
-__device__ __forceinline__ void put8(uint8_t *tile, int R_rows, int rho, int col0, const float2 (&v)[8]) {
-  uint4 lo, hi;
-  pack8(v, lo, hi);
-  *reinterpret_cast<uint4 *>(tile + swz_offset(R_rows, rho, col0)) = lo;
-  *reinterpret_cast<uint4 *>(tile + swz_offset(R_rows, 64 + rho, col0)) = hi;
-}
-
 // 16 x 8 tile of X Y (TF32 tensor cores, fp32 accumulate), as in the intra-chunk kernel
 __device__ __forceinline__ void mm_16x8(float (&d)[4], const float *X, const float *Y, int ks, int lane) {
   const int g = lane >> 2, t = lane & 3;
@@ -151,79 +155,93 @@ __device__ __forceinline__ void st_16x8(float *D, const float (&d)[4], float sgn
   *reinterpret_cast<float2 *>(D + g * kAStride + 2 * t) = make_float2(sgn * d[0], sgn * d[1]);
   *reinterpret_cast<float2 *>(D + (g + 8) * kAStride + 2 * t) = make_float2(sgn * d[2], sgn * d[3]);
 }
-__device__ __forceinline__ void st_16x8_t(uint8_t *tT, int row0, int col0, const float (&d)[4], float sgn,
-                                          const float *s_beta, int lane) {
+// the same 16 x 8 tile of L^-1 (times sgn) as bf16 pairs into T_U (rows x n_k, columns x beta) and T_W (also
+// columns x n_k); K-major, 128-byte swizzle
+__device__ __forceinline__ void st_16x8_t(uint8_t *tU, uint8_t *tW, int row0, int col0, const float (&d)[4], float sgn,
+                                          const float *s_beta, const float *s_nk, int lane) {
   const int g = lane >> 2, c = col0 + 2 * (lane & 3);
-  const float b0 = sgn * s_beta[c], b1 = sgn * s_beta[c + 1];
-  *reinterpret_cast<uint32_t *>(tT + swz_offset(64, row0 + g, c)) = pack_bf16x2(d[0] * b0, d[1] * b1);
-  *reinterpret_cast<uint32_t *>(tT + swz_offset(64, row0 + g + 8, c)) = pack_bf16x2(d[2] * b0, d[3] * b1);
+  const float r0 = sgn * s_nk[row0 + g], r1 = sgn * s_nk[row0 + g + 8];
+  const float b0 = s_beta[c], b1 = s_beta[c + 1], n0 = s_nk[c], n1 = s_nk[c + 1];
+  const float u00 = d[0] * r0 * b0, u01 = d[1] * r0 * b1, u10 = d[2] * r1 * b0, u11 = d[3] * r1 * b1;
+  *reinterpret_cast<uint32_t *>(tU + swz_offset(64, row0 + g, c)) = pack_bf16x2(u00, u01);
+  *reinterpret_cast<uint32_t *>(tU + swz_offset(64, row0 + g + 8, c)) = pack_bf16x2(u10, u11);
+  *reinterpret_cast<uint32_t *>(tW + swz_offset(64, row0 + g, c)) = pack_bf16x2(u00 * n0, u01 * n1);
+  *reinterpret_cast<uint32_t *>(tW + swz_offset(64, row0 + g + 8, c)) = pack_bf16x2(u10 * n0, u11 * n1);
 }
 
 struct Factors {
-  float2 em;    // e^(m_R)
-  float2 ems;   // scale e^(m_R)
+  float2 nems;  // -scale e^(m_R)
   float2 el;    // e^(b_63 - m_R)
   float2 eg;    // e^(a_R - m_R), a_R = b at the last row of block R
-  float2 cr;    // e^(m_1 - a_0) (block 0 only), applied after eg: k^ e^(a_0 - b) <= |k^| stays representable
+  float2 cr;    // e^(m_1 - a_0) (block 0 only), applied after eg: k e^(a_0 - b) <= |k| stays representable
 };
 
 // Operand rows of 8 tokens (rows t0 .. t0+7 of 32-row block R) for key channels (2p, 2p+1); x[j] = (b - m_R)
-// log2(e) of those rows.  F, Q, G and B_1 go to the operand tiles, Q+ and K' to the chunk's buffer; K+ comes back
-// packed (rows p and 64 + p) and is stored once the A/P product has released its tile.
+// log2(e) of those rows; k and q are the raw inputs (their norms are applied later as scalings).  F, Q, G and B_1
+// go to the operand tiles, -Q+ and K' to the chunk's buffer.
 template <int R>
-__device__ __forceinline__ void build_rows(const uint8_t *sm, uint8_t *smw, const float2 (&x)[8], int t0, int p,
-                                           const float *s_nq, const float *s_nk, const Factors &f, uint4 &kp_lo,
-                                           uint4 &kp_hi) {
+__device__ __forceinline__ void build_rows(uint8_t *sm, const float2 (&x)[8], int t0, int p, const Factors &f) {
   const int c0 = 2 * p;
+  // every tile row of this thread starts at the same swizzled offset within its 128-row panel
+  const uint32_t o = swz_offset(128, p, t0);
   float2 e[8], v[8], w[8];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) e[j] = exp2_2(x[j]);
-  // keys
+  uint32_t kw[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
-    const float nk = s_nk[t0 + j];
-    v[j] = mul2(mul2(unpack_bf16x2(ld_u32(sm + OFF_KIN + in_offset(t0 + j, c0))),
-                     make_float2(nk, nk)), e[j]);                                    // F = k^ e^(b - m_R)
+    kw[j] = ld_u32(sm + OFF_KIN + in_offset(t0 + j, c0));
+    e[j] = exp2_2(x[j]);
   }
-  put8(smw + OFF_FQ, 128, p, t0, v);
 #pragma unroll
-  for (int j = 0; j < 8; ++j) w[j] = mul2(v[j], f.em);                               // K+ = F e^(m_R)
-  pack8(w, kp_lo, kp_hi);
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const float nk = s_nk[t0 + j];
-    v[j] = mul2(mul2(unpack_bf16x2(ld_u32(sm + OFF_KIN + in_offset(t0 + j, c0))),
-                     make_float2(nk, nk)), exp2_2(make_float2(-x[j].x, -x[j].y)));  // G = k^ e^(m_R - b)
+  for (int j = 0; j < 8; ++j) v[j] = mul2(unpack_bf16x2(kw[j]), e[j]);               // F = k e^(b - m_R)
+  {
+    uint4 lo, hi;
+    pack8(v, lo, hi);
+    *reinterpret_cast<uint4 *>(sm + OFF_FQ + o) = lo;
+    *reinterpret_cast<uint4 *>(sm + OFF_FQ + o + 8192) = hi;
   }
-  put8(smw + OFF_GB, 128, p, t0, v);
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    v[j] = mul2(unpack_bf16x2(kw[j]), exp2_2(make_float2(-x[j].x, -x[j].y)));        // G = k e^(m_R - b)
+  {
+    uint4 lo, hi;
+    pack8(v, lo, hi);
+    *reinterpret_cast<uint4 *>(sm + OFF_GB + o) = lo;
+    *reinterpret_cast<uint4 *>(sm + OFF_GB + o + 8192) = hi;
+  }
 #pragma unroll
   for (int j = 0; j < 8; ++j) w[j] = mul2(v[j], f.el);                               // K' = G e^(b_63 - m_R)
   {
     uint4 lo, hi;
     pack8(w, lo, hi);
-    *reinterpret_cast<uint4 *>(smw + OFF_BUF + kBlkPK + swz_offset(kBlkPKRows, 64 + p, t0)) = lo;
-    *reinterpret_cast<uint4 *>(smw + OFF_BUF + kBlkPK + swz_offset(kBlkPKRows, 128 + p, t0)) = hi;
+    // PK rows 64 + rho: 192-row K-major tile, token columns < 64 (panel 0)
+    *reinterpret_cast<uint4 *>(sm + OFF_BUF + kBlkPK + o + 64 * 128) = lo;
+    *reinterpret_cast<uint4 *>(sm + OFF_BUF + kBlkPK + o + 128 * 128) = hi;
   }
-  if (R == 0) {   // B_1: rows of block 0 anchored at m_1, k^ e^(m_1 - b) = (k^ e^(a_0 - b)) e^(m_1 - a_0)
+  if (R == 0) {   // B_1: rows of block 0 anchored at m_1, k e^(m_1 - b) = (k e^(a_0 - b)) e^(m_1 - a_0)
 #pragma unroll
     for (int j = 0; j < 8; ++j) w[j] = mul2(mul2(v[j], f.eg), f.cr);
-    put8(smw + OFF_GB, 128, p, 64 + t0, w);
+    uint4 lo, hi;
+    pack8(w, lo, hi);
+    *reinterpret_cast<uint4 *>(sm + OFF_GB + 16384 + o) = lo;          // columns 64 + t0: panel 1
+    *reinterpret_cast<uint4 *>(sm + OFF_GB + 16384 + o + 8192) = hi;
   }
   // queries
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const float nq = s_nq[t0 + j];
-    v[j] = mul2(mul2(unpack_bf16x2(ld_u32(sm + OFF_QIN + in_offset(t0 + j, c0))),
-                     make_float2(nq, nq)), e[j]);                                    // Q = q^ e^(b - m_R)
+  for (int j = 0; j < 8; ++j)
+    v[j] = mul2(unpack_bf16x2(ld_u32(sm + OFF_QIN + in_offset(t0 + j, c0))), e[j]);  // Q = q e^(b - m_R)
+  {
+    uint4 lo, hi;
+    pack8(v, lo, hi);
+    *reinterpret_cast<uint4 *>(sm + OFF_FQ + 16384 + o) = lo;          // columns 64 + t0: panel 1
+    *reinterpret_cast<uint4 *>(sm + OFF_FQ + 16384 + o + 8192) = hi;
   }
-  put8(smw + OFF_FQ, 128, p, 64 + t0, v);
 #pragma unroll
-  for (int j = 0; j < 8; ++j) w[j] = mul2(v[j], f.ems);                              // Q+ = scale Q e^(m_R)
+  for (int j = 0; j < 8; ++j) w[j] = mul2(v[j], f.nems);                             // -Q+ = -scale Q e^(m_R)
   {
     uint4 lo, hi;
     pack8(w, lo, hi);
-    *reinterpret_cast<uint4 *>(smw + OFF_BUF + kBlkWQ + 16384 + swz_offset(128, p, t0)) = lo;
-    *reinterpret_cast<uint4 *>(smw + OFF_BUF + kBlkWQ + 16384 + swz_offset(128, 64 + p, t0)) = hi;
+    *reinterpret_cast<uint4 *>(sm + OFF_BUF + kBlkWQ + 16384 + o) = lo;
+    *reinterpret_cast<uint4 *>(sm + OFF_BUF + kBlkWQ + 16384 + o + 8192) = hi;
   }
 }
 
@@ -239,11 +257,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_fused_kernel(const __grid
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t *small = sm + OFF_SMALL;
-  float *s_nq = reinterpret_cast<float *>(small + SM_NQ);
+  float *s_nq3 = reinterpret_cast<float *>(small + SM_NQ);     // [chunk % 3][64]: read by the chain a chunk later
   float *s_nk = reinterpret_cast<float *>(small + SM_NK);
   float *s_beta2 = reinterpret_cast<float *>(small + SM_BETA);
   float *s_h = reinterpret_cast<float *>(small + SM_H);
   float *s_gamma2 = reinterpret_cast<float *>(small + SM_GAMMA);
+  float *s_em = reinterpret_cast<float *>(small + SM_EM);      // e^(m_0), e^(m_1) per key channel rho
   uint64_t *bars = reinterpret_cast<uint64_t *>(small + SM_BAR);
   uint32_t *s_tmem = reinterpret_cast<uint32_t *>(small + SM_TMEM);
   volatile uint32_t *s_abort = reinterpret_cast<volatile uint32_t *>(small + SM_ABORT);
@@ -333,6 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_fused_kernel(const __grid
       const int tok0 = t0 + n * kC;
       const int valid = min(kC, len - n * kC);
       float *s_beta = s_beta2 + 64 * (n & 1);
+      float *s_nq = s_nq3 + 64 * (n % 3);
       // this chunk's beta (loaded one chunk earlier) to shared memory; the next chunk's load is issued here
       if (ptid < kC) {
         s_beta[ptid] = ptid < valid ? sigmoid_f(bf16_bits_to_f32(beta_raw)) : 0.f;
@@ -340,36 +360,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_fused_kernel(const __grid
         beta_raw = ptid < nvalid ? prm.beta[static_cast<size_t>(tok0 + kC + ptid) * prm.beta_stride + h] : uint16_t(0);
       }
       wait_or_abort(&bars[B_IN], n & 1, s_abort, prm.status);
-
-      // ---------------------------------------------------- l2 norms (token-major)
-      {
-        const int r = ptid >> 2, part = ptid & 3;
-        const int rot = (r & 1) * 2 + (part >> 1);
-        float2 sq = zero2, sk = zero2;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int c = 32 * part + 8 * ((j + rot) & 3);
-          const uint32_t off = in_offset(r, c);
-          const uint4 wq = *reinterpret_cast<const uint4 *>(sm + OFF_QIN + off);
-          const uint4 wk = *reinterpret_cast<const uint4 *>(sm + OFF_KIN + off);
-          const uint32_t aq[4] = {wq.x, wq.y, wq.z, wq.w}, ak[4] = {wk.x, wk.y, wk.z, wk.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 fq = unpack_bf16x2(aq[e]), fk = unpack_bf16x2(ak[e]);
-            sq = fma2(fq, fq, sq);
-            sk = fma2(fk, fk, sk);
-          }
-        }
-        float ssq = sq.x + sq.y, ssk = sk.x + sk.y;
-        ssq += __shfl_xor_sync(0xffffffffu, ssq, 1);
-        ssk += __shfl_xor_sync(0xffffffffu, ssk, 1);
-        ssq += __shfl_xor_sync(0xffffffffu, ssq, 2);
-        ssk += __shfl_xor_sync(0xffffffffu, ssk, 2);
-        if (part == 0) {
-          s_nq[r] = r < valid ? rsqrtf(ssq + kL2Eps) : 0.f;
-          s_nk[r] = r < valid ? rsqrtf(ssk + kL2Eps) : 0.f;
-        }
-      }
 
       // ---------------------------------------------------- gate and in-quarter decay sums
       // thread = (channel pair p, quarter `sel` of both 32-row blocks); a quarter before its block's anchor
@@ -385,8 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_fused_kernel(const __grid
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           const int r = r0 + j;
-          const uint32_t off = in_offset(r, c0);
-          const float2 gg = unpack_bf16x2(ld_u32(sm + OFF_GIN + off));
+          const float2 gg = unpack_bf16x2(ld_u32(sm + OFF_GIN + in_offset(r, c0)));
           const float2 ex = exp2_2(fma2(gg, nea2, nd));
           const float2 den = fma2(ex, one2, one2);
           const float2 l = mul2(make_float2(fast_rcp(den.x), fast_rcp(den.y)), lb22);
@@ -409,12 +398,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_fused_kernel(const __grid
         }
         *reinterpret_cast<float2 *>(s_h + qd * kD + c0) = hs;
       }
-      named_bar_sync<kBarProd>(kProdThreads);   // norms, quarter sums and beta visible
+      named_bar_sync<kBarProd>(kProdThreads);   // quarter sums and beta visible
 
       // ---------------------------------------------------- anchors, gamma, operand tiles
-      // the chunk's buffer and gamma slot are free once the chain's output product of chunk n - 1 is done
+      // the chunk's buffer (and the producer's T tiles in it) and gamma slot are free once the chain's output
+      // product of chunk n - 1 is done
       if (n > 0) wait_or_abort(&bars[B_FREE], (n - 1) & 1, s_abort, prm.status);
-      uint4 kp[2][2];   // packed K+ rows of the thread's two quarters
       {
         float2 sq[8];
 #pragma unroll
@@ -424,20 +413,24 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_fused_kernel(const __grid
         const float2 a0 = add(add(m0, sq[2]), sq[3]);
         const float2 m1 = add(add(a0, sq[4]), sq[5]);
         const float2 tot = add(add(m1, sq[6]), sq[7]);
-        if (sel == 0) {   // gamma = e^(b_63) for rho = p and 64 + p
+        const float2 em0 = exp2_2(m0), em1 = exp2_2(m1);
+        if (sel == 0) {   // gamma = e^(b_63) and the block factors e^(m_R) for rho = p and 64 + p
           float *gam = s_gamma2 + 128 * (n & 1);
           gam[p] = fast_exp2(tot.x);
           gam[64 + p] = fast_exp2(tot.y);
+          s_em[p] = em0.x;
+          s_em[64 + p] = em0.y;
+          s_em[128 + p] = em1.x;
+          s_em[192 + p] = em1.y;
           mbar_arrive(&bars[B_GAMMA]);
         }
+        const float nsc = -prm.scale;
         Factors f0, f1;
-        f0.em = exp2_2(m0);
-        f0.ems = make_float2(f0.em.x * prm.scale, f0.em.y * prm.scale);
+        f0.nems = make_float2(nsc * em0.x, nsc * em0.y);
         f0.el = exp2_2(make_float2(tot.x - m0.x, tot.y - m0.y));
         f0.eg = exp2_2(make_float2(a0.x - m0.x, a0.y - m0.y));
         f0.cr = exp2_2(make_float2(fminf(m1.x - a0.x, 0.f), fminf(m1.y - a0.y, 0.f)));
-        f1.em = exp2_2(m1);
-        f1.ems = make_float2(f1.em.x * prm.scale, f1.em.y * prm.scale);
+        f1.nems = make_float2(nsc * em1.x, nsc * em1.y);
         f1.el = exp2_2(make_float2(tot.x - m1.x, tot.y - m1.y));
         f1.eg = zero2;
         f1.cr = zero2;
@@ -448,8 +441,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_fused_kernel(const __grid
         };
         shift(0, sel == 0 ? make_float2(-sq[1].x, -sq[1].y) : sel == 3 ? sq[2] : zero2);
         shift(1, sel == 0 ? make_float2(-sq[5].x, -sq[5].y) : sel == 3 ? sq[6] : zero2);
-        build_rows<0>(sm, sm, x[0], 8 * sel, p, s_nq, s_nk, f0, kp[0][0], kp[0][1]);
-        build_rows<1>(sm, sm, x[1], 32 + 8 * sel, p, s_nq, s_nk, f1, kp[1][0], kp[1][1]);
+        build_rows<0>(sm, x[0], 8 * sel, p, f0);
+        build_rows<1>(sm, x[1], 32 + 8 * sel, p, f1);
       }
       fence_async_smem();
       tc_fence_before();
@@ -464,8 +457,39 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_fused_kernel(const __grid
 #pragma unroll
         for (int s = 0; s < 8; ++s) mma_bf16(tmem + TM_P, fq + mnmajor_step(s), gb + mnmajor_step(s), id, s > 0);
         mma_commit(&bars[B_PMMA]);
-        // q, k, g of the next chunk into the input tiles (read for the last time above); L2 prefetch of the v
-        // and inputs one chunk further
+      }
+      // ---------------------------------------------------- l2 norms (token-major), under the product
+      {
+        const int r = ptid >> 2, part = ptid & 3;
+        const int rot = (r & 1) * 2 + (part >> 1);
+        float2 sqq = zero2, skk = zero2;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int c = 32 * part + 8 * ((j + rot) & 3);
+          const uint32_t off = in_offset(r, c);
+          const uint4 wq = *reinterpret_cast<const uint4 *>(sm + OFF_QIN + off);
+          const uint4 wk = *reinterpret_cast<const uint4 *>(sm + OFF_KIN + off);
+          const uint32_t aq[4] = {wq.x, wq.y, wq.z, wq.w}, ak[4] = {wk.x, wk.y, wk.z, wk.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 fq2 = unpack_bf16x2(aq[e]), fk2 = unpack_bf16x2(ak[e]);
+            sqq = fma2(fq2, fq2, sqq);
+            skk = fma2(fk2, fk2, skk);
+          }
+        }
+        float ssq = sqq.x + sqq.y, ssk = skk.x + skk.y;
+        ssq += __shfl_xor_sync(0xffffffffu, ssq, 1);
+        ssk += __shfl_xor_sync(0xffffffffu, ssk, 1);
+        ssq += __shfl_xor_sync(0xffffffffu, ssq, 2);
+        ssk += __shfl_xor_sync(0xffffffffu, ssk, 2);
+        if (part == 0) {
+          s_nq[r] = r < valid ? rsqrtf(ssq + kL2Eps) : 0.f;
+          s_nk[r] = r < valid ? rsqrtf(ssk + kL2Eps) : 0.f;
+        }
+      }
+      named_bar_sync<kBarProd>(kProdThreads);   // norms visible; the input tiles are read for the last time
+      if (ptid == 0) {
+        // q, k, g of the next chunk into the input tiles; L2 prefetch of its v and of the inputs one chunk further
         if (n + 1 < nchunks) {
           mbar_arrive_expect_tx(&bars[B_IN], 3 * 16384);
 #pragma unroll
@@ -485,31 +509,24 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_fused_kernel(const __grid
           }
         }
       }
-      __syncwarp();
       wait_or_abort(&bars[B_PMMA], n & 1, s_abort, prm.status);
       tc_fence_after();
-      if (ptid == 0) {   // the operand tiles are free: v may land
+      if (ptid == 0) {   // the Q and G tiles are free: v may land (F stays for W)
         mbar_arrive_expect_tx(&bars[B_V], 16384);
         tma_load_3d(sm + OFF_V, &prm.tv, 0, h, tok0, &bars[B_V]);
         tma_load_3d(sm + OFF_V + 8192, &prm.tv, 64, h, tok0, &bars[B_V]);
-      }
-      // K+ rows -> their tile (panel 0 of the released [F | Q] tile)
-#pragma unroll
-      for (int bi = 0; bi < 2; ++bi) {
-        const int r0 = 32 * bi + 8 * sel;
-        *reinterpret_cast<uint4 *>(sm + OFF_KP + swz_offset(128, p, r0)) = kp[bi][0];
-        *reinterpret_cast<uint4 *>(sm + OFF_KP + swz_offset(128, 64 + p, r0)) = kp[bi][1];
       }
 
       // ---------------------------------------------------- A (fp32) and P (bf16 rows of the buffer) from TMEM
       {
         // lanes 0..63 of the product hold rows of A (k side), lanes 64..127 rows of P (q side); the warp's lanes
-        // are one 32-row block R, ib picks the 32-column block I
+        // are one 32-row block R, ib picks the 32-column block I.  A takes beta_r n_r n_i (the key norms it was
+        // built without), P only the scale (its norms go to U' and the output rows).
         const int q4 = warp & 3, ib = warp >> 2;
         const bool is_p = q4 >= 2;
         const int r = (q4 & 1) * 32 + lane;
         const uint32_t lane_base = static_cast<uint32_t>(q4 * 32) << 16;
-        const float bscale = is_p ? prm.scale : s_beta[r];
+        const float rscale = is_p ? prm.scale : s_beta[r] * s_nk[r];
         float *sA = reinterpret_cast<float *>(sm + OFF_A);
         const int R = q4 & 1, I = ib;
         const int srcc = I == R ? 32 * I : I < R ? 64 + 32 * I : -1;
@@ -522,15 +539,26 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_fused_kernel(const __grid
         tmem_tie<32>(va);
         const int lim = r - 32 * I + (is_p ? 1 : 0);
         float v[32];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) v[e] = (srcc >= 0 && e < lim) ? __uint_as_float(va[e]) * bscale : 0.f;
         if (is_p) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[e] = (srcc >= 0 && e < lim) ? __uint_as_float(va[e]) * rscale : 0.f;
 #pragma unroll
           for (int k8 = 0; k8 < 4; ++k8)
             *reinterpret_cast<uint4 *>(sm + OFF_BUF + kBlkPK + swz_offset(kBlkPKRows, r, 32 * I + 8 * k8)) =
                 make_uint4(pack_bf16x2(v[8 * k8], v[8 * k8 + 1]), pack_bf16x2(v[8 * k8 + 2], v[8 * k8 + 3]),
                            pack_bf16x2(v[8 * k8 + 4], v[8 * k8 + 5]), pack_bf16x2(v[8 * k8 + 6], v[8 * k8 + 7]));
         } else {
+          const float4 *nk4 = reinterpret_cast<const float4 *>(s_nk + 32 * I);
+#pragma unroll
+          for (int e4 = 0; e4 < 8; ++e4) {
+            const float4 nc = nk4[e4];
+            const float ncs[4] = {nc.x, nc.y, nc.z, nc.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const int e = 4 * e4 + q;
+              v[e] = (srcc >= 0 && e < lim) ? __uint_as_float(va[e]) * rscale * ncs[q] : 0.f;
+            }
+          }
 #pragma unroll
           for (int e = 0; e < 32; e += 4)
             *reinterpret_cast<float4 *>(sA + r * kAStride + 32 * I + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
@@ -540,19 +568,27 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_fused_kernel(const __grid
       tc_fence_before();
       named_bar_sync<kBarProd>(kProdThreads);
 
-      // ---------------------------------------------------- T = (I + A)^-1 Diag(beta)
-      // (the blocked inverse of the intra-chunk kernel: 16x16 diagonal blocks by substitution in fp32, then
-      //  L^-1_10 = -D_1 A_10 D_0, L^-1_32 = -D_3 A_32 D_2, L^-1(23,01) = -I_2 A(23,01) I_1 on TF32 mma.sync)
+      // ---------------------------------------------------- T = (I + A)^-1 Diag(beta), as T_U and T_W
+      // Blocked inverse of the unit-lower L = I + A in fp32, 16x16 blocks D_R = L_RR^-1:
+      //   L^-1_10 = -D_1 A_10 D_0,  L^-1_32 = -D_3 A_32 D_2,  L^-1 (rows 32..63, cols 0..31) = -I_2 A_(23,01) I_1
+      // in place in the A tile; each block of L^-1 goes to T_U (rows x n_k, columns x beta) and T_W (columns also
+      // x n_k) in bf16; the six blocks above the diagonal of both are zero.
       {
         float *sA = reinterpret_cast<float *>(sm + OFF_A);
         float *sInv = sA;
-        uint8_t *tT = sm + OFF_T;
-        if (ptid < 192) {   // zero blocks (I, J), J > I of T
-          const int b6 = ptid >> 5, rr = (ptid >> 1) & 15, hc = ptid & 1;
+        uint8_t *tU = sm + OFF_TU, *tW = sm + OFF_TW;
+        if (ptid < 192) {   // zero blocks (I, J), J > I: 6 blocks x 16 rows x two 16-byte chunks, in both tiles
+          const int z = ptid;
+          const int b6 = z >> 5, rr = (z >> 1) & 15, hc = z & 1;
           const int I = b6 < 3 ? 0 : b6 < 5 ? 1 : 2;
           const int J = b6 < 3 ? b6 + 1 : b6 < 5 ? b6 - 1 : 3;
-          *reinterpret_cast<uint4 *>(tT + swz_offset(64, 16 * I + rr, 16 * J + 8 * hc)) = make_uint4(0, 0, 0, 0);
+          const uint32_t o = swz_offset(64, 16 * I + rr, 16 * J + 8 * hc);
+          *reinterpret_cast<uint4 *>(tU + o) = make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4 *>(tW + o) = make_uint4(0, 0, 0, 0);
         }
+        // D_R: task (block R, column jc) = 8 warp + lane / 4, so warps 2R and 2R + 1 share block R; lane
+        // q = lane % 4 of a task carries rows q, q + 4, q + 8, q + 12 of its column.  Right-looking: at step m
+        // the lane holding row m broadcasts x_m to its task's lanes, and every later row takes one FMA.
         {
           const int q = lane & 3, jc = 8 * (warp & 1) + (lane >> 2), R = warp >> 1;
           const float *a = sA + (16 * R) * kAStride + 16 * R;
@@ -568,21 +604,26 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_fused_kernel(const __grid
               if (r > m) xs[i] = fmaf(-a[r * kAStride + m], xm, xs[i]);
             }
           }
-          switch (R) {
+          switch (R) {   // both warps of the block have read its A entries (constant barrier ids)
             case 0: named_bar_sync<1>(64); break;
             case 1: named_bar_sync<2>(64); break;
             case 2: named_bar_sync<3>(64); break;
             default: named_bar_sync<4>(64); break;
           }
-          const float bc = s_beta[16 * R + jc];
+          const int c = 16 * R + jc;
+          const float bc = s_beta[c], nc = s_nk[c];
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            sInv[(16 * R + 4 * i + q) * kAStride + 16 * R + jc] = xs[i];
-            *reinterpret_cast<uint16_t *>(tT + swz_offset(64, 16 * R + 4 * i + q, 16 * R + jc)) =
-                f32_to_bf16_bits(xs[i] * bc);
+            const int row = 16 * R + 4 * i + q;
+            sInv[row * kAStride + c] = xs[i];
+            const float u = xs[i] * s_nk[row] * bc;
+            const uint32_t o = swz_offset(64, row, c);
+            *reinterpret_cast<uint16_t *>(tU + o) = f32_to_bf16_bits(u);
+            *reinterpret_cast<uint16_t *>(tW + o) = f32_to_bf16_bits(u * nc);
           }
         }
         named_bar_sync<kBarProd>(kProdThreads);
+        // Every block product below is a set of 16 x 8 output tiles, one per warp task, on TF32 tensor cores.
         if (warp < 4) {
           const int lo = warp < 2 ? 0 : 32, nj = warp & 1;
           float dd[4] = {0.f, 0.f, 0.f, 0.f};
@@ -592,7 +633,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_fused_kernel(const __grid
           float e4[4] = {0.f, 0.f, 0.f, 0.f};
           mm_16x8(e4, sInv + (lo + 16) * kAStride + lo + 16, sA + lo * kAStride + lo + 16 + 8 * nj, 2, lane);
           st_16x8(sInv + (lo + 16) * kAStride + lo + 8 * nj, e4, -1.f, lane);
-          st_16x8_t(tT, lo + 16, lo + 8 * nj, e4, -1.f, s_beta, lane);
+          st_16x8_t(tU, tW, lo + 16, lo + 8 * nj, e4, -1.f, s_beta, s_nk, lane);
         }
         named_bar_sync<kBarProd>(kProdThreads);
         {
@@ -607,14 +648,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_fused_kernel(const __grid
           const int mi = warp >> 2, nj = warp & 3;
           float dd[4] = {0.f, 0.f, 0.f, 0.f};
           mm_16x8(dd, sInv + (32 + 16 * mi) * kAStride + 32, sA + 32 + 8 * nj, mi ? 4 : 2, lane);
-          st_16x8_t(tT, 32 + 16 * mi, 8 * nj, dd, -1.f, s_beta, lane);
+          st_16x8_t(tU, tW, 32 + 16 * mi, 8 * nj, dd, -1.f, s_beta, s_nk, lane);
         }
       }
       fence_async_smem();
       tc_fence_before();
       named_bar_sync<kBarProd>(kProdThreads);
 
-      // ---------------------------------------------------- W^T = K+^T T^T, U^^T = V^T T^T
+      // ---------------------------------------------------- W^T from F per 32-row block; U^'^T = V^T T_U^T
       const bool ragged = valid < kC;
       if (ragged) {   // rows past the sequence end: T's columns there are 0, but v may hold anything
         wait_or_abort(&bars[B_V], n & 1, s_abort, prm.status);
@@ -629,80 +670,113 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_fused_kernel(const __grid
         tc_fence_after();
         const uint32_t id_w = idesc_bf16(128, 64, false, false);
         const uint32_t id_u = idesc_bf16(128, 64, true, false);
-        const uint64_t kpd = desc_kmajor_base(smem_u32(sm + OFF_KP));
+        const uint64_t ff = desc_kmajor_base(smem_u32(sm + OFF_FQ));
         const uint64_t vv = desc_mnmajor_base(smem_u32(sm + OFF_V), 64);
-        const uint64_t tt = desc_kmajor_base(smem_u32(sm + OFF_T));
+        const uint64_t tw = desc_kmajor_base(smem_u32(sm + OFF_TW));
+        const uint64_t tu = desc_kmajor_base(smem_u32(sm + OFF_TU));
+        // X_R^T = F_R^T T_W,R^T over the tokens of block R (K steps 2R, 2R + 1) -> TM_P + 64 R
 #pragma unroll
-        for (int s = 0; s < 4; ++s) mma_bf16(tmem + TM_P, kpd + kmajor_step(128, s), tt + kmajor_step(64, s), id_w, s > 0);
+        for (int s = 0; s < 4; ++s)
+          mma_bf16(tmem + TM_P + 64 * (s >> 1), ff + kmajor_step(128, s), tw + kmajor_step(64, s), id_w, s & 1);
         mma_commit(&bars[B_PW]);
         if (!ragged) wait_or_abort(&bars[B_V], n & 1, s_abort, prm.status);
 #pragma unroll
-        for (int s = 0; s < 4; ++s) mma_bf16(tmem + TM_P + 64, vv + mnmajor_step(s), tt + kmajor_step(64, s), id_u, s > 0);
+        for (int s = 0; s < 4; ++s) mma_bf16(tmem + TM_XU, vv + mnmajor_step(s), tu + kmajor_step(64, s), id_u, s > 0);
         mma_commit(&bars[B_PU]);
       }
       __syncwarp();
-      // ---------------------------------------------------- W^T, U^^T rows to the chunk's buffer
+      // ---------------------------------------------------- W^T = Diag(e^(m_0)) X_0^T + Diag(e^(m_1)) X_1^T -> buffer
       {
-        const int q4 = warp & 3, which = warp >> 2;
-        wait_or_abort(&bars[which ? B_PU : B_PW], n & 1, s_abort, prm.status);
+        const int q4 = warp & 3, half = warp >> 2;   // lane = key channel rho; half = tokens 32 half .. +31
+        wait_or_abort(&bars[B_PW], n & 1, s_abort, prm.status);
         tc_fence_after();
         const int row = q4 * 32 + lane;
-        const uint32_t taddr = tmem + TM_P + (static_cast<uint32_t>(q4 * 32) << 16) + (which ? 64u : 0u);
-        uint32_t v[64];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) tmem_ld16_async(taddr + 16 * k, v + 16 * k);
+        const uint32_t taddr = tmem + TM_P + (static_cast<uint32_t>(q4 * 32) << 16) + 32 * half;
+        uint32_t x0[32], x1[32];
+        tmem_ld16_async(taddr, x0);
+        tmem_ld16_async(taddr + 16, x0 + 16);
+        tmem_ld16_async(taddr + 64, x1);
+        tmem_ld16_async(taddr + 80, x1 + 16);
+        const float e0 = s_em[row], e1 = s_em[128 + row];
         tmem_wait_ld();
-        tmem_tie<64>(v);
-        uint8_t *dstt = sm + OFF_BUF + (which ? kBlkUH : kBlkWQ);
+        tmem_tie<32>(x0);
+        tmem_tie<32>(x1);
+        const float2 e02 = make_float2(e0, e0), e12 = make_float2(e1, e1);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const float *fv = reinterpret_cast<const float *>(v + 8 * k);
-          *reinterpret_cast<uint4 *>(dstt + swz_offset(128, row, 8 * k)) =
-              make_uint4(pack_bf16x2(fv[0], fv[1]), pack_bf16x2(fv[2], fv[3]), pack_bf16x2(fv[4], fv[5]),
-                         pack_bf16x2(fv[6], fv[7]));
+        for (int k = 0; k < 4; ++k) {
+          uint32_t wv[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int i = 8 * k + 2 * q;
+            const float2 wpair = fma2(make_float2(__uint_as_float(x1[i]), __uint_as_float(x1[i + 1])), e12,
+                                      mul2(make_float2(__uint_as_float(x0[i]), __uint_as_float(x0[i + 1])), e02));
+            wv[q] = pack2(wpair);
+          }
+          *reinterpret_cast<uint4 *>(sm + OFF_BUF + kBlkWQ + swz_offset(128, row, 32 * half + 8 * k)) =
+              make_uint4(wv[0], wv[1], wv[2], wv[3]);
         }
       }
+      if (ptid == 0) wait_or_abort(&bars[B_PU], n & 1, s_abort, prm.status);   // U^' is in TMEM
       fence_async_smem();
       tc_fence_before();
       stop = bar_any<kBarProd>(kProdThreads, *s_abort != 0);
-      if (ptid == 0) mbar_arrive(&bars[B_READY]);   // chunk n's buffer is complete
+      if (ptid == 0) mbar_arrive(&bars[B_READY]);   // chunk n's buffer and U^' are complete
     }
   } else {
     // ================================================================ chain: the state recurrence
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-    // S0 (this thread's 64 key channels rho = 64 hv + i) -> the bf16 A operand; Diag(gamma_0) S0 -> TMEM
+    // -S0 (this thread's 64 key channels rho = 64 hv + i) -> the bf16 A operand; Diag(gamma_0) S0 -> TMEM
     {
       const int col = 64 * hv;
-      float s[64];
 #pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        const int kd = kd_of_rho(col + i);
-        s[i] = src ? src[static_cast<size_t>(kd) * kD + d] : 0.f;
+      for (int part = 0; part < 2; ++part) {
+        float s[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int kd = kd_of_rho(col + 32 * part + i);
+          s[i] = src ? -src[static_cast<size_t>(kd) * kD + d] : 0.f;
+        }
+        st_bf16_pairs(tmem + lane_base + TM_SA + col / 2 + 16 * part, s);
       }
-      st_bf16_pairs(tmem + lane_base + TM_SA + col / 2, s);
-      st_bf16_pairs(tmem + lane_base + TM_SA + col / 2 + 16, s + 32);
       wait_or_abort(&bars[B_GAMMA], 0, s_abort, prm.status);
       const float *gam = s_gamma2 + col;
 #pragma unroll
-      for (int i = 0; i < 64; ++i) s[i] *= gam[i];
+      for (int part = 0; part < 2; ++part) {
+        float s[32];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) tmem_st16(tmem + lane_base + TM_S + col + 16 * k, s + 16 * k);
+        for (int i = 0; i < 32; ++i) {
+          const int kd = kd_of_rho(col + 32 * part + i);
+          s[i] = src ? src[static_cast<size_t>(kd) * kD + d] * gam[32 * part + i] : 0.f;
+        }
+        tmem_st16(tmem + lane_base + TM_S + col + 32 * part, s);
+        tmem_st16(tmem + lane_base + TM_S + col + 32 * part + 16, s + 16);
+      }
       tmem_wait_st();
     }
     tc_fence_before();
     named_bar_sync<kBarChain>(kChainThreads);
 
     uint8_t *stage = sm + OFF_STAGE;
-    auto out_to_stage = [&](int ob) {
+    // output of chunk cc (accumulated in O buffer cc & 1) -> staging, each token row times its query norm
+    auto out_to_stage = [&](int cc) {
       uint32_t ov[32];
-      const uint32_t tb = tmem + lane_base + TM_O0 + 64 * ob + 32 * hv;
+      const uint32_t tb = tmem + lane_base + TM_O0 + 64 * (cc & 1) + 32 * hv;
       tmem_ld16_async(tb, ov);
       tmem_ld16_async(tb + 16, ov + 16);
       tmem_wait_ld();
       tmem_tie<32>(ov);
+      const float4 *nq4 = reinterpret_cast<const float4 *>(s_nq3 + 64 * (cc % 3) + 32 * hv);
 #pragma unroll
-      for (int i = 0; i < 32; ++i)
-        *reinterpret_cast<uint16_t *>(stage + swz_offset(64, 32 * hv + i, d)) = f32_to_bf16_bits(__uint_as_float(ov[i]));
+      for (int i4 = 0; i4 < 8; ++i4) {
+        const float4 nq = nq4[i4];
+        const float nqs[4] = {nq.x, nq.y, nq.z, nq.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int i = 4 * i4 + q;
+          *reinterpret_cast<uint16_t *>(stage + swz_offset(64, 32 * hv + i, d)) =
+              f32_to_bf16_bits(__uint_as_float(ov[i]) * nqs[q]);
+        }
+      }
     };
     const uint8_t *buf = sm + OFF_BUF;
     bool stop = false;
@@ -710,63 +784,45 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_fused_kernel(const __grid
       const uint32_t tm_o = TM_O0 + 64 * (c & 1);
       wait_or_abort(&bars[B_READY], c & 1, s_abort, prm.status);
 
-      // ---- [U^T | O^T] = S_c^T [W | Q+]^T: the U half first (it is on the critical path), then the O half
+      // ---- [U'^T | O^T] = (-S_c)^T [W' | -Q+]^T: the U half accumulates onto U^'^T (it is on the critical path),
+      //      then the O half
       if (tid == kChainIssuer) {
-        // the previous chunk's output product reads U^T where this product writes (W S)^T
+        // the previous chunk's output product has read U^T where the producer has put U^'^T and this product adds
         if (c > 0) wait_or_abort(&bars[B_FREE], (c - 1) & 1, s_abort, prm.status);
         tc_fence_after();
         const uint64_t wq = desc_mnmajor_base(smem_u32(buf + kBlkWQ), 128);
         const uint32_t id = idesc_bf16(128, 64, false, true);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) mma_bf16_tmem_a(tmem + TM_XU, tmem + TM_SA + 8 * k, wq + mnmajor_step(k), id, k > 0);
+        for (int k = 0; k < 8; ++k) mma_bf16_tmem_a(tmem + TM_XU, tmem + TM_SA + 8 * k, wq + mnmajor_step(k), id, 1);
         mma_commit(&bars[B_M1U]);
 #pragma unroll
         for (int k = 0; k < 8; ++k)
           mma_bf16_tmem_a(tmem + tm_o, tmem + TM_SA + 8 * k, wq + desc_bytes(16384) + mnmajor_step(k), id, k > 0);
       }
-      // ---- under the product: output of chunk c - 1 (its product is done) -> staging -> global
-      if (c > 0) {
-        wait_or_abort(&bars[B_FREE], (c - 1) & 1, s_abort, prm.status);
-        tc_fence_after();
-        out_to_stage((c - 1) & 1);
-        fence_async_smem();
-        named_bar_sync<kBarChain>(kChainThreads);
-        if (tid == kChainIssuer) {   // chunk c - 1 is not the last one: all 64 rows are valid
-          const int tok = t0 + (c - 1) * kC;
-          tma_store_3d(&prm.tout, 0, h, tok, stage);
-          tma_store_3d(&prm.tout, 64, h, tok, stage + 8192);
-          bulk_commit();
-        }
-      }
       wait_or_abort(&bars[B_M1U], c & 1, s_abort, prm.status);
+      // the previous chunk's output product (done before this step's first product was issued) -- waited on here,
+      // before this step commits its own output product onto the same barrier
+      if (c > 0) wait_or_abort(&bars[B_FREE], (c - 1) & 1, s_abort, prm.status);
       tc_fence_after();
 
-      // ---- U^T = U^^T - (W S)^T -> bf16 pairs in place (columns 32 hv .. 32 hv + 15 of TM_XU)
+      // ---- U'^T (fp32) -> bf16 pairs in place (columns 32 hv .. 32 hv + 15 of TM_XU)
       {
         uint32_t v[32];
         tmem_ld16_async(tmem + lane_base + TM_XU + 32 * hv, v);
         tmem_ld16_async(tmem + lane_base + TM_XU + 32 * hv + 16, v + 16);
         tmem_wait_ld();
         tmem_tie<32>(v);
-        float u[32];
+        uint32_t w[16];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint4 w = *reinterpret_cast<const uint4 *>(buf + kBlkUH + swz_offset(128, d, 32 * hv + 8 * j));
-          const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 uh = unpack_bf16x2(ws[e]);
-            u[8 * j + 2 * e] = uh.x - __uint_as_float(v[8 * j + 2 * e]);
-            u[8 * j + 2 * e + 1] = uh.y - __uint_as_float(v[8 * j + 2 * e + 1]);
-          }
-        }
-        st_bf16_pairs(tmem + lane_base + TM_XU + 32 * hv, u);
+        for (int j = 0; j < 16; ++j) w[j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+        tmem_st16(tmem + lane_base + TM_XU + 32 * hv, w);
       }
       tmem_wait_st();
       tc_fence_before();
+      if (tid == kChainIssuer) bulk_wait_read();   // the staging tile's previous store has read it
       named_bar_sync<kBarChain>(kChainThreads);
 
-      // ---- S^T += U^T K' (N = 128), then O^T += U^T P^T (N = 64); U^T's K steps: tokens 0..31 at TM_XU + 0, 8,
+      // ---- S^T += U'^T K' (N = 128), then O^T += U'^T P^T (N = 64); U'^T's K steps: tokens 0..31 at TM_XU + 0, 8,
       //      tokens 32..63 at TM_XU + 32, 40
       if (tid == kChainIssuer) {
         tc_fence_after();
@@ -783,10 +839,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_fused_kernel(const __grid
                           id_o, 1);
         mma_commit(&bars[B_FREE]);
       }
+      // ---- the previous chunk's output -> staging (stored at the end of this step)
+      if (c > 0) {
+        out_to_stage(c - 1);
+        fence_async_smem();
+      }
       wait_or_abort(&bars[B_M2S], c & 1, s_abort, prm.status);
       tc_fence_after();
 
-      // ---- S_{c+1} -> the bf16 A operand of the next first product; Diag(gamma_{c+1}) S_{c+1} -> TMEM
+      // ---- -S_{c+1} -> the bf16 A operand of the next first product; Diag(gamma_{c+1}) S_{c+1} -> TMEM
       if (c + 1 < nchunks) {
         wait_or_abort(&bars[B_GAMMA], (c + 1) & 1, s_abort, prm.status);
         const float *gam = s_gamma2 + 128 * ((c + 1) & 1);
@@ -798,16 +859,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_fused_kernel(const __grid
           tmem_ld16_async(tmem + lane_base + TM_S + col + 16, sv + 16);
           tmem_wait_ld();
           tmem_tie<32>(sv);
-          float s[32];
+          uint32_t w[16];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) s[i] = __uint_as_float(sv[i]);
-          st_bf16_pairs(tmem + lane_base + TM_SA + col / 2, s);
+          for (int j = 0; j < 16; ++j) w[j] = pack_bf16x2(-__uint_as_float(sv[2 * j]), -__uint_as_float(sv[2 * j + 1]));
+          tmem_st16(tmem + lane_base + TM_SA + col / 2, w);
+          float s[32];
           const float4 *g4 = reinterpret_cast<const float4 *>(gam + col);
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             const float4 g = g4[i];
-            const float2 lo = mul2(make_float2(s[4 * i], s[4 * i + 1]), make_float2(g.x, g.y));
-            const float2 hi = mul2(make_float2(s[4 * i + 2], s[4 * i + 3]), make_float2(g.z, g.w));
+            const float2 lo = mul2(make_float2(__uint_as_float(sv[4 * i]), __uint_as_float(sv[4 * i + 1])), make_float2(g.x, g.y));
+            const float2 hi = mul2(make_float2(__uint_as_float(sv[4 * i + 2]), __uint_as_float(sv[4 * i + 3])), make_float2(g.z, g.w));
             s[4 * i] = lo.x;
             s[4 * i + 1] = lo.y;
             s[4 * i + 2] = hi.x;
@@ -818,17 +880,24 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_fused_kernel(const __grid
         }
         tmem_wait_st();
       }
-      if (tid == kChainIssuer) bulk_wait_read();   // the staging tile may be rewritten in the next step
       tc_fence_before();
       stop = bar_any<kBarChain>(kChainThreads, *s_abort != 0);
+      if (c > 0 && tid == kChainIssuer) {   // chunk c - 1 is not the last one: all 64 rows are valid
+        const int tok = t0 + (c - 1) * kC;
+        tma_store_3d(&prm.tout, 0, h, tok, stage);
+        tma_store_3d(&prm.tout, 64, h, tok, stage + 8192);
+        bulk_commit();
+      }
     }
 
     // output of the last chunk, and the final state
     if (!stop) {
+      if (tid == kChainIssuer) bulk_wait_read();
       wait_or_abort(&bars[B_FREE], (nchunks - 1) & 1, s_abort, prm.status);
+      named_bar_sync<kBarChain>(kChainThreads);
       tc_fence_after();
       const int last_valid = len - (nchunks - 1) * kC;
-      out_to_stage((nchunks - 1) & 1);
+      out_to_stage(nchunks - 1);
       fence_async_smem();
       named_bar_sync<kBarChain>(kChainThreads);
       if (last_valid == kC) {
