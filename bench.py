@@ -652,7 +652,8 @@ def run_gpu(args):
     del sdev, s_ws, s_out, s_inter
 
     # ---- the other prefill workloads, each timed as its own call (median of per-call CUDA events) ----
-    def time_prefill(pinp, steps, note=None):
+    # (defined here; the main workload's fused-path record is taken after them)
+    def time_prefill(pinp, steps, note=None, path=None):
         pdev = DevicePrefill(pinp, device=device)
         pws = pdev.workspace(device)
         pout = torch.empty((pinp.total_tokens, pinp.H, 128), dtype=torch.bfloat16, device=device)
@@ -660,7 +661,7 @@ def run_gpu(args):
                                                              device=device)
 
         def call():
-            pdev.run(out=pout, final_state=pfinal, workspace=pws, stream=stream)
+            pdev.run(out=pout, final_state=pfinal, workspace=pws, stream=stream, path=path)
 
         for _ in range(3):
             call()
@@ -686,13 +687,22 @@ def run_gpu(args):
                "l2": "inputs larger than L2" if nbytes > L2_BYTES else "fits in L2: launch-latency-bound"}
         if note:
             rec["note"] = note
+        if path:
+            rec["path"] = path
         return rec
+
+    def fused_record(pinp, steps):
+        """The same call on the fused one-kernel path (KDA_FUSED): every chunk's operands stay on chip."""
+        r = time_prefill(pinp, steps, path="fused")
+        return {k: r[k] for k in ("us_per_layer", "tokens_per_s", "calls_timed")} | {
+            "roofline_frac": r["roofline"]["frac"], "kernel": "prefill_fused_kernel (one launch)"}
 
     w_steps = max(20, min(args.steps, 200))
     workloads = {}
     for make in (inputs.tiny_prefill, inputs.prefill_8192x4, inputs.varlen_16384_plus_16):
         winp = make()
         workloads[winp.name] = time_prefill(winp, w_steps)
+        workloads[winp.name]["fused_path"] = fused_record(winp, w_steps)
         if winp.name.startswith("prefill_16384"):
             # the long sequence of this workload alone: its state recurrence is one serial chain of 256 chunks per
             # head, the part of the workload that no number of SMs shortens (the pages quote 16384 x 1 as well)
@@ -704,10 +714,13 @@ def run_gpu(args):
                 cu_seqlens=winp.cu_seqlens[:2].copy())
             rec = time_prefill(long_inp, w_steps)
             rec["us_per_chunk"] = rec["us_per_layer"] / rec["chunks_of_longest"]
+            rec["fused_path"] = fused_record(long_inp, w_steps)
             workloads[winp.name]["long_sequence"] = rec
         if rank == 0 and not args.no_cpu_baseline and world == 1:
             workloads[winp.name]["cpu_baseline"] = cpu_baseline(winp, budget_s=5.0)
         del winp
+
+    main_fused = fused_record(inp, w_steps)
 
     if rank != 0:
         return
@@ -737,6 +750,7 @@ def run_gpu(args):
                               "streams overlap step i's call (double-buffered device buffers)"},
         "gpu_launches": 2 * args.steps,
         "clocks": clocks,
+        "fused_path": main_fused,
         "workloads": workloads,
         "verify": vrec,
         "verify_variants": vvariants,

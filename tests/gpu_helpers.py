@@ -64,6 +64,30 @@ def _token_segments(rows, segments):
     return [(int(a), int(b)) for a, b in zip(cu[:-1], cu[1:]) if b > a]
 
 
+ROW_BINS = ((0.0, 0.05), (0.05, 0.2), (0.2, 0.5), (0.5, 2.0), (2.0, float("inf")))
+
+
+def row_error_bins(x, ref):
+    """Relative error of every (row, head) output vector, binned by its reference norm over the median norm:
+    [(bin, rows, mean, max)].  Informational: a row far below the typical output norm keeps the absolute error
+    of the bf16 products around it, so its relative error grows."""
+    if x.ndim != 3 or not x.size:
+        return []
+    nrm = np.linalg.norm(ref, axis=2).ravel()
+    err = np.linalg.norm(x - ref, axis=2).ravel()
+    live = nrm > 0
+    if not live.any():
+        return []
+    rel = err[live] / nrm[live]
+    scaled = nrm[live] / np.median(nrm[live])
+    out = []
+    for lo, hi in ROW_BINS:
+        m = (scaled >= lo) & (scaled < hi)
+        if m.any():
+            out.append([lo, hi, int(m.sum()), float(rel[m].mean()), float(rel[m].max())])
+    return out
+
+
 def check_out(out_gpu, out_ref, what, segments=None):
     """Outputs ``[rows, H, d]`` against the oracle: tensor-wide rel-L2 and max-abs, and the rel-L2 of every
     (segment, head) pair (``segments`` as in ``_token_segments``), the worst within ``PAIR_FACTOR`` x the bar."""
@@ -81,7 +105,7 @@ def check_out(out_gpu, out_ref, what, segments=None):
             h = int(np.argmax(pr))
             if pr[h] > worst[0]:
                 worst = (float(pr[h]), (a, b, h))
-    _log("out", what, rel_l2=r, max_abs=m, worst_pair=worst[0], worst_at=worst[1])
+    _log("out", what, rel_l2=r, max_abs=m, worst_pair=worst[0], worst_at=worst[1], rows=row_error_bins(x, ref))
     assert r <= OUT_REL_L2 and m <= OUT_MAX_ABS, (
         f"{what}: rel-L2 {r:.3e} (<= {OUT_REL_L2}), max-abs {m:.3e} (<= {OUT_MAX_ABS}); "
         f"worst (rows, head) {worst[1]}: {worst[0]:.3e}")
