@@ -20,15 +20,16 @@ def _parity(inp, token_pad=0, heads=None, path=None):
     assert kda.read_device_status(ws) == 0
     ref_out, ref_S, _ = oracle.run_prefill(inp, heads=heads)
     hb, he = heads or (0, inp.H)
-    check_out(out[:, hb:he], ref_out[:, hb:he], f"{inp.name} outputs", segments=inp.cu_seqlens)
+    tag = f"{inp.name} [{path or 'default'} path]"
+    check_out(out[:, hb:he], ref_out[:, hb:he], f"{tag} outputs", segments=inp.cu_seqlens)
     if inp.final_to_pool:
         got = dev.pool[torch.from_numpy(inp.slot_ids).long().cuda()]
-        check_state(got[:, hb:he], ref_S[:, hb:he], f"{inp.name} final states (pool)")
+        check_state(got[:, hb:he], ref_S[:, hb:he], f"{tag} final states (pool)")
         untouched = np.setdiff1d(np.arange(inp.pool.shape[0]), inp.slot_ids)
         idx = torch.from_numpy(untouched).long().cuda()
         assert torch.equal(dev.pool[idx], pool_before[idx]), "pool slots not in slot_ids were modified"
     else:
-        check_state(final[:, hb:he], ref_S[:, hb:he], f"{inp.name} final states")
+        check_state(final[:, hb:he], ref_S[:, hb:he], f"{tag} final states")
         if pool_before is not None:
             assert torch.equal(dev.pool, pool_before), "pool modified without KDA_FINAL_TO_POOL"
     return out, final
