@@ -85,6 +85,8 @@ KERNEL_SOURCES = {
     "prefill": ("kda_chunk_intra.cu", "kda_chunk_chain.cu", "kda_prefill.cu", "kda_prefill_block.h", "kda_sm100.cuh",
                 "kda_common.cuh", "kda_internal.h"),
     "verify": ("kda_recurrent.cu", "kda_common.cuh", "kda_internal.h"),
+    "prefill_fused": ("kda_prefill_fused.cu", "kda_prefill.cu", "kda_prefill_block.h", "kda_sm100.cuh", "kda_common.cuh",
+                      "kda_internal.h"),
 }
 
 
@@ -694,8 +696,12 @@ def run_gpu(args):
     def fused_record(pinp, steps):
         """The same call on the fused one-kernel path (KDA_FUSED): every chunk's operands stay on chip."""
         r = time_prefill(pinp, steps, path="fused")
-        return {k: r[k] for k in ("us_per_layer", "tokens_per_s", "calls_timed")} | {
+        rec = {k: r[k] for k in ("us_per_layer", "tokens_per_s", "calls_timed")} | {
             "roofline_frac": r["roofline"]["frac"], "kernel": "prefill_fused_kernel (one launch)"}
+        if pinp.name == WORKLOAD:   # DRAM bytes of one call from the committed ncu record (2048 x 8)
+            rec["traffic"] = recorded_traffic("prefill_fused")
+            rec["algorithmic_bytes"] = r["roofline"]["algorithmic_bytes"]
+        return rec
 
     w_steps = max(20, min(args.steps, 200))
     workloads = {}
