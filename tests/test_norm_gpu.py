@@ -102,7 +102,8 @@ def test_spec_step_gated_norm_matches_the_plain_calls():
                                           workspace=ws2)
     p_out, _ = kda.chunk_prefill(pre.q, pre.k, pre.v, pre.g, pre.beta, pre.A_log, pre.dt_bias, pre.cu, pre.cu_host,
                                  lower_bound=p.lower_bound, scale=p.scale, state_pool=pool, slot_ids=pre.slots,
-                                 load_initial=p.load_initial, final_to_pool=p.final_to_pool, norm=pn, workspace=ws2)
+                                 load_initial=p.load_initial, final_to_pool=p.final_to_pool, norm=pn, workspace=ws2,
+                                 path="two_pass")   # the spec step runs the two-kernel path
     torch.cuda.synchronize()
     assert kda.read_device_status(ws2) == 0
     assert torch.equal(out[ns], p_out) and torch.equal(norm.rstd[ns], pn.rstd)

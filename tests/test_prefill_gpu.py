@@ -35,11 +35,12 @@ def _parity(inp, token_pad=0, heads=None, path=None):
     return out, final
 
 
-def test_tiny_1x256_h2():
-    _parity(inputs.tiny_prefill())
+@pytest.mark.parametrize("path", [None, "two_pass", "fused"])
+def test_tiny_1x256_h2(path):
+    _parity(inputs.tiny_prefill(), path=path)
 
 
-PATHS = [None, "fused"]   # the library's pick, and the fused kernel forced
+PATHS = ["two_pass", "fused"]   # both execution paths forced (the library picks one of them by shape)
 
 
 @pytest.mark.parametrize("path", PATHS)

@@ -31,7 +31,8 @@ def _separate_calls(dev):
         p_out, final = kda.chunk_prefill(pre.q, pre.k, pre.v, pre.g, pre.beta, pre.A_log, pre.dt_bias, pre.cu,
                                          pre.cu_host, lower_bound=p.lower_bound, scale=p.scale, state_pool=pool,
                                          slot_ids=pre.slots, load_initial=p.load_initial,
-                                         final_to_pool=p.final_to_pool, workspace=ws)
+                                         final_to_pool=p.final_to_pool, workspace=ws,
+                                         path="two_pass")   # the spec step runs the two-kernel path
     torch.cuda.synchronize()
     assert kda.read_device_status(ws) == 0
     return p_out, final, v_out, inter, pool
