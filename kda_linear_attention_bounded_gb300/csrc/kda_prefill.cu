@@ -81,19 +81,19 @@ int sm_count() {
 }
 
 // The path the library takes when the caller does not force one.  The fused kernel walks a sequence's chunks
-// one at a time at ~8 us per chunk (its producer's serial phases), the two-kernel path spends ~40 us in two
-// launches before its state pass and then ~2 us per chunk; so the fused kernel wins only on short sequences
-// whose (sequence, head) pairs fill at most about one wave of SMs.  Measured on GB300 (H = 16, median of 30
-// calls): 1-4 chunks per sequence with up to 152 pairs 36-40 us fused against 43-46 us; 8 x 512 (8 chunks)
-// 70 against 68; 16 x 256 (4 chunks, 256 pairs) 79 against 78; 1-chunk sequences at 512-2048 pairs 60-197 against
-// 61-202; 2048 x 8 245 against 207.
+// one at a time at ~7 us per chunk (its producer's serial phases); the two-kernel path runs every chunk's
+// producer work at once and then ~2 us per chunk of state pass.  Measured on GB300 as CUDA-graph replays
+// (device time, H = 16): one-chunk sequences with up to 152 (sequence, head) pairs 12.9 us fused against
+// 15.0 us; from two chunks per sequence on the two-kernel path is faster (1 x 128: 17.0 against 20.7 us,
+// 1 x 256: 20.5 against 34.8 us, 2048 x 8: 207 against 245 us).  So the fused kernel is picked for one-chunk
+// sequences that fit one wave of SMs.
 bool fused_prefill_preferred(const ChunkArgs &a, const int32_t *cu_host) {
   if (!fused_prefill_applies(a)) return false;
-  int max_chunks = 0;
-  for (int i = 0; i < a.num_seqs; ++i) max_chunks = std::max(max_chunks, (cu_host[i + 1] - cu_host[i] + kChunk - 1) / kChunk);
+  for (int i = 0; i < a.num_seqs; ++i)
+    if (cu_host[i + 1] - cu_host[i] > kChunk) return false;
   const long pairs = static_cast<long>(a.num_seqs) * a.H;
   const long sms = sm_count() > 0 ? sm_count() : 152;
-  return max_chunks <= 1 || (max_chunks <= 2 && pairs <= 2 * sms) || (max_chunks <= 4 && pairs <= sms);
+  return pairs <= sms;
 }
 
 cudaError_t launch_fused(const ChunkArgs &a, const int32_t *cu_host, cudaStream_t stream) {
