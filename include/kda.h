@@ -83,15 +83,28 @@ extern "C" {
 /* ---- flags of kda_chunk_prefill ------------------------------------------ */
 #define KDA_LOAD_INITIAL 1  /* S0 of sequence n = state_pool[slot_ids[n]]; else S0 = 0          */
 #define KDA_FINAL_TO_POOL 2 /* final state of sequence n -> state_pool[slot_ids[n]]; else dense */
-/* Execution path of kda_chunk_prefill (at most one of the two; neither: the library picks).  Both paths
- * compute the same result within rounding.
+/* Execution path of kda_chunk_prefill (at most one of the three; none: the library picks).  All paths
+ * compute the same result within rounding; KDA_TWO_PASS and KDA_OVERLAP the same bits.
  *  KDA_TWO_PASS  the intra-chunk kernel over every chunk and head, then the state pass over every
  *                (sequence, head), the chunks' operands handed over through the workspace;
  *  KDA_FUSED     one kernel, one CTA per (sequence, head), every chunk's operands kept on chip; it
  *                applies without short convolutions and with lower_bound >= -5 (else the call returns
- *                KDA_ERR_UNSUPPORTED). */
+ *                KDA_ERR_UNSUPPORTED);
+ *  KDA_OVERLAP   the kernels of KDA_TWO_PASS, with the state passes of the longest sequences (as many as fit
+ *                in half of the SMs) split into segments of whole chunks: each segment's state pass runs on
+ *                a high-priority stream of the library's (one per calling thread and device) as soon as that
+ *                segment's intra-chunk launch has completed, beside the intra-chunk work of the later
+ *                segments and of the other sequences; the caller's stream waits for it before the call's
+ *                last work.  Without short convolutions only, and not in kda_spec_step (else
+ *                KDA_ERR_UNSUPPORTED); the workspace must hold kda_prefill_workspace_size() bytes (else
+ *                KDA_ERR_WORKSPACE).  Inside a stream capture it takes the KDA_TWO_PASS schedule until
+ *                the calling thread has made one call outside a capture (which creates the stream).
+ * With no path flag the library takes KDA_FUSED for sequences of one chunk that fit one wave of SMs,
+ * KDA_OVERLAP where the longest sequence has 64 chunks or more and every sequence of at least half its
+ * length fits the split's budget (and the workspace holds the scratch), else KDA_TWO_PASS. */
 #define KDA_TWO_PASS 4
 #define KDA_FUSED 8
+#define KDA_OVERLAP 16
 
 /*
  * q, k, v, g and beta_logits of one set of tokens, laid out as in the
@@ -171,7 +184,10 @@ KDA_API size_t kda_workspace_size(void);
  * Bytes of workspace kda_chunk_prefill needs for total_tokens tokens in
  * num_seqs sequences and H heads: kda_workspace_size() plus, for every chunk of
  * 64 tokens and head, the 74240-byte block the intra-chunk kernel hands to the
- * state pass (an upper bound: floor(total_tokens / 64) + num_seqs chunks).
+ * state pass (an upper bound: floor(total_tokens / 64) + num_seqs chunks), plus
+ * 64 KiB for each of min(num_seqs * H, 96) (sequence, head) states that split
+ * state passes (KDA_OVERLAP) hand from one segment to the next.  A call given
+ * the blocks but not that scratch runs without the split.
  * Returns 0 for negative sizes or H <= 0.
  */
 KDA_API size_t kda_prefill_workspace_size(int64_t total_tokens, int num_seqs, int H);
@@ -216,13 +232,16 @@ KDA_API int kda_read_device_status(const void *workspace, size_t workspace_bytes
  *                   unless KDA_FINAL_TO_POOL (then ignored, may be NULL).
  *  Inputs and outputs must not overlap, except state_pool which may be both
  *  read and written (each sequence reads its slot before writing it).
- *  workspace        at least kda_prefill_workspace_size(cu_seqlens_host[num_seqs],
- *                   num_seqs, H) bytes (KDA_ERR_WORKSPACE otherwise); its first
- *                   word is the device status word, the rest is scratch that
- *                   the call overwrites (the fused path uses only the header).
+ *  workspace        kda_prefill_workspace_size(cu_seqlens_host[num_seqs],
+ *                   num_seqs, H) bytes (fewer than its header and blocks:
+ *                   KDA_ERR_WORKSPACE; without its scratch states the call
+ *                   takes no split schedule); its first word is the device
+ *                   status word, the rest is scratch that the call overwrites
+ *                   (the fused path uses only the header).
  *                   Concurrent calls need separate workspaces.
  *  flags            KDA_LOAD_INITIAL | KDA_FINAL_TO_POOL, and at most one of
- *                   KDA_TWO_PASS, KDA_FUSED; other bits: KDA_ERR_INVALID_ARG.
+ *                   KDA_TWO_PASS, KDA_FUSED, KDA_OVERLAP; other bits:
+ *                   KDA_ERR_INVALID_ARG.
  */
 KDA_API int kda_chunk_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                       int64_t qkv_token_stride, const uint16_t *g, int64_t g_token_stride,

@@ -28,6 +28,7 @@ KDA_LOAD_INITIAL = 1
 KDA_FINAL_TO_POOL = 2
 KDA_TWO_PASS = 4
 KDA_FUSED = 8
+KDA_OVERLAP = 16
 KDA_PAD_SLOT_ID = -1
 KDA_CONV_NONE = 0
 KDA_CONV_SILU = 1
@@ -225,7 +226,8 @@ def chunk_prefill(q, k, v, g, beta_logits, A_log, dt_bias, cu_seqlens, cu_seqlen
                   stream=None, path=None):
     """``kda_chunk_prefill``.  Returns ``(out, final_state)`` (final_state is None
     when the final states go to the pool).  ``norm``: an :class:`OutputNorm` applied to the output rows.
-    ``path``: None (the library picks), ``"two_pass"`` (``KDA_TWO_PASS``) or ``"fused"`` (``KDA_FUSED``)."""
+    ``path``: None (the library picks), ``"two_pass"`` (``KDA_TWO_PASS``), ``"fused"`` (``KDA_FUSED``) or
+    ``"overlap"`` (``KDA_OVERLAP``)."""
     lib = load()
     H = q.shape[1]
     qs = _token_tensor(q, "q", H)
@@ -247,7 +249,7 @@ def chunk_prefill(q, k, v, g, beta_logits, A_log, dt_bias, cu_seqlens, cu_seqlen
     if workspace is None:
         workspace = make_workspace(dev, stream, prefill_workspace_size(T_total, N, H))
     flags = (KDA_LOAD_INITIAL if load_initial else 0) | (KDA_FINAL_TO_POOL if final_to_pool else 0) | \
-        {None: 0, "two_pass": KDA_TWO_PASS, "fused": KDA_FUSED}[path]
+        {None: 0, "two_pass": KDA_TWO_PASS, "fused": KDA_FUSED, "overlap": KDA_OVERLAP}[path]
     if scale is None:
         scale = 1.0 / math.sqrt(128.0)
     rc = lib.kda_chunk_prefill(

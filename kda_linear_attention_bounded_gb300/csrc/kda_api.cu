@@ -11,9 +11,12 @@
 
 namespace {
 
-constexpr size_t kWorkspaceBytes = 256;
+constexpr size_t kWorkspaceBytes = 1024;
 static_assert(kda::kDoneCounterOffset + sizeof(uint32_t) <= kWorkspaceBytes,
               "the spec step's CTA counter must sit in the cleared header");
+static_assert(kda::kSplitCounterOffset >= kda::kDoneCounterOffset + sizeof(uint32_t) &&
+                  kda::kSplitCounterOffset + kda::kMaxSplitCounters * sizeof(uint32_t) <= kWorkspaceBytes,
+              "the split schedule's counters lie in the part kda_workspace_reset clears");
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -91,8 +94,10 @@ int prepare_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v, int
   if (int rc = check_workspace(workspace, workspace_bytes)) return rc;
   if (num_seqs < 0) return KDA_ERR_INVALID_ARG;
   if (!cu_seqlens_dev || !cu_seqlens_host) return KDA_ERR_INVALID_ARG;
-  if (flags & ~(KDA_LOAD_INITIAL | KDA_FINAL_TO_POOL | KDA_TWO_PASS | KDA_FUSED)) return KDA_ERR_INVALID_ARG;
-  if ((flags & KDA_TWO_PASS) && (flags & KDA_FUSED)) return KDA_ERR_INVALID_ARG;
+  if (flags & ~(KDA_LOAD_INITIAL | KDA_FINAL_TO_POOL | KDA_TWO_PASS | KDA_FUSED | KDA_OVERLAP))
+    return KDA_ERR_INVALID_ARG;
+  const int path_flags = flags & (KDA_TWO_PASS | KDA_FUSED | KDA_OVERLAP);
+  if (path_flags & (path_flags - 1)) return KDA_ERR_INVALID_ARG;   // at most one path
   if (cu_seqlens_host[0] != 0) return KDA_ERR_INVALID_ARG;
   for (int n = 0; n < num_seqs; ++n)
     if (cu_seqlens_host[n + 1] < cu_seqlens_host[n]) return KDA_ERR_INVALID_ARG;
@@ -129,8 +134,15 @@ int prepare_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v, int
   a->status = static_cast<uint32_t *>(workspace);
   a->path = (flags & KDA_TWO_PASS) ? kda::PrefillPath::kTwoPass
             : (flags & KDA_FUSED)  ? kda::PrefillPath::kFused
+            : (flags & KDA_OVERLAP) ? kda::PrefillPath::kOverlap
                                    : kda::PrefillPath::kAuto;
   if (a->path == kda::PrefillPath::kFused && !kda::fused_prefill_applies(*a)) return KDA_ERR_UNSUPPORTED;
+  if (a->path == kda::PrefillPath::kOverlap) {
+    if (!kda::overlap_prefill_applies(*a)) return KDA_ERR_UNSUPPORTED;
+    if (workspace_bytes < kda::prefill_workspace_bytes(cu_seqlens_host[num_seqs], num_seqs, H) +
+                              kda::overlap_scratch_bytes(num_seqs, H))
+      return KDA_ERR_WORKSPACE;
+  }
   return KDA_OK;
 }
 
@@ -220,7 +232,7 @@ size_t kda_workspace_size(void) { return kWorkspaceBytes; }
 
 size_t kda_prefill_workspace_size(int64_t total_tokens, int num_seqs, int H) {
   if (total_tokens < 0 || num_seqs < 0 || H <= 0) return 0;
-  return kda::prefill_workspace_bytes(total_tokens, num_seqs, H);
+  return kda::prefill_workspace_bytes(total_tokens, num_seqs, H) + kda::overlap_scratch_bytes(num_seqs, H);
 }
 
 int kda_workspace_reset(void *workspace, size_t workspace_bytes, void *stream) {
@@ -256,7 +268,8 @@ int kda_chunk_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v, i
     return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t err = kda::launch_chunk_prefill(a, cu_seqlens_host,
-                                              static_cast<uint8_t *>(workspace) + kda::kWorkspaceHeader, st);
+                                              static_cast<uint8_t *>(workspace) + kda::kWorkspaceHeader,
+                                              workspace_bytes - kda::kWorkspaceHeader, st);
   if (err == cudaSuccess) err = launch_prefill_norm(a, st);
   return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
@@ -307,6 +320,8 @@ int kda_spec_step(const kda_token_tensors *prefill, const int32_t *cu_seqlens_de
                                 intermediate_states, workspace, workspace_bytes, &va))
       return rc;
   }
+  // the step's prefill rows go out by index, which the split state passes do not take
+  if (pa.path == kda::PrefillPath::kOverlap) return KDA_ERR_UNSUPPORTED;
   const bool has_prefill = pa.num_seqs > 0 && pa.total_tokens > 0, has_spec = B > 0;
   if ((has_prefill && !non_spec_token_indx) || (has_spec && !spec_token_indx)) return KDA_ERR_INVALID_ARG;
   if (num_out_tokens > INT32_MAX) return KDA_ERR_INVALID_ARG;
@@ -319,7 +334,7 @@ int kda_spec_step(const kda_token_tensors *prefill, const int32_t *cu_seqlens_de
   // pass occupies one SM per (sequence, head) and the verify CTAs fill the others while it runs
   if (pa.num_seqs > 0) {
     if (kda::launch_chunk_prefill(pa, cu_seqlens_host, static_cast<uint8_t *>(workspace) + kda::kWorkspaceHeader,
-                                  st) != cudaSuccess)
+                                  workspace_bytes - kda::kWorkspaceHeader, st) != cudaSuccess)
       return KDA_ERR_CUDA;
     va.done_counter = reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(workspace) + kda::kDoneCounterOffset);
   }

@@ -1,6 +1,8 @@
 // State pass of the chunked KDA prefill on sm_103a.
 //
-// One CTA per (sequence, head) walks the sequence's chunks in order with the
+// One CTA per (item, head) walks the item's chunks in order -- a whole
+// sequence, or one segment of it when a long sequence's state pass is split
+// (the state then arrives from and leaves to an fp32 scratch copy) -- with the
 // state S (128 key x 128 value channels, fp32) resident in TMEM, and applies
 // the state-dependent half of the chunk algebra to each chunk's block from the
 // intra-chunk kernel (kda_prefill_block.h):
@@ -80,33 +82,46 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_chain_kernel(const __grid_c
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int H = prm.H;
   const int h = blockIdx.x % H;
-  const int nl = static_cast<int>(prm.order[blockIdx.x / H]);   // local sequence, longest first
-  const int n = prm.seq0 + nl;
-  const int t0 = prm.tok_off[nl];
-  const int len = prm.tok_off[nl + 1] - t0;
-  const int nchunks = prm.chunk_off[nl + 1] - prm.chunk_off[nl];
+  const int nl = static_cast<int>(prm.order[blockIdx.x / H]);   // item, longest first
+  const int n = prm.seq[nl];
+  const int t0 = prm.tok0[nl];
+  const int len = prm.len[nl];
+  const int nchunks = (len + kC - 1) / kC;
+  const uint8_t item_flags = prm.flags[nl];
   const uint8_t *blk0 = prm.blocks + (static_cast<size_t>(prm.chunk_off[nl]) * H + h) * kBlkBytes;
   const size_t blk_step = static_cast<size_t>(H) * kBlkBytes;
 
   // every CTA of this grid has started once all have passed here: a grid launched after it as a programmatic
-  // dependent (the verify segment of a spec step) may then use the SMs this grid leaves free
-  grid_launch_dependents();
+  // dependent (the verify segment of a spec step, the next intra-chunk launch of a split schedule) may then use
+  // the SMs this grid leaves free
+  if (!prm.trigger_after_wait) grid_launch_dependents();
+  // the CTA that finishes last waits for the preceding grid (done_counter set; every exit passes here)
+  auto finish = [&] {
+    if (prm.done_counter && tid == 0 && atomicAdd(prm.done_counter, 1u) == gridDim.x - 1) {
+      grid_dependency_wait();
+      *prm.done_counter = 0;
+    }
+  };
 
   int slot = 0;
   if (prm.slot_ids) {
     slot = prm.slot_ids[n];
     if (slot < 0 || slot >= prm.num_slots) {
       if (tid == 0) atomicOr(prm.status, KDA_DEVICE_BAD_SLOT);
+      finish();
       return;
     }
   }
-  float *dst = prm.state_out_pool ? prm.state_out_pool + (static_cast<size_t>(slot) * H + h) * kD * kD
-                                  : prm.state_out_dense + (static_cast<size_t>(n) * H + h) * kD * kD;
+  float *mid = prm.state_mid ? prm.state_mid + (static_cast<size_t>(prm.mid[nl]) * H + h) * kD * kD : nullptr;
+  float *dst = (item_flags & kItemToMid) ? mid
+               : prm.state_out_pool     ? prm.state_out_pool + (static_cast<size_t>(slot) * H + h) * kD * kD
+                                        : prm.state_out_dense + (static_cast<size_t>(n) * H + h) * kD * kD;
   // epilogue thread = (value channel d, half hv of the key channels / tokens)
   const bool worker = warp < 8;
   const int quad = warp & 3, hv = (warp >> 2) & 1;
   const int d = quad * 32 + lane;
-  const float *src = prm.state_in ? prm.state_in + (static_cast<size_t>(slot) * H + h) * kD * kD : nullptr;
+  const float *src = (item_flags & kItemFromMid) ? mid
+                     : prm.state_in ? prm.state_in + (static_cast<size_t>(slot) * H + h) * kD * kD : nullptr;
 
   // The sequence's final short-convolution window (with conv): the last 3 raw inputs of q, k and v, rows of the
   // initial window (the slot's, else zeros) where the sequence has fewer than 3 tokens.  Every piece is read
@@ -144,6 +159,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_chain_kernel(const __grid_c
       const int kd = kd_of_rho(64 * hv + i);
       dst[static_cast<size_t>(kd) * kD + d] = src ? src[static_cast<size_t>(kd) * kD + d] : 0.f;
     }
+    finish();
     return;
   }
 
@@ -153,7 +169,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_chain_kernel(const __grid_c
     fence_mbar_init();
     // this grid may start while the intra-chunk grid is still finishing: the blocks are read only once it
     // has completed and its writes are visible (everything above and the initial state do not depend on it)
-    grid_dependency_wait();
+    if (prm.wait_blocks) grid_dependency_wait();
     for (int c = 0; c < kNumBuf && c < nchunks; ++c) {
       mbar_arrive_expect_tx(&bar_full[c], kBlkBytes);
       bulk_load(sm + c * kBufStride, blk0 + c * blk_step, kBlkBytes, &bar_full[c]);
@@ -166,6 +182,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_chain_kernel(const __grid_c
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (prm.trigger_after_wait) grid_launch_dependents();   // the blocks' grid has completed
   const uint32_t tmem = *s_tmem;
   const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
 
@@ -401,7 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_chain_kernel(const __grid_c
       for (int i = 0; i < 32; ++i) dst[static_cast<size_t>(kd_of_rho(col + i)) * kD + d] = __uint_as_float(sv[i]);
     }
   }
-  if (prm.conv.weight) write_window([] { __syncthreads(); });
+  if (prm.conv.weight && !(item_flags & kItemToMid)) write_window([] { __syncthreads(); });
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -409,11 +426,12 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_chain_kernel(const __grid_c
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+  finish();
 }
 
 }  // namespace
 
-cudaError_t launch_chunk_chain(const ChainParams &p, cudaStream_t stream) {
+cudaError_t launch_chunk_chain(const ChainParams &p, cudaStream_t stream, bool programmatic) {
   if (p.num_seqs <= 0) return cudaSuccess;
   static bool attr_set = false;
   if (!attr_set) {
@@ -432,7 +450,7 @@ cudaError_t launch_chunk_chain(const ChainParams &p, cudaStream_t stream) {
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = programmatic ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, chunk_chain_kernel, p);
 }
 

@@ -865,12 +865,19 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_c
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+  // launched behind a state pass (a split prefill schedule): the CTA that finishes last waits for that grid's
+  // completion, so that this grid completes after it (the next state pass waits for this grid and reads the state
+  // the previous one wrote); it then clears the counter for the next call
+  if (prm.done_counter && tid == 0 && atomicAdd(prm.done_counter, 1u) == gridDim.x - 1) {
+    grid_dependency_wait();
+    *prm.done_counter = 0;
+  }
   // ------------------------------------------------------------ end
 }
 
 }  // namespace
 
-cudaError_t launch_chunk_intra(const IntraParams &p, int num_chunks, cudaStream_t stream) {
+cudaError_t launch_chunk_intra(const IntraParams &p, int num_chunks, cudaStream_t stream, bool programmatic) {
   if (num_chunks <= 0) return cudaSuccess;
   static bool attr_set = false;
   if (!attr_set) {
@@ -884,8 +891,23 @@ cudaError_t launch_chunk_intra(const IntraParams &p, int num_chunks, cudaStream_
   const bool blk32 = p.lower_bound >= kLowerBound32, conv = p.conv.weight != nullptr;
   auto fn = blk32 ? (conv ? chunk_intra_kernel<32, true> : chunk_intra_kernel<32, false>)
                   : (conv ? chunk_intra_kernel<16, true> : chunk_intra_kernel<16, false>);
-  fn<<<num_chunks * p.H, kThreads, kSmemBytes, stream>>>(p);
-  return cudaGetLastError();
+  if (!programmatic) {
+    fn<<<num_chunks * p.H, kThreads, kSmemBytes, stream>>>(p);
+    return cudaGetLastError();
+  }
+  // a programmatic dependent of the preceding state pass: CTAs are scheduled onto the SMs that grid leaves free
+  // once each of its CTAs has started
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(num_chunks * p.H);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fn, p);
 }
 
 }  // namespace kda

@@ -59,6 +59,10 @@ struct RecurrentArgs {
 // Byte offset in the workspace of the counter a programmatic-dependent verify grid counts its CTAs with
 // (inside the part kda_workspace_reset clears).
 constexpr size_t kDoneCounterOffset = 128;
+// Counters of the launches of a split prefill schedule (one per launch that waits for its predecessor, at most
+// kMaxSplitCounters), from this byte offset of the workspace (also inside the cleared part).
+constexpr size_t kSplitCounterOffset = 256;
+constexpr int kMaxSplitCounters = 160;
 
 cudaError_t launch_recurrent(const RecurrentArgs &args, int num_items, cudaStream_t stream);
 
@@ -71,7 +75,7 @@ int check_verify_call(const uint16_t *q, const uint16_t *k, const uint16_t *v, i
                       const int32_t *slot_ids, uint16_t *out, int64_t out_token_stride, float *intermediate_states,
                       void *workspace, size_t workspace_bytes);
 
-enum class PrefillPath { kAuto, kTwoPass, kFused };
+enum class PrefillPath { kAuto, kTwoPass, kFused, kOverlap };
 
 // Arguments of the chunked prefill kernel.
 struct ChunkArgs {
@@ -140,6 +144,9 @@ struct IntraParams {
   int num_slots;                // a slot outside [0, num_slots) reads a zero window (the state pass reports it)
   int seq0;
   int conv_load_initial;        // first chunks start from the slot's window (else from zeros)
+  // non-null: the grid is launched as a programmatic dependent of a state pass (split state passes), and the CTA
+  // that finishes last waits for that grid's completion through this zeroed counter in the workspace header
+  uint32_t *done_counter;
   int32_t slot_tok0[kMaxSlotsPerLaunch];   // first token of each local chunk slot
   uint8_t slot_valid[kMaxSlotsPerLaunch];  // its tokens (1..64) | kSlotFirst for a sequence's first chunk
   int16_t slot_seq[kMaxSlotsPerLaunch];    // its sequence, local to the group
@@ -147,15 +154,20 @@ struct IntraParams {
 constexpr uint8_t kSlotFirst = 128;
 static_assert(sizeof(IntraParams) <= 32764, "kernel parameters are limited to 32764 bytes");
 
-// State pass: one CTA per (sequence, head) of a group.
+// State pass: one CTA per (item, head).  An item is a run of whole chunks of one sequence: the whole sequence,
+// or one segment of it when a long sequence's state pass is split (its state then passes from one segment to the
+// next through `state_mid`, in fp32 and in the caller's layout).
+constexpr uint8_t kItemFromMid = 1;   // the item's initial state is state_mid[mid] (else the pool slot / zero)
+constexpr uint8_t kItemToMid = 2;     // its final state goes to state_mid[mid] (else the pool slot / dense)
 struct ChainParams {
   CUtensorMap tout;             // output [tokens, H, 128] bf16, box 64 channels x 1 head x 64 tokens
   const uint8_t *blocks;
-  const int32_t *slot_ids;      // indexed by seq0 + local sequence
+  const int32_t *slot_ids;      // indexed by the item's sequence
   int num_slots;
   const float *state_in;
   float *state_out_pool;
-  float *state_out_dense;       // indexed by seq0 + local sequence
+  float *state_out_dense;       // indexed by the item's sequence
+  float *state_mid;             // [segmented sequences, H, 128, 128] fp32, or null
   uint16_t *out;
   int64_t out_stride;
   const int32_t *out_index;     // output row of each token (global token index), or null (row = token)
@@ -168,11 +180,28 @@ struct ChainParams {
   int64_t qkv_stride;
   int conv_load_initial;
   uint32_t *status;
-  int H, num_seqs, seq0;
-  int32_t chunk_off[kMaxSeqsPerLaunch + 1];
-  int32_t tok_off[kMaxSeqsPerLaunch + 1];
-  uint16_t order[kMaxSeqsPerLaunch];          // local sequences, longest first
+  // Programmatic dependent launch.  wait_blocks: one thread waits for the preceding grid (the intra-chunk
+  // launch that wrote this launch's blocks) before the first block is read; else the blocks are complete when
+  // the grid is launched.  trigger_after_wait: the grid lets its own dependent launch only once that wait has
+  // returned (else at its start).  done_counter (non-null): a zeroed counter in the workspace header through
+  // which the CTA that finishes last waits for the preceding grid's completion.
+  int wait_blocks, trigger_after_wait;
+  uint32_t *done_counter;
+  int H, num_seqs;              // num_seqs: items of the launch
+  int32_t chunk_off[kMaxSeqsPerLaunch];       // first block of each item (its ceil(len / 64) blocks follow)
+  int32_t tok0[kMaxSeqsPerLaunch];            // first token of each item
+  int32_t len[kMaxSeqsPerLaunch];             // its tokens
+  int32_t seq[kMaxSeqsPerLaunch];             // its sequence (index into slot_ids, state_out_dense, windows)
+  uint8_t flags[kMaxSeqsPerLaunch];           // kItemFromMid | kItemToMid
+  uint8_t mid[kMaxSeqsPerLaunch];             // its state's index in state_mid
+  uint16_t order[kMaxSeqsPerLaunch];          // items, longest first
 };
+static_assert(sizeof(ChainParams) <= 32764, "kernel parameters are limited to 32764 bytes");
+
+// (sequence, head) pairs whose state passes may be split into segments at once, and the fp32 scratch their
+// states pass through between segments (placed after the blocks in the prefill workspace)
+constexpr int kMaxOverlapPairs = 96;
+size_t overlap_scratch_bytes(int num_seqs, int H);
 
 // Fused prefill: one CTA per (sequence, head) of a group builds each chunk's WY operands and runs the state
 // recurrence over them without leaving the SM (kda_prefill_fused.cu).
@@ -212,13 +241,20 @@ struct GatedNormArgs {
 
 cudaError_t launch_gated_norm(const GatedNormArgs &args, cudaStream_t stream);
 
-cudaError_t launch_chunk_intra(const IntraParams &p, int num_chunks, cudaStream_t stream);
-cudaError_t launch_chunk_chain(const ChainParams &p, cudaStream_t stream);
+// programmatic: launched as a programmatic dependent of the preceding grid in the stream (a state pass)
+cudaError_t launch_chunk_intra(const IntraParams &p, int num_chunks, cudaStream_t stream, bool programmatic);
+// programmatic: launched as a programmatic dependent of the preceding grid in the stream (the intra-chunk grid)
+cudaError_t launch_chunk_chain(const ChainParams &p, cudaStream_t stream, bool programmatic);
 
-// Bytes of workspace kda_chunk_prefill needs (status header + one block per chunk and head).
+// Bytes of workspace kda_chunk_prefill needs (status header + one block per chunk and head); the split state
+// passes also need overlap_scratch_bytes after the blocks.
 size_t prefill_workspace_bytes(int64_t total_tokens, int num_seqs, int H);
 
+// Whether a call's state passes may be split into segments at all (no short convolutions, rows in token order).
+bool overlap_prefill_applies(const ChunkArgs &args);
+
+// blocks: the workspace after its header, blocks_bytes long
 cudaError_t launch_chunk_prefill(const ChunkArgs &args, const int32_t *cu_seqlens_host, uint8_t *blocks,
-                                 cudaStream_t stream);
+                                 size_t blocks_bytes, cudaStream_t stream);
 
 }  // namespace kda

@@ -62,7 +62,7 @@ FAKE = 0x10000000
 P = ctypes.c_void_p
 
 
-def _prefill(lib, *, cu=(0, 4), H=2, lb=-5.0, scale=0.1, ws=FAKE, ws_bytes=256, stride=256, flags=0,
+def _prefill(lib, *, cu=(0, 4), H=2, lb=-5.0, scale=0.1, ws=FAKE, ws_bytes=1024, stride=256, flags=0,
              q=FAKE, final=FAKE, pool=None, slots=None, nslots=0, norm=None, conv=None):
     cu_host = np.array(cu, np.int32)
     return lib.kda_chunk_prefill(P(q), P(FAKE), P(FAKE), stride, P(FAKE), stride, P(FAKE), H, P(FAKE), P(FAKE),
@@ -73,7 +73,7 @@ def _prefill(lib, *, cu=(0, 4), H=2, lb=-5.0, scale=0.1, ws=FAKE, ws_bytes=256, 
 def _verify(lib, *, B=2, T=8, H=2, lb=-5.0, ws=FAKE, pool=FAKE, inter=FAKE, norm=None, conv=None):
     return lib.kda_recurrent_verify(P(FAKE), P(FAKE), P(FAKE), H * 128, P(FAKE), H * 128, P(FAKE), H, P(FAKE),
                                     P(FAKE), lb, 0.1, B, T, H, P(pool), 4, P(FAKE), P(FAKE), H * 128, norm, conv,
-                                    P(inter), P(ws), 256, None)
+                                    P(inter), P(ws), 1024, None)
 
 
 def _conv(weight=FAKE, act=1, pool=FAKE, dense=None, steps=FAKE):
@@ -102,24 +102,32 @@ def test_prefill_rejects_bad_arguments(lib):
     assert _prefill(lib, q=None) == 1
     assert _prefill(lib, final=None) == 1              # dense final state required
     assert _prefill(lib, flags=1) == 1                 # pool + slot ids required
-    assert _prefill(lib, flags=16) == 1                # unknown flag
-    assert _prefill(lib, flags=4 | 8) == 1             # both execution paths forced
+    assert _prefill(lib, flags=32) == 1                # unknown flag
+    assert _prefill(lib, flags=4 | 8) == 1             # two execution paths forced
+    assert _prefill(lib, flags=4 | 16) == 1
+    assert _prefill(lib, flags=8 | 16) == 1
     assert _prefill(lib, flags=8, lb=-6.0, ws_bytes=1 << 30) == 2   # the fused path takes lower_bound >= -5 only
+    # the split state passes take no short convolutions
+    assert _prefill(lib, flags=16, conv=_conv(dense=FAKE), ws_bytes=1 << 30) == 2
     assert _prefill(lib, H=0) == 1
     assert _prefill(lib, cu=(0,)) == 0                 # no sequences: nothing to do
     # valid arguments but a workspace without room for the chunk blocks
     need = lib.kda_prefill_workspace_size(4, 1, 2)
-    assert _prefill(lib, ws_bytes=need - 256) == 3
+    scratch = 2 * 128 * 128 * 4                        # one sequence x two heads of fp32 state
+    assert _prefill(lib, ws_bytes=need - scratch - 256) == 3
+    # forced split state passes with the blocks but without the scratch states
+    assert _prefill(lib, flags=16, ws_bytes=need - scratch) == 3
 
 
 def test_prefill_workspace_size(lib):
     lib.kda_prefill_workspace_size.restype = ctypes.c_size_t
     lib.kda_prefill_workspace_size.argtypes = [ctypes.c_int64, ctypes.c_int, ctypes.c_int]
-    block = 74240
-    # header + (floor(T / 64) + num_seqs) chunks x H blocks: an upper bound of sum ceil(len / 64)
-    assert lib.kda_prefill_workspace_size(2048 * 8, 8, 16) == 1024 + (256 + 8) * 16 * block
-    assert lib.kda_prefill_workspace_size(0, 3, 2) == 1024 + 3 * 2 * block
-    assert lib.kda_prefill_workspace_size(130, 1, 1) == 1024 + 3 * block
+    block, state = 74240, 128 * 128 * 4
+    # header + (floor(T / 64) + num_seqs) chunks x H blocks (an upper bound of sum ceil(len / 64)) + the fp32
+    # states of min(num_seqs x H, 96) (sequence, head) pairs handed between segments of split state passes
+    assert lib.kda_prefill_workspace_size(2048 * 8, 8, 16) == 1024 + (256 + 8) * 16 * block + 96 * state
+    assert lib.kda_prefill_workspace_size(0, 3, 2) == 1024 + 3 * 2 * block + 6 * state
+    assert lib.kda_prefill_workspace_size(130, 1, 1) == 1024 + 3 * block + state
     assert lib.kda_prefill_workspace_size(-1, 1, 1) == 0
     assert lib.kda_prefill_workspace_size(10, 1, 0) == 0
 
@@ -136,14 +144,14 @@ def test_verify_rejects_bad_arguments(lib):
 
 
 def _spec_step(lib, *, cu=(0, 4), B=2, T=8, H=2, pre=True, spec=True, pre_stride=256, spec_stride=256,
-               ns_idx=FAKE, s_idx=FAKE, n_out=100, ws_bytes=None, lb=-5.0, norm=None, conv=None):
+               ns_idx=FAKE, s_idx=FAKE, n_out=100, ws_bytes=None, lb=-5.0, norm=None, conv=None, flags=0):
     from kda_linear_attention_bounded_gb300._binding import TokenTensors
     cu_host = np.array(cu, np.int32)
     ws_bytes = lib.kda_prefill_workspace_size(int(cu[-1]), len(cu) - 1, H) if ws_bytes is None else ws_bytes
     tp = TokenTensors(FAKE, FAKE, FAKE, pre_stride, FAKE, pre_stride, FAKE, H)
     ts = TokenTensors(FAKE, FAKE, FAKE, spec_stride, FAKE, spec_stride, FAKE, H)
     return lib.kda_spec_step(ctypes.byref(tp) if pre else None, P(FAKE), cu_host.ctypes.data_as(P), len(cu) - 1,
-                             None, 0, P(FAKE), ctypes.byref(ts) if spec else None, B, T, P(FAKE), P(FAKE), P(FAKE),
+                             None, flags, P(FAKE), ctypes.byref(ts) if spec else None, B, T, P(FAKE), P(FAKE), P(FAKE),
                              P(FAKE), lb, 0.1, H, P(FAKE), 4, P(FAKE), H * 128, n_out, norm, conv, P(ns_idx),
                              P(s_idx), P(FAKE), ws_bytes, None)
 
@@ -161,6 +169,7 @@ def test_spec_step_rejects_bad_arguments(lib):
     assert _spec_step(lib, n_out=-1) == 1
     assert _spec_step(lib, lb=-11.0) == 2
     assert _spec_step(lib, ws_bytes=256) == 3         # no room for the prefill's chunk blocks
+    assert _spec_step(lib, flags=16) == 2             # the step's rows go out by index: no split state passes
     assert _spec_step(lib, cu=(0,), B=0, pre=False, spec=False, ns_idx=None, s_idx=None) == 0   # empty step
 
 
@@ -185,7 +194,7 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
 def test_commit_rejects_bad_arguments(lib):
     c = lambda **kw: lib.kda_commit_accepted(P(kw.get("pool", FAKE)), 4, P(FAKE), P(FAKE), P(kw.get("inter", FAKE)),
                                              kw.get("conv"), kw.get("B", 2), kw.get("T", 8), 2, P(kw.get("ws", FAKE)),
-                                             256, None)
+                                             1024, None)
     assert c(ws=None) == 3
     assert c(pool=None) == 1
     assert c(pool=FAKE + 4) == 1

@@ -11,14 +11,16 @@ from gpu_helpers import DevicePrefill, check_out, check_state
 pytestmark = pytest.mark.gpu
 
 
-def _parity(inp, token_pad=0, heads=None, path=None):
-    dev = DevicePrefill(inp, token_pad=token_pad)
+def _run_and_check(dev, inp, ref, path, heads=None):
+    """One call on `path` (the pool first reset to the inputs' own), checked against the oracle's (ref_out, ref_S)."""
+    if dev.pool is not None:
+        dev.pool.copy_(torch.from_numpy(inp.pool).cuda())
     pool_before = dev.pool.clone() if dev.pool is not None else None
     ws = dev.workspace()
     out, final = dev.run(workspace=ws, path=path)
     torch.cuda.synchronize()
     assert kda.read_device_status(ws) == 0
-    ref_out, ref_S, _ = oracle.run_prefill(inp, heads=heads)
+    ref_out, ref_S = ref
     hb, he = heads or (0, inp.H)
     tag = f"{inp.name} [{path or 'default'} path]"
     check_out(out[:, hb:he], ref_out[:, hb:he], f"{tag} outputs", segments=inp.cu_seqlens)
@@ -28,6 +30,7 @@ def _parity(inp, token_pad=0, heads=None, path=None):
         untouched = np.setdiff1d(np.arange(inp.pool.shape[0]), inp.slot_ids)
         idx = torch.from_numpy(untouched).long().cuda()
         assert torch.equal(dev.pool[idx], pool_before[idx]), "pool slots not in slot_ids were modified"
+        final = got.clone()
     else:
         check_state(final[:, hb:he], ref_S[:, hb:he], f"{tag} final states")
         if pool_before is not None:
@@ -35,12 +38,25 @@ def _parity(inp, token_pad=0, heads=None, path=None):
     return out, final
 
 
+def _parity(inp, token_pad=0, heads=None, path=None):
+    dev = DevicePrefill(inp, token_pad=token_pad)
+    ref_out, ref_S, _ = oracle.run_prefill(inp, heads=heads)
+    return _run_and_check(dev, inp, (ref_out, ref_S), path, heads)
+
+
+def _parity_paths(inp, paths):
+    """Every path in `paths` against one oracle run; returns {path: (out, final states)}."""
+    dev = DevicePrefill(inp)
+    ref_out, ref_S, _ = oracle.run_prefill(inp)
+    return {p: _run_and_check(dev, inp, (ref_out, ref_S), p) for p in paths}
+
+
 @pytest.mark.parametrize("path", [None, "two_pass", "fused"])
 def test_tiny_1x256_h2(path):
     _parity(inputs.tiny_prefill(), path=path)
 
 
-PATHS = ["two_pass", "fused"]   # both execution paths forced (the library picks one of them by shape)
+PATHS = ["two_pass", "fused", "overlap"]   # every execution path forced (the library picks one by shape)
 
 
 @pytest.mark.parametrize("path", PATHS)
@@ -100,12 +116,16 @@ def test_bad_slot_sets_status_and_skips(path):
     assert (out[70:].float() == 7.0).all(), "skipped sequence must not be written"
 
 
-@pytest.mark.parametrize("path", ["fused", "two_pass"])
 @pytest.mark.parametrize("make", [inputs.prefill_2048x8, inputs.prefill_8192x4, inputs.varlen_16384_plus_16],
                          ids=["2048x8", "8192x4", "16384+16varlen"])
-def test_full_size(make, path):
-    # the fused one-kernel path (KDA_FUSED) and the two-kernel path (KDA_TWO_PASS)
-    _parity(make(), path=path)
+def test_full_size(make):
+    # every path against one oracle run: the library's own pick, the fused one-kernel path (KDA_FUSED), the
+    # two-kernel path (KDA_TWO_PASS) and the two kernels with split state passes (KDA_OVERLAP; on 2048 x 8 four
+    # of the eight sequences are split, the other four take the plain schedule beside them)
+    res = _parity_paths(make(), [None, "fused", "two_pass", "overlap"])
+    for p in ("overlap", None):
+        assert torch.equal(res[p][0], res["two_pass"][0]) and torch.equal(res[p][1], res["two_pass"][1]), \
+            f"{p or 'default'} path differs from the two-kernel path's bits"
 
 
 @pytest.mark.parametrize("lens", [[1, 63, 64, 65, 130, 0, 200], [1000, 3, 700]])
@@ -118,18 +138,62 @@ def test_fused_and_two_pass_paths_agree(lens):
     assert float((fin_f - fin_t).norm() / fin_t.norm()) <= 5e-3
 
 
-@pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("decay", ["weak_bound", "weak_gate"])
 @pytest.mark.parametrize("lens", [[8192] * 4, [16384]], ids=["8192x4", "16384x1"])
-def test_full_length_weak_decay(lens, decay, path):
+def test_full_length_weak_decay(lens, decay):
     # Weak decay over 128 or 256 chunks: with lower_bound -0.05, or the gate logits centred at -8 (lambda ~ -1e-3
     # per step), the state keeps what enters it for thousands of tokens, so an error the state path makes in one
-    # chunk (the rounding of the state the products read, a wrong carry) reaches the final state and every later
-    # output instead of being forgotten within a few tokens as at the workloads' decay.
+    # chunk (the rounding of the state the products read, a wrong carry, a state handed between segments of a
+    # split state pass) reaches the final state and every later output instead of being forgotten within a few
+    # tokens as at the workloads' decay.
     kw = dict(weak_bound=dict(lower_bound=-0.05), weak_gate=dict(g_mean=-8.0))[decay]
     inp = inputs.prefill_inputs(f"{decay}_{len(lens)}x{lens[0]}", lens, 16, seed=90 + len(lens), pool_slots=16,
                                 load_initial=True, final_to_pool=len(lens) > 1, **kw)
-    _parity(inp, path=path)
+    _parity_paths(inp, PATHS)
+
+
+@pytest.mark.parametrize("lens,H", [([5000, 300, 2000, 64, 1, 4500, 0], 16), ([700, 64, 129], 2), ([20000], 1)],
+                         ids=["mixed_h16", "short_h2", "20000x1_h1"])
+@pytest.mark.parametrize("final_to_pool", [False, True])
+def test_overlap_schedule_matches_two_pass_bit_for_bit(lens, H, final_to_pool):
+    # The split schedule runs the kernels of the two-kernel path; the state a segment hands to the next passes
+    # through fp32 memory and is turned into the same operands the unsplit state pass keeps on chip, so every
+    # output and final state must agree bit for bit.  mixed_h16: forced, four sequences are split (the budget of
+    # half the SMs at H = 16) and the others run beside them on the plain schedule; by default only the two of
+    # at least half the longest's 79 chunks are split.  short_h2: segments of 4 and then 1-4 chunks.
+    inp = inputs.prefill_inputs("overlap_bits", lens, H, seed=19, pool_slots=12, load_initial=True,
+                                final_to_pool=final_to_pool)
+    dev = DevicePrefill(inp)
+    pool0 = dev.pool.clone()
+    res = {}
+    for path in ("two_pass", "overlap", None):
+        dev.pool.copy_(pool0)
+        ws = dev.workspace()
+        out, final = dev.run(workspace=ws, path=path)
+        torch.cuda.synchronize()
+        assert kda.read_device_status(ws) == 0
+        res[path] = (out.clone(), (dev.pool if final_to_pool else final).clone())
+    for path in ("overlap", None):
+        assert torch.equal(res[path][0], res["two_pass"][0]), f"{path or 'default'}: outputs differ"
+        assert torch.equal(res[path][1], res["two_pass"][1]), f"{path or 'default'}: final states differ"
+    # and the two-kernel path itself against the oracle
+    _parity(inp, path="two_pass")
+
+
+def test_overlap_workspace_without_scratch_takes_the_plain_schedule():
+    # a workspace with the blocks but not the scratch states (for these lengths the blocks' bound is exact, so no
+    # spare block holds a scratch state): the call runs unsplit and gives the same bits
+    inp = inputs.prefill_inputs("overlap_ws", [6001, 1], 4, seed=23)
+    dev = DevicePrefill(inp)
+    full = kda.prefill_workspace_size(inp.total_tokens, inp.num_seqs, inp.H)
+    scratch = min(inp.num_seqs * inp.H, 96) * 128 * 128 * 4
+    ref, _ = dev.run(workspace=dev.workspace(), path="two_pass")
+    small = kda.make_workspace("cuda", nbytes=full - scratch)
+    out, _ = dev.run(workspace=small)
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref)
+    with pytest.raises(kda.KdaError):   # forced, the split needs the scratch
+        dev.run(workspace=small, path="overlap")
 
 
 @pytest.mark.parametrize("path", PATHS)
