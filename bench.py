@@ -13,7 +13,9 @@ serving step runs them), one speculative-decoding step (a 4 x 2048-token
 prefill segment beside 64 verify requests x 4 tokens, every output row stored
 by index into the layer output), the other prefill workloads (1 x 256 at H=2,
 4 x 8192, and 16384 + 16 varlen sequences with its long sequence also timed
-alone) as their own calls, and the fp64 CPU oracle on each workload (bounded
+alone) as their own calls -- the long ones take the split state-pass schedule
+by default and are also timed on the plain two-kernel schedule and on the
+fused kernel -- and the fp64 CPU oracle on each workload (bounded
 samples where the whole would take long).  Per-call times are CUDA events on
 the launching stream and the reported per-layer figures are their median; SM
 clocks are sampled through NVML inside the timed region.
@@ -726,12 +728,21 @@ def run_gpu(args):
             rec["algorithmic_bytes"] = r["roofline"]["algorithmic_bytes"]
         return rec
 
+    def two_pass_record(pinp, steps):
+        """The same call with the two kernels on the plain schedule (KDA_TWO_PASS): the long workloads' default
+        splits the longest sequences' state passes into segments that run beside later intra-chunk work."""
+        r = time_prefill(pinp, steps, path="two_pass")
+        return {k: r[k] for k in ("us_per_layer", "us_per_layer_graph", "tokens_per_s", "calls_timed")} | {
+            "roofline_frac": r["roofline"]["frac"]}
+
     w_steps = max(20, min(args.steps, 200))
     workloads = {}
     for make in (inputs.tiny_prefill, inputs.prefill_8192x4, inputs.varlen_16384_plus_16):
         winp = make()
         workloads[winp.name] = time_prefill(winp, w_steps)
         workloads[winp.name]["fused_path"] = fused_record(winp, w_steps)
+        if winp.total_tokens > 4096:
+            workloads[winp.name]["two_pass_path"] = two_pass_record(winp, w_steps)
         if winp.name.startswith("prefill_16384"):
             # the long sequence of this workload alone: its state recurrence is one serial chain of 256 chunks per
             # head, the part of the workload that no number of SMs shortens (the pages quote 16384 x 1 as well)
@@ -744,6 +755,7 @@ def run_gpu(args):
             rec = time_prefill(long_inp, w_steps)
             rec["us_per_chunk"] = rec["us_per_layer"] / rec["chunks_of_longest"]
             rec["fused_path"] = fused_record(long_inp, w_steps)
+            rec["two_pass_path"] = two_pass_record(long_inp, w_steps)
             workloads[winp.name]["long_sequence"] = rec
         if rank == 0 and not args.no_cpu_baseline and world == 1:
             workloads[winp.name]["cpu_baseline"] = cpu_baseline(winp, budget_s=5.0)
