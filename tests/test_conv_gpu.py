@@ -133,7 +133,7 @@ def _prefill_with_conv(inp, heads=None):
     check_out(out[:, hb:he], ref_out[:, hb:he], f"{inp.name} outputs with the convolutions", segments=inp.cu_seqlens)
     if inp.final_to_pool:
         slots = torch.from_numpy(inp.slot_ids).long().cuda()
-        check_state(dev.pool[slots][:, hb:he], ref_S[:, hb:he], f"{inp.name} final states (pool)")
+        check_state(dev.pool[slots][:, hb:he], ref_S[:, hb:he], f"{inp.name} final states (pool) with the convolutions")
         got_win = widen_bf16(conv.window_pool[slots])
     else:
         check_state(final[:, hb:he], ref_S[:, hb:he], f"{inp.name} final states (dense)")
