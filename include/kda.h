@@ -90,15 +90,14 @@ extern "C" {
  *  KDA_FUSED     one kernel, one CTA per (sequence, head), every chunk's operands kept on chip; it
  *                applies without short convolutions and with lower_bound >= -5 (else the call returns
  *                KDA_ERR_UNSUPPORTED);
- *  KDA_OVERLAP   the kernels of KDA_TWO_PASS, with the state passes of the longest sequences (as many as fit
- *                in half of the SMs) split into segments of whole chunks: each segment's state pass runs on
- *                a high-priority stream of the library's (one per calling thread and device) as soon as that
- *                segment's intra-chunk launch has completed, beside the intra-chunk work of the later
- *                segments and of the other sequences; the caller's stream waits for it before the call's
- *                last work.  Without short convolutions only, and not in kda_spec_step (else
- *                KDA_ERR_UNSUPPORTED); the workspace must hold kda_prefill_workspace_size() bytes (else
- *                KDA_ERR_WORKSPACE).  Inside a stream capture it takes the KDA_TWO_PASS schedule until
- *                the calling thread has made one call outside a capture (which creates the stream).
+ *  KDA_OVERLAP   the kernels of KDA_TWO_PASS, with the state passes of the longest sequences (as many
+ *                (sequence, head) pairs as fit in half of the SMs, at most 96) split into segments of whole
+ *                chunks.  The call is then one chain of programmatic dependent launches on `stream`:
+ *                intra-chunk work of segment k, the state pass of segment k, intra-chunk work of segment
+ *                k + 1 (beside it, on the SMs it leaves free), ..., and the state pass of the other
+ *                sequences beside the last segment's.  A segment's final state reaches the next through
+ *                the workspace (fp32), so the results are those of KDA_TWO_PASS bit for bit.  The
+ *                workspace must hold kda_prefill_workspace_size() bytes (else KDA_ERR_WORKSPACE).
  * With no path flag the library takes KDA_FUSED for sequences of one chunk that fit one wave of SMs,
  * KDA_OVERLAP where the longest sequence has 64 chunks or more and every sequence of at least half its
  * length fits the split's budget (and the workspace holds the scratch), else KDA_TWO_PASS. */

@@ -333,9 +333,10 @@ def _token_struct(tensors, H):
 def spec_step(prefill, cu_seqlens, cu_seqlens_host, spec, T, A_log, dt_bias, state_pool, core_attn_out,
               non_spec_token_indx, spec_token_indx, *, prefill_slot_ids=None, spec_slot_ids=None,
               load_initial=False, final_to_pool=False, final_state=None, intermediate_states=None,
-              lower_bound=-5.0, scale=None, norm=None, conv=None, workspace=None, stream=None):
+              lower_bound=-5.0, scale=None, norm=None, conv=None, workspace=None, stream=None, path=None):
     """``kda_spec_step``: the prefill segment and the verify segment of one speculative-decoding step, their
     outputs written into ``core_attn_out`` rows ``non_spec_token_indx`` / ``spec_token_indx``.
+    ``path``: the prefill segment's path, as in :func:`chunk_prefill`.
 
     ``prefill`` and ``spec`` are ``(q, k, v, g, beta_logits)`` tuples (or None for an absent segment);
     ``norm``: an :class:`OutputNorm` over the rows of ``core_attn_out``.
@@ -367,7 +368,8 @@ def spec_step(prefill, cu_seqlens, cu_seqlens_host, spec, T, A_log, dt_bias, sta
             raise ValueError(f"{name}: expected a contiguous CUDA int32 tensor of {n} entries")
     if workspace is None:
         workspace = make_workspace(dev, stream, prefill_workspace_size(Tp, N, H))
-    flags = (KDA_LOAD_INITIAL if load_initial else 0) | (KDA_FINAL_TO_POOL if final_to_pool else 0)
+    flags = (KDA_LOAD_INITIAL if load_initial else 0) | (KDA_FINAL_TO_POOL if final_to_pool else 0) | \
+        {None: 0, "two_pass": KDA_TWO_PASS, "fused": KDA_FUSED, "overlap": KDA_OVERLAP}[path]
     if scale is None:
         scale = 1.0 / math.sqrt(128.0)
     rc = lib.kda_spec_step(

@@ -137,12 +137,10 @@ int prepare_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v, int
             : (flags & KDA_OVERLAP) ? kda::PrefillPath::kOverlap
                                    : kda::PrefillPath::kAuto;
   if (a->path == kda::PrefillPath::kFused && !kda::fused_prefill_applies(*a)) return KDA_ERR_UNSUPPORTED;
-  if (a->path == kda::PrefillPath::kOverlap) {
-    if (!kda::overlap_prefill_applies(*a)) return KDA_ERR_UNSUPPORTED;
-    if (workspace_bytes < kda::prefill_workspace_bytes(cu_seqlens_host[num_seqs], num_seqs, H) +
-                              kda::overlap_scratch_bytes(num_seqs, H))
-      return KDA_ERR_WORKSPACE;
-  }
+  if (a->path == kda::PrefillPath::kOverlap &&
+      workspace_bytes < kda::prefill_workspace_bytes(cu_seqlens_host[num_seqs], num_seqs, H) +
+                            kda::overlap_scratch_bytes(num_seqs, H))
+    return KDA_ERR_WORKSPACE;
   return KDA_OK;
 }
 
@@ -320,8 +318,6 @@ int kda_spec_step(const kda_token_tensors *prefill, const int32_t *cu_seqlens_de
                                 intermediate_states, workspace, workspace_bytes, &va))
       return rc;
   }
-  // the step's prefill rows go out by index, which the split state passes do not take
-  if (pa.path == kda::PrefillPath::kOverlap) return KDA_ERR_UNSUPPORTED;
   const bool has_prefill = pa.num_seqs > 0 && pa.total_tokens > 0, has_spec = B > 0;
   if ((has_prefill && !non_spec_token_indx) || (has_spec && !spec_token_indx)) return KDA_ERR_INVALID_ARG;
   if (num_out_tokens > INT32_MAX) return KDA_ERR_INVALID_ARG;

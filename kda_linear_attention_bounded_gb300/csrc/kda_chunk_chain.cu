@@ -132,7 +132,9 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_chain_kernel(const __grid_c
     const int row = tid / 16, cc = tid % 16, m = row / (kConvW - 1), j = row % (kConvW - 1);
     uint4 val = make_uint4(0u, 0u, 0u, 0u);
     if (tid < kPieces) {
-      if (len + j < kConvW - 1) {
+      // rows before the sequence's first token come from the initial window (a segment that continues a
+      // sequence has 64 or more of its tokens before it)
+      if (!(item_flags & kItemFromMid) && len + j < kConvW - 1) {
         if (prm.conv_load_initial)
           val = *reinterpret_cast<const uint4 *>(
               prm.conv.window_pool + ((static_cast<size_t>(slot) * kRows + m * (kConvW - 1) + len + j) * H + h) * kD + 8 * cc);

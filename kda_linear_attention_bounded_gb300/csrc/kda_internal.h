@@ -250,9 +250,6 @@ cudaError_t launch_chunk_chain(const ChainParams &p, cudaStream_t stream, bool p
 // passes also need overlap_scratch_bytes after the blocks.
 size_t prefill_workspace_bytes(int64_t total_tokens, int num_seqs, int H);
 
-// Whether a call's state passes may be split into segments at all (no short convolutions, rows in token order).
-bool overlap_prefill_applies(const ChunkArgs &args);
-
 // blocks: the workspace after its header, blocks_bytes long
 cudaError_t launch_chunk_prefill(const ChunkArgs &args, const int32_t *cu_seqlens_host, uint8_t *blocks,
                                  size_t blocks_bytes, cudaStream_t stream);

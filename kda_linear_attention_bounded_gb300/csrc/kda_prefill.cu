@@ -322,8 +322,6 @@ size_t overlap_scratch_bytes(int num_seqs, int H) {
   return static_cast<size_t>(pairs) * kD * kD * sizeof(float);
 }
 
-bool overlap_prefill_applies(const ChunkArgs &a) { return a.conv.weight == nullptr && a.out_index == nullptr; }
-
 cudaError_t launch_chunk_prefill(const ChunkArgs &a, const int32_t *cu_host, uint8_t *blocks, size_t blocks_bytes,
                                  cudaStream_t stream) {
   if (a.num_seqs <= 0) return cudaSuccess;
@@ -389,7 +387,9 @@ cudaError_t launch_chunk_prefill(const ChunkArgs &a, const int32_t *cu_host, uin
   std::vector<Item> rest;   // the other sequences (whole)
   size_t all_blocks = 0;
   for (int s = 0; s < a.num_seqs; ++s) all_blocks += static_cast<size_t>(nch(s)) * blk_bytes;
-  if ((a.path == PrefillPath::kAuto || a.path == PrefillPath::kOverlap) && overlap_prefill_applies(a)) {
+  // (with the short convolutions a chunk finds its sequence's window slot through a 16-bit index)
+  if ((a.path == PrefillPath::kAuto || a.path == PrefillPath::kOverlap) &&
+      (a.conv.weight == nullptr || a.num_seqs <= INT16_MAX)) {
     lane = overlap_lane(a, cu_host, a.path == PrefillPath::kOverlap, sms);
     std::vector<char> in_lane(a.num_seqs, 0);
     int top = 0;

@@ -107,8 +107,6 @@ def test_prefill_rejects_bad_arguments(lib):
     assert _prefill(lib, flags=4 | 16) == 1
     assert _prefill(lib, flags=8 | 16) == 1
     assert _prefill(lib, flags=8, lb=-6.0, ws_bytes=1 << 30) == 2   # the fused path takes lower_bound >= -5 only
-    # the split state passes take no short convolutions
-    assert _prefill(lib, flags=16, conv=_conv(dense=FAKE), ws_bytes=1 << 30) == 2
     assert _prefill(lib, H=0) == 1
     assert _prefill(lib, cu=(0,)) == 0                 # no sequences: nothing to do
     # valid arguments but a workspace without room for the chunk blocks
@@ -169,7 +167,6 @@ def test_spec_step_rejects_bad_arguments(lib):
     assert _spec_step(lib, n_out=-1) == 1
     assert _spec_step(lib, lb=-11.0) == 2
     assert _spec_step(lib, ws_bytes=256) == 3         # no room for the prefill's chunk blocks
-    assert _spec_step(lib, flags=16) == 2             # the step's rows go out by index: no split state passes
     assert _spec_step(lib, cu=(0,), B=0, pre=False, spec=False, ns_idx=None, s_idx=None) == 0   # empty step
 
 

@@ -120,12 +120,12 @@ def test_spec_step_verify_segment_with_short_conv():
     assert np.array_equal(widen_bf16(conv.step_windows), ref_win)
 
 
-def _prefill_with_conv(inp, heads=None):
+def _prefill_with_conv(inp, heads=None, path=None):
     from gpu_helpers import DevicePrefill
     dev = DevicePrefill(inp)
     conv = device_conv(inp.conv, N=None if inp.final_to_pool else inp.num_seqs)
     ws = dev.workspace()
-    out, final = dev.run(workspace=ws, conv=conv)
+    out, final = dev.run(workspace=ws, conv=conv, path=path)
     torch.cuda.synchronize()
     assert kda.read_device_status(ws) == 0
     ref_out, ref_S, _, ref_win = oracle.run_prefill(inp, heads=heads)
@@ -139,7 +139,25 @@ def _prefill_with_conv(inp, heads=None):
         check_state(final[:, hb:he], ref_S[:, hb:he], f"{inp.name} final states (dense)")
         got_win = widen_bf16(conv.window_dense)
     assert np.array_equal(got_win[..., hb:he, :], ref_win[..., hb:he, :]), "final windows differ from the oracle's"
-    return dev, conv
+    return dev, conv, out, final
+
+
+@pytest.mark.parametrize("final_to_pool", [True, False])
+def test_prefill_with_short_conv_split_schedule(final_to_pool):
+    # KDA_OVERLAP with the convolutions at H = 16: the four longest sequences' state passes run in segments
+    # (a segment after the first starts from the scratch state; only the last one writes the final window),
+    # the one- and two-token and 64-token sequences beside them on the plain schedule (their windows keep
+    # rows of the initial one).  Against the oracle, and bit for bit against the two-kernel path.
+    inp = inputs.prefill_inputs("conv_split", [1000, 300, 130, 64, 1, 2, 77], 16, seed=750, pool_slots=9,
+                                load_initial=True, final_to_pool=final_to_pool)
+    inp.conv = inputs.conv_inputs(16, 9, seed=751)
+    dev_s, conv_s, out_s, final_s = _prefill_with_conv(inp, heads=(0, 4), path="overlap")
+    dev_t, conv_t, out_t, final_t = _prefill_with_conv(inp, heads=(0, 4), path="two_pass")
+    assert torch.equal(out_s, out_t)
+    if final_to_pool:
+        assert torch.equal(dev_s.pool, dev_t.pool) and torch.equal(conv_s.window_pool, conv_t.window_pool)
+    else:
+        assert torch.equal(final_s, final_t) and torch.equal(conv_s.window_dense, conv_t.window_dense)
 
 
 @pytest.mark.parametrize("lb", [-5.0, -8.0])
@@ -172,7 +190,7 @@ def test_prefill_then_verify_continue_through_the_window():
     pre = inputs.prefill_inputs("conv_pv", [77, 130], H, seed=730, pool_slots=4, load_initial=True,
                                 final_to_pool=True)
     pre.conv = inputs.conv_inputs(H, 4, seed=731)
-    dev, conv = _prefill_with_conv(pre)
+    dev, conv, _, _ = _prefill_with_conv(pre)
     ver = inputs.verify_inputs("conv_pv2", 2, T, H, seed=732, pool_slots=4)
     dver = DeviceVerify(ver)
     conv2 = kda.ShortConv(conv.weight, conv.window_pool, conv.silu,

@@ -38,12 +38,12 @@ def _separate_calls(dev):
     return p_out, final, v_out, inter, pool
 
 
-def _check_step(inp, heads=None):
+def _check_step(inp, heads=None, path=None):
     dev = DeviceSpecStep(inp)
     pool_before = dev.pool.clone()
     ref = _separate_calls(dev)
     ws = dev.workspace()
-    out, final, inter = dev.run(workspace=ws)
+    out, final, inter = dev.run(workspace=ws, path=path)
     # copies taken by the next kernels on the stream, with no synchronisation in between: the call's work must
     # be complete for them (the verify grid runs beside the state pass and finishes after it)
     seen = (out.clone(), dev.pool.clone(), None if final is None else final.clone())
@@ -170,3 +170,12 @@ def test_spec_step_replays_from_a_cuda_graph():
     torch.cuda.synchronize()
     assert kda.read_device_status(ws) == 0
     assert torch.equal(out, ref[0]) and torch.equal(final, ref[1]) and torch.equal(inter, ref[2])
+
+
+def test_spec_step_with_split_state_passes():
+    # the prefill segment on the split schedule (KDA_OVERLAP at H = 16: its four longest sequences' state
+    # passes in segments, the other two's beside the last segment, the verify grid behind the last launch):
+    # bit for bit the plain calls' results, rows by index
+    inp = inputs.spec_step_inputs("split_step", [1200, 700, 64, 3, 130, 1], 6, 4, 16, seed=860,
+                                  order="interleaved", extra_rows=3)
+    _check_step(inp, heads=(0, 4), path="overlap")
