@@ -180,6 +180,24 @@ def test_overlap_schedule_matches_two_pass_bit_for_bit(lens, H, final_to_pool):
     _parity(inp, path="two_pass")
 
 
+def test_overlap_schedule_with_segments_over_several_intra_launches():
+    # H = 1, 78 sequences of 9300 tokens: forced, 76 sequences are split (half the SMs) into segments of 55,
+    # 55 and 36 chunks, so a segment holds 76 x 55 = 4180 chunk slots and its intra-chunk work takes two
+    # launches (each a programmatic dependent of the one before, with its own counter); the other two
+    # sequences' chunks join those launches.  Bit for bit against the two-kernel path.
+    inp = inputs.prefill_inputs("overlap_runs", [9300] * 78, 1, seed=29, pool_slots=80, load_initial=True)
+    dev = DevicePrefill(inp)
+    res = {}
+    for path in ("two_pass", "overlap"):
+        ws = dev.workspace()
+        out, final = dev.run(workspace=ws, path=path)
+        torch.cuda.synchronize()
+        assert kda.read_device_status(ws) == 0
+        res[path] = (out.clone(), final.clone())
+    assert torch.equal(res["overlap"][0], res["two_pass"][0])
+    assert torch.equal(res["overlap"][1], res["two_pass"][1])
+
+
 def test_overlap_workspace_without_scratch_takes_the_plain_schedule():
     # a workspace with the blocks but not the scratch states (for these lengths the blocks' bound is exact, so no
     # spare block holds a scratch state): the call runs unsplit and gives the same bits
