@@ -431,29 +431,435 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_chain_kernel(const __grid_c
   finish();
 }
 
+
+// ---------------------------------------------------------------- value-split state pass
+// Two CTAs per (item, head), each owning 64 of the 128 value channels (v0 = 64 * (blockIdx.x & 1)): the
+// columns of S, U^ and O are independent, and every key-side operand (W, Q+, K', P, the decay) is shared, so
+// each CTA fetches the key-side tiles of the block and its half of U^^T.  The products run untransposed, with
+// the 128 MMA rows on tokens or keys and both operands in shared memory:
+//   D   = [W ; Q+] S                M = 128 (rows 0..63 W S, rows 64..127 Q+ S), N = 64 values, K = 128 keys
+//   X   = -[I ; 0] U^               the CTA's U^ columns transposed into TMEM (an identity tile, negated by the
+//                                   instruction, against the block's U^^T rows as a K-major B), so that the U
+//                                   epilogue reads U^ and W S from TMEM and forms U = -(W S + X) in fp32
+//   S  += K'^T U                    M = 128 keys, N = 64, K = 64 tokens (S fp32 in TMEM, lane = key rho)
+//   D  += [U^^T ; P] U              rows 64..127 of D become O = Q+ S + P U; the A tile starts at the CTA's
+//                                   U^^T rows just before P, whose products land in the rows the U epilogue
+//                                   has already consumed
+// with U = U^ - W S.  Since no product reads TMEM as an operand, the decay of S and the previous chunk's output
+// read-out run beside the first product without slowing it; the serial path per chunk is the first product,
+// the U epilogue, the state product and the bf16 copy of S.
+//   warps 0, 1, 4, 5 (TMEM lanes 0..63): the U epilogue (a token row, 32 value columns each)
+//   warps 2, 3, 6, 7 (lanes 64..127): the output epilogue of the previous chunk, then the fetch of the block
+//                                     three chunks ahead into that chunk's buffer
+//   all 8: the decay of S by the chunk's gamma (before the state product) and the bf16 copy of S after it
+//   warp 8: MMA issue
+// A chunk's buffer holds [W^T | Q+^T], then the U tile (over W^T, once the first product is done), then the
+// chunk's output staging tile (over Q+^T, once its output product is done).
+namespace vs {
+constexpr int kThreads = 288;
+constexpr int kIssuer = 256;
+constexpr int kNumBuf = 3;
+constexpr uint32_t BUF_WQ = 0, BUF_UH = 32768, BUF_PK = 40960, BUF_U = 0, BUF_STAGE = 16384;
+constexpr uint32_t kBufStride = 65536;                 // [W^T | Q+^T] 32 KB, U^^T half 8 KB, [P ; K'^T] 24 KB
+constexpr uint32_t kFetchBytes = 32768 + 8192 + 24576 + 512;   // + gamma (into its own ring)
+constexpr uint32_t OFF_STILE = kNumBuf * kBufStride;   // bf16 S [key rho][64 values], MN-major B of the first product
+constexpr uint32_t OFF_IDENT = OFF_STILE + 16384;      // bf16 [I ; 0], 128 rows x 64, K-major A
+constexpr uint32_t OFF_SMALL = OFF_IDENT + 16384;
+constexpr uint32_t SM_GAMMA = 0 /* [3][128] fp32 */, SM_BAR = 1536 /* full[3], m1, m2, m3 */, SM_TMEM = 1584,
+                   SM_ABORT = 1588, SM_END = 1600;
+constexpr uint32_t kSmemBytes = OFF_SMALL + SM_END + 1024;
+static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+static_assert(OFF_STILE % 1024 == 0 && OFF_IDENT % 1024 == 0 && BUF_UH % 1024 == 0, "operand tiles");
+static_assert(BUF_PK == BUF_UH + 8192, "the output product's A tile is the U^^T half followed by P");
+constexpr uint32_t TM_D0 = 0, TM_D1 = 64, TM_S = 128, TM_X = 192, kTmemCols = 256;
+constexpr int kBarU = 2, kBarO = 3;   // named barriers: U tile ready (all 9 warps), output warps among themselves
+}  // namespace vs
+
+template <int kId>
+__device__ __forceinline__ void named_bar_arrive(int count) {
+  static_assert(kId >= 1 && kId < 16, "barrier 0 is __syncthreads");
+  asm volatile("bar.arrive %0, %1;" ::"n"(kId), "r"(count) : "memory");
+}
+
+__global__ void __launch_bounds__(vs::kThreads, 1) chunk_chain_vsplit_kernel(const __grid_constant__ ChainParams prm) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t *small = sm + vs::OFF_SMALL;
+  float *s_gamma = reinterpret_cast<float *>(small + vs::SM_GAMMA);   // [3][128]: e^(b_63) of the buffered chunks
+  uint64_t *bar_full = reinterpret_cast<uint64_t *>(small + vs::SM_BAR);   // [3]: block landed in buffer b
+  uint64_t *bar_m1 = bar_full + 3;    // first product done
+  uint64_t *bar_m2 = bar_full + 4;    // state product done
+  uint64_t *bar_m3 = bar_full + 5;    // output product done
+  uint32_t *s_tmem = reinterpret_cast<uint32_t *>(small + vs::SM_TMEM);
+  volatile uint32_t *s_abort = reinterpret_cast<volatile uint32_t *>(small + vs::SM_ABORT);
+  uint8_t *s_tile = sm + vs::OFF_STILE, *i_tile = sm + vs::OFF_IDENT;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int H = prm.H;
+  const int half = blockIdx.x & 1, v0 = 64 * half;
+  const int pair = blockIdx.x >> 1;
+  const int h = pair % H;
+  const int nl = static_cast<int>(prm.order[pair / H]);   // item, longest first
+  const int n = prm.seq[nl];
+  const int t0 = prm.tok0[nl];
+  const int len = prm.len[nl];
+  const int nchunks = (len + kChunk - 1) / kChunk;
+  const uint8_t item_flags = prm.flags[nl];
+  const uint8_t *blk0 = prm.blocks + (static_cast<size_t>(prm.chunk_off[nl]) * H + h) * kBlkBytes;
+  const size_t blk_step = static_cast<size_t>(H) * kBlkBytes;
+
+  if (!prm.trigger_after_wait) grid_launch_dependents();
+  auto finish = [&] {
+    if (prm.done_counter && tid == 0 && atomicAdd(prm.done_counter, 1u) == gridDim.x - 1) {
+      grid_dependency_wait();
+      *prm.done_counter = 0;
+    }
+  };
+
+  int slot = 0;
+  if (prm.slot_ids) {
+    slot = prm.slot_ids[n];
+    if (slot < 0 || slot >= prm.num_slots) {
+      if (tid == 0) atomicOr(prm.status, KDA_DEVICE_BAD_SLOT);
+      finish();
+      return;
+    }
+  }
+  float *mid = prm.state_mid ? prm.state_mid + (static_cast<size_t>(prm.mid[nl]) * H + h) * kD * kD : nullptr;
+  float *dst = (item_flags & kItemToMid) ? mid
+               : prm.state_out_pool     ? prm.state_out_pool + (static_cast<size_t>(slot) * H + h) * kD * kD
+                                        : prm.state_out_dense + (static_cast<size_t>(n) * H + h) * kD * kD;
+  const float *src = (item_flags & kItemFromMid) ? mid
+                     : prm.state_in ? prm.state_in + (static_cast<size_t>(slot) * H + h) * kD * kD : nullptr;
+  // thread = (TMEM lane quadrant, 32 of the CTA's 64 value columns); lane = key rho for S, token row for D
+  const bool worker = warp < 8;
+  const int quad = warp & 3, vl = 32 * ((warp >> 2) & 1);
+  const int rho = quad * 32 + lane;
+  const size_t srow = static_cast<size_t>(kd_of_rho(rho)) * kD + v0 + vl;   // this thread's 32 state entries
+
+  // the sequence's final short-convolution window (with conv), written by the first CTA of the pair: as in the
+  // state pass above
+  auto write_window = [&](auto sync) {
+    constexpr int kRows = 3 * (kConvW - 1), kPieces = kRows * kD / 8;
+    const int row = tid / 16, cc = tid % 16, m = row / (kConvW - 1), j = row % (kConvW - 1);
+    uint4 val = make_uint4(0u, 0u, 0u, 0u);
+    if (tid < kPieces) {
+      if (!(item_flags & kItemFromMid) && len + j < kConvW - 1) {
+        if (prm.conv_load_initial)
+          val = *reinterpret_cast<const uint4 *>(
+              prm.conv.window_pool + ((static_cast<size_t>(slot) * kRows + m * (kConvW - 1) + len + j) * H + h) * kD + 8 * cc);
+      } else {
+        const uint16_t *x = m == 0 ? prm.xq : m == 1 ? prm.xk : prm.xv;
+        val = *reinterpret_cast<const uint4 *>(x + static_cast<int64_t>(t0 + len + j - (kConvW - 1)) * prm.qkv_stride +
+                                               h * kD + 8 * cc);
+      }
+    }
+    sync();
+    if (tid < kPieces) {
+      uint16_t *w = prm.state_out_pool
+                        ? prm.conv.window_pool + ((static_cast<size_t>(slot) * kRows + row) * H + h) * kD
+                        : prm.conv.window_dense + ((static_cast<size_t>(n) * kRows + row) * H + h) * kD;
+      *reinterpret_cast<uint4 *>(w + 8 * cc) = val;
+    }
+  };
+
+  if (nchunks == 0) {   // empty sequence: the final state is the initial one
+    if (!worker) return;
+    if (prm.conv.weight && half == 0) write_window([] { named_bar_sync<1>(256); });
+#pragma unroll 8
+    for (int i = 0; i < 32; ++i) dst[srow + i] = src ? src[srow + i] : 0.f;
+    finish();
+    return;
+  }
+
+  // chunk c's key-side tiles, this CTA's U^^T rows and gamma -> buffer c % 3 (one thread)
+  auto fetch = [&](int c) {
+    const int b = c % vs::kNumBuf;
+    uint8_t *buf = sm + b * vs::kBufStride;
+    const uint8_t *g = blk0 + c * blk_step;
+    mbar_arrive_expect_tx(&bar_full[b], vs::kFetchBytes);
+    bulk_load(buf + vs::BUF_WQ, g + kBlkWQ, 32768, &bar_full[b]);
+    bulk_load(buf + vs::BUF_UH, g + kBlkUH + v0 * 128, 8192, &bar_full[b]);
+    bulk_load(buf + vs::BUF_PK, g + kBlkPK, 24576, &bar_full[b]);
+    bulk_load(s_gamma + 128 * b, g + kBlkGamma, 512, &bar_full[b]);
+  };
+  if (tid == vs::kIssuer) {
+    for (int i = 0; i < 6; ++i) mbar_init(&bar_full[i], 1);
+    *s_abort = 0;
+    fence_mbar_init();
+    if (prm.wait_blocks) grid_dependency_wait();
+    for (int c = 0; c < vs::kNumBuf && c < nchunks; ++c) fetch(c);
+  }
+  if (warp == 0) {
+    tmem_alloc(s_tmem, vs::kTmemCols);
+    tmem_relinquish();
+  }
+  // the [I ; 0] tile: row r < 64 is e_r, rows 64..127 are zero (each thread one 16-byte piece of 4 rows)
+  if (worker) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int i = tid + 256 * k, r = i >> 3, pc = i & 7;   // row r, columns 8 pc .. 8 pc + 7
+      const bool on = r < 64 && (r >> 3) == pc;              // the piece holding column r of row r
+      const int wi = (r & 7) >> 1;                           // its word; bf16 1.0 in the half of column r
+      const uint32_t e = (r & 1) ? 0x3F800000u : 0x00003F80u;
+      *reinterpret_cast<uint4 *>(i_tile + swz_offset(128, r, 8 * pc)) =
+          make_uint4(on && wi == 0 ? e : 0u, on && wi == 1 ? e : 0u, on && wi == 2 ? e : 0u, on && wi == 3 ? e : 0u);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (prm.trigger_after_wait) grid_launch_dependents();   // the blocks' grid has completed
+  const uint32_t tmem = *s_tmem;
+  const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+
+  // 32 fp32 state values -> their bf16 row piece of the S tile (4 x 16 bytes)
+  auto store_s = [&](const float *s) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      *reinterpret_cast<uint4 *>(s_tile + swz_offset(128, rho, vl + 8 * q)) =
+          make_uint4(pack_bf16x2(s[8 * q], s[8 * q + 1]), pack_bf16x2(s[8 * q + 2], s[8 * q + 3]),
+                     pack_bf16x2(s[8 * q + 4], s[8 * q + 5]), pack_bf16x2(s[8 * q + 6], s[8 * q + 7]));
+  };
+  // S0 -> the S tile and (undecayed) TMEM; each chunk decays its state by its own gamma before its state product
+  if (worker) {
+    float s[32];
+    if (src) {
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const float4 x = *reinterpret_cast<const float4 *>(src + srow + 4 * q);
+        s[4 * q] = x.x; s[4 * q + 1] = x.y; s[4 * q + 2] = x.z; s[4 * q + 3] = x.w;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) s[i] = 0.f;
+    }
+    store_s(s);
+    tmem_st16(tmem + lane_base + vs::TM_S + vl, s);
+    tmem_st16(tmem + lane_base + vs::TM_S + vl + 16, s + 16);
+    tmem_wait_st();
+  }
+  fence_async_smem();
+  tc_fence_before();
+  __syncthreads();
+
+  const bool u_warp = worker && quad < 2, o_warp = worker && quad >= 2;
+  const int orow = (quad - 2) * 32 + lane;   // output warps: token row of the chunk
+  const int oi = orow + 64 * (vl >> 5);      // output warps: 0..127
+  constexpr int kStoreThread = 64;           // lane 0 of warp 2
+  // the output epilogue of chunk cc, whose output product the caller has waited for: its rows (D buffer
+  // cc & 1, rows 64..127) -> the staging tile in its buffer -> global; then the block three chunks ahead into
+  // that buffer (output warps only).  Rows go out in token order (the planner takes this kernel only without an
+  // output row index).
+  auto output_epilogue = [&](int cc, int rows) {
+    uint8_t *buf = sm + (cc % vs::kNumBuf) * vs::kBufStride;
+    uint8_t *stage = buf + vs::BUF_STAGE;
+    tc_fence_after();
+    uint32_t ov[32];
+    const uint32_t tb = tmem + lane_base + ((cc & 1) ? vs::TM_D1 : vs::TM_D0) + vl;
+    tmem_ld16_async(tb, ov);
+    tmem_ld16_async(tb + 16, ov + 16);
+    tmem_wait_ld();
+    tmem_tie<32>(ov);
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      *reinterpret_cast<uint4 *>(stage + swz_offset(64, orow, vl + 8 * q)) =
+          make_uint4(pack_bf16x2(__uint_as_float(ov[8 * q]), __uint_as_float(ov[8 * q + 1])),
+                     pack_bf16x2(__uint_as_float(ov[8 * q + 2]), __uint_as_float(ov[8 * q + 3])),
+                     pack_bf16x2(__uint_as_float(ov[8 * q + 4]), __uint_as_float(ov[8 * q + 5])),
+                     pack_bf16x2(__uint_as_float(ov[8 * q + 6]), __uint_as_float(ov[8 * q + 7])));
+    fence_async_smem();
+    named_bar_sync<vs::kBarO>(128);
+    const int tok = t0 + cc * kChunk;
+    if (rows < kChunk) {   // a ragged last chunk: its valid rows one by one, 8 pieces of 16 bytes per row
+      for (int i = oi; i < rows * 8; i += 128) {
+        const int r = i >> 3, pc = i & 7;
+        *reinterpret_cast<uint4 *>(prm.out + static_cast<int64_t>(tok + r) * prm.out_stride + h * kD + v0 + 8 * pc) =
+            *reinterpret_cast<const uint4 *>(stage + swz_offset(64, r, 8 * pc));
+      }
+      named_bar_sync<vs::kBarO>(128);   // the staging tile has been read
+      if (tid == kStoreThread && cc + vs::kNumBuf < nchunks) fetch(cc + vs::kNumBuf);
+    } else if (tid == kStoreThread) {
+      tma_store_3d(&prm.tout, v0, h, tok, stage);
+      bulk_commit();
+      if (cc + vs::kNumBuf < nchunks) {
+        bulk_wait_read();
+        fetch(cc + vs::kNumBuf);
+      }
+    }
+  };
+
+  for (int c = 0; c < nchunks; ++c) {
+    const int b = c % vs::kNumBuf;
+    uint8_t *buf = sm + b * vs::kBufStride;
+    const uint32_t tm_d = (c & 1) ? vs::TM_D1 : vs::TM_D0;
+    wait_or_abort(&bar_full[b], (c / vs::kNumBuf) & 1, s_abort, prm.status);
+
+    // ---- D = [W ; Q+] S  (A: the [W^T | Q+^T] tile read MN-major, B: the S tile); X = -[I ; 0] U^ (the
+    // identity tile against the U^^T half as a K-major B, negated)
+    if (tid == vs::kIssuer) {
+      tc_fence_after();
+      const uint64_t a = desc_mnmajor_base(smem_u32(buf + vs::BUF_WQ), 128);
+      const uint64_t bs = desc_mnmajor_base(smem_u32(s_tile), 128);
+      const uint32_t id = idesc_bf16(128, 64, true, true);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) mma_bf16(tmem + tm_d, a + mnmajor_step(k), bs + mnmajor_step(k), id, k > 0);
+      const uint64_t ai = desc_kmajor_base(smem_u32(i_tile));
+      const uint64_t bu = desc_kmajor_base(smem_u32(buf + vs::BUF_UH));
+      const uint32_t idn = idesc_bf16(128, 64, false, false, true);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) mma_bf16(tmem + vs::TM_X, ai + kmajor_step(128, k), bu + kmajor_step(64, k), idn, k > 0);
+      mma_commit(bar_m1);
+    }
+
+    // ---- beside the product: S_c <- Diag(gamma_c) S_c in TMEM (all epilogue warps)
+    if (worker) {
+      const float g = s_gamma[128 * b + rho];
+      uint32_t sv[32];
+      tmem_ld16_async(tmem + lane_base + vs::TM_S + vl, sv);
+      tmem_ld16_async(tmem + lane_base + vs::TM_S + vl + 16, sv + 16);
+      tmem_wait_ld();
+      tmem_tie<32>(sv);
+      float s[32];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float2 p = mul2(make_float2(__uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1])), make_float2(g, g));
+        s[2 * i] = p.x;
+        s[2 * i + 1] = p.y;
+      }
+      tmem_st16(tmem + lane_base + vs::TM_S + vl, s);
+      tmem_st16(tmem + lane_base + vs::TM_S + vl + 16, s + 16);
+      tmem_wait_st();
+    }
+
+    if (u_warp) {
+      // ---- U = U^ - W S = -(D + X) (token rows 0..63) -> the U tile, over the W^T tile the first product has
+      // consumed
+      wait_or_abort(bar_m1, c & 1, s_abort, prm.status);
+      tc_fence_after();
+      uint32_t dv[32], xv[32];
+      tmem_ld16_async(tmem + lane_base + tm_d + vl, dv);
+      tmem_ld16_async(tmem + lane_base + tm_d + vl + 16, dv + 16);
+      tmem_ld16_async(tmem + lane_base + vs::TM_X + vl, xv);
+      tmem_ld16_async(tmem + lane_base + vs::TM_X + vl + 16, xv + 16);
+      tmem_wait_ld();
+      tmem_tie<32>(dv);
+      tmem_tie<32>(xv);
+      float u[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) u[i] = -(__uint_as_float(dv[i]) + __uint_as_float(xv[i]));
+      uint8_t *u_tile = buf + vs::BUF_U;
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        *reinterpret_cast<uint4 *>(u_tile + swz_offset(64, rho, vl + 8 * q)) =
+            make_uint4(pack_bf16x2(u[8 * q], u[8 * q + 1]), pack_bf16x2(u[8 * q + 2], u[8 * q + 3]),
+                       pack_bf16x2(u[8 * q + 4], u[8 * q + 5]), pack_bf16x2(u[8 * q + 6], u[8 * q + 7]));
+      fence_async_smem();
+      tc_fence_before();
+      named_bar_sync<vs::kBarU>(vs::kThreads);
+    } else if (o_warp) {
+      // chunk c - 1's output product is waited for before this arrival lets chunk c's be issued (the
+      // barrier's phases then cannot run two ahead of the wait)
+      if (c > 0) wait_or_abort(bar_m3, (c - 1) & 1, s_abort, prm.status);
+      tc_fence_before();
+      named_bar_arrive<vs::kBarU>(vs::kThreads);   // the decay's TMEM stores are done
+      if (c > 0) output_epilogue(c - 1, kChunk);   // chunk c - 1 is not the last one: all its rows are valid
+    } else {   // the issuing warp
+      named_bar_sync<vs::kBarU>(vs::kThreads);
+      if (tid == vs::kIssuer) {
+        tc_fence_after();
+        // ---- S += K'^T U  (A: the K'^T rows of [P ; K'^T], K-major; B: the U tile)
+        const uint64_t pk = desc_kmajor_base(smem_u32(buf + vs::BUF_PK));
+        const uint64_t bu = desc_mnmajor_base(smem_u32(buf + vs::BUF_U), 64);
+        const uint32_t id = idesc_bf16(128, 64, false, true);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          mma_bf16(tmem + vs::TM_S, pk + desc_bytes(64 * 128) + kmajor_step(kBlkPKRows, k), bu + mnmajor_step(k), id, 1);
+        mma_commit(bar_m2);
+        // ---- D += [U^^T half ; P] U: rows 64..127 of D become O = Q+ S + P U
+        const uint64_t pj = desc_kmajor_base(smem_u32(buf + vs::BUF_UH));
+#pragma unroll
+        for (int k = 0; k < 4; ++k) mma_bf16(tmem + tm_d, pj + kmajor_step(128, k), bu + mnmajor_step(k), id, 1);
+        mma_commit(bar_m3);
+      }
+      __syncwarp();
+    }
+
+    // ---- S_{c+1} -> the S tile (the next chunk's first product)
+    if (worker && c + 1 < nchunks) {
+      wait_or_abort(bar_m2, c & 1, s_abort, prm.status);
+      tc_fence_after();
+      uint32_t sv[32];
+      tmem_ld16_async(tmem + lane_base + vs::TM_S + vl, sv);
+      tmem_ld16_async(tmem + lane_base + vs::TM_S + vl + 16, sv + 16);
+      tmem_wait_ld();
+      tmem_tie<32>(sv);
+      float s[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) s[i] = __uint_as_float(sv[i]);
+      store_s(s);
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    if (*s_abort) break;
+  }
+
+  // the last chunk's output and the final state
+  const int last_valid = len - (nchunks - 1) * kChunk;
+  if (o_warp) {
+    wait_or_abort(bar_m3, (nchunks - 1) & 1, s_abort, prm.status);
+    output_epilogue(nchunks - 1, last_valid);
+  }
+  if (worker) {
+    wait_or_abort(bar_m2, (nchunks - 1) & 1, s_abort, prm.status);
+    tc_fence_after();
+    float s[32];
+    tmem_ld16(tmem + lane_base + vs::TM_S + vl, s);
+    tmem_ld16(tmem + lane_base + vs::TM_S + vl + 16, s + 16);
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      *reinterpret_cast<float4 *>(dst + srow + 4 * q) = make_float4(s[4 * q], s[4 * q + 1], s[4 * q + 2], s[4 * q + 3]);
+  }
+  if (tid == kStoreThread) bulk_wait_all();
+  if (prm.conv.weight && half == 0 && !(item_flags & kItemToMid)) write_window([] { __syncthreads(); });
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, vs::kTmemCols);
+  }
+  finish();
+}
+
 }  // namespace
 
-cudaError_t launch_chunk_chain(const ChainParams &p, cudaStream_t stream, bool programmatic) {
+cudaError_t launch_chunk_chain(const ChainParams &p, cudaStream_t stream, bool programmatic, bool value_split) {
   if (p.num_seqs <= 0) return cudaSuccess;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(chunk_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(chunk_chain_vsplit_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, vs::kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
   // programmatic dependent launch: the grid may be scheduled while the preceding intra-chunk grid drains
   // (it waits for that grid's completion before reading any block)
+  // (value_split: two CTAs per (item, head), each with 64 of the value channels)
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.num_seqs * p.H);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.gridDim = dim3(p.num_seqs * p.H * (value_split ? 2 : 1));
+  cfg.blockDim = dim3(value_split ? vs::kThreads : kThreads);
+  cfg.dynamicSmemBytes = value_split ? vs::kSmemBytes : kSmemBytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = programmatic ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, chunk_chain_kernel, p);
+  return value_split ? cudaLaunchKernelEx(&cfg, chunk_chain_vsplit_kernel, p)
+                     : cudaLaunchKernelEx(&cfg, chunk_chain_kernel, p);
 }
 
 }  // namespace kda

@@ -243,8 +243,9 @@ cudaError_t launch_gated_norm(const GatedNormArgs &args, cudaStream_t stream);
 
 // programmatic: launched as a programmatic dependent of the preceding grid in the stream (a state pass)
 cudaError_t launch_chunk_intra(const IntraParams &p, int num_chunks, cudaStream_t stream, bool programmatic);
-// programmatic: launched as a programmatic dependent of the preceding grid in the stream (the intra-chunk grid)
-cudaError_t launch_chunk_chain(const ChainParams &p, cudaStream_t stream, bool programmatic);
+// programmatic: launched as a programmatic dependent of the preceding grid in the stream (the intra-chunk grid);
+// value_split: two CTAs per (item, head), each owning 64 of the value channels (shorter serial path per chunk)
+cudaError_t launch_chunk_chain(const ChainParams &p, cudaStream_t stream, bool programmatic, bool value_split);
 
 // Bytes of workspace kda_chunk_prefill needs (status header + one block per chunk and head); the split state
 // passes also need overlap_scratch_bytes after the blocks.

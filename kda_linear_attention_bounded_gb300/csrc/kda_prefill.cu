@@ -315,6 +315,14 @@ std::vector<int> overlap_lane(const ChunkArgs &a, const int32_t *cu_host, bool f
   return lane;
 }
 
+// Whether a state-pass launch over `pairs` (item, head) pairs takes the value-split kernel: two CTAs per pair,
+// 64 value channels each, which shortens the serial path per chunk from ~3.8 k to ~2.5 k cycles with
+// bit-identical results, at the price of twice the SMs and twice the key-side block reads.  It pays where those
+// SMs would otherwise idle: when both CTAs of every pair fit in `budget` SMs.  Not with rows stored by index
+// (the spec step), whose verify grid runs beside the state pass on the SMs it leaves free: measured there,
+// 210 us against 174.
+bool use_vsplit(const ChunkArgs &a, long pairs, long budget) { return a.out_index == nullptr && 2 * pairs <= budget; }
+
 }  // namespace
 
 size_t overlap_scratch_bytes(int num_seqs, int H) {
@@ -439,7 +447,8 @@ cudaError_t launch_chunk_prefill(const ChunkArgs &a, const int32_t *cu_host, uin
         return e;
       fill_chain(cp, items.data(), start.data(), ns);
       cp->blocks = blocks + blk;
-      if (cudaError_t e = launch_chunk_chain(*cp, stream, true)) return e;
+      if (cudaError_t e = launch_chunk_chain(*cp, stream, true, use_vsplit(a, static_cast<long>(ns) * a.H, sms)))
+        return e;
       blk += static_cast<size_t>(chunks) * blk_bytes;
     }
     return cudaSuccess;
@@ -508,7 +517,10 @@ cudaError_t launch_chunk_prefill(const ChunkArgs &a, const int32_t *cu_host, uin
     cp->wait_blocks = 1;
     cp->trigger_after_wait = (k == nseg - 1 && !rest_all.empty()) ? 1 : 0;
     cp->done_counter = nullptr;
-    if (cudaError_t e = launch_chunk_chain(*cp, stream, true)) return e;
+    // (the lane's state passes take the value split only with no other sequences beside them, whose work
+    // would want those SMs: on 16384 + 16 varlen it measured 703 us against 670)
+    if (cudaError_t e = launch_chunk_chain(*cp, stream, true, rest.empty() && use_vsplit(a, pairs, sms / 2)))
+      return e;
     blk += chunks;
   }
   if (!rest_all.empty()) {   // C_rest beside C_{n-1}: every block exists once it may start
@@ -518,7 +530,7 @@ cudaError_t launch_chunk_prefill(const ChunkArgs &a, const int32_t *cu_host, uin
     cp->trigger_after_wait = 0;
     cp->done_counter = chain.next();
     if (!cp->done_counter) return cudaErrorInvalidValue;   // the planner sizes the chain; not reached
-    if (cudaError_t e = launch_chunk_chain(*cp, stream, true)) return e;
+    if (cudaError_t e = launch_chunk_chain(*cp, stream, true, false)) return e;
   }
   return cudaSuccess;
 }

@@ -115,6 +115,16 @@ def test_spec_step_prefill_only_and_verify_only():
                                         extra_rows=2))
 
 
+def test_full_and_value_split_state_passes_agree_bit_for_bit():
+    # The step stores its prefill rows by index, so its prefill segment runs the state pass that keeps all 128
+    # value channels of a (sequence, head) in one CTA; the plain call on these few pairs runs the value-split
+    # one (two CTAs, 64 value channels each, untransposed products).  Their products are the same sums in the
+    # same order, so outputs and states must agree bit for bit, over 47 chunks of weak decay (lambda ~ -1e-3
+    # per step), where any difference would carry.
+    _check_step(inputs.spec_step_inputs("step_vs_weak", [3000, 700, 129], 0, 4, 4, seed=430, order="interleaved",
+                                        extra_rows=1, g_mean=-8.0))
+
+
 def test_spec_step_2048x4_64x4_h16_full():
     # the bench workload; the oracle runs on 4 of the 16 heads (the bit-exact checks cover all of them)
     _check_step(inputs.spec_step_2048x4_64x4(), heads=(6, 10))
