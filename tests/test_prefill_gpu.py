@@ -260,3 +260,43 @@ def test_prefill_captured_in_a_cuda_graph(path):
     assert kda.read_device_status(ws) == 0
     assert torch.equal(out_g, out_ref)
     assert torch.equal(final_g, final_ref)
+
+
+def test_concurrent_calls_from_two_threads():
+    # two host threads, each with its own stream and workspace, call the prefill at once (the planner's staging
+    # of the launch parameters is shared and locked; the split schedule's counters live in each workspace): both
+    # give the results of a call made alone, bit for bit
+    import threading
+    inps = [inputs.prefill_inputs("thread_a", [5000, 300], 4, seed=33, pool_slots=4, load_initial=True),
+            inputs.prefill_inputs("thread_b", [700, 64, 129], 4, seed=34, pool_slots=4, load_initial=True)]
+    devs = [DevicePrefill(i) for i in inps]
+    refs = []
+    for d in devs:
+        out, fin = d.run(workspace=d.workspace())
+        torch.cuda.synchronize()
+        refs.append((out.clone(), fin.clone()))
+    results = [None, None]
+    errors = []
+
+    def work(k):
+        try:
+            st = torch.cuda.Stream()
+            ws = devs[k].workspace()
+            torch.cuda.synchronize()
+            with torch.cuda.stream(st):
+                for _ in range(5):
+                    out, fin = devs[k].run(workspace=ws, stream=st)
+            st.synchronize()
+            assert kda.read_device_status(ws, stream=st) == 0
+            results[k] = (out.clone(), fin.clone())
+        except Exception as e:   # reported by the main thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=work, args=(k,)) for k in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    for k in range(2):
+        assert torch.equal(results[k][0], refs[k][0]) and torch.equal(results[k][1], refs[k][1])
