@@ -1,8 +1,11 @@
 // Host planning of the chunked prefill: chunk slots per sequence, TMA tensor
-// maps, and the two launches (intra-chunk kernel over every chunk and head,
-// then the state pass over every sequence and head, longest sequences first).
-// Everything is computed from the host copy of cu_seqlens; nothing here reads
-// device memory or synchronises.
+// maps, and the launches.  The plain schedule is two launches per group of
+// sequences (intra-chunk kernel over every chunk and head, then the state pass
+// over every sequence and head, longest sequences first); the split schedule
+// cuts the longest sequences' state passes into segments chained as
+// programmatic dependent launches; one-chunk sequences may take the fused
+// kernel.  Everything is computed from the host copy of cu_seqlens; nothing
+// here reads device memory or synchronises.
 #include <cuda.h>
 
 #include <algorithm>
@@ -140,10 +143,6 @@ cudaError_t launch_fused(const ChunkArgs &a, const int32_t *cu_host, cudaStream_
   }
   return cudaSuccess;
 }
-
-}  // namespace
-
-namespace {
 
 // A run of whole chunks of one sequence that one state-pass CTA per head walks: the whole sequence, or one
 // segment of it when the sequence's state pass is split.
