@@ -176,13 +176,13 @@ def prefill_workspace_size(total_tokens: int, num_seqs: int, H: int) -> int:
 
 
 def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    return None if t is None else t.data_ptr()
 
 
 def _stream_ptr(stream, device):
     if stream is None:
         stream = torch.cuda.current_stream(device)
-    return ctypes.c_void_p(stream.cuda_stream)
+    return stream.cuda_stream
 
 
 def make_workspace(device=None, stream=None, nbytes=None) -> torch.Tensor:
@@ -209,15 +209,19 @@ def read_device_status(workspace: torch.Tensor, stream=None) -> int:
 def _token_tensor(x, name, H):
     if x.dtype != torch.bfloat16 or not x.is_cuda or x.dim() != 3:
         raise ValueError(f"{name}: expected a CUDA bf16 tensor [tokens, H, 128]")
-    if x.shape[1] != H or x.shape[2] != 128 or x.stride(2) != 1 or x.stride(1) != 128:
+    sh, st = x.shape, x.stride()
+    if sh[1] != H or sh[2] != 128 or st[2] != 1 or st[1] != 128:
         raise ValueError(f"{name}: expected [tokens, {H}, 128] with contiguous heads")
-    return x.stride(0)
+    return st[0]
 
 
 def _beta_stride(b, H):
-    if b.dtype != torch.bfloat16 or not b.is_cuda or b.dim() != 2 or b.shape[1] != H or b.stride(1) != 1:
+    if b.dtype != torch.bfloat16 or not b.is_cuda or b.dim() != 2:
         raise ValueError("beta_logits: expected a CUDA bf16 tensor [tokens, H]")
-    return b.stride(0)
+    st = b.stride()
+    if b.shape[1] != H or st[1] != 1:
+        raise ValueError("beta_logits: expected a CUDA bf16 tensor [tokens, H]")
+    return st[0]
 
 
 def chunk_prefill(q, k, v, g, beta_logits, A_log, dt_bias, cu_seqlens, cu_seqlens_host, *,
@@ -254,7 +258,7 @@ def chunk_prefill(q, k, v, g, beta_logits, A_log, dt_bias, cu_seqlens, cu_seqlen
         scale = 1.0 / math.sqrt(128.0)
     rc = lib.kda_chunk_prefill(
         _ptr(q), _ptr(k), _ptr(v), qs, _ptr(g), gs, _ptr(beta_logits), bs, _ptr(A_log), _ptr(dt_bias),
-        float(lower_bound), float(scale), _ptr(cu_seqlens), ctypes.c_void_p(cu_host.data_ptr()), N, H,
+        float(lower_bound), float(scale), _ptr(cu_seqlens), cu_host.data_ptr(), N, H,
         _ptr(state_pool), 0 if state_pool is None else state_pool.shape[0], _ptr(slot_ids), flags,
         _ptr(out), os_, _norm_arg(norm, H), _conv_arg(conv), _ptr(None if final_to_pool else final_state),
         _ptr(workspace), workspace.numel(), _stream_ptr(stream, dev))
@@ -374,7 +378,7 @@ def spec_step(prefill, cu_seqlens, cu_seqlens_host, spec, T, A_log, dt_bias, sta
         scale = 1.0 / math.sqrt(128.0)
     rc = lib.kda_spec_step(
         None if pre is None else ctypes.byref(pre), _ptr(cu_seqlens),
-        None if cu_host is None else ctypes.c_void_p(cu_host.data_ptr()), N, _ptr(prefill_slot_ids), flags,
+        None if cu_host is None else cu_host.data_ptr(), N, _ptr(prefill_slot_ids), flags,
         _ptr(None if final_to_pool else final_state), None if spc is None else ctypes.byref(spc), B, int(T),
         _ptr(spec_slot_ids), _ptr(intermediate_states), _ptr(A_log), _ptr(dt_bias), float(lower_bound),
         float(scale), H, _ptr(state_pool), 0 if state_pool is None else state_pool.shape[0], _ptr(core_attn_out),
