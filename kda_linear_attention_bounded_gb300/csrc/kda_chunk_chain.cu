@@ -837,14 +837,16 @@ __global__ void __launch_bounds__(vs::kThreads, 1) chunk_chain_vsplit_kernel(con
 
 cudaError_t launch_chunk_chain(const ChainParams &p, cudaStream_t stream, bool programmatic, bool value_split) {
   if (p.num_seqs <= 0) return cudaSuccess;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(chunk_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(chunk_chain_vsplit_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, vs::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::mutex mu;
+  static uint64_t done = 0;
+  if (const cudaError_t e = set_attributes_once(mu, done, [] {
+        cudaError_t r = cudaFuncSetAttribute(chunk_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        if (r == cudaSuccess)
+          r = cudaFuncSetAttribute(chunk_chain_vsplit_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   vs::kSmemBytes);
+        return r;
+      }))
+    return e;
   // programmatic dependent launch: the grid may be scheduled while the preceding intra-chunk grid drains
   // (it waits for that grid's completion before reading any block)
   // (value_split: two CTAs per (item, head), each with 64 of the value channels)

@@ -879,15 +879,16 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_c
 
 cudaError_t launch_chunk_intra(const IntraParams &p, int num_chunks, cudaStream_t stream, bool programmatic) {
   if (num_chunks <= 0) return cudaSuccess;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaSuccess;
-    for (auto fn : {chunk_intra_kernel<16, false>, chunk_intra_kernel<32, false>, chunk_intra_kernel<16, true>,
-                    chunk_intra_kernel<32, true>})
-      if (e == cudaSuccess) e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::mutex mu;
+  static uint64_t done = 0;
+  if (const cudaError_t e = set_attributes_once(mu, done, [] {
+        cudaError_t r = cudaSuccess;
+        for (auto fn : {chunk_intra_kernel<16, false>, chunk_intra_kernel<32, false>, chunk_intra_kernel<16, true>,
+                        chunk_intra_kernel<32, true>})
+          if (r == cudaSuccess) r = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        return r;
+      }))
+    return e;
   const bool blk32 = p.lower_bound >= kLowerBound32, conv = p.conv.weight != nullptr;
   auto fn = blk32 ? (conv ? chunk_intra_kernel<32, true> : chunk_intra_kernel<32, false>)
                   : (conv ? chunk_intra_kernel<16, true> : chunk_intra_kernel<16, false>);

@@ -5,9 +5,26 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "kda.h"
 
 namespace kda {
+
+// Runs set() the first time a launcher runs on the current device (kernel attributes such as the dynamic
+// shared-memory limit belong to the device's context) and returns its status; later calls on that device return
+// cudaSuccess.  Thread-safe: concurrent first calls set the attributes once.
+template <typename Set>
+cudaError_t set_attributes_once(std::mutex &mu, uint64_t &done, Set set) {
+  int dev = 0;
+  if (const cudaError_t e = cudaGetDevice(&dev)) return e;
+  if (dev < 0 || dev >= 64) return set();
+  std::lock_guard<std::mutex> lock(mu);
+  if ((done >> dev) & 1u) return cudaSuccess;
+  const cudaError_t e = set();
+  if (e == cudaSuccess) done |= uint64_t(1) << dev;
+  return e;
+}
 
 // Sigmoid-gated RMSNorm of the output rows (gate == nullptr: none).
 struct OutNorm {

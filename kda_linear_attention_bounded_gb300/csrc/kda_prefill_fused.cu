@@ -944,12 +944,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_fused_kernel(const __grid
 
 cudaError_t launch_prefill_fused(const FusedParams &p, cudaStream_t stream) {
   if (p.num_seqs <= 0) return cudaSuccess;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::mutex mu;
+  static uint64_t done = 0;
+  if (const cudaError_t e = set_attributes_once(mu, done, [] {
+        return cudaFuncSetAttribute(prefill_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+      }))
+    return e;
   prefill_fused_kernel<<<p.num_seqs * p.H, kThreads, kSmemBytes, stream>>>(p);
   return cudaGetLastError();
 }
