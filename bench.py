@@ -445,12 +445,17 @@ def run_gpu(args):
         for e in ev[k]:
             e.record(stream)
 
+    copy_ev = []   # per step: (H2D start, H2D end, D2H start, D2H end) on the copy streams
+
     def e2e_step(i):
         b = i & 1
+        marks = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
         with torch.cuda.stream(s_h2d):
             s_h2d.wait_event(ev["comp"][b])          # the call that last read buffer b has finished
+            marks[0].record(s_h2d)
             for name, t in host.items():
                 bufs[b][name].copy_(t, non_blocking=True)
+            marks[1].record(s_h2d)
             ev["h2d"][b].record(s_h2d)
         stream.wait_event(ev["h2d"][b])
         stream.wait_event(ev["d2h"][b])              # output buffer b has been copied out
@@ -461,13 +466,17 @@ def run_gpu(args):
         ev["comp"][b].record(stream)
         with torch.cuda.stream(s_d2h):
             s_d2h.wait_event(ev["comp"][b])
+            marks[2].record(s_d2h)
             out_h[b].copy_(outs[b], non_blocking=True)
             final_h[b].copy_(finals[b], non_blocking=True)
+            marks[3].record(s_d2h)
             ev["d2h"][b].record(s_d2h)
+        copy_ev.append(marks)
 
     for i in range(3):
         e2e_step(i)
     torch.cuda.synchronize(device)
+    copy_ev.clear()
     barrier(world)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
@@ -480,6 +489,9 @@ def run_gpu(args):
     barrier(world)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, device)
     e2e_value = T * e2e_steps * world / (e2e_ms / 1e3)
+    h2d_ms = statistics.median(m[0].elapsed_time(m[1]) for m in copy_ev)
+    d2h_ms = statistics.median(m[2].elapsed_time(m[3]) for m in copy_ev)
+    copy_ev.clear()
     # the results of the last step came back intact
     assert torch.equal(out_h[(e2e_steps - 1) & 1], outs[(e2e_steps - 1) & 1].cpu())
     del bufs, outs, finals
@@ -787,6 +799,7 @@ def run_gpu(args):
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": e2e_steps, "ms_per_step": e2e_ms / e2e_steps,
+                "h2d_ms_per_step": h2d_ms, "d2h_ms_per_step": d2h_ms,
                 "pipelining": "step i+1's host-to-device copies and step i-1's device-to-host copies on their own "
                               "streams overlap step i's call (double-buffered device buffers)"},
         "gpu_launches": 2 * args.steps,
