@@ -75,7 +75,7 @@ constexpr uint32_t SM_NQ = 0, SM_NK = 256, SM_BETA = 512, SM_H = 768 /* [8 quart
                    SM_BAR = 4864, SM_TMEM = 4888, SM_ABORT = 4892, SM_BARU = 4896,
                    SM_HALO = 4928 /* short convolutions: [3 tensors][3 rows][64 channel pairs] u32 */,
                    SM_VW = 7232 /* v's taps [128 channels][4] f32 */, SM_END = 9280;
-constexpr int kCopyThread = 128;      // issues the block's early bulk stores (Q+, [P ; K']) and U^^T's
+constexpr int kCopyThread = 128;      // issues the block's early bulk stores (Q+, [P ; K'])
 constexpr uint32_t kSmemBytes = OFF_SMALL + SM_END + 1024;   // + alignment slack
 static_assert(2 * (kSmemBytes + 1024) <= 233472, "two CTAs per SM");
 constexpr int kAStride = 68;
@@ -845,26 +845,23 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_intra_kernel(const __grid_c
           make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
                      pack_bf16x2(f[6], f[7]));
     }
+    // ------------------------------------------------------------ block write-out, TMEM release
+    // the warp's 32 staged rows are one contiguous 4 KB piece of the tile and of the block: it leaves at once
     fence_async_smem();
     tc_fence_before();
-    if (which) named_bar_sync<8>(128); else named_bar_sync<7>(128);   // this half's rows are staged
-  }
-  // ------------------------------------------------------------ block write-out, TMEM release
-  if (tid == 0) {
-    bulk_store(blk + kBlkWQ, sm + OFF_WST, 16384);
-    bulk_commit();
-  }
-  if (tid == kCopyThread) {
-    bulk_store(blk + kBlkUH, sm + OFF_UST, 16384);
-    bulk_commit();
+    __syncwarp();
+    if (lane == 0) {
+      bulk_store(blk + (which ? kBlkUH : kBlkWQ) + q4 * 4096, dst + q4 * 4096, 4096);
+      bulk_commit();
+    }
   }
   __syncthreads();   // every TMEM read is done
-  if (tid == 0 || tid == kCopyThread) bulk_wait_read();
-  if (warp == 1) {   // the allocating warp, not held by the waits for the bulk stores
+  if (warp == 1) {   // the allocating warp, before its wait for its bulk store
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+  if (lane == 0) bulk_wait_read();   // (the copy thread's wait also covers its earlier Q+ and [P ; K'] stores)
   // launched behind a state pass (a split prefill schedule): the CTA that finishes last waits for that grid's
   // completion, so that this grid completes after it (the next state pass waits for this grid and reads the state
   // the previous one wrote); it then clears the counter for the next call
