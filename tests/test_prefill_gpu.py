@@ -214,6 +214,16 @@ def test_overlap_workspace_without_scratch_takes_the_plain_schedule():
         dev.run(workspace=small, path="overlap")
 
 
+@pytest.mark.parametrize("path", [None] + PATHS)
+@pytest.mark.parametrize("H", [3, 5, 32])
+def test_head_counts_outside_the_bench_shapes(H, path):
+    # odd head counts (a grid of chunk slots x H CTAs, value-split pairs of CTAs over (sequence, head)) and a
+    # larger one; ragged lengths with an empty and a one-token sequence, pool in and out
+    inp = inputs.prefill_inputs(f"heads_{H}", [200, 65, 0, 1, 130], H, seed=80 + H, pool_slots=7,
+                                load_initial=True, final_to_pool=True)
+    _parity(inp, path=path)
+
+
 @pytest.mark.parametrize("path", PATHS)
 def test_more_sequences_than_one_launch_plans(path):
     # 1100 sequences: the planner splits them into two launch groups of <= 1024 sequences

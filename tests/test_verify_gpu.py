@@ -43,6 +43,13 @@ def test_verify_small(T):
     _parity(inputs.verify_inputs("small", 3, T, 2, seed=60 + T, pool_slots=5))
 
 
+@pytest.mark.parametrize("H", [3, 5, 32])
+def test_verify_head_counts_outside_the_bench_shapes(H):
+    # odd head counts and a larger one, at a batch below one wave (so value channels are split) and above it
+    _parity(inputs.verify_inputs(f"heads_{H}", 2, 5, H, seed=90 + H, pool_slots=4))
+    _parity(inputs.verify_inputs(f"heads_{H}_b", 40, 3, H, seed=95 + H, pool_slots=48))
+
+
 def test_verify_repeated_slots_and_weak_decay():
     inp = inputs.verify_inputs("rep", 4, 8, 2, seed=70, pool_slots=3, g_mean=-8.0)
     inp.slot_ids = np.array([1, 1, 2, 1], np.int32)
