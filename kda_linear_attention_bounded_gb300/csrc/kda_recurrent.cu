@@ -295,8 +295,9 @@ __device__ __forceinline__ void recurrent_item(const RecurrentArgs &p) {
   }
 }
 
-template <bool kConv, bool kNorm, int kP>
-__global__ void __launch_bounds__(kThreads, 2) recurrent_kernel(RecurrentArgs p) {
+// kMinB: CTAs per SM the registers are budgeted for (two, or three for the value-split form of large batches)
+template <bool kConv, bool kNorm, int kP, int kMinB>
+__global__ void __launch_bounds__(kThreads, kMinB) recurrent_kernel(RecurrentArgs p) {
   recurrent_item<kConv, kNorm, kP>(p);
   if (p.done_counter) {
     // launched as a programmatic dependent of the grid before it, which it does not read from: the CTA that
@@ -312,11 +313,11 @@ __global__ void __launch_bounds__(kThreads, 2) recurrent_kernel(RecurrentArgs p)
 
 }  // namespace
 
-template <bool kConv, bool kNorm, int kP>
+template <bool kConv, bool kNorm, int kP, int kMinB = 2>
 cudaError_t launch_variant(const RecurrentArgs &args, int num_items, cudaStream_t stream) {
   const unsigned grid = static_cast<unsigned>(num_items) * args.H * kP;
   if (!args.done_counter) {
-    recurrent_kernel<kConv, kNorm, kP><<<grid, kThreads, 0, stream>>>(args);
+    recurrent_kernel<kConv, kNorm, kP, kMinB><<<grid, kThreads, 0, stream>>>(args);
     return cudaGetLastError();
   }
   // programmatic dependent launch: CTAs may be scheduled onto SMs the preceding grid leaves free once every
@@ -330,7 +331,7 @@ cudaError_t launch_variant(const RecurrentArgs &args, int num_items, cudaStream_
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, recurrent_kernel<kConv, kNorm, kP>, args);
+  return cudaLaunchKernelEx(&cfg, recurrent_kernel<kConv, kNorm, kP, kMinB>, args);
 }
 
 cudaError_t launch_recurrent(const RecurrentArgs &args, int num_items, cudaStream_t stream) {
@@ -347,6 +348,12 @@ cudaError_t launch_recurrent(const RecurrentArgs &args, int num_items, cudaStrea
   const long long items = static_cast<long long>(num_items) * args.H, wave = 2LL * sms;
   if (items * 4 <= wave) return launch_variant<false, false, 4>(args, num_items, stream);
   if (items * 2 <= wave) return launch_variant<false, false, 2>(args, num_items, stream);
+  // more items than one wave, with four or more tokens each (a plain call): half of an item's value channels
+  // per CTA in 80 registers, three CTAs per SM.  Measured as graph replays on H = 16: T = 8 at 32 / 48 / 64
+  // requests 49.8 / 74.6 / 97.9 us against 51.0 / 78.2 / 100.8 for whole items at two per SM, level at 256
+  // requests; T = 1 and 2 and batches below one wave are slower that way
+  if (!args.cu_seqlens && !args.done_counter && args.T >= 4 && items > wave)
+    return launch_variant<false, false, 2, 3>(args, num_items, stream);
   return launch_variant<false, false, 1>(args, num_items, stream);
 }
 

@@ -160,22 +160,24 @@ def test_verify_and_commit_replay_from_a_bucket_graph(T):
                 assert torch.equal(dev.pool[s], inter[b, acc[b] - 1])
 
 
-def test_small_batches_split_value_channels_bit_identically():
-    # a batch too small to fill one wave splits each (request, head)'s value channels over 2 or 4 CTAs; every
-    # column is computed exactly as in the unsplit kernel, so requests verified alone equal the same requests
-    # inside a full batch bit for bit
-    full = inputs.verify_inputs("split_full", 64, 4, 16, seed=96, pool_slots=256)
+@pytest.mark.parametrize("T", [3, 4])
+def test_small_batches_split_value_channels_bit_identically(T):
+    # a batch too small to fill one wave splits each (request, head)'s value channels over 2 or 4 CTAs, and a
+    # batch above one wave with T >= 4 over 2 CTAs at three per SM; every column is computed exactly as in the
+    # unsplit kernel, so requests verified alone equal the same requests inside a full batch bit for bit (the
+    # full batch runs whole items at T = 3 and the three-per-SM split at T = 4)
+    full = inputs.verify_inputs("split_full", 64, T, 16, seed=96, pool_slots=256)
     dev = DeviceVerify(full)
     ws = kda.make_workspace()
     out_all, inter_all = dev.run(workspace=ws)
     torch.cuda.synchronize()
     for B in (1, 4, 8):   # 16, 64, 128 (request, head) items: split 4, 4, 2 ways on a 152-SM GPU
-        out, inter = kda.recurrent_verify(dev.q[:B * 4], dev.k[:B * 4], dev.v[:B * 4], dev.g[:B * 4],
-                                          dev.beta[:B * 4], dev.A_log, dev.dt_bias, dev.pool, dev.slots[:B], 4,
+        out, inter = kda.recurrent_verify(dev.q[:B * T], dev.k[:B * T], dev.v[:B * T], dev.g[:B * T],
+                                          dev.beta[:B * T], dev.A_log, dev.dt_bias, dev.pool, dev.slots[:B], T,
                                           lower_bound=full.lower_bound, scale=full.scale, workspace=ws)
         torch.cuda.synchronize()
-        assert torch.equal(out, out_all[:B * 4]), f"B={B}: outputs differ from the unsplit kernel's"
-        assert torch.equal(inter, inter_all[:B]), f"B={B}: per-step states differ from the unsplit kernel's"
+        assert torch.equal(out, out_all[:B * T]), f"B={B}: outputs differ from the full batch's"
+        assert torch.equal(inter, inter_all[:B]), f"B={B}: per-step states differ from the full batch's"
     assert kda.read_device_status(ws) == 0
     small = inputs.verify_inputs("split_small", 8, 5, 16, seed=97, pool_slots=16)
     _parity(small, head_groups=2)
