@@ -348,11 +348,11 @@ cudaError_t launch_recurrent(const RecurrentArgs &args, int num_items, cudaStrea
   const long long items = static_cast<long long>(num_items) * args.H, wave = 2LL * sms;
   if (items * 4 <= wave) return launch_variant<false, false, 4>(args, num_items, stream);
   if (items * 2 <= wave) return launch_variant<false, false, 2>(args, num_items, stream);
-  // more items than one wave, with four or more tokens each (a plain call): half of an item's value channels
-  // per CTA in 80 registers, three CTAs per SM.  Measured as graph replays on H = 16: T = 8 at 32 / 48 / 64
-  // requests 49.8 / 74.6 / 97.9 us against 51.0 / 78.2 / 100.8 for whole items at two per SM, level at 256
-  // requests; T = 1 and 2 and batches below one wave are slower that way
-  if (!args.cu_seqlens && !args.done_counter && args.T >= 4 && items > wave)
+  // more items than one wave, with four or more tokens each: half of an item's value channels per CTA in 80
+  // registers, three CTAs per SM.  Measured as graph replays on H = 16: T = 8 at 32 / 48 / 64 requests 49.8 /
+  // 74.6 / 97.9 us against 51.0 / 78.2 / 100.8 for whole items at two per SM, level at 256 requests; the spec
+  // step 2048 x 4 + 64 x 4 171.6 against 173.4 us; T = 1 and 2 and batches below one wave are slower that way
+  if (!args.cu_seqlens && args.T >= 4 && items > wave)
     return launch_variant<false, false, 2, 3>(args, num_items, stream);
   return launch_variant<false, false, 1>(args, num_items, stream);
 }
