@@ -426,6 +426,16 @@ cudaError_t launch_chunk_prefill(const ChunkArgs &a, const int32_t *cu_host, uin
     if (lane.empty() || rest.size() > static_cast<size_t>(kMaxSeqsPerLaunch) || runs > kMaxSplitCounters ||
         all_blocks + lane.size() * a.H * kD * kD * sizeof(float) > blocks_bytes)
       lane.clear();
+    // where the whole call's state passes fit the value-split kernel on the plain schedule, but the lane's would
+    // keep the full-value kernel on more than 3/8 of the SMs (too few left for the intra-chunk work beside them),
+    // the plain schedule wins up to ~160 chunks (graph replays, H = 16: 8192 x 4 424.4 against 430.7 us split,
+    // 6000 x 4 315.5 against 327.2; the split stays ahead with 48 pairs, 8192 x 3: 355.0 against 362.3, and
+    // for longer sequences, 12000 x 4: 613.5 against 617.3)
+    const long lane_pairs = static_cast<long>(lane.size()) * a.H;
+    if (a.path == PrefillPath::kAuto && !lane.empty() && a.num_seqs <= kMaxSeqsPerLaunch && top <= 160 &&
+        use_vsplit(a, static_cast<long>(a.num_seqs) * a.H, sms) && 8 * lane_pairs > 3L * sms &&
+        !(rest.empty() && use_vsplit(a, lane_pairs, sms / 2)))
+      lane.clear();
   }
 
   if (lane.empty()) {   // plain schedule: per group of consecutive sequences, both kernels over all its chunks
