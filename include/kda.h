@@ -191,6 +191,32 @@ KDA_API size_t kda_workspace_size(void);
  */
 KDA_API size_t kda_prefill_workspace_size(int64_t total_tokens, int num_seqs, int H);
 
+/*
+ * The schedule kda_chunk_prefill takes for a call with these sequence lengths
+ * (cu_seqlens_host [num_seqs + 1], host memory), H heads, flags, lower_bound,
+ * short convolutions present (with_conv != 0) and workspace_bytes of workspace,
+ * on a GPU with `sms` SMs (sms <= 0: the current device's, or 152 without one).
+ * Host only: no device memory is read and nothing is launched, so it also runs
+ * without a GPU.  The arguments are checked as kda_chunk_prefill checks them
+ * (num_seqs >= 1).  On KDA_OK, info[4] holds:
+ *   info[0]  KDA_SCHEDULE_FUSED (one fused kernel), KDA_SCHEDULE_PLAIN (the
+ *            intra-chunk kernel, then the state pass over every chunk) or
+ *            KDA_SCHEDULE_SPLIT (the longest sequences' state passes split into
+ *            segments chained as programmatic dependent launches)
+ *   info[1]  1 if the state passes (plain) or the split sequences' state passes
+ *            run on two CTAs of 64 value channels per (sequence, head)
+ *   info[2]  segments of the split schedule (0 otherwise)
+ *   info[3]  sequences whose state passes are split (0 otherwise)
+ * A spec step's prefill segment (rows stored by index) never takes the fused
+ * kernel or the value split; this call describes kda_chunk_prefill.
+ */
+#define KDA_SCHEDULE_FUSED 1
+#define KDA_SCHEDULE_PLAIN 2
+#define KDA_SCHEDULE_SPLIT 3
+KDA_API int kda_prefill_schedule(const int32_t *cu_seqlens_host, int num_seqs, int H, int flags,
+                                 float lower_bound, int with_conv, size_t workspace_bytes, int sms,
+                                 int *info);
+
 /* Clear the device status word and the rest of the first kda_workspace_size()
  * bytes (an async memset on `stream`). */
 KDA_API int kda_workspace_reset(void *workspace, size_t workspace_bytes, void *stream);

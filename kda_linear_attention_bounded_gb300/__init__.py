@@ -24,4 +24,4 @@ The binding is loaded on first use and raises if libkda has not been built.
 from ._binding import (  # noqa: F401
     KDA_DEVICE_BAD_COUNT, KDA_DEVICE_BAD_INDEX, KDA_DEVICE_BAD_SLOT, KDA_DEVICE_TIMEOUT, KDA_ERR_CUDA, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_WORKSPACE,
     KDA_FINAL_TO_POOL, KDA_LOAD_INITIAL, KDA_OK, KDA_TWO_PASS, KDA_FUSED, KDA_OVERLAP, KDA_CONV_NONE, KDA_CONV_SILU, KDA_PAD_SLOT_ID, KdaError, OutputNorm, ShortConv, chunk_prefill, commit_accepted, load, make_workspace,
-    prefill_workspace_size, read_device_status, recurrent_verify, spec_step, status_string, workspace_size)
+    prefill_schedule, prefill_workspace_size, read_device_status, recurrent_verify, spec_step, status_string, workspace_size)

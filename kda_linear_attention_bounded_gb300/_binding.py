@@ -11,6 +11,8 @@ import ctypes
 import math
 import os
 
+import numpy as np
+
 import torch
 
 from . import build as _build
@@ -32,11 +34,14 @@ KDA_OVERLAP = 16
 KDA_PAD_SLOT_ID = -1
 KDA_CONV_NONE = 0
 KDA_CONV_SILU = 1
+KDA_SCHEDULE_FUSED = 1
+KDA_SCHEDULE_PLAIN = 2
+KDA_SCHEDULE_SPLIT = 3
 
 #: exported symbols of include/kda.h
 EXPORTS = ("kda_status_string", "kda_workspace_size", "kda_prefill_workspace_size", "kda_workspace_reset",
            "kda_read_device_status", "kda_chunk_prefill", "kda_recurrent_verify", "kda_commit_accepted",
-           "kda_recurrent_verify_noalloc", "kda_spec_step")
+           "kda_recurrent_verify_noalloc", "kda_spec_step", "kda_prefill_schedule")
 
 _lib = None
 
@@ -158,8 +163,30 @@ def load():
     lib.kda_spec_step.argtypes = [TT, P, P, I, P, I, P, TT, I, I, P, P, P, P, F, F, I, P, I, P, I64, I64, NP, CP, P,
                                   P, P, SZ, P]
     lib.kda_spec_step.restype = I
+    lib.kda_prefill_schedule.argtypes = [P, I, I, I, F, I, SZ, I, P]
+    lib.kda_prefill_schedule.restype = I
     _lib = lib
     return lib
+
+
+def prefill_schedule(cu_seqlens_host, H, *, lower_bound=-5.0, path=None, conv=False, workspace_bytes=None,
+                     sms=0):
+    """``kda_prefill_schedule``: the schedule ``chunk_prefill`` takes for these sequence lengths (host only, no
+    GPU needed).  Returns ``{"kind": "fused" | "plain" | "split", "value_split": bool, "segments": int,
+    "split_sequences": int}``."""
+    lib = load()
+    cu = np.ascontiguousarray(np.asarray(cu_seqlens_host, dtype=np.int32))
+    N = cu.size - 1
+    if workspace_bytes is None:
+        workspace_bytes = prefill_workspace_size(int(cu[-1]), N, H)
+    flags = {None: 0, "two_pass": KDA_TWO_PASS, "fused": KDA_FUSED, "overlap": KDA_OVERLAP}[path]
+    info = (ctypes.c_int * 4)()
+    rc = lib.kda_prefill_schedule(cu.ctypes.data, N, int(H), flags, float(lower_bound), 1 if conv else 0,
+                                  int(workspace_bytes), int(sms), info)
+    if rc != KDA_OK:
+        raise KdaError(rc, "kda_prefill_schedule")
+    kind = {KDA_SCHEDULE_FUSED: "fused", KDA_SCHEDULE_PLAIN: "plain", KDA_SCHEDULE_SPLIT: "split"}[info[0]]
+    return {"kind": kind, "value_split": bool(info[1]), "segments": int(info[2]), "split_sequences": int(info[3])}
 
 
 def status_string(status: int) -> str:

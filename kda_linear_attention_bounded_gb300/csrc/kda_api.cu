@@ -233,6 +233,37 @@ size_t kda_prefill_workspace_size(int64_t total_tokens, int num_seqs, int H) {
   return kda::prefill_workspace_bytes(total_tokens, num_seqs, H) + kda::overlap_scratch_bytes(num_seqs, H);
 }
 
+int kda_prefill_schedule(const int32_t *cu_seqlens_host, int num_seqs, int H, int flags, float lower_bound,
+                         int with_conv, size_t workspace_bytes, int sms, int *info) {
+  if (!cu_seqlens_host || !info || num_seqs < 1 || H <= 0 || H > 4096) return KDA_ERR_INVALID_ARG;
+  if (flags & ~(KDA_LOAD_INITIAL | KDA_FINAL_TO_POOL | KDA_TWO_PASS | KDA_FUSED | KDA_OVERLAP))
+    return KDA_ERR_INVALID_ARG;
+  const int path_flags = flags & (KDA_TWO_PASS | KDA_FUSED | KDA_OVERLAP);
+  if (path_flags & (path_flags - 1)) return KDA_ERR_INVALID_ARG;
+  if (cu_seqlens_host[0] != 0) return KDA_ERR_INVALID_ARG;
+  for (int n = 0; n < num_seqs; ++n)
+    if (cu_seqlens_host[n + 1] < cu_seqlens_host[n]) return KDA_ERR_INVALID_ARG;
+  if (int rc = check_gate(lower_bound, 1.0f)) return rc;
+  const size_t need = kda::prefill_workspace_bytes(cu_seqlens_host[num_seqs], num_seqs, H);
+  if (workspace_bytes < need) return KDA_ERR_WORKSPACE;
+  kda::ChunkArgs a{};
+  static const float kPresent = 0.f;   // the planner only asks whether the convolutions are there
+  a.H = H;
+  a.num_seqs = num_seqs;
+  a.total_tokens = cu_seqlens_host[num_seqs];
+  a.lower_bound = lower_bound;
+  a.conv.weight = with_conv ? &kPresent : nullptr;
+  a.path = (flags & KDA_TWO_PASS) ? kda::PrefillPath::kTwoPass
+           : (flags & KDA_FUSED)  ? kda::PrefillPath::kFused
+           : (flags & KDA_OVERLAP) ? kda::PrefillPath::kOverlap
+                                  : kda::PrefillPath::kAuto;
+  if (a.path == kda::PrefillPath::kFused && !kda::fused_prefill_applies(a)) return KDA_ERR_UNSUPPORTED;
+  if (a.path == kda::PrefillPath::kOverlap && workspace_bytes < need + kda::overlap_scratch_bytes(num_seqs, H))
+    return KDA_ERR_WORKSPACE;
+  kda::describe_prefill_schedule(a, cu_seqlens_host, workspace_bytes - kda::kWorkspaceHeader, sms, info);
+  return KDA_OK;
+}
+
 int kda_workspace_reset(void *workspace, size_t workspace_bytes, void *stream) {
   if (int rc = check_workspace(workspace, workspace_bytes)) return rc;
   return cudaMemsetAsync(workspace, 0, kWorkspaceBytes, static_cast<cudaStream_t>(stream)) == cudaSuccess

@@ -271,5 +271,11 @@ size_t prefill_workspace_bytes(int64_t total_tokens, int num_seqs, int H);
 // blocks: the workspace after its header, blocks_bytes long
 cudaError_t launch_chunk_prefill(const ChunkArgs &args, const int32_t *cu_seqlens_host, uint8_t *blocks,
                                  size_t blocks_bytes, cudaStream_t stream);
+// The schedule launch_chunk_prefill takes for `args` (host only, nothing launched): info[0] the kind (1 fused
+// kernel, 2 plain schedule, 3 split schedule), info[1] whether the state passes take the value-split kernel,
+// info[2] the split's segments, info[3] the sequences whose state passes are split.  sms <= 0: the current
+// device's SM count (152 without one).
+void describe_prefill_schedule(const ChunkArgs &args, const int32_t *cu_seqlens_host, size_t blocks_bytes, int sms,
+                               int info[4]);
 
 }  // namespace kda

@@ -91,12 +91,11 @@ int sm_count() {
 // 15.0 us; from two chunks per sequence on the two-kernel path is faster (1 x 128: 17.0 against 20.7 us,
 // 1 x 256: 20.5 against 34.8 us, 2048 x 8: 207 against 245 us).  So the fused kernel is picked for one-chunk
 // sequences that fit one wave of SMs.
-bool fused_prefill_preferred(const ChunkArgs &a, const int32_t *cu_host) {
+bool fused_prefill_preferred(const ChunkArgs &a, const int32_t *cu_host, int sms) {
   if (!fused_prefill_applies(a)) return false;
   for (int i = 0; i < a.num_seqs; ++i)
     if (cu_host[i + 1] - cu_host[i] > kChunk) return false;
   const long pairs = static_cast<long>(a.num_seqs) * a.H;
-  const long sms = sm_count() > 0 ? sm_count() : 152;
   return pairs <= sms;
 }
 
@@ -322,77 +321,31 @@ std::vector<int> overlap_lane(const ChunkArgs &a, const int32_t *cu_host, bool f
 // 210 us against 174.
 bool use_vsplit(const ChunkArgs &a, long pairs, long budget) { return a.out_index == nullptr && 2 * pairs <= budget; }
 
-}  // namespace
+// The schedule of one call, decided on the host from the sequence lengths alone: the fused kernel, the plain
+// schedule (both kernels over every chunk, per group of sequences), or the split schedule (the lane's sequences
+// in segments of chunks, the rest beside them).
+struct PrefillPlan {
+  enum Kind { kFusedKernel = 1, kPlain = 2, kSplit = 3 } kind = kPlain;
+  std::vector<int> lane;     // split: the sequences whose state passes are split
+  std::vector<int> bounds;   // split: segment bounds in chunks
+  std::vector<Item> rest;    // split: the other sequences (whole)
+  size_t all_blocks = 0;     // bytes of the blocks of every chunk
+};
 
-size_t overlap_scratch_bytes(int num_seqs, int H) {
-  const long pairs = std::min<long>(static_cast<long>(std::max(num_seqs, 0)) * std::max(H, 0), kMaxOverlapPairs);
-  return static_cast<size_t>(pairs) * kD * kD * sizeof(float);
-}
-
-cudaError_t launch_chunk_prefill(const ChunkArgs &a, const int32_t *cu_host, uint8_t *blocks, size_t blocks_bytes,
-                                 cudaStream_t stream) {
-  if (a.num_seqs <= 0) return cudaSuccess;
-  if (a.path == PrefillPath::kFused || (a.path == PrefillPath::kAuto && fused_prefill_preferred(a, cu_host)))
-    return launch_fused(a, cu_host, stream);
-  // host-side staging of the (large) kernel parameter structs; copied at launch
-  static IntraParams *ip = nullptr;
-  static ChainParams *cp = nullptr;
-  static std::mutex mu;
-  std::lock_guard<std::mutex> lock(mu);
-  if (!ip) {
-    ip = new IntraParams();
-    cp = new ChainParams();
-  }
-  if (!make_token_map(&ip->tq, a.q, a.H, a.total_tokens, a.qkv_stride, false) ||
-      !make_token_map(&ip->tk, a.k, a.H, a.total_tokens, a.qkv_stride, false) ||
-      !make_token_map(&ip->tv, a.v, a.H, a.total_tokens, a.qkv_stride) ||
-      !make_token_map(&ip->tg, a.g, a.H, a.total_tokens, a.g_stride, false) ||
-      (!a.out_index && !make_token_map(&cp->tout, a.out, a.H, a.total_tokens, a.out_stride)))
-    return cudaErrorInvalidValue;
-  ip->beta = a.beta;
-  ip->beta_stride = a.beta_stride;
-  ip->A_log = a.A_log;
-  ip->dt_bias = a.dt_bias;
-  ip->lower_bound = a.lower_bound;
-  ip->scale = a.scale;
-  ip->H = a.H;
-  const int sms = sm_count() > 0 ? sm_count() : 152;
-  ip->prefetch_ahead = 2 * sms;   // two intra-chunk CTAs per SM
-  ip->status = a.status;
-  ip->conv = a.conv;
-  ip->xq = a.q; ip->xk = a.k; ip->xv = a.v;
-  ip->qkv_stride = a.qkv_stride;
-  ip->slot_ids = a.slot_ids;
-  ip->num_slots = a.num_slots;
-  ip->conv_load_initial = a.state_in != nullptr;
-  ip->done_counter = nullptr;
-  cp->conv = a.conv;
-  cp->xq = a.q; cp->xk = a.k; cp->xv = a.v;
-  cp->qkv_stride = a.qkv_stride;
-  cp->conv_load_initial = a.state_in != nullptr;
-  cp->slot_ids = a.slot_ids;
-  cp->num_slots = a.num_slots;
-  cp->state_in = a.state_in;
-  cp->state_out_pool = a.state_out_pool;
-  cp->state_out_dense = a.state_out_dense;
-  cp->state_mid = nullptr;
-  cp->out = a.out;
-  cp->out_stride = a.out_stride;
-  cp->out_index = a.out_index;   // with an index the output tensor map is not used
-  cp->num_out_rows = a.num_out_rows;
-  cp->status = a.status;
-  cp->H = a.H;
-  cp->wait_blocks = 1;
-  cp->trigger_after_wait = 0;
-  cp->done_counter = nullptr;
+PrefillPlan plan_prefill(const ChunkArgs &a, const int32_t *cu_host, size_t blocks_bytes, int sms) {
   auto nch = [&](int s) { return (cu_host[s + 1] - cu_host[s] + kChunk - 1) / kChunk; };
   const size_t blk_bytes = static_cast<size_t>(a.H) * kBlkBytes;   // the blocks of one chunk
 
+  PrefillPlan plan;
+  if (a.path == PrefillPath::kFused || (a.path == PrefillPath::kAuto && fused_prefill_preferred(a, cu_host, sms))) {
+    plan.kind = PrefillPlan::kFusedKernel;
+    return plan;
+  }
   // the split schedule, where it applies and the workspace holds the scratch states
-  std::vector<int> lane;
-  std::vector<int> bounds;
-  std::vector<Item> rest;   // the other sequences (whole)
-  size_t all_blocks = 0;
+  std::vector<int> &lane = plan.lane;
+  std::vector<int> &bounds = plan.bounds;
+  std::vector<Item> &rest = plan.rest;   // the other sequences (whole)
+  size_t &all_blocks = plan.all_blocks;
   for (int s = 0; s < a.num_seqs; ++s) all_blocks += static_cast<size_t>(nch(s)) * blk_bytes;
   // (with the short convolutions a chunk finds its sequence's window slot through a 16-bit index)
   if ((a.path == PrefillPath::kAuto || a.path == PrefillPath::kOverlap) &&
@@ -437,6 +390,79 @@ cudaError_t launch_chunk_prefill(const ChunkArgs &a, const int32_t *cu_host, uin
         !(rest.empty() && use_vsplit(a, lane_pairs, sms / 2)))
       lane.clear();
   }
+  if (!lane.empty()) plan.kind = PrefillPlan::kSplit;
+  return plan;
+}
+
+}  // namespace
+
+size_t overlap_scratch_bytes(int num_seqs, int H) {
+  const long pairs = std::min<long>(static_cast<long>(std::max(num_seqs, 0)) * std::max(H, 0), kMaxOverlapPairs);
+  return static_cast<size_t>(pairs) * kD * kD * sizeof(float);
+}
+
+cudaError_t launch_chunk_prefill(const ChunkArgs &a, const int32_t *cu_host, uint8_t *blocks, size_t blocks_bytes,
+                                 cudaStream_t stream) {
+  if (a.num_seqs <= 0) return cudaSuccess;
+  const int sms = sm_count() > 0 ? sm_count() : 152;
+  PrefillPlan plan = plan_prefill(a, cu_host, blocks_bytes, sms);
+  if (plan.kind == PrefillPlan::kFusedKernel) return launch_fused(a, cu_host, stream);
+  // host-side staging of the (large) kernel parameter structs; copied at launch
+  static IntraParams *ip = nullptr;
+  static ChainParams *cp = nullptr;
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ip) {
+    ip = new IntraParams();
+    cp = new ChainParams();
+  }
+  if (!make_token_map(&ip->tq, a.q, a.H, a.total_tokens, a.qkv_stride, false) ||
+      !make_token_map(&ip->tk, a.k, a.H, a.total_tokens, a.qkv_stride, false) ||
+      !make_token_map(&ip->tv, a.v, a.H, a.total_tokens, a.qkv_stride) ||
+      !make_token_map(&ip->tg, a.g, a.H, a.total_tokens, a.g_stride, false) ||
+      (!a.out_index && !make_token_map(&cp->tout, a.out, a.H, a.total_tokens, a.out_stride)))
+    return cudaErrorInvalidValue;
+  ip->beta = a.beta;
+  ip->beta_stride = a.beta_stride;
+  ip->A_log = a.A_log;
+  ip->dt_bias = a.dt_bias;
+  ip->lower_bound = a.lower_bound;
+  ip->scale = a.scale;
+  ip->H = a.H;
+  ip->prefetch_ahead = 2 * sms;   // two intra-chunk CTAs per SM
+  ip->status = a.status;
+  ip->conv = a.conv;
+  ip->xq = a.q; ip->xk = a.k; ip->xv = a.v;
+  ip->qkv_stride = a.qkv_stride;
+  ip->slot_ids = a.slot_ids;
+  ip->num_slots = a.num_slots;
+  ip->conv_load_initial = a.state_in != nullptr;
+  ip->done_counter = nullptr;
+  cp->conv = a.conv;
+  cp->xq = a.q; cp->xk = a.k; cp->xv = a.v;
+  cp->qkv_stride = a.qkv_stride;
+  cp->conv_load_initial = a.state_in != nullptr;
+  cp->slot_ids = a.slot_ids;
+  cp->num_slots = a.num_slots;
+  cp->state_in = a.state_in;
+  cp->state_out_pool = a.state_out_pool;
+  cp->state_out_dense = a.state_out_dense;
+  cp->state_mid = nullptr;
+  cp->out = a.out;
+  cp->out_stride = a.out_stride;
+  cp->out_index = a.out_index;   // with an index the output tensor map is not used
+  cp->num_out_rows = a.num_out_rows;
+  cp->status = a.status;
+  cp->H = a.H;
+  cp->wait_blocks = 1;
+  cp->trigger_after_wait = 0;
+  cp->done_counter = nullptr;
+  auto nch = [&](int s) { return (cu_host[s + 1] - cu_host[s] + kChunk - 1) / kChunk; };
+  const size_t blk_bytes = static_cast<size_t>(a.H) * kBlkBytes;   // the blocks of one chunk
+  std::vector<int> &lane = plan.lane;
+  const std::vector<int> &bounds = plan.bounds;
+  std::vector<Item> &rest = plan.rest;
+  const size_t all_blocks = plan.all_blocks;
 
   if (lane.empty()) {   // plain schedule: per group of consecutive sequences, both kernels over all its chunks
     std::vector<Item> items;
@@ -542,6 +568,19 @@ cudaError_t launch_chunk_prefill(const ChunkArgs &a, const int32_t *cu_host, uin
     if (cudaError_t e = launch_chunk_chain(*cp, stream, true, false)) return e;
   }
   return cudaSuccess;
+}
+
+void describe_prefill_schedule(const ChunkArgs &a, const int32_t *cu_host, size_t blocks_bytes, int sms, int info[4]) {
+  if (sms <= 0) sms = sm_count() > 0 ? sm_count() : 152;
+  const PrefillPlan plan = plan_prefill(a, cu_host, blocks_bytes, sms);
+  info[0] = plan.kind;
+  info[1] = plan.kind == PrefillPlan::kPlain
+                ? (a.num_seqs <= kMaxSeqsPerLaunch && use_vsplit(a, static_cast<long>(a.num_seqs) * a.H, sms))
+                : plan.kind == PrefillPlan::kSplit ? (plan.rest.empty() &&
+                                                      use_vsplit(a, static_cast<long>(plan.lane.size()) * a.H, sms / 2))
+                                                   : 0;
+  info[2] = plan.kind == PrefillPlan::kSplit ? static_cast<int>(plan.bounds.size()) - 1 : 0;
+  info[3] = static_cast<int>(plan.lane.size());
 }
 
 }  // namespace kda
